@@ -1,0 +1,242 @@
+/*
+ * pkv_oracle.c -- float64 CPU oracle for paged KV-cache decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this code.  The product path
+ * (the CUDA library) shares nothing with it: no headers, no helpers, no
+ * constants.  It is deliberately slow and obvious: every loop below is the
+ * plain definition of what it computes, with no blocking, fusion or
+ * reordering.
+ *
+ * What it computes, and where the definition comes from:
+ *
+ *  - oracle_kv_append: the in-place cache write of a static KV cache
+ *    ("Inference part 1", brunomaga, section "KV cache": a static cache
+ *    writes each new entry in place; "Inference part 2", section on the
+ *    static cache and CUDA graphs, class GPTlite_StaticCache; "Efficient
+ *    Inference", obvix, the in-place slice write of the KV cache), in its
+ *    paged form: a slot s names row s % block_size of physical block
+ *    s / block_size ("Inference part 1", section "PagedAttention: memory
+ *    management for the KV cache"; "KV cache, prefill va decode",
+ *    truongducdung, section 05, "Block table").
+ *
+ *  - oracle_paged_attention: softmax(q K^T * scale) V per sequence, query
+ *    row and query head ("Inference part 1", section "Why attention
+ *    matters", the attention equation), where
+ *      * the keys and values of sequence b are read row by row through the
+ *        block table: logical row i lives in physical block
+ *        block_table[b][i / block_size], row i % block_size (section
+ *        "PagedAttention" of "Inference part 1"; "Efficient Inference",
+ *        the block-table diagram);
+ *      * query head h reads KV head h / (Hq / Hkv): consecutive query heads
+ *        share one KV head ("Inference part 1", section "Smaller KV
+ *        caches: MQA, GQA and MLA", MultiHeadAttention_GQA with
+ *        repeat_interleave; "Efficient Inference", gqa_forward);
+ *      * with Q new query rows per sequence, query row j sees the cached
+ *        rows and the new rows up to itself: row i is visible iff
+ *        i <= L - Q + j, the shifted causal mask tril(diagonal = Sk - Sq)
+ *        of scaled_dot_product_attention_kv_cache ("Inference part 1",
+ *        section "KV cache").  Q = 1 is plain decode; Q = K + 1 is the
+ *        target pass of greedy speculative verification ("Inference part
+ *        2", section "Speculative decoding", generate_speculative).
+ *    The softmax is the textbook two-pass form: all scores first, then
+ *    their maximum, then exp(s - max) weights.  It is NOT the online
+ *    recurrence the GPU path uses.
+ *
+ * Readings where the pages are silent (each also listed in the design
+ * notes): L counts every row of the sequence including the new ones; a
+ * query row that sees no row at all (L - Q + j < 0, e.g. L = 0) returns a
+ * zero vector; a negative slot is skipped (padding); slots and block ids
+ * out of range are errors.
+ *
+ * Dtype codes: 0 = float32, 1 = bfloat16, 2 = float16.  Inputs of 16-bit
+ * types are passed as their raw uint16 bit patterns and widened exactly to
+ * double here.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG -1
+#define ORACLE_ERR_SLOT -2
+#define ORACLE_ERR_BLOCK -3
+#define ORACLE_ERR_NOMEM -4
+
+static int elt_size(int dtype) { return dtype == 0 ? 4 : 2; }
+
+/* Exact widening of one stored element to double. */
+static double widen(const void *base, int64_t index, int dtype) {
+  if (dtype == 0) {
+    float f;
+    memcpy(&f, (const char *)base + index * 4, 4);
+    return (double)f;
+  }
+  uint16_t h;
+  memcpy(&h, (const char *)base + index * 2, 2);
+  if (dtype == 1) { /* bfloat16: the high half of a float32 */
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+  }
+  /* float16: 1 sign, 5 exponent (bias 15), 10 mantissa bits */
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int m = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp((double)(m + 1024), e - 25); /* (1 + m/1024) * 2^(e-15) */
+  return sign ? -v : v;
+}
+
+/*
+ * oracle_kv_append: byte copy of the new rows into their slots.
+ * k_new, v_new: [T, Hkv, D]; k_cache, v_cache: [NB, Hkv, bs, D] (host
+ * mirrors, modified in place); slot_mapping: [T].
+ */
+int oracle_kv_append(void *k_cache, void *v_cache, const void *k_new,
+                     const void *v_new, const int64_t *slot_mapping, int64_t T,
+                     int Hkv, int D, int bs, int64_t NB, int dtype) {
+  if (!k_cache || !v_cache || !k_new || !v_new || !slot_mapping || T < 0 ||
+      Hkv <= 0 || D <= 0 || bs <= 0 || NB < 0 || dtype < 0 || dtype > 2)
+    return ORACLE_ERR_ARG;
+  const int64_t row_bytes = (int64_t)D * elt_size(dtype);
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue; /* padding token: nothing to write */
+    if (slot >= NB * bs) return ORACLE_ERR_SLOT;
+    int64_t block = slot / bs, offset = slot % bs;
+    for (int h = 0; h < Hkv; ++h) {
+      int64_t dst = ((block * Hkv + h) * bs + offset) * row_bytes;
+      int64_t src = (t * Hkv + h) * row_bytes;
+      memcpy((char *)k_cache + dst, (const char *)k_new + src, row_bytes);
+      memcpy((char *)v_cache + dst, (const char *)v_new + src, row_bytes);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * One output row: sequence b, query row j (0..Q-1), query head h.
+ * Returns ORACLE_OK or an error code; writes D doubles to out_row.
+ */
+static int attend_one(double *out_row, double *scores, const void *q,
+                      const void *k_cache, const void *v_cache,
+                      const int32_t *block_table, int max_blocks,
+                      const int32_t *context_lens, int b, int j, int h, int Q,
+                      int Hq, int Hkv, int D, int bs, int64_t NB, double scale,
+                      int dtype) {
+  const int L = context_lens[b];
+  const int64_t visible = (int64_t)L - Q + 1 + j; /* rows 0 .. L-Q+j */
+  const int g = h / (Hq / Hkv);                   /* KV head of query head h */
+  for (int d = 0; d < D; ++d) out_row[d] = 0.0;
+  if (visible <= 0) return ORACLE_OK;
+  if ((visible + bs - 1) / bs > max_blocks) return ORACLE_ERR_BLOCK;
+
+  const int64_t q_base = (((int64_t)b * Q + j) * Hq + h) * D;
+
+  /* Pass 1: every score s_i = scale * <q, k_i>. */
+  for (int64_t i = 0; i < visible; ++i) {
+    int32_t phys = block_table[(int64_t)b * max_blocks + i / bs];
+    if (phys < 0 || phys >= NB) return ORACLE_ERR_BLOCK;
+    int64_t k_base = (((int64_t)phys * Hkv + g) * bs + i % bs) * D;
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d)
+      dot += widen(q, q_base + d, dtype) * widen(k_cache, k_base + d, dtype);
+    scores[i] = scale * dot;
+  }
+  /* Their maximum. */
+  double m = scores[0];
+  for (int64_t i = 1; i < visible; ++i)
+    if (scores[i] > m) m = scores[i];
+  /* Pass 2: weights exp(s_i - m), weighted sum of the value rows. */
+  double denom = 0.0;
+  for (int64_t i = 0; i < visible; ++i) {
+    double w = exp(scores[i] - m);
+    int32_t phys = block_table[(int64_t)b * max_blocks + i / bs];
+    int64_t v_base = (((int64_t)phys * Hkv + g) * bs + i % bs) * D;
+    denom += w;
+    for (int d = 0; d < D; ++d) out_row[d] += w * widen(v_cache, v_base + d, dtype);
+  }
+  for (int d = 0; d < D; ++d) out_row[d] /= denom;
+  return ORACLE_OK;
+}
+
+/*
+ * oracle_paged_attention.
+ *   out          [B, Q, Hq, D] float64 (written)
+ *   q            [B, Q, Hq, D] in `dtype`
+ *   k_cache/v_cache [NB, Hkv, bs, D] in `dtype`
+ *   block_table  [B, max_blocks] int32
+ *   context_lens [B] int32
+ *   rows, n_rows optional list of flat output-row indices ((b*Q + j)*Hq + h)
+ *                to compute; rows == NULL computes all of them.  Rows not
+ *                listed are left untouched.
+ * OpenMP (when compiled with it) runs independent output rows in parallel;
+ * each row is computed exactly as above, so the result does not depend on
+ * the thread count.
+ */
+int oracle_paged_attention(double *out, const void *q, const void *k_cache,
+                           const void *v_cache, const int32_t *block_table,
+                           int max_blocks, const int32_t *context_lens, int B,
+                           int Q, int Hq, int Hkv, int D, int bs, int64_t NB,
+                           double scale, int dtype, const int64_t *rows,
+                           int64_t n_rows) {
+  if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens ||
+      B < 0 || Q <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 ||
+      bs <= 0 || max_blocks < 0 || NB < 0 || dtype < 0 || dtype > 2)
+    return ORACLE_ERR_ARG;
+  const int64_t total = (int64_t)B * Q * Hq;
+  const int64_t count = rows ? n_rows : total;
+  int64_t max_len = 1;
+  for (int b = 0; b < B; ++b)
+    if (context_lens[b] > max_len) max_len = context_lens[b];
+  int status = ORACLE_OK;
+
+#pragma omp parallel
+  {
+    double *scores = (double *)malloc(sizeof(double) * (size_t)max_len);
+    if (!scores) {
+#pragma omp atomic write
+      status = ORACLE_ERR_NOMEM;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t n = 0; n < count; ++n) {
+      if (!scores) continue;
+      int64_t r = rows ? rows[n] : n;
+      if (r < 0 || r >= total) {
+#pragma omp atomic write
+        status = ORACLE_ERR_ARG;
+        continue;
+      }
+      int h = (int)(r % Hq);
+      int j = (int)((r / Hq) % Q);
+      int b = (int)(r / ((int64_t)Hq * Q));
+      int st = attend_one(out + r * D, scores, q, k_cache, v_cache, block_table,
+                          max_blocks, context_lens, b, j, h, Q, Hq, Hkv, D, bs,
+                          NB, scale, dtype);
+      if (st != ORACLE_OK) {
+#pragma omp atomic write
+        status = st;
+      }
+    }
+    free(scores);
+  }
+  return status;
+}
+
+/* Number of threads the parallel region above uses (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

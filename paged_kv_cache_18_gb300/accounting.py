@@ -1,0 +1,48 @@
+"""Byte accounting of the paged decode-attention path.
+
+The KV bytes per token follow the formula of "KV cache, prefill va decode"
+(truongducdung, section 03: 2 x layers x kv_heads x head_dim x bytes per
+value, the 2 being K and V) and of "Inference part 1" (brunomaga, section
+"KV cache"); for latent (MLA) caches one latent of kv_lora_rank + rope dims
+is stored per token and layer (same section 03, DeepSeek-V3 row).
+
+``attention_bytes`` is the algorithmic HBM traffic of one attention call:
+every valid K and V row once, q once, the output once, the block-table
+entries and context lengths, plus the split-K partials written and read back.
+"""
+from __future__ import annotations
+
+from typing import Sequence
+
+
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
+                       bytes_per_value: int, latent: bool = False) -> int:
+    """KV-cache bytes one token occupies across all layers."""
+    if latent:  # one shared latent vector (K and V derived from it)
+        return layers * head_dim * bytes_per_value
+    return 2 * layers * kv_heads * head_dim * bytes_per_value
+
+
+def attention_bytes(context_lens: Sequence[int], num_queries: int,
+                    num_heads: int, num_kv_heads: int, head_dim: int,
+                    block_size: int, elt_bytes: int, num_splits_per_seq=None) -> dict:
+    """Algorithmic bytes of one paged attention call, by component."""
+    lens = [max(0, int(x)) for x in context_lens]
+    B = len(lens)
+    kv = 2 * sum(lens) * num_kv_heads * head_dim * elt_bytes
+    qo = B * num_queries * num_heads * head_dim * elt_bytes
+    table = sum(-(-L // block_size) for L in lens) * 4 + B * 4
+    partials = 0
+    if num_splits_per_seq is not None:
+        rows = num_queries * num_heads
+        # fp32 O (head_dim) + one fp32 LSE per split and row, written then read
+        partials = 2 * sum(int(s) for s in num_splits_per_seq) * rows * (head_dim + 1) * 4
+    return {"kv": kv, "q": qo, "out": qo, "table": table, "partials": partials,
+            "total": kv + 2 * qo + table + partials}
+
+
+def append_bytes(num_tokens: int, num_kv_heads: int, head_dim: int,
+                 elt_bytes: int) -> int:
+    """kv_append: read k_new and v_new, write them into the cache, + slots."""
+    rows = 2 * num_tokens * num_kv_heads * head_dim * elt_bytes
+    return 2 * rows + 8 * num_tokens

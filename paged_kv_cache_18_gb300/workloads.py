@@ -1,0 +1,206 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module is the only code that both the CUDA path's tests/benchmark and the
+float64 oracle consume.  It holds none of the attention arithmetic: it draws
+random values, rounds them to the storage type, builds a shuffled block
+table (a host stand-in for the free-block pool of PagedAttention, where
+"logical blocks map to physical blocks anywhere in GPU memory"), assigns the
+cache slots of the new tokens, and poisons every cache row that no sequence
+owns with NaN so that a read outside the context shows up in the output.
+
+Workload recipe (all five named workloads use it):
+  * q, K, V ~ N(0, 1) drawn in float32 from NumPy's PCG64 with a fixed seed,
+    then rounded to nearest-even into the storage dtype;
+  * sequence b owns ceil(L_b / block_size) blocks; the physical ids are a
+    random permutation of range(NB) with NB = owned + ceil(10 %) slack;
+  * the last Q rows of every sequence are the "new" tokens: their K/V rows
+    are returned separately (k_new, v_new) together with their slots, and
+    their cache slots start out poisoned, so the step appends them first.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+STORAGE = {"f32": np.float32, "bf16": np.uint16, "f16": np.uint16}
+ELT_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
+NAN_BITS16 = {"bf16": 0x7FC0, "f16": 0x7E00}
+
+
+def round_f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns, round to nearest even (finite x)."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((bits >> 16) & 1) + np.uint32(0x7FFF)
+    return ((bits + bias) >> 16).astype(np.uint16)
+
+
+def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float32 values into the storage representation of ``dtype``."""
+    if dtype == "f32":
+        return np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == "bf16":
+        return round_f32_to_bf16_bits(x)
+    if dtype == "f16":
+        return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+    raise ValueError(dtype)
+
+
+def _normal_storage(rng: np.random.Generator, shape, dtype: str,
+                    chunk: int = 1 << 24) -> np.ndarray:
+    """N(0,1) values in storage form, drawn in chunks to bound host memory."""
+    out = np.empty(int(np.prod(shape)), dtype=STORAGE[dtype])
+    for lo in range(0, out.size, chunk):
+        hi = min(out.size, lo + chunk)
+        out[lo:hi] = to_storage(rng.standard_normal(hi - lo, dtype=np.float32), dtype)
+    return out.reshape(shape)
+
+
+def _poison_value(dtype: str):
+    return np.float32(np.nan) if dtype == "f32" else np.uint16(NAN_BITS16[dtype])
+
+
+@dataclasses.dataclass
+class Workload:
+    """Shape of one paged-attention call (and the append before it)."""
+    name: str
+    batch: int
+    num_heads: int          # Hq
+    num_kv_heads: int       # Hkv
+    head_dim: int           # D
+    dtype: str              # "f32" | "bf16" | "f16"
+    context_lens: Optional[Sequence[int]] = None   # fixed lengths, or
+    len_range: Optional[tuple] = None               # (lo, hi) inclusive uniform
+    num_queries: int = 1    # Q: 1 = decode, K+1 = speculative verify
+    block_size: int = 16
+    scale: Optional[float] = None                   # None -> 1/sqrt(D)
+    seed: int = 0
+    slack: float = 0.10
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.head_dim)
+
+    def lengths(self) -> np.ndarray:
+        if self.context_lens is not None:
+            lens = np.asarray(self.context_lens, dtype=np.int32)
+            if lens.size == 1 and self.batch > 1:
+                lens = np.full(self.batch, int(lens[0]), dtype=np.int32)
+            return lens
+        lo, hi = self.len_range
+        rng = np.random.Generator(np.random.PCG64(self.seed + 7919))
+        return rng.integers(lo, hi, size=self.batch, endpoint=True).astype(np.int32)
+
+
+# The five named workloads (seed = 1000 + index).
+WORKLOADS = {
+    "tiny": Workload("tiny GPTlite-scale decode", 4, 6, 6, 64, "f32",
+                     context_lens=[17, 64, 100, 256], seed=1001),
+    "llama2_13b": Workload("Llama-2-13B-shaped decode layer", 32, 40, 40, 128,
+                           "bf16", context_lens=[2048], seed=1002),
+    "llama3_8b_gqa": Workload("Llama-3-8B-shaped GQA decode", 128, 32, 8, 128,
+                              "bf16", len_range=(128, 4096), seed=1003),
+    "long_splitk": Workload("long-context small-batch split-K", 2, 32, 8, 128,
+                            "bf16", context_lens=[32768, 65536], seed=1004),
+    "spec_verify": Workload("speculative verify K=4", 16, 32, 8, 128, "bf16",
+                            len_range=(512, 8192), num_queries=5, seed=1005),
+}
+
+
+@dataclasses.dataclass
+class PagedBatch:
+    """Host arrays of one step: append Q new rows per sequence, then attend."""
+    wl: Workload
+    q: np.ndarray             # [B, Q, Hq, D] storage dtype
+    k_cache: np.ndarray       # [NB, Hkv, bs, D] storage dtype (new slots poisoned)
+    v_cache: np.ndarray
+    k_new: np.ndarray         # [B*Q, Hkv, D]
+    v_new: np.ndarray
+    slot_mapping: np.ndarray  # [B*Q] int64
+    block_table: np.ndarray   # [B, max_blocks] int32 (unused entries = -1)
+    context_lens: np.ndarray  # [B] int32 (includes the Q new rows)
+    num_blocks: int
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.context_lens.size else 0
+
+    def kv_bytes(self) -> int:
+        """Bytes of the valid K and V rows one attention call reads."""
+        wl = self.wl
+        return int(2 * int(self.context_lens.clip(min=0).sum()) * wl.num_kv_heads
+                   * wl.head_dim * ELT_BYTES[wl.dtype])
+
+
+def make_batch(wl: Workload, poison: bool = True) -> PagedBatch:
+    """Build the seeded host arrays of ``wl``."""
+    rng = np.random.Generator(np.random.PCG64(wl.seed))
+    B, Q, Hq, Hkv, D, bs = (wl.batch, wl.num_queries, wl.num_heads,
+                            wl.num_kv_heads, wl.head_dim, wl.block_size)
+    lens = wl.lengths()
+    assert lens.shape == (B,)
+    owned = [max(0, -(-int(L) // bs)) for L in lens]
+    total = sum(owned)
+    NB = max(1, total + int(math.ceil(wl.slack * total)))
+    perm = rng.permutation(NB).astype(np.int32)
+    max_blocks = max(1, max(owned) if owned else 1)
+    table = np.full((B, max_blocks), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        table[b, :owned[b]] = perm[pos:pos + owned[b]]
+        pos += owned[b]
+
+    k_cache = _normal_storage(rng, (NB, Hkv, bs, D), wl.dtype)
+    v_cache = _normal_storage(rng, (NB, Hkv, bs, D), wl.dtype)
+    q = _normal_storage(rng, (B, Q, Hq, D), wl.dtype)
+
+    # New rows: the last Q positions of each sequence (those that exist).
+    new_rows = []
+    for b in range(B):
+        for j in range(Q):
+            i = int(lens[b]) - Q + j
+            new_rows.append((b, i))
+    slots = np.full(len(new_rows), -1, dtype=np.int64)
+    k_new = np.empty((len(new_rows), Hkv, D), dtype=STORAGE[wl.dtype])
+    v_new = np.empty_like(k_new)
+    bad = _poison_value(wl.dtype)
+    for t, (b, i) in enumerate(new_rows):
+        if i < 0:
+            k_new[t] = bad
+            v_new[t] = bad
+            continue
+        phys = int(table[b, i // bs])
+        slots[t] = phys * bs + i % bs
+        k_new[t] = k_cache[phys, :, i % bs, :]
+        v_new[t] = v_cache[phys, :, i % bs, :]
+
+    if poison:
+        used = np.zeros(NB, dtype=bool)
+        used[perm[:total]] = True
+        k_cache[~used] = bad
+        v_cache[~used] = bad
+        for b in range(B):
+            L = int(lens[b])
+            if owned[b] and L % bs:
+                last = int(table[b, owned[b] - 1])
+                k_cache[last, :, L % bs:, :] = bad
+                v_cache[last, :, L % bs:, :] = bad
+        for t, (b, i) in enumerate(new_rows):
+            if slots[t] >= 0:
+                phys, off = divmod(int(slots[t]), bs)
+                k_cache[phys, :, off, :] = bad
+                v_cache[phys, :, off, :] = bad
+
+    return PagedBatch(wl, q, k_cache, v_cache, k_new, v_new, slots, table,
+                      lens.astype(np.int32), NB)
+
+
+def storage_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact float64 values of stored elements (for comparing outputs)."""
+    if dtype == "f32":
+        return a.astype(np.float64)
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.view(np.float16).astype(np.float64)

@@ -1,0 +1,101 @@
+"""Planted mistakes in the C oracle must be caught by its pins.
+
+Each mutation below is a plausible slip in ``oracle/pkv_oracle.c`` (a wrong
+index, a dropped term, a flipped sign, a transposed operand).  The test
+compiles a mutated copy into a temporary library, runs a battery of pins on
+it, and requires at least one pin to fail, while the unmutated oracle passes
+all of them.  Every mutation keeps memory accesses in bounds.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import twin
+from paged_kv_cache_18_gb300 import workloads as W
+
+MUTATIONS = {
+    "block index i%bs": ("block_table[(int64_t)b * max_blocks + i / bs]",
+                         "block_table[(int64_t)b * max_blocks + i % bs]"),
+    "row in block off by one": ("+ i % bs) * D;", "+ (i + 1) % bs) * D;"),
+    "gqa map h%Hkv": ("const int g = h / (Hq / Hkv);", "const int g = h % Hkv;"),
+    "mask off by one": ("(int64_t)L - Q + 1 + j;", "(int64_t)L - Q + j;"),
+    "dropped scale": ("scores[i] = scale * dot;", "scores[i] = dot;"),
+    "flipped exp sign": ("exp(scores[i] - m)", "exp(m - scores[i])"),
+    "no normalisation": ("out_row[d] /= denom;", "out_row[d] /= 1.0;"),
+    "K used as V": ("widen(v_cache, v_base + d, dtype)", "widen(k_cache, v_base + d, dtype)"),
+    "query row ignored": ("(((int64_t)b * Q + j) * Hq + h) * D;",
+                          "(((int64_t)b * Q + 0) * Hq + h) * D;"),
+    "append slot offset": ("offset = slot % bs;", "offset = (slot + 1) % bs;"),
+}
+
+PIN_CASES = [
+    W.Workload("gqa spec", 3, 8, 2, 64, "bf16", context_lens=[5, 21, 48],
+               num_queries=3, seed=14),
+    W.Workload("mha f32", 2, 3, 3, 64, "f32", context_lens=[1, 37], seed=15),
+]
+
+
+def _battery(orc) -> list:
+    """Names of the pins ``orc`` fails."""
+    failed = []
+    for wl in PIN_CASES:
+        b = W.make_batch(wl)
+        truth = W.make_batch(wl, poison=False)
+        orc.kv_append(b.k_cache, b.v_cache, b.k_new, b.v_new, b.slot_mapping, wl.dtype)
+        # append pin: every owned slot now holds the unpoisoned value
+        for bi in range(wl.batch):
+            L = int(b.context_lens[bi])
+            got = twin.gather_sequence(b.k_cache, b.block_table[bi], L)
+            want = twin.gather_sequence(truth.k_cache, truth.block_table[bi], L)
+            if not np.array_equal(got.view(np.uint8), want.view(np.uint8)):
+                failed.append(f"append {wl.name}")
+                break
+        try:
+            out = orc.paged_attention(b.q, b.k_cache, b.v_cache, b.block_table,
+                                      b.context_lens, wl.softmax_scale, wl.dtype)
+        except ValueError:
+            failed.append(f"error {wl.name}")
+            continue
+        # paged == contiguous twin
+        o2 = twin.contiguous_attention(b.q, b.k_cache, b.v_cache, b.block_table,
+                                       b.context_lens, wl.softmax_scale, wl.dtype)
+        if not np.allclose(out, o2, rtol=0, atol=1e-12):
+            failed.append(f"twin {wl.name}")
+        # causal prefill by the library routine
+        for bi in range(wl.batch):
+            L, Q = int(b.context_lens[bi]), wl.num_queries
+            k = torch.from_numpy(twin.widen(twin.gather_sequence(b.k_cache, b.block_table[bi], L), wl.dtype))
+            v = torch.from_numpy(twin.widen(twin.gather_sequence(b.v_cache, b.block_table[bi], L), wl.dtype))
+            qf = torch.zeros(L, wl.num_heads, wl.head_dim, dtype=torch.float64)
+            first = max(0, L - Q)
+            qf[first:] = torch.from_numpy(twin.widen(b.q[bi], wl.dtype))[Q - (L - first):]
+            o = torch.nn.functional.scaled_dot_product_attention(
+                qf.transpose(0, 1)[None], k.transpose(0, 1)[None], v.transpose(0, 1)[None],
+                is_causal=True, scale=wl.softmax_scale,
+                enable_gqa=wl.num_heads != wl.num_kv_heads)[0].transpose(0, 1)
+            rows = [j for j in range(Q) if L - Q + j >= 0]
+            want = np.stack([o[L - Q + j].numpy() for j in rows])
+            if not np.allclose(out[bi, rows], want, rtol=0, atol=1e-12):
+                failed.append(f"sdpa {wl.name}")
+                break
+    return failed
+
+
+def test_unmutated_oracle_passes_battery():
+    assert _battery(oracle.default()) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(oracle.SOURCE).read()
+    assert old in src, f"mutation anchor for {name!r} not found"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.compile_library(str(mutated), str(tmp_path / "libmutant.so"))
+    failed = _battery(oracle.Oracle(lib))
+    assert failed, f"planted mistake {name!r} passed every pin"
