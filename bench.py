@@ -1,0 +1,451 @@
+"""Benchmark of the paged decode-attention step on GB300.
+
+One step = the whole hot path over one batch: kv_append of the new K/V rows
+(one per sequence for decode), then paged attention through the block table
+(split-K partials and their log-sum-exp merge when the plan splits).  The
+default workload is the Llama-2-13B-shaped decode layer: batch 32, 40 query /
+40 KV heads, head_dim 128, bf16, every context 2048 rows, block size 16,
+shuffled physical blocks.  Its 1.34 GB of K/V is ten times the L2, so
+consecutive steps read from HBM (no L2 flush is needed).
+
+Prints ONE JSON line (rank 0).  `value` is the KV bytes the attention reads
+per step, summed over ranks, divided by the max-over-ranks step time (GB/s);
+`e2e` is the same metric through the public API with the step's inputs copied
+from pinned host memory and the output read back every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle, timed
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_cache_18_gb300 import accounting  # noqa: E402
+from paged_kv_cache_18_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); decode tokens/sec"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+# Sources whose change invalidates a recorded ncu traffic figure.
+KERNEL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mma.cu",
+                  "paged_kv_cache_18_gb300/csrc/attn_simt.cu",
+                  "paged_kv_cache_18_gb300/csrc/pkv_device.cuh"]
+
+
+# ---------------------------------------------------------------- helpers --
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(PROFILE_DIR, f"attn_{workload}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, with host times."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        where = "during timed region"
+        if not inside:  # timed region shorter than the sampling period
+            nearest = min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))
+            inside, where = [nearest], "nearest sample to a timed region shorter than 50 ms"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        mhz = []
+        for _, p in inside:
+            try:
+                mhz.append(float(p[0]))
+            except ValueError:
+                pass
+            for i, n in enumerate(names):
+                if p[4 + i].lower().startswith("active"):
+                    reasons.add(n)
+        try:
+            max_mhz = float(inside[0][1][1])
+        except ValueError:
+            max_mhz = None
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max_mhz,
+                "reasons": sorted(reasons), "samples": len(inside), "where": where}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_max(value: float, device=None) -> float:
+    """Max of a float over ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------ CPU oracle ---
+def oracle_sample(b: W.PagedBatch, budget_s: float):
+    """Time the float64 oracle on whole sequences of the workload, cycling
+    over them, until about `budget_s` of CPU work; returns (KV bytes covered,
+    seconds, description)."""
+    import oracle
+    wl = b.wl
+    oracle.kv_append(b.k_cache, b.v_cache, b.k_new, b.v_new, b.slot_mapping, wl.dtype)
+    per_seq_rows = wl.num_queries * wl.num_heads
+    done_bytes, elapsed, seqs = 0, 0.0, 0
+    while elapsed < budget_s:
+        bi = seqs % wl.batch
+        rows = np.arange(per_seq_rows, dtype=np.int64) + bi * per_seq_rows
+        t = time.perf_counter()
+        oracle.paged_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                               wl.softmax_scale, wl.dtype, rows=rows)
+        elapsed += time.perf_counter() - t
+        L = int(b.context_lens[bi])
+        done_bytes += 2 * L * wl.num_kv_heads * wl.head_dim * W.ELT_BYTES[wl.dtype]
+        seqs += 1
+    desc = (f"{seqs} sequence passes over the {wl.batch} sequences of the workload (all "
+            f"{wl.num_heads} heads x {wl.num_queries} queries each), float64 C oracle, "
+            f"{oracle.num_threads()} threads, {elapsed:.1f} s")
+    return done_bytes, elapsed, desc
+
+
+def run_reference(args):
+    """The float64 CPU oracle as the reference arm."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    wl = W.WORKLOADS[args.workload]
+    b = W.make_batch(wl)
+    per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(b, per_step_budget / 4)
+    total_bytes, total_s = 0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        nbytes, secs, desc = oracle_sample(b, per_step_budget)
+        total_bytes += nbytes
+        total_s += secs
+    value = total_bytes / total_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl, b),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": desc + f"; ~{per_step_budget:.1f} s per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(wl: W.Workload, b: W.PagedBatch) -> dict:
+    return {"workload": wl.name, "batch": wl.batch, "num_heads": wl.num_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+            "block_size": wl.block_size, "num_queries": wl.num_queries,
+            "context_lens": ("all " + str(int(b.context_lens[0]))
+                             if len(set(b.context_lens.tolist())) == 1 else
+                             f"{int(b.context_lens.min())}..{int(b.context_lens.max())}"
+                             f" (sum {int(b.context_lens.sum())})"),
+            "kv_bytes_per_step": b.kv_bytes(),
+            "l2": f"no flush: the step reads {b.kv_bytes() / 1e9:.2f} GB of K/V, > 129 MB L2",
+            "step": f"kv_append of {wl.batch * wl.num_queries} rows + "
+                    + ("paged_decode_attention" if wl.num_queries == 1
+                       else "spec_verify_attention")}
+
+
+# ------------------------------------------------------------ GPU arm ------
+def dev_tensor(a: np.ndarray, dtype: str, device):
+    """Upload a host array in storage form as a torch tensor of `dtype`."""
+    import torch
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(tdt)
+    return torch.from_numpy(a).to(device)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_cache_18_gb300 import build as pkv_build
+    if rank == 0 or not os.path.exists(pkv_build.LIB):
+        pkv_build.build()
+    barrier()
+    import paged_kv_cache_18_gb300 as pkv
+
+    wl = W.WORKLOADS[args.workload]
+    if rank > 0:
+        wl = W.Workload(**{**wl.__dict__, "seed": wl.seed + 100 * rank})
+    b = W.make_batch(wl)
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl.dtype]
+    k_cache = dev_tensor(b.k_cache, wl.dtype, dev)
+    v_cache = dev_tensor(b.v_cache, wl.dtype, dev)
+    k_new = dev_tensor(b.k_new, wl.dtype, dev)
+    v_new = dev_tensor(b.v_new, wl.dtype, dev)
+    q = dev_tensor(b.q, wl.dtype, dev)
+    if wl.num_queries == 1:
+        q = q[:, 0].contiguous()
+    slots = torch.from_numpy(b.slot_mapping).to(dev)
+    table = torch.from_numpy(b.block_table).to(dev)
+    lens = torch.from_numpy(b.context_lens).to(dev)
+    out = torch.empty_like(q)
+    Q = wl.num_queries
+    plan = pkv.plan(wl.batch, Q, wl.num_heads, wl.num_kv_heads, wl.head_dim,
+                    b.max_context_len, dt, kernel=args.kernel, split_blocks=args.split_blocks)
+    ws = torch.empty(max(16, plan["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    max_ctx = b.max_context_len
+    attn = pkv.paged_decode_attention if Q == 1 else pkv.spec_verify_attention
+
+    def step():
+        pkv.kv_append(k_new, v_new, k_cache, v_cache, slots)
+        attn(q, k_cache, v_cache, table, lens, scale=wl.softmax_scale, max_context_len=max_ctx,
+             out=out, workspace=ws, kernel=args.kernel, split_blocks=args.split_blocks)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # Device-timed region: K steps, events around the attention of each step.
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
+    if sampler:
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        pkv.kv_append(k_new, v_new, k_cache, v_cache, slots)
+        ev[i][0].record(stream)
+        attn(q, k_cache, v_cache, table, lens, scale=wl.softmax_scale, max_context_len=max_ctx,
+             out=out, workspace=ws, kernel=args.kernel, split_blocks=args.split_blocks)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    barrier()
+    step_ms_local = start.elapsed_time(end) / K
+    attn_ms = statistics.mean(a.elapsed_time(z) for a, z in ev)
+    step_ms = dist_max(step_ms_local, dev)
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    # End to end through the public API: inputs from pinned host memory,
+    # output read back, every step.
+    e2e = None
+    if not args.no_e2e:
+        host = {n: t.cpu().pin_memory() for n, t in
+                (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots),
+                 ("table", table), ("lens", lens))}
+        out_host = torch.empty_like(out, device="cpu").pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        dq, dkn, dvn, dsl, dtb, dln = (torch.empty_like(x) for x in (q, k_new, v_new, slots,
+                                                                     table, lens))
+        E = max(3, min(K, 200))
+
+        def e2e_step():
+            dq.copy_(host["q"], non_blocking=True)
+            dkn.copy_(host["k_new"], non_blocking=True)
+            dvn.copy_(host["v_new"], non_blocking=True)
+            dsl.copy_(host["slots"], non_blocking=True)
+            dtb.copy_(host["table"], non_blocking=True)
+            dln.copy_(host["lens"], non_blocking=True)
+            pkv.kv_append(dkn, dvn, k_cache, v_cache, dsl)
+            attn(dq, k_cache, v_cache, dtb, dln, scale=wl.softmax_scale,
+                 max_context_len=max_ctx, out=out, workspace=ws, kernel=args.kernel,
+                 split_blocks=args.split_blocks)
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(E):
+            e2e_step()
+        e2e_s = dist_max((time.perf_counter() - t0) / E, dev)
+        e2e = {"value": dist_sum(b.kv_bytes(), dev) / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
+               "ms_per_step": 1e3 * e2e_s}
+
+    total_kv = dist_sum(b.kv_bytes(), dev)
+    total_tokens = dist_sum(wl.batch * Q, dev)
+    if rank != 0:
+        return 0
+
+    value = total_kv / (step_ms * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    splits_per_seq = None
+    if plan["num_splits"] > 1:
+        nblk = [-(-int(L) // wl.block_size) for L in b.context_lens]
+        splits_per_seq = [max(1, -(-n // plan["split_blocks"])) for n in nblk]
+    algo = accounting.attention_bytes(b.context_lens.tolist(), Q, wl.num_heads, wl.num_kv_heads,
+                                      wl.head_dim, wl.block_size, W.ELT_BYTES[wl.dtype],
+                                      splits_per_seq)
+    achieved = algo["total"] / (attn_ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    traffic = recorded_traffic(args.workload)
+    launches_per_step = 2 + (1 if plan["num_splits"] > 1 else 0)
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        nbytes, secs, desc = oracle_sample(W.make_batch(W.WORKLOADS[args.workload]),
+                                           args.cpu_budget)
+        import oracle
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": workload_config(wl, b),
+        "pct_of_hbm_peak": 100.0 * value / peak,
+        "tokens_per_s": total_tokens / (step_ms * 1e-3),
+        "attention_ms": attn_ms,
+        "plan": {k: plan[k] for k in ("kernel", "rows_per_cta", "row_chunks", "split_blocks",
+                                      "num_splits", "grid_x", "grid_y", "grid_z",
+                                      "ctas_per_sm")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": algo["total"],
+                     "kernel": "attention (+ merge when split)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(W.WORKLOADS), default="llama2_13b")
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--split-blocks", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

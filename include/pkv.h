@@ -1,0 +1,250 @@
+/*
+ * pkv.h -- C ABI of libpkv: decode-phase attention over a paged KV cache on
+ * GB300 (sm_103a).
+ *
+ * The operations follow the pages' statement of the problem:
+ *   - "Inference part 1" (brunomaga), section "KV cache": each decode step
+ *     computes q, k, v for the new token only, writes the new key and value
+ *     into the cache in place (a static cache) and attends over every cached
+ *     row; queries are not cached.  Several new tokens on top of a cache see
+ *     the cached rows and the new rows up to themselves (the shifted causal
+ *     mask of scaled_dot_product_attention_kv_cache).
+ *   - same page, section "PagedAttention: memory management for the KV
+ *     cache": the cache is split into fixed-size blocks allocated on demand;
+ *     a per-sequence block table maps logical blocks to physical blocks
+ *     anywhere in GPU memory, and the attention kernel reads through it.
+ *     "KV cache, prefill va decode" (truongducdung), section 05, "Block
+ *     table": 16 tokens per block in vLLM; a new block only when the last one
+ *     is full.
+ *   - "Inference part 1", section "Why attention matters": the attention
+ *     equation softmax(Q K^T / sqrt(d_head)) V; section "Smaller KV caches:
+ *     MQA, GQA and MLA": consecutive query heads share one KV head.
+ *   - same page, section "FlashDecoding": the keys and values are split
+ *     along the sequence, each chunk yields a partial output and its softmax
+ *     statistics, and a final reduction rescales them as in the online
+ *     softmax ("KV cache, prefill va decode", section 07, Flash-Decoding:
+ *     the log-sum-exp of each chunk is kept and merged).
+ *   - "Inference part 2" (brunomaga), section "Speculative decoding": the
+ *     target scores the last accepted token and the K drafts (K + 1 queries)
+ *     in one pass.
+ *
+ * Layouts (all row-major, C order; "elt" is the element type of `dtype`):
+ *   k_cache, v_cache : [num_blocks, num_kv_heads, block_size, head_dim] elt
+ *                      (one (block, kv-head) tile is contiguous)
+ *   block_table      : [batch, max_blocks_per_seq] int32; entry n of row b is
+ *                      the physical block holding rows n*block_size ..
+ *                      (n+1)*block_size - 1 of sequence b.  Entries past the
+ *                      sequence's last block are never read.
+ *   context_lens     : [batch] int32, L_b = rows of sequence b INCLUDING the
+ *                      new rows (the token just appended; for speculative
+ *                      verification the K + 1 verified tokens).
+ *   q, out (decode)  : [batch, num_heads, head_dim] elt
+ *   q, out (verify)  : [batch, num_queries, num_heads, head_dim] elt
+ *   Query head h reads KV head h / (num_heads / num_kv_heads).
+ *   Query row j (0-based) of a sequence sees rows i <= L_b - num_queries + j.
+ *   A query row that sees no row (e.g. L_b = 0) gets a zero output.
+ *
+ * Ownership and streams: the caller owns every buffer (device pointers,
+ * including the workspace and the optional error word).  The library never
+ * allocates, frees or synchronises in these calls; all work is enqueued on
+ * `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *
+ * Errors: argument errors are reported synchronously with nothing enqueued.
+ * A failed launch returns PKV_ERR_CUDA.  Device-side precondition violations
+ * (a slot or block id out of range, a context longer than max_context_len)
+ * never fault: the offending row or block is skipped and, when `error_word`
+ * (a device int32, caller-zeroed) is given, its first violation code
+ * (PKV_DEVERR_*) is recorded there.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent shapes */
+  PKV_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim, block_size, dtype */
+  PKV_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
+  PKV_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
+  PKV_ERR_ALIGNMENT = 5    /* a tensor pointer is not 16-byte aligned */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
+
+/* Codes the kernels record in the optional device error word. */
+enum {
+  PKV_DEVERR_NONE = 0,
+  PKV_DEVERR_SLOT = 1,        /* kv_append: slot >= num_blocks * block_size */
+  PKV_DEVERR_BLOCK_ID = 2,    /* block_table entry outside [0, num_blocks) */
+  PKV_DEVERR_CONTEXT_LEN = 3, /* context_lens[b] > max_context_len or > table */
+  PKV_DEVERR_TIMEOUT = 4      /* a shared-memory copy did not arrive in time */
+};
+
+/* Kernel families. */
+typedef enum pkv_kernel {
+  PKV_KERNEL_AUTO = 0,
+  PKV_KERNEL_SIMT = 1, /* CUDA-core dot products (any dtype; fp32 path) */
+  PKV_KERNEL_MMA = 2   /* tensor-core tiles (bf16 / fp16 only) */
+} pkv_kernel;
+
+/* Optional launch controls (pass NULL for the planner's choice). */
+typedef struct pkv_options {
+  int kernel;       /* pkv_kernel */
+  int split_blocks; /* 0: planner; > 0: KV blocks per split-K chunk */
+} pkv_options;
+
+/* What one attention call launches (see pkv_attention_plan). */
+typedef struct pkv_plan {
+  int kernel;             /* PKV_KERNEL_SIMT or PKV_KERNEL_MMA */
+  int rows_per_cta;       /* query rows (queries x heads of one KV head) per CTA */
+  int row_chunks;         /* CTAs that share one (sequence, KV head) */
+  int split_blocks;       /* KV blocks per split */
+  int num_splits;         /* splits of the longest sequence; 1 = no merge */
+  int grid_x, grid_y, grid_z;
+  int threads_per_cta;
+  int ctas_per_sm;        /* occupancy the planner assumed */
+  size_t smem_bytes;      /* dynamic shared memory per CTA */
+  size_t workspace_bytes; /* device workspace the call needs (0 = none) */
+} pkv_plan;
+
+/* Human-readable name of a status code (static string). */
+PKV_API const char *pkv_status_string(pkv_status status);
+
+/* Library version string, e.g. "pkv 0.1.0 sm_103a". */
+PKV_API const char *pkv_version(void);
+
+/*
+ * pkv_kv_append -- write the K/V rows of new tokens into their cache slots.
+ * "Inference part 1", section "KV cache" (in-place write of a static cache);
+ * "Inference part 2", GPTlite_StaticCache (k_cache[..., input_pos] = k);
+ * "Efficient Inference" (obvix), the in-place slice write; in paged form a
+ * slot s is row s % block_size of physical block s / block_size
+ * ("KV cache, prefill va decode", section 05, "Block table").
+ *
+ *   k_new, v_new : [num_tokens, num_kv_heads, head_dim] elt, device
+ *   k_cache, v_cache : [num_blocks, num_kv_heads, block_size, head_dim], device,
+ *                  written in place
+ *   slot_mapping : [num_tokens] int64, device; slot < 0 = padding, skipped.
+ *                  Slots must be distinct within one call (else the row
+ *                  written last is unspecified).
+ * The copy is bit-exact.  head_dim * sizeof(elt) must be a multiple of 16 and
+ * every pointer 16-byte aligned (slot_mapping 8-byte).
+ */
+PKV_API pkv_status pkv_kv_append(const void *k_new, const void *v_new, void *k_cache,
+                         void *v_cache, const int64_t *slot_mapping,
+                         int64_t num_tokens, int num_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, pkv_dtype dtype,
+                         int32_t *error_word, pkv_stream_t stream);
+
+/*
+ * pkv_attention_plan -- the launch an attention call with these sizes makes
+ * on the current device (kernel family, split-K partition, grid, workspace).
+ * num_queries = 1 for decode.  Pure host computation plus device attribute
+ * queries; enqueues nothing.
+ */
+PKV_API pkv_status pkv_attention_plan(int batch, int num_queries, int num_heads,
+                              int num_kv_heads, int head_dim, int block_size,
+                              int max_context_len, pkv_dtype dtype,
+                              const pkv_options *options, pkv_plan *plan);
+
+/*
+ * pkv_attention_plan_for -- the same plan for a device with `num_sms` SMs
+ * and `ctas_per_sm` resident CTAs of the chosen kernel (0 = estimate from
+ * shared memory).  Needs no GPU.
+ */
+PKV_API pkv_status pkv_attention_plan_for(int batch, int num_queries, int num_heads,
+                                  int num_kv_heads, int head_dim,
+                                  int block_size, int max_context_len,
+                                  pkv_dtype dtype, const pkv_options *options,
+                                  int num_sms, int ctas_per_sm, pkv_plan *plan);
+
+/*
+ * pkv_attention_workspace_size -- device workspace bytes an attention call
+ * with these sizes needs on the current device (the split-K partials: one
+ * float32 output vector and one float32 log-sum-exp per query row and split).
+ * 0 when the plan does not split.
+ */
+PKV_API pkv_status pkv_attention_workspace_size(int batch, int num_queries,
+                                        int num_heads, int num_kv_heads,
+                                        int head_dim, int block_size,
+                                        int max_context_len, pkv_dtype dtype,
+                                        const pkv_options *options,
+                                        size_t *bytes);
+
+/*
+ * pkv_paged_decode_attention -- one query per sequence:
+ *   out[b, h, :] = sum_i softmax_i(scale * <q[b,h], K_i>) V_i
+ * over rows i < L_b of sequence b read through the block table, with the KV
+ * head h / (num_heads / num_kv_heads) ("Inference part 1", sections "Why
+ * attention matters", "PagedAttention", "Smaller KV caches"; the online
+ * softmax of section "FlashAttention"; the split-K partition and merge of
+ * section "FlashDecoding").
+ *
+ *   out, q        : [batch, num_heads, head_dim] elt, device
+ *   block_table   : [batch, max_blocks_per_seq] int32, device
+ *   context_lens  : [batch] int32, device, 0 <= L_b <= max_context_len
+ *   max_context_len: host-side upper bound of context_lens (sizes the
+ *                   split-K grid; no device read is made to find it)
+ *   scale         : softmax scale (1/sqrt(head_dim) for standard attention)
+ *   workspace     : device buffer of pkv_attention_workspace_size() bytes
+ *                   (may be NULL when that size is 0), 16-byte aligned
+ *   options       : NULL or launch controls; error_word: NULL or device int32
+ * Supported: head_dim in {64, 128, 256}, block_size 16, dtype F32/BF16/F16.
+ */
+PKV_API pkv_status pkv_paged_decode_attention(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_table, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int batch,
+    int num_heads, int num_kv_heads, int head_dim, int block_size,
+    int64_t num_blocks, float scale, pkv_dtype dtype, void *workspace,
+    size_t workspace_bytes, const pkv_options *options, int32_t *error_word,
+    pkv_stream_t stream);
+
+/*
+ * pkv_spec_verify_attention -- num_queries = K + 1 queries per sequence (the
+ * last accepted token and K drafts, "Inference part 2", section "Speculative
+ * decoding"), causal among themselves: query j sees rows
+ * i <= L_b - num_queries + j (the shifted mask tril(diagonal = Sk - Sq) of
+ * "Inference part 1", section "KV cache").  The drafts' K/V rows must already
+ * be in the cache (pkv_kv_append) and counted in context_lens.
+ *
+ *   out, q : [batch, num_queries, num_heads, head_dim] elt, device
+ * Other arguments as for pkv_paged_decode_attention; num_queries = 1 is
+ * exactly pkv_paged_decode_attention.
+ */
+PKV_API pkv_status pkv_spec_verify_attention(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_table, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int batch,
+    int num_queries, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, float scale, pkv_dtype dtype,
+    void *workspace, size_t workspace_bytes, const pkv_options *options,
+    int32_t *error_word, pkv_stream_t stream);
+
+/*
+ * pkv_read_error_word -- copy the device error word to *host_code after all
+ * work on `stream` (synchronises the stream; not for the hot path).
+ */
+PKV_API pkv_status pkv_read_error_word(const int32_t *error_word, int32_t *host_code,
+                               pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

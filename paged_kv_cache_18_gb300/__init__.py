@@ -1,0 +1,10 @@
+"""GB300-native paged KV-cache decode attention.
+
+The compute path is ``libpkv.so`` (hand-written CUDA for sm_103a behind the C
+ABI in ``include/pkv.h``); this package is its thin Python binding plus the
+seeded workload generator and byte accounting used by the tests and the
+benchmark.  Build the library with ``paged_kv_cache_18_gb300.build.build()``.
+"""
+from .binding import (PKV_KERNEL_AUTO, PKV_KERNEL_MMA, PKV_KERNEL_SIMT, PkvError,  # noqa: F401
+                      kv_append, paged_decode_attention, plan, plan_for, read_error_word,
+                      spec_verify_attention, version, workspace_size)

@@ -1,0 +1,269 @@
+"""Thin ctypes binding of libpkv (include/pkv.h): argument marshalling only.
+
+Every call checks dtypes, devices, shapes and contiguity of the torch tensors,
+then passes raw device pointers, sizes and the current CUDA stream to the C
+ABI; all the work runs in the library's CUDA kernels.  PyTorch only supplies
+device memory and streams.  There is no fallback: if ``libpkv.so`` has not
+been built, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpkv.so")
+_lock = threading.Lock()
+_lib = None
+
+PKV_KERNEL_AUTO, PKV_KERNEL_SIMT, PKV_KERNEL_MMA = 0, 1, 2
+DEVERR_NAMES = {0: "none", 1: "slot out of range", 2: "block id out of range",
+                3: "context length over max_context_len or the table",
+                4: "shared-memory copy timed out"}
+_DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+# Every symbol include/pkv.h declares.
+EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_plan",
+            "pkv_attention_plan_for", "pkv_attention_workspace_size",
+            "pkv_paged_decode_attention", "pkv_spec_verify_attention",
+            "pkv_read_error_word")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} failed: {message} (status {status})")
+        self.status = status
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("split_blocks", ctypes.c_int)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
+                ("row_chunks", ctypes.c_int), ("split_blocks", ctypes.c_int),
+                ("num_splits", ctypes.c_int), ("grid_x", ctypes.c_int),
+                ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int),
+                ("threads_per_cta", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` "
+                    "(there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+            f32 = ctypes.c_float
+            opt = ctypes.POINTER(Options)
+            plan = ctypes.POINTER(Plan)
+            L.pkv_status_string.argtypes = [i32]
+            L.pkv_status_string.restype = ctypes.c_char_p
+            L.pkv_version.argtypes = []
+            L.pkv_version.restype = ctypes.c_char_p
+            L.pkv_kv_append.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, vp, vp]
+            L.pkv_attention_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, opt, plan]
+            L.pkv_attention_plan_for.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, opt,
+                                                 i32, i32, plan]
+            L.pkv_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
+                                                       opt, ctypes.POINTER(sz)]
+            L.pkv_paged_decode_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                                     i32, i32, i32, i64, f32, i32, vp, sz, opt,
+                                                     vp, vp]
+            L.pkv_spec_verify_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                                    i32, i32, i32, i32, i64, f32, i32, vp, sz,
+                                                    opt, vp, vp]
+            L.pkv_read_error_word.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+            for name in EXPORTED:
+                if name not in ("pkv_status_string", "pkv_version"):
+                    getattr(L, name).restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise PkvError(fn, status, lib().pkv_status_string(status).decode())
+
+
+def version() -> str:
+    return lib().pkv_version().decode()
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _opts(kernel: int, split_blocks: int):
+    if kernel == 0 and split_blocks == 0:
+        return None
+    return ctypes.byref(Options(kernel, split_blocks))
+
+
+def _need(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cache_args(k_cache, v_cache):
+    _need(k_cache.is_cuda and v_cache.is_cuda, "caches must be CUDA tensors")
+    _need(k_cache.dim() == 4 and k_cache.shape == v_cache.shape,
+          "k_cache/v_cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    _need(k_cache.dtype == v_cache.dtype and k_cache.dtype in _DTYPE, "cache dtype")
+    _need(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
+    return k_cache.shape
+
+
+def _err_ptr(error_word: Optional[torch.Tensor]):
+    if error_word is None:
+        return None
+    _need(error_word.dtype == torch.int32 and error_word.is_cuda and error_word.numel() >= 1,
+          "error_word must be a CUDA int32 tensor")
+    return error_word.data_ptr()
+
+
+def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+              error_word: Optional[torch.Tensor] = None) -> None:
+    """Write k_new/v_new [T, Hkv, D] into slots ``slot_mapping`` [T] (int64,
+    negative = skip) of the paged caches, in place (pkv_kv_append)."""
+    NB, Hkv, bs, D = _cache_args(k_cache, v_cache)
+    T = k_new.shape[0]
+    _need(k_new.shape == (T, Hkv, D) and v_new.shape == (T, Hkv, D), "k_new/v_new shape")
+    _need(k_new.dtype == k_cache.dtype == v_new.dtype, "dtype mismatch")
+    _need(k_new.is_contiguous() and v_new.is_contiguous(), "k_new/v_new must be contiguous")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.shape == (T,)
+          and slot_mapping.is_cuda and slot_mapping.is_contiguous(), "slot_mapping int64 [T]")
+    _check("pkv_kv_append", lib().pkv_kv_append(
+        k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        slot_mapping.data_ptr(), T, Hkv, D, bs, NB, _DTYPE[k_cache.dtype],
+        _err_ptr(error_word), _stream(k_cache)))
+
+
+def plan(batch: int, num_queries: int, num_heads: int, num_kv_heads: int, head_dim: int,
+         max_context_len: int, dtype: torch.dtype, block_size: int = 16, kernel: int = 0,
+         split_blocks: int = 0) -> dict:
+    """The launch an attention call with these sizes makes on the current device."""
+    p = Plan()
+    _check("pkv_attention_plan", lib().pkv_attention_plan(
+        batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+        _DTYPE[dtype], _opts(kernel, split_blocks), ctypes.byref(p)))
+    return p.as_dict()
+
+
+def plan_for(batch: int, num_queries: int, num_heads: int, num_kv_heads: int, head_dim: int,
+             max_context_len: int, dtype: torch.dtype, num_sms: int, ctas_per_sm: int = 0,
+             block_size: int = 16, kernel: int = 0, split_blocks: int = 0) -> dict:
+    """The plan for a device with ``num_sms`` SMs (no GPU needed)."""
+    p = Plan()
+    _check("pkv_attention_plan_for", lib().pkv_attention_plan_for(
+        batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+        _DTYPE[dtype], _opts(kernel, split_blocks), num_sms, ctas_per_sm, ctypes.byref(p)))
+    return p.as_dict()
+
+
+def workspace_size(batch: int, num_queries: int, num_heads: int, num_kv_heads: int,
+                   head_dim: int, max_context_len: int, dtype: torch.dtype,
+                   block_size: int = 16, kernel: int = 0, split_blocks: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check("pkv_attention_workspace_size", lib().pkv_attention_workspace_size(
+        batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+        _DTYPE[dtype], _opts(kernel, split_blocks), ctypes.byref(n)))
+    return int(n.value)
+
+
+def _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_context_len, out,
+               workspace, kernel, split_blocks, error_word, num_queries):
+    NB, Hkv, bs, D = _cache_args(k_cache, v_cache)
+    B = q.shape[0]
+    Hq = q.shape[-2]
+    _need(q.shape[-1] == D and q.dtype == k_cache.dtype and q.is_cuda and q.is_contiguous(),
+          "q must be a contiguous CUDA tensor of the cache dtype and head_dim")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2
+          and block_table.shape[0] == B and block_table.is_contiguous() and block_table.is_cuda,
+          "block_table must be a contiguous CUDA int32 [batch, max_blocks_per_seq]")
+    _need(context_lens.dtype == torch.int32 and context_lens.shape == (B,)
+          and context_lens.is_cuda and context_lens.is_contiguous(),
+          "context_lens must be a contiguous CUDA int32 [batch]")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0  # device read
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
+    need = workspace_size(B, num_queries, Hq, Hkv, D, max_context_len, q.dtype, bs, kernel,
+                          split_blocks)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    L = lib()
+    args_common = (out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                   block_table.data_ptr(), block_table.shape[1], context_lens.data_ptr(),
+                   max_context_len, B)
+    if num_queries == 1:
+        st = L.pkv_paged_decode_attention(*args_common, Hq, Hkv, D, bs, NB, float(scale),
+                                          _DTYPE[q.dtype], ws_ptr, ws_bytes,
+                                          _opts(kernel, split_blocks), _err_ptr(error_word),
+                                          _stream(q))
+        _check("pkv_paged_decode_attention", st)
+    else:
+        st = L.pkv_spec_verify_attention(*args_common, num_queries, Hq, Hkv, D, bs, NB,
+                                         float(scale), _DTYPE[q.dtype], ws_ptr, ws_bytes,
+                                         _opts(kernel, split_blocks), _err_ptr(error_word),
+                                         _stream(q))
+        _check("pkv_spec_verify_attention", st)
+    return out
+
+
+def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_table: torch.Tensor, context_lens: torch.Tensor,
+                           scale: Optional[float] = None, max_context_len: Optional[int] = None,
+                           out: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, kernel: int = 0,
+                           split_blocks: int = 0,
+                           error_word: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode attention: q [B, Hq, D] -> out [B, Hq, D] over the paged cache
+    (pkv_paged_decode_attention).  Pass ``max_context_len`` (a host bound of
+    context_lens) to avoid a device read; pass ``workspace`` to avoid an
+    allocation when the plan splits."""
+    _need(q.dim() == 3, "q must be [batch, num_heads, head_dim]")
+    return _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_context_len,
+                      out, workspace, kernel, split_blocks, error_word, 1)
+
+
+def spec_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          block_table: torch.Tensor, context_lens: torch.Tensor,
+                          scale: Optional[float] = None, max_context_len: Optional[int] = None,
+                          out: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, kernel: int = 0,
+                          split_blocks: int = 0,
+                          error_word: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Speculative verification: q [B, K+1, Hq, D] -> out of the same shape;
+    query j sees rows <= L_b - (K+1) + j (pkv_spec_verify_attention)."""
+    _need(q.dim() == 4, "q must be [batch, num_queries, num_heads, head_dim]")
+    return _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_context_len,
+                      out, workspace, kernel, split_blocks, error_word, q.shape[1])
+
+
+def read_error_word(error_word: torch.Tensor) -> int:
+    """Synchronise the current stream and return the device error code."""
+    code = ctypes.c_int32(0)
+    _check("pkv_read_error_word", lib().pkv_read_error_word(
+        error_word.data_ptr(), ctypes.byref(code), _stream(error_word)))
+    return int(code.value)

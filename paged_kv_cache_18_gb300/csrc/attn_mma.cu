@@ -1,0 +1,412 @@
+// attn_mma.cu -- paged decode / speculative-verify attention on tensor cores
+// (bf16 and fp16 caches).
+//
+// One CTA serves one (sequence b, KV head, row chunk, split): the NC query
+// rows that share the KV head (the group of query heads of grouped-query
+// attention x the verified queries), so every K/V byte of a block is read
+// from HBM once for all of them ("Inference part 1", section "Smaller KV
+// caches: MQA, GQA and MLA": consecutive query heads share one KV head).
+//
+// Data movement.  Each warp owns the blocks w, w + W, w + 2W, ... of the
+// split and a private ring of NS shared-memory stages.  One lane issues, per
+// block, tiled TMA copies (cp.async.bulk.tensor) of the block's K and V tiles
+// straight from the physical block named by the block table ("Inference part
+// 1", section "PagedAttention": the kernel reads the blocks through the
+// table), with the 128-byte swizzle so that the ldmatrix reads below are
+// bank-conflict free.  Completion is counted on one mbarrier per stage.
+//
+// Math, per 16-row block, in the transposed orientation (keys on the MMA's
+// M side so that a handful of query rows only pad N up to 8):
+//   S^T[16 x NC] = K[16 x D] . Q^T[D x NC]          (mma.sync m16n8k16)
+//   online softmax over the keys of each column ("Inference part 1",
+//   section "FlashAttention", the m / l / O recurrence; "KV cache, prefill
+//   va decode", section 07, online softmax), in log2 units;
+//   O^T[D x NC] += V^T[D x 16] . P^T[16 x NC]       (P split into a bf16/fp16
+//   high and low part, two MMAs, so that rounding P costs no accuracy)
+// P^T's operand layout is obtained from S^T's accumulator layout with
+// movmatrix.trans.  Rows past the context and masked (verify) entries get
+// -inf scores; the V^T fragments of rows past the context are zeroed, so
+// NaN-filled unused rows never reach the output.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+template <int D> struct MmaGeom {
+  static constexpr int kParts = D / 64;                 // 128-byte panels per row
+  static constexpr int kPanelBytes = kBlockSize * 128;  // 2 KB
+  static constexpr int kTileBytes = kParts * kPanelBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;    // K tile + V tile
+  static constexpr int kSteps = D / 16;
+};
+
+// Byte offset of element (row, d) (d a multiple of 8) in a swizzled tile.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int d) {
+  const int part = d >> 6;
+  const int chunk = (d & 63) >> 3;
+  return part * MmaGeom<D>::kPanelBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <typename T, int D, int NT, int W, int NS>
+__global__ void __launch_bounds__(W * 32)
+    attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+  using G = MmaGeom<D>;
+  constexpr int NC = NT * 8;  // query columns of this CTA (padded)
+  constexpr int KS = G::kSteps;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_base = smem_base + W * NS * G::kStageBytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y / p.row_chunks;
+  const int chunk = blockIdx.y - kvh * p.row_chunks;
+  const int b = blockIdx.z;
+
+  const SeqExtent ext = seq_extent(p, b, split == 0 && chunk == 0 && kvh == 0 &&
+                                             threadIdx.x == 0);
+  const int L = ext.L;
+  const int blk_begin = split * p.split_blocks;
+  if (split > 0 && blk_begin >= ext.nblk) return;  // this sequence has fewer splits
+  const int blk_end = min(blk_begin + p.split_blocks, ext.nblk);
+  const int nspan = max(blk_end - blk_begin, 0);
+  const int n_my = nspan > warp ? (nspan - warp + W - 1) / W : 0;
+
+  // Q^T operand fragments (B operand: k = head dim, n = query column).
+  uint32_t qf[KS][NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int64_t row = cta_row_index(p, b, kvh, chunk, nt * 8 + g);
+    const T *qrow = reinterpret_cast<const T *>(p.q) + (row < 0 ? 0 : row) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qf[ks][nt][0] = row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
+      qf[ks][nt][1] = row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * c);
+    }
+  }
+  // Visible-row limit of the two columns this thread holds per n-tile.
+  int lim[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) lim[nt][e] = cta_row_limit(p, L, chunk, nt * 8 + 2 * c + e);
+  const int mask_from = L - p.num_queries + 1;  // first row some column cannot see
+
+  // Online-softmax state.
+  float o[KS][NT][4];
+  float m[NT][2], l[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt][0] = m[nt][1] = -INFINITY;
+    l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+  }
+
+  // Per-warp pipeline.
+  const uint32_t my_bars = bar_base + warp * NS * 8;
+  const uint32_t my_stages = smem_base + warp * NS * G::kStageBytes;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) mbar_init(my_bars + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int32_t *table = p.block_table + static_cast<int64_t>(b) * p.max_blocks_per_seq +
+                         blk_begin + warp;
+  auto load_entries = [&](int chunk32) -> int {
+    const int i = chunk32 * 32 + lane;
+    return i < n_my ? __ldg(table + static_cast<int64_t>(i) * W) : -1;
+  };
+  int tab_cur = load_entries(0);
+  int tab_next = load_entries(1);
+  uint32_t bad_mask = 0;
+
+  // Issue the copies of my i-th block into stage i % NS (all lanes call).
+  auto issue = [&](int i) {
+    if ((i & 31) == 0 && i > 0) {
+      tab_cur = tab_next;
+      tab_next = load_entries((i >> 5) + 1);
+    }
+    const int v = __shfl_sync(kFull, tab_cur, i & 31);
+    const bool bad = v < 0 || static_cast<int64_t>(v) >= p.num_blocks;
+    bad_mask = bad ? (bad_mask | (1u << (i & 31))) : (bad_mask & ~(1u << (i & 31)));
+    if (lane == 0) {
+      if (bad) record_error(p.err, PKV_DEVERR_BLOCK_ID);
+      const int phys = bad ? 0 : v;
+      const int s = i % NS;
+      const uint32_t bar = my_bars + 8 * s;
+      const uint32_t st = my_stages + s * G::kStageBytes;
+      mbar_arrive_expect_tx(bar, G::kStageBytes);
+#pragma unroll
+      for (int part = 0; part < G::kParts; ++part)
+        tma_load_4d(st + part * G::kPanelBytes, &kmap, bar, part * 64, 0, kvh, phys);
+#pragma unroll
+      for (int part = 0; part < G::kParts; ++part)
+        tma_load_4d(st + G::kTileBytes + part * G::kPanelBytes, &vmap, bar, part * 64, 0, kvh,
+                    phys);
+    }
+  };
+
+  const int npre = min(NS, n_my);
+  for (int i = 0; i < npre; ++i) issue(i);
+  int issued = npre;
+
+  bool timed_out = false;
+  int issued_done = 0;  // blocks whose copies are known to have landed
+  for (int i = 0; i < n_my; ++i) {
+    const int s = i % NS;
+    if (!mbar_wait_bounded(my_bars + 8 * s, (i / NS) & 1)) {
+      timed_out = true;
+      issued_done = i;
+      break;
+    }
+    const uint32_t ktile = my_stages + s * G::kStageBytes;
+    const uint32_t vtile = ktile + G::kTileBytes;
+    const int key0 = (blk_begin + warp + i * W) * kBlockSize;
+    const bool bad = (bad_mask >> (i & 31)) & 1u;
+
+    // S^T = K Q^T
+    float sc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(a, ktile + swz<D>(lane & 15, ks * 16 + (lane >> 4) * 8));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) Mma<T>::run(sc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+    }
+    const bool need_mask = bad || key0 + kBlockSize > mask_from;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = sc[nt][e] * p.scale_log2;
+        if (need_mask) {
+          const int key = key0 + g + ((e >> 1) << 3);
+          if (bad || key >= lim[nt][e & 1]) v = -INFINITY;
+        }
+        sc[nt][e] = v;
+      }
+    // Online softmax update, per column (max over the 16 keys of the block:
+    // 2 per thread, then across the 8 lanes that share the column).
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mx = fmaxf(sc[nt][e], sc[nt][e + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float m_new = fmaxf(m[nt][e], mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float corr = ex2(m[nt][e] - m_use);
+        const float p0 = ex2(sc[nt][e] - m_use);
+        const float p1 = ex2(sc[nt][e + 2] - m_use);
+        l[nt][e] = l[nt][e] * corr + p0 + p1;
+        m[nt][e] = m_new;
+        sc[nt][e] = p0;
+        sc[nt][e + 2] = p1;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][nt][e] *= corr;
+          o[mt][nt][e + 2] *= corr;
+        }
+      }
+    // P^T operand fragments: high part and rounding remainder.
+    uint32_t ph[NT][2], pl[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint32_t h01 = Mma<T>::pack(sc[nt][0], sc[nt][1]);
+      const uint32_t h23 = Mma<T>::pack(sc[nt][2], sc[nt][3]);
+      float r0, r1, r2, r3;
+      Mma<T>::unpack(h01, r0, r1);
+      Mma<T>::unpack(h23, r2, r3);
+      const uint32_t l01 = Mma<T>::pack(sc[nt][0] - r0, sc[nt][1] - r1);
+      const uint32_t l23 = Mma<T>::pack(sc[nt][2] - r2, sc[nt][3] - r3);
+      ph[nt][0] = movm_t(h01);
+      ph[nt][1] = movm_t(h23);
+      pl[nt][0] = movm_t(l01);
+      pl[nt][1] = movm_t(l23);
+    }
+    // O^T += V^T P^T.  Zero the V^T columns (keys) past the context.
+    const int nvalid = bad ? 0 : L - key0;
+    uint32_t km0 = 0xffffffffu, km8 = 0xffffffffu;
+    if (nvalid < kBlockSize) {
+      km0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
+      km8 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a[4];
+      ldsm_x4_t(a, vtile + swz<D>((lane & 7) + ((lane >> 4) << 3), mt * 16 + ((lane >> 3) & 1) * 8));
+      a[0] &= km0;
+      a[1] &= km0;
+      a[2] &= km8;
+      a[3] &= km8;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        Mma<T>::run(o[mt][nt], a, ph[nt][0], ph[nt][1]);
+        Mma<T>::run(o[mt][nt], a, pl[nt][0], pl[nt][1]);
+      }
+    }
+    __syncwarp();
+    if (i + NS < n_my) {
+      issue(i + NS);
+      ++issued;
+    }
+    if (i + 1 == n_my) issued_done = i + 1;
+  }
+  if (timed_out) {
+    if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT);
+    // Give the copies still in flight a bounded chance to land before the
+    // shared memory is reused.
+    for (int k = issued_done; k < issued; ++k) mbar_wait_bounded(my_bars + 8 * (k % NS), (k / NS) & 1);
+  }
+
+  // Row sums: reduce the per-thread partial sums over the 8 lanes of a column.
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = l[nt][e];
+      v += __shfl_xor_sync(kFull, v, 4);
+      v += __shfl_xor_sync(kFull, v, 8);
+      v += __shfl_xor_sync(kFull, v, 16);
+      l[nt][e] = v;
+    }
+
+  // Hand the per-warp states to the CTA epilogue (reusing the stage memory).
+  __syncthreads();
+  constexpr int DP = D + 4;
+  float *red_o = reinterpret_cast<float *>(smem);
+  float *red_m = red_o + W * NC * DP;
+  float *red_l = red_m + W * NC;
+  float *wscale = red_l + W * NC;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int col = nt * 8 + 2 * c + (e & 1);
+        const int d = mt * 16 + g + ((e >> 1) << 3);
+        red_o[(warp * NC + col) * DP + d] = o[mt][nt][e];
+      }
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        red_m[warp * NC + nt * 8 + 2 * c + e] = m[nt][e];
+        red_l[warp * NC + nt * 8 + 2 * c + e] = l[nt][e];
+      }
+  }
+  __syncthreads();
+  cta_epilogue<T, D, NC, W>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split);
+}
+
+constexpr int kMmaWarps = 4;
+
+template <int D> constexpr int mma_stages() { return D >= 256 ? 2 : 3; }
+
+template <typename T, int D, int NT>
+constexpr size_t mma_smem_bytes() {
+  constexpr int NS = mma_stages<D>();
+  constexpr size_t stages = size_t(kMmaWarps) * NS * MmaGeom<D>::kStageBytes;
+  constexpr size_t red = (size_t(kMmaWarps) * NT * 8 * (D + 4) + size_t(kMmaWarps + 2) * NT * 8 * 2 +
+                          size_t(kMmaWarps) * NT * 8) * 4;
+  static_assert(red <= stages, "epilogue scratch must fit in the stage memory");
+  return stages + size_t(kMmaWarps) * NS * 8 + 1024;
+}
+
+template <typename T, int D, int NT>
+KernelInfo mma_info_t() {
+  KernelInfo k;
+  k.func = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, NT, kMmaWarps, mma_stages<D>()>);
+  k.threads = kMmaWarps * 32;
+  k.smem = mma_smem_bytes<T, D, NT>();
+  k.warps = kMmaWarps;
+  return k;
+}
+
+template <typename T, int D, int NT>
+cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
+                     cudaStream_t stream) {
+  const KernelInfo k = mma_info_t<T, D, NT>();
+  attn_mma_kernel<T, D, NT, kMmaWarps, mma_stages<D>()>
+      <<<grid, k.threads, k.smem, stream>>>(km, vm, p);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+bool mma_pick(int nt, KernelInfo *info, cudaError_t (**launch)(const CUtensorMap &,
+                                                                 const CUtensorMap &,
+                                                                 const AttnParams &, dim3,
+                                                                 cudaStream_t)) {
+  switch (nt) {
+#define PKV_NT_CASE(N)                     \
+  case N:                                  \
+    if (N * D > 384) return false;         \
+    *info = mma_info_t<T, D, (N * D > 384 ? 1 : N)>(); \
+    *launch = &launch_t<T, D, (N * D > 384 ? 1 : N)>;  \
+    return true;
+    PKV_NT_CASE(1)
+    PKV_NT_CASE(2)
+    PKV_NT_CASE(3)
+    PKV_NT_CASE(4)
+#undef PKV_NT_CASE
+    default:
+      return false;
+  }
+}
+
+template <typename T>
+bool mma_pick_d(int D, int nt, KernelInfo *info,
+                cudaError_t (**launch)(const CUtensorMap &, const CUtensorMap &,
+                                       const AttnParams &, dim3, cudaStream_t)) {
+  switch (D) {
+    case 64: return mma_pick<T, 64>(nt, info, launch);
+    case 128: return mma_pick<T, 128>(nt, info, launch);
+    case 256: return mma_pick<T, 256>(nt, info, launch);
+    default: return false;
+  }
+}
+
+}  // namespace
+
+int mma_max_tiles(int head_dim) { return head_dim <= 64 ? 4 : (head_dim <= 128 ? 3 : 1); }
+
+bool mma_kernel_info(pkv_dtype dtype, int head_dim, int n_tiles, KernelInfo *info) {
+  cudaError_t (*launch)(const CUtensorMap &, const CUtensorMap &, const AttnParams &, dim3,
+                        cudaStream_t) = nullptr;
+  if (dtype == PKV_BF16) return mma_pick_d<__nv_bfloat16>(head_dim, n_tiles, info, &launch);
+  if (dtype == PKV_F16) return mma_pick_d<__half>(head_dim, n_tiles, info, &launch);
+  return false;
+}
+
+cudaError_t mma_launch(pkv_dtype dtype, int head_dim, int n_tiles, const CUtensorMap &kmap,
+                       const CUtensorMap &vmap, const AttnParams &p, dim3 grid,
+                       cudaStream_t stream) {
+  KernelInfo info;
+  cudaError_t (*launch)(const CUtensorMap &, const CUtensorMap &, const AttnParams &, dim3,
+                        cudaStream_t) = nullptr;
+  bool ok = false;
+  if (dtype == PKV_BF16) ok = mma_pick_d<__nv_bfloat16>(head_dim, n_tiles, &info, &launch);
+  if (dtype == PKV_F16) ok = mma_pick_d<__half>(head_dim, n_tiles, &info, &launch);
+  if (!ok) return cudaErrorInvalidValue;
+  return launch(kmap, vmap, p, grid, stream);
+}
+
+}  // namespace pkv

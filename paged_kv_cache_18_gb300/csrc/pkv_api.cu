@@ -1,0 +1,460 @@
+// pkv_api.cu -- the C ABI (include/pkv.h): argument validation, the launch
+// planner, tensor-map encoding and dispatch to the kernel families.
+//
+// Nothing here allocates, frees or synchronises (except pkv_read_error_word,
+// which documents that it does); every launch goes to the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMinSplitBlocks = 16;     // 4 blocks per warp: fills the pipeline
+constexpr int kMaxUnitBlocks = 64;      // longest split when splitting at all
+constexpr int kTargetWaves = 4;         // CTAs ~ this many times the resident slots
+constexpr size_t kUsableSmemPerSm = 228 * 1024;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elt_bytes(pkv_dtype dt) { return dt == PKV_F32 ? 4 : 2; }
+
+bool valid_dtype(int dt) { return dt == PKV_F32 || dt == PKV_BF16 || dt == PKV_F16; }
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+struct DeviceInfo {
+  std::atomic<int> sm_count{0};
+};
+DeviceInfo g_devices[kMaxDevices];
+
+cudaError_t current_sm_count(int *device, int *sms) {
+  cudaError_t e = cudaGetDevice(device);
+  if (e != cudaSuccess) return e;
+  if (*device < 0 || *device >= kMaxDevices) return cudaErrorInvalidDevice;
+  int n = g_devices[*device].sm_count.load(std::memory_order_relaxed);
+  if (n == 0) {
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *device);
+    if (e != cudaSuccess) return e;
+    g_devices[*device].sm_count.store(n, std::memory_order_relaxed);
+  }
+  *sms = n;
+  return cudaSuccess;
+}
+
+// Once per (kernel, device): allow the kernel's dynamic shared memory and
+// ask the occupancy calculator how many CTAs fit on one SM.
+struct FuncSlot {
+  const void *func;
+  std::atomic<int> ctas[kMaxDevices];
+};
+std::mutex g_func_mu;
+FuncSlot g_funcs[256];
+int g_nfuncs = 0;
+
+cudaError_t prepare_kernel(const KernelInfo &k, int device, int *ctas_per_sm) {
+  FuncSlot *slot = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_func_mu);
+    for (int i = 0; i < g_nfuncs; ++i)
+      if (g_funcs[i].func == k.func) slot = &g_funcs[i];
+    if (!slot) {
+      if (g_nfuncs >= 256) return cudaErrorMemoryAllocation;
+      slot = &g_funcs[g_nfuncs++];
+      slot->func = k.func;
+      for (auto &c : slot->ctas) c.store(0);
+    }
+  }
+  int n = slot->ctas[device].load(std::memory_order_acquire);
+  if (n == 0) {
+    cudaError_t e = cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(k.smem));
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k.func, k.threads, k.smem);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    slot->ctas[device].store(n, std::memory_order_release);
+  }
+  *ctas_per_sm = n;
+  return cudaSuccess;
+}
+
+struct Shape {
+  int batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len;
+  pkv_dtype dtype;
+};
+
+pkv_status check_shape(const Shape &s) {
+  if (s.batch < 0 || s.num_queries < 1 || s.num_heads < 1 || s.num_kv_heads < 1 ||
+      s.head_dim < 1 || s.block_size < 1 || s.max_context_len < 0 || !valid_dtype(s.dtype))
+    return PKV_ERR_INVALID_ARG;
+  if (s.num_heads % s.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (s.head_dim != 64 && s.head_dim != 128 && s.head_dim != 256) return PKV_ERR_UNSUPPORTED;
+  if (s.block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (s.batch > 65535) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+// Kernel family and per-CTA row tile.  Returns false if unsupported.
+bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelInfo *info) {
+  int kernel = opt ? opt->kernel : PKV_KERNEL_AUTO;
+  if (kernel == PKV_KERNEL_AUTO) kernel = (s.dtype == PKV_F32) ? PKV_KERNEL_SIMT : PKV_KERNEL_MMA;
+  if (kernel == PKV_KERNEL_MMA && s.dtype == PKV_F32) return false;
+  if (kernel != PKV_KERNEL_MMA && kernel != PKV_KERNEL_SIMT) return false;
+  const int rows = (s.num_heads / s.num_kv_heads) * s.num_queries;
+  const int cap = kernel == PKV_KERNEL_MMA ? 8 * mma_max_tiles(s.head_dim)
+                                           : simt_max_rows(s.head_dim);
+  const int chunks = ceil_div(rows, cap);
+  const int per_cta = ceil_div(rows, chunks);
+  bool ok;
+  if (kernel == PKV_KERNEL_MMA) {
+    ok = mma_kernel_info(s.dtype, s.head_dim, ceil_div(per_cta, 8), info);
+  } else {
+    int r = 1;
+    while (r < per_cta) r <<= 1;
+    ok = simt_kernel_info(s.dtype, s.head_dim, r, info);
+  }
+  if (!ok) return false;
+  pl->kernel = kernel;
+  pl->rows_per_cta = per_cta;
+  pl->row_chunks = chunks;
+  pl->threads_per_cta = info->threads;
+  pl->smem_bytes = info->smem;
+  return true;
+}
+
+// Split-K partition.  A sequence of n blocks is cut into chunks of
+// split_blocks blocks; each chunk is one CTA.  Splitting pays when the
+// unsplit grid leaves the GPU short of work (few sequences x KV heads, long
+// contexts) or when long sequences would dominate the tail of a ragged batch.
+void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_per_sm,
+                 pkv_plan *pl) {
+  const int max_blocks = ceil_div(s.max_context_len, s.block_size);
+  const int64_t units =
+      static_cast<int64_t>(s.batch) * s.num_kv_heads * static_cast<int64_t>(pl->row_chunks);
+  int split_blocks;
+  if (opt && opt->split_blocks > 0) {
+    split_blocks = opt->split_blocks;
+  } else {
+    const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
+    const int64_t want = kTargetWaves * slots;
+    if (units >= want || max_blocks <= kMinSplitBlocks) {
+      split_blocks = max_blocks;
+    } else {
+      const int64_t splits = (want + units - 1) / units;
+      split_blocks = ceil_div(max_blocks, splits);
+      if (split_blocks < kMinSplitBlocks) split_blocks = kMinSplitBlocks;
+      if (split_blocks > kMaxUnitBlocks && split_blocks < max_blocks) split_blocks = kMaxUnitBlocks;
+    }
+  }
+  if (split_blocks < 1) split_blocks = 1;
+  int num_splits = max_blocks > 0 ? ceil_div(max_blocks, split_blocks) : 1;
+  if (num_splits <= 1) {
+    num_splits = 1;
+    split_blocks = max_blocks > 0 ? max_blocks : 1;
+  }
+  pl->split_blocks = split_blocks;
+  pl->num_splits = num_splits;
+  pl->grid_x = num_splits;
+  pl->grid_y = s.num_kv_heads * pl->row_chunks;
+  pl->grid_z = s.batch;
+  pl->ctas_per_sm = ctas_per_sm;
+  pl->workspace_bytes = 0;
+  if (num_splits > 1) {
+    const size_t rows = static_cast<size_t>(s.batch) * s.num_queries * s.num_heads;
+    const size_t o_bytes = rows * num_splits * s.head_dim * sizeof(float);
+    const size_t lse_bytes = rows * num_splits * sizeof(float);
+    pl->workspace_bytes = ((o_bytes + 255) / 256) * 256 + ((lse_bytes + 255) / 256) * 256;
+  }
+}
+
+pkv_status make_plan(const Shape &s, const pkv_options *opt, int num_sms, int ctas_per_sm,
+                     pkv_plan *pl, KernelInfo *info) {
+  pkv_status st = check_shape(s);
+  if (st != PKV_OK) return st;
+  if (opt && opt->split_blocks < 0) return PKV_ERR_INVALID_ARG;
+  if (!choose_kernel(s, opt, pl, info)) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(s.num_kv_heads) * pl->row_chunks > 65535) return PKV_ERR_UNSUPPORTED;
+  if (ctas_per_sm <= 0) {
+    const size_t per = info->smem + 1024;
+    ctas_per_sm = static_cast<int>(kUsableSmemPerSm / per);
+    if (ctas_per_sm > 2048 / info->threads) ctas_per_sm = 2048 / info->threads;
+    if (ctas_per_sm < 1) ctas_per_sm = 1;
+  }
+  plan_splits(s, opt, num_sms, ctas_per_sm, pl);
+  return PKV_OK;
+}
+
+pkv_status device_plan(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelInfo *info,
+                       int *device, int *sms) {
+  pkv_status st = check_shape(s);
+  if (st != PKV_OK) return st;
+  if (current_sm_count(device, sms) != cudaSuccess) return PKV_ERR_CUDA;
+  pkv_plan tmp{};
+  st = make_plan(s, opt, *sms, 1, &tmp, info);  // picks the kernel
+  if (st != PKV_OK) return st;
+  int ctas = 0;
+  if (prepare_kernel(*info, *device, &ctas) != cudaSuccess) return PKV_ERR_CUDA;
+  return make_plan(s, opt, *sms, ctas, pl, info);
+}
+
+// ---- tensor maps for the tensor-core kernel ------------------------------
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// The cache [NB, Hkv, 16, D] as a 4-D tensor (D, 16, Hkv, NB); one box is a
+// 64-element (128-byte) column panel of one (block, KV head) tile, 128-byte
+// swizzled in shared memory.
+bool encode_cache_map(CUtensorMap *map, const void *base, pkv_dtype dt, int D, int Hkv,
+                      int64_t NB) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const int eb = elt_bytes(dt);
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(kBlockSize),
+                              static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(NB)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * eb,
+                                 static_cast<cuuint64_t>(D) * eb * kBlockSize,
+                                 static_cast<cuuint64_t>(D) * eb * kBlockSize * Hkv};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBlockSize), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType type =
+      dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(map, type, 4, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+pkv_status run_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_table, int max_blocks_per_seq,
+                         const int32_t *context_lens, const Shape &s, int64_t num_blocks,
+                         float scale, void *workspace, size_t workspace_bytes,
+                         const pkv_options *opt, int32_t *error_word, cudaStream_t stream) {
+  pkv_status st = check_shape(s);
+  if (st != PKV_OK) return st;
+  if (s.batch == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s.max_context_len) >
+      static_cast<int64_t>(max_blocks_per_seq) * s.block_size)
+    return PKV_ERR_INVALID_ARG;
+  if (num_blocks > (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4) ||
+      (error_word && !aligned(error_word, 4)))
+    return PKV_ERR_ALIGNMENT;
+
+  pkv_plan pl{};
+  KernelInfo info;
+  int device = 0, sms = 0;
+  st = device_plan(s, opt, &pl, &info, &device, &sms);
+  if (st != PKV_OK) return st;
+  if (pl.workspace_bytes > 0) {
+    if (!workspace || !aligned(workspace, 16) || workspace_bytes < pl.workspace_bytes)
+      return PKV_ERR_WORKSPACE;
+  }
+
+  AttnParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.err = error_word;
+  p.num_blocks = num_blocks;
+  p.batch = s.batch;
+  p.num_queries = s.num_queries;
+  p.num_heads = s.num_heads;
+  p.num_kv_heads = s.num_kv_heads;
+  p.group = s.num_heads / s.num_kv_heads;
+  p.rows = p.group * s.num_queries;
+  p.rows_per_cta = pl.rows_per_cta;
+  p.row_chunks = pl.row_chunks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_context_len = s.max_context_len;
+  p.split_blocks = pl.split_blocks;
+  p.num_splits = pl.num_splits;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  if (pl.num_splits > 1) {
+    const size_t rows = static_cast<size_t>(s.batch) * s.num_queries * s.num_heads;
+    const size_t o_bytes = rows * pl.num_splits * s.head_dim * sizeof(float);
+    p.part_o = static_cast<float *>(workspace);
+    p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                           ((o_bytes + 255) / 256) * 256);
+  }
+
+  const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
+  cudaError_t e;
+  if (pl.kernel == PKV_KERNEL_MMA) {
+    CUtensorMap kmap, vmap;
+    if (!encode_cache_map(&kmap, k_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks) ||
+        !encode_cache_map(&vmap, v_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks))
+      return PKV_ERR_CUDA;
+    e = mma_launch(s.dtype, s.head_dim, ceil_div(pl.rows_per_cta, 8), kmap, vmap, p, grid, stream);
+  } else {
+    int r = 1;
+    while (r < pl.rows_per_cta) r <<= 1;
+    e = simt_launch(s.dtype, s.head_dim, r, p, grid, stream);
+  }
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  if (pl.num_splits > 1) {
+    e = merge_launch(s.dtype, s.head_dim, p, sms, stream);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char *pkv_status_string(pkv_status status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PKV_ERR_CUDA: return "CUDA runtime or launch error";
+    case PKV_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+const char *pkv_version(void) { return "pkv 0.1.0 sm_103a"; }
+
+pkv_status pkv_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, pkv_dtype dtype,
+                         int32_t *error_word, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || num_blocks < 1 ||
+      !valid_dtype(dtype))
+    return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  const int64_t row_bytes = static_cast<int64_t>(head_dim) * elt_bytes(dtype);
+  if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(slot_mapping, 8) || (error_word && !aligned(error_word, 4)))
+    return PKV_ERR_ALIGNMENT;
+  int device = 0, sms = 0;
+  if (current_sm_count(&device, &sms) != cudaSuccess) return PKV_ERR_CUDA;
+  const cudaError_t e = append_launch(k_new, v_new, k_cache, v_cache, slot_mapping, num_tokens,
+                                      num_kv_heads, static_cast<int>(row_bytes / 16), block_size,
+                                      num_blocks, error_word, sms,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_attention_plan_for(int batch, int num_queries, int num_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int max_context_len,
+                                  pkv_dtype dtype, const pkv_options *options, int num_sms,
+                                  int ctas_per_sm, pkv_plan *plan) {
+  if (!plan || num_sms < 1 || ctas_per_sm < 0) return PKV_ERR_INVALID_ARG;
+  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype};
+  pkv_plan pl{};
+  KernelInfo info;
+  const pkv_status st = make_plan(s, options, num_sms, ctas_per_sm, &pl, &info);
+  if (st == PKV_OK) *plan = pl;
+  return st;
+}
+
+pkv_status pkv_attention_plan(int batch, int num_queries, int num_heads, int num_kv_heads,
+                              int head_dim, int block_size, int max_context_len, pkv_dtype dtype,
+                              const pkv_options *options, pkv_plan *plan) {
+  if (!plan) return PKV_ERR_INVALID_ARG;
+  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype};
+  pkv_plan pl{};
+  KernelInfo info;
+  int device = 0, sms = 0;
+  const pkv_status st = device_plan(s, options, &pl, &info, &device, &sms);
+  if (st == PKV_OK) *plan = pl;
+  return st;
+}
+
+pkv_status pkv_attention_workspace_size(int batch, int num_queries, int num_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int max_context_len, pkv_dtype dtype,
+                                        const pkv_options *options, size_t *bytes) {
+  if (!bytes) return PKV_ERR_INVALID_ARG;
+  pkv_plan pl{};
+  const pkv_status st = pkv_attention_plan(batch, num_queries, num_heads, num_kv_heads, head_dim,
+                                           block_size, max_context_len, dtype, options, &pl);
+  if (st == PKV_OK) *bytes = pl.workspace_bytes;
+  return st;
+}
+
+pkv_status pkv_paged_decode_attention(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_table,
+                                      int max_blocks_per_seq, const int32_t *context_lens,
+                                      int max_context_len, int batch, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int64_t num_blocks, float scale, pkv_dtype dtype,
+                                      void *workspace, size_t workspace_bytes,
+                                      const pkv_options *options, int32_t *error_word,
+                                      pkv_stream_t stream) {
+  const Shape s{batch, 1, num_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype};
+  return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
+                       num_blocks, scale, workspace, workspace_bytes, options, error_word,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_spec_verify_attention(void *out, const void *q, const void *k_cache,
+                                     const void *v_cache, const int32_t *block_table,
+                                     int max_blocks_per_seq, const int32_t *context_lens,
+                                     int max_context_len, int batch, int num_queries,
+                                     int num_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int64_t num_blocks, float scale,
+                                     pkv_dtype dtype, void *workspace, size_t workspace_bytes,
+                                     const pkv_options *options, int32_t *error_word,
+                                     pkv_stream_t stream) {
+  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype};
+  return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
+                       num_blocks, scale, workspace, workspace_bytes, options, error_word,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_read_error_word(const int32_t *error_word, int32_t *host_code,
+                               pkv_stream_t stream) {
+  if (!error_word || !host_code) return PKV_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_code, error_word, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // extern "C"

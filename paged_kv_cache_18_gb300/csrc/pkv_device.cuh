@@ -1,0 +1,301 @@
+// pkv_device.cuh -- device-side building blocks shared by the attention
+// kernels: kernel parameters, inline-PTX wrappers (mbarrier, bulk and tensor
+// copies, ldmatrix / movmatrix / mma), and the epilogue that merges the
+// per-warp online-softmax states of one CTA and writes the output or the
+// split-K partials.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;   // tokens per KV block (rows of one tile)
+constexpr unsigned kFull = 0xffffffffu;
+// A shared-memory copy that has not landed after this long is reported as
+// PKV_DEVERR_TIMEOUT instead of being waited for forever.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Parameters of one attention launch (passed by value).
+struct AttnParams {
+  void *out;                    // [B, Q, Hq, D] elt
+  const void *q;                // [B, Q, Hq, D] elt
+  const void *k_cache;          // [NB, Hkv, 16, D] elt
+  const void *v_cache;
+  const int32_t *block_table;   // [B, max_blocks_per_seq]
+  const int32_t *context_lens;  // [B]
+  float *part_o;                // [B*Q*Hq, num_splits, D]   (split-K only)
+  float *part_lse;              // [B*Q*Hq, num_splits]      (log2 units)
+  int32_t *err;                 // optional device error word
+  int64_t num_blocks;
+  int batch, num_queries, num_heads, num_kv_heads, group;
+  int rows;                     // group * num_queries query rows per KV head
+  int rows_per_cta, row_chunks;
+  int max_blocks_per_seq, max_context_len;
+  int split_blocks, num_splits;
+  float scale_log2;             // softmax scale * log2(e)
+};
+
+template <typename T> struct Elt;
+template <> struct Elt<float> { static constexpr int bytes = 4; };
+template <> struct Elt<__nv_bfloat16> { static constexpr int bytes = 2; };
+template <> struct Elt<__half> { static constexpr int bytes = 2; };
+
+__device__ __forceinline__ void record_error(int32_t *err, int code) {
+  if (err) atomicCAS(reinterpret_cast<int *>(err), 0, code);
+}
+
+// ---- conversions --------------------------------------------------------
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T> __device__ __forceinline__ void unpack2(uint32_t w, float &a, float &b);
+template <> __device__ __forceinline__ void unpack2<__nv_bfloat16>(uint32_t w, float &a, float &b) {
+  a = lo_bf16(w);
+  b = hi_bf16(w);
+}
+template <> __device__ __forceinline__ void unpack2<__half>(uint32_t w, float &a, float &b) {
+  __half2 h = *reinterpret_cast<__half2 *>(&w);
+  float2 f = __half22float2(h);
+  a = f.x;
+  b = f.y;
+}
+
+template <typename T> __device__ __forceinline__ T from_float(float x);
+template <> __device__ __forceinline__ float from_float<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
+
+// 2^x (PTX ex2.approx; ex2(-inf) = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- shared-memory addressing and mbarriers -----------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of the barrier, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// ---- bulk copies (TMA engine) -------------------------------------------
+// Contiguous global -> shared copy; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Tiled 4-D tensor copy (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+// ---- warp-level matrix ops ----------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+template <typename T> struct Mma;
+template <> struct Mma<__nv_bfloat16> {
+  static __device__ __forceinline__ void run(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+  static __device__ __forceinline__ void unpack(uint32_t w, float &lo, float &hi) {
+    unpack2<__nv_bfloat16>(w, lo, hi);
+  }
+};
+template <> struct Mma<__half> {
+  static __device__ __forceinline__ void run(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+  static __device__ __forceinline__ void unpack(uint32_t w, float &lo, float &hi) {
+    unpack2<__half>(w, lo, hi);
+  }
+};
+
+// ---- per-CTA bookkeeping ------------------------------------------------
+// Where query row `col` of this CTA lives: flat output row index
+// ((b * Q + j) * Hq + h), or -1 when the column is padding.
+__device__ __forceinline__ int64_t cta_row_index(const AttnParams &p, int b, int kvh, int chunk,
+                                                 int col) {
+  if (col >= p.rows_per_cta) return -1;
+  const int r = chunk * p.rows_per_cta + col;
+  if (r >= p.rows) return -1;
+  const int j = r / p.group;
+  const int h = kvh * p.group + (r - j * p.group);
+  return (static_cast<int64_t>(b) * p.num_queries + j) * p.num_heads + h;
+}
+
+// Number of key rows query row `col` may see: L - Q + 1 + j (<= 0: none).
+__device__ __forceinline__ int cta_row_limit(const AttnParams &p, int L, int chunk, int col) {
+  const int r = chunk * p.rows_per_cta + col;
+  const int j = (col < p.rows_per_cta && r < p.rows) ? r / p.group : 0;
+  return L - p.num_queries + 1 + j;
+}
+
+// Effective context length of sequence b and its block count, with the
+// precondition checks that never fault (recorded in the error word).
+struct SeqExtent {
+  int L, nblk;
+};
+__device__ __forceinline__ SeqExtent seq_extent(const AttnParams &p, int b, bool report) {
+  int L = p.context_lens[b];
+  if (L < 0) L = 0;
+  if (L > p.max_context_len) {
+    if (report) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
+    L = p.max_context_len;
+  }
+  int nblk = (L + kBlockSize - 1) / kBlockSize;
+  if (nblk > p.max_blocks_per_seq) {
+    if (report) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
+    nblk = p.max_blocks_per_seq;
+    L = nblk * kBlockSize;
+  }
+  return {L, nblk};
+}
+
+// CTA epilogue.  Every warp w has left, for each of the NC query columns of
+// this CTA, its running max m (log2 units), its sum l and its unnormalised
+// output o[0..D) in shared memory:
+//   red_m[w * NC + col], red_l[w * NC + col], red_o[(w * NC + col) * DP + d].
+// The states are merged exactly as the online softmax merges two chunks
+// (rescale each by 2^(m_w - M)), then the CTA writes either the normalised
+// output (no split) or the split's normalised output and its log-sum-exp.
+template <typename T, int D, int NC, int W>
+__device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, float *red_l,
+                                             float *red_o, float *wscale, int b, int kvh,
+                                             int chunk, int split) {
+  constexpr int DP = D + 4;
+  const int tid = threadIdx.x;
+  // 1) per column: global max, per-warp scale factors and 1 / sum.
+  if (tid < NC) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, red_m[w * NC + tid]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float s = ex2(red_m[w * NC + tid] - Mu);
+      wscale[w * NC + tid] = s;
+      lsum += red_l[w * NC + tid] * s;
+    }
+    wscale[W * NC + tid] = lsum > 0.f ? 1.f / lsum : 0.f;
+    wscale[(W + 1) * NC + tid] = lsum > 0.f ? M + __log2f(lsum) : -INFINITY;
+  }
+  __syncthreads();
+  // 2) 4 consecutive d per thread-step.
+  constexpr int QV = D / 4;
+  for (int idx = tid; idx < NC * QV; idx += W * 32) {
+    const int col = idx / QV;
+    const int d0 = (idx - col * QV) * 4;
+    const int64_t row = cta_row_index(p, b, kvh, chunk, col);
+    if (row < 0) continue;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float s = wscale[w * NC + col];
+      const float4 o = *reinterpret_cast<const float4 *>(&red_o[(w * NC + col) * DP + d0]);
+      acc[0] += s * o.x;
+      acc[1] += s * o.y;
+      acc[2] += s * o.z;
+      acc[3] += s * o.w;
+    }
+    const float inv = wscale[W * NC + col];
+    if (p.num_splits == 1) {
+      T *dst = reinterpret_cast<T *>(p.out) + row * D + d0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[e] = from_float<T>(acc[e] * inv);
+    } else {
+      float4 v = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<float4 *>(&p.part_o[(row * p.num_splits + split) * D + d0]) = v;
+      if (d0 == 0) p.part_lse[row * p.num_splits + split] = wscale[(W + 1) * NC + col];
+    }
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,46 @@
+// pkv_internal.h -- host-side declarations shared by the library's
+// translation units (kernel families, their launchers and shared-memory
+// needs).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+struct AttnParams;
+
+struct KernelInfo {
+  const void *func = nullptr;
+  int threads = 0;
+  int warps = 0;
+  size_t smem = 0;
+};
+
+// Tensor-core kernel: n_tiles = query columns / 8.
+int mma_max_tiles(int head_dim);
+bool mma_kernel_info(pkv_dtype dtype, int head_dim, int n_tiles, KernelInfo *info);
+cudaError_t mma_launch(pkv_dtype dtype, int head_dim, int n_tiles, const CUtensorMap &kmap,
+                       const CUtensorMap &vmap, const AttnParams &p, dim3 grid,
+                       cudaStream_t stream);
+
+// CUDA-core kernel: rows = query rows per CTA (1, 2, 4 or 8).
+int simt_max_rows(int head_dim);
+bool simt_kernel_info(pkv_dtype dtype, int head_dim, int rows, KernelInfo *info);
+cudaError_t simt_launch(pkv_dtype dtype, int head_dim, int rows, const AttnParams &p, dim3 grid,
+                        cudaStream_t stream);
+
+// Split-K log-sum-exp merge.
+cudaError_t merge_launch(pkv_dtype dtype, int head_dim, const AttnParams &p, int sm_count,
+                         cudaStream_t stream);
+
+// kv_append.
+cudaError_t append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                          const int64_t *slots, int64_t num_tokens, int num_kv_heads,
+                          int vec_per_row, int block_size, int64_t num_blocks, int32_t *err,
+                          int sm_count, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,137 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, validates arguments synchronously (nothing reaches CUDA on bad
+input), and its launch planner is self-consistent."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from paged_kv_cache_18_gb300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PKV_API[^;(]*?\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_list():
+    assert declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_only_the_c_abi_is_exported(L):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    ours = [l.split()[-1] for l in out.splitlines() if " T " in l and "pkv" in l]
+    assert sorted(ours) == declared_functions()
+
+
+def test_version_and_status_strings(L):
+    assert "sm_103a" in binding.version()
+    names = [L.pkv_status_string(i).decode() for i in range(7)]
+    assert names[0] == "ok" and len(set(names)) == 7
+
+
+# --- argument validation (returns before any CUDA call) -------------------
+def decode(L, **kw):
+    a = dict(out=16, q=16, k=16, v=16, table=16, max_blocks=8, lens=16, max_ctx=100, B=2,
+             Hq=8, Hkv=2, D=128, bs=16, NB=10, scale=0.1, dtype=1, ws=None, ws_bytes=0,
+             opt=None, err=None, stream=None)
+    a.update(kw)
+    return L.pkv_paged_decode_attention(a["out"], a["q"], a["k"], a["v"], a["table"],
+                                        a["max_blocks"], a["lens"], a["max_ctx"], a["B"],
+                                        a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"], a["scale"],
+                                        a["dtype"], a["ws"], a["ws_bytes"], a["opt"], a["err"],
+                                        a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(out=None), 1), (dict(table=None), 1), (dict(lens=None), 1),
+    (dict(Hq=7), 1), (dict(Hkv=0), 1), (dict(D=96), 2), (dict(bs=32), 2), (dict(dtype=9), 1),
+    (dict(max_ctx=-1), 1), (dict(max_ctx=8 * 16 + 1), 1), (dict(NB=0), 1),
+    (dict(scale=float("nan")), 1), (dict(q=8), 5), (dict(k=24), 5), (dict(B=70000), 2),
+])
+def test_attention_argument_errors(L, kw, status):
+    assert decode(L, **kw) == status
+
+
+def test_empty_batch_is_a_no_op(L):
+    assert decode(L, B=0, q=None, out=None) == 0
+
+
+def test_spec_verify_argument_errors(L):
+    f = L.pkv_spec_verify_attention
+    # num_queries = 0 is invalid
+    assert f(16, 16, 16, 16, 16, 8, 16, 100, 2, 0, 8, 2, 128, 16, 10, 0.1, 1, None, 0, None,
+             None, None) == 1
+
+
+def test_kv_append_argument_errors(L):
+    f = L.pkv_kv_append
+    assert f(16, 16, 16, 16, 16, 0, 2, 128, 16, 10, 1, None, None) == 0   # no tokens
+    assert f(None, 16, 16, 16, 16, 4, 2, 128, 16, 10, 1, None, None) == 1
+    assert f(16, 16, 16, 16, 16, 4, 2, 128, 16, 10, 7, None, None) == 1   # dtype
+    assert f(16, 16, 16, 16, 16, 4, 2, 4, 16, 10, 1, None, None) == 2     # 8-byte rows
+    assert f(16, 16, 16, 16, 12, 4, 2, 128, 16, 10, 1, None, None) == 5   # slot align
+    assert f(16, 16, 16, 24, 16, 4, 2, 128, 16, 10, 1, None, None) == 5
+
+
+# --- planner (no GPU: explicit SM count) -----------------------------------
+def test_plan_kernel_choice():
+    p = binding.plan_for(4, 1, 6, 6, 64, 256, torch.float32, num_sms=152)
+    assert p["kernel"] == binding.PKV_KERNEL_SIMT
+    p = binding.plan_for(32, 1, 40, 40, 128, 2048, torch.bfloat16, num_sms=152)
+    assert p["kernel"] == binding.PKV_KERNEL_MMA and p["rows_per_cta"] == 1
+    with pytest.raises(binding.PkvError):
+        binding.plan_for(1, 1, 8, 8, 64, 16, torch.float32, num_sms=152,
+                         kernel=binding.PKV_KERNEL_MMA)
+
+
+@pytest.mark.parametrize("B,Q,Hq,Hkv,D,ctx,dt", [
+    (4, 1, 6, 6, 64, 256, torch.float32), (32, 1, 40, 40, 128, 2048, torch.bfloat16),
+    (128, 1, 32, 8, 128, 4096, torch.bfloat16), (2, 1, 32, 8, 128, 65536, torch.bfloat16),
+    (16, 5, 32, 8, 128, 8192, torch.bfloat16), (3, 7, 64, 2, 64, 1000, torch.float16),
+    (1, 1, 128, 1, 256, 300, torch.bfloat16), (5, 3, 16, 2, 256, 70, torch.float32),
+])
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
+    p = binding.plan_for(B, Q, Hq, Hkv, D, ctx, dt, num_sms=152, kernel=kernel)
+    rows = Hq // Hkv * Q
+    assert p["rows_per_cta"] * p["row_chunks"] >= rows
+    assert (p["rows_per_cta"] - 1) * p["row_chunks"] < rows
+    max_blocks = -(-ctx // 16)
+    assert p["num_splits"] * p["split_blocks"] >= max_blocks
+    assert (p["num_splits"] - 1) * p["split_blocks"] < max(max_blocks, 1)
+    assert (p["grid_x"], p["grid_y"], p["grid_z"]) == (p["num_splits"], Hkv * p["row_chunks"], B)
+    if p["num_splits"] == 1:
+        assert p["workspace_bytes"] == 0
+    else:
+        o = B * Q * Hq * p["num_splits"] * D * 4
+        lse = B * Q * Hq * p["num_splits"] * 4
+        assert p["workspace_bytes"] == -(-o // 256) * 256 + -(-lse // 256) * 256
+    assert p["smem_bytes"] <= 227 * 1024
+
+
+def test_plan_splits_long_contexts_and_honours_override():
+    p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152)
+    assert p["num_splits"] > 16     # 16 (sequence, KV head) pairs cannot fill 152 SMs
+    p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152, split_blocks=7)
+    assert p["split_blocks"] == 7 and p["num_splits"] == -(-4096 // 7)
+    p = binding.plan_for(2, 1, 32, 8, 128, 100, torch.bfloat16, num_sms=152, split_blocks=1000)
+    assert p["num_splits"] == 1

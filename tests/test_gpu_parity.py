@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Appends are compared bit for bit over the whole cache; attention outputs
+within the tolerances of ``gpu_util.TOL``.  Unused cache rows and blocks are
+NaN-filled by the workload generator, so any read outside a context shows up
+as a non-finite output.
+"""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_18_gb300 import workloads as W
+from tests.gpu_util import (DeviceBatch, assert_close, cache_bits, errors, host_f64,
+                            oracle_after_append)
+
+pytestmark = pytest.mark.gpu
+
+EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 100]
+
+
+def run_case(wl, kernel=0, split_blocks=0):
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    out = d.attend(kernel=kernel, split_blocks=split_blocks)
+    torch.cuda.synchronize()
+    ref = oracle_after_append(b)
+    # the append is bit-exact over the whole cache
+    np.testing.assert_array_equal(cache_bits(d.k_cache), b.k_cache.view(cache_bits(d.k_cache).dtype))
+    np.testing.assert_array_equal(cache_bits(d.v_cache), b.v_cache.view(cache_bits(d.v_cache).dtype))
+    got = host_f64(out, wl.dtype)
+    assert int(d.err.item()) == 0
+    return assert_close(got, ref, wl.dtype, wl.name)
+
+
+KERNELS = {"simt": 1, "mma": 2}
+
+
+@pytest.mark.parametrize("dtype,kernel", [("f32", "simt"), ("bf16", "simt"), ("bf16", "mma"),
+                                          ("f16", "simt"), ("f16", "mma")])
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (8, 1), (16, 2)])
+def test_decode_edge_lengths(dtype, kernel, D, Hq, Hkv):
+    wl = W.Workload(f"decode {dtype} {kernel} D{D} {Hq}/{Hkv}", len(EDGE_LENS), Hq, Hkv, D,
+                    dtype, context_lens=EDGE_LENS, seed=100 + D + Hq + Hkv)
+    run_case(wl, kernel=KERNELS[kernel])
+
+
+@pytest.mark.parametrize("dtype,kernel", [("f32", "simt"), ("bf16", "simt"), ("bf16", "mma"),
+                                          ("f16", "mma")])
+@pytest.mark.parametrize("Q,Hq,Hkv", [(5, 32, 8), (3, 4, 4), (8, 16, 2), (2, 8, 1)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_spec_verify_edge_lengths(dtype, kernel, Q, Hq, Hkv, D):
+    lens = [Q, Q + 1, 15, 16, 17, 33, 64, 131]
+    wl = W.Workload(f"verify {dtype} {kernel} Q{Q} {Hq}/{Hkv} D{D}", len(lens), Hq, Hkv, D,
+                    dtype, context_lens=lens, num_queries=Q, seed=200 + Q + Hq + D)
+    run_case(wl, kernel=KERNELS[kernel])
+
+
+@pytest.mark.parametrize("kernel", ["simt", "mma"])
+@pytest.mark.parametrize("split_blocks", [1, 2, 3, 7, 64])
+def test_forced_splits(kernel, split_blocks):
+    wl = W.Workload(f"split {split_blocks}", 5, 16, 4, 128, "bf16",
+                    context_lens=[1, 40, 300, 777, 1024], seed=300 + split_blocks)
+    run_case(wl, kernel=KERNELS[kernel], split_blocks=split_blocks)
+
+
+@pytest.mark.parametrize("split_blocks", [1, 5])
+def test_forced_splits_verify(split_blocks):
+    wl = W.Workload("split verify", 4, 32, 8, 128, "bf16", context_lens=[5, 17, 21, 500],
+                    num_queries=5, seed=320 + split_blocks)
+    run_case(wl, kernel=2, split_blocks=split_blocks)
+
+
+def test_zero_and_short_contexts_give_zero_rows():
+    wl = W.Workload("zero", 3, 8, 2, 128, "bf16", context_lens=[0, 2, 40], num_queries=3, seed=7)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    for kernel in (1, 2):
+        got = host_f64(d.attend(kernel=kernel), "bf16")
+        assert (got[0] == 0).all() and (got[1, 0] == 0).all()
+        assert_close(got, oracle_after_append(b), "bf16", "zero")
+
+
+def test_split_invariance_and_determinism():
+    wl = W.Workload("inv", 4, 32, 8, 128, "bf16", context_lens=[100, 900, 2000, 33], seed=8)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    ref = oracle_after_append(b)
+    outs = {}
+    for sb in (0, 1, 4, 1000):
+        o1 = d.attend(split_blocks=sb).clone()
+        o2 = d.attend(split_blocks=sb)
+        assert torch.equal(o1, o2), "same inputs, same plan: bitwise identical"
+        outs[sb] = host_f64(o1, "bf16")
+        assert_close(outs[sb], ref, "bf16", f"split {sb}")
+    # different partitions agree to within the output rounding
+    for sb in (1, 4, 1000):
+        assert np.abs(outs[sb] - outs[0]).max() <= 2 ** -7
+
+
+def test_spec_rows_match_decode_on_prefixes():
+    wl = W.Workload("prefix", 3, 32, 8, 128, "bf16", context_lens=[20, 300, 1111],
+                    num_queries=5, seed=9)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    spec = host_f64(d.attend(), "bf16")
+    for j in range(5):
+        lens = (d.lens - 5 + 1 + j).contiguous()
+        import paged_kv_cache_18_gb300 as pkv
+        dec = pkv.paged_decode_attention(d.q[:, j].contiguous(), d.k_cache, d.v_cache, d.table,
+                                         lens, max_context_len=b.max_context_len)
+        got = host_f64(dec, "bf16")
+        assert np.abs(got - spec[:, j]).max() <= 2 ** -7
+
+
+def test_error_word_bad_block_and_long_context():
+    wl = W.Workload("bad", 2, 8, 2, 64, "bf16", context_lens=[40, 50], seed=10)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    for kernel in (1, 2):
+        d.err.zero_()
+        d.table[0, 1] = b.num_blocks + 5   # out of range: skipped and reported
+        out = d.attend(kernel=kernel)
+        torch.cuda.synchronize()
+        assert int(d.err.item()) == 2
+        assert torch.isfinite(out.float()).all()
+        d.table[0, 1] = int(b.block_table[0, 1])
+        d.err.zero_()
+        d.lens[1] = 60                      # beyond max_context_len = 50: clamped, reported
+        out = d.attend(kernel=kernel)
+        torch.cuda.synchronize()
+        assert int(d.err.item()) == 3
+        d.lens[1] = 50
+    d.err.zero_()
+    d.attend()
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+
+
+def test_kv_append_skips_padding_and_reports_bad_slots():
+    wl = W.Workload("slots", 4, 4, 4, 128, "bf16", context_lens=[3, 20, 16, 1], seed=11)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    before = cache_bits(d.k_cache).copy()
+    d.slots[1] = -1
+    d.slots[2] = b.num_blocks * 16 + 3
+    d.append()
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 1
+    after = cache_bits(d.k_cache)
+    for t in (1, 2):
+        s = int(b.slot_mapping[t])
+        np.testing.assert_array_equal(after[s // 16, :, s % 16], before[s // 16, :, s % 16])
+    for t in (0, 3):
+        s = int(b.slot_mapping[t])
+        np.testing.assert_array_equal(after[s // 16, :, s % 16], b.k_new[t])
+
+
+def test_cuda_graph_replay():
+    wl = W.Workload("graph", 8, 32, 8, 128, "bf16", len_range=(100, 3000), seed=12)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    import paged_kv_cache_18_gb300 as pkv
+    ws_bytes = pkv.workspace_size(8, 1, 32, 8, 128, b.max_context_len, torch.bfloat16)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty(8, 1, 32, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d.append()
+        d.attend(out=out[:, 0], workspace=ws)   # warm-up (plans, attributes)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d.append()
+        d.attend(out=out[:, 0], workspace=ws)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert_close(host_f64(out, "bf16"), oracle_after_append(b), "bf16", "graph")
+
+
+# ---- the five named workloads at full size, in the bench's launch config --
+def sample_rows(b, n=384, seed=0):
+    wl = b.wl
+    total = wl.batch * wl.num_queries * wl.num_heads
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(total, size=min(n, total), replace=False)
+    # always include every row of the longest sequence's first query
+    longest = int(np.argmax(b.context_lens))
+    extra = [(longest * wl.num_queries) * wl.num_heads + h for h in range(wl.num_heads)]
+    return np.unique(np.concatenate([rows, extra]))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_named_workload_full_size(name):
+    wl = W.WORKLOADS[name]
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    out = d.attend()
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    rows = None if name == "tiny" else sample_rows(b)
+    ref = oracle_after_append(b, rows=rows)
+    # bit-exact append over the whole cache
+    k_bits = cache_bits(d.k_cache)
+    assert np.array_equal(k_bits, b.k_cache.view(k_bits.dtype))
+    del k_bits
+    v_bits = cache_bits(d.v_cache)
+    assert np.array_equal(v_bits, b.v_cache.view(v_bits.dtype))
+    del v_bits
+    got = host_f64(out, wl.dtype)
+    max_abs, rel = assert_close(got, ref, wl.dtype, name)
+    # every output row is finite (no NaN-filled row was read)
+    assert np.isfinite(got).all()
+    print(f"{name}: max-abs {max_abs:.3e} rel-L2 {rel:.3e}")
