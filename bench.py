@@ -65,16 +65,18 @@ def measured_peaks():
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken on the current kernel sources (else None)."""
-    path = os.path.join(PROFILE_DIR, f"attn_{workload}_traffic.json")
-    if not os.path.exists(path):
-        return None
-    with open(path) as f:
-        rec = json.load(f)
-    if rec.get("kernel_source_hash") != kernel_source_hash():
-        return None
-    return rec.get("dram_bytes_per_launch")
+    """DRAM bytes per launch (read + write) from the committed ncu summary of
+    the attention kernel on this workload, if that summary was taken on the
+    current kernel sources (else None)."""
+    import glob
+    import re
+    for path in glob.glob(os.path.join(PROFILE_DIR, f"attn_*_{workload}.md")):
+        text = open(path).read()
+        m_b = re.search(r"dram bytes per launch \(read \+ write\): (\d+)", text)
+        m_h = re.search(r"kernel source hash: ([0-9a-f]+)", text)
+        if m_b and m_h and m_h.group(1) == kernel_source_hash():
+            return int(m_b.group(1))
+    return None
 
 
 class ClockSampler:
