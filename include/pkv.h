@@ -243,6 +243,41 @@ PKV_API pkv_status pkv_spec_verify_attention(
 PKV_API pkv_status pkv_read_error_word(const int32_t *error_word, int32_t *host_code,
                                pkv_stream_t stream);
 
+/*
+ * pkv_paged_decode_attention_noalloc -- pkv_paged_decode_attention for
+ * callers that cannot allocate device memory.  The pages have no counterpart
+ * of this call; it exists for callers such as a plugin inside a host
+ * framework that owns every device allocation, or a latency-critical loop
+ * that must not call cudaMalloc / cudaFree (they can synchronise the device
+ * and fail under memory pressure), and so cannot provide the split-K
+ * workspace.
+ *
+ * Same arguments and results as pkv_paged_decode_attention minus the
+ * workspace: the split-K partials go to a scratch array of
+ * PKV_NOALLOC_SCRATCH_BYTES that the library holds in device memory (a
+ * file-scope __device__ array, present on every GPU that loads the library
+ * until the process exits).  The call allocates nothing and calls no
+ * allocating routine.
+ *   - If the plan's partials need more than PKV_NOALLOC_SCRATCH_BYTES (see
+ *     pkv_attention_workspace_size), it returns PKV_ERR_WORKSPACE with
+ *     nothing enqueued; a larger split_blocks in `options` shrinks the need.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array.  Nothing in it needs to start at zero
+ *     (every partial is written before it is read within a call), but calls
+ *     whose work overlaps on the GPU (other streams, other threads) race on
+ *     it: serialise them.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+PKV_API pkv_status pkv_paged_decode_attention_noalloc(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_table, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int batch,
+    int num_heads, int num_kv_heads, int head_dim, int block_size,
+    int64_t num_blocks, float scale, pkv_dtype dtype,
+    const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ _DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_plan",
             "pkv_attention_plan_for", "pkv_attention_workspace_size",
             "pkv_paged_decode_attention", "pkv_spec_verify_attention",
-            "pkv_read_error_word")
+            "pkv_read_error_word", "pkv_paged_decode_attention_noalloc")
 
 
 class PkvError(RuntimeError):
@@ -88,6 +88,9 @@ def lib() -> ctypes.CDLL:
                                                     i32, i32, i32, i32, i64, f32, i32, vp, sz,
                                                     opt, vp, vp]
             L.pkv_read_error_word.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+            L.pkv_paged_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32,
+                                                             i32, i32, i32, i32, i32, i64, f32,
+                                                             i32, opt, vp, vp]
             for name in EXPORTED:
                 if name not in ("pkv_status_string", "pkv_version"):
                     getattr(L, name).restype = i32

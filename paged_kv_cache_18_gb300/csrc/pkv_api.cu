@@ -458,3 +458,56 @@ pkv_status pkv_read_error_word(const int32_t *error_word, int32_t *host_code,
 }
 
 }  // extern "C"
+
+// ---- no-allocation variant --------------------------------------------
+// Scratch for the split-K partials of pkv_paged_decode_attention_noalloc.
+// In host code this name only stands in for the array; its device address
+// is looked up per device below and passed to the kernels.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::atomic<void *> g_noalloc_ptr[pkv::kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device (looked up on
+// the first call per device).
+cudaError_t noalloc_scratch(void **ptr) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 0 || device >= pkv::kMaxDevices) return cudaErrorInvalidDevice;
+  void *p = g_noalloc_ptr[device].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    p = g_noalloc_ptr[device].load(std::memory_order_acquire);
+    if (!p) {
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) return e;
+      g_noalloc_ptr[device].store(p, std::memory_order_release);
+    }
+  }
+  *ptr = p;
+  return cudaSuccess;
+}
+}  // namespace
+
+extern "C" pkv_status pkv_paged_decode_attention_noalloc(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int batch, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, float scale, pkv_dtype dtype,
+    const pkv_options *options, int32_t *error_word, pkv_stream_t stream) {
+  if (batch == 0) return PKV_OK;
+  size_t need = 0;
+  pkv_status st = pkv_attention_workspace_size(batch, 1, num_heads, num_kv_heads, head_dim,
+                                               block_size, max_context_len, dtype, options, &need);
+  if (st != PKV_OK) return st;
+  if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return PKV_ERR_CUDA;
+  return pkv_paged_decode_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq,
+                                    context_lens, max_context_len, batch, num_heads,
+                                    num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                                    scratch, PKV_NOALLOC_SCRATCH_BYTES, options, error_word,
+                                    stream);
+}
