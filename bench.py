@@ -232,7 +232,7 @@ def run_reference(args):
     return 0
 
 
-def workload_config(wl: W.Workload, b: W.PagedBatch) -> dict:
+def workload_config(wl: W.Workload, b: W.PagedBatch, fused: bool = False) -> dict:
     return {"workload": wl.name, "batch": wl.batch, "num_heads": wl.num_heads,
             "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
             "block_size": wl.block_size, "num_queries": wl.num_queries,
@@ -242,9 +242,11 @@ def workload_config(wl: W.Workload, b: W.PagedBatch) -> dict:
                              f" (sum {int(b.context_lens.sum())})"),
             "kv_bytes_per_step": b.kv_bytes(),
             "l2": f"no flush: the step reads {b.kv_bytes() / 1e9:.2f} GB of K/V, > 129 MB L2",
-            "step": f"kv_append of {wl.batch * wl.num_queries} rows + "
-                    + ("paged_decode_attention" if wl.num_queries == 1
-                       else "spec_verify_attention")}
+            "step": (f"append_attention: {wl.batch * wl.num_queries} new rows written and "
+                     "attended in one launch" if fused else
+                     f"kv_append of {wl.batch * wl.num_queries} rows + "
+                     + ("paged_decode_attention" if wl.num_queries == 1
+                        else "spec_verify_attention"))}
 
 
 # ------------------------------------------------------------ GPU arm ------
@@ -291,15 +293,27 @@ def run_ours(args):
     out = torch.empty_like(q)
     Q = wl.num_queries
     plan = pkv.plan(wl.batch, Q, wl.num_heads, wl.num_kv_heads, wl.head_dim,
-                    b.max_context_len, dt, kernel=args.kernel, split_blocks=args.split_blocks)
+                    b.max_context_len, dt, kernel=args.kernel, split_blocks=args.split_blocks,
+                    stages=args.stages)
     ws = torch.empty(max(16, plan["workspace_bytes"]), dtype=torch.uint8, device=dev)
     max_ctx = b.max_context_len
     attn = pkv.paged_decode_attention if Q == 1 else pkv.spec_verify_attention
+    fused = not args.unfused
+    shape4 = (wl.batch, Q, wl.num_kv_heads, wl.head_dim)
+    opts = dict(scale=wl.softmax_scale, max_context_len=max_ctx, out=out, workspace=ws,
+                kernel=args.kernel, split_blocks=args.split_blocks, stages=args.stages)
+
+    def attend(qq, kn, vn, sl, tb, ln):
+        """One step's cache write and attention (fused: one launch)."""
+        if fused:
+            pkv.append_attention(qq, kn.view(shape4), vn.view(shape4), k_cache, v_cache, tb, ln,
+                                 **opts)
+        else:
+            pkv.kv_append(kn, vn, k_cache, v_cache, sl)
+            attn(qq, k_cache, v_cache, tb, ln, **opts)
 
     def step():
-        pkv.kv_append(k_new, v_new, k_cache, v_cache, slots)
-        attn(q, k_cache, v_cache, table, lens, scale=wl.softmax_scale, max_context_len=max_ctx,
-             out=out, workspace=ws, kernel=args.kernel, split_blocks=args.split_blocks)
+        attend(q, k_new, v_new, slots, table, lens)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -319,10 +333,14 @@ def run_ours(args):
     t_host0 = time.time()
     start.record(stream)
     for i in range(K):
-        pkv.kv_append(k_new, v_new, k_cache, v_cache, slots)
+        if not fused:
+            pkv.kv_append(k_new, v_new, k_cache, v_cache, slots)
         ev[i][0].record(stream)
-        attn(q, k_cache, v_cache, table, lens, scale=wl.softmax_scale, max_context_len=max_ctx,
-             out=out, workspace=ws, kernel=args.kernel, split_blocks=args.split_blocks)
+        if fused:
+            pkv.append_attention(q, k_new.view(shape4), v_new.view(shape4), k_cache, v_cache,
+                                 table, lens, **opts)
+        else:
+            attn(q, k_cache, v_cache, table, lens, **opts)
         ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
@@ -343,7 +361,8 @@ def run_ours(args):
                 (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots),
                  ("table", table), ("lens", lens))}
         out_host = torch.empty_like(out, device="cpu").pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        h2d = sum(t.numel() * t.element_size() for n, t in host.items()
+                  if fused is False or n != "slots")
         d2h = out_host.numel() * out_host.element_size()
         dq, dkn, dvn, dsl, dtb, dln = (torch.empty_like(x) for x in (q, k_new, v_new, slots,
                                                                      table, lens))
@@ -353,13 +372,11 @@ def run_ours(args):
             dq.copy_(host["q"], non_blocking=True)
             dkn.copy_(host["k_new"], non_blocking=True)
             dvn.copy_(host["v_new"], non_blocking=True)
-            dsl.copy_(host["slots"], non_blocking=True)
+            if not fused:
+                dsl.copy_(host["slots"], non_blocking=True)
             dtb.copy_(host["table"], non_blocking=True)
             dln.copy_(host["lens"], non_blocking=True)
-            pkv.kv_append(dkn, dvn, k_cache, v_cache, dsl)
-            attn(dq, k_cache, v_cache, dtb, dln, scale=wl.softmax_scale,
-                 max_context_len=max_ctx, out=out, workspace=ws, kernel=args.kernel,
-                 split_blocks=args.split_blocks)
+            attend(dq, dkn, dvn, dsl, dtb, dln)
             out_host.copy_(out, non_blocking=True)
             stream.synchronize()
 
@@ -387,11 +404,11 @@ def run_ours(args):
         splits_per_seq = [max(1, -(-n // plan["split_blocks"])) for n in nblk]
     algo = accounting.attention_bytes(b.context_lens.tolist(), Q, wl.num_heads, wl.num_kv_heads,
                                       wl.head_dim, wl.block_size, W.ELT_BYTES[wl.dtype],
-                                      splits_per_seq)
+                                      splits_per_seq, fused_append=fused)
     achieved = algo["total"] / (attn_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
     traffic = recorded_traffic(args.workload)
-    launches_per_step = 2 + (1 if plan["num_splits"] > 1 else 0)
+    launches_per_step = (1 if fused else 2) + (1 if plan["num_splits"] > 1 else 0)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -405,18 +422,19 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": workload_config(wl, b),
+        "config": workload_config(wl, b, fused),
         "pct_of_hbm_peak": 100.0 * value / peak,
         "tokens_per_s": total_tokens / (step_ms * 1e-3),
         "attention_ms": attn_ms,
         "plan": {k: plan[k] for k in ("kernel", "rows_per_cta", "row_chunks", "split_blocks",
                                       "num_splits", "grid_x", "grid_y", "grid_z",
-                                      "ctas_per_sm")},
+                                      "stages", "ctas_per_sm")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": algo["total"],
-                     "kernel": "attention (+ merge when split)"},
+                     "kernel": ("fused append + attention" if fused else "attention")
+                               + (" + split-K merge" if plan["num_splits"] > 1 else "")},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
@@ -436,8 +454,11 @@ def main(argv=None):
     ap.add_argument("--workload", choices=list(W.WORKLOADS), default="llama2_13b")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--split-blocks", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0, help="tensor-core kernel ring depth")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--unfused", action="store_true",
+                    help="kv_append and attention as two launches")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

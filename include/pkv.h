@@ -106,6 +106,8 @@ typedef enum pkv_kernel {
 typedef struct pkv_options {
   int kernel;       /* pkv_kernel */
   int split_blocks; /* 0: planner; > 0: KV blocks per split-K chunk */
+  int stages;       /* 0: planner; tensor-core kernel: per-warp ring depth
+                       (2 or 3 at head_dim <= 128, 1 or 2 at 256) */
 } pkv_options;
 
 /* What one attention call launches (see pkv_attention_plan). */
@@ -117,6 +119,7 @@ typedef struct pkv_plan {
   int num_splits;         /* splits of the longest sequence; 1 = no merge */
   int grid_x, grid_y, grid_z;
   int threads_per_cta;
+  int stages;             /* shared-memory stages per warp */
   int ctas_per_sm;        /* occupancy the planner assumed */
   size_t smem_bytes;      /* dynamic shared memory per CTA */
   size_t workspace_bytes; /* device workspace the call needs (0 = none) */
@@ -235,6 +238,31 @@ PKV_API pkv_status pkv_spec_verify_attention(
     int block_size, int64_t num_blocks, float scale, pkv_dtype dtype,
     void *workspace, size_t workspace_bytes, const pkv_options *options,
     int32_t *error_word, pkv_stream_t stream);
+
+/*
+ * pkv_append_attention -- the cache write and the attention of one step in a
+ * single launch: the num_queries new K/V rows of every sequence are written
+ * at their positions L_b - num_queries .. L_b - 1 (through the block table)
+ * and attended to, with the same results as pkv_kv_append followed by
+ * pkv_spec_verify_attention (pkv_paged_decode_attention for num_queries = 1).
+ * "Efficient Inference" (obvix) names this fusion (KV cache write +
+ * attention); "Inference part 2", section "Kernel fusion and torch.compile":
+ * a fused kernel saves a launch and a round trip through memory.
+ *
+ *   k_new, v_new : [batch, num_queries, num_kv_heads, head_dim] elt, device;
+ *                  row (b, j) is sequence b's row L_b - num_queries + j
+ *   k_cache, v_cache : written in place at those rows (the blocks must
+ *                  already be in the block table)
+ * Other arguments and layouts as for pkv_spec_verify_attention.  Rows at
+ * negative positions (L_b < num_queries) are ignored.
+ */
+PKV_API pkv_status pkv_append_attention(
+    void *out, const void *q, const void *k_new, const void *v_new, void *k_cache,
+    void *v_cache, const int32_t *block_table, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int batch, int num_queries,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+    float scale, pkv_dtype dtype, void *workspace, size_t workspace_bytes,
+    const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
 
 /*
  * pkv_read_error_word -- copy the device error word to *host_code after all

@@ -25,8 +25,11 @@ def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
 
 def attention_bytes(context_lens: Sequence[int], num_queries: int,
                     num_heads: int, num_kv_heads: int, head_dim: int,
-                    block_size: int, elt_bytes: int, num_splits_per_seq=None) -> dict:
-    """Algorithmic bytes of one paged attention call, by component."""
+                    block_size: int, elt_bytes: int, num_splits_per_seq=None,
+                    fused_append: bool = False) -> dict:
+    """Algorithmic bytes of one paged attention call, by component.  With
+    ``fused_append`` the call also reads the new K/V rows and writes them into
+    the cache (the rows it then reads are already counted in ``kv``)."""
     lens = [max(0, int(x)) for x in context_lens]
     B = len(lens)
     kv = 2 * sum(lens) * num_kv_heads * head_dim * elt_bytes
@@ -37,8 +40,11 @@ def attention_bytes(context_lens: Sequence[int], num_queries: int,
         rows = num_queries * num_heads
         # fp32 O (head_dim) + one fp32 LSE per split and row, written then read
         partials = 2 * sum(int(s) for s in num_splits_per_seq) * rows * (head_dim + 1) * 4
+    new_rows = 0
+    if fused_append:
+        new_rows = 2 * 2 * B * num_queries * num_kv_heads * head_dim * elt_bytes
     return {"kv": kv, "q": qo, "out": qo, "table": table, "partials": partials,
-            "total": kv + 2 * qo + table + partials}
+            "append": new_rows, "total": kv + 2 * qo + table + partials + new_rows}
 
 
 def append_bytes(num_tokens: int, num_kv_heads: int, head_dim: int,

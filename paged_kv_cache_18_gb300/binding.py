@@ -31,7 +31,8 @@ _DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_plan",
             "pkv_attention_plan_for", "pkv_attention_workspace_size",
             "pkv_paged_decode_attention", "pkv_spec_verify_attention",
-            "pkv_read_error_word", "pkv_paged_decode_attention_noalloc")
+            "pkv_read_error_word", "pkv_paged_decode_attention_noalloc",
+            "pkv_append_attention")
 
 
 class PkvError(RuntimeError):
@@ -41,7 +42,8 @@ class PkvError(RuntimeError):
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int), ("split_blocks", ctypes.c_int)]
+    _fields_ = [("kernel", ctypes.c_int), ("split_blocks", ctypes.c_int),
+                ("stages", ctypes.c_int)]
 
 
 class Plan(ctypes.Structure):
@@ -49,7 +51,8 @@ class Plan(ctypes.Structure):
                 ("row_chunks", ctypes.c_int), ("split_blocks", ctypes.c_int),
                 ("num_splits", ctypes.c_int), ("grid_x", ctypes.c_int),
                 ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int),
-                ("threads_per_cta", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("threads_per_cta", ctypes.c_int), ("stages", ctypes.c_int),
+                ("ctas_per_sm", ctypes.c_int),
                 ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self) -> dict:
@@ -88,6 +91,9 @@ def lib() -> ctypes.CDLL:
                                                     i32, i32, i32, i32, i64, f32, i32, vp, sz,
                                                     opt, vp, vp]
             L.pkv_read_error_word.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+            L.pkv_append_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
+                                               i32, i32, i32, i32, i32, i64, f32, i32, vp, sz,
+                                               opt, vp, vp]
             L.pkv_paged_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32,
                                                              i32, i32, i32, i32, i32, i64, f32,
                                                              i32, opt, vp, vp]
@@ -111,10 +117,10 @@ def _stream(t: torch.Tensor) -> int:
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
-def _opts(kernel: int, split_blocks: int):
-    if kernel == 0 and split_blocks == 0:
+def _opts(kernel: int, split_blocks: int, stages: int = 0):
+    if kernel == 0 and split_blocks == 0 and stages == 0:
         return None
-    return ctypes.byref(Options(kernel, split_blocks))
+    return ctypes.byref(Options(kernel, split_blocks, stages))
 
 
 def _need(cond: bool, msg: str) -> None:
@@ -159,38 +165,38 @@ def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
 
 def plan(batch: int, num_queries: int, num_heads: int, num_kv_heads: int, head_dim: int,
          max_context_len: int, dtype: torch.dtype, block_size: int = 16, kernel: int = 0,
-         split_blocks: int = 0) -> dict:
+         split_blocks: int = 0, stages: int = 0) -> dict:
     """The launch an attention call with these sizes makes on the current device."""
     p = Plan()
     _check("pkv_attention_plan", lib().pkv_attention_plan(
         batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
-        _DTYPE[dtype], _opts(kernel, split_blocks), ctypes.byref(p)))
+        _DTYPE[dtype], _opts(kernel, split_blocks, stages), ctypes.byref(p)))
     return p.as_dict()
 
 
 def plan_for(batch: int, num_queries: int, num_heads: int, num_kv_heads: int, head_dim: int,
              max_context_len: int, dtype: torch.dtype, num_sms: int, ctas_per_sm: int = 0,
-             block_size: int = 16, kernel: int = 0, split_blocks: int = 0) -> dict:
+             block_size: int = 16, kernel: int = 0, split_blocks: int = 0, stages: int = 0) -> dict:
     """The plan for a device with ``num_sms`` SMs (no GPU needed)."""
     p = Plan()
     _check("pkv_attention_plan_for", lib().pkv_attention_plan_for(
         batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
-        _DTYPE[dtype], _opts(kernel, split_blocks), num_sms, ctas_per_sm, ctypes.byref(p)))
+        _DTYPE[dtype], _opts(kernel, split_blocks, stages), num_sms, ctas_per_sm, ctypes.byref(p)))
     return p.as_dict()
 
 
 def workspace_size(batch: int, num_queries: int, num_heads: int, num_kv_heads: int,
                    head_dim: int, max_context_len: int, dtype: torch.dtype,
-                   block_size: int = 16, kernel: int = 0, split_blocks: int = 0) -> int:
+                   block_size: int = 16, kernel: int = 0, split_blocks: int = 0, stages: int = 0) -> int:
     n = ctypes.c_size_t(0)
     _check("pkv_attention_workspace_size", lib().pkv_attention_workspace_size(
         batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
-        _DTYPE[dtype], _opts(kernel, split_blocks), ctypes.byref(n)))
+        _DTYPE[dtype], _opts(kernel, split_blocks, stages), ctypes.byref(n)))
     return int(n.value)
 
 
 def _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_context_len, out,
-               workspace, kernel, split_blocks, error_word, num_queries):
+               workspace, kernel, split_blocks, error_word, num_queries, stages=0):
     NB, Hkv, bs, D = _cache_args(k_cache, v_cache)
     B = q.shape[0]
     Hq = q.shape[-2]
@@ -210,7 +216,7 @@ def _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_contex
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
     need = workspace_size(B, num_queries, Hq, Hkv, D, max_context_len, q.dtype, bs, kernel,
-                          split_blocks)
+                          split_blocks, stages)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
@@ -222,13 +228,13 @@ def _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_contex
     if num_queries == 1:
         st = L.pkv_paged_decode_attention(*args_common, Hq, Hkv, D, bs, NB, float(scale),
                                           _DTYPE[q.dtype], ws_ptr, ws_bytes,
-                                          _opts(kernel, split_blocks), _err_ptr(error_word),
+                                          _opts(kernel, split_blocks, stages), _err_ptr(error_word),
                                           _stream(q))
         _check("pkv_paged_decode_attention", st)
     else:
         st = L.pkv_spec_verify_attention(*args_common, num_queries, Hq, Hkv, D, bs, NB,
                                          float(scale), _DTYPE[q.dtype], ws_ptr, ws_bytes,
-                                         _opts(kernel, split_blocks), _err_ptr(error_word),
+                                         _opts(kernel, split_blocks, stages), _err_ptr(error_word),
                                          _stream(q))
         _check("pkv_spec_verify_attention", st)
     return out
@@ -240,14 +246,15 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            out: Optional[torch.Tensor] = None,
                            workspace: Optional[torch.Tensor] = None, kernel: int = 0,
                            split_blocks: int = 0,
-                           error_word: Optional[torch.Tensor] = None) -> torch.Tensor:
+                           error_word: Optional[torch.Tensor] = None,
+                           stages: int = 0) -> torch.Tensor:
     """Decode attention: q [B, Hq, D] -> out [B, Hq, D] over the paged cache
     (pkv_paged_decode_attention).  Pass ``max_context_len`` (a host bound of
     context_lens) to avoid a device read; pass ``workspace`` to avoid an
     allocation when the plan splits."""
     _need(q.dim() == 3, "q must be [batch, num_heads, head_dim]")
     return _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_context_len,
-                      out, workspace, kernel, split_blocks, error_word, 1)
+                      out, workspace, kernel, split_blocks, error_word, 1, stages)
 
 
 def spec_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -256,12 +263,60 @@ def spec_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
                           out: Optional[torch.Tensor] = None,
                           workspace: Optional[torch.Tensor] = None, kernel: int = 0,
                           split_blocks: int = 0,
-                          error_word: Optional[torch.Tensor] = None) -> torch.Tensor:
+                          error_word: Optional[torch.Tensor] = None,
+                          stages: int = 0) -> torch.Tensor:
     """Speculative verification: q [B, K+1, Hq, D] -> out of the same shape;
     query j sees rows <= L_b - (K+1) + j (pkv_spec_verify_attention)."""
     _need(q.dim() == 4, "q must be [batch, num_queries, num_heads, head_dim]")
     return _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_context_len,
-                      out, workspace, kernel, split_blocks, error_word, q.shape[1])
+                      out, workspace, kernel, split_blocks, error_word, q.shape[1], stages)
+
+
+def append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                     k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                     context_lens: torch.Tensor, scale: Optional[float] = None,
+                     max_context_len: Optional[int] = None, out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, kernel: int = 0,
+                     split_blocks: int = 0, error_word: Optional[torch.Tensor] = None,
+                     stages: int = 0) -> torch.Tensor:
+    """Write the new rows and attend in one launch (pkv_append_attention).
+
+    q [B, Q, Hq, D] (or [B, Hq, D] for Q = 1); k_new / v_new [B, Q, Hkv, D]
+    (or [B, Hkv, D]): row j of sequence b goes to position L_b - Q + j.
+    Returns out with q's shape."""
+    NB, Hkv, bs, D = _cache_args(k_cache, v_cache)
+    q4 = q if q.dim() == 4 else q.unsqueeze(1)
+    B, Q, Hq, _ = q4.shape
+    kn = k_new if k_new.dim() == 4 else k_new.unsqueeze(1)
+    vn = v_new if v_new.dim() == 4 else v_new.unsqueeze(1)
+    _need(kn.shape == (B, Q, Hkv, D) and vn.shape == kn.shape, "k_new/v_new [B, Q, Hkv, D]")
+    _need(kn.dtype == vn.dtype == q.dtype == k_cache.dtype, "dtype mismatch")
+    _need(kn.is_contiguous() and vn.is_contiguous() and q.is_contiguous(), "contiguity")
+    _need(q.shape[-1] == D and q.is_cuda, "q")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2
+          and block_table.shape[0] == B and block_table.is_contiguous() and block_table.is_cuda,
+          "block_table must be a contiguous CUDA int32 [batch, max_blocks_per_seq]")
+    _need(context_lens.dtype == torch.int32 and context_lens.shape == (B,)
+          and context_lens.is_cuda and context_lens.is_contiguous(), "context_lens")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0  # device read
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
+    need = workspace_size(B, Q, Hq, Hkv, D, max_context_len, q.dtype, bs, kernel, split_blocks,
+                          stages)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("pkv_append_attention", lib().pkv_append_attention(
+        out.data_ptr(), q.data_ptr(), kn.data_ptr(), vn.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), block_table.data_ptr(), block_table.shape[1], context_lens.data_ptr(),
+        max_context_len, B, Q, Hq, Hkv, D, bs, NB, float(scale), _DTYPE[q.dtype], ws_ptr,
+        ws_bytes, _opts(kernel, split_blocks, stages), _err_ptr(error_word), _stream(q)))
+    return out
 
 
 def read_error_word(error_word: torch.Tensor) -> int:

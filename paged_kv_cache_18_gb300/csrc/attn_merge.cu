@@ -11,29 +11,43 @@
 //   out = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M).
 // A split with no visible row has lse_s = -inf and weight 0; a row with no
 // visible row at all gets zeros.
+//
+// One CTA per output row.  Long contexts give rows of many splits, so the
+// loads are spread: warp w takes splits w, w + 4, ..., four at a time, which
+// keeps 16 partial vectors in flight per row; the warps meet in shared
+// memory at the end.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
 
+constexpr int kMergeWarps = 4;
+constexpr int kMergeUnroll = 4;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
-  constexpr int PER = D / 32;  // elements per lane (2, 4 or 8)
-  const int64_t nrows = static_cast<int64_t>(p.batch) * p.num_queries * p.num_heads;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= nrows) return;
+__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const AttnParams p) {
+  constexpr int PER = D / 32;  // elements per lane: 2, 4 or 8
+  const int64_t row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = static_cast<int>(row / (static_cast<int64_t>(p.num_queries) * p.num_heads));
   const SeqExtent ext = seq_extent(p, b, false);
   int ns = (ext.nblk + p.split_blocks - 1) / p.split_blocks;
   ns = ns < 1 ? 1 : (ns > p.num_splits ? p.num_splits : ns);
 
+  __shared__ float red_max[kMergeWarps];
+  __shared__ float red_sum[kMergeWarps];
+  __shared__ float red_acc[kMergeWarps][D];
+
   const float *lse = p.part_lse + row * p.num_splits;
   float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, lse[s]);
+  for (int s = threadIdx.x; s < ns; s += kMergeWarps * 32) M = fmaxf(M, lse[s]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  if (lane == 0) red_max[warp] = M;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, red_max[w]);
 
   float acc[PER];
 #pragma unroll
@@ -41,32 +55,57 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
   float wsum = 0.f;
   if (M != -INFINITY) {
     const float *po = p.part_o + row * p.num_splits * D + lane * PER;
-    for (int s = 0; s < ns; ++s) {
-      const float w = ex2(lse[s] - M);
-      wsum += w;
+    for (int s0 = warp; s0 < ns; s0 += kMergeWarps * kMergeUnroll) {
+      float w[kMergeUnroll];
+      float v[kMergeUnroll][PER];
 #pragma unroll
-      for (int e = 0; e < PER; e += 2) {
-        const float2 v = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(s) * D + e);
-        acc[e] = fmaf(w, v.x, acc[e]);
-        acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+      for (int u = 0; u < kMergeUnroll; ++u) {
+        const int s = s0 + u * kMergeWarps;
+        const bool ok = s < ns;
+        w[u] = ok ? ex2(lse[ok ? s : 0] - M) : 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; e += 2) {
+          const float2 x = ok ? *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(s) * D + e)
+                              : make_float2(0.f, 0.f);
+          v[u][e] = x.x;
+          v[u][e + 1] = x.y;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeUnroll; ++u) {
+        wsum += w[u];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(w[u], v[u][e], acc[e]);
       }
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  T *dst = reinterpret_cast<T *>(p.out) + row * D + lane * PER;
+  if (lane == 0) red_sum[warp] = wsum;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) dst[e] = from_float<T>(acc[e] * inv);
+  for (int e = 0; e < PER; ++e) red_acc[warp][lane * PER + e] = acc[e];
+  __syncthreads();
+  float total = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) total += red_sum[w];
+  const float inv = total > 0.f ? 1.f / total : 0.f;
+  T *dst = reinterpret_cast<T *>(p.out) + row * D;
+  for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) {
+    float x = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) x += red_acc[w][d];
+    dst[d] = from_float<T>(x * inv);
+  }
 }
 
 template <typename T>
 cudaError_t merge_t(int D, const AttnParams &p, cudaStream_t stream) {
   const int64_t nrows = static_cast<int64_t>(p.batch) * p.num_queries * p.num_heads;
-  const int rows_per_cta = 8;
-  const dim3 grid(static_cast<unsigned>((nrows + rows_per_cta - 1) / rows_per_cta));
+  if (nrows == 0) return cudaSuccess;
+  if (nrows > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(nrows));
   switch (D) {
-    case 64: attn_merge_kernel<T, 64><<<grid, 256, 0, stream>>>(p); break;
-    case 128: attn_merge_kernel<T, 128><<<grid, 256, 0, stream>>>(p); break;
-    case 256: attn_merge_kernel<T, 256><<<grid, 256, 0, stream>>>(p); break;
+    case 64: attn_merge_kernel<T, 64><<<grid, kMergeWarps * 32, 0, stream>>>(p); break;
+    case 128: attn_merge_kernel<T, 128><<<grid, kMergeWarps * 32, 0, stream>>>(p); break;
+    case 256: attn_merge_kernel<T, 256><<<grid, kMergeWarps * 32, 0, stream>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -27,11 +27,17 @@
 // movmatrix.trans.  Rows past the context and masked (verify) entries get
 // -inf scores; the V^T fragments of rows past the context are zeroed, so
 // NaN-filled unused rows never reach the output.
+#include <type_traits>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 namespace {
+
+// Largest excess (log2 units) of a score over its column's reference max
+// before the reference is raised: block weights stay below 2^8.
+constexpr float kRescaleSlack = 8.f;
 
 template <int D> struct MmaGeom {
   static constexpr int kParts = D / 64;                 // 128-byte panels per row
@@ -175,54 +181,80 @@ __global__ void __launch_bounds__(W * 32)
     const uint32_t vtile = ktile + G::kTileBytes;
     const int key0 = (blk_begin + warp + i * W) * kBlockSize;
     const bool bad = (bad_mask >> (i & 31)) & 1u;
+    if (p.k_new != nullptr && !bad && key0 + kBlockSize > L - p.num_queries) {
+      const int64_t phys = __ldg(table + static_cast<int64_t>(i) * W);
+      patch_new_rows<D, 2>(p, ktile, vtile, b, kvh, key0, L, phys, chunk == 0,
+                           [](int r, int vec) { return swz<D>(r, vec * 8); });
+    }
 
-    // S^T = K Q^T
-    float sc[NT][4];
+    // S^T = K Q^T, the head-dim steps split over two accumulator chains.
+    float sc[NT][4], sc2[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] = sc2[nt][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
       ldsm_x4(a, ktile + swz<D>(lane & 15, ks * 16 + (lane >> 4) * 8));
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) Mma<T>::run(sc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+      for (int nt = 0; nt < NT; ++nt) {
+        if (ks & 1)
+          Mma<T>::run(sc2[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+        else
+          Mma<T>::run(sc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+      }
     }
     const bool need_mask = bad || key0 + kBlockSize > mask_from;
+    bool above = false;  // some score exceeds its column's reference by > the slack
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float v = sc[nt][e] * p.scale_log2;
+        float v = (sc[nt][e] + sc2[nt][e]) * p.scale_log2;
         if (need_mask) {
           const int key = key0 + g + ((e >> 1) << 3);
           if (bad || key >= lim[nt][e & 1]) v = -INFINITY;
         }
         sc[nt][e] = v;
+        above |= v > m[nt][e & 1] + kRescaleSlack;
       }
-    // Online softmax update, per column (max over the 16 keys of the block:
-    // 2 per thread, then across the 8 lanes that share the column).
+    // Online softmax.  The exponentials use a per-column reference m that is
+    // raised (to the exact running max, rescaling l and O by 2^(m_old - m))
+    // only when a score exceeds it by more than kRescaleSlack; otherwise the
+    // block's weights 2^(s - m) stay below 2^kRescaleSlack and no cross-lane
+    // max, correction or rescale is needed.  The result O / l does not depend
+    // on the reference.
+    if (__any_sync(kFull, above)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float mx = fmaxf(sc[nt][e], sc[nt][e + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+          const float m_new = fmaxf(m[nt][e], mx);
+          const float corr = ex2(m[nt][e] - (m_new == -INFINITY ? 0.f : m_new));
+          l[nt][e] *= corr;
+          m[nt][e] = m_new;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            o[mt][nt][e] *= corr;
+            o[mt][nt][e + 2] *= corr;
+          }
+        }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float mx = fmaxf(sc[nt][e], sc[nt][e + 2]);
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-        const float m_new = fmaxf(m[nt][e], mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float corr = ex2(m[nt][e] - m_use);
+        const float m_use = m[nt][e] == -INFINITY ? 0.f : m[nt][e];
         const float p0 = ex2(sc[nt][e] - m_use);
         const float p1 = ex2(sc[nt][e + 2] - m_use);
-        l[nt][e] = l[nt][e] * corr + p0 + p1;
-        m[nt][e] = m_new;
+        l[nt][e] += p0 + p1;
         sc[nt][e] = p0;
         sc[nt][e + 2] = p1;
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          o[mt][nt][e] *= corr;
-          o[mt][nt][e + 2] *= corr;
-        }
       }
     // P^T operand fragments: high part and rounding remainder.
     uint32_t ph[NT][2], pl[NT][2];
@@ -240,27 +272,37 @@ __global__ void __launch_bounds__(W * 32)
       pl[nt][0] = movm_t(l01);
       pl[nt][1] = movm_t(l23);
     }
-    // O^T += V^T P^T.  Zero the V^T columns (keys) past the context.
+    // O^T += V^T P^T.  In a block that ends past the context, zero the V^T
+    // columns (keys) past it so that NaN-filled rows never enter an MMA.
     const int nvalid = bad ? 0 : L - key0;
-    uint32_t km0 = 0xffffffffu, km8 = 0xffffffffu;
-    if (nvalid < kBlockSize) {
-      km0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
-      km8 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
-    }
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      uint32_t a[4];
-      ldsm_x4_t(a, vtile + swz<D>((lane & 7) + ((lane >> 4) << 3), mt * 16 + ((lane >> 3) & 1) * 8));
-      a[0] &= km0;
-      a[1] &= km0;
-      a[2] &= km8;
-      a[3] &= km8;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        Mma<T>::run(o[mt][nt], a, ph[nt][0], ph[nt][1]);
-        Mma<T>::run(o[mt][nt], a, pl[nt][0], pl[nt][1]);
+    auto pv = [&](auto partial) {
+      uint32_t km0 = 0xffffffffu, km8 = 0xffffffffu;
+      if (decltype(partial)::value) {
+        km0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
+        km8 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
       }
-    }
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_t(a, vtile + swz<D>((lane & 7) + ((lane >> 4) << 3),
+                                    mt * 16 + ((lane >> 3) & 1) * 8));
+        if (decltype(partial)::value) {
+          a[0] &= km0;
+          a[1] &= km0;
+          a[2] &= km8;
+          a[3] &= km8;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          Mma<T>::run(o[mt][nt], a, ph[nt][0], ph[nt][1]);
+          Mma<T>::run(o[mt][nt], a, pl[nt][0], pl[nt][1]);
+        }
+      }
+    };
+    if (nvalid < kBlockSize)
+      pv(std::true_type{});
+    else
+      pv(std::false_type{});
     __syncwarp();
     if (i + NS < n_my) {
       issue(i + NS);
@@ -319,93 +361,109 @@ __global__ void __launch_bounds__(W * 32)
 
 constexpr int kMmaWarps = 4;
 
-template <int D> constexpr int mma_stages() { return D >= 256 ? 2 : 3; }
+// Stages per warp: the default (deep) ring and one stage less, which frees
+// shared memory for one more resident CTA per SM.
+template <int D, bool DEEP> constexpr int mma_stages() {
+  return (D >= 256 ? 2 : 3) - (DEEP ? 0 : 1);
+}
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool DEEP>
 constexpr size_t mma_smem_bytes() {
-  constexpr int NS = mma_stages<D>();
+  constexpr int NS = mma_stages<D, DEEP>();
   constexpr size_t stages = size_t(kMmaWarps) * NS * MmaGeom<D>::kStageBytes;
   constexpr size_t red = (size_t(kMmaWarps) * NT * 8 * (D + 4) + size_t(kMmaWarps + 2) * NT * 8 * 2 +
                           size_t(kMmaWarps) * NT * 8) * 4;
-  static_assert(red <= stages, "epilogue scratch must fit in the stage memory");
-  return stages + size_t(kMmaWarps) * NS * 8 + 1024;
+  constexpr size_t scratch = red > stages ? red : stages;
+  return scratch + size_t(kMmaWarps) * NS * 8 + 1024;
 }
 
-template <typename T, int D, int NT>
+using MmaLaunch = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const AttnParams &,
+                                  dim3, cudaStream_t);
+
+template <typename T, int D, int NT, bool DEEP>
 KernelInfo mma_info_t() {
   KernelInfo k;
-  k.func = reinterpret_cast<const void *>(&attn_mma_kernel<T, D, NT, kMmaWarps, mma_stages<D>()>);
+  k.func = reinterpret_cast<const void *>(
+      &attn_mma_kernel<T, D, NT, kMmaWarps, mma_stages<D, DEEP>()>);
   k.threads = kMmaWarps * 32;
-  k.smem = mma_smem_bytes<T, D, NT>();
+  k.smem = mma_smem_bytes<T, D, NT, DEEP>();
   k.warps = kMmaWarps;
+  k.stages = mma_stages<D, DEEP>();
   return k;
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool DEEP>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
-  const KernelInfo k = mma_info_t<T, D, NT>();
-  attn_mma_kernel<T, D, NT, kMmaWarps, mma_stages<D>()>
+  const KernelInfo k = mma_info_t<T, D, NT, DEEP>();
+  attn_mma_kernel<T, D, NT, kMmaWarps, mma_stages<D, DEEP>()>
       <<<grid, k.threads, k.smem, stream>>>(km, vm, p);
   return cudaGetLastError();
 }
 
-template <typename T, int D>
-bool mma_pick(int nt, KernelInfo *info, cudaError_t (**launch)(const CUtensorMap &,
-                                                                 const CUtensorMap &,
-                                                                 const AttnParams &, dim3,
-                                                                 cudaStream_t)) {
-  switch (nt) {
-#define PKV_NT_CASE(N)                     \
-  case N:                                  \
-    if (N * D > 384) return false;         \
-    *info = mma_info_t<T, D, (N * D > 384 ? 1 : N)>(); \
-    *launch = &launch_t<T, D, (N * D > 384 ? 1 : N)>;  \
+// Default ring: 2 stages per warp (3 CTAs per SM at head_dim <= 128; the
+// 8-row GQA tile measured 0.949 of the HBM peak against 0.932 with 3).
+template <typename T, int D, int NT>
+bool mma_pick_stages(int stages, KernelInfo *info, MmaLaunch *launch) {
+  if (stages == 0) stages = 2;
+  if (stages == mma_stages<D, true>()) {
+    *info = mma_info_t<T, D, NT, true>();
+    *launch = &launch_t<T, D, NT, true>;
     return true;
-    PKV_NT_CASE(1)
-    PKV_NT_CASE(2)
-    PKV_NT_CASE(3)
-    PKV_NT_CASE(4)
-#undef PKV_NT_CASE
-    default:
-      return false;
+  }
+  if (stages == mma_stages<D, false>()) {
+    *info = mma_info_t<T, D, NT, false>();
+    *launch = &launch_t<T, D, NT, false>;
+    return true;
+  }
+  return false;
+}
+
+// Column tiles x head dim kept within the register budget (N-tiles * D <= 384).
+template <typename T, int D>
+bool mma_pick(int nt, int stages, KernelInfo *info, MmaLaunch *launch) {
+  switch (nt) {
+    case 1: return mma_pick_stages<T, D, 1>(stages, info, launch);
+    case 2: return D <= 128 && mma_pick_stages<T, D, (D <= 128 ? 2 : 1)>(stages, info, launch);
+    case 3: return D <= 128 && mma_pick_stages<T, D, (D <= 128 ? 3 : 1)>(stages, info, launch);
+    case 4: return D <= 64 && mma_pick_stages<T, D, (D <= 64 ? 4 : 1)>(stages, info, launch);
+    default: return false;
   }
 }
 
 template <typename T>
-bool mma_pick_d(int D, int nt, KernelInfo *info,
-                cudaError_t (**launch)(const CUtensorMap &, const CUtensorMap &,
-                                       const AttnParams &, dim3, cudaStream_t)) {
+bool mma_pick_d(int D, int nt, int stages, KernelInfo *info, MmaLaunch *launch) {
   switch (D) {
-    case 64: return mma_pick<T, 64>(nt, info, launch);
-    case 128: return mma_pick<T, 128>(nt, info, launch);
-    case 256: return mma_pick<T, 256>(nt, info, launch);
+    case 64: return mma_pick<T, 64>(nt, stages, info, launch);
+    case 128: return mma_pick<T, 128>(nt, stages, info, launch);
+    case 256: return mma_pick<T, 256>(nt, stages, info, launch);
     default: return false;
   }
+}
+
+bool mma_pick_any(pkv_dtype dtype, int D, int nt, int stages, KernelInfo *info,
+                  MmaLaunch *launch) {
+  if (dtype == PKV_BF16) return mma_pick_d<__nv_bfloat16>(D, nt, stages, info, launch);
+  if (dtype == PKV_F16) return mma_pick_d<__half>(D, nt, stages, info, launch);
+  return false;
 }
 
 }  // namespace
 
 int mma_max_tiles(int head_dim) { return head_dim <= 64 ? 4 : (head_dim <= 128 ? 3 : 1); }
 
-bool mma_kernel_info(pkv_dtype dtype, int head_dim, int n_tiles, KernelInfo *info) {
-  cudaError_t (*launch)(const CUtensorMap &, const CUtensorMap &, const AttnParams &, dim3,
-                        cudaStream_t) = nullptr;
-  if (dtype == PKV_BF16) return mma_pick_d<__nv_bfloat16>(head_dim, n_tiles, info, &launch);
-  if (dtype == PKV_F16) return mma_pick_d<__half>(head_dim, n_tiles, info, &launch);
-  return false;
+bool mma_kernel_info(pkv_dtype dtype, int head_dim, int n_tiles, int stages, KernelInfo *info) {
+  MmaLaunch launch = nullptr;
+  return mma_pick_any(dtype, head_dim, n_tiles, stages, info, &launch);
 }
 
-cudaError_t mma_launch(pkv_dtype dtype, int head_dim, int n_tiles, const CUtensorMap &kmap,
-                       const CUtensorMap &vmap, const AttnParams &p, dim3 grid,
-                       cudaStream_t stream) {
+cudaError_t mma_launch(pkv_dtype dtype, int head_dim, int n_tiles, int stages,
+                       const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
+                       dim3 grid, cudaStream_t stream) {
   KernelInfo info;
-  cudaError_t (*launch)(const CUtensorMap &, const CUtensorMap &, const AttnParams &, dim3,
-                        cudaStream_t) = nullptr;
-  bool ok = false;
-  if (dtype == PKV_BF16) ok = mma_pick_d<__nv_bfloat16>(head_dim, n_tiles, &info, &launch);
-  if (dtype == PKV_F16) ok = mma_pick_d<__half>(head_dim, n_tiles, &info, &launch);
-  if (!ok) return cudaErrorInvalidValue;
+  MmaLaunch launch = nullptr;
+  if (!mma_pick_any(dtype, head_dim, n_tiles, stages, &info, &launch))
+    return cudaErrorInvalidValue;
   return launch(kmap, vmap, p, grid, stream);
 }
 

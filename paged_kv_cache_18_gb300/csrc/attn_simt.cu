@@ -170,6 +170,11 @@ __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
     const uint32_t vtile = ktile + TILE;
     const int key0 = (blk_begin + warp + i * W) * kBlockSize;
     const bool bad = (bad_mask >> (i & 31)) & 1u;
+    if (p.k_new != nullptr && !bad && key0 + kBlockSize > L - p.num_queries) {
+      const int64_t phys = __ldg(table + static_cast<int64_t>(i) * W);
+      patch_new_rows<D, ELT>(p, ktile, vtile, b, kvh, key0, L, phys, chunk == 0,
+                             [](int r, int vec) { return static_cast<uint32_t>(r * RB + vec * 16); });
+    }
 
     // Scores of rows rg, rg+4, rg+8, rg+12 for every query row.
     float sc[4][R];
@@ -307,6 +312,7 @@ KernelInfo simt_info_t() {
   k.threads = kSimtWarps * 32;
   k.smem = simt_smem_bytes<T, D, R>();
   k.warps = kSimtWarps;
+  k.stages = simt_stages<T, D>();
   return k;
 }
 

@@ -29,6 +29,8 @@ struct AttnParams {
   const void *v_cache;
   const int32_t *block_table;   // [B, max_blocks_per_seq]
   const int32_t *context_lens;  // [B]
+  const void *k_new;            // [B, Q, Hkv, D] elt: new rows appended in the same launch
+  const void *v_new;            //   (nullptr: the cache already holds them)
   float *part_o;                // [B*Q*Hq, num_splits, D]   (split-K only)
   float *part_lse;              // [B*Q*Hq, num_splits]      (log2 units)
   int32_t *err;                 // optional device error word
@@ -236,6 +238,49 @@ __device__ __forceinline__ SeqExtent seq_extent(const AttnParams &p, int b, bool
     L = nblk * kBlockSize;
   }
   return {L, nblk};
+}
+
+// Fused append.  The Q new rows of sequence b sit at logical positions
+// L - Q .. L - 1.  A warp that has just received the tile of block `blk`
+// (first row key0) overwrites the tile rows of any new position in it with
+// k_new / v_new (so the attention sees them whatever the cache held there),
+// and, when `write_cache` is set, also stores them into the cache at the
+// physical block `phys` for the steps that follow.  `row_off(r, vec)` gives
+// the byte offset of 16-byte vector `vec` of tile row r in shared memory.
+template <int D, int ELT, typename RowOff>
+__device__ __forceinline__ void patch_new_rows(const AttnParams &p, uint32_t ktile,
+                                               uint32_t vtile, int b, int kvh, int key0, int L,
+                                               int64_t phys, bool write_cache, RowOff row_off) {
+  constexpr int VPR = D * ELT / 16;  // 16-byte vectors per row
+  const int first = max(L - p.num_queries, key0);
+  const int last = min(L, key0 + kBlockSize);  // exclusive
+  const int n = (last - first) * VPR;
+  const int lane = threadIdx.x & 31;
+  for (int idx = lane; idx < n; idx += 32) {
+    const int r = first + idx / VPR;  // logical row
+    const int vec = idx - (idx / VPR) * VPR;
+    const int j = r - (L - p.num_queries);
+    const int64_t src = ((static_cast<int64_t>(b) * p.num_queries + j) * p.num_kv_heads + kvh) *
+                            VPR + vec;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(p.k_new) + src);
+    const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(p.v_new) + src);
+    const uint32_t off = row_off(r - key0, vec);
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(ktile + off), "r"(kv.x), "r"(kv.y),
+                 "r"(kv.z), "r"(kv.w)
+                 : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(vtile + off), "r"(vv.x), "r"(vv.y),
+                 "r"(vv.z), "r"(vv.w)
+                 : "memory");
+    if (write_cache) {
+      const int64_t dst = ((phys * p.num_kv_heads + kvh) * kBlockSize + (r - key0)) * VPR + vec;
+      reinterpret_cast<uint4 *>(const_cast<void *>(p.k_cache))[dst] = kv;
+      reinterpret_cast<uint4 *>(const_cast<void *>(p.v_cache))[dst] = vv;
+    }
+  }
+  // The patched stage may be refilled by a bulk copy later: order these
+  // generic writes before any later async-proxy write to the same memory.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
 }
 
 // CTA epilogue.  Every warp w has left, for each of the NC query columns of

@@ -17,15 +17,17 @@ struct KernelInfo {
   const void *func = nullptr;
   int threads = 0;
   int warps = 0;
+  int stages = 0;
   size_t smem = 0;
 };
 
-// Tensor-core kernel: n_tiles = query columns / 8.
+// Tensor-core kernel: n_tiles = query columns / 8; stages = per-warp ring
+// depth (0 = default).
 int mma_max_tiles(int head_dim);
-bool mma_kernel_info(pkv_dtype dtype, int head_dim, int n_tiles, KernelInfo *info);
-cudaError_t mma_launch(pkv_dtype dtype, int head_dim, int n_tiles, const CUtensorMap &kmap,
-                       const CUtensorMap &vmap, const AttnParams &p, dim3 grid,
-                       cudaStream_t stream);
+bool mma_kernel_info(pkv_dtype dtype, int head_dim, int n_tiles, int stages, KernelInfo *info);
+cudaError_t mma_launch(pkv_dtype dtype, int head_dim, int n_tiles, int stages,
+                       const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
+                       dim3 grid, cudaStream_t stream);
 
 // CUDA-core kernel: rows = query rows per CTA (1, 2, 4 or 8).
 int simt_max_rows(int head_dim);

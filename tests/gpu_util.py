@@ -56,20 +56,22 @@ class DeviceBatch:
         pkv.kv_append(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slots,
                       error_word=self.err)
 
-    def attend(self, kernel=0, split_blocks=0, out=None, workspace=None):
+    def attend(self, kernel=0, split_blocks=0, out=None, workspace=None, stages=0):
         wl = self.b.wl
         if wl.num_queries == 1:
             o = pkv.paged_decode_attention(self.q[:, 0], self.k_cache, self.v_cache, self.table,
                                            self.lens, scale=wl.softmax_scale,
                                            max_context_len=self.b.max_context_len, out=out,
                                            workspace=workspace, kernel=kernel,
-                                           split_blocks=split_blocks, error_word=self.err)
+                                           split_blocks=split_blocks, error_word=self.err,
+                                           stages=stages)
             return o[:, None]
         return pkv.spec_verify_attention(self.q, self.k_cache, self.v_cache, self.table,
                                          self.lens, scale=wl.softmax_scale,
                                          max_context_len=self.b.max_context_len, out=out,
                                          workspace=workspace, kernel=kernel,
-                                         split_blocks=split_blocks, error_word=self.err)
+                                         split_blocks=split_blocks, error_word=self.err,
+                                         stages=stages)
 
 
 def oracle_after_append(b: W.PagedBatch, rows=None) -> np.ndarray:

@@ -98,6 +98,8 @@ def test_plan_kernel_choice():
     assert p["kernel"] == binding.PKV_KERNEL_SIMT
     p = binding.plan_for(32, 1, 40, 40, 128, 2048, torch.bfloat16, num_sms=152)
     assert p["kernel"] == binding.PKV_KERNEL_MMA and p["rows_per_cta"] == 1
+    p = binding.plan_for(128, 1, 32, 8, 128, 4096, torch.bfloat16, num_sms=152)
+    assert p["kernel"] == binding.PKV_KERNEL_MMA and p["rows_per_cta"] == 4
     with pytest.raises(binding.PkvError):
         binding.plan_for(1, 1, 8, 8, 64, 16, torch.float32, num_sms=152,
                          kernel=binding.PKV_KERNEL_MMA)
@@ -130,7 +132,8 @@ def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
 
 def test_plan_splits_long_contexts_and_honours_override():
     p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152)
-    assert p["num_splits"] > 16     # 16 (sequence, KV head) pairs cannot fill 152 SMs
+    # 16 (sequence, KV head) pairs cannot fill 152 SMs: split, at most 16 ways
+    assert 8 <= p["num_splits"] <= 16
     p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152, split_blocks=7)
     assert p["split_blocks"] == 7 and p["num_splits"] == -(-4096 // 7)
     p = binding.plan_for(2, 1, 32, 8, 128, 100, torch.bfloat16, num_sms=152, split_blocks=1000)

@@ -18,11 +18,11 @@ pytestmark = pytest.mark.gpu
 EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 100]
 
 
-def run_case(wl, kernel=0, split_blocks=0):
+def run_case(wl, kernel=0, split_blocks=0, stages=0):
     b = W.make_batch(wl)
     d = DeviceBatch(b)
     d.append()
-    out = d.attend(kernel=kernel, split_blocks=split_blocks)
+    out = d.attend(kernel=kernel, split_blocks=split_blocks, stages=stages)
     torch.cuda.synchronize()
     ref = oracle_after_append(b)
     # the append is bit-exact over the whole cache
@@ -70,6 +70,15 @@ def test_forced_splits_verify(split_blocks):
     wl = W.Workload("split verify", 4, 32, 8, 128, "bf16", context_lens=[5, 17, 21, 500],
                     num_queries=5, seed=320 + split_blocks)
     run_case(wl, kernel=2, split_blocks=split_blocks)
+
+
+@pytest.mark.parametrize("D,stages", [(64, 2), (64, 3), (128, 2), (128, 3), (256, 1), (256, 2)])
+@pytest.mark.parametrize("Q,Hq,Hkv", [(1, 32, 8), (5, 32, 8), (1, 8, 1)])
+def test_mma_stage_depths(D, stages, Q, Hq, Hkv):
+    lens = [Q, 16, 17, 50, 257, 1000]
+    wl = W.Workload(f"stages {stages} D{D} Q{Q}", len(lens), Hq, Hkv, D, "bf16",
+                    context_lens=lens, num_queries=Q, seed=400 + D + stages + Q)
+    run_case(wl, kernel=2, stages=stages)
 
 
 def test_zero_and_short_contexts_give_zero_rows():
@@ -221,3 +230,57 @@ def test_named_workload_full_size(name):
     # every output row is finite (no NaN-filled row was read)
     assert np.isfinite(got).all()
     print(f"{name}: max-abs {max_abs:.3e} rel-L2 {rel:.3e}")
+
+
+# ---- fused append + attention (one launch) --------------------------------
+@pytest.mark.parametrize("dtype,kernel", [("f32", "simt"), ("bf16", "simt"), ("bf16", "mma"),
+                                          ("f16", "mma")])
+@pytest.mark.parametrize("Q,Hq,Hkv", [(1, 8, 2), (1, 4, 4), (5, 32, 8), (3, 8, 1)])
+@pytest.mark.parametrize("split_blocks", [0, 1, 3])
+def test_fused_append_attention(dtype, kernel, Q, Hq, Hkv, split_blocks):
+    import paged_kv_cache_18_gb300 as pkv
+    lens = [max(1, Q - 1), Q, Q + 1, 16, 17, 31, 33, 100, 250]
+    D = 128 if dtype != "f32" else 64
+    wl = W.Workload(f"fused {dtype} {kernel} Q{Q}", len(lens), Hq, Hkv, D, dtype,
+                    context_lens=lens, num_queries=Q, seed=500 + Q + Hq + split_blocks)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    B = wl.batch
+    kn = d.k_new.view(B, Q, Hkv, D)
+    vn = d.v_new.view(B, Q, Hkv, D)
+    q = d.q if Q > 1 else d.q[:, 0]
+    out = pkv.append_attention(q, kn, vn, d.k_cache, d.v_cache, d.table, d.lens,
+                               scale=wl.softmax_scale, max_context_len=b.max_context_len,
+                               kernel=KERNELS[kernel], split_blocks=split_blocks,
+                               error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    ref = oracle_after_append(b)
+    bits = cache_bits(d.k_cache)
+    np.testing.assert_array_equal(bits, b.k_cache.view(bits.dtype))
+    bits = cache_bits(d.v_cache)
+    np.testing.assert_array_equal(bits, b.v_cache.view(bits.dtype))
+    got = host_f64(out if Q > 1 else out[:, None], dtype)
+    assert_close(got, ref, dtype, wl.name)
+
+
+def test_fused_matches_two_calls_bitwise():
+    """Same plan, same arithmetic: the fused launch and append-then-attend
+    give bit-identical outputs."""
+    import paged_kv_cache_18_gb300 as pkv
+    wl = W.Workload("fused bitwise", 6, 32, 8, 128, "bf16", len_range=(20, 3000), seed=77)
+    for Q in (1, 5):
+        wl.num_queries = Q
+        b = W.make_batch(wl)
+        d1, d2 = DeviceBatch(b), DeviceBatch(b)
+        d1.append()
+        o1 = d1.attend()
+        kn = d2.k_new.view(wl.batch, Q, 8, 128)
+        vn = d2.v_new.view(wl.batch, Q, 8, 128)
+        o2 = pkv.append_attention(d2.q if Q > 1 else d2.q[:, 0], kn, vn, d2.k_cache,
+                                  d2.v_cache, d2.table, d2.lens,
+                                  max_context_len=b.max_context_len)
+        o2 = o2 if Q > 1 else o2[:, None]
+        assert torch.equal(o1, o2)
+        for a, c in ((d1.k_cache, d2.k_cache), (d1.v_cache, d2.v_cache)):
+            assert torch.equal(a.view(torch.int16), c.view(torch.int16))
