@@ -274,6 +274,7 @@ def run_ours(args):
         pkv_build.build()
     barrier()
     import paged_kv_cache_18_gb300 as pkv
+    pkv.binding.TUNING.update(rows_per_cta=args.rows_per_cta, merge=args.merge)
 
     wl = W.WORKLOADS[args.workload]
     if rank > 0:
@@ -455,6 +456,8 @@ def main(argv=None):
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--split-blocks", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0, help="tensor-core kernel ring depth")
+    ap.add_argument("--rows-per-cta", type=int, default=0, help="cap on query rows per CTA")
+    ap.add_argument("--merge", type=int, default=0, help="0 planner, 1 fused, 2 separate kernel")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--unfused", action="store_true",

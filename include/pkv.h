@@ -108,6 +108,9 @@ typedef struct pkv_options {
   int split_blocks; /* 0: planner; > 0: KV blocks per split-K chunk */
   int stages;       /* 0: planner; tensor-core kernel: per-warp ring depth
                        (2 or 3 at head_dim <= 128, 1 or 2 at 256) */
+  int rows_per_cta; /* 0: planner; cap on the query rows one CTA serves */
+  int merge;        /* split-K merge: 0 planner, 1 by the sequence's last CTA,
+                       2 by a separate kernel */
 } pkv_options;
 
 /* What one attention call launches (see pkv_attention_plan). */

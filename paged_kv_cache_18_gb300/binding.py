@@ -43,7 +43,13 @@ class PkvError(RuntimeError):
 
 class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("split_blocks", ctypes.c_int),
-                ("stages", ctypes.c_int)]
+                ("stages", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
+                ("merge", ctypes.c_int)]
+
+
+# Extra launch controls for tuning runs (pkv_options.rows_per_cta / .merge);
+# module-wide so that every binding call passes them.  Empty = planner.
+TUNING = {}
 
 
 class Plan(ctypes.Structure):
@@ -118,9 +124,10 @@ def _stream(t: torch.Tensor) -> int:
 
 
 def _opts(kernel: int, split_blocks: int, stages: int = 0):
-    if kernel == 0 and split_blocks == 0 and stages == 0:
+    rows, merge = TUNING.get("rows_per_cta", 0), TUNING.get("merge", 0)
+    if kernel == 0 and split_blocks == 0 and stages == 0 and rows == 0 and merge == 0:
         return None
-    return ctypes.byref(Options(kernel, split_blocks, stages))
+    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge))
 
 
 def _need(cond: bool, msg: str) -> None:

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(W * 32)
   const int blk_begin = split * p.split_blocks;
   if (split > 0 && blk_begin >= ext.nblk) return;  // this sequence has fewer splits
   const int blk_end = min(blk_begin + p.split_blocks, ext.nblk);
+  const int ns_b = max(1, min(p.num_splits, (ext.nblk + p.split_blocks - 1) / p.split_blocks));
   const int nspan = max(blk_end - blk_begin, 0);
   const int n_my = nspan > warp ? (nspan - warp + W - 1) / W : 0;
 
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(W * 32)
       }
   }
   __syncthreads();
-  cta_epilogue<T, D, NC, W>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split);
+  cta_epilogue<T, D, NC, W>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split, ns_b);
 }
 
 constexpr int kMmaWarps = 4;

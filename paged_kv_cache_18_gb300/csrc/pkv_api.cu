@@ -116,8 +116,9 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
     kernel = (s.dtype == PKV_F32) ? PKV_KERNEL_SIMT : PKV_KERNEL_MMA;
   if (kernel == PKV_KERNEL_MMA && s.dtype == PKV_F32) return false;
   if (kernel != PKV_KERNEL_MMA && kernel != PKV_KERNEL_SIMT) return false;
-  const int cap = kernel == PKV_KERNEL_MMA ? 8 * mma_max_tiles(s.head_dim)
-                                           : simt_max_rows(s.head_dim);
+  int cap = kernel == PKV_KERNEL_MMA ? 8 * mma_max_tiles(s.head_dim)
+                                     : simt_max_rows(s.head_dim);
+  if (opt && opt->rows_per_cta > 0 && opt->rows_per_cta < cap) cap = opt->rows_per_cta;
   const int chunks = ceil_div(rows, cap);
   const int per_cta = ceil_div(rows, chunks);
   bool ok;
@@ -139,6 +140,35 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
   pl->smem_bytes = info->smem;
   return true;
 }
+
+// Split-K workspace: float32 partial outputs, their log-sum-exps and, when
+// the last CTA of a sequence merges (at most kMaxFusedSplits splits), one
+// 64-bit arrival counter per (sequence, KV head, row chunk).  Regions are
+// 256-byte aligned.
+struct WorkspaceLayout {
+  size_t lse_off, ctr_off, total;
+  bool fused_merge;
+};
+WorkspaceLayout workspace_layout(const Shape &s, int num_splits, int row_chunks, int rows_per_cta,
+                                 int merge) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = static_cast<size_t>(s.batch) * s.num_queries * s.num_heads;
+  WorkspaceLayout w{};
+  w.lse_off = up(rows * num_splits * s.head_dim * sizeof(float));
+  w.ctr_off = w.lse_off + up(rows * num_splits * sizeof(float));
+  // The completing CTA reads back rows x splits partial vectors in its tail:
+  // worth it for a few (GQA, long contexts: 0.949 vs 0.936 of the HBM peak),
+  // not for the 20 x 10 of speculative verification (0.567 vs 0.603).
+  const bool small = static_cast<int64_t>(rows_per_cta) * num_splits <= 64;
+  w.fused_merge = num_splits <= kMaxFusedSplits && (merge == 1 || (merge == 0 && small));
+  w.total = w.ctr_off;
+  if (w.fused_merge)
+    w.total += up(static_cast<size_t>(s.batch) * s.num_kv_heads * row_chunks *
+                  sizeof(unsigned long long));
+  return w;
+}
+
+std::atomic<uint32_t> g_epoch{1};
 
 // Split-K partition.  A sequence of n blocks is cut into chunks of
 // split_blocks blocks; each chunk is one CTA.  Splitting pays when the
@@ -179,10 +209,9 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
   pl->ctas_per_sm = ctas_per_sm;
   pl->workspace_bytes = 0;
   if (num_splits > 1) {
-    const size_t rows = static_cast<size_t>(s.batch) * s.num_queries * s.num_heads;
-    const size_t o_bytes = rows * num_splits * s.head_dim * sizeof(float);
-    const size_t lse_bytes = rows * num_splits * sizeof(float);
-    pl->workspace_bytes = ((o_bytes + 255) / 256) * 256 + ((lse_bytes + 255) / 256) * 256;
+    const WorkspaceLayout w =
+        workspace_layout(s, num_splits, pl->row_chunks, pl->rows_per_cta, opt ? opt->merge : 0);
+    pl->workspace_bytes = w.total;
   }
 }
 
@@ -190,7 +219,9 @@ pkv_status make_plan(const Shape &s, const pkv_options *opt, int num_sms, int ct
                      pkv_plan *pl, KernelInfo *info) {
   pkv_status st = check_shape(s);
   if (st != PKV_OK) return st;
-  if (opt && (opt->split_blocks < 0 || opt->stages < 0)) return PKV_ERR_INVALID_ARG;
+  if (opt && (opt->split_blocks < 0 || opt->stages < 0 || opt->rows_per_cta < 0 ||
+              opt->merge < 0 || opt->merge > 2))
+    return PKV_ERR_INVALID_ARG;
   if (!choose_kernel(s, opt, pl, info)) return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(s.num_kv_heads) * pl->row_chunks > 65535) return PKV_ERR_UNSUPPORTED;
   if (ctas_per_sm <= 0) {
@@ -314,12 +345,21 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   p.split_blocks = pl.split_blocks;
   p.num_splits = pl.num_splits;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  bool merge_kernel = false;
   if (pl.num_splits > 1) {
-    const size_t rows = static_cast<size_t>(s.batch) * s.num_queries * s.num_heads;
-    const size_t o_bytes = rows * pl.num_splits * s.head_dim * sizeof(float);
-    p.part_o = static_cast<float *>(workspace);
-    p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                           ((o_bytes + 255) / 256) * 256);
+    const WorkspaceLayout w = workspace_layout(s, pl.num_splits, pl.row_chunks, pl.rows_per_cta,
+                                               opt ? opt->merge : 0);
+    char *base = static_cast<char *>(workspace);
+    p.part_o = reinterpret_cast<float *>(base);
+    p.part_lse = reinterpret_cast<float *>(base + w.lse_off);
+    if (w.fused_merge) {
+      p.counters = reinterpret_cast<unsigned long long *>(base + w.ctr_off);
+      uint32_t e = g_epoch.fetch_add(1, std::memory_order_relaxed);
+      if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed);  // 0 never tags a call
+      p.epoch = e;
+    } else {
+      merge_kernel = true;
+    }
   }
 
   const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
@@ -337,7 +377,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
     e = simt_launch(s.dtype, s.head_dim, r, p, grid, stream);
   }
   if (e != cudaSuccess) return PKV_ERR_CUDA;
-  if (pl.num_splits > 1) {
+  if (merge_kernel) {
     e = merge_launch(s.dtype, s.head_dim, p, sms, stream);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }

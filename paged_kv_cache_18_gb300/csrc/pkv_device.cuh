@@ -33,6 +33,9 @@ struct AttnParams {
   const void *v_new;            //   (nullptr: the cache already holds them)
   float *part_o;                // [B*Q*Hq, num_splits, D]   (split-K only)
   float *part_lse;              // [B*Q*Hq, num_splits]      (log2 units)
+  unsigned long long *counters; // [B, Hkv, row_chunks] arrivals (epoch << 32 | count);
+                                //   nullptr: a separate merge kernel runs after
+  uint32_t epoch;               // tag of this call in the counters
   int32_t *err;                 // optional device error word
   int64_t num_blocks;
   int batch, num_queries, num_heads, num_kv_heads, group;
@@ -283,18 +286,46 @@ __device__ __forceinline__ void patch_new_rows(const AttnParams &p, uint32_t kti
   __syncwarp();
 }
 
+// Largest split count whose merge the last-arriving CTA does itself.
+constexpr int kMaxFusedSplits = 32;
+
+// Split-K arrival: count this CTA in its (sequence, KV head, row chunk)
+// counter; true for the CTA that completes the count.  The counter word
+// holds (epoch << 32 | arrivals); a word left with another call's epoch
+// (or garbage) restarts at 1, and the completing CTA resets the count to 0
+// for the next call with the same epoch (a replayed CUDA graph).
+__device__ __forceinline__ bool split_arrive(const AttnParams &p, int b, int kvh, int chunk,
+                                             int ns_b) {
+  unsigned long long *ctr =
+      p.counters + (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * p.row_chunks + chunk;
+  const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+  unsigned long long cur = atomicAdd(ctr, 0ull);
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned long long next = ((cur >> 32) == p.epoch) ? cur + 1 : (tag | 1ull);
+    const unsigned long long prev = atomicCAS(ctr, cur, next);
+    if (prev == cur) return static_cast<int>(next & 0xffffffffull) == ns_b;
+    cur = prev;
+  }
+  record_error(p.err, PKV_DEVERR_TIMEOUT);
+  return false;
+}
+
 // CTA epilogue.  Every warp w has left, for each of the NC query columns of
 // this CTA, its running max m (log2 units), its sum l and its unnormalised
 // output o[0..D) in shared memory:
 //   red_m[w * NC + col], red_l[w * NC + col], red_o[(w * NC + col) * DP + d].
 // The states are merged exactly as the online softmax merges two chunks
-// (rescale each by 2^(m_w - M)), then the CTA writes either the normalised
-// output (no split) or the split's normalised output and its log-sum-exp.
+// (rescale each by 2^(m_w - M)).  Then the CTA writes
+//   - the normalised output, when the launch or this sequence has one split;
+//   - otherwise this split's normalised output and its log-sum-exp, and, with
+//     counters, the CTA that completes the sequence's splits merges them
+//     (the Flash-Decoding reduction: weights 2^(lse_s - max lse)).
 template <typename T, int D, int NC, int W>
 __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, float *red_l,
                                              float *red_o, float *wscale, int b, int kvh,
-                                             int chunk, int split) {
+                                             int chunk, int split, int ns_b) {
   constexpr int DP = D + 4;
+  constexpr int QV = D / 4;
   const int tid = threadIdx.x;
   // 1) per column: global max, per-warp scale factors and 1 / sum.
   if (tid < NC) {
@@ -313,8 +344,8 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
     wscale[(W + 1) * NC + tid] = lsum > 0.f ? M + __log2f(lsum) : -INFINITY;
   }
   __syncthreads();
+  const bool direct = p.num_splits == 1 || (ns_b == 1 && p.counters != nullptr);
   // 2) 4 consecutive d per thread-step.
-  constexpr int QV = D / 4;
   for (int idx = tid; idx < NC * QV; idx += W * 32) {
     const int col = idx / QV;
     const int d0 = (idx - col * QV) * 4;
@@ -331,7 +362,7 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
       acc[3] += s * o.w;
     }
     const float inv = wscale[W * NC + col];
-    if (p.num_splits == 1) {
+    if (direct) {
       T *dst = reinterpret_cast<T *>(p.out) + row * D + d0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) dst[e] = from_float<T>(acc[e] * inv);
@@ -341,6 +372,61 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
       if (d0 == 0) p.part_lse[row * p.num_splits + split] = wscale[(W + 1) * NC + col];
     }
   }
+  if (direct || p.counters == nullptr) return;
+
+  // 3) publish the partials, count the arrival.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = split_arrive(p, b, kvh, chunk, ns_b) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // 4) the last CTA merges the ns_b splits of its rows.  Shared memory
+  // (free now): weights[NC][kMaxFusedSplits], then 1 / sum per column.
+  float *wts = red_o;
+  float *winv = red_o + NC * kMaxFusedSplits;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int col = warp; col < NC; col += W) {
+    const int64_t row = cta_row_index(p, b, kvh, chunk, col);
+    if (row < 0) continue;
+    const float lse = lane < ns_b ? __ldcg(p.part_lse + row * p.num_splits + lane) : -INFINITY;
+    float M = lse;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    const float w = (M == -INFINITY) ? 0.f : ex2(lse - M);
+    float sum = w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    wts[col * kMaxFusedSplits + lane] = w;
+    if (lane == 0) winv[col] = sum > 0.f ? 1.f / sum : 0.f;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < NC * QV; idx += W * 32) {
+    const int col = idx / QV;
+    const int d0 = (idx - col * QV) * 4;
+    const int64_t row = cta_row_index(p, b, kvh, chunk, col);
+    if (row < 0) continue;
+    const float *po = p.part_o + row * p.num_splits * D + d0;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int sp = 0; sp < ns_b; ++sp) {
+      const float w = wts[col * kMaxFusedSplits + sp];
+      const float4 o = __ldcg(reinterpret_cast<const float4 *>(po + static_cast<int64_t>(sp) * D));
+      acc[0] += w * o.x;
+      acc[1] += w * o.y;
+      acc[2] += w * o.z;
+      acc[3] += w * o.w;
+    }
+    const float inv = winv[col];
+    T *dst = reinterpret_cast<T *>(p.out) + row * D + d0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dst[e] = from_float<T>(acc[e] * inv);
+  }
+  if (tid == 0)
+    atomicExch(p.counters + (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * p.row_chunks + chunk,
+               static_cast<unsigned long long>(p.epoch) << 32);
 }
 
 }  // namespace pkv

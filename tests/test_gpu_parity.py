@@ -188,10 +188,12 @@ def test_cuda_graph_replay():
     with torch.cuda.graph(g):
         d.append()
         d.attend(out=out[:, 0], workspace=ws)
-    out.zero_()
-    g.replay()
-    torch.cuda.synchronize()
-    assert_close(host_f64(out, "bf16"), oracle_after_append(b), "bf16", "graph")
+    ref = oracle_after_append(b)
+    for _ in range(3):  # replays reuse the captured call's merge counters
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(host_f64(out, "bf16"), ref, "bf16", "graph")
 
 
 # ---- the five named workloads at full size, in the bench's launch config --
@@ -284,3 +286,37 @@ def test_fused_matches_two_calls_bitwise():
         assert torch.equal(o1, o2)
         for a, c in ((d1.k_cache, d2.k_cache), (d1.v_cache, d2.v_cache)):
             assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_split_merge_ignores_stale_workspace():
+    """The split-K workspace may hold anything before a call (another call's
+    counters, garbage): results do not depend on it."""
+    import paged_kv_cache_18_gb300 as pkv
+    wl = W.Workload("stale", 6, 32, 8, 128, "bf16", len_range=(500, 4000), seed=13)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    ref = oracle_after_append(b)
+    for sb in (0, 16, 40):
+        need = pkv.workspace_size(6, 1, 32, 8, 128, b.max_context_len, torch.bfloat16,
+                                  split_blocks=sb)
+        assert need > 0
+        ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            out = d.attend(split_blocks=sb, workspace=ws)
+            torch.cuda.synchronize()
+            assert_close(host_f64(out, "bf16"), ref, "bf16", f"stale ws sb={sb}")
+
+
+@pytest.mark.parametrize("rows_per_cta,merge", [(0, 2), (16, 0), (8, 1), (3, 2)])
+def test_row_caps_and_merge_modes(rows_per_cta, merge):
+    from paged_kv_cache_18_gb300 import binding
+    wl = W.Workload("caps", 5, 32, 8, 128, "bf16", context_lens=[5, 40, 700, 1500, 2222],
+                    num_queries=5, seed=600 + rows_per_cta + merge)
+    binding.TUNING.update(rows_per_cta=rows_per_cta, merge=merge)
+    try:
+        for sb in (0, 8):
+            run_case(wl, kernel=2, split_blocks=sb)
+        run_case(wl, kernel=1, split_blocks=8)
+    finally:
+        binding.TUNING.clear()
