@@ -409,7 +409,7 @@ def run_ours(args):
     achieved = algo["total"] / (attn_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
     traffic = recorded_traffic(args.workload)
-    launches_per_step = (1 if fused else 2) + (1 if plan["num_splits"] > 1 else 0)
+    launches_per_step = (1 if fused else 2) + plan["merge_kernel"]
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -429,13 +429,14 @@ def run_ours(args):
         "attention_ms": attn_ms,
         "plan": {k: plan[k] for k in ("kernel", "rows_per_cta", "row_chunks", "split_blocks",
                                       "num_splits", "grid_x", "grid_y", "grid_z",
-                                      "stages", "ctas_per_sm")},
+                                      "stages", "ctas_per_sm", "merge_kernel")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": algo["total"],
                      "kernel": ("fused append + attention" if fused else "attention")
-                               + (" + split-K merge" if plan["num_splits"] > 1 else "")},
+                               + (" + split-K merge" if plan["num_splits"] > 1 else ""),
+                     "launches_per_step": launches_per_step},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

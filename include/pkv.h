@@ -126,6 +126,8 @@ typedef struct pkv_plan {
   int ctas_per_sm;        /* occupancy the planner assumed */
   size_t smem_bytes;      /* dynamic shared memory per CTA */
   size_t workspace_bytes; /* device workspace the call needs (0 = none) */
+  int merge_kernel;       /* 1: a separate split-K merge launch follows;
+                             0: no split, or the last CTA of each sequence merges */
 } pkv_plan;
 
 /* Human-readable name of a status code (static string). */

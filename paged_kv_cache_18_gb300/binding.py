@@ -59,7 +59,8 @@ class Plan(ctypes.Structure):
                 ("grid_y", ctypes.c_int), ("grid_z", ctypes.c_int),
                 ("threads_per_cta", ctypes.c_int), ("stages", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int),
-                ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t)]
+                ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
+                ("merge_kernel", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

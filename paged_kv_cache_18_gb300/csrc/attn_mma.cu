@@ -55,21 +55,38 @@ __device__ __forceinline__ uint32_t swz(int row, int d) {
   return part * MmaGeom<D>::kPanelBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <typename T, int D, int NT, int W, int NS>
-__global__ void __launch_bounds__(W * 32)
+// Named barrier over the `count` warps of one block lane (id 1 + lane).
+__device__ __forceinline__ void lane_sync(int id, int count) {
+  if (count == 1) {
+    __syncwarp();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count * 32) : "memory");
+  }
+}
+
+// BL block lanes x CG column groups = BL * CG warps.  Block lane bl owns the
+// blocks bl, bl + BL, ... of the split and a ring of NS stages; the CG warps
+// of a lane share each staged block, warp cg computing query columns
+// 8 cg .. 8 cg + 7.  The lane's first warp issues the copies.
+template <typename T, int D, int CG, int BL, int NS>
+__global__ void __launch_bounds__(BL * CG * 32)
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   using G = MmaGeom<D>;
-  constexpr int NC = NT * 8;  // query columns of this CTA (padded)
+  constexpr int NC = CG * 8;  // query columns of this CTA (padded)
   constexpr int KS = G::kSteps;
+  constexpr int NW = BL * CG;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t smem_base = smem_u32(smem);
-  const uint32_t bar_base = smem_base + W * NS * G::kStageBytes;
+  __shared__ uint64_t bars[BL * NS];  // the stage's copies landed
+  __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bl = warp / CG, cg = warp - (warp / CG) * CG;
+  const bool leader = cg == 0;
   const int g = lane >> 2, c = lane & 3;
   const int split = blockIdx.x;
   const int kvh = blockIdx.y / p.row_chunks;
@@ -84,62 +101,57 @@ __global__ void __launch_bounds__(W * 32)
   const int blk_end = min(blk_begin + p.split_blocks, ext.nblk);
   const int ns_b = max(1, min(p.num_splits, (ext.nblk + p.split_blocks - 1) / p.split_blocks));
   const int nspan = max(blk_end - blk_begin, 0);
-  const int n_my = nspan > warp ? (nspan - warp + W - 1) / W : 0;
+  const int n_my = nspan > bl ? (nspan - bl + BL - 1) / BL : 0;
+  const int col0 = cg * 8;
 
-  // Q^T operand fragments (B operand: k = head dim, n = query column).
-  uint32_t qf[KS][NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int64_t row = cta_row_index(p, b, kvh, chunk, nt * 8 + g);
+  // Q^T operand fragments of this warp's 8 columns (B operand: k = head dim).
+  uint32_t qf[KS][2];
+  {
+    const int64_t row = cta_row_index(p, b, kvh, chunk, col0 + g);
     const T *qrow = reinterpret_cast<const T *>(p.q) + (row < 0 ? 0 : row) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qf[ks][nt][0] = row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
-      qf[ks][nt][1] = row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * c);
+      qf[ks][0] = row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
+      qf[ks][1] = row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * c);
     }
   }
-  // Visible-row limit of the two columns this thread holds per n-tile.
-  int lim[NT][2];
+  // Visible-row limit of the two columns this thread holds.
+  int lim[2];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) lim[nt][e] = cta_row_limit(p, L, chunk, nt * 8 + 2 * c + e);
+  for (int e = 0; e < 2; ++e) lim[e] = cta_row_limit(p, L, chunk, col0 + 2 * c + e);
   const int mask_from = L - p.num_queries + 1;  // first row some column cannot see
 
   // Online-softmax state.
-  float o[KS][NT][4];
-  float m[NT][2], l[NT][2];
+  float o[KS][4];
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m[nt][0] = m[nt][1] = -INFINITY;
-    l[nt][0] = l[nt][1] = 0.f;
+  for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-  }
+    for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
 
-  // Per-warp pipeline.
-  const uint32_t my_bars = bar_base + warp * NS * 8;
-  const uint32_t my_stages = smem_base + warp * NS * G::kStageBytes;
-  if (lane == 0) {
+  // The lane's ring.
+  const uint32_t my_bars = smem_u32(&bars[bl * NS]);
+  const uint32_t my_stages = smem_base + bl * NS * G::kStageBytes;
+  if (threadIdx.x == 0) s_abort = 0;
+  if (leader && lane == 0) {
 #pragma unroll
     for (int s = 0; s < NS; ++s) mbar_init(my_bars + 8 * s, 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
 
   const int32_t *table = p.block_table + static_cast<int64_t>(b) * p.max_blocks_per_seq +
-                         blk_begin + warp;
+                         blk_begin + bl;
   auto load_entries = [&](int chunk32) -> int {
     const int i = chunk32 * 32 + lane;
-    return i < n_my ? __ldg(table + static_cast<int64_t>(i) * W) : -1;
+    return i < n_my ? __ldg(table + static_cast<int64_t>(i) * BL) : -1;
   };
   int tab_cur = load_entries(0);
   int tab_next = load_entries(1);
   uint32_t bad_mask = 0;
 
-  // Issue the copies of my i-th block into stage i % NS (all lanes call).
+  // Track block i's table entry (every warp of the lane), and have the
+  // lane's leader issue its copies into stage i % NS.
   auto issue = [&](int i) {
     if ((i & 31) == 0 && i > 0) {
       tab_cur = tab_next;
@@ -148,7 +160,7 @@ __global__ void __launch_bounds__(W * 32)
     const int v = __shfl_sync(kFull, tab_cur, i & 31);
     const bool bad = v < 0 || static_cast<int64_t>(v) >= p.num_blocks;
     bad_mask = bad ? (bad_mask | (1u << (i & 31))) : (bad_mask & ~(1u << (i & 31)));
-    if (lane == 0) {
+    if (leader && lane == 0) {
       if (bad) record_error(p.err, PKV_DEVERR_BLOCK_ID);
       const int phys = bad ? 0 : v;
       const int s = i % NS;
@@ -169,261 +181,269 @@ __global__ void __launch_bounds__(W * 32)
   for (int i = 0; i < npre; ++i) issue(i);
   int issued = npre;
 
-  bool timed_out = false;
-  int issued_done = 0;  // blocks whose copies are known to have landed
+  int consumed = 0;
+  bool aborted = false;
   for (int i = 0; i < n_my; ++i) {
     const int s = i % NS;
-    if (!mbar_wait_bounded(my_bars + 8 * s, (i / NS) & 1)) {
-      timed_out = true;
-      issued_done = i;
-      break;
+    // A copy that never lands aborts the CTA (with column groups, through a
+    // shared flag): from then on no warp waits or computes, but every warp
+    // still takes part in each lane_sync.
+    if (!aborted && !mbar_wait_bounded(my_bars + 8 * s, (i / NS) & 1)) {
+      aborted = true;
+      if (CG > 1) s_abort = 1;
+      if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT);
     }
+    if (CG > 1 && !aborted) aborted = s_abort != 0;
+    const bool live = !aborted;
+    if (live) consumed = i + 1;
     const uint32_t ktile = my_stages + s * G::kStageBytes;
     const uint32_t vtile = ktile + G::kTileBytes;
-    const int key0 = (blk_begin + warp + i * W) * kBlockSize;
+    const int key0 = (blk_begin + bl + i * BL) * kBlockSize;
     const bool bad = (bad_mask >> (i & 31)) & 1u;
     if (p.k_new != nullptr && !bad && key0 + kBlockSize > L - p.num_queries) {
-      const int64_t phys = __ldg(table + static_cast<int64_t>(i) * W);
-      patch_new_rows<D, 2>(p, ktile, vtile, b, kvh, key0, L, phys, chunk == 0,
-                           [](int r, int vec) { return swz<D>(r, vec * 8); });
+      if (leader && live) {
+        const int64_t phys = __ldg(table + static_cast<int64_t>(i) * BL);
+        patch_new_rows<D, 2>(p, ktile, vtile, b, kvh, key0, L, phys, chunk == 0,
+                             [](int r, int vec) { return swz<D>(r, vec * 8); });
+      }
+      lane_sync(1 + bl, CG);
     }
 
-    // S^T = K Q^T, the head-dim steps split over two accumulator chains.
-    float sc[NT][4], sc2[NT][4];
+    if (live) {
+      // S^T = K Q^T, the head-dim steps spread over four accumulator chains.
+      constexpr int NCH = KS < 4 ? KS : 4;
+      float acc[NCH][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int ch = 0; ch < NCH; ++ch) acc[ch][0] = acc[ch][1] = acc[ch][2] = acc[ch][3] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sc[nt][e] = sc2[nt][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(a, ktile + swz<D>(lane & 15, ks * 16 + (lane >> 4) * 8));
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (ks & 1)
-          Mma<T>::run(sc2[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
-        else
-          Mma<T>::run(sc[nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, ktile + swz<D>(lane & 15, ks * 16 + (lane >> 4) * 8));
+        Mma<T>::run(acc[ks % NCH], a, qf[ks][0], qf[ks][1]);
       }
-    }
-    const bool need_mask = bad || key0 + kBlockSize > mask_from;
-    bool above = false;  // some score exceeds its column's reference by > the slack
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      float sc[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float v = (sc[nt][e] + sc2[nt][e]) * p.scale_log2;
+        float t = acc[0][e];
+#pragma unroll
+        for (int ch = 1; ch < NCH; ++ch) t += acc[ch][e];
+        sc[e] = t;
+      }
+      const bool need_mask = bad || key0 + kBlockSize > mask_from;
+      bool above = false;  // some score exceeds its column's reference by > the slack
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = sc[e] * p.scale_log2;
         if (need_mask) {
           const int key = key0 + g + ((e >> 1) << 3);
-          if (bad || key >= lim[nt][e & 1]) v = -INFINITY;
+          if (bad || key >= lim[e & 1]) v = -INFINITY;
         }
-        sc[nt][e] = v;
-        above |= v > m[nt][e & 1] + kRescaleSlack;
+        sc[e] = v;
+        above |= v > m[e & 1] + kRescaleSlack;
       }
-    // Online softmax.  The exponentials use a per-column reference m that is
-    // raised (to the exact running max, rescaling l and O by 2^(m_old - m))
-    // only when a score exceeds it by more than kRescaleSlack; otherwise the
-    // block's weights 2^(s - m) stay below 2^kRescaleSlack and no cross-lane
-    // max, correction or rescale is needed.  The result O / l does not depend
-    // on the reference.
-    if (__any_sync(kFull, above)) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      // Online softmax.  The exponentials use a per-column reference m that
+      // is raised (to the exact running max, rescaling l and O by
+      // 2^(m_old - m)) only when a score exceeds it by more than
+      // kRescaleSlack; otherwise the block's weights 2^(s - m) stay below
+      // 2^kRescaleSlack and no cross-lane max, correction or rescale is
+      // needed.  The result O / l does not depend on the reference.
+      if (__any_sync(kFull, above)) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float mx = fmaxf(sc[nt][e], sc[nt][e + 2]);
+          float mx = fmaxf(sc[e], sc[e + 2]);
           mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-          const float m_new = fmaxf(m[nt][e], mx);
-          const float corr = ex2(m[nt][e] - (m_new == -INFINITY ? 0.f : m_new));
-          l[nt][e] *= corr;
-          m[nt][e] = m_new;
+          const float m_new = fmaxf(m[e], mx);
+          const float corr = ex2(m[e] - (m_new == -INFINITY ? 0.f : m_new));
+          l[e] *= corr;
+          m[e] = m_new;
 #pragma unroll
           for (int mt = 0; mt < KS; ++mt) {
-            o[mt][nt][e] *= corr;
-            o[mt][nt][e + 2] *= corr;
+            o[mt][e] *= corr;
+            o[mt][e + 2] *= corr;
           }
         }
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float m_use = m[nt][e] == -INFINITY ? 0.f : m[nt][e];
-        const float p0 = ex2(sc[nt][e] - m_use);
-        const float p1 = ex2(sc[nt][e + 2] - m_use);
-        l[nt][e] += p0 + p1;
-        sc[nt][e] = p0;
-        sc[nt][e + 2] = p1;
+        const float m_use = m[e] == -INFINITY ? 0.f : m[e];
+        const float p0 = ex2(sc[e] - m_use);
+        const float p1 = ex2(sc[e + 2] - m_use);
+        l[e] += p0 + p1;
+        sc[e] = p0;
+        sc[e + 2] = p1;
       }
-    // P^T operand fragments: high part and rounding remainder.
-    uint32_t ph[NT][2], pl[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint32_t h01 = Mma<T>::pack(sc[nt][0], sc[nt][1]);
-      const uint32_t h23 = Mma<T>::pack(sc[nt][2], sc[nt][3]);
+      // P^T operand fragments: high part and rounding remainder.
+      const uint32_t h01 = Mma<T>::pack(sc[0], sc[1]);
+      const uint32_t h23 = Mma<T>::pack(sc[2], sc[3]);
       float r0, r1, r2, r3;
       Mma<T>::unpack(h01, r0, r1);
       Mma<T>::unpack(h23, r2, r3);
-      const uint32_t l01 = Mma<T>::pack(sc[nt][0] - r0, sc[nt][1] - r1);
-      const uint32_t l23 = Mma<T>::pack(sc[nt][2] - r2, sc[nt][3] - r3);
-      ph[nt][0] = movm_t(h01);
-      ph[nt][1] = movm_t(h23);
-      pl[nt][0] = movm_t(l01);
-      pl[nt][1] = movm_t(l23);
-    }
-    // O^T += V^T P^T.  In a block that ends past the context, zero the V^T
-    // columns (keys) past it so that NaN-filled rows never enter an MMA.
-    const int nvalid = bad ? 0 : L - key0;
-    auto pv = [&](auto partial) {
-      uint32_t km0 = 0xffffffffu, km8 = 0xffffffffu;
-      if (decltype(partial)::value) {
-        km0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
-        km8 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
-      }
-#pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        uint32_t a[4];
-        ldsm_x4_t(a, vtile + swz<D>((lane & 7) + ((lane >> 4) << 3),
-                                    mt * 16 + ((lane >> 3) & 1) * 8));
+      const uint32_t ph0 = movm_t(h01), ph1 = movm_t(h23);
+      const uint32_t pl0 = movm_t(Mma<T>::pack(sc[0] - r0, sc[1] - r1));
+      const uint32_t pl1 = movm_t(Mma<T>::pack(sc[2] - r2, sc[3] - r3));
+      // O^T += V^T P^T.  In a block that ends past the context, zero the V^T
+      // columns (keys) past it so that NaN-filled rows never enter an MMA.
+      const int nvalid = bad ? 0 : L - key0;
+      auto pv = [&](auto partial) {
+        uint32_t km0 = 0xffffffffu, km8 = 0xffffffffu;
         if (decltype(partial)::value) {
-          a[0] &= km0;
-          a[1] &= km0;
-          a[2] &= km8;
-          a[3] &= km8;
+          km0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
+          km8 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
         }
+        // Four head-dim tiles at a time: their high-part MMAs first, then the
+        // low parts, so that no MMA waits on the one just issued.
+        constexpr int GRP = KS < 4 ? KS : 4;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          Mma<T>::run(o[mt][nt], a, ph[nt][0], ph[nt][1]);
-          Mma<T>::run(o[mt][nt], a, pl[nt][0], pl[nt][1]);
+        for (int m0 = 0; m0 < KS; m0 += GRP) {
+          uint32_t a[GRP][4];
+#pragma unroll
+          for (int u = 0; u < GRP; ++u) {
+            ldsm_x4_t(a[u], vtile + swz<D>((lane & 7) + ((lane >> 4) << 3),
+                                           (m0 + u) * 16 + ((lane >> 3) & 1) * 8));
+            if (decltype(partial)::value) {
+              a[u][0] &= km0;
+              a[u][1] &= km0;
+              a[u][2] &= km8;
+              a[u][3] &= km8;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < GRP; ++u) Mma<T>::run(o[m0 + u], a[u], ph0, ph1);
+#pragma unroll
+          for (int u = 0; u < GRP; ++u) Mma<T>::run(o[m0 + u], a[u], pl0, pl1);
         }
-      }
-    };
-    if (nvalid < kBlockSize)
-      pv(std::true_type{});
-    else
-      pv(std::false_type{});
-    __syncwarp();
+      };
+      if (nvalid < kBlockSize)
+        pv(std::true_type{});
+      else
+        pv(std::false_type{});
+    }
+    lane_sync(1 + bl, CG);  // every warp of the lane is done with stage s
     if (i + NS < n_my) {
-      issue(i + NS);
+      if (!aborted) issue(i + NS);
       ++issued;
     }
-    if (i + 1 == n_my) issued_done = i + 1;
   }
-  if (timed_out) {
-    if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT);
+  if (aborted && leader && lane == 0) {
     // Give the copies still in flight a bounded chance to land before the
     // shared memory is reused.
-    for (int k = issued_done; k < issued; ++k) mbar_wait_bounded(my_bars + 8 * (k % NS), (k / NS) & 1);
+    for (int k = consumed; k < issued; ++k)
+      mbar_wait_bounded(my_bars + 8 * (k % NS), (k / NS) & 1);
   }
 
   // Row sums: reduce the per-thread partial sums over the 8 lanes of a column.
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float v = l[nt][e];
-      v += __shfl_xor_sync(kFull, v, 4);
-      v += __shfl_xor_sync(kFull, v, 8);
-      v += __shfl_xor_sync(kFull, v, 16);
-      l[nt][e] = v;
-    }
+  for (int e = 0; e < 2; ++e) {
+    float v = l[e];
+    v += __shfl_xor_sync(kFull, v, 4);
+    v += __shfl_xor_sync(kFull, v, 8);
+    v += __shfl_xor_sync(kFull, v, 16);
+    l[e] = v;
+  }
 
-  // Hand the per-warp states to the CTA epilogue (reusing the stage memory).
+  // Hand the per-warp states to the CTA epilogue (reusing the stage memory):
+  // one state per (block lane, column).
   __syncthreads();
   constexpr int DP = D + 4;
   float *red_o = reinterpret_cast<float *>(smem);
-  float *red_m = red_o + W * NC * DP;
-  float *red_l = red_m + W * NC;
-  float *wscale = red_l + W * NC;
+  float *red_m = red_o + BL * NC * DP;
+  float *red_l = red_m + BL * NC;
+  float *wscale = red_l + BL * NC;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = nt * 8 + 2 * c + (e & 1);
-        const int d = mt * 16 + g + ((e >> 1) << 3);
-        red_o[(warp * NC + col) * DP + d] = o[mt][nt][e];
-      }
+    for (int e = 0; e < 4; ++e) {
+      const int col = col0 + 2 * c + (e & 1);
+      const int d = mt * 16 + g + ((e >> 1) << 3);
+      red_o[(bl * NC + col) * DP + d] = o[mt][e];
+    }
   if (g == 0) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        red_m[warp * NC + nt * 8 + 2 * c + e] = m[nt][e];
-        red_l[warp * NC + nt * 8 + 2 * c + e] = l[nt][e];
-      }
+    for (int e = 0; e < 2; ++e) {
+      red_m[bl * NC + col0 + 2 * c + e] = m[e];
+      red_l[bl * NC + col0 + 2 * c + e] = l[e];
+    }
   }
   __syncthreads();
-  cta_epilogue<T, D, NC, W>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split, ns_b);
+  cta_epilogue<T, D, NC, BL, NW * 32>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split,
+                                      ns_b);
 }
 
-constexpr int kMmaWarps = 4;
+// Block lanes for CG column groups: about four warps per CTA.
+template <int CG> constexpr int mma_lanes() { return CG >= 3 ? 1 : 4 / CG; }
 
-// Stages per warp: the default (deep) ring and one stage less, which frees
-// shared memory for one more resident CTA per SM.
-template <int D, bool DEEP> constexpr int mma_stages() {
-  return (D >= 256 ? 2 : 3) - (DEEP ? 0 : 1);
+// Stages per block lane, shallow and deep.  Fewer lanes per CTA take deeper
+// rings so that every CTA keeps about the same bytes in flight: 2 / 3 stages
+// for four lanes (single column group), 3 / 4 for two, 4 / 6 for one (1 / 2
+// at head_dim 256).
+template <int D, int CG, bool DEEP> constexpr int mma_stages() {
+  return D >= 256 ? (DEEP ? 2 : 1)
+                  : (CG >= 3 ? (DEEP ? 6 : 4) : (CG == 2 ? (DEEP ? 4 : 3) : (DEEP ? 3 : 2)));
 }
 
-template <typename T, int D, int NT, bool DEEP>
+template <typename T, int D, int CG, bool DEEP>
 constexpr size_t mma_smem_bytes() {
-  constexpr int NS = mma_stages<D, DEEP>();
-  constexpr size_t stages = size_t(kMmaWarps) * NS * MmaGeom<D>::kStageBytes;
-  constexpr size_t red = (size_t(kMmaWarps) * NT * 8 * (D + 4) + size_t(kMmaWarps + 2) * NT * 8 * 2 +
-                          size_t(kMmaWarps) * NT * 8) * 4;
-  constexpr size_t scratch = red > stages ? red : stages;
-  return scratch + size_t(kMmaWarps) * NS * 8 + 1024;
+  constexpr int BL = mma_lanes<CG>();
+  constexpr int NS = mma_stages<D, CG, DEEP>();
+  constexpr int NC = CG * 8;
+  constexpr size_t stages = size_t(BL) * NS * MmaGeom<D>::kStageBytes;
+  constexpr size_t red = (size_t(BL) * NC * (D + 4) + size_t(3 * BL + 2) * NC) * 4;
+  constexpr size_t merge = (size_t(NC) * kMaxFusedSplits + NC) * 4;
+  constexpr size_t need = red > merge ? red : merge;
+  constexpr size_t scratch = need > stages ? need : stages;
+  return scratch + 1024;
 }
 
 using MmaLaunch = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const AttnParams &,
                                   dim3, cudaStream_t);
 
-template <typename T, int D, int NT, bool DEEP>
+template <typename T, int D, int CG, bool DEEP>
 KernelInfo mma_info_t() {
+  constexpr int BL = mma_lanes<CG>();
   KernelInfo k;
   k.func = reinterpret_cast<const void *>(
-      &attn_mma_kernel<T, D, NT, kMmaWarps, mma_stages<D, DEEP>()>);
-  k.threads = kMmaWarps * 32;
-  k.smem = mma_smem_bytes<T, D, NT, DEEP>();
-  k.warps = kMmaWarps;
-  k.stages = mma_stages<D, DEEP>();
+      &attn_mma_kernel<T, D, CG, BL, mma_stages<D, CG, DEEP>()>);
+  k.threads = BL * CG * 32;
+  k.smem = mma_smem_bytes<T, D, CG, DEEP>();
+  k.warps = BL * CG;
+  k.stages = mma_stages<D, CG, DEEP>();
   return k;
 }
 
-template <typename T, int D, int NT, bool DEEP>
+template <typename T, int D, int CG, bool DEEP>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
-  const KernelInfo k = mma_info_t<T, D, NT, DEEP>();
-  attn_mma_kernel<T, D, NT, kMmaWarps, mma_stages<D, DEEP>()>
+  const KernelInfo k = mma_info_t<T, D, CG, DEEP>();
+  attn_mma_kernel<T, D, CG, mma_lanes<CG>(), mma_stages<D, CG, DEEP>()>
       <<<grid, k.threads, k.smem, stream>>>(km, vm, p);
   return cudaGetLastError();
 }
 
-// Default ring: 2 stages per warp (3 CTAs per SM at head_dim <= 128; the
-// 8-row GQA tile measured 0.949 of the HBM peak against 0.932 with 3).
-template <typename T, int D, int NT>
+// Default ring: the shallow one (for one column group at head_dim <= 128,
+// 3 CTAs per SM; the 8-row GQA tile measured 0.949 of the HBM peak against
+// 0.932 with the deep ring).
+template <typename T, int D, int CG>
 bool mma_pick_stages(int stages, KernelInfo *info, MmaLaunch *launch) {
-  if (stages == 0) stages = 2;
-  if (stages == mma_stages<D, true>()) {
-    *info = mma_info_t<T, D, NT, true>();
-    *launch = &launch_t<T, D, NT, true>;
+  if (stages == 0) stages = mma_stages<D, CG, false>();
+  if (stages == mma_stages<D, CG, true>()) {
+    *info = mma_info_t<T, D, CG, true>();
+    *launch = &launch_t<T, D, CG, true>;
     return true;
   }
-  if (stages == mma_stages<D, false>()) {
-    *info = mma_info_t<T, D, NT, false>();
-    *launch = &launch_t<T, D, NT, false>;
+  if (stages == mma_stages<D, CG, false>()) {
+    *info = mma_info_t<T, D, CG, false>();
+    *launch = &launch_t<T, D, CG, false>;
     return true;
   }
   return false;
 }
 
-// Column tiles x head dim kept within the register budget (N-tiles * D <= 384).
+// Column groups x head dim within the budget (CG * D <= 384).
 template <typename T, int D>
-bool mma_pick(int nt, int stages, KernelInfo *info, MmaLaunch *launch) {
-  switch (nt) {
+bool mma_pick(int cg, int stages, KernelInfo *info, MmaLaunch *launch) {
+  switch (cg) {
     case 1: return mma_pick_stages<T, D, 1>(stages, info, launch);
     case 2: return D <= 128 && mma_pick_stages<T, D, (D <= 128 ? 2 : 1)>(stages, info, launch);
     case 3: return D <= 128 && mma_pick_stages<T, D, (D <= 128 ? 3 : 1)>(stages, info, launch);
@@ -433,19 +453,19 @@ bool mma_pick(int nt, int stages, KernelInfo *info, MmaLaunch *launch) {
 }
 
 template <typename T>
-bool mma_pick_d(int D, int nt, int stages, KernelInfo *info, MmaLaunch *launch) {
+bool mma_pick_d(int D, int cg, int stages, KernelInfo *info, MmaLaunch *launch) {
   switch (D) {
-    case 64: return mma_pick<T, 64>(nt, stages, info, launch);
-    case 128: return mma_pick<T, 128>(nt, stages, info, launch);
-    case 256: return mma_pick<T, 256>(nt, stages, info, launch);
+    case 64: return mma_pick<T, 64>(cg, stages, info, launch);
+    case 128: return mma_pick<T, 128>(cg, stages, info, launch);
+    case 256: return mma_pick<T, 256>(cg, stages, info, launch);
     default: return false;
   }
 }
 
-bool mma_pick_any(pkv_dtype dtype, int D, int nt, int stages, KernelInfo *info,
+bool mma_pick_any(pkv_dtype dtype, int D, int cg, int stages, KernelInfo *info,
                   MmaLaunch *launch) {
-  if (dtype == PKV_BF16) return mma_pick_d<__nv_bfloat16>(D, nt, stages, info, launch);
-  if (dtype == PKV_F16) return mma_pick_d<__half>(D, nt, stages, info, launch);
+  if (dtype == PKV_BF16) return mma_pick_d<__nv_bfloat16>(D, cg, stages, info, launch);
+  if (dtype == PKV_F16) return mma_pick_d<__half>(D, cg, stages, info, launch);
   return false;
 }
 

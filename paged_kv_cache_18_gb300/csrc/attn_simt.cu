@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
     }
   }
   __syncthreads();
-  cta_epilogue<T, D, NC, W>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split, ns_b);
+  cta_epilogue<T, D, NC, W, W * 32>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split, ns_b);
 }
 
 constexpr int kSimtWarps = 4;

@@ -208,10 +208,12 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
   pl->grid_z = s.batch;
   pl->ctas_per_sm = ctas_per_sm;
   pl->workspace_bytes = 0;
+  pl->merge_kernel = 0;
   if (num_splits > 1) {
     const WorkspaceLayout w =
         workspace_layout(s, num_splits, pl->row_chunks, pl->rows_per_cta, opt ? opt->merge : 0);
     pl->workspace_bytes = w.total;
+    pl->merge_kernel = w.fused_merge ? 0 : 1;
   }
 }
 

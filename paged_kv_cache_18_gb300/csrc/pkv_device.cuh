@@ -320,7 +320,7 @@ __device__ __forceinline__ bool split_arrive(const AttnParams &p, int b, int kvh
 //   - otherwise this split's normalised output and its log-sum-exp, and, with
 //     counters, the CTA that completes the sequence's splits merges them
 //     (the Flash-Decoding reduction: weights 2^(lse_s - max lse)).
-template <typename T, int D, int NC, int W>
+template <typename T, int D, int NC, int W, int NTHR>
 __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, float *red_l,
                                              float *red_o, float *wscale, int b, int kvh,
                                              int chunk, int split, int ns_b) {
@@ -346,7 +346,7 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
   __syncthreads();
   const bool direct = p.num_splits == 1 || (ns_b == 1 && p.counters != nullptr);
   // 2) 4 consecutive d per thread-step.
-  for (int idx = tid; idx < NC * QV; idx += W * 32) {
+  for (int idx = tid; idx < NC * QV; idx += NTHR) {
     const int col = idx / QV;
     const int d0 = (idx - col * QV) * 4;
     const int64_t row = cta_row_index(p, b, kvh, chunk, col);
@@ -388,7 +388,7 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
   float *wts = red_o;
   float *winv = red_o + NC * kMaxFusedSplits;
   const int warp = tid >> 5, lane = tid & 31;
-  for (int col = warp; col < NC; col += W) {
+  for (int col = warp; col < NC; col += NTHR / 32) {
     const int64_t row = cta_row_index(p, b, kvh, chunk, col);
     if (row < 0) continue;
     const float lse = lane < ns_b ? __ldcg(p.part_lse + row * p.num_splits + lane) : -INFINITY;
@@ -403,7 +403,7 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
     if (lane == 0) winv[col] = sum > 0.f ? 1.f / sum : 0.f;
   }
   __syncthreads();
-  for (int idx = tid; idx < NC * QV; idx += W * 32) {
+  for (int idx = tid; idx < NC * QV; idx += NTHR) {
     const int col = idx / QV;
     const int d0 = (idx - col * QV) * 4;
     const int64_t row = cta_row_index(p, b, kvh, chunk, col);

@@ -130,6 +130,7 @@ def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
         ctr = B * Hkv * p["row_chunks"] * 8 if fused else 0
         assert p["workspace_bytes"] == (-(-o // 256) * 256 + -(-lse // 256) * 256
                                         + -(-ctr // 256) * 256)
+        assert p["merge_kernel"] == (0 if fused else 1)
     assert p["smem_bytes"] <= 227 * 1024
 
 
