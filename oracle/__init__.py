@@ -83,6 +83,10 @@ class Oracle:
             vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64,
             ctypes.c_double, i32, vp, i64]
         lib.oracle_paged_attention.restype = i32
+        lib.oracle_tree_attention.argtypes = [
+            vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64,
+            ctypes.c_double, i32, vp, i64]
+        lib.oracle_tree_attention.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         self.lib = lib
@@ -147,6 +151,33 @@ class Oracle:
         return out
 
 
+    def tree_attention(self, q, k_cache, v_cache, block_table, context_lens,
+                       scale: float, dtype: str, tree_mask) -> np.ndarray:
+        """Float64 output [B, Q, Hq, D] of tree verification: node j of
+        sequence b sees the cached rows and the tree rows whose bits are set
+        in tree_mask [B, Q] (or [Q], shared by every sequence) uint64."""
+        q = np.ascontiguousarray(q)
+        _check_storage(q, dtype, "q")
+        _check_storage(k_cache, dtype, "k_cache")
+        _check_storage(v_cache, dtype, "v_cache")
+        B, Q, Hq, D = q.shape
+        NB, Hkv, bs, _ = k_cache.shape
+        mask = np.ascontiguousarray(tree_mask, dtype=np.uint64)
+        stride = 0 if mask.ndim == 1 else Q
+        if mask.shape not in ((Q,), (B, Q)):
+            raise ValueError("tree_mask must be [Q] or [B, Q]")
+        table = np.ascontiguousarray(block_table, dtype=np.int32)
+        lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.full((B, Q, Hq, D), np.nan, dtype=np.float64)
+        st = self.lib.oracle_tree_attention(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(table),
+            table.shape[1], _ptr(lens), B, Q, Hq, Hkv, D, bs, NB, float(scale),
+            DTYPE_CODES[dtype], _ptr(mask), stride)
+        if st != 0:
+            raise ValueError(f"oracle_tree_attention failed with code {st}")
+        return out
+
+
 def default() -> Oracle:
     """The oracle built from ``pkv_oracle.c`` (compiled on first use)."""
     global _default
@@ -166,3 +197,7 @@ def kv_append(*args, **kwargs) -> None:
 
 def paged_attention(*args, **kwargs) -> np.ndarray:
     return default().paged_attention(*args, **kwargs)
+
+
+def tree_attention(*args, **kwargs) -> np.ndarray:
+    return default().tree_attention(*args, **kwargs)

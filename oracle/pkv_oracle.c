@@ -43,6 +43,10 @@
  *    their maximum, then exp(s - max) weights.  It is NOT the online
  *    recurrence the GPU path uses.
  *
+ *  - oracle_tree_attention: the same attention for the Q nodes of a
+ *    candidate tree, each seeing the cached rows and its own ancestors
+ *    (tree attention of Medusa, "Inference part 2", section "Medusa").
+ *
  * Readings where the pages are silent (each also listed in the design
  * notes): L counts every row of the sequence including the new ones; a
  * query row that sees no row at all (L - Q + j < 0, e.g. L = 0) returns a
@@ -227,6 +231,97 @@ int oracle_paged_attention(double *out, const void *q, const void *k_cache,
       }
     }
     free(scores);
+  }
+  return status;
+}
+
+/*
+ * oracle_tree_attention: attention of Q tree nodes per sequence (Medusa-style
+ * tree verification, "Inference part 2", section "Medusa": every candidate
+ * of the tree is verified in one pass with a mask that lets each candidate
+ * attend only to its own ancestors).  The Q nodes of sequence b occupy the
+ * last Q rows L - Q .. L - 1; node j sees every cached row i < L - Q, and
+ * row L - Q + k exactly when bit k of tree_mask[b * mask_stride + j] is set.
+ * Q <= 64.  A node that sees no row gets zeros.  Same layouts as
+ * oracle_paged_attention; two-pass softmax over the visible rows.
+ */
+int oracle_tree_attention(double *out, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *block_table,
+                          int max_blocks, const int32_t *context_lens, int B,
+                          int Q, int Hq, int Hkv, int D, int bs, int64_t NB,
+                          double scale, int dtype, const uint64_t *tree_mask,
+                          int64_t mask_stride) {
+  if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens ||
+      !tree_mask || B < 0 || Q <= 0 || Q > 64 || Hq <= 0 || Hkv <= 0 ||
+      Hq % Hkv != 0 || D <= 0 || bs <= 0 || max_blocks < 0 || NB < 0 ||
+      dtype < 0 || dtype > 2)
+    return ORACLE_ERR_ARG;
+  int64_t max_len = 1;
+  for (int b = 0; b < B; ++b)
+    if (context_lens[b] > max_len) max_len = context_lens[b];
+  int status = ORACLE_OK;
+  const int64_t total = (int64_t)B * Q * Hq;
+#pragma omp parallel
+  {
+    double *scores = (double *)malloc(sizeof(double) * (size_t)max_len);
+    char *seen = (char *)malloc((size_t)max_len);
+    if (!scores || !seen) {
+#pragma omp atomic write
+      status = ORACLE_ERR_NOMEM;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t r = 0; r < total; ++r) {
+      if (!scores || !seen) continue;
+      const int h = (int)(r % Hq), j = (int)((r / Hq) % Q);
+      const int b = (int)(r / ((int64_t)Hq * Q));
+      const int L = context_lens[b];
+      const int g = h / (Hq / Hkv);
+      const int64_t base = (int64_t)L - Q; /* first tree row */
+      const uint64_t mask = tree_mask[(int64_t)b * mask_stride + j];
+      double *o = out + r * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      if (L <= 0) continue;
+      if ((L + bs - 1) / bs > max_blocks) {
+#pragma omp atomic write
+        status = ORACLE_ERR_BLOCK;
+        continue;
+      }
+      const int64_t q_base = (((int64_t)b * Q + j) * Hq + h) * D;
+      int any = 0, bad = 0;
+      double m = 0.0;
+      for (int64_t i = 0; i < L; ++i) {
+        /* row i is visible if cached, or if its tree node is marked */
+        seen[i] = (i < base) || ((mask >> (i - base)) & 1u);
+        if (!seen[i]) continue;
+        int32_t phys = block_table[(int64_t)b * max_blocks + i / bs];
+        if (phys < 0 || phys >= NB) { bad = 1; break; }
+        int64_t k_base = (((int64_t)phys * Hkv + g) * bs + i % bs) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+          dot += widen(q, q_base + d, dtype) * widen(k_cache, k_base + d, dtype);
+        scores[i] = scale * dot;
+        if (!any || scores[i] > m) m = scores[i];
+        any = 1;
+      }
+      if (bad) {
+#pragma omp atomic write
+        status = ORACLE_ERR_BLOCK;
+        continue;
+      }
+      if (!any) continue;
+      double denom = 0.0;
+      for (int64_t i = 0; i < L; ++i) {
+        if (!seen[i]) continue;
+        double w = exp(scores[i] - m);
+        int32_t phys = block_table[(int64_t)b * max_blocks + i / bs];
+        int64_t v_base = (((int64_t)phys * Hkv + g) * bs + i % bs) * D;
+        denom += w;
+        for (int d = 0; d < D; ++d) o[d] += w * widen(v_cache, v_base + d, dtype);
+      }
+      for (int d = 0; d < D; ++d) o[d] /= denom;
+    }
+    free(scores);
+    free(seen);
   }
   return status;
 }

@@ -76,3 +76,41 @@ def contiguous_attention(q: np.ndarray, k_cache: np.ndarray,
             w /= w.sum(axis=-1, keepdims=True)
             out[b, j] = np.einsum("hi,ihd->hd", w, v)
     return out
+
+
+def tree_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                   block_table: np.ndarray, context_lens: np.ndarray, scale: float,
+                   dtype: str, tree_mask: np.ndarray) -> np.ndarray:
+    """Dense twin of tree verification: the boolean visibility matrix of the
+    Q tree nodes over the L rows is built from the bitmasks (every cached row
+    visible; tree row k visible to node j iff bit k of mask[j] is set) and
+    applied to dense scores, as in contiguous_attention."""
+    B, Q, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    group = Hq // Hkv
+    masks = np.broadcast_to(np.asarray(tree_mask, dtype=np.uint64), (B, Q))
+    out = np.zeros((B, Q, Hq, D), dtype=np.float64)
+    for b in range(B):
+        L = int(context_lens[b])
+        if L <= 0:
+            continue
+        k = np.repeat(widen(gather_sequence(k_cache, block_table[b], L), dtype), group, axis=1)
+        v = np.repeat(widen(gather_sequence(v_cache, block_table[b], L), dtype), group, axis=1)
+        qb = widen(q[b], dtype)
+        scores = np.einsum("jhd,ihd->hji", qb, k) * scale
+        vis = np.zeros((Q, L), dtype=bool)
+        base = L - Q
+        vis[:, :max(base, 0)] = True
+        for j in range(Q):
+            for kk in range(Q):
+                if base + kk >= 0 and (int(masks[b, j]) >> kk) & 1:
+                    vis[j, base + kk] = True
+        scores = np.where(vis[None], scores, -np.inf)
+        for j in range(Q):
+            if not vis[j].any():
+                continue
+            s = scores[:, j, :]
+            w = np.exp(s - s.max(axis=-1, keepdims=True))
+            w /= w.sum(axis=-1, keepdims=True)
+            out[b, j] = np.einsum("hi,ihd->hd", w, v)
+    return out

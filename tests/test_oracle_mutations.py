@@ -99,3 +99,56 @@ def test_mutation_is_caught(name, tmp_path):
     lib = oracle.compile_library(str(mutated), str(tmp_path / "libmutant.so"))
     failed = _battery(oracle.Oracle(lib))
     assert failed, f"planted mistake {name!r} passed every pin"
+
+
+# ---- tree verification --------------------------------------------------
+TREE_MUTATIONS = {
+    "tree bit off by one": ("((mask >> (i - base)) & 1u)", "((mask >> (i - base + 1)) & 1u)"),
+    "tree drops a cached row": ("seen[i] = (i < base) ||", "seen[i] = (i + 1 < base) ||"),
+    "tree ignores mask": ("seen[i] = (i < base) || ((mask >> (i - base)) & 1u);",
+                          "seen[i] = 1;"),
+}
+
+
+def _tree_battery(orc) -> list:
+    from tests.toy_decoder import ancestor_masks
+    failed = []
+    rng = np.random.default_rng(9)
+    wl = W.Workload("tree m", 3, 8, 2, 64, "f32", context_lens=[9, 40, 77], num_queries=6,
+                    seed=120)
+    b = W.make_batch(wl)
+    orc.kv_append(b.k_cache, b.v_cache, b.k_new, b.v_new, b.slot_mapping, "f32")
+    chain = np.array([(2 << j) - 1 for j in range(6)], dtype=np.uint64)
+    causal = orc.paged_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                 wl.softmax_scale, "f32")
+    try:
+        got = orc.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                 wl.softmax_scale, "f32", chain)
+        if not np.array_equal(got, causal):
+            failed.append("chain == causal")
+        parents = [-1] + [int(rng.integers(0, j)) for j in range(1, 6)]
+        masks = ancestor_masks(parents)
+        got = orc.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                 wl.softmax_scale, "f32", masks)
+        want = twin.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                   wl.softmax_scale, "f32", masks)
+        if not np.allclose(got, want, rtol=0, atol=1e-12):
+            failed.append("twin")
+    except ValueError:
+        failed.append("error")
+    return failed
+
+
+def test_unmutated_tree_oracle_passes_battery():
+    assert _tree_battery(oracle.default()) == []
+
+
+@pytest.mark.parametrize("name", sorted(TREE_MUTATIONS))
+def test_tree_mutation_is_caught(name, tmp_path):
+    old, new = TREE_MUTATIONS[name]
+    src = open(oracle.SOURCE).read()
+    assert old in src, f"mutation anchor for {name!r} not found"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.compile_library(str(mutated), str(tmp_path / "libmutant.so"))
+    assert _tree_battery(oracle.Oracle(lib)), f"planted mistake {name!r} passed every pin"

@@ -318,3 +318,94 @@ def test_greedy_speculative_equals_greedy():
     got, passes, acc = speculative(ToyDecoder(seed=3), prompt, n, propose, 4)
     assert got == ref
     assert passes < n and acc > 0  # drafts were actually accepted
+
+
+# ---- tree verification (Medusa tree attention, "Inference part 2") -------
+def random_tree(Q, rng):
+    parents = [-1] + [int(rng.integers(0, j)) for j in range(1, Q)]
+    from tests.toy_decoder import ancestor_masks
+    return parents, ancestor_masks(parents)
+
+
+def test_tree_chain_mask_is_causal_verify():
+    wl = W.Workload("tree chain", 3, 8, 2, 64, "bf16", context_lens=[9, 40, 77],
+                    num_queries=6, seed=101)
+    b = appended(wl)
+    chain = np.array([(2 << j) - 1 for j in range(6)], dtype=np.uint64)
+    np.testing.assert_array_equal(
+        oracle.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                              wl.softmax_scale, "bf16", chain), run(b))
+
+
+@pytest.mark.parametrize("Q", [2, 7, 33, 64])
+def test_tree_paged_equals_dense_twin(Q):
+    rng = np.random.default_rng(Q)
+    wl = W.Workload("tree", 3, 8, 2, 64, "f32", context_lens=[Q, Q + 5, Q + 100],
+                    num_queries=Q, seed=102 + Q)
+    b = appended(wl)
+    masks = np.stack([random_tree(Q, rng)[1] for _ in range(3)])
+    o1 = oracle.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                               wl.softmax_scale, "f32", masks)
+    o2 = twin.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                             wl.softmax_scale, "f32", masks)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+
+
+def test_tree_node_equals_decode_on_its_path():
+    """Node j of a tree sees exactly the cache and its ancestors: moving its
+    path's rows in front of it and decoding gives the same output."""
+    rng = np.random.default_rng(5)
+    Q = 9
+    parents, masks = random_tree(Q, rng)
+    wl = W.Workload("tree path", 1, 4, 2, 64, "f32", context_lens=[50], num_queries=Q,
+                    seed=103)
+    b = appended(wl)
+    tree = oracle.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                 wl.softmax_scale, "f32", masks)
+    L, base = 50, 50 - Q
+    k = twin.gather_sequence(b.k_cache, b.block_table[0], L)
+    v = twin.gather_sequence(b.v_cache, b.block_table[0], L)
+    for j in range(Q):
+        path = [kk for kk in range(Q) if (int(masks[j]) >> kk) & 1]
+        rows = list(range(base)) + [base + kk for kk in path]
+        n = len(rows)
+        nb = -(-n // 16)
+        kc = np.full((nb, 2, 16, 64), np.nan, np.float32)
+        vc = np.full_like(kc, np.nan)
+        for r, src in enumerate(rows):
+            kc[r // 16, :, r % 16] = k[src]
+            vc[r // 16, :, r % 16] = v[src]
+        dec = oracle.paged_attention(np.ascontiguousarray(b.q[:, j]), kc, vc,
+                                     np.arange(nb, dtype=np.int32)[None],
+                                     np.array([n], np.int32), wl.softmax_scale, "f32")
+        np.testing.assert_allclose(tree[0, j], dec[0, 0], rtol=0, atol=1e-13)
+
+
+def test_tree_speculative_equals_greedy():
+    """Verifying a candidate tree and keeping the longest accepted path
+    reproduces plain greedy decoding ("Inference part 2", Medusa)."""
+    from tests.toy_decoder import ToyDecoder, greedy, tree_speculative
+    prompt = [3, 17, 5, 9, 30, 2, 11]
+    n = 40
+    ref = greedy(ToyDecoder(seed=3), prompt, n)
+    rng = np.random.default_rng(2)
+
+    def propose_tree(tokens):
+        # two candidates per level, one of them the true continuation half
+        # of the time; level d's nodes hang off the first node of level d-1
+        pos = len(tokens)
+        toks, pars = [], []
+        prev = 0
+        for d in range(3):
+            truth = ref[pos + d] if pos + d < len(ref) else 0
+            first = len(toks) + 1
+            for c in range(2):
+                good = c == 0 and rng.random() < 0.7
+                toks.append(truth if good else int(rng.integers(48)))
+                pars.append(prev)
+            prev = first
+        return toks, pars
+
+    got, passes = tree_speculative(ToyDecoder(seed=3), prompt, n, propose_tree)
+    assert got == ref
+    assert passes < n

@@ -84,3 +84,72 @@ def speculative(model, prompt, n_tokens, propose, n_drafts):
         passes += 1
         accepted_total += n_acc
     return tokens[:len(prompt) + n_tokens], passes, accepted_total
+
+
+def ancestor_masks(parents):
+    """Bit k of mask[j] set iff node k is node j or one of its ancestors
+    (parents[0] = -1 for the root; parents[j] < j)."""
+    masks = []
+    for j, par in enumerate(parents):
+        masks.append((1 << j) | (masks[par] if par >= 0 else 0))
+    return np.array(masks, dtype=np.uint64)
+
+
+def forward_tree(model, tokens, parents, start):
+    """Logits of the tree nodes: node j sits at position start + depth(j) but
+    in cache slot start + j; it attends to the cache and its ancestors."""
+    n = len(tokens)
+    depth = [0] * n
+    for j in range(1, n):
+        depth[j] = depth[parents[j]] + 1
+    pos = start + np.array(depth)
+    x = model.emb[tokens] + model.pos[pos]
+    q = (x @ model.wq).reshape(n, model.H, model.D).astype(np.float32)
+    k = (x @ model.wk).reshape(n, model.Hkv, model.D).astype(np.float32)
+    v = (x @ model.wv).reshape(n, model.Hkv, model.D).astype(np.float32)
+    rows = np.arange(start, start + n)
+    slots = model.table[0, rows // model.bs].astype(np.int64) * model.bs + rows % model.bs
+    oracle.kv_append(model.k_cache, model.v_cache, np.ascontiguousarray(k),
+                     np.ascontiguousarray(v), slots, "f32")
+    att = oracle.tree_attention(np.ascontiguousarray(q[None]), model.k_cache, model.v_cache,
+                                model.table, np.array([start + n], np.int32),
+                                1.0 / np.sqrt(model.D), "f32", ancestor_masks(parents))[0]
+    h = x + att.reshape(n, model.H * model.D) @ model.wo
+    return h @ model.head, depth
+
+
+def _move_row(model, src, dst):
+    """Copy cache row `src` of the sequence to row `dst` (K and V)."""
+    bs = model.bs
+    for cache in (model.k_cache, model.v_cache):
+        cache[model.table[0, dst // bs], :, dst % bs] = cache[model.table[0, src // bs], :, src % bs]
+
+
+def tree_speculative(model, prompt, n_tokens, propose_tree):
+    """Greedy verification of a candidate tree per pass: the longest path
+    whose tokens match the target's argmax is kept, plus the target's own
+    next token; the accepted nodes' K/V rows are moved to their positions."""
+    tokens = list(prompt)
+    if len(prompt) > 1:
+        model.forward(np.array(prompt[:-1]), 0)
+    passes = 0
+    while len(tokens) < len(prompt) + n_tokens:
+        cand_tokens, cand_parents = propose_tree(tokens)
+        node_tokens = [tokens[-1]] + cand_tokens
+        parents = [-1] + cand_parents
+        start = len(tokens) - 1
+        logits, depth = forward_tree(model, np.array(node_tokens), parents, start)
+        pred = np.argmax(logits, axis=-1)
+        path, node = [0], 0
+        while True:
+            nxt = [c for c in range(1, len(node_tokens))
+                   if parents[c] == node and node_tokens[c] == pred[node]]
+            if not nxt:
+                break
+            node = nxt[0]
+            path.append(node)
+        for d, idx in enumerate(path):
+            _move_row(model, start + idx, start + d)
+        tokens += [node_tokens[i] for i in path[1:]] + [int(pred[path[-1]])]
+        passes += 1
+    return tokens[:len(prompt) + n_tokens], passes
