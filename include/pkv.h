@@ -270,6 +270,32 @@ PKV_API pkv_status pkv_append_attention(
     const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
 
 /*
+ * pkv_tree_verify_attention -- verification of a candidate tree (Medusa):
+ * "Inference part 2", section "Medusa": the candidates of a tree are
+ * verified in one pass with tree attention, a mask that lets each candidate
+ * attend only to its own ancestors.  The num_queries tree nodes of sequence
+ * b occupy its last rows L_b - num_queries .. L_b - 1 (their K/V already
+ * appended, node k at row L_b - num_queries + k); node j sees every earlier
+ * (cached) row and tree row k exactly when bit k of
+ * tree_mask[b * mask_batch_stride + j] is set (normally node j and its
+ * ancestors).  The chain tree (bits 0..j) is pkv_spec_verify_attention.
+ *
+ *   tree_mask : device uint64 [batch, num_queries] (mask_batch_stride =
+ *               num_queries) or [num_queries] shared by all sequences
+ *               (mask_batch_stride = 0); 8-byte aligned
+ *   num_queries <= 64.  Other arguments as for pkv_spec_verify_attention.
+ */
+PKV_API pkv_status pkv_tree_verify_attention(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_table, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int batch,
+    int num_queries, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, float scale, pkv_dtype dtype,
+    const uint64_t *tree_mask, int64_t mask_batch_stride, void *workspace,
+    size_t workspace_bytes, const pkv_options *options, int32_t *error_word,
+    pkv_stream_t stream);
+
+/*
  * pkv_read_error_word -- copy the device error word to *host_code after all
  * work on `stream` (synchronises the stream; not for the hot path).
  */

@@ -32,7 +32,7 @@ EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_
             "pkv_attention_plan_for", "pkv_attention_workspace_size",
             "pkv_paged_decode_attention", "pkv_spec_verify_attention",
             "pkv_read_error_word", "pkv_paged_decode_attention_noalloc",
-            "pkv_append_attention")
+            "pkv_append_attention", "pkv_tree_verify_attention")
 
 
 class PkvError(RuntimeError):
@@ -101,6 +101,9 @@ def lib() -> ctypes.CDLL:
             L.pkv_append_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
                                                i32, i32, i32, i32, i32, i64, f32, i32, vp, sz,
                                                opt, vp, vp]
+            L.pkv_tree_verify_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                                    i32, i32, i32, i32, i64, f32, i32, vp, i64,
+                                                    vp, sz, opt, vp, vp]
             L.pkv_paged_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32,
                                                              i32, i32, i32, i32, i32, i64, f32,
                                                              i32, opt, vp, vp]
@@ -324,6 +327,52 @@ def append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
         v_cache.data_ptr(), block_table.data_ptr(), block_table.shape[1], context_lens.data_ptr(),
         max_context_len, B, Q, Hq, Hkv, D, bs, NB, float(scale), _DTYPE[q.dtype], ws_ptr,
         ws_bytes, _opts(kernel, split_blocks, stages), _err_ptr(error_word), _stream(q)))
+    return out
+
+
+def tree_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          block_table: torch.Tensor, context_lens: torch.Tensor,
+                          tree_mask: torch.Tensor, scale: Optional[float] = None,
+                          max_context_len: Optional[int] = None,
+                          out: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, kernel: int = 0,
+                          split_blocks: int = 0, error_word: Optional[torch.Tensor] = None,
+                          stages: int = 0) -> torch.Tensor:
+    """Tree verification (pkv_tree_verify_attention): q [B, Q, Hq, D]; node j
+    of sequence b sees the cached rows and tree row k iff bit k of
+    tree_mask[b, j] (or tree_mask[j], shared) is set.  tree_mask: CUDA int64
+    (the uint64 bit patterns), [Q] or [B, Q]."""
+    NB, Hkv, bs, D = _cache_args(k_cache, v_cache)
+    _need(q.dim() == 4 and q.is_cuda and q.is_contiguous() and q.dtype == k_cache.dtype
+          and q.shape[-1] == D, "q must be [batch, num_queries, num_heads, head_dim]")
+    B, Q, Hq, _ = q.shape
+    _need(tree_mask.dtype == torch.int64 and tree_mask.is_cuda and tree_mask.is_contiguous()
+          and tree_mask.shape in ((Q,), (B, Q)), "tree_mask: CUDA int64 [Q] or [B, Q]")
+    stride = 0 if tree_mask.dim() == 1 else Q
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2
+          and block_table.shape[0] == B and block_table.is_contiguous() and block_table.is_cuda,
+          "block_table must be a contiguous CUDA int32 [batch, max_blocks_per_seq]")
+    _need(context_lens.dtype == torch.int32 and context_lens.shape == (B,)
+          and context_lens.is_cuda and context_lens.is_contiguous(), "context_lens")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0  # device read
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
+    need = workspace_size(B, Q, Hq, Hkv, D, max_context_len, q.dtype, bs, kernel, split_blocks,
+                          stages)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("pkv_tree_verify_attention", lib().pkv_tree_verify_attention(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_table.data_ptr(), block_table.shape[1], context_lens.data_ptr(), max_context_len,
+        B, Q, Hq, Hkv, D, bs, NB, float(scale), _DTYPE[q.dtype], tree_mask.data_ptr(), stride,
+        ws_ptr, ws_bytes, _opts(kernel, split_blocks, stages), _err_ptr(error_word),
+        _stream(q)))
     return out
 
 

@@ -117,9 +117,13 @@ __global__ void __launch_bounds__(BL * CG * 32)
   }
   // Visible-row limit of the two columns this thread holds.
   int lim[2];
+  unsigned long long tm[2];
 #pragma unroll
-  for (int e = 0; e < 2; ++e) lim[e] = cta_row_limit(p, L, chunk, col0 + 2 * c + e);
-  const int mask_from = L - p.num_queries + 1;  // first row some column cannot see
+  for (int e = 0; e < 2; ++e) {
+    lim[e] = cta_row_limit(p, L, chunk, col0 + 2 * c + e);
+    tm[e] = cta_row_tree_mask(p, b, chunk, col0 + 2 * c + e);
+  }
+  const int mask_from = L - p.num_queries;  // first row some column may not see
 
   // Online-softmax state.
   float o[KS][4];
@@ -234,10 +238,8 @@ __global__ void __launch_bounds__(BL * CG * 32)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float v = sc[e] * p.scale_log2;
-        if (need_mask) {
-          const int key = key0 + g + ((e >> 1) << 3);
-          if (bad || key >= lim[e & 1]) v = -INFINITY;
-        }
+        if (need_mask && !key_visible(p, key0 + g + ((e >> 1) << 3), L, bad, lim[e & 1], tm[e & 1]))
+          v = -INFINITY;
         sc[e] = v;
         above |= v > m[e & 1] + kRescaleSlack;
       }

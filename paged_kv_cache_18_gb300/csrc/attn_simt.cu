@@ -89,10 +89,12 @@ __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
   // Query rows in registers (this lane's slice of the head dim).
   float qv[R][EPL];
   int lim[R];
+  unsigned long long tm[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int64_t row = cta_row_index(p, b, kvh, chunk, r);
     lim[r] = row < 0 ? -1 : cta_row_limit(p, L, chunk, r);
+    tm[r] = cta_row_tree_mask(p, b, chunk, r);
     const uint8_t *qrow = reinterpret_cast<const uint8_t *>(p.q) + (row < 0 ? 0 : row) * RB;
 #pragma unroll
     for (int cv = 0; cv < VPL; ++cv) {
@@ -194,8 +196,8 @@ __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
         d += __shfl_xor_sync(kFull, d, 1);
         d += __shfl_xor_sync(kFull, d, 2);
         d += __shfl_xor_sync(kFull, d, 4);
-        const int key = key0 + row;
-        sc[k][r] = (!bad && key < lim[r]) ? d * p.scale_log2 : -INFINITY;
+        const bool vis = lim[r] >= 0 && key_visible(p, key0 + row, L, bad, lim[r], tm[r]);
+        sc[k][r] = vis ? d * p.scale_log2 : -INFINITY;
       }
     }
     // Online softmax over these 4 rows.

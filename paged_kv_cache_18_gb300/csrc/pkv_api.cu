@@ -296,7 +296,8 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
                          const int32_t *context_lens, const Shape &s, int64_t num_blocks,
                          float scale, void *workspace, size_t workspace_bytes,
                          const pkv_options *opt, int32_t *error_word, cudaStream_t stream,
-                         const void *k_new = nullptr, const void *v_new = nullptr) {
+                         const void *k_new = nullptr, const void *v_new = nullptr,
+                         const uint64_t *tree_mask = nullptr, int64_t mask_stride = 0) {
   pkv_status st = check_shape(s);
   if (st != PKV_OK) return st;
   if (s.batch == 0) return PKV_OK;
@@ -332,6 +333,8 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   p.context_lens = context_lens;
   p.k_new = k_new;
   p.v_new = v_new;
+  p.tree_mask = reinterpret_cast<const unsigned long long *>(tree_mask);
+  p.mask_stride = mask_stride;
   p.err = error_word;
   p.num_blocks = num_blocks;
   p.batch = s.batch;
@@ -515,6 +518,27 @@ pkv_status pkv_append_attention(void *out, const void *q, const void *k_new, con
   return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
                        num_blocks, scale, workspace, workspace_bytes, options, error_word,
                        reinterpret_cast<cudaStream_t>(stream), k_new, v_new);
+}
+
+pkv_status pkv_tree_verify_attention(void *out, const void *q, const void *k_cache,
+                                     const void *v_cache, const int32_t *block_table,
+                                     int max_blocks_per_seq, const int32_t *context_lens,
+                                     int max_context_len, int batch, int num_queries,
+                                     int num_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int64_t num_blocks, float scale,
+                                     pkv_dtype dtype, const uint64_t *tree_mask,
+                                     int64_t mask_batch_stride, void *workspace,
+                                     size_t workspace_bytes, const pkv_options *options,
+                                     int32_t *error_word, pkv_stream_t stream) {
+  if (num_queries > 64 || mask_batch_stride < 0) return PKV_ERR_INVALID_ARG;
+  if (batch > 0 && !tree_mask) return PKV_ERR_INVALID_ARG;
+  if (!aligned(tree_mask, 8)) return PKV_ERR_ALIGNMENT;
+  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype};
+  return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
+                       num_blocks, scale, workspace, workspace_bytes, options, error_word,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, tree_mask,
+                       mask_batch_stride);
 }
 
 pkv_status pkv_read_error_word(const int32_t *error_word, int32_t *host_code,

@@ -36,6 +36,9 @@ struct AttnParams {
   unsigned long long *counters; // [B, Hkv, row_chunks] arrivals (epoch << 32 | count);
                                 //   nullptr: a separate merge kernel runs after
   uint32_t epoch;               // tag of this call in the counters
+  const unsigned long long *tree_mask;  // [B, Q] with stride mask_stride (0: shared),
+                                        //   or nullptr: causal among the Q rows
+  int64_t mask_stride;
   int32_t *err;                 // optional device error word
   int64_t num_blocks;
   int batch, num_queries, num_heads, num_kv_heads, group;
@@ -220,6 +223,27 @@ __device__ __forceinline__ int cta_row_limit(const AttnParams &p, int L, int chu
   const int r = chunk * p.rows_per_cta + col;
   const int j = (col < p.rows_per_cta && r < p.rows) ? r / p.group : 0;
   return L - p.num_queries + 1 + j;
+}
+
+// Tree mask of query row `col` of this CTA (tree verification): bit k set
+// when the row may see row L - Q + k.  0 for padding columns.
+__device__ __forceinline__ unsigned long long cta_row_tree_mask(const AttnParams &p, int b,
+                                                                int chunk, int col) {
+  const int r = chunk * p.rows_per_cta + col;
+  if (p.tree_mask == nullptr || col >= p.rows_per_cta || r >= p.rows) return 0ull;
+  return __ldg(p.tree_mask + static_cast<int64_t>(b) * p.mask_stride + r / p.group);
+}
+
+// Whether key row `key` is visible to a query row: rows past the context and
+// rows of a bad block never are; with a tree mask, cached rows (before the Q
+// new ones) always are and new row k when bit k is set; otherwise the causal
+// limit `lim` (rows < L - Q + 1 + j) applies.
+__device__ __forceinline__ bool key_visible(const AttnParams &p, int key, int L, bool bad, int lim,
+                                            unsigned long long tm) {
+  if (bad || key >= L) return false;
+  if (p.tree_mask == nullptr) return key < lim;
+  const int t = key - (L - p.num_queries);
+  return t < 0 || ((tm >> t) & 1ull);
 }
 
 // Effective context length of sequence b and its block count, with the

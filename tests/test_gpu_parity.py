@@ -329,3 +329,58 @@ def test_row_caps_and_merge_modes(rows_per_cta, merge):
         run_case(wl, kernel=1, split_blocks=8)
     finally:
         binding.TUNING.clear()
+
+
+# ---- tree verification (Medusa tree attention) ----------------------------
+def _tree_masks(Q, n, rng):
+    from tests.toy_decoder import ancestor_masks
+    out = []
+    for _ in range(n):
+        parents = [-1] + [int(rng.integers(0, j)) for j in range(1, Q)]
+        out.append(ancestor_masks(parents))
+    return np.stack(out)
+
+
+@pytest.mark.parametrize("dtype,kernel", [("f32", 1), ("bf16", 1), ("bf16", 2)])
+@pytest.mark.parametrize("Q,Hq,Hkv,shared", [(2, 8, 2, True), (5, 32, 8, False),
+                                             (16, 8, 1, False), (33, 4, 4, True),
+                                             (64, 8, 2, False)])
+@pytest.mark.parametrize("split_blocks", [0, 2])
+def test_tree_verify(dtype, kernel, Q, Hq, Hkv, shared, split_blocks):
+    import oracle
+    import paged_kv_cache_18_gb300 as pkv
+    rng = np.random.default_rng(Q * 7 + split_blocks)
+    lens = [Q, Q + 3, Q + 40, Q + 300]
+    D = 64 if dtype == "f32" else 128
+    wl = W.Workload(f"tree {dtype} k{kernel} Q{Q}", len(lens), Hq, Hkv, D, dtype,
+                    context_lens=lens, num_queries=Q, seed=700 + Q + split_blocks)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    masks = _tree_masks(Q, 1 if shared else wl.batch, rng)
+    masks = masks[0] if shared else masks
+    tm = torch.from_numpy(np.ascontiguousarray(masks).view(np.int64)).cuda()
+    out = pkv.tree_verify_attention(d.q, d.k_cache, d.v_cache, d.table, d.lens, tm,
+                                    scale=wl.softmax_scale, max_context_len=b.max_context_len,
+                                    kernel=kernel, split_blocks=split_blocks, error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    oracle.kv_append(b.k_cache, b.v_cache, b.k_new, b.v_new, b.slot_mapping, dtype)
+    ref = oracle.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                wl.softmax_scale, dtype, masks)
+    assert_close(host_f64(out, dtype), ref, dtype, wl.name)
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_chain_tree_equals_spec_verify_bitwise(kernel):
+    import paged_kv_cache_18_gb300 as pkv
+    wl = W.Workload("chain", 4, 32, 8, 128, "bf16", context_lens=[5, 50, 700, 2000],
+                    num_queries=5, seed=720)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    chain = torch.tensor([(2 << j) - 1 for j in range(5)], dtype=torch.int64, device="cuda")
+    t = pkv.tree_verify_attention(d.q, d.k_cache, d.v_cache, d.table, d.lens, chain,
+                                  max_context_len=b.max_context_len, kernel=kernel)
+    s = d.attend(kernel=kernel)
+    assert torch.equal(t, s)
