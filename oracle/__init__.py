@@ -87,6 +87,17 @@ class Oracle:
             vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64,
             ctypes.c_double, i32, vp, i64]
         lib.oracle_tree_attention.restype = i32
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint]
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint
+        lib.oracle_kv_append_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64,
+                                             ctypes.c_float, ctypes.c_float]
+        lib.oracle_kv_append_fp8.restype = i32
+        lib.oracle_paged_attention_fp8.argtypes = [
+            vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64,
+            ctypes.c_double, i32, ctypes.c_double, ctypes.c_double]
+        lib.oracle_paged_attention_fp8.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         self.lib = lib
@@ -178,6 +189,54 @@ class Oracle:
         return out
 
 
+    # ---- FP8 E4M3 cache -------------------------------------------------
+    def e4m3_value(self, code: int) -> float:
+        return float(self.lib.oracle_e4m3_value(int(code)))
+
+    def e4m3_encode(self, x: float) -> int:
+        return int(self.lib.oracle_e4m3_encode(float(x)))
+
+    def kv_append_fp8(self, k_cache, v_cache, k_new, v_new, slot_mapping, src_dtype: str,
+                      k_scale: float, v_scale: float) -> None:
+        """Quantise k_new/v_new [T, Hkv, D] (storage of src_dtype) into the
+        e4m3 byte caches [NB, Hkv, bs, D] at their slots."""
+        from .twin import widen
+        for name, a in (("k_cache", k_cache), ("v_cache", v_cache)):
+            if a.dtype != np.uint8 or not a.flags["C_CONTIGUOUS"]:
+                raise ValueError(f"{name}: expected C-contiguous uint8 codes")
+        kf = np.ascontiguousarray(widen(k_new, src_dtype).astype(np.float32))
+        vf = np.ascontiguousarray(widen(v_new, src_dtype).astype(np.float32))
+        slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        NB, Hkv, bs, D = k_cache.shape
+        st = self.lib.oracle_kv_append_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(kf), _ptr(vf),
+                                           _ptr(slots), kf.shape[0], Hkv, D, bs, NB,
+                                           float(k_scale), float(v_scale))
+        if st != 0:
+            raise ValueError(f"oracle_kv_append_fp8 failed with code {st}")
+
+    def paged_attention_fp8(self, q, k_cache, v_cache, block_table, context_lens,
+                            scale: float, q_dtype: str, k_scale: float,
+                            v_scale: float) -> np.ndarray:
+        """Float64 attention [B, Q, Hq, D] over e4m3 byte caches."""
+        if q.ndim == 3:
+            q = q[:, None]
+        q = np.ascontiguousarray(q)
+        _check_storage(q, q_dtype, "q")
+        B, Q, Hq, D = q.shape
+        NB, Hkv, bs, _ = k_cache.shape
+        table = np.ascontiguousarray(block_table, dtype=np.int32)
+        lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.full((B, Q, Hq, D), np.nan, dtype=np.float64)
+        st = self.lib.oracle_paged_attention_fp8(
+            _ptr(out), _ptr(q), _ptr(np.ascontiguousarray(k_cache)),
+            _ptr(np.ascontiguousarray(v_cache)), _ptr(table), table.shape[1], _ptr(lens), B, Q,
+            Hq, Hkv, D, bs, NB, float(scale), DTYPE_CODES[q_dtype], float(k_scale),
+            float(v_scale))
+        if st != 0:
+            raise ValueError(f"oracle_paged_attention_fp8 failed with code {st}")
+        return out
+
+
 def default() -> Oracle:
     """The oracle built from ``pkv_oracle.c`` (compiled on first use)."""
     global _default
@@ -201,3 +260,11 @@ def paged_attention(*args, **kwargs) -> np.ndarray:
 
 def tree_attention(*args, **kwargs) -> np.ndarray:
     return default().tree_attention(*args, **kwargs)
+
+
+def kv_append_fp8(*args, **kwargs) -> None:
+    default().kv_append_fp8(*args, **kwargs)
+
+
+def paged_attention_fp8(*args, **kwargs) -> np.ndarray:
+    return default().paged_attention_fp8(*args, **kwargs)

@@ -47,6 +47,10 @@
  *    candidate tree, each seeing the cached rows and its own ancestors
  *    (tree attention of Medusa, "Inference part 2", section "Medusa").
  *
+ *  - oracle_kv_append_fp8 / oracle_paged_attention_fp8: the same append and
+ *    attention over an FP8 E4M3 cache with one scale per tensor (see the
+ *    comment above oracle_e4m3_value).
+ *
  * Readings where the pages are silent (each also listed in the design
  * notes): L counts every row of the sequence including the new ones; a
  * query row that sees no row at all (L - Q + j < 0, e.g. L = 0) returns a
@@ -322,6 +326,160 @@ int oracle_tree_attention(double *out, const void *q, const void *k_cache,
     }
     free(scores);
     free(seen);
+  }
+  return status;
+}
+
+/*
+ * FP8 E4M3 KV cache ("Inference part 2", section "Quantization": the format
+ * table gives FP8 E4M3 as 1 sign / 4 exponent / 3 mantissa bits with largest
+ * value 448, used for the KV cache; section "KV cache quantization": storing
+ * the cache in FP8 halves its size and the bytes read at each decode step).
+ * Reading adopted where the pages leave the scheme open: one float32 scale
+ * per cache tensor, code = round-to-nearest-even(x / scale) with saturation
+ * at +-448, value = code * scale; the division x / scale is the float32 one.
+ *
+ * The decoding below is the definition of the format: exponent bias 7,
+ * exponent field 0 = subnormal (m / 8 * 2^-6), all ones with mantissa 7 =
+ * NaN (there is no infinity).
+ */
+double oracle_e4m3_value(unsigned code) {
+  const int sign = (code >> 7) & 1, e = (code >> 3) & 0xf, m = code & 7;
+  double v;
+  if (e == 15 && m == 7)
+    v = NAN;
+  else if (e == 0)
+    v = ldexp((double)m, -9); /* m/8 * 2^-6 */
+  else
+    v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+  return sign ? -v : v;
+}
+
+/* Nearest e4m3 code of a float32 value: round to nearest, ties to the even
+ * code, saturating at the largest finite magnitude (448); NaN -> 0x7f. */
+unsigned oracle_e4m3_encode(float x) {
+  if (x != x) return 0x7f;
+  const unsigned sign = (x < 0.0f || (x == 0.0f && signbit(x))) ? 0x80u : 0u;
+  const double a = fabs((double)x);
+  /* the 127 non-negative finite codes, in increasing value; pick the closest
+     and on a tie the one whose code is even */
+  unsigned best = 0;
+  double best_err = a;
+  for (unsigned c = 1; c <= 0x7e; ++c) {
+    const double err = fabs(oracle_e4m3_value(c) - a);
+    if (err < best_err || (err == best_err && (c & 1u) == 0u)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  if (a >= 448.0) best = 0x7e; /* saturate */
+  return sign | best;
+}
+
+/*
+ * oracle_kv_append_fp8: quantise new rows [T, Hkv, D] (float32 values, the
+ * caller widens 16-bit inputs exactly) into e4m3 codes written at their slots
+ * of the byte caches [NB, Hkv, bs, D].  Negative slots are skipped.
+ */
+int oracle_kv_append_fp8(uint8_t *k_cache, uint8_t *v_cache, const float *k_new,
+                         const float *v_new, const int64_t *slot_mapping, int64_t T,
+                         int Hkv, int D, int bs, int64_t NB, float k_scale,
+                         float v_scale) {
+  if (!k_cache || !v_cache || !k_new || !v_new || !slot_mapping || T < 0 ||
+      Hkv <= 0 || D <= 0 || bs <= 0 || NB < 0 || !(k_scale > 0.0f) ||
+      !(v_scale > 0.0f))
+    return ORACLE_ERR_ARG;
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= NB * bs) return ORACLE_ERR_SLOT;
+    const int64_t block = slot / bs, offset = slot % bs;
+    for (int h = 0; h < Hkv; ++h)
+      for (int d = 0; d < D; ++d) {
+        const int64_t src = (t * Hkv + h) * D + d;
+        const int64_t dst = ((block * Hkv + h) * bs + offset) * D + d;
+        const float kq = k_new[src] / k_scale; /* float32 division */
+        const float vq = v_new[src] / v_scale;
+        k_cache[dst] = (uint8_t)oracle_e4m3_encode(kq);
+        v_cache[dst] = (uint8_t)oracle_e4m3_encode(vq);
+      }
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * oracle_paged_attention_fp8: oracle_paged_attention over an e4m3 cache:
+ * every key element is code value * k_scale and every value element code
+ * value * v_scale (exact in float64); q is in q_dtype (0 f32, 1 bf16, 2 f16).
+ * Output [B, Q, Hq, D] float64.  Same masking (shifted causal) and readings.
+ */
+int oracle_paged_attention_fp8(double *out, const void *q, const uint8_t *k_cache,
+                               const uint8_t *v_cache, const int32_t *block_table,
+                               int max_blocks, const int32_t *context_lens, int B,
+                               int Q, int Hq, int Hkv, int D, int bs, int64_t NB,
+                               double scale, int q_dtype, double k_scale,
+                               double v_scale) {
+  if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens ||
+      B < 0 || Q <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 ||
+      bs <= 0 || max_blocks < 0 || NB < 0 || q_dtype < 0 || q_dtype > 2)
+    return ORACLE_ERR_ARG;
+  int64_t max_len = 1;
+  for (int b = 0; b < B; ++b)
+    if (context_lens[b] > max_len) max_len = context_lens[b];
+  int status = ORACLE_OK;
+  const int64_t total = (int64_t)B * Q * Hq;
+#pragma omp parallel
+  {
+    double *scores = (double *)malloc(sizeof(double) * (size_t)max_len);
+    if (!scores) {
+#pragma omp atomic write
+      status = ORACLE_ERR_NOMEM;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t r = 0; r < total; ++r) {
+      if (!scores) continue;
+      const int h = (int)(r % Hq), j = (int)((r / Hq) % Q);
+      const int b = (int)(r / ((int64_t)Hq * Q));
+      const int64_t visible = (int64_t)context_lens[b] - Q + 1 + j;
+      const int g = h / (Hq / Hkv);
+      double *o = out + r * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      if (visible <= 0) continue;
+      if ((visible + bs - 1) / bs > max_blocks) {
+#pragma omp atomic write
+        status = ORACLE_ERR_BLOCK;
+        continue;
+      }
+      const int64_t q_base = (((int64_t)b * Q + j) * Hq + h) * D;
+      int bad = 0;
+      for (int64_t i = 0; i < visible; ++i) {
+        const int32_t phys = block_table[(int64_t)b * max_blocks + i / bs];
+        if (phys < 0 || phys >= NB) { bad = 1; break; }
+        const int64_t kb = (((int64_t)phys * Hkv + g) * bs + i % bs) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+          dot += widen(q, q_base + d, q_dtype) * (oracle_e4m3_value(k_cache[kb + d]) * k_scale);
+        scores[i] = scale * dot;
+      }
+      if (bad) {
+#pragma omp atomic write
+        status = ORACLE_ERR_BLOCK;
+        continue;
+      }
+      double m = scores[0];
+      for (int64_t i = 1; i < visible; ++i)
+        if (scores[i] > m) m = scores[i];
+      double denom = 0.0;
+      for (int64_t i = 0; i < visible; ++i) {
+        const double w = exp(scores[i] - m);
+        const int32_t phys = block_table[(int64_t)b * max_blocks + i / bs];
+        const int64_t vb = (((int64_t)phys * Hkv + g) * bs + i % bs) * D;
+        denom += w;
+        for (int d = 0; d < D; ++d) o[d] += w * (oracle_e4m3_value(v_cache[vb + d]) * v_scale);
+      }
+      for (int d = 0; d < D; ++d) o[d] /= denom;
+    }
+    free(scores);
   }
   return status;
 }

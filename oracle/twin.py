@@ -114,3 +114,50 @@ def tree_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
             w /= w.sum(axis=-1, keepdims=True)
             out[b, j] = np.einsum("hi,ihd->hd", w, v)
     return out
+
+
+def e4m3_values() -> np.ndarray:
+    """Value of each of the 256 FP8 E4M3 codes from the format's definition
+    (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is
+    subnormal; S.1111.111 is NaN), computed with NumPy."""
+    c = np.arange(256)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    v = np.where((e == 15) & ((c & 7) == 7), np.nan, v)
+    return sign * v
+
+
+def contiguous_attention_fp8(q, k_codes, v_codes, block_table, context_lens, scale, q_dtype,
+                             k_scale, v_scale):
+    """contiguous_attention over an e4m3 cache: dequantise every code to
+    code value * tensor scale in float64, then the dense computation."""
+    table = e4m3_values()
+    B = q.shape[0]
+    kf = (table[k_codes] * k_scale)
+    vf = (table[v_codes] * v_scale)
+    # reuse the dense path on float64 caches
+    if q.ndim == 3:
+        q = q[:, None]
+    Bq, Q, Hq, D = q.shape
+    Hkv = k_codes.shape[1]
+    group = Hq // Hkv
+    out = np.zeros((Bq, Q, Hq, D))
+    for b in range(B):
+        L = int(context_lens[b])
+        if L <= 0:
+            continue
+        k = np.repeat(gather_sequence(kf, block_table[b], L), group, axis=1)
+        v = np.repeat(gather_sequence(vf, block_table[b], L), group, axis=1)
+        qb = widen(q[b], q_dtype)
+        s = np.einsum("jhd,ihd->hji", qb, k) * scale
+        mask = np.tril(np.ones((Q, L), dtype=bool), k=L - Q)
+        s = np.where(mask[None], s, -np.inf)
+        for j in range(Q):
+            if not mask[j].any():
+                continue
+            w = np.exp(s[:, j] - s[:, j].max(axis=-1, keepdims=True))
+            w /= w.sum(axis=-1, keepdims=True)
+            out[b, j] = np.einsum("hi,ihd->hd", w, v)
+    return out

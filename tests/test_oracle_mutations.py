@@ -152,3 +152,56 @@ def test_tree_mutation_is_caught(name, tmp_path):
     mutated.write_text(src.replace(old, new))
     lib = oracle.compile_library(str(mutated), str(tmp_path / "libmutant.so"))
     assert _tree_battery(oracle.Oracle(lib)), f"planted mistake {name!r} passed every pin"
+
+
+# ---- FP8 E4M3 cache -------------------------------------------------------
+FP8_MUTATIONS = {
+    "e4m3 exponent bias": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 11);"),
+    "e4m3 subnormal scale": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    "ties to odd": ("(err == best_err && (c & 1u) == 0u)", "(err == best_err && (c & 1u) == 1u)"),
+    "no saturation": ("if (a >= 448.0) best = 0x7e;", "if (a >= 1e30) best = 0x7e;"),
+    "k scale dropped": ("* (oracle_e4m3_value(k_cache[kb + d]) * k_scale)",
+                        "* (oracle_e4m3_value(k_cache[kb + d]))"),
+}
+
+
+def _fp8_battery(orc) -> list:
+    failed = []
+    vals = np.array([orc.e4m3_value(c) for c in range(256)])
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    if not np.array_equal(vals, lib, equal_nan=True):
+        failed.append("decode vs library")
+    x = np.array([1.0625, 1.1875, -3.25, 500.0, 1e-3, 0.3], dtype=np.float32)
+    ours = [orc.e4m3_encode(v) for v in x]
+    want = [0x38, 0x3A, torch.tensor([-3.25]).to(torch.float8_e4m3fn).view(torch.uint8).item(),
+            0x7E, torch.tensor([1e-3]).to(torch.float8_e4m3fn).view(torch.uint8).item(),
+            torch.tensor([0.3]).to(torch.float8_e4m3fn).view(torch.uint8).item()]
+    if ours != want:
+        failed.append("encode")
+    wl = W.Workload("fp8 m", 2, 4, 2, 64, "bf16", context_lens=[17, 40], seed=44)
+    b = W.make_batch(wl, poison=False)
+    NB, Hkv, bs, D = b.k_cache.shape
+    kc = (np.arange(NB * Hkv * bs * D) * 37 % 126).astype(np.uint8).reshape(NB, Hkv, bs, D)
+    vc = (np.arange(NB * Hkv * bs * D) * 53 % 126).astype(np.uint8).reshape(NB, Hkv, bs, D)
+    got = orc.paged_attention_fp8(b.q, kc, vc, b.block_table, b.context_lens, wl.softmax_scale,
+                                  "bf16", 0.03, 0.02)
+    want = twin.contiguous_attention_fp8(b.q, kc, vc, b.block_table, b.context_lens,
+                                         wl.softmax_scale, "bf16", 0.03, 0.02)
+    if not np.allclose(got, want, rtol=0, atol=1e-12):
+        failed.append("attention vs twin")
+    return failed
+
+
+def test_unmutated_fp8_oracle_passes_battery():
+    assert _fp8_battery(oracle.default()) == []
+
+
+@pytest.mark.parametrize("name", sorted(FP8_MUTATIONS))
+def test_fp8_mutation_is_caught(name, tmp_path):
+    old, new = FP8_MUTATIONS[name]
+    src = open(oracle.SOURCE).read()
+    assert old in src, f"mutation anchor for {name!r} not found"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.compile_library(str(mutated), str(tmp_path / "libmutant.so"))
+    assert _fp8_battery(oracle.Oracle(lib)), f"planted mistake {name!r} passed every pin"
