@@ -361,6 +361,7 @@ unsigned oracle_e4m3_encode(float x) {
   if (x != x) return 0x7f;
   const unsigned sign = (x < 0.0f || (x == 0.0f && signbit(x))) ? 0x80u : 0u;
   const double a = fabs((double)x);
+  if (a > 448.0) return sign | 0x7eu; /* saturate at the largest finite value */
   /* the 127 non-negative finite codes, in increasing value; pick the closest
      and on a tie the one whose code is even */
   unsigned best = 0;
@@ -372,7 +373,6 @@ unsigned oracle_e4m3_encode(float x) {
       best_err = err;
     }
   }
-  if (a >= 448.0) best = 0x7e; /* saturate */
   return sign | best;
 }
 

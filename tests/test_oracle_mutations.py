@@ -159,7 +159,7 @@ FP8_MUTATIONS = {
     "e4m3 exponent bias": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 11);"),
     "e4m3 subnormal scale": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
     "ties to odd": ("(err == best_err && (c & 1u) == 0u)", "(err == best_err && (c & 1u) == 1u)"),
-    "no saturation": ("if (a >= 448.0) best = 0x7e;", "if (a >= 1e30) best = 0x7e;"),
+    "overflow to NaN": ("if (a > 448.0) return sign | 0x7eu;", "if (a > 448.0) return sign | 0x7fu;"),
     "k scale dropped": ("* (oracle_e4m3_value(k_cache[kb + d]) * k_scale)",
                         "* (oracle_e4m3_value(k_cache[kb + d]))"),
 }
