@@ -39,6 +39,8 @@ from paged_kv_cache_18_gb300 import accounting  # noqa: E402
 from paged_kv_cache_18_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); decode tokens/sec"
+# Tensor scales of the FP8 cache runs: N(0,1) values land well inside +-448.
+FP8_K_SCALE, FP8_V_SCALE = 0.0123, 0.0171
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 # Sources whose change invalidates a recorded ncu traffic figure.
@@ -281,8 +283,15 @@ def run_ours(args):
         wl = W.Workload(**{**wl.__dict__, "seed": wl.seed + 100 * rank})
     b = W.make_batch(wl)
     dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl.dtype]
-    k_cache = dev_tensor(b.k_cache, wl.dtype, dev)
-    v_cache = dev_tensor(b.v_cache, wl.dtype, dev)
+    fp8 = args.kv_dtype == "fp8"
+    if fp8:
+        kc8, vc8 = W.fp8_caches(b, FP8_K_SCALE, FP8_V_SCALE)
+        k_cache = torch.from_numpy(kc8).to(dev)
+        v_cache = torch.from_numpy(vc8).to(dev)
+        del kc8, vc8
+    else:
+        k_cache = dev_tensor(b.k_cache, wl.dtype, dev)
+        v_cache = dev_tensor(b.v_cache, wl.dtype, dev)
     k_new = dev_tensor(b.k_new, wl.dtype, dev)
     v_new = dev_tensor(b.v_new, wl.dtype, dev)
     q = dev_tensor(b.q, wl.dtype, dev)
@@ -294,19 +303,23 @@ def run_ours(args):
     out = torch.empty_like(q)
     Q = wl.num_queries
     plan = pkv.plan(wl.batch, Q, wl.num_heads, wl.num_kv_heads, wl.head_dim,
-                    b.max_context_len, dt, kernel=args.kernel, split_blocks=args.split_blocks,
-                    stages=args.stages)
+                    b.max_context_len, "fp8" if fp8 else dt, kernel=args.kernel,
+                    split_blocks=args.split_blocks, stages=args.stages)
     ws = torch.empty(max(16, plan["workspace_bytes"]), dtype=torch.uint8, device=dev)
     max_ctx = b.max_context_len
     attn = pkv.paged_decode_attention if Q == 1 else pkv.spec_verify_attention
-    fused = not args.unfused
+    fused = not args.unfused and not fp8
     shape4 = (wl.batch, Q, wl.num_kv_heads, wl.head_dim)
     opts = dict(scale=wl.softmax_scale, max_context_len=max_ctx, out=out, workspace=ws,
                 kernel=args.kernel, split_blocks=args.split_blocks, stages=args.stages)
 
     def attend(qq, kn, vn, sl, tb, ln):
         """One step's cache write and attention (fused: one launch)."""
-        if fused:
+        if fp8:
+            pkv.kv_append_fp8(kn, vn, k_cache, v_cache, sl, FP8_K_SCALE, FP8_V_SCALE)
+            pkv.paged_attention_fp8(qq, k_cache, v_cache, tb, ln, FP8_K_SCALE, FP8_V_SCALE,
+                                    **opts)
+        elif fused:
             pkv.append_attention(qq, kn.view(shape4), vn.view(shape4), k_cache, v_cache, tb, ln,
                                  **opts)
         else:
@@ -334,10 +347,15 @@ def run_ours(args):
     t_host0 = time.time()
     start.record(stream)
     for i in range(K):
-        if not fused:
+        if fp8:
+            pkv.kv_append_fp8(k_new, v_new, k_cache, v_cache, slots, FP8_K_SCALE, FP8_V_SCALE)
+        elif not fused:
             pkv.kv_append(k_new, v_new, k_cache, v_cache, slots)
         ev[i][0].record(stream)
-        if fused:
+        if fp8:
+            pkv.paged_attention_fp8(q, k_cache, v_cache, table, lens, FP8_K_SCALE, FP8_V_SCALE,
+                                    **opts)
+        elif fused:
             pkv.append_attention(q, k_new.view(shape4), v_new.view(shape4), k_cache, v_cache,
                                  table, lens, **opts)
         else:
@@ -388,11 +406,12 @@ def run_ours(args):
         for _ in range(E):
             e2e_step()
         e2e_s = dist_max((time.perf_counter() - t0) / E, dev)
-        e2e = {"value": dist_sum(b.kv_bytes(), dev) / e2e_s / 1e9, "unit": "GB/s",
+        e2e = {"value": dist_sum(kv_step, dev) / e2e_s / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
                "ms_per_step": 1e3 * e2e_s}
 
-    total_kv = dist_sum(b.kv_bytes(), dev)
+    kv_step = b.kv_bytes() // W.ELT_BYTES[wl.dtype] if fp8 else b.kv_bytes()  # 1 byte / element
+    total_kv = dist_sum(kv_step, dev)
     total_tokens = dist_sum(wl.batch * Q, dev)
     if rank != 0:
         return 0
@@ -404,8 +423,9 @@ def run_ours(args):
         nblk = [-(-int(L) // wl.block_size) for L in b.context_lens]
         splits_per_seq = [max(1, -(-n // plan["split_blocks"])) for n in nblk]
     algo = accounting.attention_bytes(b.context_lens.tolist(), Q, wl.num_heads, wl.num_kv_heads,
-                                      wl.head_dim, wl.block_size, W.ELT_BYTES[wl.dtype],
-                                      splits_per_seq, fused_append=fused)
+                                      wl.head_dim, wl.block_size,
+                                      1 if fp8 else W.ELT_BYTES[wl.dtype], splits_per_seq,
+                                      fused_append=fused, q_elt_bytes=W.ELT_BYTES[wl.dtype])
     achieved = algo["total"] / (attn_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
     traffic = recorded_traffic(args.workload)
@@ -422,8 +442,13 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": workload_config(wl, b, fused),
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 cache, " + wl.dtype
+        if fp8 else wl.dtype, "data": "synthetic",
+        "config": {**workload_config(wl, b, fused),
+                   **({"kv_cache": f"fp8 e4m3, scales {FP8_K_SCALE}/{FP8_V_SCALE}",
+                       "kv_bytes_per_step": kv_step,
+                       "step": f"kv_append_fp8 of {wl.batch * Q} rows + paged_attention_fp8"}
+                      if fp8 else {})},
         "pct_of_hbm_peak": 100.0 * value / peak,
         "tokens_per_s": total_tokens / (step_ms * 1e-3),
         "attention_ms": attn_ms,
@@ -461,6 +486,8 @@ def main(argv=None):
     ap.add_argument("--merge", type=int, default=0, help="0 planner, 1 fused, 2 separate kernel")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",
+                    help="fp8: the cache in FP8 E4M3 (quantising append + fp8 attention)")
     ap.add_argument("--unfused", action="store_true",
                     help="kv_append and attention as two launches")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -84,7 +84,9 @@ typedef enum pkv_status {
   PKV_ERR_ALIGNMENT = 5    /* a tensor pointer is not 16-byte aligned */
 } pkv_status;
 
-typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
+/* Element types.  PKV_FP8_E4M3 is a cache type only (one byte per element,
+ * one float scale per cache tensor; see pkv_kv_append_fp8). */
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2, PKV_FP8_E4M3 = 3 } pkv_dtype;
 
 /* Codes the kernels record in the optional device error word. */
 enum {
@@ -294,6 +296,43 @@ PKV_API pkv_status pkv_tree_verify_attention(
     const uint64_t *tree_mask, int64_t mask_batch_stride, void *workspace,
     size_t workspace_bytes, const pkv_options *options, int32_t *error_word,
     pkv_stream_t stream);
+
+/*
+ * FP8 E4M3 KV cache.  "Inference part 2" (brunomaga), section "KV cache
+ * quantization": storing the cache in FP8 halves its size and the bytes read
+ * at each decode step; section "Number formats": E4M3 is 1 sign / 4 exponent
+ * / 3 mantissa bits, largest value 448.  Scheme (the pages leave it open):
+ * one float scale per cache tensor, element value = code value * scale.
+ *
+ * pkv_kv_append_fp8 -- quantise and write the new rows: code = e4m3 nearest
+ * to x / scale (IEEE float32 division, round to nearest even, saturating at
+ * +-448).  k_new, v_new: [num_tokens, num_kv_heads, head_dim] of src_dtype
+ * (F32/BF16/F16); caches: [num_blocks, num_kv_heads, block_size, head_dim]
+ * bytes; other arguments as for pkv_kv_append.  head_dim % 16 == 0.
+ */
+PKV_API pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache,
+                                     void *v_cache, const int64_t *slot_mapping,
+                                     int64_t num_tokens, int num_kv_heads, int head_dim,
+                                     int block_size, int64_t num_blocks, pkv_dtype src_dtype,
+                                     float k_scale, float v_scale, int32_t *error_word,
+                                     pkv_stream_t stream);
+
+/*
+ * pkv_paged_attention_fp8 -- decode (num_queries = 1) or causal verification
+ * over FP8 E4M3 caches: the attention of pkv_spec_verify_attention with every
+ * key element code * k_scale and every value element code * v_scale.  q and
+ * out are of q_dtype (F32/BF16/F16), [batch, num_queries, num_heads,
+ * head_dim]; head_dim 128 or 256.  Plans and workspace sizes: the plan and
+ * workspace functions with dtype PKV_FP8_E4M3.
+ */
+PKV_API pkv_status pkv_paged_attention_fp8(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_table, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int batch,
+    int num_queries, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, float scale, pkv_dtype q_dtype,
+    float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+    const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
 
 /*
  * pkv_read_error_word -- copy the device error word to *host_code after all

@@ -26,14 +26,17 @@ def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
 def attention_bytes(context_lens: Sequence[int], num_queries: int,
                     num_heads: int, num_kv_heads: int, head_dim: int,
                     block_size: int, elt_bytes: int, num_splits_per_seq=None,
-                    fused_append: bool = False) -> dict:
+                    fused_append: bool = False, q_elt_bytes=None) -> dict:
     """Algorithmic bytes of one paged attention call, by component.  With
     ``fused_append`` the call also reads the new K/V rows and writes them into
-    the cache (the rows it then reads are already counted in ``kv``)."""
+    the cache (the rows it then reads are already counted in ``kv``).
+    ``q_elt_bytes`` is the element size of q and out when it differs from the
+    cache's (an FP8 cache read with bf16 queries)."""
     lens = [max(0, int(x)) for x in context_lens]
     B = len(lens)
     kv = 2 * sum(lens) * num_kv_heads * head_dim * elt_bytes
-    qo = B * num_queries * num_heads * head_dim * elt_bytes
+    qe = elt_bytes if q_elt_bytes is None else q_elt_bytes
+    qo = B * num_queries * num_heads * head_dim * qe
     table = sum(-(-L // block_size) for L in lens) * 4 + B * 4
     partials = 0
     if num_splits_per_seq is not None:

@@ -26,13 +26,15 @@ DEVERR_NAMES = {0: "none", 1: "slot out of range", 2: "block id out of range",
                 3: "context length over max_context_len or the table",
                 4: "shared-memory copy timed out"}
 _DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+PKV_FP8_E4M3 = 3
 
 # Every symbol include/pkv.h declares.
 EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_plan",
             "pkv_attention_plan_for", "pkv_attention_workspace_size",
             "pkv_paged_decode_attention", "pkv_spec_verify_attention",
             "pkv_read_error_word", "pkv_paged_decode_attention_noalloc",
-            "pkv_append_attention", "pkv_tree_verify_attention")
+            "pkv_append_attention", "pkv_tree_verify_attention", "pkv_kv_append_fp8",
+            "pkv_paged_attention_fp8")
 
 
 class PkvError(RuntimeError):
@@ -104,6 +106,11 @@ def lib() -> ctypes.CDLL:
             L.pkv_tree_verify_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                                     i32, i32, i32, i32, i64, f32, i32, vp, i64,
                                                     vp, sz, opt, vp, vp]
+            L.pkv_kv_append_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32, f32,
+                                            f32, vp, vp]
+            L.pkv_paged_attention_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                                  i32, i32, i32, i64, f32, i32, f32, f32, vp, sz,
+                                                  opt, vp, vp]
             L.pkv_paged_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32,
                                                              i32, i32, i32, i32, i32, i64, f32,
                                                              i32, opt, vp, vp]
@@ -174,6 +181,14 @@ def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
         _err_ptr(error_word), _stream(k_cache)))
 
 
+def _plan_dtype(dtype) -> int:
+    """Plan/workspace element type: a torch dtype of q and cache, or
+    torch.uint8 / "fp8" for an FP8 E4M3 cache."""
+    if dtype in (torch.uint8, "fp8"):
+        return PKV_FP8_E4M3
+    return _DTYPE[dtype]
+
+
 def plan(batch: int, num_queries: int, num_heads: int, num_kv_heads: int, head_dim: int,
          max_context_len: int, dtype: torch.dtype, block_size: int = 16, kernel: int = 0,
          split_blocks: int = 0, stages: int = 0) -> dict:
@@ -181,7 +196,7 @@ def plan(batch: int, num_queries: int, num_heads: int, num_kv_heads: int, head_d
     p = Plan()
     _check("pkv_attention_plan", lib().pkv_attention_plan(
         batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
-        _DTYPE[dtype], _opts(kernel, split_blocks, stages), ctypes.byref(p)))
+        _plan_dtype(dtype), _opts(kernel, split_blocks, stages), ctypes.byref(p)))
     return p.as_dict()
 
 
@@ -192,7 +207,8 @@ def plan_for(batch: int, num_queries: int, num_heads: int, num_kv_heads: int, he
     p = Plan()
     _check("pkv_attention_plan_for", lib().pkv_attention_plan_for(
         batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
-        _DTYPE[dtype], _opts(kernel, split_blocks, stages), num_sms, ctas_per_sm, ctypes.byref(p)))
+        _plan_dtype(dtype), _opts(kernel, split_blocks, stages), num_sms, ctas_per_sm,
+        ctypes.byref(p)))
     return p.as_dict()
 
 
@@ -202,7 +218,7 @@ def workspace_size(batch: int, num_queries: int, num_heads: int, num_kv_heads: i
     n = ctypes.c_size_t(0)
     _check("pkv_attention_workspace_size", lib().pkv_attention_workspace_size(
         batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
-        _DTYPE[dtype], _opts(kernel, split_blocks, stages), ctypes.byref(n)))
+        _plan_dtype(dtype), _opts(kernel, split_blocks, stages), ctypes.byref(n)))
     return int(n.value)
 
 
@@ -373,6 +389,74 @@ def tree_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         B, Q, Hq, Hkv, D, bs, NB, float(scale), _DTYPE[q.dtype], tree_mask.data_ptr(), stride,
         ws_ptr, ws_bytes, _opts(kernel, split_blocks, stages), _err_ptr(error_word),
         _stream(q)))
+    return out
+
+
+def _fp8_cache_args(k_cache, v_cache):
+    _need(k_cache.is_cuda and v_cache.is_cuda and k_cache.dim() == 4
+          and k_cache.shape == v_cache.shape and k_cache.dtype == torch.uint8
+          and v_cache.dtype == torch.uint8 and k_cache.is_contiguous() and v_cache.is_contiguous(),
+          "FP8 caches: contiguous CUDA uint8 [num_blocks, num_kv_heads, block_size, head_dim]")
+    return k_cache.shape
+
+
+def kv_append_fp8(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                  v_scale: float, error_word: Optional[torch.Tensor] = None) -> None:
+    """Quantise k_new/v_new [T, Hkv, D] (float32/bf16/f16) to e4m3 codes in the
+    uint8 caches at their slots (pkv_kv_append_fp8)."""
+    NB, Hkv, bs, D = _fp8_cache_args(k_cache, v_cache)
+    T = k_new.shape[0]
+    _need(k_new.shape == (T, Hkv, D) and v_new.shape == (T, Hkv, D)
+          and k_new.dtype == v_new.dtype and k_new.dtype in _DTYPE
+          and k_new.is_contiguous() and v_new.is_contiguous(), "k_new/v_new [T, Hkv, D]")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.shape == (T,)
+          and slot_mapping.is_cuda and slot_mapping.is_contiguous(), "slot_mapping int64 [T]")
+    _check("pkv_kv_append_fp8", lib().pkv_kv_append_fp8(
+        k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        slot_mapping.data_ptr(), T, Hkv, D, bs, NB, _DTYPE[k_new.dtype], float(k_scale),
+        float(v_scale), _err_ptr(error_word), _stream(k_cache)))
+
+
+def paged_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        block_table: torch.Tensor, context_lens: torch.Tensor, k_scale: float,
+                        v_scale: float, scale: Optional[float] = None,
+                        max_context_len: Optional[int] = None,
+                        out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, kernel: int = 0,
+                        split_blocks: int = 0, error_word: Optional[torch.Tensor] = None,
+                        stages: int = 0) -> torch.Tensor:
+    """Decode (q [B, Hq, D]) or causal verification (q [B, Q, Hq, D]) over
+    e4m3 caches (pkv_paged_attention_fp8); out has q's shape and type."""
+    NB, Hkv, bs, D = _fp8_cache_args(k_cache, v_cache)
+    q4 = q if q.dim() == 4 else q.unsqueeze(1)
+    B, Q, Hq, _ = q4.shape
+    _need(q.is_cuda and q.is_contiguous() and q.dtype in _DTYPE and q.shape[-1] == D, "q")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2
+          and block_table.shape[0] == B and block_table.is_contiguous() and block_table.is_cuda,
+          "block_table must be a contiguous CUDA int32 [batch, max_blocks_per_seq]")
+    _need(context_lens.dtype == torch.int32 and context_lens.shape == (B,)
+          and context_lens.is_cuda and context_lens.is_contiguous(), "context_lens")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0  # device read
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
+    n = ctypes.c_size_t(0)
+    _check("pkv_attention_workspace_size", lib().pkv_attention_workspace_size(
+        B, Q, Hq, Hkv, D, bs, max_context_len, PKV_FP8_E4M3, _opts(kernel, split_blocks, stages),
+        ctypes.byref(n)))
+    if n.value and workspace is None:
+        workspace = torch.empty(n.value, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("pkv_paged_attention_fp8", lib().pkv_paged_attention_fp8(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_table.data_ptr(), block_table.shape[1], context_lens.data_ptr(), max_context_len,
+        B, Q, Hq, Hkv, D, bs, NB, float(scale), _DTYPE[q.dtype], float(k_scale), float(v_scale),
+        ws_ptr, ws_bytes, _opts(kernel, split_blocks, stages), _err_ptr(error_word), _stream(q)))
     return out
 
 

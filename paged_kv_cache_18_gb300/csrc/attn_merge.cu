@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   float total = 0.f;
 #pragma unroll
   for (int w = 0; w < kMergeWarps; ++w) total += red_sum[w];
-  const float inv = total > 0.f ? 1.f / total : 0.f;
+  const float inv = total > 0.f ? p.out_scale / total : 0.f;
   T *dst = reinterpret_cast<T *>(p.out) + row * D;
   for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) {
     float x = 0.f;

@@ -1,386 +1,55 @@
-// attn_simt.cu -- paged decode / speculative-verify attention with CUDA-core
-// dot products (float32, bfloat16 and float16 caches).
-//
-// Same work split as the tensor-core kernel: one CTA per (sequence, KV head,
-// row chunk, split) serving the R query rows that share the KV head, each
-// warp owning every W-th block of the split with its own ring of NS stages.
-// A block's K tile and V tile (each one contiguous run of 16 rows) arrive by
-// one 1-D bulk copy each (cp.async.bulk, completion on an mbarrier), from the
-// physical block the table names ("Inference part 1", section
-// "PagedAttention").
-//
-// Lane layout: the 32 lanes form 4 row groups of 8 lanes; a row group takes
-// rows g, g + 4, g + 8, g + 12 of the block, and each of its 8 lanes holds
-// every 8th 16-byte vector of the row (128 contiguous bytes per quarter warp:
-// no bank conflicts).  Scores are reduced over the 8 lanes with shuffles; the
-// online softmax ("Inference part 1", section "FlashAttention", m / l / O
-// recurrence, in log2 units) runs per row group over 4 rows at a time, and
-// the 4 row groups and W warps are merged at the end like chunks of
-// Flash-Decoding.  Rows past the context are skipped entirely, so NaN-filled
-// unused rows never reach the output.
-#include "pkv_device.cuh"
-#include "pkv_internal.h"
+// attn_simt.cu -- CUDA-core attention for float32, bfloat16 and float16
+// caches (q, cache and output of one type); the kernel is in attn_simt.cuh.
+#include "attn_simt.cuh"
 
 namespace pkv {
-namespace {
-
-template <typename T> __device__ __forceinline__ void vec_to_float(const uint4 &v, float *f);
-template <> __device__ __forceinline__ void vec_to_float<float>(const uint4 &v, float *f) {
-  f[0] = __uint_as_float(v.x);
-  f[1] = __uint_as_float(v.y);
-  f[2] = __uint_as_float(v.z);
-  f[3] = __uint_as_float(v.w);
-}
-template <> __device__ __forceinline__ void vec_to_float<__nv_bfloat16>(const uint4 &v, float *f) {
-  unpack2<__nv_bfloat16>(v.x, f[0], f[1]);
-  unpack2<__nv_bfloat16>(v.y, f[2], f[3]);
-  unpack2<__nv_bfloat16>(v.z, f[4], f[5]);
-  unpack2<__nv_bfloat16>(v.w, f[6], f[7]);
-}
-template <> __device__ __forceinline__ void vec_to_float<__half>(const uint4 &v, float *f) {
-  unpack2<__half>(v.x, f[0], f[1]);
-  unpack2<__half>(v.y, f[2], f[3]);
-  unpack2<__half>(v.z, f[4], f[5]);
-  unpack2<__half>(v.w, f[6], f[7]);
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-template <typename T, int D, int R, int W, int NS>
-__global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
-  constexpr int ELT = Elt<T>::bytes;
-  constexpr int RB = D * ELT;             // bytes of one row
-  constexpr int TILE = kBlockSize * RB;   // bytes of one (block, kv head) tile
-  constexpr int STAGE = 2 * TILE;
-  constexpr int VPL = RB / 128;           // 16-byte vectors per lane per row
-  constexpr int EV = 16 / ELT;            // elements per vector
-  constexpr int EPL = VPL * EV;           // elements per lane per row (= D / 8)
-  static_assert(RB % 128 == 0, "row must be a multiple of 128 bytes");
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-  const uint32_t smem_base = smem_u32(smem);
-  const uint32_t bar_base = smem_base + W * NS * STAGE;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rg = lane >> 3, t = lane & 7;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / p.row_chunks;
-  const int chunk = blockIdx.y - kvh * p.row_chunks;
-  const int b = blockIdx.z;
-
-  const SeqExtent ext = seq_extent(p, b, split == 0 && chunk == 0 && kvh == 0 &&
-                                             threadIdx.x == 0);
-  const int L = ext.L;
-  const int blk_begin = split * p.split_blocks;
-  if (split > 0 && blk_begin >= ext.nblk) return;
-  const int blk_end = min(blk_begin + p.split_blocks, ext.nblk);
-  const int ns_b = max(1, min(p.num_splits, (ext.nblk + p.split_blocks - 1) / p.split_blocks));
-  const int nspan = max(blk_end - blk_begin, 0);
-  const int n_my = nspan > warp ? (nspan - warp + W - 1) / W : 0;
-
-  // Query rows in registers (this lane's slice of the head dim).
-  float qv[R][EPL];
-  int lim[R];
-  unsigned long long tm[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int64_t row = cta_row_index(p, b, kvh, chunk, r);
-    lim[r] = row < 0 ? -1 : cta_row_limit(p, L, chunk, r);
-    tm[r] = cta_row_tree_mask(p, b, chunk, r);
-    const uint8_t *qrow = reinterpret_cast<const uint8_t *>(p.q) + (row < 0 ? 0 : row) * RB;
-#pragma unroll
-    for (int cv = 0; cv < VPL; ++cv) {
-      uint4 v = row < 0 ? make_uint4(0, 0, 0, 0)
-                        : *reinterpret_cast<const uint4 *>(qrow + (t + 8 * cv) * 16);
-      vec_to_float<T>(v, &qv[r][cv * EV]);
-    }
-  }
-
-  float acc[R][EPL];
-  float m[R], l[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[r][e] = 0.f;
-  }
-
-  const uint32_t my_bars = bar_base + warp * NS * 8;
-  const uint32_t my_stages = smem_base + warp * NS * STAGE;
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < NS; ++s) mbar_init(my_bars + 8 * s, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  const int32_t *table = p.block_table + static_cast<int64_t>(b) * p.max_blocks_per_seq +
-                         blk_begin + warp;
-  auto load_entries = [&](int chunk32) -> int {
-    const int i = chunk32 * 32 + lane;
-    return i < n_my ? __ldg(table + static_cast<int64_t>(i) * W) : -1;
-  };
-  int tab_cur = load_entries(0);
-  int tab_next = load_entries(1);
-  uint32_t bad_mask = 0;
-  const uint8_t *kbase = reinterpret_cast<const uint8_t *>(p.k_cache);
-  const uint8_t *vbase = reinterpret_cast<const uint8_t *>(p.v_cache);
-
-  auto issue = [&](int i) {
-    if ((i & 31) == 0 && i > 0) {
-      tab_cur = tab_next;
-      tab_next = load_entries((i >> 5) + 1);
-    }
-    const int v = __shfl_sync(kFull, tab_cur, i & 31);
-    const bool bad = v < 0 || static_cast<int64_t>(v) >= p.num_blocks;
-    bad_mask = bad ? (bad_mask | (1u << (i & 31))) : (bad_mask & ~(1u << (i & 31)));
-    if (lane == 0) {
-      if (bad) record_error(p.err, PKV_DEVERR_BLOCK_ID);
-      const int64_t phys = bad ? 0 : v;
-      const int64_t off = (phys * p.num_kv_heads + kvh) * static_cast<int64_t>(TILE);
-      const int s = i % NS;
-      const uint32_t bar = my_bars + 8 * s;
-      const uint32_t st = my_stages + s * STAGE;
-      mbar_arrive_expect_tx(bar, STAGE);
-      bulk_g2s(st, kbase + off, TILE, bar);
-      bulk_g2s(st + TILE, vbase + off, TILE, bar);
-    }
-  };
-
-  const int npre = min(NS, n_my);
-  for (int i = 0; i < npre; ++i) issue(i);
-  int issued = npre;
-
-  bool timed_out = false;
-  int landed = 0;
-  for (int i = 0; i < n_my; ++i) {
-    const int s = i % NS;
-    if (!mbar_wait_bounded(my_bars + 8 * s, (i / NS) & 1)) {
-      timed_out = true;
-      landed = i;
-      break;
-    }
-    const uint32_t ktile = my_stages + s * STAGE;
-    const uint32_t vtile = ktile + TILE;
-    const int key0 = (blk_begin + warp + i * W) * kBlockSize;
-    const bool bad = (bad_mask >> (i & 31)) & 1u;
-    if (p.k_new != nullptr && !bad && key0 + kBlockSize > L - p.num_queries) {
-      const int64_t phys = __ldg(table + static_cast<int64_t>(i) * W);
-      patch_new_rows<D, ELT>(p, ktile, vtile, b, kvh, key0, L, phys, chunk == 0,
-                             [](int r, int vec) { return static_cast<uint32_t>(r * RB + vec * 16); });
-    }
-
-    // Scores of rows rg, rg+4, rg+8, rg+12 for every query row.
-    float sc[4][R];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int row = rg + 4 * k;
-      float kf[EPL];
-#pragma unroll
-      for (int cv = 0; cv < VPL; ++cv)
-        vec_to_float<T>(lds128(ktile + row * RB + (t + 8 * cv) * 16), &kf[cv * EV]);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float d = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) d = fmaf(qv[r][e], kf[e], d);
-        d += __shfl_xor_sync(kFull, d, 1);
-        d += __shfl_xor_sync(kFull, d, 2);
-        d += __shfl_xor_sync(kFull, d, 4);
-        const bool vis = lim[r] >= 0 && key_visible(p, key0 + row, L, bad, lim[r], tm[r]);
-        sc[k][r] = vis ? d * p.scale_log2 : -INFINITY;
-      }
-    }
-    // Online softmax over these 4 rows.
-    float pw[4][R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float mx = fmaxf(fmaxf(sc[0][r], sc[1][r]), fmaxf(sc[2][r], sc[3][r]));
-      const float m_new = fmaxf(m[r], mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float corr = ex2(m[r] - m_use);
-      float sum = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        pw[k][r] = ex2(sc[k][r] - m_use);
-        sum += pw[k][r];
-      }
-      l[r] = l[r] * corr + sum;
-      m[r] = m_new;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[r][e] *= corr;
-    }
-    // P V over the rows that exist.
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int row = rg + 4 * k;
-      if (!bad && key0 + row < L) {
-        float vf[EPL];
-#pragma unroll
-        for (int cv = 0; cv < VPL; ++cv)
-          vec_to_float<T>(lds128(vtile + row * RB + (t + 8 * cv) * 16), &vf[cv * EV]);
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[r][e] = fmaf(pw[k][r], vf[e], acc[r][e]);
-      }
-    }
-    __syncwarp();
-    if (i + NS < n_my) {
-      issue(i + NS);
-      ++issued;
-    }
-  }
-  if (timed_out) {
-    if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT);
-    for (int k = landed; k < issued; ++k) mbar_wait_bounded(my_bars + 8 * (k % NS), (k / NS) & 1);
-  }
-
-  // Merge the 4 row groups of the warp (lanes t, t+8, t+16, t+24).
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    float M = fmaxf(m[r], __shfl_xor_sync(kFull, m[r], 8));
-    M = fmaxf(M, __shfl_xor_sync(kFull, M, 16));
-    const float s = ex2(m[r] - ((M == -INFINITY) ? 0.f : M));
-    float lv = l[r] * s;
-    lv += __shfl_xor_sync(kFull, lv, 8);
-    lv += __shfl_xor_sync(kFull, lv, 16);
-    l[r] = lv;
-    m[r] = M;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      float a = acc[r][e] * s;
-      a += __shfl_xor_sync(kFull, a, 8);
-      a += __shfl_xor_sync(kFull, a, 16);
-      acc[r][e] = a;
-    }
-  }
-
-  __syncthreads();
-  constexpr int NC = R;
-  constexpr int DP = D + 4;
-  float *red_o = reinterpret_cast<float *>(smem);
-  float *red_m = red_o + W * NC * DP;
-  float *red_l = red_m + W * NC;
-  float *wscale = red_l + W * NC;
-  if (rg == 0) {
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-#pragma unroll
-      for (int cv = 0; cv < VPL; ++cv)
-#pragma unroll
-        for (int e = 0; e < EV; ++e)
-          red_o[(warp * NC + r) * DP + (t + 8 * cv) * EV + e] = acc[r][cv * EV + e];
-      if (t == 0) {
-        red_m[warp * NC + r] = m[r];
-        red_l[warp * NC + r] = l[r];
-      }
-    }
-  }
-  __syncthreads();
-  cta_epilogue<T, D, NC, W, W * 32>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split, ns_b);
-}
-
-constexpr int kSimtWarps = 4;
-
-// Stages per warp: about 32 KB of K/V tiles per warp, between 1 and 3.
-template <typename T, int D>
-constexpr int simt_stages() {
-  constexpr int stage = 2 * kBlockSize * D * Elt<T>::bytes;
-  return (32768 / stage) < 1 ? 1 : ((32768 / stage) > 3 ? 3 : (32768 / stage));
-}
-
-template <typename T, int D, int R>
-constexpr size_t simt_smem_bytes() {
-  constexpr int kSimtStages = simt_stages<T, D>();
-  constexpr size_t stages = size_t(kSimtWarps) * kSimtStages * 2 * kBlockSize * D * Elt<T>::bytes;
-  constexpr size_t red = (size_t(kSimtWarps) * R * (D + 4) + size_t(3 * kSimtWarps + 2) * R) * 4;
-  static_assert(red <= stages, "epilogue scratch must fit in the stage memory");
-  return stages + size_t(kSimtWarps) * kSimtStages * 8 + 128;
-}
-
-template <typename T, int D, int R>
-KernelInfo simt_info_t() {
-  KernelInfo k;
-  k.func = reinterpret_cast<const void *>(&attn_simt_kernel<T, D, R, kSimtWarps, simt_stages<T, D>()>);
-  k.threads = kSimtWarps * 32;
-  k.smem = simt_smem_bytes<T, D, R>();
-  k.warps = kSimtWarps;
-  k.stages = simt_stages<T, D>();
-  return k;
-}
-
-template <typename T, int D, int R>
-cudaError_t simt_launch_t(const AttnParams &p, dim3 grid, cudaStream_t stream) {
-  const KernelInfo k = simt_info_t<T, D, R>();
-  attn_simt_kernel<T, D, R, kSimtWarps, simt_stages<T, D>()><<<grid, k.threads, k.smem, stream>>>(p);
-  return cudaGetLastError();
-}
-
-using SimtLaunch = cudaError_t (*)(const AttnParams &, dim3, cudaStream_t);
-
-template <typename T, int D>
-bool simt_pick(int r, KernelInfo *info, SimtLaunch *launch) {
-  // R * D / 8 registers of query and of accumulator per lane: keep <= 64 each.
-  switch (r) {
-    case 1: *info = simt_info_t<T, D, 1>(); *launch = &simt_launch_t<T, D, 1>; return true;
-    case 2: *info = simt_info_t<T, D, 2>(); *launch = &simt_launch_t<T, D, 2>; return true;
-    case 4:
-      if (D > 128) return false;
-      *info = simt_info_t<T, D, (D > 128 ? 1 : 4)>();
-      *launch = &simt_launch_t<T, D, (D > 128 ? 1 : 4)>;
-      return true;
-    case 8:
-      if (D > 64) return false;
-      *info = simt_info_t<T, D, (D > 64 ? 1 : 8)>();
-      *launch = &simt_launch_t<T, D, (D > 64 ? 1 : 8)>;
-      return true;
-    default: return false;
-  }
-}
+namespace simt {
 
 template <typename T>
-bool simt_pick_d(int D, int r, KernelInfo *info, SimtLaunch *launch) {
+bool pick_d(int D, int r, KernelInfo *info, SimtLaunch *launch) {
   switch (D) {
-    case 64: return simt_pick<T, 64>(r, info, launch);
-    case 128: return simt_pick<T, 128>(r, info, launch);
-    case 256: return simt_pick<T, 256>(r, info, launch);
+    case 64: return simt_pick<T, T, 64>(r, info, launch);
+    case 128: return simt_pick<T, T, 128>(r, info, launch);
+    case 256: return simt_pick<T, T, 256>(r, info, launch);
     default: return false;
   }
 }
 
-bool simt_pick_any(pkv_dtype dt, int D, int r, KernelInfo *info, SimtLaunch *launch) {
+bool pick_same(pkv_dtype dt, int D, int r, KernelInfo *info, SimtLaunch *launch) {
   switch (dt) {
-    case PKV_F32: return simt_pick_d<float>(D, r, info, launch);
-    case PKV_BF16: return simt_pick_d<__nv_bfloat16>(D, r, info, launch);
-    case PKV_F16: return simt_pick_d<__half>(D, r, info, launch);
+    case PKV_F32: return pick_d<float>(D, r, info, launch);
+    case PKV_BF16: return pick_d<__nv_bfloat16>(D, r, info, launch);
+    case PKV_F16: return pick_d<__half>(D, r, info, launch);
     default: return false;
   }
 }
 
-}  // namespace
+// FP8 caches (attn_simt_fp8.cu).
+bool pick_fp8(pkv_dtype q_dtype, int D, int r, KernelInfo *info, SimtLaunch *launch);
+
+bool pick(pkv_dtype cache_dtype, pkv_dtype q_dtype, int D, int r, KernelInfo *info,
+          SimtLaunch *launch) {
+  if (cache_dtype == PKV_FP8_E4M3) return pick_fp8(q_dtype, D, r, info, launch);
+  if (q_dtype != cache_dtype) return false;
+  return pick_same(cache_dtype, D, r, info, launch);
+}
+
+}  // namespace simt
 
 int simt_max_rows(int head_dim) { return head_dim <= 64 ? 8 : (head_dim <= 128 ? 4 : 2); }
 
-bool simt_kernel_info(pkv_dtype dtype, int head_dim, int rows, KernelInfo *info) {
-  SimtLaunch launch = nullptr;
-  return simt_pick_any(dtype, head_dim, rows, info, &launch);
+bool simt_kernel_info(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int rows,
+                      KernelInfo *info) {
+  simt::SimtLaunch launch = nullptr;
+  return simt::pick(cache_dtype, q_dtype, head_dim, rows, info, &launch);
 }
 
-cudaError_t simt_launch(pkv_dtype dtype, int head_dim, int rows, const AttnParams &p, dim3 grid,
-                        cudaStream_t stream) {
+cudaError_t simt_launch(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int rows,
+                        const AttnParams &p, dim3 grid, cudaStream_t stream) {
   KernelInfo info;
-  SimtLaunch launch = nullptr;
-  if (!simt_pick_any(dtype, head_dim, rows, &info, &launch)) return cudaErrorInvalidValue;
+  simt::SimtLaunch launch = nullptr;
+  if (!simt::pick(cache_dtype, q_dtype, head_dim, rows, &info, &launch))
+    return cudaErrorInvalidValue;
   return launch(p, grid, stream);
 }
 

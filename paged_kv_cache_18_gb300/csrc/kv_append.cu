@@ -61,3 +61,119 @@ cudaError_t append_launch(const void *k_new, const void *v_new, void *k_cache, v
 }
 
 }  // namespace pkv
+
+// ---- FP8 E4M3 caches ------------------------------------------------------
+// Quantised append ("Inference part 2", section "KV cache quantization": the
+// cache is stored in FP8): each element becomes the e4m3 code nearest to
+// x / scale (IEEE float32 division, round to nearest even, saturating at
+// +-448).  One thread per 16 elements (one 16-byte store).
+#include <cuda_fp8.h>
+
+namespace pkv {
+namespace {
+
+template <typename TS> __device__ __forceinline__ float src_float(const TS *p, int64_t i);
+template <> __device__ __forceinline__ float src_float<float>(const float *p, int64_t i) {
+  return p[i];
+}
+template <> __device__ __forceinline__ float src_float<__nv_bfloat16>(const __nv_bfloat16 *p,
+                                                                     int64_t i) {
+  return __bfloat162float(p[i]);
+}
+template <> __device__ __forceinline__ float src_float<__half>(const __half *p, int64_t i) {
+  return __half2float(p[i]);
+}
+
+template <typename TS>
+__device__ __forceinline__ uint4 quantise16(const TS *src, int64_t base, float scale) {
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const int64_t e = base + k * 4 + pr * 2;
+      const float2 f = make_float2(__fdiv_rn(src_float<TS>(src, e), scale),
+                                   __fdiv_rn(src_float<TS>(src, e + 1), scale));
+      const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      word |= static_cast<uint32_t>(c) << (16 * pr);
+    }
+    w[k] = word;
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename TS>
+__global__ void __launch_bounds__(256)
+    kv_append_fp8_kernel(const TS *__restrict__ k_new, const TS *__restrict__ v_new,
+                         uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                         const int64_t *__restrict__ slots, int64_t num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, float k_scale,
+                         float v_scale, int32_t *err) {
+  const int vpr = head_dim / 16;  // 16-byte code vectors per row
+  const int64_t per_token = static_cast<int64_t>(num_kv_heads) * vpr;
+  const int64_t total = num_tokens * per_token;
+  const int64_t capacity = num_blocks * block_size;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = idx / per_token;
+    const int64_t rem = idx - t * per_token;
+    const int h = static_cast<int>(rem / vpr);
+    const int v = static_cast<int>(rem - static_cast<int64_t>(h) * vpr);
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;
+    if (slot >= capacity) {
+      if (rem == 0) record_error(err, PKV_DEVERR_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / block_size;
+    const int64_t off = slot - blk * block_size;
+    const int64_t src = ((t * num_kv_heads + h) * head_dim) + v * 16;
+    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * vpr + v;
+    k_cache[dst] = quantise16<TS>(k_new, src, k_scale);
+    v_cache[dst] = quantise16<TS>(v_new, src, v_scale);
+  }
+}
+
+template <typename TS>
+cudaError_t append_fp8_t(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         const int64_t *slots, int64_t num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, float k_scale,
+                         float v_scale, int32_t *err, int sm_count, cudaStream_t stream) {
+  const int64_t total = num_tokens * num_kv_heads * static_cast<int64_t>(head_dim / 16);
+  if (total == 0) return cudaSuccess;
+  int64_t ctas = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  if (ctas > cap) ctas = cap;
+  kv_append_fp8_kernel<TS><<<static_cast<unsigned>(ctas), 256, 0, stream>>>(
+      static_cast<const TS *>(k_new), static_cast<const TS *>(v_new),
+      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slots, num_tokens,
+      num_kv_heads, head_dim, block_size, num_blocks, k_scale, v_scale, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t append_fp8_launch(pkv_dtype src_dtype, const void *k_new, const void *v_new,
+                              void *k_cache, void *v_cache, const int64_t *slots,
+                              int64_t num_tokens, int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, float k_scale, float v_scale, int32_t *err,
+                              int sm_count, cudaStream_t stream) {
+  switch (src_dtype) {
+    case PKV_F32:
+      return append_fp8_t<float>(k_new, v_new, k_cache, v_cache, slots, num_tokens, num_kv_heads,
+                                 head_dim, block_size, num_blocks, k_scale, v_scale, err,
+                                 sm_count, stream);
+    case PKV_BF16:
+      return append_fp8_t<__nv_bfloat16>(k_new, v_new, k_cache, v_cache, slots, num_tokens,
+                                         num_kv_heads, head_dim, block_size, num_blocks, k_scale,
+                                         v_scale, err, sm_count, stream);
+    case PKV_F16:
+      return append_fp8_t<__half>(k_new, v_new, k_cache, v_cache, slots, num_tokens, num_kv_heads,
+                                  head_dim, block_size, num_blocks, k_scale, v_scale, err,
+                                  sm_count, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

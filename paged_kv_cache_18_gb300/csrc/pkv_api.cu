@@ -27,9 +27,11 @@ constexpr size_t kUsableSmemPerSm = 228 * 1024;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int elt_bytes(pkv_dtype dt) { return dt == PKV_F32 ? 4 : 2; }
+int elt_bytes(pkv_dtype dt) { return dt == PKV_F32 ? 4 : (dt == PKV_FP8_E4M3 ? 1 : 2); }
 
 bool valid_dtype(int dt) { return dt == PKV_F32 || dt == PKV_BF16 || dt == PKV_F16; }
+
+bool valid_cache_dtype(int dt) { return valid_dtype(dt) || dt == PKV_FP8_E4M3; }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -89,15 +91,30 @@ cudaError_t prepare_kernel(const KernelInfo &k, int device, int *ctas_per_sm) {
   return cudaSuccess;
 }
 
+// dtype is the cache's element type, qdtype that of q and out (equal unless
+// the cache is FP8 E4M3).
 struct Shape {
   int batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_context_len;
   pkv_dtype dtype;
+  pkv_dtype qdtype;
 };
+
+Shape make_shape(int batch, int num_queries, int num_heads, int num_kv_heads, int head_dim,
+                 int block_size, int max_context_len, pkv_dtype dtype) {
+  // Plans over an FP8 cache do not depend on q's type.
+  const pkv_dtype q = dtype == PKV_FP8_E4M3 ? PKV_BF16 : dtype;
+  return Shape{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+               max_context_len, dtype, q};
+}
 
 pkv_status check_shape(const Shape &s) {
   if (s.batch < 0 || s.num_queries < 1 || s.num_heads < 1 || s.num_kv_heads < 1 ||
-      s.head_dim < 1 || s.block_size < 1 || s.max_context_len < 0 || !valid_dtype(s.dtype))
+      s.head_dim < 1 || s.block_size < 1 || s.max_context_len < 0 ||
+      !valid_cache_dtype(s.dtype) || !valid_dtype(s.qdtype))
     return PKV_ERR_INVALID_ARG;
+  if (s.dtype != PKV_FP8_E4M3 && s.qdtype != s.dtype) return PKV_ERR_INVALID_ARG;
+  if (s.dtype == PKV_FP8_E4M3 && s.head_dim != 128 && s.head_dim != 256)
+    return PKV_ERR_UNSUPPORTED;
   if (s.num_heads % s.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (s.head_dim != 64 && s.head_dim != 128 && s.head_dim != 256) return PKV_ERR_UNSUPPORTED;
   if (s.block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
@@ -113,8 +130,8 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
   // head (0.995 of the HBM peak on the 40-head, 2048-row bf16 layer, against
   // 0.974 for the CUDA-core kernel); float32 has no exact tensor-core path.
   if (kernel == PKV_KERNEL_AUTO)
-    kernel = (s.dtype == PKV_F32) ? PKV_KERNEL_SIMT : PKV_KERNEL_MMA;
-  if (kernel == PKV_KERNEL_MMA && s.dtype == PKV_F32) return false;
+    kernel = (s.dtype == PKV_F32 || s.dtype == PKV_FP8_E4M3) ? PKV_KERNEL_SIMT : PKV_KERNEL_MMA;
+  if (kernel == PKV_KERNEL_MMA && (s.dtype == PKV_F32 || s.dtype == PKV_FP8_E4M3)) return false;
   if (kernel != PKV_KERNEL_MMA && kernel != PKV_KERNEL_SIMT) return false;
   int cap = kernel == PKV_KERNEL_MMA ? 8 * mma_max_tiles(s.head_dim)
                                      : simt_max_rows(s.head_dim);
@@ -129,7 +146,7 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
     if (stages != 0) return false;
     int r = 1;
     while (r < per_cta) r <<= 1;
-    ok = simt_kernel_info(s.dtype, s.head_dim, r, info);
+    ok = simt_kernel_info(s.dtype, s.qdtype, s.head_dim, r, info);
   }
   if (!ok) return false;
   pl->kernel = kernel;
@@ -297,9 +314,11 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
                          float scale, void *workspace, size_t workspace_bytes,
                          const pkv_options *opt, int32_t *error_word, cudaStream_t stream,
                          const void *k_new = nullptr, const void *v_new = nullptr,
-                         const uint64_t *tree_mask = nullptr, int64_t mask_stride = 0) {
+                         const uint64_t *tree_mask = nullptr, int64_t mask_stride = 0,
+                         float k_scale = 1.f, float v_scale = 1.f) {
   pkv_status st = check_shape(s);
   if (st != PKV_OK) return st;
+  if (k_new && s.dtype == PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
   if (s.batch == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens)
     return PKV_ERR_INVALID_ARG;
@@ -349,7 +368,9 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   p.max_context_len = s.max_context_len;
   p.split_blocks = pl.split_blocks;
   p.num_splits = pl.num_splits;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale_log2 =
+      static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * k_scale);
+  p.out_scale = v_scale;
   bool merge_kernel = false;
   if (pl.num_splits > 1) {
     const WorkspaceLayout w = workspace_layout(s, pl.num_splits, pl.row_chunks, pl.rows_per_cta,
@@ -379,11 +400,11 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   } else {
     int r = 1;
     while (r < pl.rows_per_cta) r <<= 1;
-    e = simt_launch(s.dtype, s.head_dim, r, p, grid, stream);
+    e = simt_launch(s.dtype, s.qdtype, s.head_dim, r, p, grid, stream);
   }
   if (e != cudaSuccess) return PKV_ERR_CUDA;
   if (merge_kernel) {
-    e = merge_launch(s.dtype, s.head_dim, p, sms, stream);
+    e = merge_launch(s.qdtype, s.head_dim, p, sms, stream);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
@@ -438,8 +459,8 @@ pkv_status pkv_attention_plan_for(int batch, int num_queries, int num_heads, int
                                   pkv_dtype dtype, const pkv_options *options, int num_sms,
                                   int ctas_per_sm, pkv_plan *plan) {
   if (!plan || num_sms < 1 || ctas_per_sm < 0) return PKV_ERR_INVALID_ARG;
-  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
-                max_context_len, dtype};
+  const Shape s = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype);
   pkv_plan pl{};
   KernelInfo info;
   const pkv_status st = make_plan(s, options, num_sms, ctas_per_sm, &pl, &info);
@@ -451,8 +472,8 @@ pkv_status pkv_attention_plan(int batch, int num_queries, int num_heads, int num
                               int head_dim, int block_size, int max_context_len, pkv_dtype dtype,
                               const pkv_options *options, pkv_plan *plan) {
   if (!plan) return PKV_ERR_INVALID_ARG;
-  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
-                max_context_len, dtype};
+  const Shape s = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype);
   pkv_plan pl{};
   KernelInfo info;
   int device = 0, sms = 0;
@@ -482,7 +503,8 @@ pkv_status pkv_paged_decode_attention(void *out, const void *q, const void *k_ca
                                       void *workspace, size_t workspace_bytes,
                                       const pkv_options *options, int32_t *error_word,
                                       pkv_stream_t stream) {
-  const Shape s{batch, 1, num_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype};
+  if (dtype == PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;  // pkv_paged_attention_fp8
+  const Shape s = make_shape(batch, 1, num_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype);
   return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
                        num_blocks, scale, workspace, workspace_bytes, options, error_word,
                        reinterpret_cast<cudaStream_t>(stream));
@@ -497,8 +519,9 @@ pkv_status pkv_spec_verify_attention(void *out, const void *q, const void *k_cac
                                      pkv_dtype dtype, void *workspace, size_t workspace_bytes,
                                      const pkv_options *options, int32_t *error_word,
                                      pkv_stream_t stream) {
-  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
-                max_context_len, dtype};
+  if (dtype == PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;  // pkv_paged_attention_fp8
+  const Shape s = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype);
   return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
                        num_blocks, scale, workspace, workspace_bytes, options, error_word,
                        reinterpret_cast<cudaStream_t>(stream));
@@ -512,9 +535,10 @@ pkv_status pkv_append_attention(void *out, const void *q, const void *k_new, con
                                 float scale, pkv_dtype dtype, void *workspace,
                                 size_t workspace_bytes, const pkv_options *options,
                                 int32_t *error_word, pkv_stream_t stream) {
+  if (dtype == PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;  // pkv_paged_attention_fp8
   if (batch > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
-  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
-                max_context_len, dtype};
+  const Shape s = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype);
   return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
                        num_blocks, scale, workspace, workspace_bytes, options, error_word,
                        reinterpret_cast<cudaStream_t>(stream), k_new, v_new);
@@ -530,15 +554,61 @@ pkv_status pkv_tree_verify_attention(void *out, const void *q, const void *k_cac
                                      int64_t mask_batch_stride, void *workspace,
                                      size_t workspace_bytes, const pkv_options *options,
                                      int32_t *error_word, pkv_stream_t stream) {
+  if (dtype == PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;  // pkv_paged_attention_fp8
   if (num_queries > 64 || mask_batch_stride < 0) return PKV_ERR_INVALID_ARG;
   if (batch > 0 && !tree_mask) return PKV_ERR_INVALID_ARG;
   if (!aligned(tree_mask, 8)) return PKV_ERR_ALIGNMENT;
-  const Shape s{batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
-                max_context_len, dtype};
+  const Shape s = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                max_context_len, dtype);
   return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
                        num_blocks, scale, workspace, workspace_bytes, options, error_word,
                        reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, tree_mask,
                        mask_batch_stride);
+}
+
+pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks,
+                             pkv_dtype src_dtype, float k_scale, float v_scale,
+                             int32_t *error_word, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || num_blocks < 1 ||
+      !valid_dtype(src_dtype) || !(k_scale > 0.f) || !(v_scale > 0.f) ||
+      !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (head_dim % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(slot_mapping, 8) || (error_word && !aligned(error_word, 4)))
+    return PKV_ERR_ALIGNMENT;
+  int device = 0, sms = 0;
+  if (current_sm_count(&device, &sms) != cudaSuccess) return PKV_ERR_CUDA;
+  const cudaError_t e = append_fp8_launch(src_dtype, k_new, v_new, k_cache, v_cache, slot_mapping,
+                                          num_tokens, num_kv_heads, head_dim, block_size,
+                                          num_blocks, k_scale, v_scale, error_word, sms,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_paged_attention_fp8(void *out, const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_table,
+                                   int max_blocks_per_seq, const int32_t *context_lens,
+                                   int max_context_len, int batch, int num_queries, int num_heads,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int64_t num_blocks, float scale, pkv_dtype q_dtype,
+                                   float k_scale, float v_scale, void *workspace,
+                                   size_t workspace_bytes, const pkv_options *options,
+                                   int32_t *error_word, pkv_stream_t stream) {
+  if (!valid_dtype(q_dtype) || !(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
+      !std::isfinite(v_scale))
+    return PKV_ERR_INVALID_ARG;
+  Shape s = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                       max_context_len, PKV_FP8_E4M3);
+  s.qdtype = q_dtype;
+  return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
+                       num_blocks, scale, workspace, workspace_bytes, options, error_word,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, 0,
+                       k_scale, v_scale);
 }
 
 pkv_status pkv_read_error_word(const int32_t *error_word, int32_t *host_code,

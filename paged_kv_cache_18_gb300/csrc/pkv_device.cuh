@@ -46,10 +46,15 @@ struct AttnParams {
   int rows_per_cta, row_chunks;
   int max_blocks_per_seq, max_context_len;
   int split_blocks, num_splits;
-  float scale_log2;             // softmax scale * log2(e)
+  float scale_log2;             // softmax scale * log2(e) (* key scale of an FP8 cache)
+  float out_scale;              // multiplies every output (value scale of an FP8 cache; else 1)
 };
 
+// FP8 E4M3 cache element (one byte; value = code value * tensor scale).
+struct E4M3 {};
+
 template <typename T> struct Elt;
+template <> struct Elt<E4M3> { static constexpr int bytes = 1; };
 template <> struct Elt<float> { static constexpr int bytes = 4; };
 template <> struct Elt<__nv_bfloat16> { static constexpr int bytes = 2; };
 template <> struct Elt<__half> { static constexpr int bytes = 2; };
@@ -387,9 +392,10 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
     }
     const float inv = wscale[W * NC + col];
     if (direct) {
+      const float os = inv * p.out_scale;
       T *dst = reinterpret_cast<T *>(p.out) + row * D + d0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) dst[e] = from_float<T>(acc[e] * inv);
+      for (int e = 0; e < 4; ++e) dst[e] = from_float<T>(acc[e] * os);
     } else {
       float4 v = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
       *reinterpret_cast<float4 *>(&p.part_o[(row * p.num_splits + split) * D + d0]) = v;
@@ -443,7 +449,7 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
       acc[2] += w * o.z;
       acc[3] += w * o.w;
     }
-    const float inv = winv[col];
+    const float inv = winv[col] * p.out_scale;
     T *dst = reinterpret_cast<T *>(p.out) + row * D + d0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) dst[e] = from_float<T>(acc[e] * inv);

@@ -29,15 +29,25 @@ cudaError_t mma_launch(pkv_dtype dtype, int head_dim, int n_tiles, int stages,
                        const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
                        dim3 grid, cudaStream_t stream);
 
-// CUDA-core kernel: rows = query rows per CTA (1, 2, 4 or 8).
+// CUDA-core kernel: rows = query rows per CTA (1, 2, 4 or 8); the cache type
+// may be FP8 E4M3 with q of another type, else both types are equal.
 int simt_max_rows(int head_dim);
-bool simt_kernel_info(pkv_dtype dtype, int head_dim, int rows, KernelInfo *info);
-cudaError_t simt_launch(pkv_dtype dtype, int head_dim, int rows, const AttnParams &p, dim3 grid,
-                        cudaStream_t stream);
+bool simt_kernel_info(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int rows,
+                      KernelInfo *info);
+cudaError_t simt_launch(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int rows,
+                        const AttnParams &p, dim3 grid, cudaStream_t stream);
 
 // Split-K log-sum-exp merge.
 cudaError_t merge_launch(pkv_dtype dtype, int head_dim, const AttnParams &p, int sm_count,
                          cudaStream_t stream);
+
+// kv_append into an FP8 E4M3 cache: src_dtype rows quantised with the
+// tensor scales (x / scale, round to nearest even, saturating).
+cudaError_t append_fp8_launch(pkv_dtype src_dtype, const void *k_new, const void *v_new,
+                              void *k_cache, void *v_cache, const int64_t *slots,
+                              int64_t num_tokens, int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, float k_scale, float v_scale, int32_t *err,
+                              int sm_count, cudaStream_t stream);
 
 // kv_append.
 cudaError_t append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,

@@ -204,3 +204,18 @@ def storage_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return a.view(np.float16).astype(np.float64)
+
+
+def fp8_caches(b: PagedBatch, k_scale: float, v_scale: float):
+    """e4m3 code caches (uint8) of a batch's float caches: every stored value
+    divided by the tensor scale in float32 and cast to FP8 E4M3 (round to
+    nearest even); NaN-filled rows become the NaN code.  The new rows stay in
+    b.k_new / b.v_new for a quantising append."""
+    import torch
+
+    def codes(cache, scale):
+        f = storage_to_f64(cache, b.wl.dtype).astype(np.float32) / np.float32(scale)
+        return torch.from_numpy(np.ascontiguousarray(f)).to(torch.float8_e4m3fn).view(
+            torch.uint8).numpy()
+
+    return codes(b.k_cache, k_scale), codes(b.v_cache, v_scale)

@@ -1,0 +1,76 @@
+"""GPU parity of the FP8 E4M3 KV cache: the quantising append bit for bit
+against the oracle's, and attention over the code caches against the
+float64 oracle (keys and values dequantised as code * tensor scale)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_18_gb300 as pkv
+from paged_kv_cache_18_gb300 import workloads as W
+from tests.gpu_util import TORCH_DT, assert_close, dev_tensor, host_f64
+
+pytestmark = pytest.mark.gpu
+
+K_SCALE, V_SCALE = 0.0123, 0.0171
+
+
+def run_fp8(wl, split_blocks=0, k_scale=K_SCALE, v_scale=V_SCALE):
+    b = W.make_batch(wl)
+    kc, vc = W.fp8_caches(b, k_scale, v_scale)
+    dev = "cuda"
+    dkc, dvc = torch.from_numpy(kc).to(dev), torch.from_numpy(vc).to(dev)
+    kn, vn = dev_tensor(b.k_new, wl.dtype, dev), dev_tensor(b.v_new, wl.dtype, dev)
+    slots = torch.from_numpy(b.slot_mapping).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.kv_append_fp8(kn, vn, dkc, dvc, slots, k_scale, v_scale, error_word=err)
+    q = dev_tensor(b.q, wl.dtype, dev)
+    if wl.num_queries == 1:
+        q = q[:, 0].contiguous()
+    out = pkv.paged_attention_fp8(q, dkc, dvc, torch.from_numpy(b.block_table).to(dev),
+                                  torch.from_numpy(b.context_lens).to(dev), k_scale, v_scale,
+                                  scale=wl.softmax_scale, max_context_len=b.max_context_len,
+                                  split_blocks=split_blocks, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # the quantising append, bit for bit
+    oracle.kv_append_fp8(kc, vc, b.k_new, b.v_new, b.slot_mapping, wl.dtype, k_scale, v_scale)
+    np.testing.assert_array_equal(dkc.cpu().numpy(), kc)
+    np.testing.assert_array_equal(dvc.cpu().numpy(), vc)
+    ref = oracle.paged_attention_fp8(b.q, kc, vc, b.block_table, b.context_lens,
+                                     wl.softmax_scale, wl.dtype, k_scale, v_scale)
+    got = host_f64(out if wl.num_queries > 1 else out[:, None], wl.dtype)
+    return assert_close(got, ref, wl.dtype, wl.name)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("Q,Hq,Hkv", [(1, 8, 8), (1, 8, 2), (5, 8, 2), (2, 4, 1)])
+def test_fp8_append_and_attention(dtype, D, Q, Hq, Hkv):
+    lens = [max(Q, 1), 16, 17, 33, 250, 1000]
+    wl = W.Workload(f"fp8 {dtype} D{D} Q{Q} {Hq}/{Hkv}", len(lens), Hq, Hkv, D, dtype,
+                    context_lens=lens, num_queries=Q, seed=800 + D + Q + Hq)
+    run_fp8(wl)
+
+
+@pytest.mark.parametrize("split_blocks", [1, 3, 16])
+def test_fp8_splits(split_blocks):
+    wl = W.Workload("fp8 split", 4, 32, 8, 128, "bf16", context_lens=[1, 200, 1500, 3000],
+                    seed=830 + split_blocks)
+    run_fp8(wl, split_blocks=split_blocks)
+
+
+def test_fp8_saturation_and_scales():
+    # a small scale pushes x / scale past 448: codes saturate, results still match
+    wl = W.Workload("fp8 sat", 3, 8, 2, 128, "bf16", context_lens=[10, 90, 300], seed=840)
+    run_fp8(wl, k_scale=0.002, v_scale=1.0)
+
+
+def test_fp8_rejected_by_16bit_entry_points():
+    wl = W.Workload("fp8 rej", 1, 4, 4, 128, "bf16", context_lens=[20], seed=841)
+    b = W.make_batch(wl)
+    kc, vc = W.fp8_caches(b, 1.0, 1.0)
+    L = pkv.binding.lib()
+    st = L.pkv_paged_decode_attention(16, 16, 16, 16, 16, 2, 16, 20, 1, 4, 4, 128, 16, 10, 0.1,
+                                      3, None, 0, None, None, None)
+    assert st == 1
