@@ -101,7 +101,7 @@ enum {
 typedef enum pkv_kernel {
   PKV_KERNEL_AUTO = 0,
   PKV_KERNEL_SIMT = 1, /* CUDA-core dot products (any dtype; fp32 path) */
-  PKV_KERNEL_MMA = 2   /* tensor-core tiles (bf16 / fp16 only) */
+  PKV_KERNEL_MMA = 2   /* tensor-core tiles (bf16 / fp16 q; 16-bit or FP8 cache) */
 } pkv_kernel;
 
 /* Optional launch controls (pass NULL for the planner's choice). */
@@ -323,7 +323,12 @@ PKV_API pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, void 
  * key element code * k_scale and every value element code * v_scale.  q and
  * out are of q_dtype (F32/BF16/F16), [batch, num_queries, num_heads,
  * head_dim]; head_dim 128 or 256.  Plans and workspace sizes: the plan and
- * workspace functions with dtype PKV_FP8_E4M3.
+ * workspace functions with dtype PKV_FP8_E4M3 (the plan is the one for
+ * 16-bit q; the workspace size covers float32 q too).  Kernels: BF16/F16 q
+ * run on the tensor-core kernel by default (codes widened exactly to f16, q
+ * rescaled by a power of two per row into f16 range, f16 products with
+ * float32 accumulation); F32 q, or PKV_KERNEL_SIMT, run the CUDA-core kernel
+ * in float32.
  */
 PKV_API pkv_status pkv_paged_attention_fp8(
     void *out, const void *q, const void *k_cache, const void *v_cache,

@@ -126,12 +126,13 @@ pkv_status check_shape(const Shape &s) {
 bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelInfo *info) {
   const int rows = (s.num_heads / s.num_kv_heads) * s.num_queries;
   int kernel = opt ? opt->kernel : PKV_KERNEL_AUTO;
-  // 16-bit caches go to the tensor-core kernel even for one query row per KV
-  // head (0.995 of the HBM peak on the 40-head, 2048-row bf16 layer, against
-  // 0.974 for the CUDA-core kernel); float32 has no exact tensor-core path.
-  if (kernel == PKV_KERNEL_AUTO)
-    kernel = (s.dtype == PKV_F32 || s.dtype == PKV_FP8_E4M3) ? PKV_KERNEL_SIMT : PKV_KERNEL_MMA;
-  if (kernel == PKV_KERNEL_MMA && (s.dtype == PKV_F32 || s.dtype == PKV_FP8_E4M3)) return false;
+  // 16-bit and FP8 caches go to the tensor-core kernel even for one query row
+  // per KV head (0.995 of the HBM peak on the 40-head, 2048-row bf16 layer,
+  // against 0.974 for the CUDA-core kernel); float32 (cache or q) has no exact
+  // tensor-core path.
+  const bool f32 = s.dtype == PKV_F32 || s.qdtype == PKV_F32;
+  if (kernel == PKV_KERNEL_AUTO) kernel = f32 ? PKV_KERNEL_SIMT : PKV_KERNEL_MMA;
+  if (kernel == PKV_KERNEL_MMA && f32) return false;
   if (kernel != PKV_KERNEL_MMA && kernel != PKV_KERNEL_SIMT) return false;
   int cap = kernel == PKV_KERNEL_MMA ? 8 * mma_max_tiles(s.head_dim)
                                      : simt_max_rows(s.head_dim);
@@ -141,7 +142,7 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
   bool ok;
   const int stages = opt ? opt->stages : 0;
   if (kernel == PKV_KERNEL_MMA) {
-    ok = mma_kernel_info(s.dtype, s.head_dim, ceil_div(per_cta, 8), stages, info);
+    ok = mma_kernel_info(s.dtype, s.qdtype, s.head_dim, ceil_div(per_cta, 8), stages, info);
   } else {
     if (stages != 0) return false;
     int r = 1;
@@ -287,8 +288,8 @@ EncodeTiled encode_fn() {
 }
 
 // The cache [NB, Hkv, 16, D] as a 4-D tensor (D, 16, Hkv, NB); one box is a
-// 64-element (128-byte) column panel of one (block, KV head) tile, 128-byte
-// swizzled in shared memory.
+// 128-byte column panel (64 16-bit elements or 128 FP8 codes) of one (block,
+// KV head) tile, 128-byte swizzled in shared memory.
 bool encode_cache_map(CUtensorMap *map, const void *base, pkv_dtype dt, int D, int Hkv,
                       int64_t NB) {
   EncodeTiled fn = encode_fn();
@@ -299,10 +300,12 @@ bool encode_cache_map(CUtensorMap *map, const void *base, pkv_dtype dt, int D, i
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * eb,
                                  static_cast<cuuint64_t>(D) * eb * kBlockSize,
                                  static_cast<cuuint64_t>(D) * eb * kBlockSize * Hkv};
-  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBlockSize), 1, 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb),
+                             static_cast<cuuint32_t>(kBlockSize), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUtensorMapDataType type =
-      dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType type = dt == PKV_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dt == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   return fn(map, type, 4, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -395,7 +398,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
     if (!encode_cache_map(&kmap, k_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks) ||
         !encode_cache_map(&vmap, v_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks))
       return PKV_ERR_CUDA;
-    e = mma_launch(s.dtype, s.head_dim, ceil_div(pl.rows_per_cta, 8), pl.stages, kmap, vmap, p,
+    e = mma_launch(s.dtype, s.qdtype, s.head_dim, ceil_div(pl.rows_per_cta, 8), pl.stages, kmap, vmap, p,
                    grid, stream);
   } else {
     int r = 1;
@@ -490,8 +493,22 @@ pkv_status pkv_attention_workspace_size(int batch, int num_queries, int num_head
   pkv_plan pl{};
   const pkv_status st = pkv_attention_plan(batch, num_queries, num_heads, num_kv_heads, head_dim,
                                            block_size, max_context_len, dtype, options, &pl);
-  if (st == PKV_OK) *bytes = pl.workspace_bytes;
-  return st;
+  if (st != PKV_OK) return st;
+  *bytes = pl.workspace_bytes;
+  if (dtype == PKV_FP8_E4M3 && (!options || options->kernel != PKV_KERNEL_MMA)) {
+    // float32 queries over an FP8 cache take the CUDA-core kernel: report
+    // enough for either plan.
+    Shape s = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim, block_size,
+                         max_context_len, dtype);
+    s.qdtype = PKV_F32;
+    pkv_plan p32{};
+    KernelInfo info;
+    int device = 0, sms = 0;
+    if (device_plan(s, options, &p32, &info, &device, &sms) == PKV_OK &&
+        p32.workspace_bytes > *bytes)
+      *bytes = p32.workspace_bytes;
+  }
+  return PKV_OK;
 }
 
 pkv_status pkv_paged_decode_attention(void *out, const void *q, const void *k_cache,

@@ -22,12 +22,14 @@ struct KernelInfo {
 };
 
 // Tensor-core kernel: n_tiles = query columns / 8; stages = per-warp ring
-// depth (0 = default).
+// depth (0 = default).  The cache type is q's 16-bit type, or FP8 E4M3 with
+// bf16 / f16 q (head_dim 128 or 256).
 int mma_max_tiles(int head_dim);
-bool mma_kernel_info(pkv_dtype dtype, int head_dim, int n_tiles, int stages, KernelInfo *info);
-cudaError_t mma_launch(pkv_dtype dtype, int head_dim, int n_tiles, int stages,
-                       const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
-                       dim3 grid, cudaStream_t stream);
+bool mma_kernel_info(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int n_tiles,
+                     int stages, KernelInfo *info);
+cudaError_t mma_launch(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int n_tiles,
+                       int stages, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                       const AttnParams &p, dim3 grid, cudaStream_t stream);
 
 // CUDA-core kernel: rows = query rows per CTA (1, 2, 4 or 8); the cache type
 // may be FP8 E4M3 with q of another type, else both types are equal.

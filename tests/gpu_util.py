@@ -99,3 +99,38 @@ def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what=""):
     assert max_abs <= tol_abs and rel <= tol_rel, \
         f"{what}: max-abs {max_abs:.3e} (tol {tol_abs}), rel-L2 {rel:.3e} (tol {tol_rel})"
     return max_abs, rel
+
+
+# Output rounding of each type: half a unit in the last place at |x|.
+_MANT_BITS = {"bf16": 7, "f16": 10, "f32": 23}
+_MIN_EXP = {"bf16": -126, "f16": -14, "f32": -126}
+
+
+def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    e = np.floor(np.log2(np.maximum(np.abs(x), np.finfo(np.float64).tiny)))
+    e = np.maximum(e, _MIN_EXP[dtype])
+    return np.ldexp(1.0, (e - _MANT_BITS[dtype] - 1).astype(np.int64))
+
+
+# FP8 caches: an output element is a weighted mean of code * v_scale values,
+# which the output type does not hold exactly (a 16-bit V cache gives outputs
+# that are often V elements themselves), so the element bound is the output
+# rounding plus the arithmetic's own error: for 16-bit q, the f16 rounding
+# of the softmax weights (2^-11 relative, at most 2^-11 * max|v| ~ 3.7e-3 for
+# |v| <= 448 * 0.0171); float32 q keeps the float32 bound.  The relative L2
+# bound stays the stated one.
+FP8_EXTRA = {"bf16": 4e-3, "f16": 4e-3, "f32": 1e-5}
+
+
+def assert_close_fp8(got: np.ndarray, ref: np.ndarray, dtype: str, what=""):
+    mask = ~np.isnan(ref)
+    assert np.isfinite(got[mask]).all(), f"{what}: non-finite output"
+    d = np.abs(got[mask] - ref[mask])
+    excess = d - half_ulp(ref[mask], dtype)
+    worst = float(excess.max()) if d.size else 0.0
+    _, rel = errors(got, ref)
+    tol_rel = TOL[dtype][1]
+    assert worst <= FP8_EXTRA[dtype] and rel <= tol_rel, \
+        (f"{what}: max (|err| - half ulp) {worst:.3e} (tol {FP8_EXTRA[dtype]}), "
+         f"rel-L2 {rel:.3e} (tol {tol_rel})")
+    return float(d.max()) if d.size else 0.0, rel
