@@ -20,9 +20,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMinSplitBlocks = 16;     // 4 blocks per warp: fills the pipeline
-constexpr int kMaxUnitBlocks = 64;      // longest split when splitting at all
+constexpr int kMaxUnitBytes = 64 * 8192;  // longest split, in K+V bytes of one KV head
+                                          // (64 blocks of a 16-bit, 128-dim cache)
 constexpr int kTargetWaves = 4;         // CTAs ~ this many times the resident slots
-constexpr int kMaxSplits = 16;          // per sequence: each split adds merge work
+constexpr int kMaxSplits = 32;          // per sequence: each split adds merge work
 constexpr size_t kUsableSmemPerSm = 228 * 1024;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -203,14 +204,25 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
   } else {
     const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
     const int64_t want = kTargetWaves * slots;
+    const int block_bytes = 2 * s.block_size * s.head_dim * elt_bytes(s.dtype);
+    const int max_unit_blocks = kMaxUnitBytes / block_bytes > 1 ? kMaxUnitBytes / block_bytes : 1;
     if (units >= want || max_blocks <= kMinSplitBlocks) {
       split_blocks = max_blocks;
     } else {
       const int64_t splits = (want + units - 1) / units;
       split_blocks = ceil_div(max_blocks, splits);
       if (split_blocks < kMinSplitBlocks) split_blocks = kMinSplitBlocks;
-      if (split_blocks > kMaxUnitBlocks && split_blocks < max_blocks) split_blocks = kMaxUnitBlocks;
+      if (split_blocks > max_unit_blocks && split_blocks < max_blocks) split_blocks = max_unit_blocks;
       if (split_blocks < ceil_div(max_blocks, kMaxSplits)) split_blocks = ceil_div(max_blocks, kMaxSplits);
+      // Keep the split only if it shortens the schedule: with every sequence
+      // at the longest length, ceil(CTAs / slots) waves of split_blocks each
+      // against ceil(units / slots) waves of max_blocks.  (1280 equal
+      // 128-block units on 456 slots take 3 waves whole and 6 waves of 64
+      // blocks split: the same, plus the merge.)
+      const int64_t ns = ceil_div(max_blocks, split_blocks);
+      const int64_t whole = (units + slots - 1) / slots * max_blocks;
+      const int64_t split = (units * ns + slots - 1) / slots * split_blocks;
+      if (whole <= split) split_blocks = max_blocks;
     }
   }
   if (split_blocks < 1) split_blocks = 1;

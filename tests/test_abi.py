@@ -136,9 +136,26 @@ def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
 
 def test_plan_splits_long_contexts_and_honours_override():
     p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152)
-    # 16 (sequence, KV head) pairs cannot fill 152 SMs: split, at most 16 ways
-    assert 8 <= p["num_splits"] <= 16
+    # 16 (sequence, KV head) pairs cannot fill 152 SMs: split, at most 32 ways
+    assert 16 <= p["num_splits"] <= 32
     p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152, split_blocks=7)
     assert p["split_blocks"] == 7 and p["num_splits"] == -(-4096 // 7)
     p = binding.plan_for(2, 1, 32, 8, 128, 100, torch.bfloat16, num_sms=152, split_blocks=1000)
     assert p["num_splits"] == 1
+
+
+def test_plan_does_not_split_when_waves_gain_nothing():
+    # 1280 equal units of 128 blocks on 152 SMs x 3 CTAs: 3 waves whole, and
+    # 6 waves of 64-block halves: no split
+    p = binding.plan_for(32, 1, 40, 40, 128, 2048, torch.bfloat16, num_sms=152, ctas_per_sm=3)
+    assert p["num_splits"] == 1
+    # 1024 units of up to 256 blocks: 3 waves of 256 against 9 of 64: split
+    p = binding.plan_for(128, 1, 32, 8, 128, 4096, torch.bfloat16, num_sms=152, ctas_per_sm=3)
+    assert p["num_splits"] == 4 and p["split_blocks"] == 64
+
+
+def test_plan_caps_split_length_in_bytes():
+    # the same KV bytes per split for a one-byte cache: twice the blocks
+    p16 = binding.plan_for(128, 1, 32, 8, 128, 4096, torch.bfloat16, num_sms=152, ctas_per_sm=3)
+    p8 = binding.plan_for(128, 1, 32, 8, 128, 4096, "fp8", num_sms=152, ctas_per_sm=3)
+    assert p8["split_blocks"] == 2 * p16["split_blocks"]
