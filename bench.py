@@ -276,7 +276,8 @@ def run_ours(args):
         pkv_build.build()
     barrier()
     import paged_kv_cache_18_gb300 as pkv
-    pkv.binding.TUNING.update(rows_per_cta=args.rows_per_cta, merge=args.merge)
+    pkv.binding.TUNING.update(rows_per_cta=args.rows_per_cta, merge=args.merge,
+                              warp_tiles=args.warp_tiles)
 
     wl = W.WORKLOADS[args.workload]
     if rank > 0:
@@ -484,6 +485,8 @@ def main(argv=None):
     ap.add_argument("--stages", type=int, default=0, help="tensor-core kernel ring depth")
     ap.add_argument("--rows-per-cta", type=int, default=0, help="cap on query rows per CTA")
     ap.add_argument("--merge", type=int, default=0, help="0 planner, 1 fused, 2 separate kernel")
+    ap.add_argument("--warp-tiles", type=int, default=0,
+                    help="tensor-core kernel: 8-column query tiles per warp (0 planner)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",

@@ -113,6 +113,8 @@ typedef struct pkv_options {
   int rows_per_cta; /* 0: planner; cap on the query rows one CTA serves */
   int merge;        /* split-K merge: 0 planner, 1 by the sequence's last CTA,
                        2 by a separate kernel */
+  int warp_tiles;   /* 0: planner; tensor-core kernel: 8-column query tiles
+                       per warp (1..3 at head_dim <= 128, 1..4 at 64, 1 at 256) */
 } pkv_options;
 
 /* What one attention call launches (see pkv_attention_plan). */
@@ -130,6 +132,7 @@ typedef struct pkv_plan {
   size_t workspace_bytes; /* device workspace the call needs (0 = none) */
   int merge_kernel;       /* 1: a separate split-K merge launch follows;
                              0: no split, or the last CTA of each sequence merges */
+  int warp_tiles;         /* tensor-core kernel: 8-column query tiles per warp */
 } pkv_plan;
 
 /* Human-readable name of a status code (static string). */

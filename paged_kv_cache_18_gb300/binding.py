@@ -46,11 +46,12 @@ class PkvError(RuntimeError):
 class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("split_blocks", ctypes.c_int),
                 ("stages", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
-                ("merge", ctypes.c_int)]
+                ("merge", ctypes.c_int), ("warp_tiles", ctypes.c_int)]
 
 
-# Extra launch controls for tuning runs (pkv_options.rows_per_cta / .merge);
-# module-wide so that every binding call passes them.  Empty = planner.
+# Extra launch controls for tuning runs (pkv_options.rows_per_cta / .merge /
+# .warp_tiles); module-wide so that every binding call passes them.  Empty =
+# planner.
 TUNING = {}
 
 
@@ -62,7 +63,7 @@ class Plan(ctypes.Structure):
                 ("threads_per_cta", ctypes.c_int), ("stages", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int),
                 ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
-                ("merge_kernel", ctypes.c_int)]
+                ("merge_kernel", ctypes.c_int), ("warp_tiles", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -134,11 +135,12 @@ def _stream(t: torch.Tensor) -> int:
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
-def _opts(kernel: int, split_blocks: int, stages: int = 0):
+def _opts(kernel: int, split_blocks: int, stages: int = 0, warp_tiles: int = 0):
     rows, merge = TUNING.get("rows_per_cta", 0), TUNING.get("merge", 0)
-    if kernel == 0 and split_blocks == 0 and stages == 0 and rows == 0 and merge == 0:
+    warp_tiles = warp_tiles or TUNING.get("warp_tiles", 0)
+    if not any((kernel, split_blocks, stages, rows, merge, warp_tiles)):
         return None
-    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge))
+    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge, warp_tiles))
 
 
 def _need(cond: bool, msg: str) -> None:

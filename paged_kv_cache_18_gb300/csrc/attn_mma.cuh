@@ -116,21 +116,23 @@ __device__ __forceinline__ void lane_sync(int id, int count) {
 
 // BL block lanes x CG column groups = BL * CG warps.  Block lane bl owns the
 // blocks bl, bl + BL, ... of the split and a ring of NS stages; the CG warps
-// of a lane share each staged block, warp cg computing query columns
-// 8 cg .. 8 cg + 7.  The lane's first warp issues the copies.
+// of a lane share each staged block, warp cg computing the NT 8-column tiles
+// of query columns 8 NT cg .. 8 NT (cg + 1) - 1 (a warp with several tiles
+// reads each K / V fragment once for all of them).  The lane's first warp
+// issues the copies.
 //
 // T: element type of q and out (bf16 / f16); TC: cache element (T, or E4M3:
 // one-byte codes, widened to f16 for f16 MMAs; q then enters as f16 after a
 // per-row power-of-two shift that keeps it in f16 range, undone in the score
 // scale).
-template <typename T, typename TC, int D, int CG, int BL, int NS>
+template <typename T, typename TC, int D, int CG, int NT, int BL, int NS>
 __global__ void __launch_bounds__(BL * CG * 32)
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   constexpr bool FP8 = std::is_same<TC, E4M3>::value;
   using TM = typename MmaType<T, TC>::type;
   using G = MmaGeom<D, Elt<TC>::bytes>;
-  constexpr int NC = CG * 8;  // query columns of this CTA (padded)
+  constexpr int NC = CG * NT * 8;  // query columns of this CTA (padded)
   constexpr int KS = G::kSteps;
   constexpr int NW = BL * CG;
 
@@ -140,6 +142,8 @@ __global__ void __launch_bounds__(BL * CG * 32)
   const uint32_t smem_base = smem_u32(smem);
   __shared__ uint64_t bars[BL * NS];  // the stage's copies landed
   __shared__ volatile int s_abort;
+  __shared__ int s_lim[NC];                  // causal visible-row limit per column
+  __shared__ unsigned long long s_tm[NC];    // tree mask per column
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bl = warp / CG, cg = warp - (warp / CG) * CG;
@@ -159,22 +163,26 @@ __global__ void __launch_bounds__(BL * CG * 32)
   const int ns_b = max(1, min(p.num_splits, (ext.nblk + p.split_blocks - 1) / p.split_blocks));
   const int nspan = max(blk_end - blk_begin, 0);
   const int n_my = nspan > bl ? (nspan - bl + BL - 1) / BL : 0;
-  const int col0 = cg * 8;
+  const int col0 = cg * NT * 8;
 
-  // Q^T operand fragments of this warp's 8 columns (B operand: k = head dim).
+  // Q^T operand fragments of this warp's columns (B operand: k = head dim).
   // 16-bit caches: the natural k order.  FP8 caches: k-step ks covers head
   // dims 16 ks .. 16 ks + 15 with lane c holding 16 ks + 4c .. 4c + 3 (the
   // order the K fragments arrive in), shifted by 2^qshift into f16 range.
-  uint32_t qf[KS][2];
-  float colfac[2] = {p.scale_log2, p.scale_log2};  // score scale of my two columns
-  {
-    const int64_t row = cta_row_index(p, b, kvh, chunk, col0 + g);
+  uint32_t qf[KS][NT][2];
+  float colfac[NT][2];  // score scale of my two columns of each tile
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int64_t row = cta_row_index(p, b, kvh, chunk, col0 + nt * 8 + g);
     const T *qrow = reinterpret_cast<const T *>(p.q) + (row < 0 ? 0 : row) * D;
+    colfac[nt][0] = colfac[nt][1] = p.scale_log2;
     if constexpr (!FP8) {
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        qf[ks][0] = row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
-        qf[ks][1] = row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * c);
+        qf[ks][nt][0] =
+            row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
+        qf[ks][nt][1] =
+            row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * c);
       }
     } else {
       float qv[KS][4];
@@ -201,39 +209,40 @@ __global__ void __launch_bounds__(BL * CG * 32)
       const float up = exp2f(static_cast<float>(qshift));
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        qf[ks][0] = Mma<__half>::pack(qv[ks][0] * up, qv[ks][1] * up);
-        qf[ks][1] = Mma<__half>::pack(qv[ks][2] * up, qv[ks][3] * up);
+        qf[ks][nt][0] = Mma<__half>::pack(qv[ks][0] * up, qv[ks][1] * up);
+        qf[ks][nt][1] = Mma<__half>::pack(qv[ks][2] * up, qv[ks][3] * up);
       }
       // my score columns 2c, 2c+1 were shifted by the lanes of groups 2c, 2c+1
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int sh = __shfl_sync(kFull, qshift, 4 * (2 * c + e));
-        colfac[e] = p.scale_log2 * exp2f(static_cast<float>(-sh));
+        colfac[nt][e] = p.scale_log2 * exp2f(static_cast<float>(-sh));
       }
     }
-  }
-  // Visible-row limit of the two columns this thread holds.
-  int lim[2];
-  unsigned long long tm[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    lim[e] = cta_row_limit(p, L, chunk, col0 + 2 * c + e);
-    tm[e] = cta_row_tree_mask(p, b, chunk, col0 + 2 * c + e);
   }
   const int mask_from = L - p.num_queries;  // first row some column may not see
 
   // Online-softmax state.
-  float o[KS][4];
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float o[KS][NT][4];
+  float m[NT][2], l[NT][2];
 #pragma unroll
-  for (int mt = 0; mt < KS; ++mt)
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt][0] = m[nt][1] = -INFINITY;
+    l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+  }
 
-  // The lane's ring.
+  // The lane's ring; per-column visibility.
   const uint32_t my_bars = smem_u32(&bars[bl * NS]);
   const uint32_t my_stages = smem_base + bl * NS * G::kStageBytes;
   if (threadIdx.x == 0) s_abort = 0;
+  for (int col = threadIdx.x; col < NC; col += NW * 32) {
+    s_lim[col] = cta_row_limit(p, L, chunk, col);
+    s_tm[col] = cta_row_tree_mask(p, b, chunk, col);
+  }
   if (leader && lane == 0) {
 #pragma unroll
     for (int s = 0; s < NS; ++s) mbar_init(my_bars + 8 * s, 1);
@@ -313,17 +322,23 @@ __global__ void __launch_bounds__(BL * CG * 32)
     }
 
     if (live) {
-      // S^T = K Q^T, the head-dim steps spread over four accumulator chains.
-      constexpr int NCH = KS < 4 ? KS : 4;
-      float acc[NCH][4];
+      // S^T = K Q^T.  One tile: the head-dim steps spread over four
+      // accumulator chains; several tiles: their MMAs interleave.
+      constexpr int NCH = NT == 1 ? (KS < 4 ? KS : 4) : (NT == 2 ? 2 : 1);
+      float acc[NCH][NT][4];
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) acc[ch][0] = acc[ch][1] = acc[ch][2] = acc[ch][3] = 0.f;
+      for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          acc[ch][nt][0] = acc[ch][nt][1] = acc[ch][nt][2] = acc[ch][nt][3] = 0.f;
       if constexpr (!FP8) {
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t a[4];
           ldsm_x4(a, ktile + swz<D>(lane & 15, ks * 16 + (lane >> 4) * 8));
-          Mma<TM>::run(acc[ks % NCH], a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            Mma<TM>::run(acc[ks % NCH][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
         }
       } else {
         // One ldmatrix brings 16 keys x 32 head dims of codes: lane (g, c)
@@ -338,27 +353,31 @@ __global__ void __launch_bounds__(BL * CG * 32)
             e4m3x4_to_f16(r[2 * u], a[0], a[2]);      // key g: dims 4c, 4c+1 | 4c+2, 4c+3
             e4m3x4_to_f16(r[2 * u + 1], a[1], a[3]);  // key g + 8
             const int ks = 2 * pr + u;
-            Mma<TM>::run(acc[ks % NCH], a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              Mma<TM>::run(acc[ks % NCH][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
           }
         }
       }
-      float sc[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float t = acc[0][e];
-#pragma unroll
-        for (int ch = 1; ch < NCH; ++ch) t += acc[ch][e];
-        sc[e] = t;
-      }
+      float sc[NT][4];
       const bool need_mask = bad || key0 + kBlockSize > mask_from;
       bool above = false;  // some score exceeds its column's reference by > the slack
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = sc[e] * colfac[e & 1];
-        if (need_mask && !key_visible(p, key0 + g + ((e >> 1) << 3), L, bad, lim[e & 1], tm[e & 1]))
-          v = -INFINITY;
-        sc[e] = v;
-        above |= v > m[e & 1] + kRescaleSlack;
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float t = acc[0][nt][e];
+#pragma unroll
+          for (int ch = 1; ch < NCH; ++ch) t += acc[ch][nt][e];
+          float v = t * colfac[nt][e & 1];
+          if (need_mask) {
+            const int col = col0 + nt * 8 + 2 * c + (e & 1);
+            if (!key_visible(p, key0 + g + ((e >> 1) << 3), L, bad, s_lim[col], s_tm[col]))
+              v = -INFINITY;
+          }
+          sc[nt][e] = v;
+          above |= v > m[nt][e & 1] + kRescaleSlack;
+        }
       }
       // Online softmax.  The exponentials use a per-column reference m that
       // is raised (to the exact running max, rescaling l and O by
@@ -368,45 +387,54 @@ __global__ void __launch_bounds__(BL * CG * 32)
       // needed.  The result O / l does not depend on the reference.
       if (__any_sync(kFull, above)) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float mx = fmaxf(sc[e], sc[e + 2]);
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-          const float m_new = fmaxf(m[e], mx);
-          const float corr = ex2(m[e] - (m_new == -INFINITY ? 0.f : m_new));
-          l[e] *= corr;
-          m[e] = m_new;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int mt = 0; mt < KS; ++mt) {
-            o[mt][e] *= corr;
-            o[mt][e + 2] *= corr;
+          for (int e = 0; e < 2; ++e) {
+            float mx = fmaxf(sc[nt][e], sc[nt][e + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+            const float m_new = fmaxf(m[nt][e], mx);
+            const float corr = ex2(m[nt][e] - (m_new == -INFINITY ? 0.f : m_new));
+            l[nt][e] *= corr;
+            m[nt][e] = m_new;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+              o[mt][nt][e] *= corr;
+              o[mt][nt][e + 2] *= corr;
+            }
           }
-        }
       }
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float m_use = m[e] == -INFINITY ? 0.f : m[e];
-        const float p0 = ex2(sc[e] - m_use);
-        const float p1 = ex2(sc[e + 2] - m_use);
-        l[e] += p0 + p1;
-        sc[e] = p0;
-        sc[e + 2] = p1;
-      }
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float m_use = m[nt][e] == -INFINITY ? 0.f : m[nt][e];
+          const float p0 = ex2(sc[nt][e] - m_use);
+          const float p1 = ex2(sc[nt][e + 2] - m_use);
+          l[nt][e] += p0 + p1;
+          sc[nt][e] = p0;
+          sc[nt][e + 2] = p1;
+        }
       // P^T operand fragments.  bf16 / f16 MMAs on 16-bit caches: high part
       // and rounding remainder (a single bf16 P would add about 1.6e-3 of
       // relative error).  FP8 caches: one f16 P (weights <= 2^8; 2^-11
       // relative rounding).
-      const uint32_t h01 = Mma<TM>::pack(sc[0], sc[1]);
-      const uint32_t h23 = Mma<TM>::pack(sc[2], sc[3]);
-      const uint32_t ph0 = movm_t(h01), ph1 = movm_t(h23);
-      uint32_t pl0 = 0u, pl1 = 0u;
-      if constexpr (!FP8) {
-        float r0, r1, r2, r3;
-        Mma<TM>::unpack(h01, r0, r1);
-        Mma<TM>::unpack(h23, r2, r3);
-        pl0 = movm_t(Mma<TM>::pack(sc[0] - r0, sc[1] - r1));
-        pl1 = movm_t(Mma<TM>::pack(sc[2] - r2, sc[3] - r3));
+      uint32_t ph[NT][2], pl[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t h01 = Mma<TM>::pack(sc[nt][0], sc[nt][1]);
+        const uint32_t h23 = Mma<TM>::pack(sc[nt][2], sc[nt][3]);
+        ph[nt][0] = movm_t(h01);
+        ph[nt][1] = movm_t(h23);
+        pl[nt][0] = pl[nt][1] = 0u;
+        if constexpr (!FP8) {
+          float r0, r1, r2, r3;
+          Mma<TM>::unpack(h01, r0, r1);
+          Mma<TM>::unpack(h23, r2, r3);
+          pl[nt][0] = movm_t(Mma<TM>::pack(sc[nt][0] - r0, sc[nt][1] - r1));
+          pl[nt][1] = movm_t(Mma<TM>::pack(sc[nt][2] - r2, sc[nt][3] - r3));
+        }
       }
       // O^T += V^T P^T.  In a block that ends past the context, zero the V^T
       // columns (keys) past it so that NaN-filled rows never enter an MMA.
@@ -418,9 +446,9 @@ __global__ void __launch_bounds__(BL * CG * 32)
           km8 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
         }
         if constexpr (!FP8) {
-          // Four head-dim tiles at a time: their high-part MMAs first, then
-          // the low parts, so that no MMA waits on the one just issued.
-          constexpr int GRP = KS < 4 ? KS : 4;
+          // Head-dim tiles a group at a time: their high-part MMAs first,
+          // then the low parts, so that no MMA waits on the one just issued.
+          constexpr int GRP = NT > 1 ? 2 : (KS < 4 ? KS : 4);
 #pragma unroll
           for (int m0 = 0; m0 < KS; m0 += GRP) {
             uint32_t a[GRP][4];
@@ -436,9 +464,13 @@ __global__ void __launch_bounds__(BL * CG * 32)
               }
             }
 #pragma unroll
-            for (int u = 0; u < GRP; ++u) Mma<TM>::run(o[m0 + u], a[u], ph0, ph1);
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int u = 0; u < GRP; ++u) Mma<TM>::run(o[m0 + u], a[u], pl0, pl1);
+              for (int u = 0; u < GRP; ++u) Mma<TM>::run(o[m0 + u][nt], a[u], ph[nt][0], ph[nt][1]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int u = 0; u < GRP; ++u) Mma<TM>::run(o[m0 + u][nt], a[u], pl[nt][0], pl[nt][1]);
           }
         } else {
           // V^T fragments from codes: one transposed ldmatrix of byte pairs
@@ -466,7 +498,9 @@ __global__ void __launch_bounds__(BL * CG * 32)
                 a[u][2] &= km8;
                 a[u][3] &= km8;
               }
-              Mma<TM>::run(o[2 * pr + u], a[u], ph0, ph1);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                Mma<TM>::run(o[2 * pr + u][nt], a[u], ph[nt][0], ph[nt][1]);
             }
           }
         }
@@ -491,13 +525,15 @@ __global__ void __launch_bounds__(BL * CG * 32)
 
   // Row sums: reduce the per-thread partial sums over the 8 lanes of a column.
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    float v = l[e];
-    v += __shfl_xor_sync(kFull, v, 4);
-    v += __shfl_xor_sync(kFull, v, 8);
-    v += __shfl_xor_sync(kFull, v, 16);
-    l[e] = v;
-  }
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = l[nt][e];
+      v += __shfl_xor_sync(kFull, v, 4);
+      v += __shfl_xor_sync(kFull, v, 8);
+      v += __shfl_xor_sync(kFull, v, 16);
+      l[nt][e] = v;
+    }
 
   // Hand the per-warp states to the CTA epilogue (reusing the stage memory):
   // one state per (block lane, column).
@@ -508,18 +544,22 @@ __global__ void __launch_bounds__(BL * CG * 32)
   float *red_l = red_m + BL * NC;
   float *wscale = red_l + BL * NC;
 #pragma unroll
-  for (int mt = 0; mt < KS; ++mt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int col = col0 + 2 * c + (e & 1);
-      red_o[(bl * NC + col) * DP + o_dim<FP8>(mt, g, e)] = o[mt][e];
-    }
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int col = col0 + nt * 8 + 2 * c + (e & 1);
+        red_o[(bl * NC + col) * DP + o_dim<FP8>(mt, g, e)] = o[mt][nt][e];
+      }
   if (g == 0) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      red_m[bl * NC + col0 + 2 * c + e] = m[e];
-      red_l[bl * NC + col0 + 2 * c + e] = l[e];
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        red_m[bl * NC + col0 + nt * 8 + 2 * c + e] = m[nt][e];
+        red_l[bl * NC + col0 + nt * 8 + 2 * c + e] = l[nt][e];
+      }
   }
   __syncthreads();
   cta_epilogue<T, D, NC, BL, NW * 32>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split,
@@ -543,11 +583,11 @@ template <typename TC, int D, int CG, bool DEEP> constexpr int mma_stages_t() {
   return mma_stages<D, CG, DEEP>() * (std::is_same<TC, E4M3>::value ? 2 : 1);
 }
 
-template <typename T, typename TC, int D, int CG, bool DEEP>
+template <typename T, typename TC, int D, int CG, int NT, bool DEEP>
 constexpr size_t mma_smem_bytes() {
   constexpr int BL = mma_lanes<CG>();
   constexpr int NS = mma_stages_t<TC, D, CG, DEEP>();
-  constexpr int NC = CG * 8;
+  constexpr int NC = CG * NT * 8;
   constexpr size_t stages = size_t(BL) * NS * MmaGeom<D, Elt<TC>::bytes>::kStageBytes;
   constexpr size_t red = (size_t(BL) * NC * (D + 4) + size_t(3 * BL + 2) * NC) * 4;
   constexpr size_t merge = (size_t(NC) * kMaxFusedSplits + NC) * 4;
@@ -559,24 +599,25 @@ constexpr size_t mma_smem_bytes() {
 using MmaLaunch = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const AttnParams &,
                                   dim3, cudaStream_t);
 
-template <typename T, typename TC, int D, int CG, bool DEEP>
+template <typename T, typename TC, int D, int CG, int NT, bool DEEP>
 KernelInfo mma_info_t() {
   constexpr int BL = mma_lanes<CG>();
   KernelInfo k;
   k.func = reinterpret_cast<const void *>(
-      &attn_mma_kernel<T, TC, D, CG, BL, mma_stages_t<TC, D, CG, DEEP>()>);
+      &attn_mma_kernel<T, TC, D, CG, NT, BL, mma_stages_t<TC, D, CG, DEEP>()>);
   k.threads = BL * CG * 32;
-  k.smem = mma_smem_bytes<T, TC, D, CG, DEEP>();
+  k.smem = mma_smem_bytes<T, TC, D, CG, NT, DEEP>();
   k.warps = BL * CG;
   k.stages = mma_stages_t<TC, D, CG, DEEP>();
+  k.warp_tiles = NT;
   return k;
 }
 
-template <typename T, typename TC, int D, int CG, bool DEEP>
+template <typename T, typename TC, int D, int CG, int NT, bool DEEP>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
-  const KernelInfo k = mma_info_t<T, TC, D, CG, DEEP>();
-  attn_mma_kernel<T, TC, D, CG, mma_lanes<CG>(), mma_stages_t<TC, D, CG, DEEP>()>
+  const KernelInfo k = mma_info_t<T, TC, D, CG, NT, DEEP>();
+  attn_mma_kernel<T, TC, D, CG, NT, mma_lanes<CG>(), mma_stages_t<TC, D, CG, DEEP>()>
       <<<grid, k.threads, k.smem, stream>>>(km, vm, p);
   return cudaGetLastError();
 }
@@ -584,32 +625,45 @@ cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnPar
 // Default ring: the shallow one (for one column group at head_dim <= 128,
 // 3 CTAs per SM; the 8-row GQA tile measured 0.949 of the HBM peak against
 // 0.932 with the deep ring).
-template <typename T, typename TC, int D, int CG>
+template <typename T, typename TC, int D, int CG, int NT>
 bool mma_pick_stages(int stages, KernelInfo *info, MmaLaunch *launch) {
   if (stages == 0) stages = mma_stages_t<TC, D, CG, false>();
   if (stages == mma_stages_t<TC, D, CG, true>()) {
-    *info = mma_info_t<T, TC, D, CG, true>();
-    *launch = &launch_t<T, TC, D, CG, true>;
+    *info = mma_info_t<T, TC, D, CG, NT, true>();
+    *launch = &launch_t<T, TC, D, CG, NT, true>;
     return true;
   }
   if (stages == mma_stages_t<TC, D, CG, false>()) {
-    *info = mma_info_t<T, TC, D, CG, false>();
-    *launch = &launch_t<T, TC, D, CG, false>;
+    *info = mma_info_t<T, TC, D, CG, NT, false>();
+    *launch = &launch_t<T, TC, D, CG, NT, false>;
     return true;
   }
   return false;
 }
 
-// Column groups x head dim within the budget (CG * D <= 384).
+// Column groups x tiles per warp x head dim within the register and shared
+// memory budgets: cg warps of nt 8-column tiles each.  One tile per warp:
+// cg * D <= 384.  Several tiles in one warp (its O^T accumulators hold
+// nt * D / 4 floats per thread): nt * D <= 384, one column group.
 template <typename T, typename TC, int D>
-bool mma_pick(int cg, int stages, KernelInfo *info, MmaLaunch *launch) {
-  switch (cg) {
-    case 1: return mma_pick_stages<T, TC, D, 1>(stages, info, launch);
-    case 2:
-      return D <= 128 && mma_pick_stages<T, TC, D, (D <= 128 ? 2 : 1)>(stages, info, launch);
-    case 3:
-      return D <= 128 && mma_pick_stages<T, TC, D, (D <= 128 ? 3 : 1)>(stages, info, launch);
-    case 4: return D <= 64 && mma_pick_stages<T, TC, D, (D <= 64 ? 4 : 1)>(stages, info, launch);
+bool mma_pick(int cg, int nt, int stages, KernelInfo *info, MmaLaunch *launch) {
+  if (nt == 1) {
+    switch (cg) {
+      case 1: return mma_pick_stages<T, TC, D, 1, 1>(stages, info, launch);
+      case 2:
+        return D <= 128 && mma_pick_stages<T, TC, D, (D <= 128 ? 2 : 1), 1>(stages, info, launch);
+      case 3:
+        return D <= 128 && mma_pick_stages<T, TC, D, (D <= 128 ? 3 : 1), 1>(stages, info, launch);
+      case 4:
+        return D <= 64 && mma_pick_stages<T, TC, D, (D <= 64 ? 4 : 1), 1>(stages, info, launch);
+      default: return false;
+    }
+  }
+  if (cg != 1) return false;
+  switch (nt) {
+    case 2: return D <= 128 && mma_pick_stages<T, TC, D, 1, (D <= 128 ? 2 : 1)>(stages, info, launch);
+    case 3: return D <= 128 && mma_pick_stages<T, TC, D, 1, (D <= 128 ? 3 : 1)>(stages, info, launch);
+    case 4: return D <= 64 && mma_pick_stages<T, TC, D, 1, (D <= 64 ? 4 : 1)>(stages, info, launch);
     default: return false;
   }
 }

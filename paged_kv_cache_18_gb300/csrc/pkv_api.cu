@@ -143,7 +143,9 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
   bool ok;
   const int stages = opt ? opt->stages : 0;
   if (kernel == PKV_KERNEL_MMA) {
-    ok = mma_kernel_info(s.dtype, s.qdtype, s.head_dim, ceil_div(per_cta, 8), stages, info);
+    const int warp_tiles = opt ? opt->warp_tiles : 0;
+    ok = mma_kernel_info(s.dtype, s.qdtype, s.head_dim, ceil_div(per_cta, 8), warp_tiles, stages,
+                         info);
   } else {
     if (stages != 0) return false;
     int r = 1;
@@ -157,6 +159,7 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
   pl->threads_per_cta = info->threads;
   pl->stages = info->stages;
   pl->smem_bytes = info->smem;
+  pl->warp_tiles = info->warp_tiles;
   return true;
 }
 
@@ -410,8 +413,8 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
     if (!encode_cache_map(&kmap, k_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks) ||
         !encode_cache_map(&vmap, v_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks))
       return PKV_ERR_CUDA;
-    e = mma_launch(s.dtype, s.qdtype, s.head_dim, ceil_div(pl.rows_per_cta, 8), pl.stages, kmap, vmap, p,
-                   grid, stream);
+    e = mma_launch(s.dtype, s.qdtype, s.head_dim, ceil_div(pl.rows_per_cta, 8), pl.warp_tiles,
+                   pl.stages, kmap, vmap, p, grid, stream);
   } else {
     int r = 1;
     while (r < pl.rows_per_cta) r <<= 1;

@@ -18,11 +18,16 @@ pytestmark = pytest.mark.gpu
 EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 100]
 
 
-def run_case(wl, kernel=0, split_blocks=0, stages=0):
+def run_case(wl, kernel=0, split_blocks=0, stages=0, warp_tiles=0):
     b = W.make_batch(wl)
     d = DeviceBatch(b)
     d.append()
-    out = d.attend(kernel=kernel, split_blocks=split_blocks, stages=stages)
+    import paged_kv_cache_18_gb300 as pkv
+    pkv.binding.TUNING["warp_tiles"] = warp_tiles
+    try:
+        out = d.attend(kernel=kernel, split_blocks=split_blocks, stages=stages)
+    finally:
+        pkv.binding.TUNING.pop("warp_tiles", None)
     torch.cuda.synchronize()
     ref = oracle_after_append(b)
     # the append is bit-exact over the whole cache
@@ -384,3 +389,31 @@ def test_chain_tree_equals_spec_verify_bitwise(kernel):
                                   max_context_len=b.max_context_len, kernel=kernel)
     s = d.attend(kernel=kernel)
     assert torch.equal(t, s)
+
+
+# Several 8-column query tiles in one warp (K / V fragments read once for
+# all of them): every tile count each head dim takes, ragged lengths,
+# partial last tiles and splits.
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D,warp_tiles,Q,Hq,Hkv", [
+    (128, 2, 3, 16, 4), (128, 2, 1, 16, 1), (128, 3, 5, 32, 8), (128, 3, 3, 24, 3),
+    (128, 3, 1, 24, 1), (64, 2, 2, 8, 1), (64, 3, 5, 16, 4), (64, 4, 4, 64, 8),
+    (64, 4, 7, 36, 9)])
+@pytest.mark.parametrize("split_blocks", [0, 3])
+def test_mma_multi_tile_warps(dtype, D, warp_tiles, Q, Hq, Hkv, split_blocks):
+    lens = [Q, 15, 16, 33, 250, 700]
+    wl = W.Workload(f"{dtype} D{D} nt{warp_tiles} Q{Q} {Hq}/{Hkv} sb{split_blocks}", len(lens),
+                    Hq, Hkv, D, dtype, context_lens=lens, num_queries=Q,
+                    seed=1300 + D + 7 * warp_tiles + Q + Hq + split_blocks)
+    assert -(-Q * (Hq // Hkv) // 8) == warp_tiles  # one column group of warp_tiles tiles
+    run_case(wl, kernel=2, split_blocks=split_blocks, warp_tiles=warp_tiles)
+
+
+def test_mma_multi_tile_rejects_oversize():
+    import paged_kv_cache_18_gb300 as pkv
+    pkv.binding.TUNING["warp_tiles"] = 2
+    try:
+        with pytest.raises(pkv.PkvError):  # two 8-column tiles of a 256-dim head per warp
+            pkv.plan(2, 3, 16, 4, 256, 100, torch.bfloat16, kernel=2)
+    finally:
+        pkv.binding.TUNING.pop("warp_tiles", None)
