@@ -44,8 +44,9 @@ FP8_K_SCALE, FP8_V_SCALE = 0.0123, 0.0171
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 # Sources whose change invalidates a recorded ncu traffic figure.
-KERNEL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mma.cu",
-                  "paged_kv_cache_18_gb300/csrc/attn_simt.cu",
+KERNEL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mma.cuh",
+                  "paged_kv_cache_18_gb300/csrc/attn_mma.cu",
+                  "paged_kv_cache_18_gb300/csrc/attn_simt.cuh",
                   "paged_kv_cache_18_gb300/csrc/pkv_device.cuh"]
 
 
@@ -277,7 +278,7 @@ def run_ours(args):
     barrier()
     import paged_kv_cache_18_gb300 as pkv
     pkv.binding.TUNING.update(rows_per_cta=args.rows_per_cta, merge=args.merge,
-                              warp_tiles=args.warp_tiles)
+                              warp_tiles=args.warp_tiles, blocks_per_iter=args.blocks_per_iter)
 
     wl = W.WORKLOADS[args.workload]
     if rank > 0:
@@ -376,6 +377,7 @@ def run_ours(args):
     # End to end through the public API: inputs from pinned host memory,
     # output read back, every step.
     e2e = None
+    kv_step = b.kv_bytes() // W.ELT_BYTES[wl.dtype] if fp8 else b.kv_bytes()  # 1 byte / element
     if not args.no_e2e:
         host = {n: t.cpu().pin_memory() for n, t in
                 (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots),
@@ -411,7 +413,6 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
                "ms_per_step": 1e3 * e2e_s}
 
-    kv_step = b.kv_bytes() // W.ELT_BYTES[wl.dtype] if fp8 else b.kv_bytes()  # 1 byte / element
     total_kv = dist_sum(kv_step, dev)
     total_tokens = dist_sum(wl.batch * Q, dev)
     if rank != 0:
@@ -487,6 +488,8 @@ def main(argv=None):
     ap.add_argument("--merge", type=int, default=0, help="0 planner, 1 fused, 2 separate kernel")
     ap.add_argument("--warp-tiles", type=int, default=0,
                     help="tensor-core kernel: 8-column query tiles per warp (0 planner)")
+    ap.add_argument("--blocks-per-iter", type=int, default=0,
+                    help="tensor-core kernel: KV blocks per warp loop iteration (0 planner)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",

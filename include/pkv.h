@@ -115,6 +115,8 @@ typedef struct pkv_options {
                        2 by a separate kernel */
   int warp_tiles;   /* 0: planner; tensor-core kernel: 8-column query tiles
                        per warp (1..3 at head_dim <= 128, 1..4 at 64, 1 at 256) */
+  int blocks_per_iter; /* 0: planner; tensor-core kernel: KV blocks one warp
+                          takes per loop iteration (1 or 2; 2 with one tile) */
 } pkv_options;
 
 /* What one attention call launches (see pkv_attention_plan). */
@@ -133,6 +135,7 @@ typedef struct pkv_plan {
   int merge_kernel;       /* 1: a separate split-K merge launch follows;
                              0: no split, or the last CTA of each sequence merges */
   int warp_tiles;         /* tensor-core kernel: 8-column query tiles per warp */
+  int blocks_per_iter;    /* tensor-core kernel: KV blocks per loop iteration */
 } pkv_plan;
 
 /* Human-readable name of a status code (static string). */

@@ -46,12 +46,13 @@ class PkvError(RuntimeError):
 class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("split_blocks", ctypes.c_int),
                 ("stages", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
-                ("merge", ctypes.c_int), ("warp_tiles", ctypes.c_int)]
+                ("merge", ctypes.c_int), ("warp_tiles", ctypes.c_int),
+                ("blocks_per_iter", ctypes.c_int)]
 
 
 # Extra launch controls for tuning runs (pkv_options.rows_per_cta / .merge /
-# .warp_tiles); module-wide so that every binding call passes them.  Empty =
-# planner.
+# .warp_tiles / .blocks_per_iter); module-wide so that every binding call
+# passes them.  Empty = planner.
 TUNING = {}
 
 
@@ -63,7 +64,8 @@ class Plan(ctypes.Structure):
                 ("threads_per_cta", ctypes.c_int), ("stages", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int),
                 ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
-                ("merge_kernel", ctypes.c_int), ("warp_tiles", ctypes.c_int)]
+                ("merge_kernel", ctypes.c_int), ("warp_tiles", ctypes.c_int),
+                ("blocks_per_iter", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -138,9 +140,10 @@ def _stream(t: torch.Tensor) -> int:
 def _opts(kernel: int, split_blocks: int, stages: int = 0, warp_tiles: int = 0):
     rows, merge = TUNING.get("rows_per_cta", 0), TUNING.get("merge", 0)
     warp_tiles = warp_tiles or TUNING.get("warp_tiles", 0)
-    if not any((kernel, split_blocks, stages, rows, merge, warp_tiles)):
+    kb = TUNING.get("blocks_per_iter", 0)
+    if not any((kernel, split_blocks, stages, rows, merge, warp_tiles, kb)):
         return None
-    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge, warp_tiles))
+    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge, warp_tiles, kb))
 
 
 def _need(cond: bool, msg: str) -> None:

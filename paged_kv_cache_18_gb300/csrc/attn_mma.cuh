@@ -125,10 +125,15 @@ __device__ __forceinline__ void lane_sync(int id, int count) {
 // one-byte codes, widened to f16 for f16 MMAs; q then enters as f16 after a
 // per-row power-of-two shift that keeps it in f16 range, undone in the score
 // scale).
-template <typename T, typename TC, int D, int CG, int NT, int BL, int NS>
-__global__ void __launch_bounds__(BL * CG * 32)
+// Resident CTAs a kernel is compiled for: the three-warp tile fits six per
+// SM in shared memory, which its registers must then allow (<= 112 each).
+template <int CG, int NT> constexpr int mma_min_ctas() { return (CG >= 3 && NT == 1) ? 6 : 1; }
+
+template <typename T, typename TC, int D, int CG, int NT, int KB, int BL, int NS>
+__global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+  static_assert(NS >= KB, "an iteration's blocks must all be in flight at once");
   constexpr bool FP8 = std::is_same<TC, E4M3>::value;
   using TM = typename MmaType<T, TC>::type;
   using G = MmaGeom<D, Elt<TC>::bytes>;
@@ -293,96 +298,123 @@ __global__ void __launch_bounds__(BL * CG * 32)
 
   int consumed = 0;
   bool aborted = false;
-  for (int i = 0; i < n_my; ++i) {
-    const int s = i % NS;
-    // A copy that never lands aborts the CTA (with column groups, through a
-    // shared flag): from then on no warp waits or computes, but every warp
-    // still takes part in each lane_sync.
-    if (!aborted && !mbar_wait_bounded(my_bars + 8 * s, (i / NS) & 1)) {
-      aborted = true;
-      if (CG > 1) s_abort = 1;
-      if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT);
+  for (int i0 = 0; i0 < n_my; i0 += KB) {
+    // This iteration's KB blocks (the last may hold fewer).  A copy that
+    // never lands aborts the CTA (with column groups, through a shared
+    // flag): from then on no warp waits or computes, but every warp still
+    // takes part in each lane_sync.
+    bool has[KB], bad[KB];
+    int key0[KB];
+    uint32_t ktile[KB], vtile[KB];
+#pragma unroll
+    for (int u = 0; u < KB; ++u) {
+      const int i = i0 + u;
+      const int s = i % NS;
+      has[u] = KB == 1 || i < n_my;
+      if (has[u] && !aborted) {
+        // one decision per warp: its lanes then agree on every later shuffle
+        if (__all_sync(kFull, mbar_wait_bounded(my_bars + 8 * s, (i / NS) & 1))) {
+          consumed = i + 1;
+        } else {
+          aborted = true;
+          if (CG > 1) s_abort = 1;
+          if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT);
+        }
+      }
+      ktile[u] = my_stages + s * G::kStageBytes;
+      vtile[u] = ktile[u] + G::kTileBytes;
+      key0[u] = (blk_begin + bl + i * BL) * kBlockSize;
+      bad[u] = !has[u] || ((bad_mask >> (i & 31)) & 1u);
     }
     if (CG > 1 && !aborted) aborted = s_abort != 0;
     const bool live = !aborted;
-    if (live) consumed = i + 1;
-    const uint32_t ktile = my_stages + s * G::kStageBytes;
-    const uint32_t vtile = ktile + G::kTileBytes;
-    const int key0 = (blk_begin + bl + i * BL) * kBlockSize;
-    const bool bad = (bad_mask >> (i & 31)) & 1u;
     if constexpr (!FP8) {  // the fused append (16-bit caches only)
-      if (p.k_new != nullptr && !bad && key0 + kBlockSize > L - p.num_queries) {
-        if (leader && live) {
-          const int64_t phys = __ldg(table + static_cast<int64_t>(i) * BL);
-          patch_new_rows<D, 2>(p, ktile, vtile, b, kvh, key0, L, phys, chunk == 0,
-                               [](int r, int vec) { return swz<D>(r, vec * 8); });
+      if (p.k_new != nullptr) {
+        bool any = false;
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          if (bad[u] || key0[u] + kBlockSize <= L - p.num_queries) continue;
+          any = true;
+          if (leader && live) {
+            const int64_t phys = __ldg(table + static_cast<int64_t>(i0 + u) * BL);
+            patch_new_rows<D, 2>(p, ktile[u], vtile[u], b, kvh, key0[u], L, phys, chunk == 0,
+                                 [](int r, int vec) { return swz<D>(r, vec * 8); });
+          }
         }
-        lane_sync(1 + bl, CG);
+        if (any) lane_sync(1 + bl, CG);
       }
     }
 
     if (live) {
-      // S^T = K Q^T.  One tile: the head-dim steps spread over four
-      // accumulator chains; several tiles: their MMAs interleave.
-      constexpr int NCH = NT == 1 ? (KS < 4 ? KS : 4) : (NT == 2 ? 2 : 1);
-      float acc[NCH][NT][4];
+      // S^T = K Q^T per block.  One tile of one block: the head-dim steps
+      // spread over four accumulator chains; otherwise the tiles' and
+      // blocks' MMAs interleave.  (A block past the sequence's end, in the
+      // last iteration, is computed on whatever its stage holds and masked
+      // out entirely.)
+      constexpr int NCH = (NT * KB) == 1 ? (KS < 4 ? KS : 4) : ((NT * KB) == 2 ? 2 : 1);
+      float sc[KB][NT][4];
+      bool above = false;  // some score exceeds its column's reference by > the slack
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch)
+      for (int u = 0; u < KB; ++u) {
+        float acc[NCH][NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          acc[ch][nt][0] = acc[ch][nt][1] = acc[ch][nt][2] = acc[ch][nt][3] = 0.f;
-      if constexpr (!FP8) {
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a[4];
-          ldsm_x4(a, ktile + swz<D>(lane & 15, ks * 16 + (lane >> 4) * 8));
+        for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            Mma<TM>::run(acc[ks % NCH][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
-        }
-      } else {
-        // One ldmatrix brings 16 keys x 32 head dims of codes: lane (g, c)
-        // gets 4 consecutive codes of keys g and g + 8 from each 16-byte half.
+            acc[ch][nt][0] = acc[ch][nt][1] = acc[ch][nt][2] = acc[ch][nt][3] = 0.f;
+        if constexpr (!FP8) {
 #pragma unroll
-        for (int pr = 0; pr < KS / 2; ++pr) {
-          uint32_t r[4];
-          ldsm_x4(r, ktile + swzb(lane & 15, pr * 32 + (lane >> 4) * 16));
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
+          for (int ks = 0; ks < KS; ++ks) {
             uint32_t a[4];
-            e4m3x4_to_f16(r[2 * u], a[0], a[2]);      // key g: dims 4c, 4c+1 | 4c+2, 4c+3
-            e4m3x4_to_f16(r[2 * u + 1], a[1], a[3]);  // key g + 8
-            const int ks = 2 * pr + u;
+            ldsm_x4(a, ktile[u] + swz<D>(lane & 15, ks * 16 + (lane >> 4) * 8));
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               Mma<TM>::run(acc[ks % NCH][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
           }
-        }
-      }
-      float sc[NT][4];
-      const bool need_mask = bad || key0 + kBlockSize > mask_from;
-      bool above = false;  // some score exceeds its column's reference by > the slack
+        } else {
+          // One ldmatrix brings 16 keys x 32 head dims of codes: lane (g, c)
+          // gets 4 consecutive codes of keys g and g + 8 from each 16-byte
+          // half.
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+          for (int pr = 0; pr < KS / 2; ++pr) {
+            uint32_t r[4];
+            ldsm_x4(r, ktile[u] + swzb(lane & 15, pr * 32 + (lane >> 4) * 16));
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float t = acc[0][nt][e];
+            for (int h = 0; h < 2; ++h) {
+              uint32_t a[4];
+              e4m3x4_to_f16(r[2 * h], a[0], a[2]);      // key g: dims 4c, 4c+1 | 4c+2, 4c+3
+              e4m3x4_to_f16(r[2 * h + 1], a[1], a[3]);  // key g + 8
+              const int ks = 2 * pr + h;
 #pragma unroll
-          for (int ch = 1; ch < NCH; ++ch) t += acc[ch][nt][e];
-          float v = t * colfac[nt][e & 1];
-          if (need_mask) {
-            const int col = col0 + nt * 8 + 2 * c + (e & 1);
-            if (!key_visible(p, key0 + g + ((e >> 1) << 3), L, bad, s_lim[col], s_tm[col]))
-              v = -INFINITY;
+              for (int nt = 0; nt < NT; ++nt)
+                Mma<TM>::run(acc[ks % NCH][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+            }
           }
-          sc[nt][e] = v;
-          above |= v > m[nt][e & 1] + kRescaleSlack;
+        }
+        const bool need_mask = bad[u] || key0[u] + kBlockSize > mask_from;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float t = acc[0][nt][e];
+#pragma unroll
+            for (int ch = 1; ch < NCH; ++ch) t += acc[ch][nt][e];
+            float v = t * colfac[nt][e & 1];
+            if (need_mask) {
+              const int col = col0 + nt * 8 + 2 * c + (e & 1);
+              if (!key_visible(p, key0[u] + g + ((e >> 1) << 3), L, bad[u], s_lim[col],
+                               s_tm[col]))
+                v = -INFINITY;
+            }
+            sc[u][nt][e] = v;
+            above |= v > m[nt][e & 1] + kRescaleSlack;
+          }
         }
       }
       // Online softmax.  The exponentials use a per-column reference m that
       // is raised (to the exact running max, rescaling l and O by
       // 2^(m_old - m)) only when a score exceeds it by more than
-      // kRescaleSlack; otherwise the block's weights 2^(s - m) stay below
+      // kRescaleSlack; otherwise the weights 2^(s - m) stay below
       // 2^kRescaleSlack and no cross-lane max, correction or rescale is
       // needed.  The result O / l does not depend on the reference.
       if (__any_sync(kFull, above)) {
@@ -390,7 +422,9 @@ __global__ void __launch_bounds__(BL * CG * 32)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float mx = fmaxf(sc[nt][e], sc[nt][e + 2]);
+            float mx = fmaxf(sc[0][nt][e], sc[0][nt][e + 2]);
+#pragma unroll
+            for (int u = 1; u < KB; ++u) mx = fmaxf(mx, fmaxf(sc[u][nt][e], sc[u][nt][e + 2]));
             mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
@@ -405,72 +439,97 @@ __global__ void __launch_bounds__(BL * CG * 32)
             }
           }
       }
+      // Weights, and the P^T operand fragments.  bf16 / f16 MMAs on 16-bit
+      // caches: high part and rounding remainder (a single bf16 P would add
+      // about 1.6e-3 of relative error).  FP8 caches: one f16 P (weights
+      // <= 2^8; 2^-11 relative rounding).
+      uint32_t ph[KB][NT][2], pl[KB][NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float m_use = m[nt][e] == -INFINITY ? 0.f : m[nt][e];
-          const float p0 = ex2(sc[nt][e] - m_use);
-          const float p1 = ex2(sc[nt][e + 2] - m_use);
-          l[nt][e] += p0 + p1;
-          sc[nt][e] = p0;
-          sc[nt][e + 2] = p1;
-        }
-      // P^T operand fragments.  bf16 / f16 MMAs on 16-bit caches: high part
-      // and rounding remainder (a single bf16 P would add about 1.6e-3 of
-      // relative error).  FP8 caches: one f16 P (weights <= 2^8; 2^-11
-      // relative rounding).
-      uint32_t ph[NT][2], pl[NT][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t h01 = Mma<TM>::pack(sc[nt][0], sc[nt][1]);
-        const uint32_t h23 = Mma<TM>::pack(sc[nt][2], sc[nt][3]);
-        ph[nt][0] = movm_t(h01);
-        ph[nt][1] = movm_t(h23);
-        pl[nt][0] = pl[nt][1] = 0u;
-        if constexpr (!FP8) {
-          float r0, r1, r2, r3;
-          Mma<TM>::unpack(h01, r0, r1);
-          Mma<TM>::unpack(h23, r2, r3);
-          pl[nt][0] = movm_t(Mma<TM>::pack(sc[nt][0] - r0, sc[nt][1] - r1));
-          pl[nt][1] = movm_t(Mma<TM>::pack(sc[nt][2] - r2, sc[nt][3] - r3));
+          for (int u = 0; u < KB; ++u) {
+            const float p0 = ex2(sc[u][nt][e] - m_use);
+            const float p1 = ex2(sc[u][nt][e + 2] - m_use);
+            l[nt][e] += p0 + p1;
+            sc[u][nt][e] = p0;
+            sc[u][nt][e + 2] = p1;
+          }
         }
-      }
+#pragma unroll
+      for (int u = 0; u < KB; ++u)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t h01 = Mma<TM>::pack(sc[u][nt][0], sc[u][nt][1]);
+          const uint32_t h23 = Mma<TM>::pack(sc[u][nt][2], sc[u][nt][3]);
+          ph[u][nt][0] = movm_t(h01);
+          ph[u][nt][1] = movm_t(h23);
+          pl[u][nt][0] = pl[u][nt][1] = 0u;
+          if constexpr (!FP8) {
+            float r0, r1, r2, r3;
+            Mma<TM>::unpack(h01, r0, r1);
+            Mma<TM>::unpack(h23, r2, r3);
+            pl[u][nt][0] = movm_t(Mma<TM>::pack(sc[u][nt][0] - r0, sc[u][nt][1] - r1));
+            pl[u][nt][1] = movm_t(Mma<TM>::pack(sc[u][nt][2] - r2, sc[u][nt][3] - r3));
+          }
+        }
       // O^T += V^T P^T.  In a block that ends past the context, zero the V^T
       // columns (keys) past it so that NaN-filled rows never enter an MMA.
-      const int nvalid = bad ? 0 : L - key0;
+      int nvalid[KB];
+      bool full = true;
+#pragma unroll
+      for (int u = 0; u < KB; ++u) {
+        nvalid[u] = bad[u] ? 0 : L - key0[u];
+        full = full && nvalid[u] >= kBlockSize;
+      }
       auto pv = [&](auto partial) {
-        uint32_t km0 = 0xffffffffu, km8 = 0xffffffffu;
-        if (decltype(partial)::value) {
-          km0 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
-          km8 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
+        uint32_t km0[KB], km8[KB];
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          km0[u] = km8[u] = 0xffffffffu;
+          if (decltype(partial)::value) {
+            const int nv = nvalid[u];
+            km0[u] = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
+            km8[u] = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
+          }
         }
         if constexpr (!FP8) {
-          // Head-dim tiles a group at a time: their high-part MMAs first,
-          // then the low parts, so that no MMA waits on the one just issued.
-          constexpr int GRP = NT > 1 ? 2 : (KS < 4 ? KS : 4);
+          // Head-dim tiles a group at a time: the high-part MMAs of every
+          // block first, then the low parts, so that no MMA waits on the
+          // one just issued.
+          constexpr int GRP = (NT * KB) > 1 ? 2 : (KS < 4 ? KS : 4);
 #pragma unroll
           for (int m0 = 0; m0 < KS; m0 += GRP) {
-            uint32_t a[GRP][4];
+            uint32_t a[KB][GRP][4];
 #pragma unroll
-            for (int u = 0; u < GRP; ++u) {
-              ldsm_x4_t(a[u], vtile + swz<D>((lane & 7) + ((lane >> 4) << 3),
-                                             (m0 + u) * 16 + ((lane >> 3) & 1) * 8));
-              if (decltype(partial)::value) {
-                a[u][0] &= km0;
-                a[u][1] &= km0;
-                a[u][2] &= km8;
-                a[u][3] &= km8;
+            for (int u = 0; u < KB; ++u)
+#pragma unroll
+              for (int w = 0; w < GRP; ++w) {
+                ldsm_x4_t(a[u][w], vtile[u] + swz<D>((lane & 7) + ((lane >> 4) << 3),
+                                                     (m0 + w) * 16 + ((lane >> 3) & 1) * 8));
+                if (decltype(partial)::value) {
+                  a[u][w][0] &= km0[u];
+                  a[u][w][1] &= km0[u];
+                  a[u][w][2] &= km8[u];
+                  a[u][w][3] &= km8[u];
+                }
               }
-            }
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int u = 0; u < KB; ++u)
 #pragma unroll
-              for (int u = 0; u < GRP; ++u) Mma<TM>::run(o[m0 + u][nt], a[u], ph[nt][0], ph[nt][1]);
+              for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                for (int w = 0; w < GRP; ++w)
+                  Mma<TM>::run(o[m0 + w][nt], a[u][w], ph[u][nt][0], ph[u][nt][1]);
 #pragma unroll
-              for (int u = 0; u < GRP; ++u) Mma<TM>::run(o[m0 + u][nt], a[u], pl[nt][0], pl[nt][1]);
+            for (int u = 0; u < KB; ++u)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int w = 0; w < GRP; ++w)
+                  Mma<TM>::run(o[m0 + w][nt], a[u][w], pl[u][nt][0], pl[u][nt][1]);
           }
         } else {
           // V^T fragments from codes: one transposed ldmatrix of byte pairs
@@ -479,41 +538,47 @@ __global__ void __launch_bounds__(BL * CG * 32)
           // byte permute pairs the two keys of each dim (see o_dim).
 #pragma unroll
           for (int pr = 0; pr < KS / 2; ++pr) {
-            uint32_t r[4];
-            ldsm_x4_t(r, vtile + swzb(lane & 15, pr * 32 + (lane >> 4) * 16));
-            uint32_t a[2][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              // r[j]: keys (2c | 2c+8) and (2c+1 | 2c+9), dims 2g, 2g+1
-              uint32_t lo, hi;
-              e4m3x4_to_f16(prmt(r[j], 0u, 0x3120), lo, hi);
-              a[j >> 1][(j & 1) * 2] = lo;       // dim 2g
-              a[j >> 1][(j & 1) * 2 + 1] = hi;   // dim 2g + 1
-            }
+            for (int u = 0; u < KB; ++u) {
+              uint32_t r[4];
+              ldsm_x4_t(r, vtile[u] + swzb(lane & 15, pr * 32 + (lane >> 4) * 16));
+              uint32_t a[2][4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              if (decltype(partial)::value) {
-                a[u][0] &= km0;
-                a[u][1] &= km0;
-                a[u][2] &= km8;
-                a[u][3] &= km8;
+              for (int j = 0; j < 4; ++j) {
+                // r[j]: keys (2c | 2c+8) and (2c+1 | 2c+9), dims 2g, 2g+1
+                uint32_t lo, hi;
+                e4m3x4_to_f16(prmt(r[j], 0u, 0x3120), lo, hi);
+                a[j >> 1][(j & 1) * 2] = lo;       // dim 2g
+                a[j >> 1][(j & 1) * 2 + 1] = hi;   // dim 2g + 1
               }
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                Mma<TM>::run(o[2 * pr + u][nt], a[u], ph[nt][0], ph[nt][1]);
+              for (int h = 0; h < 2; ++h) {
+                if (decltype(partial)::value) {
+                  a[h][0] &= km0[u];
+                  a[h][1] &= km0[u];
+                  a[h][2] &= km8[u];
+                  a[h][3] &= km8[u];
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  Mma<TM>::run(o[2 * pr + h][nt], a[h], ph[u][nt][0], ph[u][nt][1]);
+              }
             }
           }
         }
       };
-      if (nvalid < kBlockSize)
-        pv(std::true_type{});
-      else
+      if (full)
         pv(std::false_type{});
+      else
+        pv(std::true_type{});
     }
-    lane_sync(1 + bl, CG);  // every warp of the lane is done with stage s
-    if (i + NS < n_my) {
-      if (!aborted) issue(i + NS);
-      ++issued;
+    lane_sync(1 + bl, CG);  // every warp of the lane is done with these stages
+#pragma unroll
+    for (int u = 0; u < KB; ++u) {
+      if (i0 + u + NS < n_my && !aborted) {
+        issue(i0 + u + NS);
+        ++issued;
+      }
     }
   }
   if (aborted && leader && lane == 0) {
@@ -599,25 +664,26 @@ constexpr size_t mma_smem_bytes() {
 using MmaLaunch = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const AttnParams &,
                                   dim3, cudaStream_t);
 
-template <typename T, typename TC, int D, int CG, int NT, bool DEEP>
+template <typename T, typename TC, int D, int CG, int NT, int KB, bool DEEP>
 KernelInfo mma_info_t() {
   constexpr int BL = mma_lanes<CG>();
   KernelInfo k;
   k.func = reinterpret_cast<const void *>(
-      &attn_mma_kernel<T, TC, D, CG, NT, BL, mma_stages_t<TC, D, CG, DEEP>()>);
+      &attn_mma_kernel<T, TC, D, CG, NT, KB, BL, mma_stages_t<TC, D, CG, DEEP>()>);
   k.threads = BL * CG * 32;
   k.smem = mma_smem_bytes<T, TC, D, CG, NT, DEEP>();
   k.warps = BL * CG;
   k.stages = mma_stages_t<TC, D, CG, DEEP>();
   k.warp_tiles = NT;
+  k.blocks_per_iter = KB;
   return k;
 }
 
-template <typename T, typename TC, int D, int CG, int NT, bool DEEP>
+template <typename T, typename TC, int D, int CG, int NT, int KB, bool DEEP>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
-  const KernelInfo k = mma_info_t<T, TC, D, CG, NT, DEEP>();
-  attn_mma_kernel<T, TC, D, CG, NT, mma_lanes<CG>(), mma_stages_t<TC, D, CG, DEEP>()>
+  const KernelInfo k = mma_info_t<T, TC, D, CG, NT, KB, DEEP>();
+  attn_mma_kernel<T, TC, D, CG, NT, KB, mma_lanes<CG>(), mma_stages_t<TC, D, CG, DEEP>()>
       <<<grid, k.threads, k.smem, stream>>>(km, vm, p);
   return cudaGetLastError();
 }
@@ -625,20 +691,38 @@ cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnPar
 // Default ring: the shallow one (for one column group at head_dim <= 128,
 // 3 CTAs per SM; the 8-row GQA tile measured 0.949 of the HBM peak against
 // 0.932 with the deep ring).
-template <typename T, typename TC, int D, int CG, int NT>
+//
+// A warp waits for the KB blocks of an iteration before it issues the next
+// ones, so KB blocks per iteration need a ring of at least KB stages (else
+// the wait could never end); rings of fewer than 2 KB stages are not built
+// either (no pair in flight while a pair is computed).
+template <typename T, typename TC, int D, int CG, int NT, int KB, bool DEEP>
+bool mma_pick_ring(KernelInfo *info, MmaLaunch *launch) {
+  if constexpr (KB > 1 && mma_stages_t<TC, D, CG, DEEP>() < 2 * KB) {
+    return false;
+  } else {
+    *info = mma_info_t<T, TC, D, CG, NT, KB, DEEP>();
+    *launch = &launch_t<T, TC, D, CG, NT, KB, DEEP>;
+    return true;
+  }
+}
+
+template <typename T, typename TC, int D, int CG, int NT, int KB>
 bool mma_pick_stages(int stages, KernelInfo *info, MmaLaunch *launch) {
   if (stages == 0) stages = mma_stages_t<TC, D, CG, false>();
-  if (stages == mma_stages_t<TC, D, CG, true>()) {
-    *info = mma_info_t<T, TC, D, CG, NT, true>();
-    *launch = &launch_t<T, TC, D, CG, NT, true>;
-    return true;
-  }
-  if (stages == mma_stages_t<TC, D, CG, false>()) {
-    *info = mma_info_t<T, TC, D, CG, NT, false>();
-    *launch = &launch_t<T, TC, D, CG, NT, false>;
-    return true;
-  }
+  if (stages == mma_stages_t<TC, D, CG, true>())
+    return mma_pick_ring<T, TC, D, CG, NT, KB, true>(info, launch);
+  if (stages == mma_stages_t<TC, D, CG, false>())
+    return mma_pick_ring<T, TC, D, CG, NT, KB, false>(info, launch);
   return false;
+}
+
+// Blocks per iteration: one or two for single-tile warps (two need rings of
+// four stages or more to keep a pair in flight), one for multi-tile warps.
+template <typename T, typename TC, int D, int CG>
+bool mma_pick_kb(int kb, int stages, KernelInfo *info, MmaLaunch *launch) {
+  if (kb == 2) return mma_pick_stages<T, TC, D, CG, 1, 2>(stages, info, launch);
+  return kb == 1 && mma_pick_stages<T, TC, D, CG, 1, 1>(stages, info, launch);
 }
 
 // Column groups x tiles per warp x head dim within the register and shared
@@ -646,24 +730,24 @@ bool mma_pick_stages(int stages, KernelInfo *info, MmaLaunch *launch) {
 // cg * D <= 384.  Several tiles in one warp (its O^T accumulators hold
 // nt * D / 4 floats per thread): nt * D <= 384, one column group.
 template <typename T, typename TC, int D>
-bool mma_pick(int cg, int nt, int stages, KernelInfo *info, MmaLaunch *launch) {
+bool mma_pick(int cg, int nt, int kb, int stages, KernelInfo *info, MmaLaunch *launch) {
   if (nt == 1) {
     switch (cg) {
-      case 1: return mma_pick_stages<T, TC, D, 1, 1>(stages, info, launch);
-      case 2:
-        return D <= 128 && mma_pick_stages<T, TC, D, (D <= 128 ? 2 : 1), 1>(stages, info, launch);
-      case 3:
-        return D <= 128 && mma_pick_stages<T, TC, D, (D <= 128 ? 3 : 1), 1>(stages, info, launch);
-      case 4:
-        return D <= 64 && mma_pick_stages<T, TC, D, (D <= 64 ? 4 : 1), 1>(stages, info, launch);
+      case 1: return mma_pick_kb<T, TC, D, 1>(kb, stages, info, launch);
+      case 2: return D <= 128 && mma_pick_kb<T, TC, D, (D <= 128 ? 2 : 1)>(kb, stages, info, launch);
+      case 3: return D <= 128 && mma_pick_kb<T, TC, D, (D <= 128 ? 3 : 1)>(kb, stages, info, launch);
+      case 4: return D <= 64 && mma_pick_kb<T, TC, D, (D <= 64 ? 4 : 1)>(kb, stages, info, launch);
       default: return false;
     }
   }
-  if (cg != 1) return false;
+  if (cg != 1 || kb != 1) return false;
   switch (nt) {
-    case 2: return D <= 128 && mma_pick_stages<T, TC, D, 1, (D <= 128 ? 2 : 1)>(stages, info, launch);
-    case 3: return D <= 128 && mma_pick_stages<T, TC, D, 1, (D <= 128 ? 3 : 1)>(stages, info, launch);
-    case 4: return D <= 64 && mma_pick_stages<T, TC, D, 1, (D <= 64 ? 4 : 1)>(stages, info, launch);
+    case 2:
+      return D <= 128 && mma_pick_stages<T, TC, D, 1, (D <= 128 ? 2 : 1), 1>(stages, info, launch);
+    case 3:
+      return D <= 128 && mma_pick_stages<T, TC, D, 1, (D <= 128 ? 3 : 1), 1>(stages, info, launch);
+    case 4:
+      return D <= 64 && mma_pick_stages<T, TC, D, 1, (D <= 64 ? 4 : 1), 1>(stages, info, launch);
     default: return false;
   }
 }

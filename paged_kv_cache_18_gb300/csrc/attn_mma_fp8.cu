@@ -9,18 +9,19 @@ namespace pkv {
 namespace mma {
 
 template <typename T>
-bool pick_fp8_d(int D, int cg, int nt, int stages, KernelInfo *info, MmaLaunch *launch) {
+bool pick_fp8_d(int D, int cg, int nt, int kb, int stages, KernelInfo *info, MmaLaunch *launch) {
   switch (D) {
-    case 128: return mma_pick<T, E4M3, 128>(cg, nt, stages, info, launch);
-    case 256: return mma_pick<T, E4M3, 256>(cg, nt, stages, info, launch);
+    case 128: return mma_pick<T, E4M3, 128>(cg, nt, kb, stages, info, launch);
+    case 256: return mma_pick<T, E4M3, 256>(cg, nt, kb, stages, info, launch);
     default: return false;
   }
 }
 
-bool pick_fp8(pkv_dtype q_dtype, int D, int cg, int nt, int stages, KernelInfo *info,
+bool pick_fp8(pkv_dtype q_dtype, int D, int cg, int nt, int kb, int stages, KernelInfo *info,
               MmaLaunch *launch) {
-  if (q_dtype == PKV_BF16) return pick_fp8_d<__nv_bfloat16>(D, cg, nt, stages, info, launch);
-  if (q_dtype == PKV_F16) return pick_fp8_d<__half>(D, cg, nt, stages, info, launch);
+  if (q_dtype == PKV_BF16)
+    return pick_fp8_d<__nv_bfloat16>(D, cg, nt, kb, stages, info, launch);
+  if (q_dtype == PKV_F16) return pick_fp8_d<__half>(D, cg, nt, kb, stages, info, launch);
   return false;
 }
 

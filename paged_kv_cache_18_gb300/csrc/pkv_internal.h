@@ -19,19 +19,25 @@ struct KernelInfo {
   int warps = 0;
   int stages = 0;
   int warp_tiles = 1;
+  int blocks_per_iter = 1;
   size_t smem = 0;
 };
 
-// Tensor-core kernel: n_tiles = query columns / 8, warp_tiles of them per
-// warp (0 = one); stages = per-lane ring depth (0 = default).  The cache type
-// is q's 16-bit type, or FP8 E4M3 with bf16 / f16 q (head_dim 128 or 256).
+// Tensor-core kernel shape: n_tiles = query columns / 8, warp_tiles of them
+// per warp (0 = one), blocks_per_iter KV blocks per loop iteration (0 =
+// one), stages = per-lane ring depth (0 = default).
+struct MmaShape {
+  int n_tiles, warp_tiles, blocks_per_iter, stages;
+};
+
+// The cache type is q's 16-bit type, or FP8 E4M3 with bf16 / f16 q
+// (head_dim 128 or 256).
 int mma_max_tiles(int head_dim);
-bool mma_kernel_info(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int n_tiles,
-                     int warp_tiles, int stages, KernelInfo *info);
-cudaError_t mma_launch(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int n_tiles,
-                       int warp_tiles, int stages, const CUtensorMap &kmap,
-                       const CUtensorMap &vmap, const AttnParams &p, dim3 grid,
-                       cudaStream_t stream);
+bool mma_kernel_info(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, const MmaShape &m,
+                     KernelInfo *info);
+cudaError_t mma_launch(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, const MmaShape &m,
+                       const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
+                       dim3 grid, cudaStream_t stream);
 
 // CUDA-core kernel: rows = query rows per CTA (1, 2, 4 or 8); the cache type
 // may be FP8 E4M3 with q of another type, else both types are equal.

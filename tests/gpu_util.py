@@ -1,6 +1,8 @@
 """Helpers of the GPU parity tests: move a seeded batch to the device, run one
 step (append, then attention) through the C ABI, and compare with the
 float64 oracle."""
+import contextlib
+
 import numpy as np
 import torch
 
@@ -93,11 +95,23 @@ def errors(got: np.ndarray, ref: np.ndarray):
 
 
 def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what=""):
-    assert np.isfinite(got[~np.isnan(ref)]).all(), f"{what}: non-finite output"
+    """The stated bound per element, max-abs tol_abs, except where the output
+    type cannot hold it: a bf16 output of |ref| >= 2.56 is already up to half
+    an ulp (> 1e-2) from the exact value when correctly rounded (for example
+    4.07614 -> 4.0625), so there the bound is that half ulp plus 1e-3 of
+    arithmetic error.  Relative L2 over all elements: tol_rel."""
+    mask = ~np.isnan(ref)
+    assert np.isfinite(got[mask]).all(), f"{what}: non-finite output"
     max_abs, rel = errors(got, ref)
     tol_abs, tol_rel = TOL[dtype]
-    assert max_abs <= tol_abs and rel <= tol_rel, \
-        f"{what}: max-abs {max_abs:.3e} (tol {tol_abs}), rel-L2 {rel:.3e} (tol {tol_rel})"
+    d = np.abs(got[mask] - ref[mask])
+    bound = np.full(d.shape, tol_abs)
+    if dtype != "f32":
+        bound = np.maximum(bound, half_ulp(ref[mask], dtype) + 1e-3)
+    worst = float((d - bound).max()) if d.size else 0.0
+    assert worst <= 0 and rel <= tol_rel, \
+        (f"{what}: max-abs {max_abs:.3e} (tol {tol_abs}, or half an output ulp + 1e-3 where "
+         f"that is larger), rel-L2 {rel:.3e} (tol {tol_rel})")
     return max_abs, rel
 
 
@@ -134,3 +148,16 @@ def assert_close_fp8(got: np.ndarray, ref: np.ndarray, dtype: str, what=""):
         (f"{what}: max (|err| - half ulp) {worst:.3e} (tol {FP8_EXTRA[dtype]}), "
          f"rel-L2 {rel:.3e} (tol {tol_rel})")
     return float(d.max()) if d.size else 0.0, rel
+
+
+@contextlib.contextmanager
+def tuning(**kw):
+    """Pass extra launch controls (pkv_options fields) to every binding call
+    inside the block."""
+    saved = dict(pkv.binding.TUNING)
+    pkv.binding.TUNING.update(kw)
+    try:
+        yield
+    finally:
+        pkv.binding.TUNING.clear()
+        pkv.binding.TUNING.update(saved)

@@ -8,7 +8,7 @@ import torch
 import oracle
 import paged_kv_cache_18_gb300 as pkv
 from paged_kv_cache_18_gb300 import workloads as W
-from tests.gpu_util import TORCH_DT, assert_close_fp8, dev_tensor, host_f64
+from tests.gpu_util import TORCH_DT, assert_close_fp8, dev_tensor, host_f64, tuning
 
 pytestmark = pytest.mark.gpu
 
@@ -133,3 +133,17 @@ def test_fp8_rejected_by_16bit_entry_points():
     st = L.pkv_paged_decode_attention(16, 16, 16, 16, 16, 2, 16, 20, 1, 4, 4, 128, 16, 10, 0.1,
                                       3, None, 0, None, None, None)
     assert st == 1
+
+
+# Two KV blocks per warp iteration over FP8 caches (rings of 4 / 6 stages
+# for one column group, 8 / 12 for three).
+@pytest.mark.parametrize("D,Q,Hq,Hkv,stages", [(128, 1, 8, 8, 0), (128, 1, 32, 8, 6),
+                                               (128, 5, 32, 8, 0), (256, 1, 8, 8, 4),
+                                               (128, 3, 16, 4, 0)])
+@pytest.mark.parametrize("split_blocks", [0, 3])
+def test_fp8_two_blocks_per_iteration(D, Q, Hq, Hkv, stages, split_blocks):
+    lens = [Q, 15, 16, 17, 47, 129, 701]
+    wl = W.Workload(f"fp8 kb2 D{D} Q{Q} {Hq}/{Hkv}", len(lens), Hq, Hkv, D, "bf16",
+                    context_lens=lens, num_queries=Q, seed=1500 + D + Q + Hq + split_blocks)
+    with tuning(blocks_per_iter=2):
+        run_fp8(wl, kernel=2, stages=stages, split_blocks=split_blocks)

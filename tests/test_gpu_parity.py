@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from paged_kv_cache_18_gb300 import workloads as W
-from tests.gpu_util import (DeviceBatch, assert_close, cache_bits, errors, host_f64,
+from tests.gpu_util import (DeviceBatch, assert_close, cache_bits, errors, host_f64, tuning,
                             oracle_after_append)
 
 pytestmark = pytest.mark.gpu
@@ -18,16 +18,12 @@ pytestmark = pytest.mark.gpu
 EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 100]
 
 
-def run_case(wl, kernel=0, split_blocks=0, stages=0, warp_tiles=0):
+def run_case(wl, kernel=0, split_blocks=0, stages=0, warp_tiles=0, blocks_per_iter=0):
     b = W.make_batch(wl)
     d = DeviceBatch(b)
     d.append()
-    import paged_kv_cache_18_gb300 as pkv
-    pkv.binding.TUNING["warp_tiles"] = warp_tiles
-    try:
+    with tuning(warp_tiles=warp_tiles, blocks_per_iter=blocks_per_iter):
         out = d.attend(kernel=kernel, split_blocks=split_blocks, stages=stages)
-    finally:
-        pkv.binding.TUNING.pop("warp_tiles", None)
     torch.cuda.synchronize()
     ref = oracle_after_append(b)
     # the append is bit-exact over the whole cache
@@ -411,9 +407,85 @@ def test_mma_multi_tile_warps(dtype, D, warp_tiles, Q, Hq, Hkv, split_blocks):
 
 def test_mma_multi_tile_rejects_oversize():
     import paged_kv_cache_18_gb300 as pkv
-    pkv.binding.TUNING["warp_tiles"] = 2
-    try:
-        with pytest.raises(pkv.PkvError):  # two 8-column tiles of a 256-dim head per warp
-            pkv.plan(2, 3, 16, 4, 256, 100, torch.bfloat16, kernel=2)
-    finally:
-        pkv.binding.TUNING.pop("warp_tiles", None)
+    with tuning(warp_tiles=2), pytest.raises(pkv.PkvError):
+        # two 8-column tiles of a 256-dim head per warp
+        pkv.plan(2, 3, 16, 4, 256, 100, torch.bfloat16, kernel=2)
+
+
+# Two KV blocks per warp iteration (their chains interleave): every ring of
+# four or more stages, odd block counts (a last iteration with one block),
+# splits, the fused append and tree masks.
+TWO_BLOCK_CASES = [  # D, Q, Hq, Hkv, stages
+    (128, 5, 32, 8, 0), (128, 5, 32, 8, 6), (128, 3, 16, 4, 4), (64, 4, 64, 8, 0),
+    (64, 3, 40, 5, 0), (128, 7, 24, 8, 0)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D,Q,Hq,Hkv,stages", TWO_BLOCK_CASES)
+@pytest.mark.parametrize("split_blocks", [0, 3, 5])
+def test_mma_two_blocks_per_iteration(dtype, D, Q, Hq, Hkv, stages, split_blocks):
+    lens = [Q, 15, 16, 17, 33, 48, 250, 701]
+    wl = W.Workload(f"{dtype} kb2 D{D} Q{Q} {Hq}/{Hkv} st{stages} sb{split_blocks}", len(lens),
+                    Hq, Hkv, D, dtype, context_lens=lens, num_queries=Q,
+                    seed=1400 + D + Q + Hq + stages + split_blocks)
+    run_case(wl, kernel=2, split_blocks=split_blocks, stages=stages, blocks_per_iter=2)
+
+
+@pytest.mark.parametrize("D,Q,Hq,Hkv", [(128, 1, 8, 8), (128, 2, 8, 2), (256, 1, 8, 2),
+                                        (128, 1, 16, 1)])
+def test_two_blocks_need_four_stages(D, Q, Hq, Hkv):
+    import paged_kv_cache_18_gb300 as pkv
+    # one-tile rings of 2 / 3 stages (and 1 / 2 at head_dim 256) cannot
+    # keep a pair in flight: refused, not run
+    with tuning(blocks_per_iter=2), pytest.raises(pkv.PkvError):
+        pkv.plan(2, Q, Hq, Hkv, D, 100, torch.bfloat16, kernel=2)
+
+
+@pytest.mark.parametrize("split_blocks", [0, 3])
+def test_two_blocks_fused_append(split_blocks):
+    import paged_kv_cache_18_gb300 as pkv
+    Q, Hq, Hkv, D = 5, 32, 8, 128
+    lens = [Q - 1, Q, Q + 1, 16, 17, 31, 33, 100, 250]
+    wl = W.Workload(f"kb2 fused sb{split_blocks}", len(lens), Hq, Hkv, D, "bf16",
+                    context_lens=lens, num_queries=Q, seed=1450 + split_blocks)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    kn = d.k_new.view(wl.batch, Q, Hkv, D)
+    vn = d.v_new.view(wl.batch, Q, Hkv, D)
+    with tuning(blocks_per_iter=2):
+        out = pkv.append_attention(d.q, kn, vn, d.k_cache, d.v_cache, d.table, d.lens,
+                                   scale=wl.softmax_scale, max_context_len=b.max_context_len,
+                                   kernel=2, split_blocks=split_blocks, error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    ref = oracle_after_append(b)
+    for cache, host in ((d.k_cache, b.k_cache), (d.v_cache, b.v_cache)):
+        bits = cache_bits(cache)
+        np.testing.assert_array_equal(bits, host.view(bits.dtype))
+    assert_close(host_f64(out, "bf16"), ref, "bf16", wl.name)
+
+
+@pytest.mark.parametrize("Q,Hq,Hkv", [(5, 32, 8), (16, 8, 1), (9, 16, 8)])
+def test_two_blocks_tree_verify(Q, Hq, Hkv):
+    import oracle
+    import paged_kv_cache_18_gb300 as pkv
+    rng = np.random.default_rng(Q + 31)
+    lens = [Q, Q + 3, Q + 40, Q + 301]
+    wl = W.Workload(f"kb2 tree Q{Q}", len(lens), Hq, Hkv, 128, "bf16", context_lens=lens,
+                    num_queries=Q, seed=1460 + Q)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    masks = _tree_masks(Q, wl.batch, rng)
+    tm = torch.from_numpy(np.ascontiguousarray(masks).view(np.int64)).cuda()
+    with tuning(blocks_per_iter=2):
+        out = pkv.tree_verify_attention(d.q, d.k_cache, d.v_cache, d.table, d.lens, tm,
+                                        scale=wl.softmax_scale,
+                                        max_context_len=b.max_context_len, kernel=2,
+                                        error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    oracle.kv_append(b.k_cache, b.v_cache, b.k_new, b.v_new, b.slot_mapping, "bf16")
+    ref = oracle.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                wl.softmax_scale, "bf16", masks)
+    assert_close(host_f64(out, "bf16"), ref, "bf16", wl.name)
