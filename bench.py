@@ -278,7 +278,8 @@ def run_ours(args):
     barrier()
     import paged_kv_cache_18_gb300 as pkv
     pkv.binding.TUNING.update(rows_per_cta=args.rows_per_cta, merge=args.merge,
-                              warp_tiles=args.warp_tiles, blocks_per_iter=args.blocks_per_iter)
+                              warp_tiles=args.warp_tiles, blocks_per_iter=args.blocks_per_iter,
+                              persistent=args.persistent)
 
     wl = W.WORKLOADS[args.workload]
     if rank > 0:
@@ -490,6 +491,8 @@ def main(argv=None):
                     help="tensor-core kernel: 8-column query tiles per warp (0 planner)")
     ap.add_argument("--blocks-per-iter", type=int, default=0,
                     help="tensor-core kernel: KV blocks per warp loop iteration (0 planner)")
+    ap.add_argument("--persistent", type=int, default=0,
+                    help="tcgen05 kernel: 1 CTAs walk work items, 2 one CTA per item (0 planner)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",

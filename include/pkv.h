@@ -101,7 +101,9 @@ enum {
 typedef enum pkv_kernel {
   PKV_KERNEL_AUTO = 0,
   PKV_KERNEL_SIMT = 1, /* CUDA-core dot products (any dtype; fp32 path) */
-  PKV_KERNEL_MMA = 2   /* tensor-core tiles (bf16 / fp16 q; 16-bit or FP8 cache) */
+  PKV_KERNEL_MMA = 2,  /* tensor-core tiles (bf16 / fp16 q; 16-bit or FP8 cache) */
+  PKV_KERNEL_TC = 3    /* tcgen05 tiles with TMEM accumulators: bf16 / fp16 caches,
+                          head_dim 128, up to 32 query rows per CTA, no fused append */
 } pkv_kernel;
 
 /* Optional launch controls (pass NULL for the planner's choice). */
@@ -117,6 +119,8 @@ typedef struct pkv_options {
                        per warp (1..3 at head_dim <= 128, 1..4 at 64, 1 at 256) */
   int blocks_per_iter; /* 0: planner; tensor-core kernel: KV blocks one warp
                           takes per loop iteration (1 or 2; 2 with one tile) */
+  int persistent;   /* tcgen05 kernel: 0 planner, 1 one CTA per resident slot
+                       walks the work items, 2 one CTA per item */
 } pkv_options;
 
 /* What one attention call launches (see pkv_attention_plan). */

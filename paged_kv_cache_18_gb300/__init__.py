@@ -5,7 +5,7 @@ ABI in ``include/pkv.h``); this package is its thin Python binding plus the
 seeded workload generator and byte accounting used by the tests and the
 benchmark.  Build the library with ``paged_kv_cache_18_gb300.build.build()``.
 """
-from .binding import (PKV_KERNEL_AUTO, PKV_KERNEL_MMA, PKV_KERNEL_SIMT, PkvError,  # noqa: F401
+from .binding import (PKV_KERNEL_AUTO, PKV_KERNEL_MMA, PKV_KERNEL_SIMT, PKV_KERNEL_TC, PkvError,  # noqa: F401
                       append_attention, kv_append, kv_append_fp8,
                       paged_attention_fp8, paged_decode_attention, plan, plan_for, read_error_word,
                       spec_verify_attention, tree_verify_attention, version,

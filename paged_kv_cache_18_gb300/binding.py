@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libpkv.so")
 _lock = threading.Lock()
 _lib = None
 
-PKV_KERNEL_AUTO, PKV_KERNEL_SIMT, PKV_KERNEL_MMA = 0, 1, 2
+PKV_KERNEL_AUTO, PKV_KERNEL_SIMT, PKV_KERNEL_MMA, PKV_KERNEL_TC = 0, 1, 2, 3
 DEVERR_NAMES = {0: "none", 1: "slot out of range", 2: "block id out of range",
                 3: "context length over max_context_len or the table",
                 4: "shared-memory copy timed out"}
@@ -47,7 +47,7 @@ class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("split_blocks", ctypes.c_int),
                 ("stages", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
                 ("merge", ctypes.c_int), ("warp_tiles", ctypes.c_int),
-                ("blocks_per_iter", ctypes.c_int)]
+                ("blocks_per_iter", ctypes.c_int), ("persistent", ctypes.c_int)]
 
 
 # Extra launch controls for tuning runs (pkv_options.rows_per_cta / .merge /
@@ -140,10 +140,10 @@ def _stream(t: torch.Tensor) -> int:
 def _opts(kernel: int, split_blocks: int, stages: int = 0, warp_tiles: int = 0):
     rows, merge = TUNING.get("rows_per_cta", 0), TUNING.get("merge", 0)
     warp_tiles = warp_tiles or TUNING.get("warp_tiles", 0)
-    kb = TUNING.get("blocks_per_iter", 0)
-    if not any((kernel, split_blocks, stages, rows, merge, warp_tiles, kb)):
+    kb, pers = TUNING.get("blocks_per_iter", 0), TUNING.get("persistent", 0)
+    if not any((kernel, split_blocks, stages, rows, merge, warp_tiles, kb, pers)):
         return None
-    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge, warp_tiles, kb))
+    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge, warp_tiles, kb, pers))
 
 
 def _need(cond: bool, msg: str) -> None:

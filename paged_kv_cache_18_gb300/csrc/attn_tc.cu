@@ -1,0 +1,859 @@
+// attn_tc.cu -- paged decode / verification attention on the fifth-generation
+// tensor cores (tcgen05), accumulators in tensor memory (TMEM).
+//
+// Same arithmetic as attn_mma.cuh ("Inference part 1", sections "PagedAttention",
+// "FlashAttention" and "FlashDecoding"), organised for tcgen05: one thread
+// issues asynchronous 128-row MMAs over eight cache blocks at a time, and the
+// softmax runs on values read from TMEM.  It serves tiles of 9 to 32 query rows
+// (NC = 16 or 32 columns): the verification tile of K+1 drafts x the query
+// heads of one KV head, where the mma.sync kernel spends its time repeating a
+// per-block chain once per 8-column tile.
+//
+// One CTA per (split, KV head x row chunk, sequence), 320 threads:
+//   warps 0-7  softmax and epilogue; warp w reads TMEM lanes 32 (w % 4) ..
+//              32 (w % 4) + 31 -- keys of the current 128-key chunk in S^T,
+//              head dims in O^T -- for half w / 4 of the query columns (two
+//              warps per lane quadrant keep each warp's chain short);
+//   warp 8     TMA producer: K and V tiles of each block, through the block
+//              table, into a ring of NS chunk stages;
+//   warp 9     MMA issuer (one lane) and TMEM owner.
+// Per chunk c of 128 keys (8 blocks):
+//   S^T[128 keys x NC] = K_c[128 x D] . Q^T[D x NC]          (TMEM, 2 buffers)
+//   softmax over keys per column, lazy per-column reference max m (raised,
+//   with l and O rescaled, only when a score exceeds it by more than 2^8:
+//   a CTA-wide vote per chunk, a cross-thread max only then)
+//   P^T (bf16/f16 high part + remainder) -> shared memory
+//   O^T[D x 2 NC] += V_c^T[D x 128] . [P_hi^T P_lo^T][128 x 2 NC]  (TMEM;
+//   the two halves are summed at the end)
+// Operands: K and Q^T K-major with the 128-byte swizzle (as the TMA writes
+// K), V^T MN-major with the 128-byte swizzle (V's own layout), P^T MN-major
+// without swizzle.  Keys that no column may see (past the context, past the
+// split, bad blocks) get -inf scores and their V rows are zeroed in shared
+// memory, so NaN-filled rows never enter an MMA (0 x NaN would be NaN).
+#include <type_traits>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace tc {
+
+constexpr int kChunkBlocks = 8;                    // blocks per 128-key chunk
+constexpr int kChunkKeys = kChunkBlocks * kBlockSize;
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kKProducerWarp = kSoftmaxWarps;
+constexpr int kIssuerWarp = kSoftmaxWarps + 1;
+constexpr int kVProducerWarp = kSoftmaxWarps + 2;
+constexpr int kThreads = kSoftmaxThreads + 96;
+constexpr float kRescaleSlack = 8.f;
+
+// ---- tcgen05 / TMEM wrappers -----------------------------------------------
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  uint64_t d = static_cast<uint64_t>((addr >> 4) & 0x3fffu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
+  d |= 1ull << 46;  // descriptor version
+  d |= static_cast<uint64_t>(layout) << 61;
+  return d;
+}
+constexpr uint32_t kSwizzle128 = 2, kSwizzleNone = 0;
+
+// kind::f16 instruction descriptor: f32 accumulate, A and B of one 16-bit
+// type, A / B K-major (0) or MN-major (1), M x N.
+template <typename T>
+__device__ __forceinline__ uint32_t instr_desc(int M, int N, int a_mn, int b_mn) {
+  const uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc ? 1u : 0u));
+}
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Non-blocking test of a barrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+      : "memory");
+}
+template <int N> __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 8) tmem_ld8(taddr, v); else tmem_ld16(taddr, v);
+}
+template <int N> __device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[N]) {
+  if constexpr (N == 8) tmem_st8(taddr, v); else tmem_st16(taddr, v);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// CTA-wide OR over the 256 softmax threads (named barrier 1).
+__device__ __forceinline__ bool softmax_any(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, 256, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return out != 0;
+}
+// CTA-wide AND over the 256 softmax threads (named barrier 1): every wait's
+// outcome is decided once for the eight warps, so none of them leaves the
+// loop while the others wait at a named barrier.
+__device__ __forceinline__ bool softmax_all(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, 256, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return out != 0;
+}
+__device__ __forceinline__ void softmax_sync() {
+  asm volatile("bar.sync 2, 256;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// ---- geometry ----------------------------------------------------------------
+// Two rings of NS stages, one for K and one for V: a stage is one chunk's K
+// (or V) tile, two 64-dim panels of 128 rows x 128 B (block j of the chunk
+// at rows 16 j .. 16 j + 15).  K is free again as soon as S^T is computed,
+// V only after P.V, so the K ring runs ahead.
+template <int D, int NC, int NS, int PB> struct TcGeom {
+  static_assert(D == 128, "head_dim 128");
+  static constexpr int kPanelBytes = kChunkKeys * 128;      // 16 KB
+  static constexpr int kTileBytes = 2 * kPanelBytes;        // 32 KB: one stage
+  static constexpr int kVOff = NS * kTileBytes;             // the V ring
+  static constexpr int kQtPanelBytes = NC * 128;            // Q^T: NC rows per panel
+  static constexpr int kQtOff = 2 * NS * kTileBytes;        // two Q^T buffers of 2 panels
+  static constexpr int kPOff = kQtOff + 4 * kQtPanelBytes;  // P^T buffers: (high, low) x PB
+  static constexpr int kPBytes = kChunkKeys * NC * 2;
+  static constexpr int kBytes = kPOff + PB * 2 * kPBytes;
+  // S^T (two buffers of NC) and two O^T buffers (items alternate) of 2 NC
+  // (NC columns for the high part of P, NC for the remainder, summed at
+  // the end)
+  static constexpr int kTmemCols = 6 * NC <= 128 ? 128 : 256;
+};
+
+// Per-stage facts the producer hands to the consumers (published before its
+// mbarrier arrive, which orders them).
+struct StageInfo {
+  int nb;             // blocks present (1..8)
+  uint32_t bad_mask;  // bit j: block j's table entry was out of range
+};
+
+// --------------------------------------------------------------------------------
+//
+// NS chunk stages; PB = 1 or 2 P^T buffers (with one, chunk c's softmax
+// writes P^T only after chunk c - 1's P.V has read it).
+// A work item: one split of one (sequence, KV head, row chunk).  Items are
+// numbered split-fastest; the persistent CTA g takes items g, g + G, ...,
+// every role enumerating the same sequence.
+struct Item {
+  int b, kvh, chunk_row, split, L, blk_begin, nspan, n_chunks, ns_b;
+  bool valid;
+};
+__device__ __forceinline__ Item decode_item(const AttnParams &p, int i, bool report) {
+  Item it;
+  const int ns = p.num_splits, Y = p.num_kv_heads * p.row_chunks;
+  it.split = i % ns;
+  const int t = i / ns;
+  const int y = t % Y;
+  it.b = t / Y;
+  it.kvh = y / p.row_chunks;
+  it.chunk_row = y - it.kvh * p.row_chunks;
+  const SeqExtent ext = seq_extent(p, it.b, report && it.split == 0 && y == 0);
+  it.L = ext.L;
+  it.blk_begin = it.split * p.split_blocks;
+  it.valid = !(it.split > 0 && it.blk_begin >= ext.nblk);
+  const int blk_end = min(it.blk_begin + p.split_blocks, ext.nblk);
+  it.nspan = max(blk_end - it.blk_begin, 0);
+  it.n_chunks = (it.nspan + kChunkBlocks - 1) / kChunkBlocks;
+  it.ns_b = max(1, min(ns, (ext.nblk + p.split_blocks - 1) / p.split_blocks));
+  return it;
+}
+
+template <typename T, int D, int NC, int NS, int PB>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const AttnParams p, int num_items) {
+  using G = TcGeom<D, NC, NS, PB>;
+  constexpr int NCW = NC / 2;  // query columns of one softmax warp
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+
+  // One barrier per buffer wherever a producer may run two phases ahead of
+  // a waiter otherwise (P^T is double-buffered: the softmax can write chunk
+  // g + 1's P^T before the issuer has waited for chunk g's).
+  __shared__ uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], s_free[2],
+      p_full[PB], pv_done[PB], qt_full[2], qt_empty[2], o_free[2], mma_idle;
+  // Chunk facts from the K producer, a ring of NS + 2: the slot of chunk g
+  // is rewritten (for chunk g + NS + 2) only after a K stage reuse that
+  // waits on the softmax having released S^T of chunk g, read after them.
+  __shared__ StageInfo stage_info[NS + 2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ __align__(16) float red[4][NC];
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G0 = blockIdx.x, GS = gridDim.x;
+
+  // Softmax warp w: TMEM lane quadrant quad = w % 4 (keys / head dims
+  // 32 quad .. 32 quad + 31) and column half half = w / 4 (columns
+  // NCW half .. NCW half + NCW - 1).
+  const int quad = warp & 3, half = (warp >> 2) & 1;
+  const int kl = quad * 32 + lane;
+  const int col0 = half * NCW;
+
+  if (tid == 0) {
+    s_abort = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&s_free[i]), kSoftmaxWarps);
+      mbar_init(smem_u32(&qt_full[i]), 1);
+      mbar_init(smem_u32(&qt_empty[i]), 1);
+      mbar_init(smem_u32(&o_free[i]), kSoftmaxWarps);
+    }
+    for (int i = 0; i < PB; ++i) {
+      mbar_init(smem_u32(&p_full[i]), kSoftmaxWarps);
+      mbar_init(smem_u32(&pv_done[i]), 1);
+    }
+    mbar_init(smem_u32(&mma_idle), 1);
+    fence_mbar_init();
+  }
+  if (warp == kIssuerWarp) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            smem_u32(&tmem_base_s)),
+        "r"(G::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t tmem_s[2] = {tmem, tmem + NC};
+  const uint32_t tmem_o[2] = {tmem + 2 * NC, tmem + 4 * NC};
+
+  auto abort_all = [&]() {
+    s_abort = 1;
+    record_error(p.err, PKV_DEVERR_TIMEOUT);
+  };
+  // Items with keys (items of an empty sequence are written directly by the
+  // softmax warps and take no part in the pipeline).
+  auto active = [](const Item &it) { return it.valid && it.n_chunks > 0; };
+
+  if (warp == kKProducerWarp || warp == kVProducerWarp) {
+    // ---- TMA producers: one warp for K (and each item's Q^T), one for V -------
+    const bool is_k = warp == kKProducerWarp;
+    uint64_t *full = is_k ? k_full : v_full;
+    uint64_t *empty = is_k ? k_empty : v_empty;
+    const CUtensorMap *map = is_k ? &kmap : &vmap;
+    const uint32_t ring = sbase + (is_k ? 0 : G::kVOff);
+    int g = 0, na = 0, issued = 0;
+    bool ok = true;
+    for (int i = G0; i < num_items && ok; i += GS) {
+      const Item it = decode_item(p, i, false);
+      if (!active(it)) continue;
+      const int qb = na & 1;
+      if (is_k) {
+        // Q^T of the item: query columns as rows of the K-major swizzled
+        // operand (padding columns zero), once the Q^T buffer is free.
+        bool w = na < 2 || mbar_wait_bounded(smem_u32(&qt_empty[qb]), ((na >> 1) - 1) & 1);
+        if (!__all_sync(kFull, w && !s_abort)) {
+          ok = false;
+          break;
+        }
+        // (all of the lane's loads in flight first, then the stores)
+        const uint32_t qt = sbase + G::kQtOff + qb * 2 * G::kQtPanelBytes;
+        constexpr int kPer = NC * (D / 8) / 32;  // 16-byte pieces per lane
+        uint4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int e = lane + 32 * k, col = e / (D / 8), q = e - col * (D / 8);
+          const int64_t row = cta_row_index(p, it.b, it.kvh, it.chunk_row, col);
+          v[k] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(
+                                reinterpret_cast<const T *>(p.q) + row * D + q * 8))
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int e = lane + 32 * k, col = e / (D / 8), q = e - col * (D / 8);
+          st_shared_v4(qt + (q >> 3) * G::kQtPanelBytes + col * 128 + (((q & 7) ^ (col & 7)) << 4),
+                       v[k].x, v[k].y, v[k].z, v[k].w);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&qt_full[qb]));
+      }
+      const int32_t *table = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks_per_seq;
+      for (int c = 0; c < it.n_chunks; ++c, ++g) {
+        const int s = g % NS;
+        bool w = !s_abort;
+        if (w && g >= NS) w = mbar_wait_bounded(smem_u32(&empty[s]), ((g / NS) - 1) & 1);
+        if (!__all_sync(kFull, w)) {
+          ok = false;
+          break;
+        }
+        const int nb = min(kChunkBlocks, it.nspan - c * kChunkBlocks);
+        const int entry = lane < nb ? __ldg(table + it.blk_begin + c * kChunkBlocks + lane) : 0;
+        const bool bad = lane < nb && (entry < 0 || static_cast<int64_t>(entry) >= p.num_blocks);
+        const uint32_t bad_mask = __ballot_sync(kFull, bad);
+        const uint32_t bar = smem_u32(&full[s]);
+        if (lane == 0) {
+          if (is_k) {
+            if (bad_mask) record_error(p.err, PKV_DEVERR_BLOCK_ID);
+            stage_info[g % (NS + 2)].nb = nb;
+            stage_info[g % (NS + 2)].bad_mask = bad_mask;
+          }
+          mbar_arrive_expect_tx(bar, nb * 2 * 2048);
+        }
+        __syncwarp();
+        if (lane < nb) {
+          const int phys = bad ? 0 : entry;
+          const uint32_t st = ring + s * G::kTileBytes + lane * 2048;
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+            tma_load_4d(st + part * G::kPanelBytes, map, bar, part * 64, 0, it.kvh, phys);
+        }
+        issued = g + 1;
+      }
+      ++na;
+    }
+    if (!ok && lane == 0) abort_all();
+    // Copies issued but perhaps never consumed (an aborted CTA): give them a
+    // bounded chance to land before the CTA exits.
+    if (lane == 0 && s_abort)
+      for (int c = max(0, issued - NS); c < issued; ++c)
+        mbar_wait_bounded(smem_u32(&full[c % NS]), (c / NS) & 1);
+  } else if (warp == kIssuerWarp) {
+    // ---- MMA issuer --------------------------------------------------------------
+    if (lane == 0) {
+      const uint32_t id_s = instr_desc<T>(128, NC, 0, 0);
+      // P.V with the high part and the remainder of P^T side by side as one
+      // operand of 2 NC columns: half the MMAs of two N = NC products
+      const uint32_t id_pv = instr_desc<T>(128, 2 * NC, 1, 1);
+      // Descriptors differ only in their start address (bits 0..13, address
+      // >> 4): build each kind once and add the address per MMA.
+      const uint64_t dk = smem_desc(0, 16, 1024, kSwizzle128);
+      const uint64_t dv = smem_desc(0, G::kPanelBytes, 1024, kSwizzle128);
+      const uint64_t dp = smem_desc(0, 128, kChunkKeys * 16, kSwizzleNone);
+      // Cursors over the flat chunk sequence: S^T runs up to one chunk ahead
+      // of P.V (two S^T buffers), across item boundaries.
+      int i_s = G0, c_s = 0, na_s = 0, g_s = 0;   // next S^T: item, chunk, active index, flat
+      int i_v = G0, c_v = 0, na_v = 0, g_v = 0;   // next P.V
+      Item it_s{}, it_v{};
+      auto next_active = [&](int &i, Item &it) {
+        for (; i < num_items; i += GS) {
+          it = decode_item(p, i, false);
+          if (active(it)) return true;
+        }
+        return false;
+      };
+      bool more_s = next_active(i_s, it_s), more_v = next_active(i_v, it_v);
+      auto s_ready = [&](bool block) -> bool {
+        const int s = g_s % NS, sb = g_s & 1, qb = na_s & 1;
+        const uint32_t kf = smem_u32(&k_full[s]), sf = smem_u32(&s_free[sb]);
+        const uint32_t qf = smem_u32(&qt_full[qb]);
+        const uint32_t pk = (g_s / NS) & 1, ps = ((g_s >> 1) - 1) & 1, pq = (na_s >> 1) & 1;
+        if (block)
+          return (c_s > 0 || mbar_wait_bounded(qf, pq)) && mbar_wait_bounded(kf, pk) &&
+                 (g_s < 2 || mbar_wait_bounded(sf, ps));
+        return (c_s > 0 || mbar_test(qf, pq)) && mbar_test(kf, pk) &&
+               (g_s < 2 || mbar_test(sf, ps));
+      };
+      auto issue_s = [&]() {
+        const int s = g_s % NS, sb = g_s & 1, qb = na_s & 1;
+        fence_after();
+        const uint64_t ka = dk | ((sbase + s * G::kTileBytes) >> 4);
+        const uint64_t qa = dk | ((sbase + G::kQtOff + qb * 2 * G::kQtPanelBytes) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * G::kPanelBytes + (ks & 3) * 32) >> 4;
+          const uint32_t offq = ((ks >> 2) * G::kQtPanelBytes + (ks & 3) * 32) >> 4;
+          mma(tmem_s[sb], ka + off, qa + offq, id_s, ks > 0);
+        }
+        commit(smem_u32(&s_full[sb]));
+        commit(smem_u32(&k_empty[s]));
+        ++g_s;
+        if (++c_s == it_s.n_chunks) {  // the item's last S^T: its Q^T buffer is free
+          commit(smem_u32(&qt_empty[qb]));
+          c_s = 0;
+          ++na_s;
+          i_s += GS;
+          more_s = next_active(i_s, it_s);
+        }
+      };
+      bool ok = true;
+      if (more_s) {
+        ok = s_ready(true);
+        if (ok) issue_s();
+      }
+      while (ok && more_v) {
+        if (more_s && g_s == g_v + 1 && s_ready(false)) issue_s();
+        const int ob = na_v & 1;
+        if (!mbar_wait_bounded(smem_u32(&p_full[g_v % PB]), (g_v / PB) & 1) ||
+            !mbar_wait_bounded(smem_u32(&v_full[g_v % NS]), (g_v / NS) & 1) ||
+            (c_v == 0 && na_v >= 2 &&
+             !mbar_wait_bounded(smem_u32(&o_free[ob]), ((na_v >> 1) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint64_t va = dv | ((sbase + G::kVOff + (g_v % NS) * G::kTileBytes) >> 4);
+        const uint64_t pa = dp | ((sbase + G::kPOff + (g_v % PB) * 2 * G::kPBytes) >> 4);
+#pragma unroll
+        for (int j = 0; j < kChunkKeys / 16; ++j)
+          mma(tmem_o[ob], va + ((j * 2048) >> 4), pa + ((j * 256) >> 4), id_pv, c_v > 0 || j > 0);
+        commit(smem_u32(&v_empty[g_v % NS]));
+        commit(smem_u32(&pv_done[g_v % PB]));
+        ++g_v;
+        if (++c_v == it_v.n_chunks) {
+          c_v = 0;
+          ++na_v;
+          i_v += GS;
+          more_v = next_active(i_v, it_v);
+        }
+        if (more_s && g_s == g_v) {
+          if (!s_ready(true)) {
+            ok = false;
+            break;
+          }
+          issue_s();
+        }
+      }
+      if (!ok) abort_all();
+      // every MMA this thread issued has completed before TMEM is released
+      commit(smem_u32(&mma_idle));
+      mbar_wait_bounded(smem_u32(&mma_idle), 0);
+    }
+  } else {
+    // ---- softmax warps -------------------------------------------------------------
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const float colfac = p.scale_log2;
+    // per item: the columns' references m (the same in every thread of the
+    // column half) and this thread's partial column sums l
+    float m[NCW], l[NCW];
+    int g = 0, na = 0;
+    bool ok = true;
+    for (int i = G0; i < num_items && ok; i += GS) {
+      const Item it = decode_item(p, i, tid == 0);
+      if (!it.valid) continue;
+      if (it.n_chunks == 0) {
+        // an empty sequence: zero output rows (one split)
+        for (int j = 0; j < NCW; ++j) {
+          const int64_t row = cta_row_index(p, it.b, it.kvh, it.chunk_row, col0 + j);
+          if (row < 0) continue;
+          if (p.num_splits == 1) {
+            reinterpret_cast<T *>(p.out)[row * D + kl] = from_float<T>(0.f);
+          } else {
+            p.part_o[(row * p.num_splits + it.split) * D + kl] = 0.f;
+            if (quad == 0 && lane == 0) p.part_lse[row * p.num_splits + it.split] = -INFINITY;
+          }
+        }
+        continue;
+      }
+      const int ob = na & 1;
+      const int mask_from = it.L - p.num_queries;
+#pragma unroll
+      for (int j = 0; j < NCW; ++j) {
+        m[j] = -INFINITY;
+        l[j] = 0.f;
+      }
+      for (int c = 0; c < it.n_chunks; ++c, ++g) {
+        const int s = g % NS, sb = g & 1;
+        if (!softmax_all(mbar_wait_bounded(smem_u32(&s_full[sb]), (g >> 1) & 1) && !s_abort)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        // Which keys are real: the producer's block count and bad blocks (read
+        // before S^T is released, see stage_info).
+        const StageInfo info = stage_info[g % (NS + 2)];
+        float sc[NCW];
+        tmem_ld<NCW>(tmem_s[sb] + lane_base + col0, sc);
+        tmem_wait_ld();
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
+
+        const int key0 = (it.blk_begin + c * kChunkBlocks) * kBlockSize;
+        const int key = key0 + kl;
+        const bool bad = kl >= info.nb * kBlockSize || ((info.bad_mask >> (kl >> 4)) & 1u);
+        const bool need_mask = info.nb < kChunkBlocks || info.bad_mask != 0 ||
+                               key0 + kChunkKeys > mask_from;
+        bool above = false;
+#pragma unroll
+        for (int j = 0; j < NCW; ++j) sc[j] *= colfac;
+        if (need_mask) {
+          // (a uniform branch) column col is query row r = chunk_row *
+          // rows_per_cta + col: query r / G, visible rows < L - Q + 1 + r / G;
+          // walked without divisions
+          const int r0 = it.chunk_row * p.rows_per_cta + col0;
+          int jq = r0 / p.group, hh = r0 - jq * p.group;
+#pragma unroll
+          for (int j = 0; j < NCW; ++j) {
+            const bool real = col0 + j < p.rows_per_cta && r0 + j < p.rows;
+            const int lim = it.L - p.num_queries + 1 + (real ? jq : 0);
+            const unsigned long long tm =
+                (p.tree_mask != nullptr && real)
+                    ? __ldg(p.tree_mask + static_cast<int64_t>(it.b) * p.mask_stride + jq)
+                    : 0ull;
+            if (!key_visible(p, key, it.L, bad, lim, tm)) sc[j] = -INFINITY;
+            if (++hh == p.group) {
+              hh = 0;
+              ++jq;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NCW; ++j) above |= sc[j] > m[j] + kRescaleSlack;
+        if (softmax_any(above)) {
+          // Raise the references to the columns' running maxima: a max over
+          // the 128 keys (shuffles, then the four quadrant warps of this
+          // column half in shared memory).
+          float corr[NCW];
+#pragma unroll
+          for (int j = 0; j < NCW; ++j) {
+            float mx = sc[j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+            if (lane == 0) red[quad][col0 + j] = mx;
+          }
+          softmax_sync();
+#pragma unroll
+          for (int j = 0; j < NCW; ++j) {
+            const int col = col0 + j;
+            const float mx = fmaxf(fmaxf(red[0][col], red[1][col]), fmaxf(red[2][col], red[3][col]));
+            const float m_new = fmaxf(m[j], mx);
+            corr[j] = ex2(m[j] - (m_new == -INFINITY ? 0.f : m_new));
+            m[j] = m_new;
+            l[j] *= corr[j];
+          }
+          softmax_sync();  // red[] is reused by the next vote
+          if (c > 0) {
+            // O^T (head dims kl, this thread's columns) times corr, once chunk
+            // g - 1's P.V, the last writer of O^T, has landed.
+            if (!softmax_all(mbar_wait_bounded(smem_u32(&pv_done[(g - 1) % PB]),
+                                               ((g - 1) / PB) & 1))) {
+              ok = false;
+              break;
+            }
+            fence_after();
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {  // O^T of the high part and of the remainder
+              float v[NCW];
+              tmem_ld<NCW>(tmem_o[ob] + lane_base + part * NC + col0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k2 = 0; k2 < NCW; ++k2) v[k2] *= corr[k2];
+              tmem_st<NCW>(tmem_o[ob] + lane_base + part * NC + col0, v);
+            }
+            tmem_wait_st();
+          }
+        }
+        // Weights and their 16-bit high part / remainder, column pairs packed.
+        uint32_t hi[NCW / 2], lo[NCW / 2];
+#pragma unroll
+        for (int j = 0; j < NCW; j += 2) {
+          const float m0 = m[j] == -INFINITY ? 0.f : m[j];
+          const float m1 = m[j + 1] == -INFINITY ? 0.f : m[j + 1];
+          const float p0 = ex2(sc[j] - m0), p1 = ex2(sc[j + 1] - m1);
+          l[j] += p0;
+          l[j + 1] += p1;
+          const uint32_t h01 = Mma<T>::pack(p0, p1);
+          float r0, r1;
+          Mma<T>::unpack(h01, r0, r1);
+          hi[j / 2] = h01;
+          lo[j / 2] = Mma<T>::pack(p0 - r0, p1 - r1);
+        }
+        // P^T buffer g % PB was last read by chunk g - PB's P.V.
+        if (g >= PB && !softmax_all(mbar_wait_bounded(smem_u32(&pv_done[g % PB]),
+                                                       ((g / PB) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        // Keys no column sees get their V rows zeroed, once V has landed.
+        if (need_mask && !softmax_all(mbar_wait_bounded(smem_u32(&v_full[s]), (g / NS) & 1))) {
+          ok = false;
+          break;
+        }
+        if (half == 0 && need_mask && (bad || key >= it.L)) {
+          const uint32_t vrow = sbase + G::kVOff + s * G::kTileBytes + kl * 128;
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(vrow + part * G::kPanelBytes + q * 16, 0u, 0u, 0u, 0u);
+        }
+        // P^T rows (key kl): core matrices of 8 keys x 8 columns.
+        const uint32_t prow =
+            sbase + G::kPOff + (g % PB) * 2 * G::kPBytes + (kl >> 3) * 128 + (kl & 7) * 16;
+#pragma unroll
+        for (int gg = 0; gg < NCW / 8; ++gg) {
+          const int g8 = (col0 >> 3) + gg;
+          st_shared_v4(prow + g8 * (kChunkKeys * 16), hi[4 * gg], hi[4 * gg + 1],
+                       hi[4 * gg + 2], hi[4 * gg + 3]);
+          st_shared_v4(prow + G::kPBytes + g8 * (kChunkKeys * 16), lo[4 * gg], lo[4 * gg + 1],
+                       lo[4 * gg + 2], lo[4 * gg + 3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_full[g % PB]));
+      }
+      if (!ok) break;
+      // The item's result: O^T once its last P.V has landed, column sums
+      // over the four quadrant warps, then out (or this split's partial).
+      const int gl = g - 1;
+      if (!softmax_all(mbar_wait_bounded(smem_u32(&pv_done[gl % PB]), (gl / PB) & 1))) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      float o_hi[NCW], o_lo[NCW];
+      tmem_ld<NCW>(tmem_o[ob] + lane_base + col0, o_hi);
+      tmem_ld<NCW>(tmem_o[ob] + lane_base + NC + col0, o_lo);
+      tmem_wait_ld();
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&o_free[ob]));
+#pragma unroll
+      for (int j = 0; j < NCW; ++j) {
+        float v = l[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+        if (lane == 0) red[quad][col0 + j] = v;
+      }
+      softmax_sync();
+      // Every shared-memory read first (vectorised), then only stores: the
+      // tensor core and the copies keep shared memory busy, and a read
+      // queued behind each store would cost a round trip per column.
+      float lsum[NCW];
+#pragma unroll
+      for (int j = 0; j < NCW; j += 4) {
+        float4 a = *reinterpret_cast<const float4 *>(&red[0][col0 + j]);
+#pragma unroll
+        for (int q = 1; q < 4; ++q) {
+          const float4 v = *reinterpret_cast<const float4 *>(&red[q][col0 + j]);
+          a.x += v.x;
+          a.y += v.y;
+          a.z += v.z;
+          a.w += v.w;
+        }
+        lsum[j] = a.x;
+        lsum[j + 1] = a.y;
+        lsum[j + 2] = a.z;
+        lsum[j + 3] = a.w;
+      }
+      // Output rows of the columns, walked without divisions: column col is
+      // query row r = chunk_row * rows_per_cta + col, query r / G, head
+      // kvh * G + r % G.
+      const int r0 = it.chunk_row * p.rows_per_cta + col0;
+      int jq = r0 / p.group, hh = r0 - jq * p.group;
+      float lse_mine = -INFINITY;  // column col0 + lane's log-sum-exp (lanes < NCW)
+      int64_t row_mine = -1;
+#pragma unroll
+      for (int j = 0; j < NCW; ++j) {
+        const int col = col0 + j;
+        const bool real = col < p.rows_per_cta && r0 + j < p.rows;
+        const int64_t row =
+            (static_cast<int64_t>(it.b) * p.num_queries + jq) * p.num_heads + it.kvh * p.group + hh;
+        if (++hh == p.group) {
+          hh = 0;
+          ++jq;
+        }
+        if (!real) continue;
+        const float inv = lsum[j] > 0.f ? __fdividef(1.f, lsum[j]) : 0.f;
+        const float o = o_hi[j] + o_lo[j];
+        if (p.num_splits == 1) {
+          reinterpret_cast<T *>(p.out)[row * D + kl] = from_float<T>(o * inv * p.out_scale);
+        } else {
+          __stcg(p.part_o + (row * p.num_splits + it.split) * D + kl, o * inv);
+          if (lane == j) {
+            lse_mine = lsum[j] > 0.f ? m[j] + __log2f(lsum[j]) : -INFINITY;
+            row_mine = row;
+          }
+        }
+      }
+      if (quad == 0 && row_mine >= 0) __stcg(p.part_lse + row_mine * p.num_splits + it.split, lse_mine);
+      softmax_sync();  // red[] is reused by the next item
+      ++na;
+    }
+    if (!ok && tid == 0) abort_all();
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == kIssuerWarp) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(G::kTmemCols));
+  }
+}
+
+}  // namespace tc
+}  // namespace pkv
+namespace pkv {
+namespace tc {
+
+// Rings: 1, 2 or 3 stages of 32 KB each for K and for V (bf16/fp16,
+// head_dim 128), with two P^T buffers (one with three stages, for shared
+// memory).
+template <int NS> constexpr int p_buffers() { return NS >= 3 ? 1 : 2; }
+constexpr int kDefaultStages = 2;
+
+template <typename T, int NC, int NS>
+KernelInfo info_t() {
+  KernelInfo k;
+  k.func = reinterpret_cast<const void *>(&attn_tc_kernel<T, 128, NC, NS, p_buffers<NS>()>);
+  k.threads = kThreads;
+  k.warps = kThreads / 32;
+  k.stages = NS;
+  k.smem = static_cast<size_t>(TcGeom<128, NC, NS, p_buffers<NS>()>::kBytes) + 1024;
+  k.warp_tiles = NC / 8;
+  return k;
+}
+
+template <typename T, int NC, int NS>
+cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
+                     cudaStream_t stream) {
+  const KernelInfo k = info_t<T, NC, NS>();
+  // persistent: grid.x CTAs walk the grid.y x grid.z x splits items
+  const int items = p.num_splits * p.num_kv_heads * p.row_chunks * p.batch;
+  attn_tc_kernel<T, 128, NC, NS, p_buffers<NS>()>
+      <<<dim3(grid.x), k.threads, k.smem, stream>>>(km, vm, p, items);
+  return cudaGetLastError();
+}
+
+using Launch = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const AttnParams &, dim3,
+                               cudaStream_t);
+
+template <typename T, int NC>
+bool pick_ns(int stages, KernelInfo *info, Launch *launch) {
+  switch (stages == 0 ? kDefaultStages : stages) {
+    case 1: *info = info_t<T, NC, 1>(); if (launch) *launch = &launch_t<T, NC, 1>; return true;
+    case 2: *info = info_t<T, NC, 2>(); if (launch) *launch = &launch_t<T, NC, 2>; return true;
+    case 3: *info = info_t<T, NC, 3>(); if (launch) *launch = &launch_t<T, NC, 3>; return true;
+    default: return false;
+  }
+}
+
+template <typename T>
+bool pick_t(int rows, int stages, KernelInfo *info, Launch *launch) {
+  if (rows <= 16) return pick_ns<T, 16>(stages, info, launch);
+  if (rows <= 32) return pick_ns<T, 32>(stages, info, launch);
+  return false;
+}
+
+bool pick(pkv_dtype dtype, int head_dim, int rows, int stages, KernelInfo *info, Launch *launch) {
+  if (head_dim != 128 || rows < 1) return false;
+  if (dtype == PKV_BF16) return pick_t<__nv_bfloat16>(rows, stages, info, launch);
+  if (dtype == PKV_F16) return pick_t<__half>(rows, stages, info, launch);
+  return false;
+}
+
+}  // namespace tc
+
+bool tc_kernel_info(pkv_dtype dtype, int head_dim, int rows_per_cta, int stages,
+                    KernelInfo *info) {
+  return tc::pick(dtype, head_dim, rows_per_cta, stages, info, nullptr);
+}
+
+cudaError_t tc_launch(pkv_dtype dtype, int head_dim, int rows_per_cta, int stages,
+                      const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
+                      dim3 grid, cudaStream_t stream) {
+  KernelInfo info;
+  tc::Launch launch = nullptr;
+  if (!tc::pick(dtype, head_dim, rows_per_cta, stages, &info, &launch))
+    return cudaErrorInvalidValue;
+  return launch(kmap, vmap, p, grid, stream);
+}
+
+}  // namespace pkv

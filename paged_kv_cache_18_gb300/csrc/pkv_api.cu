@@ -12,6 +12,8 @@
 #include <mutex>
 
 #include "../../include/pkv.h"
+#include <algorithm>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -133,10 +135,13 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
   // tensor-core path.
   const bool f32 = s.dtype == PKV_F32 || s.qdtype == PKV_F32;
   if (kernel == PKV_KERNEL_AUTO) kernel = f32 ? PKV_KERNEL_SIMT : PKV_KERNEL_MMA;
-  if (kernel == PKV_KERNEL_MMA && f32) return false;
-  if (kernel != PKV_KERNEL_MMA && kernel != PKV_KERNEL_SIMT) return false;
-  int cap = kernel == PKV_KERNEL_MMA ? 8 * mma_max_tiles(s.head_dim)
-                                     : simt_max_rows(s.head_dim);
+  if ((kernel == PKV_KERNEL_MMA || kernel == PKV_KERNEL_TC) && f32) return false;
+  if (kernel == PKV_KERNEL_TC && s.dtype != s.qdtype) return false;
+  if (kernel != PKV_KERNEL_MMA && kernel != PKV_KERNEL_SIMT && kernel != PKV_KERNEL_TC)
+    return false;
+  int cap = kernel == PKV_KERNEL_MMA  ? 8 * mma_max_tiles(s.head_dim)
+            : kernel == PKV_KERNEL_TC ? kTcMaxRows
+                                      : simt_max_rows(s.head_dim);
   if (opt && opt->rows_per_cta > 0 && opt->rows_per_cta < cap) cap = opt->rows_per_cta;
   const int chunks = ceil_div(rows, cap);
   const int per_cta = ceil_div(rows, chunks);
@@ -154,6 +159,8 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
       if (!ok) m.blocks_per_iter = 0;
     }
     if (!ok) ok = mma_kernel_info(s.dtype, s.qdtype, s.head_dim, m, info);
+  } else if (kernel == PKV_KERNEL_TC) {
+    ok = tc_kernel_info(s.dtype, s.head_dim, per_cta, stages, info);
   } else {
     if (stages != 0) return false;
     int r = 1;
@@ -210,9 +217,19 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
   const int max_blocks = ceil_div(s.max_context_len, s.block_size);
   const int64_t units =
       static_cast<int64_t>(s.batch) * s.num_kv_heads * static_cast<int64_t>(pl->row_chunks);
+  const bool persistent = pl->kernel == PKV_KERNEL_TC;
   int split_blocks;
   if (opt && opt->split_blocks > 0) {
     split_blocks = opt->split_blocks;
+  } else if (persistent) {
+    // tcgen05 kernel: items of 256 blocks (32 chunks; the 20-row verify tile
+    // measured 0.492 of the HBM peak against 0.439 at 64 and 0.489 at 128,
+    // one CTA per item), or fewer when that leaves SMs idle.
+    const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
+    const int64_t per = (units * max_blocks + slots - 1) / slots;
+    split_blocks = static_cast<int>(std::min<int64_t>(256, std::max<int64_t>(32, (per + 7) / 8 * 8)));
+    if (split_blocks < ceil_div(max_blocks, kMaxSplits))
+      split_blocks = (ceil_div(max_blocks, kMaxSplits) + 7) / 8 * 8;
   } else {
     const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
     const int64_t want = kTargetWaves * slots;
@@ -248,12 +265,23 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
   pl->grid_x = num_splits;
   pl->grid_y = s.num_kv_heads * pl->row_chunks;
   pl->grid_z = s.batch;
+  if (persistent) {
+    // one CTA per resident slot walks the items (split x KV head x row chunk
+    // x sequence), or (persistent = 2) one CTA per item
+    const int64_t items = units * num_splits;
+    const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
+    // one CTA per item by default (0.492 against 0.449 walking 56-block items)
+    const bool walk = opt && opt->persistent == 1;
+    pl->grid_x = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(walk ? std::min(items, slots) : items, 0x7fffffff)));
+    pl->grid_y = pl->grid_z = 1;
+  }
   pl->ctas_per_sm = ctas_per_sm;
   pl->workspace_bytes = 0;
   pl->merge_kernel = 0;
   if (num_splits > 1) {
-    const WorkspaceLayout w =
-        workspace_layout(s, num_splits, pl->row_chunks, pl->rows_per_cta, opt ? opt->merge : 0);
+    const WorkspaceLayout w = workspace_layout(s, num_splits, pl->row_chunks, pl->rows_per_cta,
+                                               persistent ? 2 : (opt ? opt->merge : 0));
     pl->workspace_bytes = w.total;
     pl->merge_kernel = w.fused_merge ? 0 : 1;
   }
@@ -365,6 +393,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   int device = 0, sms = 0;
   st = device_plan(s, opt, &pl, &info, &device, &sms);
   if (st != PKV_OK) return st;
+  if (k_new && pl.kernel == PKV_KERNEL_TC) return PKV_ERR_UNSUPPORTED;
   if (pl.workspace_bytes > 0) {
     if (!workspace || !aligned(workspace, 16) || workspace_bytes < pl.workspace_bytes)
       return PKV_ERR_WORKSPACE;
@@ -400,8 +429,9 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   p.out_scale = v_scale;
   bool merge_kernel = false;
   if (pl.num_splits > 1) {
-    const WorkspaceLayout w = workspace_layout(s, pl.num_splits, pl.row_chunks, pl.rows_per_cta,
-                                               opt ? opt->merge : 0);
+    const WorkspaceLayout w =
+        workspace_layout(s, pl.num_splits, pl.row_chunks, pl.rows_per_cta,
+                         pl.kernel == PKV_KERNEL_TC ? 2 : (opt ? opt->merge : 0));
     char *base = static_cast<char *>(workspace);
     p.part_o = reinterpret_cast<float *>(base);
     p.part_lse = reinterpret_cast<float *>(base + w.lse_off);
@@ -424,6 +454,12 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
       return PKV_ERR_CUDA;
     const MmaShape m{ceil_div(pl.rows_per_cta, 8), pl.warp_tiles, pl.blocks_per_iter, pl.stages};
     e = mma_launch(s.dtype, s.qdtype, s.head_dim, m, kmap, vmap, p, grid, stream);
+  } else if (pl.kernel == PKV_KERNEL_TC) {
+    CUtensorMap kmap, vmap;
+    if (!encode_cache_map(&kmap, k_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks) ||
+        !encode_cache_map(&vmap, v_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks))
+      return PKV_ERR_CUDA;
+    e = tc_launch(s.dtype, s.head_dim, pl.rows_per_cta, pl.stages, kmap, vmap, p, grid, stream);
   } else {
     int r = 1;
     while (r < pl.rows_per_cta) r <<= 1;

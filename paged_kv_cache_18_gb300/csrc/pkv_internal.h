@@ -39,6 +39,16 @@ cudaError_t mma_launch(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, c
                        const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
                        dim3 grid, cudaStream_t stream);
 
+// tcgen05 kernel (TMEM accumulators, 128-key chunks): bf16 / f16 caches, q of
+// the same type, head_dim 128, up to 32 query rows per CTA.
+constexpr int kTcMaxRows = 32;
+// stages: chunk ring depth 1..3 (0 = default).
+bool tc_kernel_info(pkv_dtype dtype, int head_dim, int rows_per_cta, int stages,
+                    KernelInfo *info);
+cudaError_t tc_launch(pkv_dtype dtype, int head_dim, int rows_per_cta, int stages,
+                      const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
+                      dim3 grid, cudaStream_t stream);
+
 // CUDA-core kernel: rows = query rows per CTA (1, 2, 4 or 8); the cache type
 // may be FP8 E4M3 with q of another type, else both types are equal.
 int simt_max_rows(int head_dim);

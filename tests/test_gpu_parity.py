@@ -489,3 +489,100 @@ def test_two_blocks_tree_verify(Q, Hq, Hkv):
     ref = oracle.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
                                 wl.softmax_scale, "bf16", masks)
     assert_close(host_f64(out, "bf16"), ref, "bf16", wl.name)
+
+
+# ---- tcgen05 kernel (TMEM accumulators, 128-key chunks) -------------------
+TC_CASES = [  # Q, Hq, Hkv: 20, 9, 16, 16, 32, 32, 28, 15, 4 and 1 query rows per KV head
+    (5, 32, 8), (3, 24, 8), (2, 32, 4), (1, 16, 1), (4, 32, 4), (8, 16, 4), (7, 36, 9),
+    (3, 40, 8), (1, 32, 8), (1, 8, 8)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("Q,Hq,Hkv", TC_CASES)
+@pytest.mark.parametrize("split_blocks", [0, 3, 8, 9])
+def test_tc_kernel(dtype, Q, Hq, Hkv, split_blocks):
+    lens = [Q, 15, 16, 17, 127, 128, 129, 300, 1000]
+    wl = W.Workload(f"tc {dtype} Q{Q} {Hq}/{Hkv} sb{split_blocks}", len(lens), Hq, Hkv, 128,
+                    dtype, context_lens=lens, num_queries=Q,
+                    seed=1600 + Q + Hq + Hkv + split_blocks)
+    run_case(wl, kernel=3, split_blocks=split_blocks)
+
+
+def test_tc_kernel_long_and_ragged():
+    wl = W.Workload("tc long", 6, 32, 8, 128, "bf16", len_range=(1, 9000), num_queries=5,
+                    seed=1650)
+    run_case(wl, kernel=3)
+    run_case(wl, kernel=3, split_blocks=40)
+
+
+@pytest.mark.parametrize("Q,Hq,Hkv", [(5, 32, 8), (16, 8, 4), (9, 16, 8)])
+def test_tc_tree_verify(Q, Hq, Hkv):
+    import oracle
+    import paged_kv_cache_18_gb300 as pkv
+    rng = np.random.default_rng(Q + 77)
+    lens = [Q, Q + 3, Q + 140, Q + 301]
+    wl = W.Workload(f"tc tree Q{Q}", len(lens), Hq, Hkv, 128, "bf16", context_lens=lens,
+                    num_queries=Q, seed=1660 + Q)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    masks = _tree_masks(Q, wl.batch, rng)
+    tm = torch.from_numpy(np.ascontiguousarray(masks).view(np.int64)).cuda()
+    out = pkv.tree_verify_attention(d.q, d.k_cache, d.v_cache, d.table, d.lens, tm,
+                                    scale=wl.softmax_scale, max_context_len=b.max_context_len,
+                                    kernel=3, error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    oracle.kv_append(b.k_cache, b.v_cache, b.k_new, b.v_new, b.slot_mapping, "bf16")
+    ref = oracle.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                wl.softmax_scale, "bf16", masks)
+    assert_close(host_f64(out, "bf16"), ref, "bf16", wl.name)
+
+
+def test_tc_refuses_what_it_does_not_build():
+    import paged_kv_cache_18_gb300 as pkv
+    for args in [(2, 1, 8, 8, 64, 100, torch.bfloat16),    # head_dim 64
+                 (2, 1, 8, 8, 128, 100, torch.float32)]:   # float32
+        with pytest.raises(pkv.PkvError):
+            pkv.plan(*args, kernel=3)
+    # more than 32 rows per KV head: split over row chunks of <= 32
+    p = pkv.plan(2, 9, 32, 8, 128, 100, torch.bfloat16, kernel=3)
+    assert p["rows_per_cta"] <= 32 and p["row_chunks"] == 2
+    # the fused append stays on the other kernels
+    wl = W.Workload("tc fused", 2, 32, 8, 128, "bf16", context_lens=[20, 40], num_queries=5,
+                    seed=1670)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    with pytest.raises(pkv.PkvError):
+        pkv.append_attention(d.q, d.k_new.view(2, 5, 8, 128), d.v_new.view(2, 5, 8, 128),
+                             d.k_cache, d.v_cache, d.table, d.lens,
+                             max_context_len=b.max_context_len, kernel=3)
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3])
+@pytest.mark.parametrize("Q,Hq,Hkv", [(5, 32, 8), (2, 32, 4), (1, 8, 8)])
+@pytest.mark.parametrize("split_blocks", [0, 3, 17])
+def test_tc_ring_depths(stages, Q, Hq, Hkv, split_blocks):
+    lens = [Q, 16, 129, 300, 1000, 2100]
+    wl = W.Workload(f"tc st{stages} Q{Q} {Hq}/{Hkv} sb{split_blocks}", len(lens), Hq, Hkv, 128,
+                    "bf16", context_lens=lens, num_queries=Q,
+                    seed=1700 + 10 * stages + Q + Hq + split_blocks)
+    run_case(wl, kernel=3, stages=stages, split_blocks=split_blocks)
+
+
+@pytest.mark.parametrize("persistent", [1, 2])
+@pytest.mark.parametrize("stages", [1, 2, 3])
+@pytest.mark.parametrize("split_blocks", [8, 13, 56])
+def test_tc_many_items_per_cta(persistent, stages, split_blocks):
+    # enough (split, KV head, sequence) items that every CTA walking them
+    # (persistent 1) takes several, reusing its Q^T and O^T buffers across
+    # items; persistent 2: one CTA per item
+    with tuning(persistent=persistent):
+        wl = W.Workload(f"tc items p{persistent} st{stages} sb{split_blocks}", 16, 32, 8, 128,
+                        "bf16", len_range=(1, 6000), num_queries=5,
+                        seed=1800 + stages + split_blocks)
+        run_case(wl, kernel=3, stages=stages, split_blocks=split_blocks)
+        wl = W.Workload(f"tc items gqa p{persistent} st{stages} sb{split_blocks}", 64, 32, 8,
+                        128, "bf16", len_range=(1, 3000), num_queries=3,
+                        seed=1850 + stages + split_blocks)
+        run_case(wl, kernel=3, stages=stages, split_blocks=split_blocks)
