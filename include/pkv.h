@@ -391,6 +391,107 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
     int64_t num_blocks, float scale, pkv_dtype dtype,
     const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
 
+/*
+ * ---- Block manager (host) and copy-on-write (device) ----------------------
+ * "KV cache, prefill và decode" (blog.truongducdung.dev), section 05, "Block
+ * table", "Chia sẻ block và copy-on-write" and "Prefix caching"; "Inference
+ * part 1", section "Prefix caching"; "Efficient Inference", the paged
+ * attention section.  The pages fix: fixed-size blocks, a new block only
+ * when a sequence's last one is full; a reference count per physical block;
+ * sequences forked from one prompt share its blocks and copy a shared block
+ * before writing into it; a full block is identified by a hash of its tokens
+ * chained with its parent block's hash, and a prompt's lookup walks its
+ * blocks from the start to the first miss, reusing each hit (reference
+ * count + 1); finished requests return their blocks to the free pool.
+ * Readings of this library where the pages are silent:
+ *   - free blocks are reused last-freed first;
+ *   - a block is cached (registered under its hash) the moment it is full;
+ *     a second full block with the same hash is not merged;
+ *   - cached blocks that no sequence holds stay reusable until the pool runs
+ *     dry, then the least recently used goes first (ties: lower id); a hit
+ *     or a release is a use;
+ *   - hash = 64-bit FNV-1a over (parent hash as 8 little-endian bytes, 0 for
+ *     the first block) then the block's token ids as 4 little-endian bytes.
+ * The manager is host memory only and not thread-safe: serialise calls on
+ * one manager.  Block ids index the caches' first dimension.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager of num_blocks blocks of block_size tokens, all free; NULL on a
+ * bad size or allocation failure.  Destroy frees it (NULL is a no-op). */
+PKV_API pkv_block_manager *pkv_bm_create(int64_t num_blocks, int block_size);
+PKV_API void pkv_bm_destroy(pkv_block_manager *m);
+
+/*
+ * pkv_bm_add_sequence -- a new sequence `seq_id` holding the n tokens of a
+ * prompt.  With use_prefix_cache, its leading full blocks whose hash chain is
+ * cached are shared (*cached_tokens = their token count, a multiple of the
+ * block size; the caller prefills only the rest).  slots[0 .. n - cached)
+ * receive the cache slots (block * block_size + offset) of tokens
+ * cached .. n - 1, in order: the slot_mapping of pkv_kv_append.
+ * PKV_ERR_INVALID_ARG for a known seq_id; PKV_ERR_WORKSPACE when the pool
+ * cannot hold the prompt (nothing changes).
+ */
+PKV_API pkv_status pkv_bm_add_sequence(pkv_block_manager *m, int64_t seq_id,
+                                       const int32_t *tokens, int n, int use_prefix_cache,
+                                       int *cached_tokens, int64_t *slots);
+
+/*
+ * pkv_bm_append -- append n tokens to a sequence (decode: n = 1; verify:
+ * K + 1).  slots[0 .. n) receive their cache slots.  If the sequence's last
+ * block is partly filled and shared, it is first replaced by a copy: one
+ * (cow_src[0], cow_dst[0]) pair, *num_cow = 1, which the caller must copy
+ * (pkv_copy_blocks) before writing the new rows; else *num_cow = 0.
+ * PKV_ERR_WORKSPACE when the pool is short (nothing changes).
+ */
+PKV_API pkv_status pkv_bm_append(pkv_block_manager *m, int64_t seq_id, const int32_t *tokens,
+                                 int n, int64_t *slots, int32_t *cow_src, int32_t *cow_dst,
+                                 int *num_cow);
+
+/* pkv_bm_fork -- sequence `child` shares all of `parent`'s blocks (parallel
+ * sampling; every block's reference count + 1). */
+PKV_API pkv_status pkv_bm_fork(pkv_block_manager *m, int64_t parent, int64_t child);
+
+/* pkv_bm_free -- drop a sequence: its blocks' counts - 1; blocks reaching 0
+ * return to the pool (cached ones stay reusable until evicted). */
+PKV_API pkv_status pkv_bm_free(pkv_block_manager *m, int64_t seq_id);
+
+/* pkv_bm_sequence -- a sequence's blocks (blocks[0 .. *num_blocks), NULL to
+ * query the count) and token count. */
+PKV_API pkv_status pkv_bm_sequence(const pkv_block_manager *m, int64_t seq_id, int32_t *blocks,
+                                   int max_blocks, int *num_blocks, int *num_tokens);
+
+/* pkv_bm_block_table -- the block_table [num_seqs, max_blocks_per_seq]
+ * (unused entries -1) and context_lens [num_seqs] of the attention calls,
+ * for the listed sequences. */
+PKV_API pkv_status pkv_bm_block_table(const pkv_block_manager *m, const int64_t *seq_ids,
+                                      int num_seqs, int32_t *table, int max_blocks_per_seq,
+                                      int32_t *context_lens);
+
+/* Counts: free (unreferenced, uncached) blocks, cached blocks, sequences. */
+PKV_API pkv_status pkv_bm_stats(const pkv_block_manager *m, int64_t *free_blocks,
+                                int64_t *cached_blocks, int64_t *num_sequences);
+
+/* One block's reference count, whether it is cached, and its hash (valid
+ * once the block has been full). */
+PKV_API pkv_status pkv_bm_block_info(const pkv_block_manager *m, int32_t block, int32_t *ref,
+                                     int32_t *cached, uint64_t *hash);
+
+/* The block hash of the chain rule above, for n tokens after parent_hash. */
+PKV_API uint64_t pkv_bm_hash(uint64_t parent_hash, const int32_t *tokens, int n);
+
+/*
+ * pkv_copy_blocks -- copy whole blocks src[i] -> dst[i] (i < num_pairs) in
+ * both device caches [num_blocks, num_kv_heads, block_size, head_dim] of
+ * dtype (any cache type): the copies of copy-on-write.  src / dst: device
+ * int32 arrays; destinations distinct and not among the sources.
+ * Out-of-range ids are skipped and recorded (PKV_DEVERR_BLOCK_ID).
+ */
+PKV_API pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
+                                   const int32_t *dst, int num_pairs, int num_kv_heads,
+                                   int head_dim, int block_size, int64_t num_blocks,
+                                   pkv_dtype dtype, int32_t *error_word, pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

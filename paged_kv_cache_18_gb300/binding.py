@@ -34,7 +34,10 @@ EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_
             "pkv_paged_decode_attention", "pkv_spec_verify_attention",
             "pkv_read_error_word", "pkv_paged_decode_attention_noalloc",
             "pkv_append_attention", "pkv_tree_verify_attention", "pkv_kv_append_fp8",
-            "pkv_paged_attention_fp8")
+            "pkv_paged_attention_fp8", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence",
+            "pkv_bm_append", "pkv_bm_fork", "pkv_bm_free", "pkv_bm_sequence",
+            "pkv_bm_block_table", "pkv_bm_stats", "pkv_bm_block_info", "pkv_bm_hash",
+            "pkv_copy_blocks")
 
 
 class PkvError(RuntimeError):
@@ -117,9 +120,27 @@ def lib() -> ctypes.CDLL:
             L.pkv_paged_decode_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32,
                                                              i32, i32, i32, i32, i32, i64, f32,
                                                              i32, opt, vp, vp]
+            pi32, pi64 = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+            pint, u64 = ctypes.POINTER(ctypes.c_int), ctypes.c_uint64
+            L.pkv_bm_create.argtypes = [i64, i32]
+            L.pkv_bm_destroy.argtypes = [vp]
+            L.pkv_bm_add_sequence.argtypes = [vp, i64, pi32, i32, i32, pint, pi64]
+            L.pkv_bm_append.argtypes = [vp, i64, pi32, i32, pi64, pi32, pi32, pint]
+            L.pkv_bm_fork.argtypes = [vp, i64, i64]
+            L.pkv_bm_free.argtypes = [vp, i64]
+            L.pkv_bm_sequence.argtypes = [vp, i64, pi32, i32, pint, pint]
+            L.pkv_bm_block_table.argtypes = [vp, pi64, i32, pi32, i32, pi32]
+            L.pkv_bm_stats.argtypes = [vp, pi64, pi64, pi64]
+            L.pkv_bm_block_info.argtypes = [vp, ctypes.c_int32, pi32, pi32,
+                                            ctypes.POINTER(u64)]
+            L.pkv_bm_hash.argtypes = [u64, pi32, i32]
+            L.pkv_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64, i32, vp, vp]
             for name in EXPORTED:
                 if name not in ("pkv_status_string", "pkv_version"):
                     getattr(L, name).restype = i32
+            L.pkv_bm_create.restype = vp
+            L.pkv_bm_destroy.restype = None
+            L.pkv_bm_hash.restype = u64
             _lib = L
     return _lib
 
@@ -471,3 +492,118 @@ def read_error_word(error_word: torch.Tensor) -> int:
     _check("pkv_read_error_word", lib().pkv_read_error_word(
         error_word.data_ptr(), ctypes.byref(code), _stream(error_word)))
     return int(code.value)
+
+
+# ---- block manager and copy-on-write ---------------------------------------
+def _i32_array(values):
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(values, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def bm_hash(parent_hash: int, tokens) -> int:
+    """Block hash of the prefix chain (pkv_bm_hash)."""
+    a, ptr = _i32_array(tokens)
+    return int(lib().pkv_bm_hash(ctypes.c_uint64(parent_hash), ptr, len(a)))
+
+
+class BlockManager:
+    """Physical blocks, reference counts, copy-on-write and the prefix hash
+    chain of a paged KV cache (pkv_bm_*): host memory, not thread-safe."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        self.block_size = block_size
+        self.num_blocks = num_blocks
+        self._h = lib().pkv_bm_create(num_blocks, block_size)
+        if not self._h:
+            raise PkvError("pkv_bm_create", 1, "bad size or out of memory")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def add_sequence(self, seq_id: int, tokens, prefix_cache: bool = True):
+        """New sequence from a prompt -> (cached_tokens, slots of the rest)."""
+        import numpy as np
+        a, ptr = _i32_array(tokens)
+        slots = np.zeros(max(len(a), 1), dtype=np.int64)
+        cached = ctypes.c_int(0)
+        _check("pkv_bm_add_sequence", lib().pkv_bm_add_sequence(
+            self._h, seq_id, ptr, len(a), int(prefix_cache), ctypes.byref(cached),
+            slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))))
+        return cached.value, slots[:len(a) - cached.value].copy()
+
+    def append(self, seq_id: int, tokens):
+        """Append tokens -> (slots, [(cow_src, cow_dst)])."""
+        import numpy as np
+        a, ptr = _i32_array(tokens)
+        slots = np.zeros(max(len(a), 1), dtype=np.int64)
+        src, dst, n = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int(0)
+        _check("pkv_bm_append", lib().pkv_bm_append(
+            self._h, seq_id, ptr, len(a), slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            ctypes.byref(src), ctypes.byref(dst), ctypes.byref(n)))
+        return slots[:len(a)].copy(), [(src.value, dst.value)] if n.value else []
+
+    def fork(self, parent: int, child: int):
+        _check("pkv_bm_fork", lib().pkv_bm_fork(self._h, parent, child))
+
+    def free(self, seq_id: int):
+        _check("pkv_bm_free", lib().pkv_bm_free(self._h, seq_id))
+
+    def sequence(self, seq_id: int):
+        """(block ids, token count) of a sequence."""
+        nb, nt = ctypes.c_int(0), ctypes.c_int(0)
+        _check("pkv_bm_sequence", lib().pkv_bm_sequence(self._h, seq_id, None, 0,
+                                                         ctypes.byref(nb), ctypes.byref(nt)))
+        buf = (ctypes.c_int32 * max(nb.value, 1))()
+        _check("pkv_bm_sequence", lib().pkv_bm_sequence(self._h, seq_id, buf, nb.value,
+                                                         ctypes.byref(nb), ctypes.byref(nt)))
+        return list(buf[:nb.value]), nt.value
+
+    def block_table(self, seq_ids, max_blocks: int = 0):
+        """(block_table int32 [n, max_blocks], context_lens int32 [n])."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        if max_blocks <= 0:
+            max_blocks = max([len(self.sequence(int(i))[0]) for i in ids] + [1])
+        table = np.zeros((len(ids), max_blocks), dtype=np.int32)
+        lens = np.zeros(len(ids), dtype=np.int32)
+        _check("pkv_bm_block_table", lib().pkv_bm_block_table(
+            self._h, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(ids),
+            table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), max_blocks,
+            lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+        return table, lens
+
+    def stats(self) -> dict:
+        f, c, n = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        _check("pkv_bm_stats", lib().pkv_bm_stats(self._h, ctypes.byref(f), ctypes.byref(c),
+                                                  ctypes.byref(n)))
+        return {"free": f.value, "cached": c.value, "sequences": n.value}
+
+    def block_info(self, block: int):
+        """(reference count, cached, hash) of one block."""
+        r, c, h = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_uint64(0)
+        _check("pkv_bm_block_info", lib().pkv_bm_block_info(self._h, block, ctypes.byref(r),
+                                                            ctypes.byref(c), ctypes.byref(h)))
+        return r.value, bool(c.value), h.value
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src, dst,
+                error_word: Optional[torch.Tensor] = None) -> None:
+    """Copy whole blocks src[i] -> dst[i] of both caches (pkv_copy_blocks)."""
+    _need(k_cache.is_cuda and k_cache.is_contiguous() and v_cache.shape == k_cache.shape
+          and v_cache.dtype == k_cache.dtype and v_cache.is_contiguous() and k_cache.dim() == 4,
+          "k_cache / v_cache: contiguous CUDA [num_blocks, num_kv_heads, block_size, head_dim]")
+    dev = k_cache.device
+    src = torch.as_tensor(src, dtype=torch.int32, device=dev).contiguous()
+    dst = torch.as_tensor(dst, dtype=torch.int32, device=dev).contiguous()
+    _need(src.shape == dst.shape and src.dim() == 1, "src / dst: equal-length 1-D")
+    NB, Hkv, bs, D = k_cache.shape
+    dt = PKV_FP8_E4M3 if k_cache.dtype == torch.uint8 else _DTYPE[k_cache.dtype]
+    _check("pkv_copy_blocks", lib().pkv_copy_blocks(
+        k_cache.data_ptr(), v_cache.data_ptr(), src.data_ptr(), dst.data_ptr(), src.numel(),
+        Hkv, D, bs, NB, dt, _err_ptr(error_word), _stream(k_cache)))

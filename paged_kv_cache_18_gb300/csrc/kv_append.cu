@@ -177,3 +177,51 @@ cudaError_t append_fp8_launch(pkv_dtype src_dtype, const void *k_new, const void
 }
 
 }  // namespace pkv
+
+// ---- copy_blocks: whole physical blocks, for copy-on-write ------------------
+// ("KV cache, prefill và decode", section 05, "Chia sẻ block và
+// copy-on-write": a shared block is copied to a fresh one before a sequence
+// writes into it.)  One block of one cache is num_kv_heads x block_size x
+// head_dim elements, contiguous; pair i copies block src[i] to dst[i] in both
+// caches.  Out-of-range ids are skipped and recorded.
+namespace pkv {
+namespace {
+
+__global__ void copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                   const int32_t *__restrict__ src,
+                                   const int32_t *__restrict__ dst, int num_pairs,
+                                   int64_t vec_per_block, int64_t num_blocks, int32_t *err) {
+  const int64_t total = static_cast<int64_t>(num_pairs) * vec_per_block;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int pair = static_cast<int>(i / vec_per_block);
+    const int64_t off = i - static_cast<int64_t>(pair) * vec_per_block;
+    const int32_t s = __ldg(src + pair), d = __ldg(dst + pair);
+    if (s < 0 || d < 0 || s >= num_blocks || d >= num_blocks) {
+      if (off == 0) record_error(err, PKV_DEVERR_BLOCK_ID);
+      continue;
+    }
+    k_cache[d * vec_per_block + off] = k_cache[s * vec_per_block + off];
+    v_cache[d * vec_per_block + off] = v_cache[s * vec_per_block + off];
+  }
+}
+
+}  // namespace
+
+cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src,
+                               const int32_t *dst, int num_pairs, int64_t block_bytes,
+                               int64_t num_blocks, int32_t *err, int sm_count,
+                               cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  const int64_t vpb = block_bytes / 16;
+  const int64_t total = static_cast<int64_t>(num_pairs) * vpb;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
+  copy_blocks_kernel<<<grid, threads, 0, stream>>>(static_cast<uint4 *>(k_cache),
+                                                  static_cast<uint4 *>(v_cache), src, dst,
+                                                  num_pairs, vpb, num_blocks, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -517,6 +517,29 @@ pkv_status pkv_kv_append(const void *k_new, const void *v_new, void *k_cache, vo
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, const int32_t *dst,
+                           int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                           int64_t num_blocks, pkv_dtype dtype, int32_t *error_word,
+                           pkv_stream_t stream) {
+  if (num_pairs < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || num_blocks < 1 ||
+      !valid_cache_dtype(dtype))
+    return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src || !dst) return PKV_ERR_INVALID_ARG;
+  const int64_t block_bytes =
+      static_cast<int64_t>(num_kv_heads) * block_size * head_dim * elt_bytes(dtype);
+  if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src, 4) || !aligned(dst, 4) ||
+      (error_word && !aligned(error_word, 4)))
+    return PKV_ERR_ALIGNMENT;
+  int device = 0, sms = 0;
+  if (current_sm_count(&device, &sms) != cudaSuccess) return PKV_ERR_CUDA;
+  const cudaError_t e = copy_blocks_launch(k_cache, v_cache, src, dst, num_pairs, block_bytes,
+                                           num_blocks, error_word, sms,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_attention_plan_for(int batch, int num_queries, int num_heads, int num_kv_heads,
                                   int head_dim, int block_size, int max_context_len,
                                   pkv_dtype dtype, const pkv_options *options, int num_sms,

@@ -69,6 +69,12 @@ cudaError_t append_fp8_launch(pkv_dtype src_dtype, const void *k_new, const void
                               int64_t num_blocks, float k_scale, float v_scale, int32_t *err,
                               int sm_count, cudaStream_t stream);
 
+// Whole-block copies (copy-on-write) in both caches.
+cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src,
+                               const int32_t *dst, int num_pairs, int64_t block_bytes,
+                               int64_t num_blocks, int32_t *err, int sm_count,
+                               cudaStream_t stream);
+
 // kv_append.
 cudaError_t append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           const int64_t *slots, int64_t num_tokens, int num_kv_heads,
