@@ -350,6 +350,38 @@ PKV_API pkv_status pkv_paged_attention_fp8(
     const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
 
 /*
+ * pkv_paged_prefill_attention -- chunked prefill: each sequence brings a
+ * chunk of new query rows whose K and V have already been appended
+ * (pkv_kv_append), and every row attends to the cache up to itself
+ * ("Inference part 1", sections "KV cache" and "Chunked prefill"; the
+ * arithmetic of its section "FlashAttention").
+ *   q, out       [total_q, num_heads, head_dim] of dtype (BF16 or F16),
+ *                16-byte aligned; the rows of sequence b are
+ *                query_start[b] .. query_start[b + 1] - 1 (q_len_b rows).
+ *   query_start  device int32 [batch + 1], non-decreasing, query_start[0] >= 0,
+ *                query_start[batch] <= total_q, each q_len_b <= max_query_len.
+ *   context_lens device int32 [batch]: rows in sequence b's cache, the
+ *                chunk's own rows included (L_b >= q_len_b).
+ *   Row j of sequence b sees cache rows i <= L_b - q_len_b + j.
+ *   head_dim 64 or 128; block_size 16; num_heads / num_kv_heads must divide
+ *   128.  No workspace: the work is split over query rows (256 per CTA),
+ *   not over keys.  options: only `stages` (K/V ring depth; 0 = default) is
+ *   read.  Runs on the fifth-generation tensor cores (tcgen05), S and O in
+ *   tensor memory, P rounded to dtype.
+ * A sequence whose query_start / context_lens break these rules is skipped
+ * (its rows are not written) and recorded as PKV_DEVERR_CONTEXT_LEN; an
+ * out-of-range block id is recorded as PKV_DEVERR_BLOCK_ID and its keys are
+ * ignored.  Argument errors return synchronously with nothing enqueued.
+ */
+PKV_API pkv_status pkv_paged_prefill_attention(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_table, int max_blocks_per_seq,
+    const int32_t *context_lens, const int32_t *query_start, int max_query_len,
+    int batch, int total_q, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, float scale, pkv_dtype dtype,
+    const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
+
+/*
  * pkv_read_error_word -- copy the device error word to *host_code after all
  * work on `stream` (synchronises the stream; not for the hot path).
  */

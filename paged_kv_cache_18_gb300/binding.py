@@ -37,7 +37,7 @@ EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_
             "pkv_paged_attention_fp8", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence",
             "pkv_bm_append", "pkv_bm_fork", "pkv_bm_free", "pkv_bm_sequence",
             "pkv_bm_block_table", "pkv_bm_stats", "pkv_bm_block_info", "pkv_bm_hash",
-            "pkv_copy_blocks")
+            "pkv_copy_blocks", "pkv_paged_prefill_attention")
 
 
 class PkvError(RuntimeError):
@@ -135,6 +135,9 @@ def lib() -> ctypes.CDLL:
                                             ctypes.POINTER(u64)]
             L.pkv_bm_hash.argtypes = [u64, pi32, i32]
             L.pkv_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64, i32, vp, vp]
+            L.pkv_paged_prefill_attention.argtypes = [
+                vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64,
+                ctypes.c_float, i32, ctypes.POINTER(Options), vp, vp]
             for name in EXPORTED:
                 if name not in ("pkv_status_string", "pkv_version"):
                     getattr(L, name).restype = i32
@@ -607,3 +610,44 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src, dst,
     _check("pkv_copy_blocks", lib().pkv_copy_blocks(
         k_cache.data_ptr(), v_cache.data_ptr(), src.data_ptr(), dst.data_ptr(), src.numel(),
         Hkv, D, bs, NB, dt, _err_ptr(error_word), _stream(k_cache)))
+
+
+# ---- chunked prefill ------------------------------------------------------------
+def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_table: torch.Tensor, context_lens: torch.Tensor,
+                            query_start: torch.Tensor, max_query_len: Optional[int] = None,
+                            scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                            stages: int = 0,
+                            error_word: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Chunked prefill: q [total_q, Hq, D], the rows of sequence b being
+    query_start[b] .. query_start[b + 1] - 1, whose K/V rows are already the
+    last rows of its cache -> out of q's shape (pkv_paged_prefill_attention).
+    Pass ``max_query_len`` (a host bound of the chunk lengths) to avoid a
+    device read."""
+    NB, Hkv, bs, D = _cache_args(k_cache, v_cache)
+    _need(q.dim() == 3 and q.shape[-1] == D and q.dtype == k_cache.dtype and q.is_cuda
+          and q.is_contiguous(), "q must be a contiguous CUDA [total_q, Hq, D] of the cache dtype")
+    total_q, Hq = q.shape[0], q.shape[1]
+    B = context_lens.shape[0]
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2
+          and block_table.shape[0] == B and block_table.is_contiguous() and block_table.is_cuda,
+          "block_table must be a contiguous CUDA int32 [batch, max_blocks_per_seq]")
+    _need(context_lens.dtype == torch.int32 and context_lens.dim() == 1
+          and context_lens.is_cuda and context_lens.is_contiguous(),
+          "context_lens must be a contiguous CUDA int32 [batch]")
+    _need(query_start.dtype == torch.int32 and query_start.shape == (B + 1,)
+          and query_start.is_cuda and query_start.is_contiguous(),
+          "query_start must be a contiguous CUDA int32 [batch + 1]")
+    if max_query_len is None:
+        max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if B else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
+    _check("pkv_paged_prefill_attention", lib().pkv_paged_prefill_attention(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_table.data_ptr(), block_table.shape[1], context_lens.data_ptr(),
+        query_start.data_ptr(), int(max_query_len), B, total_q, Hq, Hkv, D, bs, NB,
+        float(scale), _DTYPE[q.dtype], _opts(0, 0, stages), _err_ptr(error_word), _stream(q)))
+    return out

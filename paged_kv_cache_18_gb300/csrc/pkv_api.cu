@@ -540,6 +540,82 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src, con
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// Q [total_q, Hq, D] as a 3-D tensor (D, Hq, total_q); one box is a
+// 128-byte column panel of 128 rows: 128 / group positions x the group's
+// heads, 128-byte swizzled.  Rows past total_q read as zero.
+bool encode_query_map(CUtensorMap *map, const void *base, pkv_dtype dt, int D, int Hq,
+                      int total_q, int group) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const int eb = elt_bytes(dt);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                              static_cast<cuuint64_t>(total_q)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * eb,
+                                 static_cast<cuuint64_t>(D) * eb * Hq};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(group),
+                             static_cast<cuuint32_t>(128 / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType type =
+      dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(map, type, 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+pkv_status pkv_paged_prefill_attention(void *out, const void *q, const void *k_cache,
+                                       const void *v_cache, const int32_t *block_table,
+                                       int max_blocks_per_seq, const int32_t *context_lens,
+                                       const int32_t *query_start, int max_query_len, int batch,
+                                       int total_q, int num_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int64_t num_blocks, float scale,
+                                       pkv_dtype dtype, const pkv_options *options,
+                                       int32_t *error_word, pkv_stream_t stream) {
+  if (batch < 0 || total_q < 0 || max_query_len < 0 || num_heads < 1 || num_kv_heads < 1 ||
+      num_heads % num_kv_heads != 0 || !valid_dtype(dtype))
+    return PKV_ERR_INVALID_ARG;
+  const int group = num_heads / num_kv_heads;
+  const int stages = options ? options->stages : 0;
+  if (block_size != kBlockSize || !prefill_supported(dtype, head_dim, group, stages))
+    return PKV_ERR_UNSUPPORTED;
+  if (batch == 0 || total_q == 0 || max_query_len == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens || !query_start)
+    return PKV_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale) || batch > 65535 ||
+      num_kv_heads > 65535)
+    return PKV_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(max_query_len) * group;
+  const int64_t pairs = (rows + prefill_rows_per_cta() - 1) / prefill_rows_per_cta();
+  if (pairs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(query_start, 4) ||
+      (error_word && !aligned(error_word, 4)))
+    return PKV_ERR_ALIGNMENT;
+  CUtensorMap qmap, kmap, vmap;
+  if (!encode_query_map(&qmap, q, dtype, head_dim, num_heads, total_q, group) ||
+      !encode_cache_map(&kmap, k_cache, dtype, head_dim, num_kv_heads, num_blocks) ||
+      !encode_cache_map(&vmap, v_cache, dtype, head_dim, num_kv_heads, num_blocks))
+    return PKV_ERR_INVALID_ARG;
+  PrefillParams p{};
+  p.out = out;
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.query_start = query_start;
+  p.err = error_word;
+  p.num_blocks = num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.batch = batch;
+  p.total_q = total_q;
+  p.max_query_len = max_query_len;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.pairs = static_cast<int>(pairs);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cudaError_t e = prefill_launch(dtype, head_dim, stages, qmap, kmap, vmap, p,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_attention_plan_for(int batch, int num_queries, int num_heads, int num_kv_heads,
                                   int head_dim, int block_size, int max_context_len,
                                   pkv_dtype dtype, const pkv_options *options, int num_sms,

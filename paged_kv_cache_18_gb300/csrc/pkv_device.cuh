@@ -50,6 +50,21 @@ struct AttnParams {
   float out_scale;              // multiplies every output (value scale of an FP8 cache; else 1)
 };
 
+// Chunked prefill: the query rows of sequence b are q[query_start[b] ..
+// query_start[b + 1]) ([total_q, Hq, D]); its cache holds context_lens[b]
+// rows, the chunk's own rows last.
+struct PrefillParams {
+  void *out;                     // [total_q, Hq, D] elt
+  const int32_t *block_table;    // [B, max_blocks_per_seq]
+  const int32_t *context_lens;   // [B]
+  const int32_t *query_start;    // [B + 1]
+  int32_t *err;                  // optional device error word
+  int64_t num_blocks;
+  int max_blocks_per_seq, batch, total_q, max_query_len;
+  int num_heads, num_kv_heads, group, pairs;
+  float scale_log2;              // softmax scale * log2(e)
+};
+
 // FP8 E4M3 cache element (one byte; value = code value * tensor scale).
 struct E4M3 {};
 
@@ -144,6 +159,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Tiled 3-D tensor copy (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
 

@@ -12,6 +12,7 @@
 namespace pkv {
 
 struct AttnParams;
+struct PrefillParams;
 
 struct KernelInfo {
   const void *func = nullptr;
@@ -48,6 +49,15 @@ bool tc_kernel_info(pkv_dtype dtype, int head_dim, int rows_per_cta, int stages,
 cudaError_t tc_launch(pkv_dtype dtype, int head_dim, int rows_per_cta, int stages,
                       const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
                       dim3 grid, cudaStream_t stream);
+
+// Chunked prefill on the tcgen05 tensor cores (attn_prefill.cu): head_dim 64
+// or 128, bf16 / f16, group size dividing 128.  `stages` is the K/V ring
+// depth (0: default).
+bool prefill_supported(pkv_dtype dtype, int head_dim, int group, int stages);
+int prefill_rows_per_cta();
+cudaError_t prefill_launch(pkv_dtype dtype, int head_dim, int stages, const CUtensorMap &qmap,
+                           const CUtensorMap &kmap, const CUtensorMap &vmap,
+                           const PrefillParams &p, cudaStream_t stream);
 
 // CUDA-core kernel: rows = query rows per CTA (1, 2, 4 or 8); the cache type
 // may be FP8 E4M3 with q of another type, else both types are equal.

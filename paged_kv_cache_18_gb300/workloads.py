@@ -197,6 +197,129 @@ def make_batch(wl: Workload, poison: bool = True) -> PagedBatch:
                       lens.astype(np.int32), NB)
 
 
+# ---- chunked prefill ----------------------------------------------------------------
+@dataclasses.dataclass
+class PrefillWorkload:
+    """One chunked-prefill call: each sequence has `prefix` cached rows and
+    brings a chunk of `chunk` new rows (appended first, then attending)."""
+    name: str
+    batch: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    dtype: str
+    chunk_lens: Optional[Sequence[int]] = None      # fixed chunk lengths (or one for all)
+    chunk_range: Optional[tuple] = None             # (lo, hi) inclusive uniform
+    prefix_lens: Optional[Sequence[int]] = None
+    prefix_range: Optional[tuple] = None
+    block_size: int = 16
+    scale: Optional[float] = None
+    seed: int = 0
+    slack: float = 0.10
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.head_dim)
+
+    def _draw(self, fixed, rng_range, salt):
+        if fixed is not None:
+            a = np.asarray(fixed, dtype=np.int32)
+            return np.full(self.batch, int(a[0]), np.int32) if a.size == 1 else a
+        lo, hi = rng_range
+        rng = np.random.Generator(np.random.PCG64(self.seed + salt))
+        return rng.integers(lo, hi, size=self.batch, endpoint=True).astype(np.int32)
+
+    def chunks(self) -> np.ndarray:
+        return self._draw(self.chunk_lens, self.chunk_range, 7907)
+
+    def prefixes(self) -> np.ndarray:
+        return self._draw(self.prefix_lens, self.prefix_range, 7919)
+
+    def flops(self) -> int:
+        """Multiply-adds x 2 of both products, over the keys each row sees."""
+        tot = 0
+        for P, C in zip(self.prefixes().tolist(), self.chunks().tolist()):
+            tot += C * P + C * (C + 1) // 2           # sum over rows of visible keys
+        return 4 * self.num_heads * self.head_dim * tot
+
+
+PREFILL_WORKLOADS = {
+    "prefill_llama3_8b": PrefillWorkload(
+        "Llama-3-8B-shaped chunked prefill, 512-token chunks", 8, 32, 8, 128, "bf16",
+        chunk_lens=[512], prefix_range=(0, 3584), seed=1006),
+}
+
+
+@dataclasses.dataclass
+class PrefillBatch:
+    wl: PrefillWorkload
+    q: np.ndarray             # [total_q, Hq, D] storage dtype
+    k_cache: np.ndarray       # [NB, Hkv, bs, D] (the chunk's slots poisoned)
+    v_cache: np.ndarray
+    k_new: np.ndarray         # [total_q, Hkv, D]: the chunk rows to append
+    v_new: np.ndarray
+    slot_mapping: np.ndarray  # [total_q] int64
+    block_table: np.ndarray   # [B, max_blocks] int32 (unused = -1)
+    context_lens: np.ndarray  # [B] int32: prefix + chunk
+    query_start: np.ndarray   # [B + 1] int32
+    num_blocks: int
+
+    @property
+    def max_query_len(self) -> int:
+        d = np.diff(self.query_start)
+        return int(d.max()) if d.size else 0
+
+    @property
+    def total_q(self) -> int:
+        return int(self.query_start[-1])
+
+
+def make_prefill_batch(wl: PrefillWorkload, poison: bool = True) -> PrefillBatch:
+    """Seeded host arrays of one chunked-prefill step: random block tables
+    over a shuffled pool, N(0, 1) q/K/V, NaN in every unused row."""
+    rng = np.random.Generator(np.random.PCG64(wl.seed))
+    B, Hq, Hkv, D, bs = wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
+    chunks, prefixes = wl.chunks(), wl.prefixes()
+    lens = (chunks + prefixes).astype(np.int32)
+    owned = [-(-int(L) // bs) for L in lens]
+    total = sum(owned)
+    NB = max(1, total + int(math.ceil(wl.slack * total)))
+    perm = rng.permutation(NB).astype(np.int32)
+    table = np.full((B, max(1, max(owned) if owned else 1)), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        table[b, :owned[b]] = perm[pos:pos + owned[b]]
+        pos += owned[b]
+    k_cache = _normal_storage(rng, (NB, Hkv, bs, D), wl.dtype)
+    v_cache = _normal_storage(rng, (NB, Hkv, bs, D), wl.dtype)
+    qs = np.zeros(B + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(chunks)
+    q = _normal_storage(rng, (int(qs[-1]), Hq, D), wl.dtype)
+    slots = np.empty(int(qs[-1]), dtype=np.int64)
+    for b in range(B):
+        for j in range(int(chunks[b])):
+            i = int(prefixes[b]) + j
+            slots[qs[b] + j] = int(table[b, i // bs]) * bs + i % bs
+    phys, off = slots // bs, slots % bs
+    k_new = np.ascontiguousarray(k_cache[phys, :, off, :])
+    v_new = np.ascontiguousarray(v_cache[phys, :, off, :])
+    if poison:
+        bad = _poison_value(wl.dtype)
+        used = np.zeros(NB, dtype=bool)
+        used[perm[:total]] = True
+        k_cache[~used] = bad
+        v_cache[~used] = bad
+        for b in range(B):
+            L = int(lens[b])
+            if owned[b] and L % bs:
+                last = int(table[b, owned[b] - 1])
+                k_cache[last, :, L % bs:, :] = bad
+                v_cache[last, :, L % bs:, :] = bad
+        k_cache[phys, :, off, :] = bad
+        v_cache[phys, :, off, :] = bad
+    return PrefillBatch(wl, q, k_cache, v_cache, k_new, v_new, slots, table, lens, qs, NB)
+
+
 def storage_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
     """Exact float64 values of stored elements (for comparing outputs)."""
     if dtype == "f32":
