@@ -363,6 +363,7 @@ PKV_API pkv_status pkv_paged_attention_fp8(
  *   context_lens device int32 [batch]: rows in sequence b's cache, the
  *                chunk's own rows included (L_b >= q_len_b).
  *   Row j of sequence b sees cache rows i <= L_b - q_len_b + j.
+ *   scale: the softmax scale, > 0 (PKV_ERR_INVALID_ARG otherwise).
  *   head_dim 64 or 128; block_size 16; num_heads / num_kv_heads must divide
  *   128.  No workspace: the work is split over query rows (256 per CTA),
  *   not over keys.  options: only `stages` (K/V ring depth; 0 = default) is

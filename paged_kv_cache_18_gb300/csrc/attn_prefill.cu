@@ -14,30 +14,36 @@
 // sum at the end.  Prefill is a dense contraction (many query rows per key),
 // so both products run on the tensor cores.
 //
-// One CTA per 256 query rows of one (sequence, KV head).  A row is a (query
+// One CTA per 256 query rows of one (sequence, KV head), longest first.  A row is a (query
 // position, head of the KV head's group) pair, so each K/V chunk streamed
-// once serves every query head that shares the KV head.  320 threads:
-//   warps 0-3 / 4-7  softmax and epilogue of query tile 0 / 1 (128 rows each,
-//                    one row per thread: TMEM lane = row);
-//   warp 8           TMA producer: the Q tiles, then K and V chunks of 128
-//                    keys (8 blocks through the block table) into a ring of
+// once serves every query head that shares the KV head.  352 threads:
+//   warps 0-3 / 4-7  softmax and epilogue of query tile 0 / 1 (128 rows
+//                    each, one row per thread: TMEM lane = row); the two
+//                    tiles' softmaxes take turns chunk by chunk;
+//   warp 8           TMA producer: the Q tiles, then K and V chunks of 64
+//                    keys (4 blocks through the block table) into a ring of
 //                    NS stages, K and V alternating;
-//   warp 9           MMA issuer (one lane) and TMEM owner.
-// Per 128-key chunk c and tile t:
-//   S_t[128 x 128] = Q_t[128 x D] . K_c^T                  (TMEM, fp32)
+//   warps 9 / 10     MMA issuer of tile 0 / 1 (one lane each); warp 9 owns
+//                    the TMEM allocation.
+// Per 64-key chunk c and tile t:
+//   S[128 x 64] = Q_t[128 x D] . K_c^T    (TMEM, fp32; buffer c & 1 of the
+//                                          tile, so S_{c+1} is computed while
+//                                          the softmax works on S_c)
 //   softmax per row, thread-local: masked scores in log2 units, a lazy
 //   reference max m (raised, with l and O rescaled, only when a score exceeds
-//   it by more than 2^8), P = 2^(s - m) written back over S_t in the 16-bit
-//   input type: for bf16 as a high part (columns 0..63) and the remainder
-//   P - high (columns 64..127), since one bf16 rounding of P alone costs
-//   about 1.6e-3 of relative L2 error, as much as the output's own rounding;
-//   f16 (11 significant bits) needs no remainder
-//   O_t[128 x D]  += P_t[128 x 128] . V_c[128 x D]         (A read from TMEM;
-//                    bf16: a second product with the remainder)
-// The issuer interleaves the tiles (P.V of tile 0 then the next S of tile 0,
-// then the same for tile 1), so one tile's MMAs run while the other's softmax
-// does.  TMEM: S_0, S_1 (128 columns each) and O_0, O_1 (D columns each),
-// 512 columns: one CTA per SM.
+//   it by more than 2^8), P = 2^(s - m) written back over the S buffer in the
+//   16-bit input type, each 32-key group over its own 32 columns: for bf16 a
+//   high part (16 columns) and the remainder P - high (16), since one bf16
+//   rounding of P alone costs about 1.6e-3 of relative L2 error, as much as
+//   the output's own rounding; f16 (11 significant bits) needs no remainder
+//   O_t[128 x D] += P[128 x 64] . V_c[64 x D]   (A read from TMEM; bf16: a
+//                                               second product with the
+//                                               remainder)
+// TMEM: two S buffers of 64 columns and O (D columns) per tile, 512 columns:
+// one CTA per SM.  (64-key chunks keep two S buffers per tile within TMEM:
+// with one, each tile's softmax would wait for its own P.V and next S.)
+// While one tile's softmax runs, the tensor cores run the other tile's P.V
+// and next S: the two tiles' work interleaves.
 // Operands: Q and K K-major with the 128-byte swizzle (as the TMA writes
 // them), V MN-major with the 128-byte swizzle (its own layout), P from TMEM.
 // Keys past the context or in a bad block never reach an MMA as NaN: their
@@ -55,23 +61,29 @@ namespace prefill {
 constexpr int kTileRows = 128;                     // query rows per MMA tile (M)
 constexpr int kTiles = 2;                          // tiles per CTA
 constexpr int kCtaRows = kTiles * kTileRows;
-constexpr int kChunkKeys = 128;                    // keys per chunk
+constexpr int kChunkKeys = 64;                     // keys per chunk (N of S)
 constexpr int kChunkBlocks = kChunkKeys / kBlockSize;
-constexpr int kSoftmaxWarps = 4 * kTiles;
+constexpr int kSoftmaxWarps = 4 * kTiles;          // one per TMEM lane quadrant per tile
 constexpr int kProducerWarp = kSoftmaxWarps;
-constexpr int kIssuerWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kIssuerWarp = kSoftmaxWarps + 1;     // tile t's MMAs: warp kIssuerWarp + t
+constexpr int kThreads = (kSoftmaxWarps + 1 + kTiles) * 32;
 constexpr float kRescaleSlack = 8.f;
+// Named barrier kTurnBar + t: tile t's softmax hands over to the other tile's.
+constexpr int kTurnBar = 1;
 
 template <int D, int NS> struct Geom {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
-  static constexpr int kPanels = D / 64;                      // 128-byte column panels
-  static constexpr int kPanelBytes = 128 * 128;               // 128 rows x 128 B
-  static constexpr int kStageBytes = kPanels * kPanelBytes;   // a Q tile, or one K / V chunk
-  static constexpr int kRingOff = kTiles * kStageBytes;
+  static constexpr int kPanels = D / 64;                        // 128-byte column panels
+  static constexpr int kQPanelBytes = kTileRows * 128;          // 128 rows x 128 B
+  static constexpr int kQBytes = kPanels * kQPanelBytes;        // one Q tile
+  static constexpr int kKVPanelBytes = kChunkKeys * 128;        // 64 rows x 128 B
+  static constexpr int kStageBytes = kPanels * kKVPanelBytes;   // one K or V chunk
+  static constexpr int kRingOff = kTiles * kQBytes;
   static constexpr int kBytes = kRingOff + NS * kStageBytes;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kOCol = kTiles * kChunkKeys;           // O_t at kOCol + D t
+  // tile t: S (and P over it) of chunk c at column 128 t + 64 (c & 1);
+  // O_t at kOCol + D t
+  static constexpr int kOCol = kTiles * 2 * kChunkKeys;
   static_assert(kOCol + kTiles * D <= 512, "TMEM columns");
 };
 
@@ -93,38 +105,144 @@ struct Work {
   int b, kvh, row0;   // rows row0 .. row0 + rows - 1 of the sequence's (position, head) rows
   int rows, q0, qlen, L;
   int tiles;          // 1 or 2
-  int chunks[kTiles]; // 128-key chunks each tile reads
+  int chunks0, chunks1;  // 64-key chunks tile 0 / tile 1 reads
   int nblk;           // cache blocks the CTA reads
+  __device__ __forceinline__ int chunks(int t) const { return t == 0 ? chunks0 : chunks1; }
 };
+
+// A sequence's extent: its chunk rows, cached rows and CTA row pairs (256
+// (position, head) rows each); a sequence whose query_start / context_lens
+// break the rules has no pairs.
+struct SeqShape {
+  int q0, qlen, L, pairs;
+};
+__device__ __forceinline__ SeqShape seq_shape(const PrefillParams &p, int b) {
+  SeqShape q;
+  const int q0 = __ldg(p.query_start + b), q1 = __ldg(p.query_start + b + 1);
+  q.L = __ldg(p.context_lens + b);
+  q.q0 = q0;
+  const bool sane = q0 >= 0 && q1 >= q0 && q1 <= p.total_q && q1 - q0 <= p.max_query_len &&
+                    q.L >= q1 - q0 &&
+                    static_cast<int64_t>(q.L) <=
+                        static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize;
+  q.qlen = sane ? q1 - q0 : 0;
+  q.pairs = (q.qlen * p.group + kCtaRows - 1) / kCtaRows;
+  return q;
+}
+// Chunks the CTA of row pair `pair` runs (those of its last row): the cost
+// that orders the work.  Non-decreasing in `pair`.
+__device__ __forceinline__ int pair_cost(const SeqShape &q, int group, int pair) {
+  const int last = min(pair * kCtaRows + kCtaRows, q.qlen * group) - 1;
+  return (q.L - q.qlen + last / group) / kChunkKeys + 1;
+}
+// First pair of the sequence whose cost is at least v (q.pairs if none).
+__device__ __forceinline__ int first_pair_at_least(const SeqShape &q, int group, int v) {
+  int lo = 0, hi = q.pairs;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (pair_cost(q, group, mid) >= v)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  return lo;
+}
+
+// CTAs take the (sequence, row pair) units longest first: the hardware starts
+// CTAs in index order as SMs free up, so this is a longest-first list
+// schedule (the costs differ by up to the ratio of the longest context to
+// the shortest).  Unit rank r (descending cost; ties by sequence, then pair)
+// is found by each warp on its own: a binary search over the cost value of
+// the count of units at or above it (per sequence a binary search over its
+// pairs), then a walk over the sequences within that cost.  Returns
+// false when rank r has no unit.
+__device__ __forceinline__ bool locate_unit(const PrefillParams &p, int r, int *b_out,
+                                            int *pair_out) {
+  const int lane = threadIdx.x & 31;
+  auto count_ge = [&](int v) {
+    int n = 0;
+    for (int b = lane; b < p.batch; b += 32) {
+      const SeqShape q = seq_shape(p, b);
+      n += q.pairs - first_pair_at_least(q, p.group, v);
+    }
+    return __reduce_add_sync(kFull, n);
+  };
+  int vmax = 0;
+  for (int b = lane; b < p.batch; b += 32) {
+    const SeqShape q = seq_shape(p, b);
+    if (q.pairs > 0) vmax = max(vmax, pair_cost(q, p.group, q.pairs - 1));
+  }
+  vmax = __reduce_max_sync(kFull, vmax);
+  if (vmax == 0 || count_ge(1) <= r) return false;
+  int lo = 1, hi = vmax;  // the largest v with count_ge(v) > r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (count_ge(mid) > r)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  int skip = r - (lo < vmax ? count_ge(lo + 1) : 0);  // units of cost lo before rank r
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int f = 0, m = 0;
+    if (b < p.batch) {
+      const SeqShape q = seq_shape(p, b);
+      f = first_pair_at_least(q, p.group, lo);
+      m = first_pair_at_least(q, p.group, lo + 1) - f;
+    }
+    int incl = m;  // inclusive prefix sum over the lanes
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, d);
+      if (lane >= d) incl += y;
+    }
+    const int total = __shfl_sync(kFull, incl, 31);
+    if (skip < total) {
+      const int src = __ffs(__ballot_sync(kFull, incl > skip)) - 1;
+      const int before = __shfl_sync(kFull, incl - m, src);
+      *b_out = b0 + src;
+      *pair_out = __shfl_sync(kFull, f, src) + (skip - before);
+      return true;
+    }
+    skip -= total;
+  }
+  return false;  // (not reached when the counts agree)
+}
 
 __device__ __forceinline__ Work make_work(const PrefillParams &p) {
   Work w;
-  w.kvh = blockIdx.x;
-  w.b = blockIdx.y;
-  // the sequence's last rows (the most keys) are launched first
-  w.row0 = (p.pairs - 1 - static_cast<int>(blockIdx.z)) * kCtaRows;
-  const int q0 = __ldg(p.query_start + w.b), q1 = __ldg(p.query_start + w.b + 1);
-  const int L = __ldg(p.context_lens + w.b);
-  const bool sane = q0 >= 0 && q1 >= q0 && q1 <= p.total_q && q1 - q0 <= p.max_query_len &&
-                    L >= q1 - q0 &&
-                    static_cast<int64_t>(L) <=
-                        static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize;
-  if (!sane && blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
-    record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
-  w.q0 = q0;
-  w.qlen = sane ? q1 - q0 : 0;
-  w.L = L;
+  w.kvh = static_cast<int>(blockIdx.x % p.num_kv_heads);
+  int pair = 0;
+  if (!locate_unit(p, static_cast<int>(blockIdx.x / p.num_kv_heads), &w.b, &pair)) {
+    w.rows = 0;
+    return w;
+  }
+  const SeqShape q = seq_shape(p, w.b);
+  w.q0 = q.q0;
+  w.qlen = q.qlen;
+  w.L = q.L;
+  w.row0 = pair * kCtaRows;
   w.rows = min(kCtaRows, w.qlen * p.group - w.row0);
   w.tiles = w.rows > kTileRows ? 2 : 1;
-  int lim = 0;
-#pragma unroll
-  for (int t = 0; t < kTiles; ++t) {
-    const int last = w.row0 + min(t * kTileRows + kTileRows, w.rows) - 1;
-    lim = w.L - w.qlen + last / p.group;  // the last key tile t's rows see
-    w.chunks[t] = t < w.tiles ? lim / kChunkKeys + 1 : 0;
-    if (t == w.tiles - 1) w.nblk = lim / kBlockSize + 1;
-  }
+  // the last key each tile's rows see
+  const int lim0 = w.L - w.qlen + (w.row0 + min(kTileRows, w.rows) - 1) / p.group;
+  const int lim1 = w.L - w.qlen + (w.row0 + w.rows - 1) / p.group;
+  w.chunks0 = lim0 / kChunkKeys + 1;
+  w.chunks1 = w.tiles == 2 ? lim1 / kChunkKeys + 1 : 0;
+  w.nblk = (w.tiles == 2 ? lim1 : lim0) / kBlockSize + 1;
   return w;
+}
+
+// Sequences that break the rules are recorded once (by the first CTA).
+__device__ __forceinline__ void check_sequences(const PrefillParams &p) {
+  if (blockIdx.x != 0 || threadIdx.x >= 32) return;
+  bool bad = false;
+  for (int b = threadIdx.x; b < p.batch; b += 32) {
+    const int q0 = __ldg(p.query_start + b), q1 = __ldg(p.query_start + b + 1);
+    bad |= seq_shape(p, b).qlen == 0 && q1 != q0;
+  }
+  if (__any_sync(kFull, bad) && threadIdx.x == 0) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
 }
 
 template <typename T, int D, int NS>
@@ -133,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using G = Geom<D, NS>;
+  check_sequences(p);
   const Work w = make_work(p);
   if (w.rows <= 0) return;  // the whole CTA, before any barrier or TMEM use
 
@@ -140,8 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  __shared__ uint64_t full[NS], empty[NS], q_full, landed, s_full[kTiles], p_full[kTiles],
-      pv_done[kTiles], mma_idle;
+  // per tile and S buffer u (chunk c uses u = c & 1)
+  __shared__ uint64_t full[NS], empty[NS], q_full, landed, s_full[kTiles][2], p_full[kTiles][2],
+      pv_done[kTiles][2], mma_idle[kTiles];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int s_abort;
 
@@ -150,15 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kTiles);  // one release per tile's issuer
     }
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&landed), 1);
-    mbar_init(smem_u32(&mma_idle), 1);
     for (int t = 0; t < kTiles; ++t) {
-      mbar_init(smem_u32(&s_full[t]), 1);
-      mbar_init(smem_u32(&p_full[t]), 4);
-      mbar_init(smem_u32(&pv_done[t]), 1);
+      mbar_init(smem_u32(&mma_idle[t]), 1);
+      for (int u = 0; u < 2; ++u) {
+        mbar_init(smem_u32(&s_full[t][u]), 1);
+        mbar_init(smem_u32(&p_full[t][u]), 4);
+        mbar_init(smem_u32(&pv_done[t][u]), 1);
+      }
     }
     fence_mbar_init();
   }
@@ -168,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tmem = tmem_base_s;
   const int32_t *table = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks_per_seq;
-  const int n_chunks = w.chunks[w.tiles - 1];
+  const int n_chunks = w.chunks(w.tiles - 1);
   auto abort_all = [&]() {
     s_abort = 1;
     record_error(p.err, PKV_DEVERR_TIMEOUT);
@@ -179,13 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int issued = 0;
     uint32_t nfix = 0;
-    if (lane == 0) mbar_arrive_expect_tx(smem_u32(&q_full), w.tiles * G::kStageBytes);
+    if (lane == 0) mbar_arrive_expect_tx(smem_u32(&q_full), w.tiles * G::kQBytes);
     __syncwarp();
     if (lane < w.tiles * G::kPanels) {
       // a Q tile: 128 / group positions x the group's heads, one 128-byte
       // panel per box; rows past the query tensor read as zero
       const int t = lane / G::kPanels, pn = lane % G::kPanels;
-      tma_load_3d(sbase + t * G::kStageBytes + pn * G::kPanelBytes, &qmap, smem_u32(&q_full),
+      tma_load_3d(sbase + t * G::kQBytes + pn * G::kQPanelBytes, &qmap, smem_u32(&q_full),
                   pn * 64, w.kvh * p.group, w.q0 + (w.row0 + t * kTileRows) / p.group);
     }
     for (int c = 0; c < n_chunks && ok; ++c) {
@@ -217,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < nb && !bad) {
 #pragma unroll
           for (int pn = 0; pn < G::kPanels; ++pn)
-            tma_load_4d(dst + pn * G::kPanelBytes + lane * kBlockSize * 128, kv ? &vmap : &kmap,
-                        bar, pn * 64, 0, w.kvh, entry);
+            tma_load_4d(dst + pn * G::kKVPanelBytes + lane * kBlockSize * 128,
+                        kv ? &vmap : &kmap, bar, pn * 64, 0, w.kvh, entry);
         }
         issued = idx + 1;
         if (fix) {
@@ -232,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = lane; e < kChunkKeys * G::kPanels * 8; e += 32) {
             const int row = e / (G::kPanels * 8), pn = (e / 8) % G::kPanels, piece = e % 8;
             if (row >= zfrom || ((bad_mask >> (row / kBlockSize)) & 1u))
-              tc::st_shared_v4(dst + pn * G::kPanelBytes + row * 128 + piece * 16, 0u, 0u, 0u, 0u);
+              tc::st_shared_v4(dst + pn * G::kKVPanelBytes + row * 128 + piece * 16, 0u, 0u, 0u,
+                               0u);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
@@ -249,85 +372,116 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, issued - NS); i < issued; ++i)
         mbar_wait_bounded(smem_u32(&full[i % NS]), (i / NS) & 1);
     }
-  } else if (warp == kIssuerWarp) {
-    // ---- MMA issuer ---------------------------------------------------------------
+  } else if (warp >= kIssuerWarp) {
+    // ---- MMA issuers: one thread per tile ----------------------------------------
+    // Chunk c: S_c into the tile's buffer c & 1 (two chunks ahead, so S_{c+1}
+    // is there when the softmax finishes chunk c), then P_c . V_c once the
+    // softmax has written P_c over S_c.  Each tile has its own issuing thread,
+    // so one tile's waits never hold up the other's MMAs; every K / V stage is
+    // released by both (a tile that is done, or absent, releases the stages
+    // it no longer reads as they arrive).  The issuers poll their barriers
+    // (no suspension): their wake-up is on the critical path.
+    const int t = warp - kIssuerWarp;
     if (lane == 0) {
       const uint32_t id_s = tc::instr_desc<T>(kTileRows, kChunkKeys, 0, 0);
       const uint32_t id_o = tc::instr_desc<T>(kTileRows, D, 0, 1);
       // descriptors differ only in their start address (bits 0..13: addr >> 4)
       const uint64_t dk = tc::smem_desc(0, 16, 1024, tc::kSwizzle128);
-      const uint64_t dv = tc::smem_desc(0, G::kPanelBytes, 1024, tc::kSwizzle128);
+      const uint64_t dv = tc::smem_desc(0, G::kKVPanelBytes, 1024, tc::kSwizzle128);
+      const int mine = t < w.tiles ? w.chunks(t) : 0;
       auto ring = [&](int idx) { return sbase + G::kRingOff + (idx % NS) * G::kStageBytes; };
-      auto issue_s = [&](int c, int t) {
-        const uint32_t qa = sbase + t * G::kStageBytes, ka = ring(2 * c);
+      auto sbuf = [&](int c) { return tmem + t * 2 * kChunkKeys + (c & 1) * kChunkKeys; };
+      auto issue_s = [&](int c) {
+        const uint32_t qa = sbase + t * G::kQBytes, ka = ring(2 * c);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * G::kPanelBytes + (ks & 3) * 32;
-          tc::mma(tmem + t * kChunkKeys, dk | ((qa + off) >> 4), dk | ((ka + off) >> 4), id_s,
-                  ks > 0);
+          const uint32_t offq = (ks >> 2) * G::kQPanelBytes + (ks & 3) * 32;
+          const uint32_t offk = (ks >> 2) * G::kKVPanelBytes + (ks & 3) * 32;
+          tc::mma(sbuf(c), dk | ((qa + offq) >> 4), dk | ((ka + offk) >> 4), id_s, ks > 0);
         }
-        tc::commit(smem_u32(&s_full[t]));
+        tc::commit(smem_u32(&s_full[t][c & 1]));
       };
-      auto issue_o = [&](int c, int t) {
+      auto issue_o = [&](int c) {
         const uint32_t va = ring(2 * c + 1);
 #pragma unroll
         for (int ks = 0; ks < kChunkKeys / 16; ++ks) {
+          // keys 16 ks .. 16 ks + 15: P columns of 32-key group ks / 2
           const uint64_t vb = dv | ((va + ks * 16 * 128) >> 4);
-          tc::mma_ts(tmem + G::kOCol + t * D, tmem + t * kChunkKeys + ks * 8, vb, id_o,
-                     c > 0 || ks > 0);
-          if constexpr (kSplitP<T>)
-            tc::mma_ts(tmem + G::kOCol + t * D, tmem + t * kChunkKeys + 64 + ks * 8, vb, id_o,
-                       true);
+          const uint32_t pc = sbuf(c) + 32 * (ks >> 1) + 8 * (ks & 1);
+          tc::mma_ts(tmem + G::kOCol + t * D, pc, vb, id_o, c > 0 || ks > 0);
+          if constexpr (kSplitP<T>) tc::mma_ts(tmem + G::kOCol + t * D, pc + 16, vb, id_o, true);
         }
-        tc::commit(smem_u32(&pv_done[t]));
+        tc::commit(smem_u32(&pv_done[t][c & 1]));
       };
-      auto full_wait = [&](int idx) {
-        return mbar_wait_bounded(smem_u32(&full[idx % NS]), (idx / NS) & 1);
+      auto spin = [&](uint64_t &bar, uint32_t parity) {
+        return tc::mbar_spin_bounded(smem_u32(&bar), parity);
       };
-      bool ok = mbar_wait_bounded(smem_u32(&q_full), 0) && full_wait(0);
-      if (ok) {
-        tc::fence_after();
-        for (int t = 0; t < w.tiles; ++t) issue_s(0, t);
-        tc::commit(smem_u32(&empty[0]));
+      auto full_wait = [&](int idx) { return spin(full[idx % NS], (idx / NS) & 1); };
+      // release a stage: when this thread's MMAs reading it complete, or now
+      auto release = [&](int idx, bool read) {
+        if (read)
+          tc::commit(smem_u32(&empty[idx % NS]));
+        else
+          tc::mbar_arrive(smem_u32(&empty[idx % NS]));
+      };
+      bool ok = spin(q_full, 0);
+      for (int c = 0; ok && c < 2 && c < n_chunks; ++c) {
+        if (!full_wait(2 * c)) {
+          ok = false;
+          break;
+        }
+        if (c < mine) {
+          tc::fence_after();
+          issue_s(c);
+        }
+        release(2 * c, c < mine);
       }
       for (int c = 0; ok && c < n_chunks; ++c) {
         if (!full_wait(2 * c + 1)) {
           ok = false;
           break;
         }
-        bool next_k = false;
-        for (int t = 0; t < w.tiles && ok; ++t) {
-          if (c >= w.chunks[t]) continue;
-          if (!mbar_wait_bounded(smem_u32(&p_full[t]), c & 1)) {
+        if (c < mine) {
+          if (!spin(p_full[t][c & 1], (c >> 1) & 1)) {
             ok = false;
             break;
           }
           tc::fence_after();
-          issue_o(c, t);
-          if (c + 1 < w.chunks[t]) {
-            // S_{c+1} overwrites the columns P_c is read from: after P.V
-            if ((!next_k && !full_wait(2 * c + 2)) ||
-                !mbar_wait_bounded(smem_u32(&pv_done[t]), c & 1)) {
+          issue_o(c);
+        }
+        release(2 * c + 1, c < mine);
+        if (c + 2 < n_chunks) {
+          if (!full_wait(2 * c + 4)) {
+            ok = false;
+            break;
+          }
+          if (c + 2 < mine) {
+            // S_{c+2} overwrites the buffer P_c is read from: after P_c . V_c
+            if (!spin(pv_done[t][c & 1], (c >> 1) & 1)) {
               ok = false;
               break;
             }
-            next_k = true;
             tc::fence_after();
-            issue_s(c + 1, t);
+            issue_s(c + 2);
           }
+          release(2 * c + 4, c + 2 < mine);
         }
-        if (!ok) break;
-        tc::commit(smem_u32(&empty[(2 * c + 1) % NS]));
-        if (next_k) tc::commit(smem_u32(&empty[(2 * c + 2) % NS]));
       }
       if (!ok) abort_all();
-      // every MMA issued has completed before TMEM is released
-      tc::commit(smem_u32(&mma_idle));
-      mbar_wait_bounded(smem_u32(&mma_idle), 0);
+      // every MMA this thread issued has completed before TMEM is released
+      tc::commit(smem_u32(&mma_idle[t]));
+      spin(mma_idle[t], 0);
     }
     __syncwarp();
   } else {
     // ---- softmax and epilogue: one query row per thread ----------------------------
+    // Warp w: tile t = w / 4, TMEM lane quadrant w % 4.  The two tiles'
+    // softmaxes take turns (tile 0's chunk c, tile 1's chunk c, tile 0's
+    // chunk c + 1, ...), so each has the SM's issue slots and exp2 units to
+    // itself while the tensor cores work on the other tile.  The hand-over is
+    // a pair of named barriers (one tile's 128 threads arrive, the other's
+    // wait); a warp that has given up keeps executing the same sequence of
+    // them, so no warp is ever left waiting at one.
     const int t = warp / 4, quad = warp % 4;
     if (t < w.tiles) {
       const int r = w.row0 + t * kTileRows + quad * 32 + lane;
@@ -335,98 +489,133 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = r / p.group, h = r - j * p.group;
       const int lim = valid ? w.L - w.qlen + j : -1;  // the last key this row sees
       const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-      const uint32_t s_addr = tmem + lane_base + t * kChunkKeys;
       const uint32_t o_addr = tmem + lane_base + G::kOCol + t * D;
-      const int nch = w.chunks[t];
+      const int nch = w.chunks(t);
+      const bool turns = w.tiles == 2;
+      const int n_other = turns ? w.chunks(1 - t) : 0;
+      auto turn_wait = [&](int c) {  // before chunk c: the other tile's turn is over
+        const int oc = t == 0 ? c - 1 : c;
+        if (turns && oc >= 0 && oc < n_other)
+          asm volatile("bar.sync %0, 256;" ::"r"(kTurnBar + (1 - t)) : "memory");
+      };
+      auto turn_pass = [&](int c) {  // after chunk c: the other tile may go
+        const int oc = t == 0 ? c : c + 1;  // its chunk that waits for this one
+        if (turns && oc < n_other)
+          asm volatile("bar.arrive %0, 256;" ::"r"(kTurnBar + t) : "memory");
+      };
+      const float sl = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int c = 0; c < nch; ++c) {
-        const int nb = min(kChunkBlocks, w.nblk - c * kChunkBlocks);
-        const int entry = lane < nb ? __ldg(table + c * kChunkBlocks + lane) : 0;
-        const uint32_t bad_mask = __ballot_sync(
-            kFull, lane < nb && (entry < 0 || static_cast<int64_t>(entry) >= p.num_blocks));
-        const bool wt = mbar_wait_bounded(smem_u32(&s_full[t]), c & 1);
-        if (!__all_sync(kFull, wt && !s_abort)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
-        uint32_t sr[kChunkKeys / 32][32];
-#pragma unroll
-        for (int q = 0; q < kChunkKeys / 32; ++q) tc::tmem_ld32(s_addr + 32 * q, sr[q]);
-        tc::tmem_wait_ld();
+        const uint32_t s_addr = tmem + lane_base + t * 2 * kChunkKeys + (c & 1) * kChunkKeys;
         const int key0 = c * kChunkKeys;
-        const bool need_mask = key0 + kChunkKeys - 1 > lim || bad_mask != 0;
-        float mc = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < kChunkKeys; ++k) {
-          float x = __uint_as_float(sr[k / 32][k % 32]) * p.scale_log2;
-          if (need_mask && (key0 + k > lim || ((bad_mask >> (k / kBlockSize)) & 1u)))
-            x = -INFINITY;
-          sr[k / 32][k % 32] = __float_as_uint(x);
-          mc = fmaxf(mc, x);
+        uint32_t va[32], vb[32];
+        uint32_t bad_mask = 0;
+        if (ok) {
+          const int nb = min(kChunkBlocks, w.nblk - c * kChunkBlocks);
+          const int entry = lane < nb ? __ldg(table + c * kChunkBlocks + lane) : 0;
+          bad_mask = __ballot_sync(
+              kFull, lane < nb && (entry < 0 || static_cast<int64_t>(entry) >= p.num_blocks));
+          const bool wt = mbar_wait_bounded(smem_u32(&s_full[t][c & 1]), (c >> 1) & 1);
+          ok = __all_sync(kFull, wt && !s_abort);
+          if (ok) {
+            tc::fence_after();
+            tc::tmem_ld32(s_addr, va);  // in flight across the turn wait
+            tc::tmem_ld32(s_addr + 32, vb);
+          }
         }
+        turn_wait(c);
+        if (!ok) {
+          turn_pass(c);
+          continue;
+        }
+        tc::tmem_wait_ld_regs(va);
+        tc::tmem_wait_ld_regs(vb);
+        // keys this row may not see (past its last key, or in a bad block):
+        // score -inf
+        auto mask32 = [&](uint32_t(&v)[32], int g) {
+          if (key0 + 32 * g + 31 > lim || ((bad_mask >> (2 * g)) & 3u) != 0) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int k = 32 * g + e;
+              if (key0 + k > lim || ((bad_mask >> (k / kBlockSize)) & 1u))
+                v[e] = __float_as_uint(-INFINITY);
+            }
+          }
+        };
+        mask32(va, 0);
+        mask32(vb, 1);
+        // the chunk's largest raw score (the scale is positive, so scaling
+        // after the maximum is the same)
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          mx[0] = fmaxf(mx[0], __uint_as_float(va[e]));
+          mx[1] = fmaxf(mx[1], __uint_as_float(va[e + 1]));
+          mx[2] = fmaxf(mx[2], __uint_as_float(vb[e]));
+          mx[3] = fmaxf(mx[3], __uint_as_float(vb[e + 1]));
+        }
+        const float mc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
         const bool raise = mc > m_ref + kRescaleSlack;
         const float m_new = raise ? mc : m_ref;
         const float alpha = !raise ? 1.f : (m_ref == -INFINITY ? 0.f : ex2(m_ref - m_new));
         l *= alpha;
         if (c > 0 && __any_sync(kFull, raise)) {
-          // P.V of chunk c - 1 has completed: S_c was computed after it
+          // O holds P_{c-1} . V_{c-1} once that product has completed
+          const bool pw =
+              mbar_wait_bounded(smem_u32(&pv_done[t][(c - 1) & 1]), ((c - 1) >> 1) & 1);
+          if (!__all_sync(kFull, pw && !s_abort)) {
+            ok = false;
+            turn_pass(c);
+            continue;
+          }
+          tc::fence_after();
 #pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
             tc::tmem_ld32(o_addr + 32 * q, o);
-            tc::tmem_wait_ld();
+            tc::tmem_wait_ld_regs(o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             tc::tmem_st32(o_addr + 32 * q, o);
           }
         }
         m_ref = m_new;
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        float rs = 0.f;
-        if constexpr (kSplitP<T>) {
-          // the 64 columns of P's high part, then the 64 of its remainder
-          // (S_t has been read in full into registers)
+        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+        // P = 2^(s scale_log2 - m) written over each 32-key group's own S
+        // columns: the high part in its first 16, the remainder in the other
+        // 16 (f16: P alone in the first 16)
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t hi[32], lo[32];
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t(&v)[32] = g ? vb : va;
+          uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int k = 64 * q + 2 * e;
-              const float a = ex2(__uint_as_float(sr[k / 32][k % 32]) - m_use);
-              const float b = ex2(__uint_as_float(sr[k / 32][k % 32 + 1]) - m_use);
-              rs += a + b;
-              const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-              hi[e] = *reinterpret_cast<const uint32_t *>(&h);
-              lo[e] = pack2<T>(a - __low2float(h), b - __high2float(h));
+          for (int e = 0; e < 16; ++e) {
+            const float x = ex2(fmaf(__uint_as_float(v[2 * e]), sl, neg_m));
+            const float y = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sl, neg_m));
+            rs[e & 3] += x + y;
+            if constexpr (kSplitP<T>) {
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
+              hi[e] = *reinterpret_cast<const uint32_t *>(&hv);
+              lo[e] = pack2<T>(x - __low2float(hv), y - __high2float(hv));
+            } else {
+              hi[e] = pack2<T>(x, y);
             }
-            tc::tmem_st32(s_addr + 32 * q, hi);
-            tc::tmem_st32(s_addr + 64 + 32 * q, lo);
           }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int k = 64 * q + 2 * e;
-              const float a = ex2(__uint_as_float(sr[k / 32][k % 32]) - m_use);
-              const float b = ex2(__uint_as_float(sr[k / 32][k % 32 + 1]) - m_use);
-              rs += a + b;
-              pk[e] = pack2<T>(a, b);
-            }
-            tc::tmem_st32(s_addr + 32 * q, pk);
-          }
+          tc::tmem_st16u(s_addr + 32 * g, hi);
+          if constexpr (kSplitP<T>) tc::tmem_st16u(s_addr + 32 * g + 16, lo);
         }
-        l += rs;
+        l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         tc::tmem_wait_st();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(smem_u32(&p_full[t]));
+        if (lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c & 1]));
+        turn_pass(c);
       }
       if (ok) {
-        const bool wt = mbar_wait_bounded(smem_u32(&pv_done[t]), (nch - 1) & 1);
+        const bool wt =
+            mbar_wait_bounded(smem_u32(&pv_done[t][(nch - 1) & 1]), ((nch - 1) >> 1) & 1);
         ok = __all_sync(kFull, wt && !s_abort);
       }
       if (ok) {
@@ -438,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < D / 32; ++q) {
           uint32_t o[32];
           tc::tmem_ld32(o_addr + 32 * q, o);
-          tc::tmem_wait_ld();
+          tc::tmem_wait_ld_regs(o);
           if (valid) {
             uint32_t pk[16];
 #pragma unroll
@@ -464,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---- host side -----------------------------------------------------------------
-constexpr int kDefaultStages128 = 4, kDefaultStages64 = 8;
+constexpr int kDefaultStages128 = 8, kDefaultStages64 = 12;
 
 template <typename T, int D, int NS>
 cudaError_t launch_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
@@ -474,7 +663,8 @@ cudaError_t launch_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUt
   const cudaError_t e = cudaFuncSetAttribute(
       prefill_kernel<T, D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const dim3 grid(p.num_kv_heads, p.batch, p.pairs);
+  // one CTA per (sequence, row pair, KV head) unit, longest units first
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.pairs) * p.batch * p.num_kv_heads));
   prefill_kernel<T, D, NS><<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
@@ -485,17 +675,17 @@ using LaunchFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const
 template <typename T> LaunchFn pick_t(int D, int stages) {
   if (D == 128) {
     switch (stages == 0 ? kDefaultStages128 : stages) {
-      case 3: return launch_t<T, 128, 3>;
       case 4: return launch_t<T, 128, 4>;
-      case 5: return launch_t<T, 128, 5>;
+      case 6: return launch_t<T, 128, 6>;
+      case 8: return launch_t<T, 128, 8>;
       default: return nullptr;
     }
   }
   if (D == 64) {
     switch (stages == 0 ? kDefaultStages64 : stages) {
-      case 4: return launch_t<T, 64, 4>;
-      case 6: return launch_t<T, 64, 6>;
       case 8: return launch_t<T, 64, 8>;
+      case 12: return launch_t<T, 64, 12>;
+      case 16: return launch_t<T, 64, 16>;
       default: return nullptr;
     }
   }

@@ -580,12 +580,11 @@ pkv_status pkv_paged_prefill_attention(void *out, const void *q, const void *k_c
   if (batch == 0 || total_q == 0 || max_query_len == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens || !query_start)
     return PKV_ERR_INVALID_ARG;
-  if (num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale) || batch > 65535 ||
-      num_kv_heads > 65535)
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || !(scale > 0.f) || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
   const int64_t rows = static_cast<int64_t>(max_query_len) * group;
   const int64_t pairs = (rows + prefill_rows_per_cta() - 1) / prefill_rows_per_cta();
-  if (pairs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (pairs * batch * num_kv_heads > 0x7fffffff) return PKV_ERR_UNSUPPORTED;  // one CTA each
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(block_table, 4) || !aligned(context_lens, 4) || !aligned(query_start, 4) ||
       (error_word && !aligned(error_word, 4)))

@@ -102,7 +102,7 @@ def test_prefill_after_a_cached_prefix(prefix):
     check(W.make_prefill_batch(wl), rows_per_seq=512, what=f"prefix {prefix}")
 
 
-@pytest.mark.parametrize("D,stages", [(128, 3), (128, 4), (128, 5), (64, 4), (64, 6), (64, 8)])
+@pytest.mark.parametrize("D,stages", [(128, 4), (128, 6), (128, 8), (64, 8), (64, 12), (64, 16)])
 def test_prefill_ring_depths(D, stages):
     wl = W.PrefillWorkload("stages", 3, 8, 2, D, "bf16", chunk_lens=[64, 300, 513],
                            prefix_lens=[700, 0, 260], seed=14)
@@ -199,6 +199,12 @@ def test_prefill_rejects_what_it_does_not_run():
     d = DevicePrefill(W.make_prefill_batch(wl))   # group 3 does not divide 128
     with pytest.raises(binding.PkvError):
         pkv.paged_prefill_attention(d.q, d.k, d.v, d.table, d.lens, d.qs, max_query_len=8)
+    wl = W.PrefillWorkload("rej", 1, 8, 2, 128, "bf16", chunk_lens=[8], prefix_lens=[0])
+    d = DevicePrefill(W.make_prefill_batch(wl))   # the scale must be positive
+    for bad in (0.0, -0.1):
+        with pytest.raises(binding.PkvError):
+            pkv.paged_prefill_attention(d.q, d.k, d.v, d.table, d.lens, d.qs, max_query_len=8,
+                                        scale=bad)
     wl = W.PrefillWorkload("rej", 1, 8, 2, 256, "bf16", chunk_lens=[8], prefix_lens=[0])
     d = DevicePrefill(W.make_prefill_batch(wl))   # head_dim 256
     with pytest.raises(binding.PkvError):
