@@ -15,6 +15,10 @@ from pinned host memory and the output read back every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the float64 CPU oracle, timed
+
+`--workload prefill_llama3_8b` times the chunked-prefill step instead
+(kv_append of each sequence's 512 chunk rows, then paged_prefill_attention):
+its `value` is attention TFLOP/s against the bf16 tensor peak.
 """
 from __future__ import annotations
 
@@ -39,9 +43,11 @@ from paged_kv_cache_18_gb300 import accounting  # noqa: E402
 from paged_kv_cache_18_gb300 import workloads as W  # noqa: E402
 
 METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); decode tokens/sec"
+PREFILL_METRIC = "chunked-prefill attention TFLOP/s (% of GB300 bf16 tensor peak)"
 # Tensor scales of the FP8 cache runs: N(0,1) values land well inside +-448.
 FP8_K_SCALE, FP8_V_SCALE = 0.0123, 0.0171
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 # Sources whose change invalidates a recorded ncu traffic figure.
 KERNEL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mma.cuh",
@@ -51,9 +57,14 @@ KERNEL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mma.cuh",
 
 
 # ---------------------------------------------------------------- helpers --
-def kernel_source_hash() -> str:
+PREFILL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_prefill.cu",
+                   "paged_kv_cache_18_gb300/csrc/tc_ptx.cuh",
+                   "paged_kv_cache_18_gb300/csrc/pkv_device.cuh"]
+
+
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -67,7 +78,7 @@ def measured_peaks():
     return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, sources=None):
     """DRAM bytes per launch (read + write) from the committed ncu summary of
     the attention kernel on this workload, if that summary was taken on the
     current kernel sources (else None)."""
@@ -77,7 +88,7 @@ def recorded_traffic(workload: str):
         text = open(path).read()
         m_b = re.search(r"dram bytes per launch \(read \+ write\): (\d+)", text)
         m_h = re.search(r"kernel source hash: ([0-9a-f]+)", text)
-        if m_b and m_h and m_h.group(1) == kernel_source_hash():
+        if m_b and m_h and m_h.group(1) == kernel_source_hash(sources):
             return int(m_b.group(1))
     return None
 
@@ -232,6 +243,212 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------ prefill ------
+def prefill_oracle_sample(b: W.PrefillBatch, budget_s: float):
+    """Time the float64 oracle on the prefill workload: every head of a run of
+    query positions of one sequence per call, cycling over the sequences,
+    until about `budget_s` of CPU work; returns (FLOPs covered, seconds,
+    description)."""
+    import oracle
+    wl = b.wl
+    if b.slot_mapping.size:
+        oracle.kv_append(b.k_cache, b.v_cache, b.k_new, b.v_new, b.slot_mapping, wl.dtype)
+    Hq, D, P = wl.num_heads, wl.head_dim, 16  # positions per call
+    done, elapsed, calls = 0, 0.0, 0
+    while elapsed < budget_s:
+        s = calls % wl.batch
+        q0, q1 = int(b.query_start[s]), int(b.query_start[s + 1])
+        qlen, L = q1 - q0, int(b.context_lens[s])
+        j0 = (calls // wl.batch * P) % max(1, qlen)
+        rows = np.arange(j0 * Hq, min(qlen, j0 + P) * Hq, dtype=np.int64)
+        t = time.perf_counter()
+        oracle.paged_attention(b.q[q0:q1][None], b.k_cache, b.v_cache, b.block_table[s:s + 1],
+                               b.context_lens[s:s + 1], wl.softmax_scale, wl.dtype, rows=rows)
+        elapsed += time.perf_counter() - t
+        done += sum(4 * D * (L - qlen + int(r) // Hq + 1) for r in rows)
+        calls += 1
+    desc = (f"{calls} calls of {P} query positions x {Hq} heads, cycling over the "
+            f"{wl.batch} sequences, float64 C oracle, {oracle.num_threads()} threads, "
+            f"{elapsed:.1f} s")
+    return done, elapsed, desc
+
+
+def prefill_config(wl: W.PrefillWorkload, b: W.PrefillBatch) -> dict:
+    return {"workload": wl.name, "batch": wl.batch, "num_heads": wl.num_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+            "block_size": wl.block_size,
+            "chunk_lens": sorted(set(int(x) for x in np.diff(b.query_start))),
+            "context_lens": f"{int(b.context_lens.min())}..{int(b.context_lens.max())}"
+                            f" (cached prefix + chunk)",
+            "flops_per_step": wl.flops(),
+            "l2": "no flush: K/V and q are re-read from L2 by design (tensor-bound); "
+                  "each step rewrites the chunk rows",
+            "step": f"kv_append of {b.total_q} chunk rows + paged_prefill_attention"}
+
+
+def run_prefill(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from paged_kv_cache_18_gb300 import build as pkv_build
+    if rank == 0 or not os.path.exists(pkv_build.LIB):
+        pkv_build.build()
+    barrier()
+    import paged_kv_cache_18_gb300 as pkv
+
+    wl = W.PREFILL_WORKLOADS[args.workload]
+    if rank > 0:
+        wl = W.PrefillWorkload(**{**wl.__dict__, "seed": wl.seed + 100 * rank})
+    b = W.make_prefill_batch(wl)
+    k_cache = dev_tensor(b.k_cache, wl.dtype, dev)
+    v_cache = dev_tensor(b.v_cache, wl.dtype, dev)
+    k_new = dev_tensor(b.k_new, wl.dtype, dev)
+    v_new = dev_tensor(b.v_new, wl.dtype, dev)
+    q = dev_tensor(b.q, wl.dtype, dev)
+    slots = torch.from_numpy(b.slot_mapping).to(dev)
+    table = torch.from_numpy(b.block_table).to(dev)
+    lens = torch.from_numpy(b.context_lens).to(dev)
+    qs = torch.from_numpy(b.query_start).to(dev)
+    out = torch.empty_like(q)
+    mq = b.max_query_len
+    opts = dict(max_query_len=mq, scale=wl.softmax_scale, out=out, stages=args.stages)
+
+    def attend(qq, kn, vn, sl, tb, ln, st):
+        pkv.kv_append(kn, vn, k_cache, v_cache, sl)
+        pkv.paged_prefill_attention(qq, k_cache, v_cache, tb, ln, st, **opts)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        attend(q, k_new, v_new, slots, table, lens, qs)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
+    if sampler:
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        pkv.kv_append(k_new, v_new, k_cache, v_cache, slots)
+        ev[i][0].record(stream)
+        pkv.paged_prefill_attention(q, k_cache, v_cache, table, lens, qs, **opts)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    barrier()
+    step_ms = dist_max(start.elapsed_time(end) / K, dev)
+    attn_ms = statistics.mean(a.elapsed_time(z) for a, z in ev)
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    e2e = None
+    flops = wl.flops()
+    if not args.no_e2e:
+        host = {n: t.cpu().pin_memory() for n, t in
+                (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots),
+                 ("table", table), ("lens", lens), ("qs", qs))}
+        out_host = torch.empty_like(out, device="cpu").pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+        E = max(3, min(K, 100))
+
+        def e2e_step():
+            for n in dev_in:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            attend(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["slots"],
+                   dev_in["table"], dev_in["lens"], dev_in["qs"])
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(E):
+            e2e_step()
+        e2e_s = dist_max((time.perf_counter() - t0) / E, dev)
+        e2e = {"value": dist_sum(flops, dev) / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
+               "ms_per_step": 1e3 * e2e_s}
+    total_flops = dist_sum(flops, dev)
+    total_tokens = dist_sum(b.total_q, dev)
+    if rank != 0:
+        return 0
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_BF16_TFLOPS_SUSTAINED))
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        f, secs, desc = prefill_oracle_sample(W.make_prefill_batch(W.PREFILL_WORKLOADS[
+            args.workload]), args.cpu_budget)
+        import oracle
+        cpu = {"value": f / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": desc}
+    line = {
+        "metric": PREFILL_METRIC, "value": total_flops / (step_ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": prefill_config(wl, b),
+        "pct_of_tensor_peak": 100.0 * achieved / peak,
+        "tokens_per_s": total_tokens / (step_ms * 1e-3),
+        "attention_ms": attn_ms,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(args.workload, PREFILL_SOURCES),
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained (back-to-back launches)",
+                     "algorithmic_flops_per_launch": flops,
+                     "kernel": "paged_prefill_attention", "launches_per_step": 2},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_reference_prefill(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    wl = W.PREFILL_WORKLOADS[args.workload]
+    b = W.make_prefill_batch(wl)
+    per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        prefill_oracle_sample(b, per_step_budget / 4)
+    total, total_s, desc = 0, 0.0, ""
+    for _ in range(args.steps):
+        f, secs, desc = prefill_oracle_sample(b, per_step_budget)
+        total += f
+        total_s += secs
+    value = total / total_s / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": prefill_config(wl, b),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": desc + f"; ~{per_step_budget:.1f} s per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
     return 0
 
 
@@ -481,7 +698,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(W.WORKLOADS), default="llama2_13b")
+    ap.add_argument("--workload", choices=list(W.WORKLOADS) + list(W.PREFILL_WORKLOADS),
+                    default="llama2_13b")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--split-blocks", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0, help="tensor-core kernel ring depth")
@@ -505,6 +723,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in W.PREFILL_WORKLOADS:
+        return run_reference_prefill(args) if args.impl == "reference" else run_prefill(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
