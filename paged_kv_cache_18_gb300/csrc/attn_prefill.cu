@@ -506,14 +506,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sl = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
+      // A warp whose 32 rows are all past the tile's last row (a short
+      // chunk) has no softmax to do: it only keeps pace with the chunks
+      // (waits for S so that it never arrives for a chunk two ahead) and
+      // releases P; the P.V rows it leaves are never stored.
+      const bool idle = w.row0 + t * kTileRows + quad * 32 >= w.row0 + w.rows;
+      // block-table entries of a chunk (lanes 0..3), loaded one chunk ahead
+      auto table_entry = [&](int c) {
+        const int nb = min(kChunkBlocks, w.nblk - c * kChunkBlocks);
+        return lane < nb ? __ldg(table + c * kChunkBlocks + lane) : 0;
+      };
+      int entry_next = idle ? 0 : table_entry(0);
       for (int c = 0; c < nch; ++c) {
         const uint32_t s_addr = tmem + lane_base + t * 2 * kChunkKeys + (c & 1) * kChunkKeys;
         const int key0 = c * kChunkKeys;
         uint32_t va[32], vb[32];
         uint32_t bad_mask = 0;
+        if (idle) {
+          if (ok) {
+            const bool wt = mbar_wait_bounded(smem_u32(&s_full[t][c & 1]), (c >> 1) & 1);
+            ok = __all_sync(kFull, wt && !s_abort);
+          }
+          turn_wait(c);
+          if (ok && lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c & 1]));
+          turn_pass(c);
+          continue;
+        }
         if (ok) {
           const int nb = min(kChunkBlocks, w.nblk - c * kChunkBlocks);
-          const int entry = lane < nb ? __ldg(table + c * kChunkBlocks + lane) : 0;
+          const int entry = entry_next;
+          if (c + 1 < nch) entry_next = table_entry(c + 1);
           bad_mask = __ballot_sync(
               kFull, lane < nb && (entry < 0 || static_cast<int64_t>(entry) >= p.num_blocks));
           const bool wt = mbar_wait_bounded(smem_u32(&s_full[t][c & 1]), (c >> 1) & 1);
@@ -613,12 +635,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c & 1]));
         turn_pass(c);
       }
-      if (ok) {
+      if (ok && !idle) {
         const bool wt =
             mbar_wait_bounded(smem_u32(&pv_done[t][(nch - 1) & 1]), ((nch - 1) >> 1) & 1);
         ok = __all_sync(kFull, wt && !s_abort);
       }
-      if (ok) {
+      if (ok && !idle) {
         tc::fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         T *orow = reinterpret_cast<T *>(p.out) +
