@@ -390,6 +390,19 @@ PKV_API pkv_status pkv_read_error_word(const int32_t *error_word, int32_t *host_
                                pkv_stream_t stream);
 
 /*
+ * pkv_check_bounded_wait -- exercise the give-up path of the kernels' waits.
+ * Every wait on an mbarrier in this library's kernels is bounded: past its
+ * time limit it records PKV_DEVERR_TIMEOUT in the error word and the kernel
+ * returns, so a lost completion never hangs the GPU.  This call launches one
+ * thread that waits, through the same wait loop, on a barrier nothing ever
+ * arrives on, for limit_us microseconds (1 .. 10^7); afterwards the error
+ * word holds PKV_DEVERR_TIMEOUT (if it held 0) and *waited_ns (optional,
+ * device memory) the time the wait took.  Asynchronous on `stream`.
+ */
+PKV_API pkv_status pkv_check_bounded_wait(int32_t *error_word, uint32_t limit_us,
+                                          uint64_t *waited_ns, pkv_stream_t stream);
+
+/*
  * pkv_paged_decode_attention_noalloc -- pkv_paged_decode_attention for
  * callers that cannot allocate device memory.  The pages have no counterpart
  * of this call; it exists for callers such as a plugin inside a host

@@ -37,7 +37,7 @@ EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_
             "pkv_paged_attention_fp8", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence",
             "pkv_bm_append", "pkv_bm_fork", "pkv_bm_free", "pkv_bm_sequence",
             "pkv_bm_block_table", "pkv_bm_stats", "pkv_bm_block_info", "pkv_bm_hash",
-            "pkv_copy_blocks", "pkv_paged_prefill_attention")
+            "pkv_copy_blocks", "pkv_paged_prefill_attention", "pkv_check_bounded_wait")
 
 
 class PkvError(RuntimeError):
@@ -135,6 +135,7 @@ def lib() -> ctypes.CDLL:
                                             ctypes.POINTER(u64)]
             L.pkv_bm_hash.argtypes = [u64, pi32, i32]
             L.pkv_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i64, i32, vp, vp]
+            L.pkv_check_bounded_wait.argtypes = [vp, ctypes.c_uint32, vp, vp]
             L.pkv_paged_prefill_attention.argtypes = [
                 vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64,
                 ctypes.c_float, i32, ctypes.POINTER(Options), vp, vp]
@@ -651,3 +652,17 @@ def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
         query_start.data_ptr(), int(max_query_len), B, total_q, Hq, Hkv, D, bs, NB,
         float(scale), _DTYPE[q.dtype], _opts(0, 0, stages), _err_ptr(error_word), _stream(q)))
     return out
+
+
+def check_bounded_wait(error_word: torch.Tensor, limit_us: int,
+                       waited_ns: Optional[torch.Tensor] = None) -> None:
+    """Launch a bounded wait on a barrier nothing arrives on
+    (pkv_check_bounded_wait): it gives up after limit_us and records
+    PKV_DEVERR_TIMEOUT in error_word."""
+    _need(error_word.dtype == torch.int32 and error_word.is_cuda, "error_word: CUDA int32")
+    ptr = None
+    if waited_ns is not None:
+        _need(waited_ns.dtype == torch.int64 and waited_ns.is_cuda, "waited_ns: CUDA int64")
+        ptr = waited_ns.data_ptr()
+    _check("pkv_check_bounded_wait", lib().pkv_check_bounded_wait(
+        error_word.data_ptr(), int(limit_us), ptr, _stream(error_word)))

@@ -225,3 +225,33 @@ cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src,
 }
 
 }  // namespace pkv
+
+// ---- the bounded wait, exercised ---------------------------------------------
+// Every wait of the library's kernels on an mbarrier gives up after a time
+// limit, records PKV_DEVERR_TIMEOUT and lets the kernel return.  This kernel
+// waits on a barrier that nothing ever arrives on, through the same wait
+// loop with a caller-chosen limit, so the give-up path can be checked on a
+// GPU without hanging or faulting it.
+namespace pkv {
+namespace {
+
+__global__ void bounded_wait_kernel(int32_t *err, unsigned long long limit_ns,
+                                    unsigned long long *waited_ns) {
+  __shared__ uint64_t never;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&never), 1);
+  fence_mbar_init();
+  const unsigned long long t0 = global_ns();
+  if (!mbar_wait_bounded_ns(smem_u32(&never), 0, limit_ns)) record_error(err, PKV_DEVERR_TIMEOUT);
+  if (waited_ns) *waited_ns = global_ns() - t0;
+}
+
+}  // namespace
+
+cudaError_t bounded_wait_launch(int32_t *err, unsigned long long limit_ns,
+                                unsigned long long *waited_ns, cudaStream_t stream) {
+  bounded_wait_kernel<<<1, 32, 0, stream>>>(err, limit_ns, waited_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

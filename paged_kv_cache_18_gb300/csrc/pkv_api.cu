@@ -615,6 +615,16 @@ pkv_status pkv_paged_prefill_attention(void *out, const void *q, const void *k_c
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+pkv_status pkv_check_bounded_wait(int32_t *error_word, uint32_t limit_us,
+                                  uint64_t *waited_ns, pkv_stream_t stream) {
+  if (!error_word || limit_us < 1 || limit_us > 10000000u) return PKV_ERR_INVALID_ARG;
+  if (!aligned(error_word, 4) || (waited_ns && !aligned(waited_ns, 8))) return PKV_ERR_ALIGNMENT;
+  const cudaError_t e = bounded_wait_launch(
+      error_word, 1000ull * limit_us, reinterpret_cast<unsigned long long *>(waited_ns),
+      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_attention_plan_for(int batch, int num_queries, int num_heads, int num_kv_heads,
                                   int head_dim, int block_size, int max_context_len,
                                   pkv_dtype dtype, const pkv_options *options, int num_sms,

@@ -142,14 +142,18 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Wait for phase `parity` of the barrier, giving up after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of the barrier, giving up after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded_ns(uint32_t bar, uint32_t parity,
+                                                     unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
   return true;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  return mbar_wait_bounded_ns(bar, parity, kWaitLimitNs);
 }
 
 // ---- bulk copies (TMA engine) -------------------------------------------

@@ -50,6 +50,10 @@ cudaError_t tc_launch(pkv_dtype dtype, int head_dim, int rows_per_cta, int stage
                       const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnParams &p,
                       dim3 grid, cudaStream_t stream);
 
+// A one-thread wait on a barrier nothing arrives on, bounded by limit_ns.
+cudaError_t bounded_wait_launch(int32_t *err, unsigned long long limit_ns,
+                                unsigned long long *waited_ns, cudaStream_t stream);
+
 // Chunked prefill on the tcgen05 tensor cores (attn_prefill.cu): head_dim 64
 // or 128, bf16 / f16, group size dividing 128.  `stages` is the K/V ring
 // depth (0: default).

@@ -159,3 +159,10 @@ def test_plan_caps_split_length_in_bytes():
     p16 = binding.plan_for(128, 1, 32, 8, 128, 4096, torch.bfloat16, num_sms=152, ctas_per_sm=3)
     p8 = binding.plan_for(128, 1, 32, 8, 128, 4096, "fp8", num_sms=152, ctas_per_sm=3)
     assert p8["split_blocks"] == 2 * p16["split_blocks"]
+
+
+def test_bounded_wait_check_validates_its_arguments(L):
+    assert L.pkv_check_bounded_wait(None, 100, None, None) == 1
+    assert L.pkv_check_bounded_wait(16, 0, None, None) == 1
+    assert L.pkv_check_bounded_wait(16, 10**8, None, None) == 1
+    assert L.pkv_check_bounded_wait(18, 100, None, None) == 5   # misaligned error word
