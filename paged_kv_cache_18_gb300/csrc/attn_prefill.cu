@@ -87,6 +87,34 @@ template <int D, int NS> struct Geom {
   static_assert(kOCol + kTiles * D <= 512, "TMEM columns");
 };
 
+// Packed pairs of floats (the f32x2 arithmetic of sm_100 and later: one
+// instruction for both halves).
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // P is split into a high part and a remainder for bf16 (see above).
 template <typename T> constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
 
@@ -607,20 +635,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(s scale_log2 - m) written over each 32-key group's own S
         // columns: the high part in its first 16, the remainder in the other
         // 16 (f16: P alone in the first 16)
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};
+        // (pairs of scores in f32x2 arithmetic: the scale-and-shift, the
+        // row-sum accumulation and the remainder of the bf16 split)
+        const uint64_t sl2 = f2pack(sl, sl), nm2 = f2pack(neg_m, neg_m);
+        uint64_t rs2[2] = {0ull, 0ull};  // (+0.0f, +0.0f)
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const uint32_t(&v)[32] = g ? vb : va;
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float x = ex2(fmaf(__uint_as_float(v[2 * e]), sl, neg_m));
-            const float y = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sl, neg_m));
-            rs[e & 3] += x + y;
+            const uint64_t t2 =
+                ffma2(f2pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2, nm2);
+            const float2 t = f2unpack(t2);
+            const float x = ex2(t.x), y = ex2(t.y);
+            const uint64_t pxy = f2pack(x, y);
+            rs2[e & 1] = fadd2(rs2[e & 1], pxy);
             if constexpr (kSplitP<T>) {
               const __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
-              hi[e] = *reinterpret_cast<const uint32_t *>(&hv);
-              lo[e] = pack2<T>(x - __low2float(hv), y - __high2float(hv));
+              const uint32_t hb = *reinterpret_cast<const uint32_t *>(&hv);
+              hi[e] = hb;
+              const float2 r = f2unpack(fsub2(
+                  pxy, f2pack(__uint_as_float(hb << 16), __uint_as_float(hb & 0xffff0000u))));
+              lo[e] = pack2<T>(r.x, r.y);
             } else {
               hi[e] = pack2<T>(x, y);
             }
@@ -628,7 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st16u(s_addr + 32 * g, hi);
           if constexpr (kSplitP<T>) tc::tmem_st16u(s_addr + 32 * g + 16, lo);
         }
-        l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        const float2 ra = f2unpack(rs2[0]), rb = f2unpack(rs2[1]);
+        l += (ra.x + ra.y) + (rb.x + rb.y);
         tc::tmem_wait_st();
         tc::fence_before();
         __syncwarp();
