@@ -226,3 +226,52 @@ def test_eviction_under_memory_pressure_keeps_live_rows_intact():
                 pass
         if live:
             e.check_attention(live)
+
+
+def test_copy_on_write_and_decode_replay_from_a_cuda_graph():
+    # a decode step whose slots and copy pairs came from the manager: the
+    # block copy, the append and the attention capture into one graph
+    e = Engine(32)
+    prompt = e.rng.integers(0, 1000, 24).tolist()
+    e.add(0, prompt)
+    e.fork(0, 1)
+    token = 7
+    slots, copies = e.mgr.append(1, [token])
+    assert len(copies) == 1
+    e.tokens[1] = e.tokens[1] + [token]
+    toks = e.tokens[1]
+    kb, vb = e.rows(toks)
+    k_new = dev_tensor(kb[None], "bf16", DEV)
+    v_new = dev_tensor(vb[None], "bf16", DEV)
+    slot_t = torch.from_numpy(np.asarray(slots, dtype=np.int64)).to(DEV)
+    src = torch.tensor([copies[0][0]], dtype=torch.int32, device=DEV)
+    dst = torch.tensor([copies[0][1]], dtype=torch.int32, device=DEV)
+    table, lens = e.mgr.block_table([0, 1])
+    tab, ln = torch.from_numpy(table).to(DEV), torch.from_numpy(lens).to(DEV)
+    q = dev_tensor(W.to_storage(e.rng.standard_normal((2, 1, e.Hq, e.D), dtype=np.float32),
+                                "bf16"), "bf16", DEV)
+    out = torch.empty(2, e.Hq, e.D, dtype=torch.bfloat16, device=DEV)
+
+    def step():
+        pkv.copy_blocks(e.k, e.v, src, dst, error_word=e.err)
+        pkv.kv_append(k_new, v_new, e.k, e.v, slot_t, error_word=e.err)
+        pkv.paged_decode_attention(q[:, 0], e.k, e.v, tab, ln, scale=1.0 / math.sqrt(e.D),
+                                   max_context_len=int(lens.max()), out=out,
+                                   error_word=e.err)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    qbits = q.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = e.reference([0, 1], qbits)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(host_f64(out, "bf16")[:, None], ref, "bf16", "graph replay")
+    assert binding.read_error_word(e.err) == 0

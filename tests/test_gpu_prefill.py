@@ -214,3 +214,35 @@ def test_prefill_rejects_what_it_does_not_run():
 def test_prefill_full_size_workload():
     wl = W.PREFILL_WORKLOADS["prefill_llama3_8b"]
     check(W.make_prefill_batch(wl), rows_per_seq=384, what=wl.name)
+
+
+def test_prefill_step_replays_from_a_cuda_graph():
+    # the append and the prefill call capture into one graph (no host sync,
+    # no allocation inside the calls) and replay to the same result
+    wl = W.PrefillWorkload("graph", 3, 32, 8, 128, "bf16", chunk_lens=[64, 300, 17],
+                           prefix_lens=[500, 40, 1200], seed=21)
+    b = W.make_prefill_batch(wl)
+    d = DevicePrefill(b)
+    out = torch.empty_like(d.q)
+
+    def step():
+        pkv.kv_append(d.k_new, d.v_new, d.k, d.v, d.slots, error_word=d.err)
+        pkv.paged_prefill_attention(d.q, d.k, d.v, d.table, d.lens, d.qs,
+                                    max_query_len=b.max_query_len, scale=wl.softmax_scale,
+                                    out=out, error_word=d.err)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up: kernel attributes are set outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    ref = oracle_prefill(b, rows_per_seq=256)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(host_f64(out, "bf16"), ref, "bf16", "graph replay")
+    assert binding.read_error_word(d.err) == 0
