@@ -570,12 +570,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(kFull, wt && !s_abort);
           if (ok) {
             tc::fence_after();
-            tc::tmem_ld32(s_addr, va);  // in flight across the turn wait
+            tc::tmem_ld32(s_addr, va);
             tc::tmem_ld32(s_addr + 32, vb);
           }
         }
-        turn_wait(c);
         if (!ok) {
+          turn_wait(c);
           turn_pass(c);
           continue;
         }
@@ -616,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_wait_bounded(smem_u32(&pv_done[t][(c - 1) & 1]), ((c - 1) >> 1) & 1);
           if (!__all_sync(kFull, pw && !s_abort)) {
             ok = false;
+            turn_wait(c);
             turn_pass(c);
             continue;
           }
@@ -639,6 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // row-sum accumulation and the remainder of the bf16 split)
         const uint64_t sl2 = f2pack(sl, sl), nm2 = f2pack(neg_m, neg_m);
         uint64_t rs2[2] = {0ull, 0ull};  // (+0.0f, +0.0f)
+        // the exp2 phase is the part the tiles take turns at: the other
+        // tile's loads, maximum and rescale test overlap it
+        turn_wait(c);
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const uint32_t(&v)[32] = g ? vb : va;
@@ -665,13 +669,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st16u(s_addr + 32 * g, hi);
           if constexpr (kSplitP<T>) tc::tmem_st16u(s_addr + 32 * g + 16, lo);
         }
+        turn_pass(c);
         const float2 ra = f2unpack(rs2[0]), rb = f2unpack(rs2[1]);
         l += (ra.x + ra.y) + (rb.x + rb.y);
         tc::tmem_wait_st();
         tc::fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c & 1]));
-        turn_pass(c);
       }
       if (ok && !idle) {
         const bool wt =
