@@ -521,15 +521,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nch = w.chunks(t);
       const bool turns = w.tiles == 2;
       const int n_other = turns ? w.chunks(1 - t) : 0;
-      auto turn_wait = [&](int c) {  // before chunk c: the other tile's turn is over
+      // The barriers order memory, not arithmetic: the exp2 work is pure
+      // register arithmetic, which the compiler may move across them.  So the
+      // wait hands out, from the same asm statement, a value the exp2 loop
+      // consumes (it cannot start before the wait), and the hand-over takes
+      // the loop's row sums as inputs (it cannot leave before the loop ends).
+      auto turn_wait = [&](int c, float dep) -> float {  // before chunk c's exp2
         const int oc = t == 0 ? c - 1 : c;
         if (turns && oc >= 0 && oc < n_other)
-          asm volatile("bar.sync %0, 256;" ::"r"(kTurnBar + (1 - t)) : "memory");
+          asm volatile("bar.sync %1, 256;\n\tmov.b32 %0, %0;"
+                       : "+f"(dep)
+                       : "r"(kTurnBar + (1 - t))
+                       : "memory");
+        return dep;
       };
-      auto turn_pass = [&](int c) {  // after chunk c: the other tile may go
+      auto turn_pass = [&](int c, uint64_t dep0, uint64_t dep1) {  // after chunk c's exp2
         const int oc = t == 0 ? c : c + 1;  // its chunk that waits for this one
         if (turns && oc < n_other)
-          asm volatile("bar.arrive %0, 256;" ::"r"(kTurnBar + t) : "memory");
+          asm volatile("bar.arrive %0, 256;" ::"r"(kTurnBar + t), "l"(dep0), "l"(dep1)
+                       : "memory");
       };
       const float sl = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
@@ -555,9 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool wt = mbar_wait_bounded(smem_u32(&s_full[t][c & 1]), (c >> 1) & 1);
             ok = __all_sync(kFull, wt && !s_abort);
           }
-          turn_wait(c);
+          turn_wait(c, 0.f);
           if (ok && lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c & 1]));
-          turn_pass(c);
+          turn_pass(c, 0ull, 0ull);
           continue;
         }
         if (ok) {
@@ -575,8 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) {
-          turn_wait(c);
-          turn_pass(c);
+          turn_wait(c, 0.f);
+          turn_pass(c, 0ull, 0ull);
           continue;
         }
         tc::tmem_wait_ld_regs(va);
@@ -616,8 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_wait_bounded(smem_u32(&pv_done[t][(c - 1) & 1]), ((c - 1) >> 1) & 1);
           if (!__all_sync(kFull, pw && !s_abort)) {
             ok = false;
-            turn_wait(c);
-            turn_pass(c);
+            turn_wait(c, 0.f);
+            turn_pass(c, 0ull, 0ull);
             continue;
           }
           tc::fence_after();
@@ -632,17 +642,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         m_ref = m_new;
-        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
         // P = 2^(s scale_log2 - m) written over each 32-key group's own S
         // columns: the high part in its first 16, the remainder in the other
         // 16 (f16: P alone in the first 16)
         // (pairs of scores in f32x2 arithmetic: the scale-and-shift, the
         // row-sum accumulation and the remainder of the bf16 split)
-        const uint64_t sl2 = f2pack(sl, sl), nm2 = f2pack(neg_m, neg_m);
-        uint64_t rs2[2] = {0ull, 0ull};  // (+0.0f, +0.0f)
         // the exp2 phase is the part the tiles take turns at: the other
         // tile's loads, maximum and rescale test overlap it
-        turn_wait(c);
+        const float neg_m = turn_wait(c, m_ref == -INFINITY ? 0.f : -m_ref);
+        const uint64_t sl2 = f2pack(sl, sl), nm2 = f2pack(neg_m, neg_m);
+        uint64_t rs2[2] = {0ull, 0ull};  // (+0.0f, +0.0f)
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const uint32_t(&v)[32] = g ? vb : va;
@@ -669,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st16u(s_addr + 32 * g, hi);
           if constexpr (kSplitP<T>) tc::tmem_st16u(s_addr + 32 * g + 16, lo);
         }
-        turn_pass(c);
+        turn_pass(c, rs2[0], rs2[1]);
         const float2 ra = f2unpack(rs2[0]), rb = f2unpack(rs2[1]);
         l += (ra.x + ra.y) + (rb.x + rb.y);
         tc::tmem_wait_st();
