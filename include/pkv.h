@@ -366,8 +366,10 @@ PKV_API pkv_status pkv_paged_attention_fp8(
  *   scale: the softmax scale, > 0 (PKV_ERR_INVALID_ARG otherwise).
  *   head_dim 64 or 128; block_size 16; num_heads / num_kv_heads must divide
  *   128.  No workspace: the work is split over query rows (256 per CTA),
- *   not over keys.  options: only `stages` (K/V ring depth; 0 = default) is
- *   read.  Runs on the fifth-generation tensor cores (tcgen05), S and O in
+ *   not over keys.  options: only `stages` is read: the K/V ring depth
+ *   in chunks, which also picks the chunk (head_dim 128: 6 or 8 stages of
+ *   64 keys, 3-5 of 128; head_dim 64: 12 or 16 of 64, 4, 6 or 8 of 128;
+ *   0 = 8 or 12 stages of 64 keys); any other value is PKV_ERR_UNSUPPORTED.  Runs on the fifth-generation tensor cores (tcgen05), S and O in
  *   tensor memory, P rounded to dtype.
  * A sequence whose query_start / context_lens break these rules is skipped
  * (its rows are not written) and recorded as PKV_DEVERR_CONTEXT_LEN; an

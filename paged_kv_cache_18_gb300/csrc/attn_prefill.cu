@@ -20,15 +20,16 @@
 //   warps 0-3 / 4-7  softmax and epilogue of query tile 0 / 1 (128 rows
 //                    each, one row per thread: TMEM lane = row); the two
 //                    tiles' softmaxes take turns chunk by chunk;
-//   warp 8           TMA producer: the Q tiles, then K and V chunks of 64
-//                    keys (4 blocks through the block table) into a ring of
-//                    NS stages, K and V alternating;
+//   warp 8           TMA producer: the Q tiles, then K and V chunks of CK
+//                    keys (CK / 16 blocks through the block table) into a
+//                    ring of NS stages, K and V alternating;
 //   warps 9 / 10     MMA issuer of tile 0 / 1 (one lane each); warp 9 owns
 //                    the TMEM allocation.
-// Per 64-key chunk c and tile t:
-//   S[128 x 64] = Q_t[128 x D] . K_c^T    (TMEM, fp32; buffer c & 1 of the
-//                                          tile, so S_{c+1} is computed while
-//                                          the softmax works on S_c)
+// Per chunk c of CK keys (64, or 128) and tile t:
+//   S[128 x CK] = Q_t[128 x D] . K_c^T    (TMEM, fp32; 64-key chunks: buffer
+//                                          c & 1 of the tile, so S_{c+1} is
+//                                          computed while the softmax works
+//                                          on S_c; 128-key chunks: one buffer)
 //   softmax per row, thread-local: masked scores in log2 units, a lazy
 //   reference max m (raised, with l and O rescaled, only when a score exceeds
 //   it by more than 2^8), P = 2^(s - m) written back over the S buffer in the
@@ -36,12 +37,12 @@
 //   high part (16 columns) and the remainder P - high (16), since one bf16
 //   rounding of P alone costs about 1.6e-3 of relative L2 error, as much as
 //   the output's own rounding; f16 (11 significant bits) needs no remainder
-//   O_t[128 x D] += P[128 x 64] . V_c[64 x D]   (A read from TMEM; bf16: a
+//   O_t[128 x D] += P[128 x CK] . V_c[CK x D]   (A read from TMEM; bf16: a
 //                                               second product with the
 //                                               remainder)
-// TMEM: two S buffers of 64 columns and O (D columns) per tile, 512 columns:
-// one CTA per SM.  (64-key chunks keep two S buffers per tile within TMEM:
-// with one, each tile's softmax would wait for its own P.V and next S.)
+// TMEM: 128 S columns (two buffers of 64, or one of 128) and O (D columns)
+// per tile, 512 columns: one CTA per SM.  (With 128-key chunks each tile's
+// softmax waits for its own P.V and next S; the 64-key default does not.)
 // While one tile's softmax runs, the tensor cores run the other tile's P.V
 // and next S: the two tiles' work interleaves.
 // Operands: Q and K K-major with the 128-byte swizzle (as the TMA writes
@@ -61,29 +62,30 @@ namespace prefill {
 constexpr int kTileRows = 128;                     // query rows per MMA tile (M)
 constexpr int kTiles = 2;                          // tiles per CTA
 constexpr int kCtaRows = kTiles * kTileRows;
-constexpr int kChunkKeys = 64;                     // keys per chunk (N of S)
-constexpr int kChunkBlocks = kChunkKeys / kBlockSize;
+constexpr int kCostKeys = 64;                      // keys per unit of the work order's cost
 constexpr int kSoftmaxWarps = 4 * kTiles;          // one per TMEM lane quadrant per tile
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kIssuerWarp = kSoftmaxWarps + 1;     // tile t's MMAs: warp kIssuerWarp + t
 constexpr int kThreads = (kSoftmaxWarps + 1 + kTiles) * 32;
 constexpr float kRescaleSlack = 8.f;
-// Named barrier kTurnBar + t: tile t's softmax hands over to the other tile's.
-constexpr int kTurnBar = 1;
+// Named barrier 1 + t: tile t's softmax hands over to the other tile's.
 
-template <int D, int NS> struct Geom {
+// CK keys per chunk (the N of S): 128 with one S buffer per tile, or 64 with
+// two (S of the next chunk computed during the softmax of this one).
+template <int D, int NS, int CK> struct Geom {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static constexpr int kPanels = D / 64;                        // 128-byte column panels
   static constexpr int kQPanelBytes = kTileRows * 128;          // 128 rows x 128 B
   static constexpr int kQBytes = kPanels * kQPanelBytes;        // one Q tile
-  static constexpr int kKVPanelBytes = kChunkKeys * 128;        // 64 rows x 128 B
+  static constexpr int kKVPanelBytes = CK * 128;                // CK rows x 128 B
   static constexpr int kStageBytes = kPanels * kKVPanelBytes;   // one K or V chunk
   static constexpr int kRingOff = kTiles * kQBytes;
   static constexpr int kBytes = kRingOff + NS * kStageBytes;
   static constexpr uint32_t kTmemCols = 512;
-  // tile t: S (and P over it) of chunk c at column 128 t + 64 (c & 1);
+  // tile t: S (and P over it) of chunk c at column 128 t + CK (c % kBufs);
   // O_t at kOCol + D t
-  static constexpr int kOCol = kTiles * 2 * kChunkKeys;
+  static constexpr int kBufs = 128 / CK;
+  static constexpr int kOCol = kTiles * 128;
   static_assert(kOCol + kTiles * D <= 512, "TMEM columns");
 };
 
@@ -133,7 +135,7 @@ struct Work {
   int b, kvh, row0;   // rows row0 .. row0 + rows - 1 of the sequence's (position, head) rows
   int rows, q0, qlen, L;
   int tiles;          // 1 or 2
-  int chunks0, chunks1;  // 64-key chunks tile 0 / tile 1 reads
+  int chunks0, chunks1;  // chunks tile 0 / tile 1 reads
   int nblk;           // cache blocks the CTA reads
   __device__ __forceinline__ int chunks(int t) const { return t == 0 ? chunks0 : chunks1; }
 };
@@ -161,7 +163,7 @@ __device__ __forceinline__ SeqShape seq_shape(const PrefillParams &p, int b) {
 // that orders the work.  Non-decreasing in `pair`.
 __device__ __forceinline__ int pair_cost(const SeqShape &q, int group, int pair) {
   const int last = min(pair * kCtaRows + kCtaRows, q.qlen * group) - 1;
-  return (q.L - q.qlen + last / group) / kChunkKeys + 1;
+  return (q.L - q.qlen + last / group) / kCostKeys + 1;
 }
 // First pair of the sequence whose cost is at least v (q.pairs if none).
 __device__ __forceinline__ int first_pair_at_least(const SeqShape &q, int group, int v) {
@@ -238,7 +240,7 @@ __device__ __forceinline__ bool locate_unit(const PrefillParams &p, int r, int *
   return false;  // (not reached when the counts agree)
 }
 
-__device__ __forceinline__ Work make_work(const PrefillParams &p) {
+template <int CK> __device__ __forceinline__ Work make_work(const PrefillParams &p) {
   Work w;
   w.kvh = static_cast<int>(blockIdx.x % p.num_kv_heads);
   int pair = 0;
@@ -256,8 +258,8 @@ __device__ __forceinline__ Work make_work(const PrefillParams &p) {
   // the last key each tile's rows see
   const int lim0 = w.L - w.qlen + (w.row0 + min(kTileRows, w.rows) - 1) / p.group;
   const int lim1 = w.L - w.qlen + (w.row0 + w.rows - 1) / p.group;
-  w.chunks0 = lim0 / kChunkKeys + 1;
-  w.chunks1 = w.tiles == 2 ? lim1 / kChunkKeys + 1 : 0;
+  w.chunks0 = lim0 / CK + 1;
+  w.chunks1 = w.tiles == 2 ? lim1 / CK + 1 : 0;
   w.nblk = (w.tiles == 2 ? lim1 : lim0) / kBlockSize + 1;
   return w;
 }
@@ -273,21 +275,23 @@ __device__ __forceinline__ void check_sequences(const PrefillParams &p) {
   if (__any_sync(kFull, bad) && threadIdx.x == 0) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
 }
 
-template <typename T, int D, int NS>
+template <typename T, int D, int NS, int CK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  using G = Geom<D, NS>;
+  using G = Geom<D, NS, CK>;
+  constexpr int kChunkKeys = CK, kChunkBlocks = CK / kBlockSize, kBufs = G::kBufs;
+  constexpr int kHalves = CK / 64;  // 64-key halves of a chunk in the softmax
   check_sequences(p);
-  const Work w = make_work(p);
+  const Work w = make_work<CK>(p);
   if (w.rows <= 0) return;  // the whole CTA, before any barrier or TMEM use
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  // per tile and S buffer u (chunk c uses u = c & 1)
+  // per tile and S buffer u (chunk c uses u = c % kBufs)
   __shared__ uint64_t full[NS], empty[NS], q_full, landed, s_full[kTiles][2], p_full[kTiles][2],
       pv_done[kTiles][2], mma_idle[kTiles];
   __shared__ uint32_t tmem_base_s;
@@ -402,12 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kIssuerWarp) {
     // ---- MMA issuers: one thread per tile ----------------------------------------
-    // Chunk c: S_c into the tile's buffer c & 1 (two chunks ahead, so S_{c+1}
-    // is there when the softmax finishes chunk c), then P_c . V_c once the
-    // softmax has written P_c over S_c.  Each tile has its own issuing thread,
-    // so one tile's waits never hold up the other's MMAs; every K / V stage is
-    // released by both (a tile that is done, or absent, releases the stages
-    // it no longer reads as they arrive).  The issuers poll their barriers
+    // Chunk c: S_c into the tile's buffer c % kBufs (64-key chunks: two
+    // chunks ahead, so S_{c+1} is there when the softmax finishes chunk c),
+    // then P_c . V_c once the softmax has written P_c over S_c.  Each tile
+    // has its own issuing thread, so one tile's waits never hold up the
+    // other's MMAs; every K / V stage is released by both (a tile that is
+    // done, or absent, releases the stages it no longer reads as they arrive).  The issuers poll their barriers
     // (no suspension): their wake-up is on the critical path.
     const int t = warp - kIssuerWarp;
     if (lane == 0) {
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv = tc::smem_desc(0, G::kKVPanelBytes, 1024, tc::kSwizzle128);
       const int mine = t < w.tiles ? w.chunks(t) : 0;
       auto ring = [&](int idx) { return sbase + G::kRingOff + (idx % NS) * G::kStageBytes; };
-      auto sbuf = [&](int c) { return tmem + t * 2 * kChunkKeys + (c & 1) * kChunkKeys; };
+      auto sbuf = [&](int c) { return tmem + t * 128 + (c % kBufs) * kChunkKeys; };
       auto issue_s = [&](int c) {
         const uint32_t qa = sbase + t * G::kQBytes, ka = ring(2 * c);
 #pragma unroll
@@ -427,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t offk = (ks >> 2) * G::kKVPanelBytes + (ks & 3) * 32;
           tc::mma(sbuf(c), dk | ((qa + offq) >> 4), dk | ((ka + offk) >> 4), id_s, ks > 0);
         }
-        tc::commit(smem_u32(&s_full[t][c & 1]));
+        tc::commit(smem_u32(&s_full[t][c % kBufs]));
       };
       auto issue_o = [&](int c) {
         const uint32_t va = ring(2 * c + 1);
@@ -439,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_ts(tmem + G::kOCol + t * D, pc, vb, id_o, c > 0 || ks > 0);
           if constexpr (kSplitP<T>) tc::mma_ts(tmem + G::kOCol + t * D, pc + 16, vb, id_o, true);
         }
-        tc::commit(smem_u32(&pv_done[t][c & 1]));
+        tc::commit(smem_u32(&pv_done[t][c % kBufs]));
       };
       auto spin = [&](uint64_t &bar, uint32_t parity) {
         return tc::mbar_spin_bounded(smem_u32(&bar), parity);
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_arrive(smem_u32(&empty[idx % NS]));
       };
       bool ok = spin(q_full, 0);
-      for (int c = 0; ok && c < 2 && c < n_chunks; ++c) {
+      for (int c = 0; ok && c < kBufs && c < n_chunks; ++c) {
         if (!full_wait(2 * c)) {
           ok = false;
           break;
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (c < mine) {
-          if (!spin(p_full[t][c & 1], (c >> 1) & 1)) {
+          if (!spin(p_full[t][c % kBufs], (c / kBufs) & 1)) {
             ok = false;
             break;
           }
@@ -478,21 +482,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_o(c);
         }
         release(2 * c + 1, c < mine);
-        if (c + 2 < n_chunks) {
-          if (!full_wait(2 * c + 4)) {
+        if (c + kBufs < n_chunks) {
+          if (!full_wait(2 * (c + kBufs))) {
             ok = false;
             break;
           }
-          if (c + 2 < mine) {
-            // S_{c+2} overwrites the buffer P_c is read from: after P_c . V_c
-            if (!spin(pv_done[t][c & 1], (c >> 1) & 1)) {
+          if (c + kBufs < mine) {
+            // S_{c+kBufs} overwrites the buffer P_c is read from: after P_c . V_c
+            if (!spin(pv_done[t][c % kBufs], (c / kBufs) & 1)) {
               ok = false;
               break;
             }
             tc::fence_after();
-            issue_s(c + 2);
+            issue_s(c + kBufs);
           }
-          release(2 * c + 4, c + 2 < mine);
+          release(2 * (c + kBufs), c + kBufs < mine);
         }
       }
       if (!ok) abort_all();
@@ -526,20 +530,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // wait hands out, from the same asm statement, a value the exp2 loop
       // consumes (it cannot start before the wait), and the hand-over takes
       // the loop's row sums as inputs (it cannot leave before the loop ends).
+      // (Immediate barrier ids: a bar.arrive / bar.sync pair naming its
+      // barrier through a register measured as not waiting on this GPU.)
       auto turn_wait = [&](int c, float dep) -> float {  // before chunk c's exp2
         const int oc = t == 0 ? c - 1 : c;
-        if (turns && oc >= 0 && oc < n_other)
-          asm volatile("bar.sync %1, 256;\n\tmov.b32 %0, %0;"
-                       : "+f"(dep)
-                       : "r"(kTurnBar + (1 - t))
-                       : "memory");
+        if (turns && oc >= 0 && oc < n_other) {
+          if (t == 0)  // tile 1's hand-over
+            asm volatile("bar.sync 2, 256;\n\tmov.b32 %0, %0;" : "+f"(dep) : : "memory");
+          else         // tile 0's hand-over
+            asm volatile("bar.sync 1, 256;\n\tmov.b32 %0, %0;" : "+f"(dep) : : "memory");
+        }
         return dep;
       };
       auto turn_pass = [&](int c, uint64_t dep0, uint64_t dep1) {  // after chunk c's exp2
         const int oc = t == 0 ? c : c + 1;  // its chunk that waits for this one
-        if (turns && oc < n_other)
-          asm volatile("bar.arrive %0, 256;" ::"r"(kTurnBar + t), "l"(dep0), "l"(dep1)
-                       : "memory");
+        if (turns && oc < n_other) {
+          if (t == 0)
+            asm volatile("bar.arrive 1, 256;" ::"l"(dep0), "l"(dep1) : "memory");
+          else
+            asm volatile("bar.arrive 2, 256;" ::"l"(dep0), "l"(dep1) : "memory");
+        }
       };
       const float sl = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
@@ -556,17 +566,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int entry_next = idle ? 0 : table_entry(0);
       for (int c = 0; c < nch; ++c) {
-        const uint32_t s_addr = tmem + lane_base + t * 2 * kChunkKeys + (c & 1) * kChunkKeys;
+        const uint32_t s_addr = tmem + lane_base + t * 128 + (c % kBufs) * kChunkKeys;
         const int key0 = c * kChunkKeys;
         uint32_t va[32], vb[32];
         uint32_t bad_mask = 0;
         if (idle) {
           if (ok) {
-            const bool wt = mbar_wait_bounded(smem_u32(&s_full[t][c & 1]), (c >> 1) & 1);
+            const bool wt = mbar_wait_bounded(smem_u32(&s_full[t][c % kBufs]), (c / kBufs) & 1);
             ok = __all_sync(kFull, wt && !s_abort);
           }
           turn_wait(c, 0.f);
-          if (ok && lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c & 1]));
+          if (ok && lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c % kBufs]));
           turn_pass(c, 0ull, 0ull);
           continue;
         }
@@ -576,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c + 1 < nch) entry_next = table_entry(c + 1);
           bad_mask = __ballot_sync(
               kFull, lane < nb && (entry < 0 || static_cast<int64_t>(entry) >= p.num_blocks));
-          const bool wt = mbar_wait_bounded(smem_u32(&s_full[t][c & 1]), (c >> 1) & 1);
+          const bool wt = mbar_wait_bounded(smem_u32(&s_full[t][c % kBufs]), (c / kBufs) & 1);
           ok = __all_sync(kFull, wt && !s_abort);
           if (ok) {
             tc::fence_after();
@@ -589,10 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           turn_pass(c, 0ull, 0ull);
           continue;
         }
-        tc::tmem_wait_ld_regs(va);
-        tc::tmem_wait_ld_regs(vb);
         // keys this row may not see (past its last key, or in a bad block):
-        // score -inf
+        // score -inf (g: the chunk's 32-key group)
         auto mask32 = [&](uint32_t(&v)[32], int g) {
           if (key0 + 32 * g + 31 > lim || ((bad_mask >> (2 * g)) & 3u) != 0) {
 #pragma unroll
@@ -603,17 +611,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         };
+        // one 64-key half of the chunk's scores into va / vb, masked
+        auto load_half = [&](int hh) {
+          tc::tmem_ld32(s_addr + 64 * hh, va);
+          tc::tmem_ld32(s_addr + 64 * hh + 32, vb);
+          tc::tmem_wait_ld_regs(va);
+          tc::tmem_wait_ld_regs(vb);
+          mask32(va, 2 * hh);
+          mask32(vb, 2 * hh + 1);
+        };
+        // the chunk's largest raw score (the scale is positive, so scaling
+        // after the maximum is the same); a 128-key chunk is read in two
+        // halves, the second staying in registers for the exp2 pass
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        auto max_half = [&]() {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            mx[0] = fmaxf(mx[0], __uint_as_float(va[e]));
+            mx[1] = fmaxf(mx[1], __uint_as_float(va[e + 1]));
+            mx[2] = fmaxf(mx[2], __uint_as_float(vb[e]));
+            mx[3] = fmaxf(mx[3], __uint_as_float(vb[e + 1]));
+          }
+        };
+        tc::tmem_wait_ld_regs(va);
+        tc::tmem_wait_ld_regs(vb);
         mask32(va, 0);
         mask32(vb, 1);
-        // the chunk's largest raw score (the scale is positive, so scaling
-        // after the maximum is the same)
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          mx[0] = fmaxf(mx[0], __uint_as_float(va[e]));
-          mx[1] = fmaxf(mx[1], __uint_as_float(va[e + 1]));
-          mx[2] = fmaxf(mx[2], __uint_as_float(vb[e]));
-          mx[3] = fmaxf(mx[3], __uint_as_float(vb[e + 1]));
+        max_half();
+#pragma unroll 1
+        for (int hh = 1; hh < kHalves; ++hh) {
+          load_half(hh);
+          max_half();
         }
         const float mc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
         const bool raise = mc > m_ref + kRescaleSlack;
@@ -623,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c > 0 && __any_sync(kFull, raise)) {
           // O holds P_{c-1} . V_{c-1} once that product has completed
           const bool pw =
-              mbar_wait_bounded(smem_u32(&pv_done[t][(c - 1) & 1]), ((c - 1) >> 1) & 1);
+              mbar_wait_bounded(smem_u32(&pv_done[t][(c - 1) % kBufs]), ((c - 1) / kBufs) & 1);
           if (!__all_sync(kFull, pw && !s_abort)) {
             ok = false;
             turn_wait(c, 0.f);
@@ -652,31 +680,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float neg_m = turn_wait(c, m_ref == -INFINITY ? 0.f : -m_ref);
         const uint64_t sl2 = f2pack(sl, sl), nm2 = f2pack(neg_m, neg_m);
         uint64_t rs2[2] = {0ull, 0ull};  // (+0.0f, +0.0f)
+#pragma unroll 1
+        for (int hh = kHalves - 1; hh >= 0; --hh) {
+          if (hh < kHalves - 1) load_half(hh);  // (the last half read is still in va / vb)
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const uint32_t(&v)[32] = g ? vb : va;
-          uint32_t hi[16], lo[16];
+          for (int g = 0; g < 2; ++g) {
+            const uint32_t(&v)[32] = g ? vb : va;
+            uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const uint64_t t2 =
-                ffma2(f2pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2, nm2);
-            const float2 t = f2unpack(t2);
-            const float x = ex2(t.x), y = ex2(t.y);
-            const uint64_t pxy = f2pack(x, y);
-            rs2[e & 1] = fadd2(rs2[e & 1], pxy);
-            if constexpr (kSplitP<T>) {
-              const __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
-              const uint32_t hb = *reinterpret_cast<const uint32_t *>(&hv);
-              hi[e] = hb;
-              const float2 r = f2unpack(fsub2(
-                  pxy, f2pack(__uint_as_float(hb << 16), __uint_as_float(hb & 0xffff0000u))));
-              lo[e] = pack2<T>(r.x, r.y);
-            } else {
-              hi[e] = pack2<T>(x, y);
+            for (int e = 0; e < 16; ++e) {
+              const uint64_t t2 =
+                  ffma2(f2pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2, nm2);
+              const float2 t = f2unpack(t2);
+              const float x = ex2(t.x), y = ex2(t.y);
+              const uint64_t pxy = f2pack(x, y);
+              rs2[e & 1] = fadd2(rs2[e & 1], pxy);
+              if constexpr (kSplitP<T>) {
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
+                const uint32_t hb = *reinterpret_cast<const uint32_t *>(&hv);
+                hi[e] = hb;
+                const float2 r = f2unpack(fsub2(
+                    pxy, f2pack(__uint_as_float(hb << 16), __uint_as_float(hb & 0xffff0000u))));
+                lo[e] = pack2<T>(r.x, r.y);
+              } else {
+                hi[e] = pack2<T>(x, y);
+              }
             }
+            tc::tmem_st16u(s_addr + 64 * hh + 32 * g, hi);
+            if constexpr (kSplitP<T>) tc::tmem_st16u(s_addr + 64 * hh + 32 * g + 16, lo);
           }
-          tc::tmem_st16u(s_addr + 32 * g, hi);
-          if constexpr (kSplitP<T>) tc::tmem_st16u(s_addr + 32 * g + 16, lo);
         }
         turn_pass(c, rs2[0], rs2[1]);
         const float2 ra = f2unpack(rs2[0]), rb = f2unpack(rs2[1]);
@@ -684,11 +716,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_wait_st();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c & 1]));
+        if (lane == 0) tc::mbar_arrive(smem_u32(&p_full[t][c % kBufs]));
       }
       if (ok && !idle) {
         const bool wt =
-            mbar_wait_bounded(smem_u32(&pv_done[t][(nch - 1) & 1]), ((nch - 1) >> 1) & 1);
+            mbar_wait_bounded(smem_u32(&pv_done[t][(nch - 1) % kBufs]), ((nch - 1) / kBufs) & 1);
         ok = __all_sync(kFull, wt && !s_abort);
       }
       if (ok && !idle) {
@@ -705,7 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              pk[e] = pack2<T>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+              pk[e] = pack2<T>(__uint_as_float(o[2 * e]) * inv,
+                               __uint_as_float(o[2 * e + 1]) * inv);
             uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * q);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -726,19 +759,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---- host side -----------------------------------------------------------------
+// `stages` is the K / V ring depth in chunks; it also chooses the chunk:
+// head_dim 128: 3-5 stages of 128-key chunks, 6 or 8 of 64-key ones;
+// head_dim 64: 4-8 stages of 128-key chunks, 12 or 16 of 64-key ones.
+// 64-key chunks are the default: with 128-key ones each tile's softmax also
+// waits for its own P.V and next S (one S buffer), and the Llama-3-8B-shaped
+// prefill (head_dim 128) ran at 521-537 TFLOP/s against 603-617.
 constexpr int kDefaultStages128 = 8, kDefaultStages64 = 12;
 
-template <typename T, int D, int NS>
+template <typename T, int D, int NS, int CK>
 cudaError_t launch_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                      const PrefillParams &p, cudaStream_t stream) {
-  using G = Geom<D, NS>;
+  using G = Geom<D, NS, CK>;
   const size_t smem = G::kBytes + 1024;  // + alignment slack
-  const cudaError_t e = cudaFuncSetAttribute(
-      prefill_kernel<T, D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, D, NS, CK>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // one CTA per (sequence, row pair, KV head) unit, longest units first
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.pairs) * p.batch * p.num_kv_heads));
-  prefill_kernel<T, D, NS><<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, p);
+  prefill_kernel<T, D, NS, CK><<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
 
@@ -748,17 +788,21 @@ using LaunchFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const
 template <typename T> LaunchFn pick_t(int D, int stages) {
   if (D == 128) {
     switch (stages == 0 ? kDefaultStages128 : stages) {
-      case 4: return launch_t<T, 128, 4>;
-      case 6: return launch_t<T, 128, 6>;
-      case 8: return launch_t<T, 128, 8>;
+      case 3: return launch_t<T, 128, 3, 128>;
+      case 4: return launch_t<T, 128, 4, 128>;
+      case 5: return launch_t<T, 128, 5, 128>;
+      case 6: return launch_t<T, 128, 6, 64>;
+      case 8: return launch_t<T, 128, 8, 64>;
       default: return nullptr;
     }
   }
   if (D == 64) {
     switch (stages == 0 ? kDefaultStages64 : stages) {
-      case 8: return launch_t<T, 64, 8>;
-      case 12: return launch_t<T, 64, 12>;
-      case 16: return launch_t<T, 64, 16>;
+      case 4: return launch_t<T, 64, 4, 128>;
+      case 6: return launch_t<T, 64, 6, 128>;
+      case 8: return launch_t<T, 64, 8, 128>;
+      case 12: return launch_t<T, 64, 12, 64>;
+      case 16: return launch_t<T, 64, 16, 64>;
       default: return nullptr;
     }
   }

@@ -102,7 +102,8 @@ def test_prefill_after_a_cached_prefix(prefix):
     check(W.make_prefill_batch(wl), rows_per_seq=512, what=f"prefix {prefix}")
 
 
-@pytest.mark.parametrize("D,stages", [(128, 4), (128, 6), (128, 8), (64, 8), (64, 12), (64, 16)])
+@pytest.mark.parametrize("D,stages", [(128, 3), (128, 4), (128, 5), (128, 6), (128, 8), (64, 4),
+                                      (64, 8), (64, 12), (64, 16)])
 def test_prefill_ring_depths(D, stages):
     wl = W.PrefillWorkload("stages", 3, 8, 2, D, "bf16", chunk_lens=[64, 300, 513],
                            prefix_lens=[700, 0, 260], seed=14)
