@@ -282,6 +282,44 @@ PKV_API pkv_status pkv_append_attention(
     const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
 
 /*
+ * pkv_host_step_staging_size -- device bytes pkv_append_attention_host needs
+ * for its staging buffer: room for the step's inputs (q, k_new, v_new,
+ * block_table, context_lens), its output and the attention workspace, each
+ * at a 256-byte boundary.  Enqueues nothing.  dtype F32/BF16/F16.
+ */
+PKV_API pkv_status pkv_host_step_staging_size(int batch, int num_queries, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              int max_blocks_per_seq, int max_context_len,
+                                              pkv_dtype dtype, const pkv_options *options,
+                                              size_t *bytes);
+
+/*
+ * pkv_append_attention_host -- one decode (or verify) step with the inputs
+ * and the output in HOST memory: q_host, k_new_host, v_new_host,
+ * block_table_host and context_lens_host (same layouts as for
+ * pkv_append_attention) are copied into `staging`, one host-to-device copy
+ * each; pkv_append_attention runs on those copies (the caches k_cache /
+ * v_cache are device memory, written in place); out is copied back into
+ * out_host.  All of it is enqueued on `stream` in that order, and the call
+ * returns without waiting: the caller synchronises the stream before it
+ * reads out_host or rewrites the host inputs.  Page-locked (pinned) host
+ * buffers make the copies asynchronous.
+ *
+ *   staging : device, 256-byte aligned, >= pkv_host_step_staging_size()
+ *             bytes (PKV_ERR_WORKSPACE otherwise); owned by the caller and
+ *             in use until the stream has passed this step
+ * A copy that cannot be enqueued returns PKV_ERR_CUDA (the copies enqueued
+ * before it stay enqueued).  Other errors as for pkv_append_attention.
+ */
+PKV_API pkv_status pkv_append_attention_host(
+    void *out_host, const void *q_host, const void *k_new_host, const void *v_new_host,
+    void *k_cache, void *v_cache, const int32_t *block_table_host, int max_blocks_per_seq,
+    const int32_t *context_lens_host, int max_context_len, int batch, int num_queries,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+    float scale, pkv_dtype dtype, void *staging, size_t staging_bytes,
+    const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
+
+/*
  * pkv_tree_verify_attention -- verification of a candidate tree (Medusa):
  * "Inference part 2", section "Medusa": the candidates of a tree are
  * verified in one pass with tree attention, a mask that lets each candidate

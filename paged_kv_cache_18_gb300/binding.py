@@ -37,7 +37,8 @@ EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_
             "pkv_paged_attention_fp8", "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_add_sequence",
             "pkv_bm_append", "pkv_bm_fork", "pkv_bm_free", "pkv_bm_sequence",
             "pkv_bm_block_table", "pkv_bm_stats", "pkv_bm_block_info", "pkv_bm_hash",
-            "pkv_copy_blocks", "pkv_paged_prefill_attention", "pkv_check_bounded_wait")
+            "pkv_copy_blocks", "pkv_paged_prefill_attention", "pkv_check_bounded_wait",
+            "pkv_host_step_staging_size", "pkv_append_attention_host")
 
 
 class PkvError(RuntimeError):
@@ -109,6 +110,11 @@ def lib() -> ctypes.CDLL:
             L.pkv_append_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
                                                i32, i32, i32, i32, i32, i64, f32, i32, vp, sz,
                                                opt, vp, vp]
+            L.pkv_host_step_staging_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
+                                                     i32, opt, ctypes.POINTER(sz)]
+            L.pkv_append_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
+                                                    i32, i32, i32, i32, i32, i32, i64, f32, i32,
+                                                    vp, sz, opt, vp, vp]
             L.pkv_tree_verify_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                                     i32, i32, i32, i32, i64, f32, i32, vp, i64,
                                                     vp, sz, opt, vp, vp]
@@ -373,6 +379,59 @@ def append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
         v_cache.data_ptr(), block_table.data_ptr(), block_table.shape[1], context_lens.data_ptr(),
         max_context_len, B, Q, Hq, Hkv, D, bs, NB, float(scale), _DTYPE[q.dtype], ws_ptr,
         ws_bytes, _opts(kernel, split_blocks, stages), _err_ptr(error_word), _stream(q)))
+    return out
+
+
+def host_step_staging_size(batch: int, num_queries: int, num_heads: int, num_kv_heads: int,
+                           head_dim: int, max_blocks_per_seq: int, max_context_len: int,
+                           dtype: torch.dtype, block_size: int = 16, kernel: int = 0,
+                           split_blocks: int = 0, stages: int = 0) -> int:
+    """Device staging bytes of append_attention_host (pkv_host_step_staging_size)."""
+    n = ctypes.c_size_t(0)
+    _check("pkv_host_step_staging_size", lib().pkv_host_step_staging_size(
+        batch, num_queries, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+        max_context_len, _DTYPE[dtype], _opts(kernel, split_blocks, stages), ctypes.byref(n)))
+    return int(n.value)
+
+
+def append_attention_host(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                          k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          block_table: torch.Tensor, context_lens: torch.Tensor,
+                          out: torch.Tensor, staging: torch.Tensor, max_context_len: int,
+                          scale: Optional[float] = None, kernel: int = 0, split_blocks: int = 0,
+                          stages: int = 0, error_word: Optional[torch.Tensor] = None
+                          ) -> torch.Tensor:
+    """One step with host inputs and output (pkv_append_attention_host).
+
+    q, k_new, v_new, block_table, context_lens and out are CPU tensors in the
+    layouts of append_attention (pinned memory makes the copies asynchronous);
+    the caches and ``staging`` (uint8, host_step_staging_size bytes) live on
+    the GPU.  The copies in, the fused append + attention and the copy of the
+    output into ``out`` are enqueued on the caches' current stream; ``out``
+    holds the result once that stream has been synchronised."""
+    NB, Hkv, bs, D = _cache_args(k_cache, v_cache)
+    q4 = q if q.dim() == 4 else q.unsqueeze(1)
+    B, Q, Hq, _ = q4.shape
+    host = (q, k_new, v_new, block_table, context_lens, out)
+    _need(not any(t.is_cuda for t in host), "q, k_new, v_new, block_table, context_lens and "
+          "out must be host tensors")
+    _need(all(t.is_contiguous() for t in host), "contiguity")
+    _need(k_new.numel() == B * Q * Hkv * D and v_new.numel() == k_new.numel(),
+          "k_new/v_new [B, Q, Hkv, D]")
+    _need(k_new.dtype == v_new.dtype == q.dtype == out.dtype == k_cache.dtype, "dtype mismatch")
+    _need(q.shape[-1] == D and out.shape == q.shape, "q/out")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2
+          and block_table.shape[0] == B, "block_table int32 [batch, max_blocks_per_seq]")
+    _need(context_lens.dtype == torch.int32 and context_lens.shape == (B,), "context_lens")
+    _need(staging.is_cuda and staging.device == k_cache.device, "staging must be on the caches' GPU")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    _check("pkv_append_attention_host", lib().pkv_append_attention_host(
+        out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), block_table.data_ptr(), block_table.shape[1],
+        context_lens.data_ptr(), max_context_len, B, Q, Hq, Hkv, D, bs, NB, float(scale),
+        _DTYPE[q.dtype], staging.data_ptr(), staging.numel() * staging.element_size(),
+        _opts(kernel, split_blocks, stages), _err_ptr(error_word), _stream(k_cache)))
     return out
 
 

@@ -2,7 +2,8 @@
 // planner, tensor-map encoding and dispatch to the kernel families.
 //
 // Nothing here allocates, frees or synchronises (except pkv_read_error_word,
-// which documents that it does); every launch goes to the caller's stream.
+// which documents that it does); every launch, and every host <-> device copy
+// of pkv_append_attention_host, goes to the caller's stream.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -370,7 +371,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
                          const pkv_options *opt, int32_t *error_word, cudaStream_t stream,
                          const void *k_new = nullptr, const void *v_new = nullptr,
                          const uint64_t *tree_mask = nullptr, int64_t mask_stride = 0,
-                         float k_scale = 1.f, float v_scale = 1.f) {
+                         float k_scale = 1.f, float v_scale = 1.f, bool check_only = false) {
   pkv_status st = check_shape(s);
   if (st != PKV_OK) return st;
   if (k_new && s.dtype == PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
@@ -398,6 +399,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
     if (!workspace || !aligned(workspace, 16) || workspace_bytes < pl.workspace_bytes)
       return PKV_ERR_WORKSPACE;
   }
+  if (check_only) return PKV_OK;  // every check of a call, nothing enqueued
 
   AttnParams p{};
   p.out = out;
@@ -727,6 +729,122 @@ pkv_status pkv_append_attention(void *out, const void *q, const void *k_new, con
   return run_attention(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, s,
                        num_blocks, scale, workspace, workspace_bytes, options, error_word,
                        reinterpret_cast<cudaStream_t>(stream), k_new, v_new);
+}
+
+namespace {
+// The staging buffer of a host-buffer step, in this order, each piece at a
+// 256-byte boundary: q, k_new, v_new, block_table, context_lens, out, then
+// the attention workspace.
+struct Staging {
+  size_t q, k_new, v_new, table, lens, out, ws, total;
+};
+size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+pkv_status staging_layout(int batch, int num_queries, int num_heads, int num_kv_heads,
+                          int head_dim, int block_size, int max_blocks_per_seq,
+                          int max_context_len, pkv_dtype dtype, const pkv_options *options,
+                          Staging *st) {
+  if (!valid_dtype(dtype) || batch < 0 || num_queries < 1 || num_heads < 1 ||
+      num_kv_heads < 1 || head_dim < 1 || max_blocks_per_seq < 1)
+    return PKV_ERR_INVALID_ARG;
+  size_t ws = 0;
+  const pkv_status s = pkv_attention_workspace_size(batch, num_queries, num_heads, num_kv_heads,
+                                                    head_dim, block_size, max_context_len, dtype,
+                                                    options, &ws);
+  if (s != PKV_OK) return s;
+  const size_t rows = static_cast<size_t>(batch) * num_queries;
+  const size_t q = rows * num_heads * head_dim * elt_bytes(dtype);
+  const size_t kv = rows * num_kv_heads * head_dim * elt_bytes(dtype);
+  size_t at = 0;
+  auto take = [&](size_t n) {
+    const size_t here = at;
+    at += round256(n);
+    return here;
+  };
+  st->q = take(q);
+  st->k_new = take(kv);
+  st->v_new = take(kv);
+  st->table = take(static_cast<size_t>(batch) * max_blocks_per_seq * sizeof(int32_t));
+  st->lens = take(static_cast<size_t>(batch) * sizeof(int32_t));
+  st->out = take(q);
+  st->ws = take(ws);
+  st->total = at;
+  return PKV_OK;
+}
+}  // namespace
+
+pkv_status pkv_host_step_staging_size(int batch, int num_queries, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int max_blocks_per_seq, int max_context_len,
+                                      pkv_dtype dtype, const pkv_options *options,
+                                      size_t *bytes) {
+  if (!bytes) return PKV_ERR_INVALID_ARG;
+  Staging st{};
+  const pkv_status s = staging_layout(batch, num_queries, num_heads, num_kv_heads, head_dim,
+                                      block_size, max_blocks_per_seq, max_context_len, dtype,
+                                      options, &st);
+  if (s == PKV_OK) *bytes = st.total;
+  return s;
+}
+
+pkv_status pkv_append_attention_host(void *out_host, const void *q_host, const void *k_new_host,
+                                     const void *v_new_host, void *k_cache, void *v_cache,
+                                     const int32_t *block_table_host, int max_blocks_per_seq,
+                                     const int32_t *context_lens_host, int max_context_len,
+                                     int batch, int num_queries, int num_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int64_t num_blocks,
+                                     float scale, pkv_dtype dtype, void *staging,
+                                     size_t staging_bytes, const pkv_options *options,
+                                     int32_t *error_word, pkv_stream_t stream) {
+  if (!valid_dtype(dtype) || batch < 0 || num_queries < 1 || max_blocks_per_seq < 1)
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!out_host || !q_host || !k_new_host || !v_new_host || !block_table_host ||
+      !context_lens_host)
+    return PKV_ERR_INVALID_ARG;
+  if (!staging || !aligned(staging, 256)) return PKV_ERR_WORKSPACE;
+  Staging st{};
+  pkv_status s = staging_layout(batch, num_queries, num_heads, num_kv_heads, head_dim,
+                                block_size, max_blocks_per_seq, max_context_len, dtype, options,
+                                &st);
+  if (s != PKV_OK) return s;
+  if (staging_bytes < st.total) return PKV_ERR_WORKSPACE;
+  uint8_t *base = static_cast<uint8_t *>(staging);
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const Shape shape = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim,
+                                 block_size, max_context_len, dtype);
+  // Every check of the launch, on the staged pointers, before anything is enqueued.
+  auto attend = [&](bool check_only) {
+    return run_attention(base + st.out, base + st.q, k_cache, v_cache,
+                         reinterpret_cast<const int32_t *>(base + st.table), max_blocks_per_seq,
+                         reinterpret_cast<const int32_t *>(base + st.lens), shape, num_blocks,
+                         scale, base + st.ws, staging_bytes - st.ws, options, error_word, cs,
+                         base + st.k_new, base + st.v_new, nullptr, 0, 1.f, 1.f, check_only);
+  };
+  s = attend(true);
+  if (s != PKV_OK) return s;
+  const size_t rows = static_cast<size_t>(batch) * num_queries;
+  const size_t q_bytes = rows * num_heads * head_dim * elt_bytes(dtype);
+  const size_t kv_bytes = rows * num_kv_heads * head_dim * elt_bytes(dtype);
+  // The inputs, one copy each (host to device), in stream order before the launch.
+  const struct {
+    size_t off;
+    const void *src;
+    size_t n;
+  } in[] = {{st.q, q_host, q_bytes},
+            {st.k_new, k_new_host, kv_bytes},
+            {st.v_new, v_new_host, kv_bytes},
+            {st.table, block_table_host,
+             static_cast<size_t>(batch) * max_blocks_per_seq * sizeof(int32_t)},
+            {st.lens, context_lens_host, static_cast<size_t>(batch) * sizeof(int32_t)}};
+  for (const auto &c : in)
+    if (cudaMemcpyAsync(base + c.off, c.src, c.n, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  s = attend(false);
+  if (s != PKV_OK) return s;
+  if (cudaMemcpyAsync(out_host, base + st.out, q_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 pkv_status pkv_tree_verify_attention(void *out, const void *q, const void *k_cache,

@@ -166,3 +166,34 @@ def test_bounded_wait_check_validates_its_arguments(L):
     assert L.pkv_check_bounded_wait(16, 0, None, None) == 1
     assert L.pkv_check_bounded_wait(16, 10**8, None, None) == 1
     assert L.pkv_check_bounded_wait(18, 100, None, None) == 5   # misaligned error word
+
+
+def host_step(L, **kw):
+    a = dict(out=16, q=16, kn=16, vn=16, k=256, v=256, table=16, max_blocks=8, lens=16,
+             max_ctx=100, B=2, Q=1, Hq=8, Hkv=2, D=128, bs=16, NB=10, scale=0.1, dtype=1,
+             staging=256, staging_bytes=1 << 20, opt=None, err=None, stream=None)
+    a.update(kw)
+    return L.pkv_append_attention_host(
+        a["out"], a["q"], a["kn"], a["vn"], a["k"], a["v"], a["table"], a["max_blocks"],
+        a["lens"], a["max_ctx"], a["B"], a["Q"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
+        a["scale"], a["dtype"], a["staging"], a["staging_bytes"], a["opt"], a["err"],
+        a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0, q=None, out=None, staging=None), 0),        # nothing to do
+    (dict(q=None), 1), (dict(out=None), 1), (dict(kn=None), 1), (dict(table=None), 1),
+    (dict(lens=None), 1), (dict(Q=0), 1), (dict(B=-1), 1), (dict(max_blocks=0), 1),
+    (dict(dtype=3), 1),                                    # FP8 caches: not this call
+    (dict(staging=None), 3), (dict(staging=16), 3),        # staging missing / misaligned
+])
+def test_host_step_argument_errors(L, kw, status):
+    assert host_step(L, **kw) == status
+
+
+def test_host_step_staging_size_argument_errors(L):
+    f = L.pkv_host_step_staging_size
+    n = ctypes.c_size_t(0)
+    assert f(2, 1, 8, 2, 128, 16, 8, 100, 1, None, None) == 1             # no result pointer
+    assert f(2, 1, 8, 2, 128, 16, 8, 100, 3, None, ctypes.byref(n)) == 1  # FP8
+    assert f(2, 1, 8, 2, 128, 16, 0, 100, 1, None, ctypes.byref(n)) == 1  # no table width
