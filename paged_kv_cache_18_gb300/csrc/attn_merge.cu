@@ -16,6 +16,9 @@
 // loads are spread: warp w takes splits w, w + 4, ..., four at a time, which
 // keeps 16 partial vectors in flight per row; the warps meet in shared
 // memory at the end.
+// The kernel is a programmatic dependent of the attention kernel: it may be
+// scheduled while that kernel still runs (which hides its launch), reads
+// only the call's inputs before pdl_wait, and the partials after it.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -39,6 +42,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   __shared__ float red_sum[kMergeWarps];
   __shared__ float red_acc[kMergeWarps][D];
 
+  pdl_wait();  // the attention kernel's partials are complete and visible
   const float *lse = p.part_lse + row * p.num_splits;
   float M = -INFINITY;
   for (int s = threadIdx.x; s < ns; s += kMergeWarps * 32) M = fmaxf(M, lse[s]);
@@ -101,14 +105,25 @@ cudaError_t merge_t(int D, const AttnParams &p, cudaStream_t stream) {
   const int64_t nrows = static_cast<int64_t>(p.batch) * p.num_queries * p.num_heads;
   if (nrows == 0) return cudaSuccess;
   if (nrows > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(nrows));
+  void (*kernel)(const AttnParams);
   switch (D) {
-    case 64: attn_merge_kernel<T, 64><<<grid, kMergeWarps * 32, 0, stream>>>(p); break;
-    case 128: attn_merge_kernel<T, 128><<<grid, kMergeWarps * 32, 0, stream>>>(p); break;
-    case 256: attn_merge_kernel<T, 256><<<grid, kMergeWarps * 32, 0, stream>>>(p); break;
+    case 64: kernel = attn_merge_kernel<T, 64>; break;
+    case 128: kernel = attn_merge_kernel<T, 128>; break;
+    case 256: kernel = attn_merge_kernel<T, 256>; break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  // launched as a programmatic dependent of the attention kernel before it
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nrows));
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace

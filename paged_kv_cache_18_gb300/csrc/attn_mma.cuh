@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   static_assert(NS >= KB, "an iteration's blocks must all be in flight at once");
+  pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for this grid
   constexpr bool FP8 = std::is_same<TC, E4M3>::value;
   using TM = typename MmaType<T, TC>::type;
   using G = MmaGeom<D, Elt<TC>::bytes>;

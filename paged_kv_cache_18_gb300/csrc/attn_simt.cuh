@@ -89,6 +89,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // TQ: element type of q and out; TC: element type of the caches.
 template <typename TQ, typename TC, int D, int R, int W, int NS>
 __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
+  pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for this grid
   constexpr int ELT = Elt<TC>::bytes;
   constexpr int RB = D * ELT;             // bytes of one row
   constexpr int TILE = kBlockSize * RB;   // bytes of one (block, kv head) tile

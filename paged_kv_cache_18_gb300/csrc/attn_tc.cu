@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap vmap, const AttnParams p, int num_items) {
   using G = TcGeom<D, NC, NS, PB>;
   constexpr int NCW = NC / 2;  // query columns of one softmax warp
+  pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for this grid
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

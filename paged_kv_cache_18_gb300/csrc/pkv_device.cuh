@@ -111,6 +111,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  A kernel that calls pdl_launch_dependents
+// lets the next kernel of its stream, when that one is launched with
+// programmatic stream serialisation, be scheduled before it finishes; the
+// dependent kernel calls pdl_wait before it reads anything this kernel
+// writes (the wait returns once this grid has completed and its memory
+// operations are visible).  Both are no-ops without such a pairing.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }

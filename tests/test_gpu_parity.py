@@ -180,24 +180,29 @@ def test_kv_append_skips_padding_and_reports_bad_slots():
         np.testing.assert_array_equal(after[s // 16, :, s % 16], b.k_new[t])
 
 
-def test_cuda_graph_replay():
+@pytest.mark.parametrize("merge", [0, 1, 2])
+def test_cuda_graph_replay(merge):
+    """Capture and replay; merge 1 is the last CTA's in-kernel merge, 2 the
+    merge kernel launched as a programmatic dependent of the attention."""
     wl = W.Workload("graph", 8, 32, 8, 128, "bf16", len_range=(100, 3000), seed=12)
     b = W.make_batch(wl)
     d = DeviceBatch(b)
     import paged_kv_cache_18_gb300 as pkv
-    ws_bytes = pkv.workspace_size(8, 1, 32, 8, 128, b.max_context_len, torch.bfloat16)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
-    out = torch.empty(8, 1, 32, 128, dtype=torch.bfloat16, device="cuda")
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        d.append()
-        d.attend(out=out[:, 0], workspace=ws)   # warm-up (plans, attributes)
-    torch.cuda.current_stream().wait_stream(s)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        d.append()
-        d.attend(out=out[:, 0], workspace=ws)
+    with tuning(merge=merge):
+        ws_bytes = pkv.workspace_size(8, 1, 32, 8, 128, b.max_context_len, torch.bfloat16)
+        assert pkv.plan(8, 1, 32, 8, 128, b.max_context_len, torch.bfloat16)["num_splits"] > 1
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        out = torch.empty(8, 1, 32, 128, dtype=torch.bfloat16, device="cuda")
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            d.append()
+            d.attend(out=out[:, 0], workspace=ws)   # warm-up (plans, attributes)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            d.append()
+            d.attend(out=out[:, 0], workspace=ws)
     ref = oracle_after_append(b)
     for _ in range(3):  # replays reuse the captured call's merge counters
         out.zero_()
