@@ -12,10 +12,13 @@
 // A split with no visible row has lse_s = -inf and weight 0; a row with no
 // visible row at all gets zeros.
 //
-// One CTA per output row.  Long contexts give rows of many splits, so the
-// loads are spread: warp w takes splits w, w + 4, ..., four at a time, which
-// keeps 16 partial vectors in flight per row; the warps meet in shared
-// memory at the end.
+// One CTA per output row, four warps.  Warp w merges splits w, w + 4, ...
+// on its own, eight at a time: the log-sum-exps and partial vectors of a
+// group are loaded together (one memory round trip per group; up to 32
+// splits are one group per warp), against the warp's own maximum M_w:
+//   acc_w = sum_s 2^(lse_s - M_w) O_s,   l_w = sum_s 2^(lse_s - M_w).
+// The warps then meet in shared memory: with M = max_w M_w,
+//   out = sum_w 2^(M_w - M) acc_w / sum_w 2^(M_w - M) l_w.
 // The kernel is a programmatic dependent of the attention kernel: it may be
 // scheduled while that kernel still runs (which hides its launch), reads
 // only the call's inputs before pdl_wait, and the partials after it.
@@ -26,7 +29,7 @@ namespace pkv {
 namespace {
 
 constexpr int kMergeWarps = 4;
-constexpr int kMergeUnroll = 4;
+constexpr int kMergeUnroll = 8;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const AttnParams p) {
@@ -44,58 +47,67 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
 
   pdl_wait();  // the attention kernel's partials are complete and visible
   const float *lse = p.part_lse + row * p.num_splits;
-  float M = -INFINITY;
-  for (int s = threadIdx.x; s < ns; s += kMergeWarps * 32) M = fmaxf(M, lse[s]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-  if (lane == 0) red_max[warp] = M;
-  __syncthreads();
-#pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, red_max[w]);
-
+  const float *po = p.part_o + row * p.num_splits * D + lane * PER;
+  float Mw = -INFINITY, wsum = 0.f;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    const float *po = p.part_o + row * p.num_splits * D + lane * PER;
-    for (int s0 = warp; s0 < ns; s0 += kMergeWarps * kMergeUnroll) {
-      float w[kMergeUnroll];
-      float v[kMergeUnroll][PER];
+  for (int s0 = warp; s0 < ns; s0 += kMergeWarps * kMergeUnroll) {
+    float ls[kMergeUnroll];
+    float v[kMergeUnroll][PER];
 #pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) {
-        const int s = s0 + u * kMergeWarps;
-        const bool ok = s < ns;
-        w[u] = ok ? ex2(lse[ok ? s : 0] - M) : 0.f;
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const int s = s0 + u * kMergeWarps;
+      const bool ok = s < ns;
+      ls[u] = ok ? lse[s] : -INFINITY;
 #pragma unroll
-        for (int e = 0; e < PER; e += 2) {
-          const float2 x = ok ? *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(s) * D + e)
-                              : make_float2(0.f, 0.f);
-          v[u][e] = x.x;
-          v[u][e + 1] = x.y;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kMergeUnroll; ++u) {
-        wsum += w[u];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = fmaf(w[u], v[u][e], acc[e]);
+      for (int e = 0; e < PER; e += 2) {
+        const float2 x = ok ? *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(s) * D + e)
+                            : make_float2(0.f, 0.f);
+        v[u][e] = x.x;
+        v[u][e + 1] = x.y;
       }
     }
+    float mg = Mw;
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) mg = fmaxf(mg, ls[u]);
+    if (mg == -INFINITY) continue;  // nothing visible in these splits yet
+    const float r = ex2(Mw - mg);   // rescale what the warp holds (0 while it holds nothing)
+    wsum *= r;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] *= r;
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const float w = ex2(ls[u] - mg);  // 0 for empty or absent splits
+      wsum += w;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+    }
+    Mw = mg;
   }
-  if (lane == 0) red_sum[warp] = wsum;
+  if (lane == 0) {
+    red_max[warp] = Mw;
+    red_sum[warp] = wsum;
+  }
 #pragma unroll
   for (int e = 0; e < PER; ++e) red_acc[warp][lane * PER + e] = acc[e];
   __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, red_max[w]);
+  float f[kMergeWarps];
   float total = 0.f;
 #pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) total += red_sum[w];
+  for (int w = 0; w < kMergeWarps; ++w) {
+    f[w] = red_max[w] == -INFINITY ? 0.f : ex2(red_max[w] - M);
+    total += f[w] * red_sum[w];
+  }
   const float inv = total > 0.f ? p.out_scale / total : 0.f;
   T *dst = reinterpret_cast<T *>(p.out) + row * D;
   for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) {
     float x = 0.f;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) x += red_acc[w][d];
+    for (int w = 0; w < kMergeWarps; ++w) x = fmaf(f[w], red_acc[w][d], x);
     dst[d] = from_float<T>(x * inv);
   }
 }

@@ -25,7 +25,9 @@ constexpr int kMaxDevices = 64;
 constexpr int kMinSplitBlocks = 16;     // 4 blocks per warp: fills the pipeline
 constexpr int kMaxUnitBytes = 64 * 8192;  // longest split, in K+V bytes of one KV head
                                           // (64 blocks of a 16-bit, 128-dim cache)
-constexpr int kTargetWaves = 4;         // CTAs ~ this many times the resident slots
+constexpr int kTargetWaves = 3;         // CTAs ~ this many times the resident slots
+                                        // (the 20-row verify tile: 0.641 of the HBM
+                                        // peak at 4 waves, 0.673 at 3)
 constexpr int kMaxSplits = 32;          // per sequence: each split adds merge work
 constexpr size_t kUsableSmemPerSm = 228 * 1024;
 
