@@ -388,6 +388,57 @@ PKV_API pkv_status pkv_paged_attention_fp8(
     const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
 
 /*
+ * Multi-head latent attention (MLA) decode.  "Inference part 1", section
+ * "Smaller KV caches: MQA, GQA and MLA": each token's keys and values are
+ * compressed into one latent vector c and only c is cached; with the key
+ * and value up-projections absorbed into the query and output projections,
+ * attention runs directly over the cached latents, which act as both keys
+ * and values (multi-query attention with one large shared head).  A small
+ * separate key part carries the rotary position ("KV cache, prefill va
+ * decode", section 04: d_c = 512 latent and d_h^R = 64 rotary values per
+ * token and layer).
+ *
+ * Cache: one tensor [num_blocks, block_size, latent_dim + rope_dim] elt,
+ * row = [c ; k_rope], paged through the block table like the other caches.
+ *   q   : [batch, num_heads, latent_dim + rope_dim] elt, device: the
+ *         absorbed query [q_c ; q_r] of each head
+ *   out : [batch, num_heads, latent_dim] elt, device: the latent output
+ *         sum_i softmax_i(scale q_h . row_i) c_i (the caller applies the
+ *         value up-projection and the output projection)
+ * Supported: latent_dim 512, rope_dim 0 or 64, num_heads a multiple of 16,
+ * block_size 16, dtype BF16 / F16 (PKV_ERR_UNSUPPORTED otherwise).  options:
+ * only `stages` (3..5, 0 = 4) and `split_blocks` apply; the other fields
+ * must be 0.  Other arguments, errors and the workspace (the split-K
+ * partials, 256-byte aligned) as for pkv_paged_decode_attention; context
+ * lengths above max_context_len are clamped and recorded, bad block ids
+ * recorded and their rows ignored.
+ */
+PKV_API pkv_status pkv_mla_workspace_size(int batch, int num_heads, int latent_dim,
+                                          int rope_dim, int block_size, int max_context_len,
+                                          pkv_dtype dtype, const pkv_options *options,
+                                          size_t *bytes);
+
+PKV_API pkv_status pkv_mla_decode_attention(
+    void *out, const void *q, const void *ckv_cache, const int32_t *block_table,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int batch,
+    int num_heads, int latent_dim, int rope_dim, int block_size, int64_t num_blocks,
+    float scale, pkv_dtype dtype, void *workspace, size_t workspace_bytes,
+    const pkv_options *options, int32_t *error_word, pkv_stream_t stream);
+
+/*
+ * pkv_mla_append -- write new tokens' latent rows [c ; k_rope] into their
+ * slots of the latent cache (the same slot rule and error behaviour as
+ * pkv_kv_append, with one cache and no heads).
+ *   ckv_new   : [num_tokens, width] elt, device
+ *   ckv_cache : [num_blocks, block_size, width] elt, device, written in place
+ * width * sizeof(elt) must be a multiple of 16 and pointers 16-byte aligned.
+ */
+PKV_API pkv_status pkv_mla_append(const void *ckv_new, void *ckv_cache,
+                                  const int64_t *slot_mapping, int64_t num_tokens, int width,
+                                  int block_size, int64_t num_blocks, pkv_dtype dtype,
+                                  int32_t *error_word, pkv_stream_t stream);
+
+/*
  * pkv_paged_prefill_attention -- chunked prefill: each sequence brings a
  * chunk of new query rows whose K and V have already been appended
  * (pkv_kv_append), and every row attends to the cache up to itself

@@ -38,7 +38,8 @@ EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_
             "pkv_bm_append", "pkv_bm_fork", "pkv_bm_free", "pkv_bm_sequence",
             "pkv_bm_block_table", "pkv_bm_stats", "pkv_bm_block_info", "pkv_bm_hash",
             "pkv_copy_blocks", "pkv_paged_prefill_attention", "pkv_check_bounded_wait",
-            "pkv_host_step_staging_size", "pkv_append_attention_host")
+            "pkv_host_step_staging_size", "pkv_append_attention_host",
+            "pkv_mla_workspace_size", "pkv_mla_decode_attention", "pkv_mla_append")
 
 
 class PkvError(RuntimeError):
@@ -115,6 +116,11 @@ def lib() -> ctypes.CDLL:
             L.pkv_append_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
                                                     i32, i32, i32, i32, i32, i32, i64, f32, i32,
                                                     vp, sz, opt, vp, vp]
+            L.pkv_mla_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, opt,
+                                                 ctypes.POINTER(sz)]
+            L.pkv_mla_decode_attention.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                                   i32, i32, i64, f32, i32, vp, sz, opt, vp, vp]
+            L.pkv_mla_append.argtypes = [vp, vp, vp, i64, i32, i32, i64, i32, vp, vp]
             L.pkv_tree_verify_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                                     i32, i32, i32, i32, i64, f32, i32, vp, i64,
                                                     vp, sz, opt, vp, vp]
@@ -432,6 +438,86 @@ def append_attention_host(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
         context_lens.data_ptr(), max_context_len, B, Q, Hq, Hkv, D, bs, NB, float(scale),
         _DTYPE[q.dtype], staging.data_ptr(), staging.numel() * staging.element_size(),
         _opts(kernel, split_blocks, stages), _err_ptr(error_word), _stream(k_cache)))
+    return out
+
+
+MLA_LATENT = 512
+
+
+def _mla_opts(stages: int, split_blocks: int):
+    if not (stages or split_blocks):
+        return None
+    return ctypes.byref(Options(0, split_blocks, stages, 0, 0, 0, 0, 0))
+
+
+def mla_workspace_size(batch: int, num_heads: int, rope_dim: int, max_context_len: int,
+                       dtype: torch.dtype, stages: int = 0, split_blocks: int = 0) -> int:
+    """Split-K workspace bytes of mla_decode_attention (pkv_mla_workspace_size)."""
+    n = ctypes.c_size_t(0)
+    _check("pkv_mla_workspace_size", lib().pkv_mla_workspace_size(
+        batch, num_heads, MLA_LATENT, rope_dim, 16, max_context_len, _DTYPE[dtype],
+        _mla_opts(stages, split_blocks), ctypes.byref(n)))
+    return int(n.value)
+
+
+def mla_append(ckv_new: torch.Tensor, ckv_cache: torch.Tensor, slot_mapping: torch.Tensor,
+               error_word: Optional[torch.Tensor] = None) -> None:
+    """Write latent rows ckv_new [T, W] into slots ``slot_mapping`` [T] (int64,
+    negative = skip) of the latent cache [NB, 16, W] (pkv_mla_append)."""
+    _need(ckv_cache.is_cuda and ckv_cache.dim() == 3 and ckv_cache.is_contiguous(),
+          "ckv_cache must be a contiguous CUDA [num_blocks, block_size, width] tensor")
+    NB, bs, W = ckv_cache.shape
+    T = ckv_new.shape[0]
+    _need(ckv_new.shape == (T, W) and ckv_new.dtype == ckv_cache.dtype
+          and ckv_new.is_contiguous(), "ckv_new [T, width] of the cache's dtype")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.shape == (T,)
+          and slot_mapping.is_cuda and slot_mapping.is_contiguous(), "slot_mapping int64 [T]")
+    _check("pkv_mla_append", lib().pkv_mla_append(
+        ckv_new.data_ptr(), ckv_cache.data_ptr(), slot_mapping.data_ptr(), T, W, bs, NB,
+        _DTYPE[ckv_cache.dtype], _err_ptr(error_word), _stream(ckv_cache)))
+
+
+def mla_decode_attention(q: torch.Tensor, ckv_cache: torch.Tensor, block_table: torch.Tensor,
+                         context_lens: torch.Tensor, scale: float,
+                         max_context_len: Optional[int] = None,
+                         out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, stages: int = 0,
+                         split_blocks: int = 0,
+                         error_word: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """MLA decode over the latent cache (pkv_mla_decode_attention).
+
+    q [B, H, 512 + r] (the absorbed query of each head, r = 0 or 64);
+    ckv_cache [NB, 16, 512 + r]; returns the latent output [B, H, 512]."""
+    _need(ckv_cache.is_cuda and ckv_cache.dim() == 3 and ckv_cache.is_contiguous()
+          and ckv_cache.dtype in _DTYPE, "ckv_cache must be a contiguous CUDA [NB, 16, W] tensor")
+    NB, bs, W = ckv_cache.shape
+    _need(q.is_cuda and q.dim() == 3 and q.shape[2] == W and q.dtype == ckv_cache.dtype
+          and q.is_contiguous(), "q [B, H, width] of the cache's dtype")
+    B, H, _ = q.shape
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2
+          and block_table.shape[0] == B and block_table.is_contiguous() and block_table.is_cuda,
+          "block_table must be a contiguous CUDA int32 [batch, max_blocks_per_seq]")
+    _need(context_lens.dtype == torch.int32 and context_lens.shape == (B,)
+          and context_lens.is_cuda and context_lens.is_contiguous(), "context_lens")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else 0  # device read
+    rope = W - MLA_LATENT
+    if out is None:
+        out = torch.empty(B, H, MLA_LATENT, dtype=q.dtype, device=q.device)
+    _need(out.shape == (B, H, MLA_LATENT) and out.dtype == q.dtype and out.is_contiguous(),
+          "out [B, H, 512]")
+    if B == 0:
+        return out
+    need = mla_workspace_size(B, H, rope, max_context_len, q.dtype, stages, split_blocks)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("pkv_mla_decode_attention", lib().pkv_mla_decode_attention(
+        out.data_ptr(), q.data_ptr(), ckv_cache.data_ptr(), block_table.data_ptr(),
+        block_table.shape[1], context_lens.data_ptr(), max_context_len, B, H, MLA_LATENT, rope,
+        bs, NB, float(scale), _DTYPE[q.dtype], ws_ptr, ws_bytes, _mla_opts(stages, split_blocks),
+        _err_ptr(error_word), _stream(q)))
     return out
 
 

@@ -20,6 +20,7 @@ LIB = os.path.join(PKG, "libpkv.so")
 
 SOURCES = ["pkv_api.cu", "kv_append.cu", "attn_merge.cu", "attn_simt.cu", "attn_simt_fp8.cu",
            "attn_mma.cu", "attn_mma_f16.cu", "attn_mma_fp8.cu", "attn_tc.cu", "attn_prefill.cu",
+           "attn_mla.cu",
            "block_manager.cpp"]  # .cpp: host code, passed to the host compiler by nvcc
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -13,9 +13,10 @@
 // visible row at all gets zeros.
 //
 // One CTA per output row, four warps.  Warp w merges splits w, w + 4, ...
-// on its own, eight at a time: the log-sum-exps and partial vectors of a
-// group are loaded together (one memory round trip per group; up to 32
-// splits are one group per warp), against the warp's own maximum M_w:
+// on its own, eight at a time (two for 512-wide rows): the log-sum-exps and
+// partial vectors of a group are loaded together (one memory round trip per
+// group; up to 32 splits are one group per warp), against the warp's own
+// maximum M_w:
 //   acc_w = sum_s 2^(lse_s - M_w) O_s,   l_w = sum_s 2^(lse_s - M_w).
 // The warps then meet in shared memory: with M = max_w M_w,
 //   out = sum_w 2^(M_w - M) acc_w / sum_w 2^(M_w - M) l_w.
@@ -29,11 +30,15 @@ namespace pkv {
 namespace {
 
 constexpr int kMergeWarps = 4;
-constexpr int kMergeUnroll = 8;
+
+// Splits a warp loads at once: eight (up to 32 splits in one round trip),
+// two for the 512-wide latent rows of MLA (register budget).
+template <int D> __host__ __device__ constexpr int merge_unroll() { return D <= 256 ? 8 : 2; }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const AttnParams p) {
-  constexpr int PER = D / 32;  // elements per lane: 2, 4 or 8
+  constexpr int PER = D / 32;  // elements per lane: 2, 4, 8 or 16
+  constexpr int kMergeUnroll = merge_unroll<D>();
   const int64_t row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = static_cast<int>(row / (static_cast<int64_t>(p.num_queries) * p.num_heads));
@@ -122,6 +127,7 @@ cudaError_t merge_t(int D, const AttnParams &p, cudaStream_t stream) {
     case 64: kernel = attn_merge_kernel<T, 64>; break;
     case 128: kernel = attn_merge_kernel<T, 128>; break;
     case 256: kernel = attn_merge_kernel<T, 256>; break;
+    case 512: kernel = attn_merge_kernel<T, 512>; break;
     default: return cudaErrorInvalidValue;
   }
   // launched as a programmatic dependent of the attention kernel before it

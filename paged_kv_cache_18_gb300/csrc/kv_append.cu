@@ -5,8 +5,9 @@
 // decode", section 05, "Block table").
 //
 // Pure data movement: one thread per 16-byte vector of a (token, kv head)
-// row, for K and V; the copy is bit-exact.  Negative slots are padding and
-// skipped; slots past the cache are skipped and reported in the error word.
+// row, for K and V (K only when no V cache is given: the single latent cache
+// of MLA); the copy is bit-exact.  Negative slots are padding and skipped;
+// slots past the cache are skipped and reported in the error word.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -38,7 +39,7 @@ __global__ void __launch_bounds__(256)
     const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * vec_per_row + v;
     const int64_t src = (t * num_kv_heads + h) * vec_per_row + v;
     k_cache[dst] = __ldg(k_new + src);
-    v_cache[dst] = __ldg(v_new + src);
+    if (v_cache != nullptr) v_cache[dst] = __ldg(v_new + src);
   }
 }
 

@@ -916,6 +916,179 @@ pkv_status pkv_paged_attention_fp8(void *out, const void *q, const void *k_cache
                        k_scale, v_scale);
 }
 
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// An MLA decode call's checked sizes and launch plan: split-K over the
+// latent rows with the rules of the other decode kernels (about kTargetWaves
+// waves of CTAs, >= kMinSplitBlocks blocks and <= kMaxSplits splits per
+// sequence), units being (sequence, 16 query heads).
+struct MlaPlan {
+  KernelInfo info;
+  int device = 0, sms = 0, ctas_per_sm = 0;
+  int split_blocks = 1, num_splits = 1;
+  size_t lse_off = 0, workspace = 0;
+};
+
+pkv_status mla_plan(int batch, int num_heads, int latent_dim, int rope_dim, int block_size,
+                    int max_context_len, pkv_dtype dtype, const pkv_options *opt, MlaPlan *pl) {
+  if (batch < 0 || num_heads < 1 || latent_dim < 1 || rope_dim < 0 || block_size < 1 ||
+      max_context_len < 0 || !valid_dtype(dtype))
+    return PKV_ERR_INVALID_ARG;
+  if (latent_dim != kMlaLatent || (rope_dim != 0 && rope_dim != 64) || dtype == PKV_F32 ||
+      block_size != kBlockSize || num_heads % kMlaHeadsPerCta != 0 || batch > 65535 ||
+      num_heads / kMlaHeadsPerCta > 65535)
+    return PKV_ERR_UNSUPPORTED;
+  if (opt && (opt->kernel != PKV_KERNEL_AUTO || opt->rows_per_cta != 0 || opt->merge != 0 ||
+              opt->warp_tiles != 0 || opt->blocks_per_iter != 0 || opt->persistent != 0))
+    return PKV_ERR_UNSUPPORTED;  // only stages and split_blocks apply here
+  if (!mla_kernel_info(dtype, rope_dim, opt ? opt->stages : 0, &pl->info))
+    return PKV_ERR_UNSUPPORTED;
+  if (current_sm_count(&pl->device, &pl->sms) != cudaSuccess) return PKV_ERR_CUDA;
+  if (prepare_kernel(pl->info, pl->device, &pl->ctas_per_sm) != cudaSuccess) return PKV_ERR_CUDA;
+  const int max_blocks = ceil_div(max_context_len, kBlockSize);
+  const int64_t units = static_cast<int64_t>(batch) * (num_heads / kMlaHeadsPerCta);
+  int sb = max_blocks;
+  if (opt && opt->split_blocks > 0) {
+    sb = opt->split_blocks;
+  } else if (units > 0 && max_blocks > kMinSplitBlocks) {
+    const int64_t slots = static_cast<int64_t>(pl->sms) * pl->ctas_per_sm;
+    const int64_t want = kTargetWaves * slots;
+    if (units < want) {
+      const int64_t splits = (want + units - 1) / units;
+      sb = std::max(kMinSplitBlocks, ceil_div(max_blocks, splits));
+      sb = std::max(sb, ceil_div(max_blocks, kMaxSplits));
+      // keep the split only if it shortens the wave-quantised schedule
+      const int64_t ns = ceil_div(max_blocks, sb);
+      const int64_t whole = (units + slots - 1) / slots * max_blocks;
+      const int64_t split = (units * ns + slots - 1) / slots * sb;
+      if (whole <= split) sb = max_blocks;
+    }
+  }
+  if (sb < 1) sb = 1;
+  int ns = max_blocks > 0 ? ceil_div(max_blocks, sb) : 1;
+  if (ns <= 1) {
+    ns = 1;
+    sb = max_blocks > 0 ? max_blocks : 1;
+  }
+  if (ns > 65535) return PKV_ERR_UNSUPPORTED;
+  pl->split_blocks = sb;
+  pl->num_splits = ns;
+  if (ns > 1) {
+    const size_t rows = static_cast<size_t>(batch) * num_heads * ns;
+    pl->lse_off = (rows * kMlaLatent * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    pl->workspace = pl->lse_off + rows * sizeof(float);
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_mla_workspace_size(int batch, int num_heads, int latent_dim, int rope_dim,
+                                  int block_size, int max_context_len, pkv_dtype dtype,
+                                  const pkv_options *options, size_t *bytes) {
+  if (!bytes) return PKV_ERR_INVALID_ARG;
+  MlaPlan pl;
+  const pkv_status st = mla_plan(batch, num_heads, latent_dim, rope_dim, block_size,
+                                 max_context_len, dtype, options, &pl);
+  if (st == PKV_OK) *bytes = pl.workspace;
+  return st;
+}
+
+pkv_status pkv_mla_decode_attention(void *out, const void *q, const void *ckv_cache,
+                                    const int32_t *block_table, int max_blocks_per_seq,
+                                    const int32_t *context_lens, int max_context_len, int batch,
+                                    int num_heads, int latent_dim, int rope_dim, int block_size,
+                                    int64_t num_blocks, float scale, pkv_dtype dtype,
+                                    void *workspace, size_t workspace_bytes,
+                                    const pkv_options *options, int32_t *error_word,
+                                    pkv_stream_t stream) {
+  // argument checks that need no device come first
+  if (batch < 0 || num_heads < 1 || max_context_len < 0 || !valid_dtype(dtype))
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!out || !q || !ckv_cache || !block_table || !context_lens) return PKV_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * kBlockSize)
+    return PKV_ERR_INVALID_ARG;
+  if (num_blocks > (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(ckv_cache, 16) ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4) ||
+      (error_word && !aligned(error_word, 4)))
+    return PKV_ERR_ALIGNMENT;
+  MlaPlan pl;
+  pkv_status st = mla_plan(batch, num_heads, latent_dim, rope_dim, block_size, max_context_len,
+                           dtype, options, &pl);
+  if (st != PKV_OK) return st;
+  if (pl.workspace > 0 &&
+      (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.workspace))
+    return PKV_ERR_WORKSPACE;
+  CUtensorMap cmap;
+  if (!encode_cache_map(&cmap, ckv_cache, dtype, latent_dim + rope_dim, 1, num_blocks))
+    return PKV_ERR_CUDA;
+
+  AttnParams p{};
+  p.out = out;
+  p.q = q;
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.err = error_word;
+  p.num_blocks = num_blocks;
+  p.batch = batch;
+  p.num_queries = 1;
+  p.num_heads = num_heads;
+  p.num_kv_heads = 1;
+  p.group = num_heads;
+  p.rows = num_heads;
+  p.rows_per_cta = kMlaHeadsPerCta;
+  p.row_chunks = num_heads / kMlaHeadsPerCta;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_context_len = max_context_len;
+  p.split_blocks = pl.split_blocks;
+  p.num_splits = pl.num_splits;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.out_scale = 1.f;
+  if (pl.num_splits > 1) {
+    p.part_o = static_cast<float *>(workspace);
+    p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + pl.lse_off);
+  }
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(pl.num_splits, num_heads / kMlaHeadsPerCta, batch);
+  if (mla_launch(dtype, rope_dim, options ? options->stages : 0, cmap, p, grid, cs) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (pl.num_splits > 1 && merge_launch(dtype, kMlaLatent, p, pl.sms, cs) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+pkv_status pkv_mla_append(const void *ckv_new, void *ckv_cache, const int64_t *slot_mapping,
+                          int64_t num_tokens, int width, int block_size, int64_t num_blocks,
+                          pkv_dtype dtype, int32_t *error_word, pkv_stream_t stream) {
+  if (num_tokens < 0 || width < 1 || block_size < 1 || num_blocks < 1 || !valid_dtype(dtype))
+    return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!ckv_new || !ckv_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  const int64_t row_bytes = static_cast<int64_t>(width) * elt_bytes(dtype);
+  if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(ckv_new, 16) || !aligned(ckv_cache, 16) || !aligned(slot_mapping, 8) ||
+      (error_word && !aligned(error_word, 4)))
+    return PKV_ERR_ALIGNMENT;
+  int device = 0, sms = 0;
+  if (current_sm_count(&device, &sms) != cudaSuccess) return PKV_ERR_CUDA;
+  return append_launch(ckv_new, nullptr, ckv_cache, nullptr, slot_mapping, num_tokens, 1,
+                       static_cast<int>(row_bytes / 16), block_size, num_blocks, error_word, sms,
+                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_read_error_word(const int32_t *error_word, int32_t *host_code,
                                pkv_stream_t stream) {
   if (!error_word || !host_code) return PKV_ERR_INVALID_ARG;

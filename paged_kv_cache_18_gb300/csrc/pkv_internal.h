@@ -71,6 +71,14 @@ bool simt_kernel_info(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, in
 cudaError_t simt_launch(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, int rows,
                         const AttnParams &p, dim3 grid, cudaStream_t stream);
 
+// MLA decode (attn_mla.cu): latent width 512, rotary part rope_dim 0 or 64,
+// bf16 / f16, 16 query heads per CTA; `stages` 3..5 (0: default).  The
+// partials and the merge are those of the other decode kernels.
+constexpr int kMlaLatent = 512;
+constexpr int kMlaHeadsPerCta = 16;
+bool mla_kernel_info(pkv_dtype dtype, int rope_dim, int stages, KernelInfo *info);
+cudaError_t mla_launch(pkv_dtype dtype, int rope_dim, int stages, const CUtensorMap &cmap,
+                       const AttnParams &p, dim3 grid, cudaStream_t stream);
 // Split-K log-sum-exp merge.
 cudaError_t merge_launch(pkv_dtype dtype, int head_dim, const AttnParams &p, int sm_count,
                          cudaStream_t stream);

@@ -342,3 +342,117 @@ def fp8_caches(b: PagedBatch, k_scale: float, v_scale: float):
             torch.uint8).numpy()
 
     return codes(b.k_cache, k_scale), codes(b.v_cache, v_scale)
+
+
+# ---- multi-head latent attention (MLA) decode -------------------------------------
+@dataclasses.dataclass
+class MlaWorkload:
+    """One MLA decode step over a paged latent cache: each sequence appends
+    its newest latent row [c ; k_rope], then every query head attends over
+    the sequence's rows with the absorbed query [q_c ; q_r]."""
+    name: str
+    batch: int
+    num_heads: int
+    rope_dim: int                                   # 0 or 64
+    dtype: str                                      # "bf16" | "f16"
+    context_lens: Optional[Sequence[int]] = None
+    len_range: Optional[tuple] = None
+    latent_dim: int = 512
+    head_dim: int = 128                             # per-head dim before absorption
+    block_size: int = 16
+    scale: Optional[float] = None                   # None -> 1/sqrt(head_dim + rope_dim)
+    seed: int = 0
+    slack: float = 0.10
+
+    @property
+    def width(self) -> int:
+        return self.latent_dim + self.rope_dim
+
+    @property
+    def softmax_scale(self) -> float:
+        if self.scale is not None:
+            return self.scale
+        return 1.0 / math.sqrt(self.head_dim + self.rope_dim)
+
+    def lengths(self) -> np.ndarray:
+        if self.context_lens is not None:
+            lens = np.asarray(self.context_lens, dtype=np.int32)
+            if lens.size == 1 and self.batch > 1:
+                lens = np.full(self.batch, int(lens[0]), dtype=np.int32)
+            return lens
+        lo, hi = self.len_range
+        rng = np.random.Generator(np.random.PCG64(self.seed + 7919))
+        return rng.integers(lo, hi, size=self.batch, endpoint=True).astype(np.int32)
+
+
+# DeepSeek-V2's latent sizes (d_c 512, d_h^R 64) with 16 query heads per GPU.
+MLA_WORKLOADS = {
+    "mla_deepseek_v2": MlaWorkload("DeepSeek-V2-shaped MLA decode, 16 heads", 64, 16, 64,
+                                   "bf16", len_range=(1024, 8192), seed=1007),
+}
+
+
+@dataclasses.dataclass
+class MlaBatch:
+    wl: MlaWorkload
+    q: np.ndarray             # [B, H, W] storage dtype
+    ckv_cache: np.ndarray     # [NB, bs, W] storage dtype (the new slots poisoned)
+    ckv_new: np.ndarray       # [B, W]: the newest row of each sequence
+    slot_mapping: np.ndarray  # [B] int64 (-1: the sequence is empty)
+    block_table: np.ndarray   # [B, max_blocks] int32 (unused entries = -1)
+    context_lens: np.ndarray  # [B] int32 (includes the new row)
+    num_blocks: int
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.context_lens.size else 0
+
+    def kv_bytes(self) -> int:
+        """Bytes of the valid latent rows one decode call reads (each once)."""
+        return int(int(self.context_lens.clip(min=0).sum()) * self.wl.width
+                   * ELT_BYTES[self.wl.dtype])
+
+
+def make_mla_batch(wl: MlaWorkload, poison: bool = True) -> MlaBatch:
+    """Seeded host arrays of ``wl``: latent and rotary values ~ N(0, 1) in the
+    storage dtype, physical blocks a random permutation with 10% spare, rows
+    past each context and spare blocks NaN-filled (poison), and each
+    sequence's newest row held back as the step's append."""
+    rng = np.random.Generator(np.random.PCG64(wl.seed))
+    B, H, W, bs = wl.batch, wl.num_heads, wl.width, wl.block_size
+    lens = wl.lengths()
+    assert lens.shape == (B,)
+    owned = [max(0, -(-int(L) // bs)) for L in lens]
+    total = sum(owned)
+    NB = max(1, total + int(math.ceil(wl.slack * total)))
+    perm = rng.permutation(NB).astype(np.int32)
+    table = np.full((B, max(1, max(owned) if owned else 1)), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        table[b, :owned[b]] = perm[pos:pos + owned[b]]
+        pos += owned[b]
+    cache = _normal_storage(rng, (NB, bs, W), wl.dtype)
+    q = _normal_storage(rng, (B, H, W), wl.dtype)
+    slots = np.full(B, -1, dtype=np.int64)
+    new = np.empty((B, W), dtype=STORAGE[wl.dtype])
+    bad = _poison_value(wl.dtype)
+    for b in range(B):
+        i = int(lens[b]) - 1
+        if i < 0:
+            new[b] = bad
+            continue
+        phys = int(table[b, i // bs])
+        slots[b] = phys * bs + i % bs
+        new[b] = cache[phys, i % bs]
+    if poison:
+        used = np.zeros(NB, dtype=bool)
+        used[perm[:total]] = True
+        cache[~used] = bad
+        for b in range(B):
+            L = int(lens[b])
+            if owned[b] and L % bs:
+                cache[int(table[b, owned[b] - 1]), L % bs:] = bad
+            if slots[b] >= 0:
+                phys, off = divmod(int(slots[b]), bs)
+                cache[phys, off] = bad
+    return MlaBatch(wl, q, cache, new, slots, table, lens.astype(np.int32), NB)

@@ -197,3 +197,40 @@ def test_host_step_staging_size_argument_errors(L):
     assert f(2, 1, 8, 2, 128, 16, 8, 100, 1, None, None) == 1             # no result pointer
     assert f(2, 1, 8, 2, 128, 16, 8, 100, 3, None, ctypes.byref(n)) == 1  # FP8
     assert f(2, 1, 8, 2, 128, 16, 0, 100, 1, None, ctypes.byref(n)) == 1  # no table width
+
+
+def mla_decode(L, **kw):
+    a = dict(out=16, q=16, c=256, table=16, max_blocks=8, lens=16, max_ctx=100, B=2, H=16,
+             latent=512, rope=64, bs=16, NB=10, scale=0.1, dtype=1, ws=None, ws_bytes=0,
+             opt=None, err=None, stream=None)
+    a.update(kw)
+    return L.pkv_mla_decode_attention(
+        a["out"], a["q"], a["c"], a["table"], a["max_blocks"], a["lens"], a["max_ctx"], a["B"],
+        a["H"], a["latent"], a["rope"], a["bs"], a["NB"], a["scale"], a["dtype"], a["ws"],
+        a["ws_bytes"], a["opt"], a["err"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0, q=None, out=None), 0),                      # nothing to do
+    (dict(q=None), 1), (dict(c=None), 1), (dict(table=None), 1), (dict(lens=None), 1),
+    (dict(dtype=9), 1), (dict(NB=0), 1), (dict(max_ctx=8 * 16 + 1), 1),
+    (dict(scale=float("nan")), 1), (dict(q=8), 5), (dict(c=24), 5),
+    (dict(H=8), 2), (dict(latent=256), 2), (dict(rope=32), 2), (dict(dtype=0), 2),  # f32
+    (dict(bs=32), 2),
+])
+def test_mla_argument_errors(L, kw, status):
+    assert mla_decode(L, **kw) == status
+
+
+def test_mla_append_and_workspace_argument_errors(L):
+    f = L.pkv_mla_append
+    assert f(16, 16, 16, 0, 576, 16, 10, 1, None, None) == 0      # no tokens
+    assert f(None, 16, 16, 4, 576, 16, 10, 1, None, None) == 1
+    assert f(16, 16, 16, 4, 4, 16, 10, 1, None, None) == 2        # 8-byte rows
+    assert f(16, 24, 16, 4, 576, 16, 10, 1, None, None) == 5      # cache misaligned
+    n = ctypes.c_size_t(0)
+    g = L.pkv_mla_workspace_size
+    assert g(2, 16, 512, 64, 16, 100, 1, None, None) == 1            # no result pointer
+    assert g(2, 8, 512, 64, 16, 100, 1, None, ctypes.byref(n)) == 2  # heads
+    opt = binding.Options(2, 0, 0, 0, 0, 0, 0, 0)                   # a kernel choice
+    assert g(2, 16, 512, 64, 16, 100, 1, ctypes.byref(opt), ctypes.byref(n)) == 2
