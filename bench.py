@@ -16,6 +16,10 @@ from pinned host memory and the output read back every step.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the float64 CPU oracle, timed
 
+`--workload mla_deepseek_v2` times an MLA decode step (mla_append of each
+sequence's newest latent row, then mla_decode_attention over the latent
+cache; value = latent GB/s).
+
 `--workload prefill_llama3_8b` times the chunked-prefill step instead
 (kv_append of each sequence's 512 chunk rows, then paged_prefill_attention):
 its `value` is attention TFLOP/s against the bf16 tensor peak.  Its K/V
@@ -711,6 +715,231 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------- MLA decode ------
+MLA_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mla.cu",
+               "paged_kv_cache_18_gb300/csrc/attn_merge.cu",
+               "paged_kv_cache_18_gb300/csrc/pkv_device.cuh"]
+
+
+def mla_algorithmic_bytes(b: W.MlaBatch, plan: dict) -> int:
+    """Bytes one MLA decode call must move: every valid latent row once, the
+    queries and outputs, the block-table entries read and, when split, the
+    float32 partials and log-sum-exps of every split that has rows, written
+    and read back."""
+    wl = b.wl
+    elt = W.ELT_BYTES[wl.dtype]
+    rows = wl.batch * wl.num_heads
+    nblk = [-(-int(L) // wl.block_size) for L in b.context_lens]
+    total = b.kv_bytes() + rows * wl.width * elt + rows * wl.latent_dim * elt + 4 * sum(nblk)
+    if plan["num_splits"] > 1:
+        parts = sum(max(1, -(-n // plan["split_blocks"])) for n in nblk)
+        total += 2 * parts * wl.num_heads * (wl.latent_dim + 1) * 4
+    return int(total)
+
+
+def mla_oracle_sample(b: W.MlaBatch, budget_s: float):
+    """Time the float64 MLA oracle: whole sequences (all heads) per call,
+    cycling, until about `budget_s`; returns (latent bytes covered, seconds,
+    description)."""
+    from oracle import mla as oracle_mla
+    wl = b.wl
+    elt = W.ELT_BYTES[wl.dtype]
+    done, elapsed, calls = 0, 0.0, 0
+    while elapsed < budget_s:
+        s = calls % wl.batch
+        t = time.perf_counter()
+        oracle_mla.mla_decode(b.q[s:s + 1], b.ckv_cache, b.block_table[s:s + 1],
+                              b.context_lens[s:s + 1], wl.latent_dim, wl.softmax_scale,
+                              wl.dtype)
+        elapsed += time.perf_counter() - t
+        done += int(b.context_lens[s]) * wl.width * elt
+        calls += 1
+    threads = (os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+               or str(os.cpu_count()))
+    desc = (f"{calls} sequence passes (all {wl.num_heads} heads) cycling over the "
+            f"{wl.batch} sequences, float64 NumPy oracle (BLAS threads: {threads}), "
+            f"{elapsed:.1f} s")
+    return done, elapsed, desc, int(threads)
+
+
+def mla_config(wl: W.MlaWorkload, b: W.MlaBatch) -> dict:
+    return {"workload": wl.name, "batch": wl.batch, "num_heads": wl.num_heads,
+            "latent_dim": wl.latent_dim, "rope_dim": wl.rope_dim, "block_size": wl.block_size,
+            "context_lens": f"{int(b.context_lens.min())}..{int(b.context_lens.max())}"
+                            f" (sum {int(b.context_lens.sum())})",
+            "kv_bytes_per_step": b.kv_bytes(),
+            "l2": f"no flush: the step reads {b.kv_bytes() / 1e9:.2f} GB of latent rows, "
+                  "> 129 MB L2",
+            "step": f"mla_append of {wl.batch} rows + mla_decode_attention"}
+
+
+def run_mla(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from paged_kv_cache_18_gb300 import build as pkv_build
+    if rank == 0 or not os.path.exists(pkv_build.LIB):
+        pkv_build.build()
+    barrier()
+    import paged_kv_cache_18_gb300 as pkv
+
+    wl = W.MLA_WORKLOADS[args.workload]
+    if rank > 0:
+        wl = W.MlaWorkload(**{**wl.__dict__, "seed": wl.seed + 100 * rank})
+    b = W.make_mla_batch(wl)
+    dt = {"bf16": torch.bfloat16, "f16": torch.float16}[wl.dtype]
+    cache = dev_tensor(b.ckv_cache, wl.dtype, dev)
+    new = dev_tensor(b.ckv_new, wl.dtype, dev)
+    q = dev_tensor(b.q, wl.dtype, dev)
+    slots = torch.from_numpy(b.slot_mapping).to(dev)
+    table = torch.from_numpy(b.block_table).to(dev)
+    lens = torch.from_numpy(b.context_lens).to(dev)
+    max_ctx = b.max_context_len
+    plan = pkv.mla_plan(wl.batch, wl.num_heads, wl.rope_dim, max_ctx, dt, stages=args.stages,
+                        split_blocks=args.split_blocks)
+    ws = torch.empty(max(16, plan["workspace_bytes"]), dtype=torch.uint8, device=dev)
+    out = torch.empty(wl.batch, wl.num_heads, wl.latent_dim, dtype=dt, device=dev)
+    opts = dict(max_context_len=max_ctx, out=out, workspace=ws, stages=args.stages,
+                split_blocks=args.split_blocks)
+
+    def attend(qq, nn, sl, tb, ln):
+        pkv.mla_append(nn, cache, sl)
+        pkv.mla_decode_attention(qq, cache, tb, ln, wl.softmax_scale, **opts)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        attend(q, new, slots, table, lens)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
+    if sampler:
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        pkv.mla_append(new, cache, slots)
+        ev[i][0].record(stream)
+        pkv.mla_decode_attention(q, cache, table, lens, wl.softmax_scale, **opts)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    barrier()
+    step_ms = dist_max(start.elapsed_time(end) / K, dev)
+    attn_ms = statistics.mean(a.elapsed_time(z) for a, z in ev)
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    kv_step = b.kv_bytes()
+    e2e = None
+    if not args.no_e2e:
+        host = {n: t.cpu().pin_memory() for n, t in
+                (("q", q), ("new", new), ("slots", slots), ("table", table), ("lens", lens))}
+        out_host = torch.empty_like(out, device="cpu").pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+        E = max(3, min(K, 200))
+
+        def e2e_step():
+            for n in dev_in:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            attend(dev_in["q"], dev_in["new"], dev_in["slots"], dev_in["table"], dev_in["lens"])
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(E):
+            e2e_step()
+        e2e_s = dist_max((time.perf_counter() - t0) / E, dev)
+        e2e = {"value": dist_sum(kv_step, dev) / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
+               "ms_per_step": 1e3 * e2e_s,
+               "api": "pinned host tensors copied in with torch, mla_append and "
+                      "mla_decode_attention, the output copied out, then a stream synchronise"}
+
+    total_kv = dist_sum(kv_step, dev)
+    total_tokens = dist_sum(wl.batch, dev)
+    if rank != 0:
+        return 0
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    ns = plan["num_splits"]
+    algo = mla_algorithmic_bytes(b, plan)
+    achieved = algo / (attn_ms * 1e-3) / 1e9
+    launches_per_step = 2 + (1 if ns > 1 else 0)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        nbytes, secs, desc, threads = mla_oracle_sample(W.make_mla_batch(wl), args.cpu_budget)
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": threads,
+               "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": total_kv / (step_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic", "config": mla_config(wl, b),
+        "pct_of_hbm_peak": 100.0 * total_kv / (step_ms * 1e-3) / 1e9 / peak,
+        "tokens_per_s": total_tokens / (step_ms * 1e-3),
+        "attention_ms": attn_ms,
+        "plan": {k: plan[k] for k in ("split_blocks", "num_splits", "grid_x", "grid_y",
+                                      "grid_z", "stages", "ctas_per_sm", "merge_kernel")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(args.workload, MLA_SOURCES),
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": algo,
+                     "kernel": "mla decode" + (" + split-K merge" if ns > 1 else ""),
+                     "launches_per_step": launches_per_step - 1},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_reference_mla(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = W.MLA_WORKLOADS[args.workload]
+    b = W.make_mla_batch(wl)
+    per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        mla_oracle_sample(b, per_step_budget / 4)
+    total, total_s, desc, threads = 0, 0.0, "", 1
+    for _ in range(args.steps):
+        nb, secs, desc, threads = mla_oracle_sample(b, per_step_budget)
+        total += nb
+        total_s += secs
+    value = total / total_s / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": mla_config(wl, b),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": desc + f"; ~{per_step_budget:.1f} s per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -718,7 +947,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(W.WORKLOADS) + list(W.PREFILL_WORKLOADS),
+    ap.add_argument("--workload", choices=list(W.WORKLOADS) + list(W.PREFILL_WORKLOADS)
+                    + list(W.MLA_WORKLOADS),
                     default="llama2_13b")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--split-blocks", type=int, default=0)
@@ -745,6 +975,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.workload in W.PREFILL_WORKLOADS:
         return run_reference_prefill(args) if args.impl == "reference" else run_prefill(args)
+    if args.workload in W.MLA_WORKLOADS:
+        return run_reference_mla(args) if args.impl == "reference" else run_mla(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

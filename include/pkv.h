@@ -413,6 +413,12 @@ PKV_API pkv_status pkv_paged_attention_fp8(
  * lengths above max_context_len are clamped and recorded, bad block ids
  * recorded and their rows ignored.
  */
+/* The launch an MLA decode call with these sizes makes on the current device
+ * (split-K partition, grid, ring depth, workspace); enqueues nothing. */
+PKV_API pkv_status pkv_mla_plan(int batch, int num_heads, int latent_dim, int rope_dim,
+                                int block_size, int max_context_len, pkv_dtype dtype,
+                                const pkv_options *options, pkv_plan *plan);
+
 PKV_API pkv_status pkv_mla_workspace_size(int batch, int num_heads, int latent_dim,
                                           int rope_dim, int block_size, int max_context_len,
                                           pkv_dtype dtype, const pkv_options *options,

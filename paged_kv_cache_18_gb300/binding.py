@@ -39,7 +39,8 @@ EXPORTED = ("pkv_status_string", "pkv_version", "pkv_kv_append", "pkv_attention_
             "pkv_bm_block_table", "pkv_bm_stats", "pkv_bm_block_info", "pkv_bm_hash",
             "pkv_copy_blocks", "pkv_paged_prefill_attention", "pkv_check_bounded_wait",
             "pkv_host_step_staging_size", "pkv_append_attention_host",
-            "pkv_mla_workspace_size", "pkv_mla_decode_attention", "pkv_mla_append")
+            "pkv_mla_plan", "pkv_mla_workspace_size", "pkv_mla_decode_attention",
+            "pkv_mla_append")
 
 
 class PkvError(RuntimeError):
@@ -116,6 +117,7 @@ def lib() -> ctypes.CDLL:
             L.pkv_append_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
                                                     i32, i32, i32, i32, i32, i32, i64, f32, i32,
                                                     vp, sz, opt, vp, vp]
+            L.pkv_mla_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, opt, plan]
             L.pkv_mla_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, opt,
                                                  ctypes.POINTER(sz)]
             L.pkv_mla_decode_attention.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
@@ -448,6 +450,16 @@ def _mla_opts(stages: int, split_blocks: int):
     if not (stages or split_blocks):
         return None
     return ctypes.byref(Options(0, split_blocks, stages, 0, 0, 0, 0, 0))
+
+
+def mla_plan(batch: int, num_heads: int, rope_dim: int, max_context_len: int,
+             dtype: torch.dtype, stages: int = 0, split_blocks: int = 0) -> dict:
+    """The launch an MLA decode call with these sizes makes (pkv_mla_plan)."""
+    p = Plan()
+    _check("pkv_mla_plan", lib().pkv_mla_plan(
+        batch, num_heads, MLA_LATENT, rope_dim, 16, max_context_len, _DTYPE[dtype],
+        _mla_opts(stages, split_blocks), ctypes.byref(p)))
+    return p.as_dict()
 
 
 def mla_workspace_size(batch: int, num_heads: int, rope_dim: int, max_context_len: int,

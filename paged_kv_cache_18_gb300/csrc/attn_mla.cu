@@ -274,17 +274,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t km0 = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
         const uint32_t km8 =
             (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
+        // value tiles four at a time: the high parts, then the remainders, so
+        // that no MMA waits on the one just issued to its accumulator
 #pragma unroll
-        for (int mt = 0; mt < kVTiles; ++mt) {
-          uint32_t a[4];
-          ldsm_x4_t(a, tile + tile_off((lane & 7) + ((lane >> 4) << 3),
-                                       qw * 128 + mt * 16 + ((lane >> 3) & 1) * 8));
-          a[0] &= km0;
-          a[1] &= km0;
-          a[2] &= km8;
-          a[3] &= km8;
-          Mma<T>::run(o[mt], a, ph0, ph1);
-          Mma<T>::run(o[mt], a, pl0, pl1);
+        for (int m0 = 0; m0 < kVTiles; m0 += 4) {
+          uint32_t a[4][4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            ldsm_x4_t(a[w], tile + tile_off((lane & 7) + ((lane >> 4) << 3),
+                                            qw * 128 + (m0 + w) * 16 + ((lane >> 3) & 1) * 8));
+            a[w][0] &= km0;
+            a[w][1] &= km0;
+            a[w][2] &= km8;
+            a[w][3] &= km8;
+          }
+#pragma unroll
+          for (int w = 0; w < 4; ++w) Mma<T>::run(o[m0 + w], a[w], ph0, ph1);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) Mma<T>::run(o[m0 + w], a[w], pl0, pl1);
         }
       }
       __syncwarp();

@@ -989,6 +989,34 @@ pkv_status mla_plan(int batch, int num_heads, int latent_dim, int rope_dim, int 
 
 extern "C" {
 
+pkv_status pkv_mla_plan(int batch, int num_heads, int latent_dim, int rope_dim, int block_size,
+                        int max_context_len, pkv_dtype dtype, const pkv_options *options,
+                        pkv_plan *plan) {
+  if (!plan) return PKV_ERR_INVALID_ARG;
+  MlaPlan pl;
+  const pkv_status st = mla_plan(batch, num_heads, latent_dim, rope_dim, block_size,
+                                 max_context_len, dtype, options, &pl);
+  if (st != PKV_OK) return st;
+  *plan = pkv_plan{};
+  plan->kernel = PKV_KERNEL_MMA;
+  plan->rows_per_cta = kMlaHeadsPerCta;
+  plan->row_chunks = num_heads / kMlaHeadsPerCta;
+  plan->split_blocks = pl.split_blocks;
+  plan->num_splits = pl.num_splits;
+  plan->grid_x = pl.num_splits;
+  plan->grid_y = num_heads / kMlaHeadsPerCta;
+  plan->grid_z = batch;
+  plan->threads_per_cta = pl.info.threads;
+  plan->stages = pl.info.stages;
+  plan->ctas_per_sm = pl.ctas_per_sm;
+  plan->smem_bytes = pl.info.smem;
+  plan->workspace_bytes = pl.workspace;
+  plan->merge_kernel = pl.num_splits > 1 ? 1 : 0;
+  plan->warp_tiles = 1;
+  plan->blocks_per_iter = 1;
+  return PKV_OK;
+}
+
 pkv_status pkv_mla_workspace_size(int batch, int num_heads, int latent_dim, int rope_dim,
                                   int block_size, int max_context_len, pkv_dtype dtype,
                                   const pkv_options *options, size_t *bytes) {
