@@ -193,6 +193,12 @@ def barrier():
 
 
 # ------------------------------------------------------------ CPU oracle ---
+def decode_workload(name: str) -> W.Workload:
+    """A decode / verify workload by name (the named configurations and the
+    tree-verification ones)."""
+    return W.WORKLOADS[name] if name in W.WORKLOADS else W.TREE_WORKLOADS[name]
+
+
 def oracle_sample(b: W.PagedBatch, budget_s: float):
     """Time the float64 oracle on whole sequences of the workload, cycling
     over them, until about `budget_s` of CPU work; returns (KV bytes covered,
@@ -206,8 +212,13 @@ def oracle_sample(b: W.PagedBatch, budget_s: float):
         bi = seqs % wl.batch
         rows = np.arange(per_seq_rows, dtype=np.int64) + bi * per_seq_rows
         t = time.perf_counter()
-        oracle.paged_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
-                               wl.softmax_scale, wl.dtype, rows=rows)
+        if wl.tree_parents is not None:
+            oracle.tree_attention(b.q[bi:bi + 1], b.k_cache, b.v_cache, b.block_table[bi:bi + 1],
+                                  b.context_lens[bi:bi + 1], wl.softmax_scale, wl.dtype,
+                                  W.tree_mask_bits(wl.tree_parents))
+        else:
+            oracle.paged_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                   wl.softmax_scale, wl.dtype, rows=rows)
         elapsed += time.perf_counter() - t
         L = int(b.context_lens[bi])
         done_bytes += 2 * L * wl.num_kv_heads * wl.head_dim * W.ELT_BYTES[wl.dtype]
@@ -224,7 +235,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    wl = W.WORKLOADS[args.workload]
+    wl = decode_workload(args.workload)
     b = W.make_batch(wl)
     per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -471,7 +482,9 @@ def workload_config(wl: W.Workload, b: W.PagedBatch, fused: bool = False) -> dic
             "step": (f"append_attention: {wl.batch * wl.num_queries} new rows written and "
                      "attended in one launch" if fused else
                      f"kv_append of {wl.batch * wl.num_queries} rows + "
-                     + ("paged_decode_attention" if wl.num_queries == 1
+                     + ("tree_verify_attention (one shared tree, parents "
+                        f"{list(wl.tree_parents)})" if wl.tree_parents is not None
+                        else "paged_decode_attention" if wl.num_queries == 1
                         else "spec_verify_attention"))}
 
 
@@ -504,11 +517,14 @@ def run_ours(args):
                               warp_tiles=args.warp_tiles, blocks_per_iter=args.blocks_per_iter,
                               persistent=args.persistent)
 
-    wl = W.WORKLOADS[args.workload]
+    wl = decode_workload(args.workload)
     if rank > 0:
         wl = W.Workload(**{**wl.__dict__, "seed": wl.seed + 100 * rank})
     b = W.make_batch(wl)
     dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl.dtype]
+    tree = wl.tree_parents is not None
+    if tree and args.kv_dtype == "fp8":
+        raise SystemExit("tree verification reads 16-bit caches only")
     fp8 = args.kv_dtype == "fp8"
     if fp8:
         kc8, vc8 = W.fp8_caches(b, FP8_K_SCALE, FP8_V_SCALE)
@@ -534,7 +550,12 @@ def run_ours(args):
     ws = torch.empty(max(16, plan["workspace_bytes"]), dtype=torch.uint8, device=dev)
     max_ctx = b.max_context_len
     attn = pkv.paged_decode_attention if Q == 1 else pkv.spec_verify_attention
-    fused = not args.unfused and not fp8
+    if tree:
+        mask = torch.from_numpy(W.tree_mask_bits(wl.tree_parents).view(np.int64)).to(dev)
+
+        def attn(qq, kc, vc, tb, ln, **kw):
+            return pkv.tree_verify_attention(qq, kc, vc, tb, ln, mask, **kw)
+    fused = not args.unfused and not fp8 and not tree
     shape4 = (wl.batch, Q, wl.num_kv_heads, wl.head_dim)
     opts = dict(scale=wl.softmax_scale, max_context_len=max_ctx, out=out, workspace=ws,
                 kernel=args.kernel, split_blocks=args.split_blocks, stages=args.stages)
@@ -677,7 +698,7 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        nbytes, secs, desc = oracle_sample(W.make_batch(W.WORKLOADS[args.workload]),
+        nbytes, secs, desc = oracle_sample(W.make_batch(decode_workload(args.workload)),
                                            args.cpu_budget)
         import oracle
         cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
@@ -947,8 +968,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(W.WORKLOADS) + list(W.PREFILL_WORKLOADS)
-                    + list(W.MLA_WORKLOADS),
+    ap.add_argument("--workload", choices=list(W.WORKLOADS) + list(W.TREE_WORKLOADS)
+                    + list(W.PREFILL_WORKLOADS) + list(W.MLA_WORKLOADS),
                     default="llama2_13b")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--split-blocks", type=int, default=0)

@@ -78,6 +78,7 @@ class Workload:
     scale: Optional[float] = None                   # None -> 1/sqrt(D)
     seed: int = 0
     slack: float = 0.10
+    tree_parents: Optional[Sequence[int]] = None    # tree verification: parent of each node
 
     @property
     def softmax_scale(self) -> float:
@@ -106,6 +107,40 @@ WORKLOADS = {
                             "bf16", context_lens=[32768, 65536], seed=1004),
     "spec_verify": Workload("speculative verify K=4", 16, 32, 8, 128, "bf16",
                             len_range=(512, 8192), num_queries=5, seed=1005),
+}
+
+
+def medusa_parents(branching: Sequence[int]) -> list:
+    """Parents of a candidate tree in breadth-first order ("Inference part 2",
+    section "Medusa": the top candidates of each extra head are combined into
+    a tree of continuations): node 0 is the last accepted token, and every
+    node of depth d has branching[d] children.  parents[0] = -1."""
+    parents, level = [-1], [0]
+    for k in branching:
+        nxt = []
+        for p in level:
+            for _ in range(k):
+                parents.append(p)
+                nxt.append(len(parents) - 1)
+        level = nxt
+    return parents
+
+
+def tree_mask_bits(parents: Sequence[int]) -> np.ndarray:
+    """Visibility bitmask of each tree node: bit k of mask[j] is set when node
+    k is node j or one of its ancestors (parents[j] < j)."""
+    masks = np.zeros(len(parents), dtype=np.uint64)
+    for j, p in enumerate(parents):
+        masks[j] = (masks[p] if p >= 0 else np.uint64(0)) | np.uint64(1 << j)
+    return masks
+
+
+# Tree verification on the speculative-verify shape: two extra heads, top-3
+# and top-2 candidates (1 + 3 + 6 = 10 nodes).
+TREE_WORKLOADS = {
+    "medusa_tree": Workload("Medusa tree verify, 10 nodes (top-3 x top-2)", 16, 32, 8, 128,
+                            "bf16", len_range=(512, 8192), num_queries=10, seed=1008,
+                            tree_parents=medusa_parents((3, 2))),
 }
 
 

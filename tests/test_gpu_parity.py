@@ -249,6 +249,31 @@ def test_named_workload_full_size(name):
     print(f"{name}: max-abs {max_abs:.3e} rel-L2 {rel:.3e}")
 
 
+@pytest.mark.slow
+def test_tree_workload_full_size():
+    """The Medusa-tree bench workload, in the bench's launch configuration."""
+    import oracle
+    import paged_kv_cache_18_gb300 as pkv
+    wl = W.TREE_WORKLOADS["medusa_tree"]
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    masks = W.tree_mask_bits(wl.tree_parents)
+    out = pkv.tree_verify_attention(d.q, d.k_cache, d.v_cache, d.table, d.lens,
+                                    torch.from_numpy(masks.view(np.int64)).cuda(),
+                                    scale=wl.softmax_scale, max_context_len=b.max_context_len,
+                                    error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    oracle.kv_append(b.k_cache, b.v_cache, b.k_new, b.v_new, b.slot_mapping, wl.dtype)
+    ref = oracle.tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.context_lens,
+                                wl.softmax_scale, wl.dtype, masks)
+    got = host_f64(out, wl.dtype)
+    assert np.isfinite(got).all()
+    max_abs, rel = assert_close(got, ref, wl.dtype, wl.name)
+    print(f"medusa_tree: max-abs {max_abs:.3e} rel-L2 {rel:.3e}")
+
+
 # ---- fused append + attention (one launch) --------------------------------
 @pytest.mark.parametrize("dtype,kernel", [("f32", "simt"), ("bf16", "simt"), ("bf16", "mma"),
                                           ("f16", "mma")])
