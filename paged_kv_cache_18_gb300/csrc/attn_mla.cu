@@ -20,7 +20,8 @@
 //              128 bytes, 128-byte swizzle) into a ring of NS stages.
 // Per block, in the transposed orientation of the decode kernels (keys on M):
 //   partial S^T[16 x 8] = K[16 x W/4] . Q^T[W/4 x 8] over the warp's quarter
-//   of the W = 512 + DR score dims; the four quarters of a column group meet
+//   of the W = 512 + DR score dims (16-value steps qw, qw + 4, ...: one per
+//   128-byte panel, at the same swizzled offset); the four quarters of a column group meet
 //   in shared memory and are summed in a fixed order, so all four warps hold
 //   the same scores, maxima and weights;
 //   online softmax with a lazy reference maximum, in log2 units ("Inference
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t qf[G::kQSteps][2];
 #pragma unroll
     for (int kk = 0; kk < G::kQSteps; ++kk) {
-      const int d = (qw * G::kQSteps + kk) * 16 + 2 * c;
+      const int d = (kk * kQuarters + qw) * 16 + 2 * c;  // score step 4 kk + qw
       qf[kk][0] = *reinterpret_cast<const uint32_t *>(qp + d);
       qf[kk][1] = *reinterpret_cast<const uint32_t *>(qp + d + 8);
     }
@@ -187,16 +188,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         s_abort = 1;
         if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT);
       }
-      // partial scores over this warp's quarter of the row
+      // partial scores over this warp's quarter of the row (steps qw, qw + 4, ...)
+      const uint32_t kbase = tile + tile_off(lane & 15, qw * 16 + (lane >> 4) * 8);
+      // V^T fragments: rows (lane & 7) + 8 (lane >> 4), value dims 128 qw + 16 mt
+      // + 8 h (h = bit 3 of the lane), in panel 2 qw + mt / 4; their 16-byte chunk
+      // 2 (mt % 4) + h sits at (2 (mt % 4)) ^ h ^ (row & 7), 2 (mt % 4) being even
+      const int vrow = (lane & 7) + ((lane >> 4) << 3);
+      const uint32_t vbase = tile + 2 * qw * G::kPanelBytes + vrow * 128;
+      const uint32_t vx = static_cast<uint32_t>((((lane >> 3) & 1) ^ (vrow & 7)) << 4);
       float part[4] = {0.f, 0.f, 0.f, 0.f};
       if (!aborted) {
         float acc[G::kChains][4];
 #pragma unroll
         for (int ch = 0; ch < G::kChains; ++ch) acc[ch][0] = acc[ch][1] = acc[ch][2] = acc[ch][3] = 0.f;
+        // step 4 kk + qw covers values 64 kk + 16 qw ..: panel kk, the same
+        // swizzled 16-byte chunk in every panel
 #pragma unroll
         for (int kk = 0; kk < G::kQSteps; ++kk) {
           uint32_t a[4];
-          ldsm_x4(a, tile + tile_off(lane & 15, (qw * G::kQSteps + kk) * 16 + (lane >> 4) * 8));
+          ldsm_x4(a, kbase + kk * G::kPanelBytes);
           Mma<T>::run(acc[kk % G::kChains], a, qf[kk][0], qf[kk][1]);
         }
 #pragma unroll
@@ -281,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           uint32_t a[4][4];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            ldsm_x4_t(a[w], tile + tile_off((lane & 7) + ((lane >> 4) << 3),
-                                            qw * 128 + (m0 + w) * 16 + ((lane >> 3) & 1) * 8));
+            const int mt = m0 + w;
+            ldsm_x4_t(a[w], vbase + (mt >> 2) * G::kPanelBytes + ((32 * (mt & 3)) ^ vx));
             a[w][0] &= km0;
             a[w][1] &= km0;
             a[w][2] &= km8;
