@@ -36,7 +36,7 @@ bool pick(pkv_dtype cache_dtype, pkv_dtype q_dtype, int D, const MmaShape &m, Ke
 
 }  // namespace mma
 
-int mma_max_tiles(int head_dim) { return head_dim <= 64 ? 4 : (head_dim <= 128 ? 3 : 1); }
+int mma_max_tiles(int head_dim) { return head_dim <= 128 ? 5 : 1; }
 
 bool mma_kernel_info(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, const MmaShape &m,
                      KernelInfo *info) {

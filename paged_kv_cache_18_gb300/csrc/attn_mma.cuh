@@ -126,8 +126,11 @@ __device__ __forceinline__ void lane_sync(int id, int count) {
 // per-row power-of-two shift that keeps it in f16 range, undone in the score
 // scale).
 // Resident CTAs a kernel is compiled for: the three-warp tile fits six per
-// SM in shared memory, which its registers must then allow (<= 112 each).
-template <int CG, int NT> constexpr int mma_min_ctas() { return (CG >= 3 && NT == 1) ? 6 : 1; }
+// SM in shared memory, which its registers must then allow (<= 112 each);
+// the four- and five-warp tiles five and four (<= 102 each).
+template <int CG, int NT> constexpr int mma_min_ctas() {
+  return NT != 1 ? 1 : (CG == 3 ? 6 : (CG == 4 ? 5 : (CG == 5 ? 4 : 1)));
+}
 
 template <typename T, typename TC, int D, int CG, int NT, int KB, int BL, int NS>
 __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
@@ -727,8 +730,10 @@ bool mma_pick_kb(int kb, int stages, KernelInfo *info, MmaLaunch *launch) {
 }
 
 // Column groups x tiles per warp x head dim within the register and shared
-// memory budgets: cg warps of nt 8-column tiles each.  One tile per warp:
-// cg * D <= 384.  Several tiles in one warp (its O^T accumulators hold
+// memory budgets: cg warps of nt 8-column tiles each.  One tile per warp: up
+// to five column groups (40 query rows, e.g. a 10-node tree over four query
+// heads per KV head, read from one staged copy of each block) at head_dim
+// <= 128, one at 256.  Several tiles in one warp (its O^T accumulators hold
 // nt * D / 4 floats per thread): nt * D <= 384, one column group.
 template <typename T, typename TC, int D>
 bool mma_pick(int cg, int nt, int kb, int stages, KernelInfo *info, MmaLaunch *launch) {
@@ -737,7 +742,8 @@ bool mma_pick(int cg, int nt, int kb, int stages, KernelInfo *info, MmaLaunch *l
       case 1: return mma_pick_kb<T, TC, D, 1>(kb, stages, info, launch);
       case 2: return D <= 128 && mma_pick_kb<T, TC, D, (D <= 128 ? 2 : 1)>(kb, stages, info, launch);
       case 3: return D <= 128 && mma_pick_kb<T, TC, D, (D <= 128 ? 3 : 1)>(kb, stages, info, launch);
-      case 4: return D <= 64 && mma_pick_kb<T, TC, D, (D <= 64 ? 4 : 1)>(kb, stages, info, launch);
+      case 4: return D <= 128 && mma_pick_kb<T, TC, D, (D <= 128 ? 4 : 1)>(kb, stages, info, launch);
+      case 5: return D <= 128 && mma_pick_kb<T, TC, D, (D <= 128 ? 5 : 1)>(kb, stages, info, launch);
       default: return false;
     }
   }

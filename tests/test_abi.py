@@ -100,6 +100,12 @@ def test_plan_kernel_choice():
     assert p["kernel"] == binding.PKV_KERNEL_MMA and p["rows_per_cta"] == 1
     p = binding.plan_for(128, 1, 32, 8, 128, 4096, torch.bfloat16, num_sms=152)
     assert p["kernel"] == binding.PKV_KERNEL_MMA and p["rows_per_cta"] == 4
+    # a 10-node tree over four query heads per KV head: 40 rows, one CTA of
+    # five column-group warps per (sequence, KV head)
+    p = binding.plan_for(16, 10, 32, 8, 128, 8192, torch.bfloat16, num_sms=152)
+    assert (p["rows_per_cta"], p["row_chunks"], p["threads_per_cta"]) == (40, 1, 160)
+    p = binding.plan_for(16, 11, 32, 8, 128, 8192, torch.bfloat16, num_sms=152)
+    assert (p["rows_per_cta"], p["row_chunks"]) == (22, 2)
     with pytest.raises(binding.PkvError):
         binding.plan_for(1, 1, 8, 8, 64, 16, torch.float32, num_sms=152,
                          kernel=binding.PKV_KERNEL_MMA)

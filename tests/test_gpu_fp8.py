@@ -74,6 +74,19 @@ def test_fp8_kernels(kernel, dtype, D, Q, Hq, Hkv):
     run_fp8(wl, kernel=kernel)
 
 
+# Four and five column groups over FP8 codes (25 to 40 query rows per KV
+# head in one CTA), with and without splits.
+@pytest.mark.parametrize("Q,Hq,Hkv,cg", [(4, 32, 4, 4), (5, 32, 4, 5), (9, 12, 3, 5)])
+@pytest.mark.parametrize("split_blocks", [0, 3])
+def test_fp8_wide_column_groups(Q, Hq, Hkv, cg, split_blocks):
+    lens = [Q, Q + 1, Q + 15, Q + 33, 250, 700]
+    p = pkv.plan(len(lens), Q, Hq, Hkv, 128, max(lens), "fp8", kernel=2)
+    assert p["row_chunks"] == 1 and p["threads_per_cta"] == 32 * cg
+    wl = W.Workload(f"fp8 cg{cg} Q{Q} {Hq}/{Hkv} sb{split_blocks}", len(lens), Hq, Hkv, 128,
+                    "bf16", context_lens=lens, num_queries=Q, seed=1500 + Q + Hq + split_blocks)
+    run_fp8(wl, kernel=2, split_blocks=split_blocks)
+
+
 @pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("split_blocks", [1, 3, 16])
 def test_fp8_splits(kernel, split_blocks):

@@ -435,6 +435,34 @@ def test_mma_multi_tile_warps(dtype, D, warp_tiles, Q, Hq, Hkv, split_blocks):
     run_case(wl, kernel=2, split_blocks=split_blocks, warp_tiles=warp_tiles)
 
 
+# Four and five column groups: 25 to 40 query rows per KV head in one CTA,
+# each staged block read once for all of them.  Full and partial last
+# tiles, both rings, splits.
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D,Q,Hq,Hkv,cg", [
+    (128, 4, 32, 4, 4), (128, 5, 32, 4, 5), (128, 9, 12, 3, 5), (128, 33, 1, 1, 5),
+    (64, 10, 16, 4, 5), (64, 26, 1, 1, 4)])
+@pytest.mark.parametrize("split_blocks", [0, 3])
+def test_mma_wide_column_groups(dtype, D, Q, Hq, Hkv, cg, split_blocks):
+    import paged_kv_cache_18_gb300 as pkv
+    lens = [Q, Q + 1, Q + 15, Q + 33, 250, 700]
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    accepted = []
+    for stages in (1, 2, 3, 4, 6):
+        try:
+            p = pkv.plan(len(lens), Q, Hq, Hkv, D, max(lens), tdt, kernel=2, stages=stages)
+        except pkv.PkvError:
+            continue
+        accepted.append(stages)
+        assert p["row_chunks"] == 1 and -(-p["rows_per_cta"] // 8) == cg
+        assert p["threads_per_cta"] == 32 * cg
+        wl = W.Workload(f"{dtype} D{D} cg{cg} Q{Q} {Hq}/{Hkv} st{stages} sb{split_blocks}",
+                        len(lens), Hq, Hkv, D, dtype, context_lens=lens, num_queries=Q,
+                        seed=1400 + D + 11 * Q + Hq + stages + split_blocks)
+        run_case(wl, kernel=2, split_blocks=split_blocks, stages=stages)
+    assert accepted == [4, 6], accepted
+
+
 def test_mma_multi_tile_rejects_oversize():
     import paged_kv_cache_18_gb300 as pkv
     with tuning(warp_tiles=2), pytest.raises(pkv.PkvError):
