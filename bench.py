@@ -60,6 +60,7 @@ PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mma.cuh",
                   "paged_kv_cache_18_gb300/csrc/attn_mma.cu",
                   "paged_kv_cache_18_gb300/csrc/attn_simt.cuh",
+                  "paged_kv_cache_18_gb300/csrc/attn_merge.cu",
                   "paged_kv_cache_18_gb300/csrc/pkv_device.cuh"]
 PREFILL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_prefill.cu",
                    "paged_kv_cache_18_gb300/csrc/tc_ptx.cuh",
