@@ -101,7 +101,9 @@ enum {
 typedef enum pkv_kernel {
   PKV_KERNEL_AUTO = 0,
   PKV_KERNEL_SIMT = 1, /* CUDA-core dot products (any dtype; fp32 path) */
-  PKV_KERNEL_MMA = 2,  /* tensor-core tiles (bf16 / fp16 q; 16-bit or FP8 cache) */
+  PKV_KERNEL_MMA = 2,  /* tensor-core tiles (bf16 / fp16 q; 16-bit or FP8 cache);
+                          up to 40 query rows per KV head in one CTA at head_dim
+                          <= 128 (8 at 256), more cut into row chunks */
   PKV_KERNEL_TC = 3    /* tcgen05 tiles with TMEM accumulators: bf16 / fp16 caches,
                           head_dim 128, up to 32 query rows per CTA, no fused append */
 } pkv_kernel;
@@ -110,8 +112,11 @@ typedef enum pkv_kernel {
 typedef struct pkv_options {
   int kernel;       /* pkv_kernel */
   int split_blocks; /* 0: planner; > 0: KV blocks per split-K chunk */
-  int stages;       /* 0: planner; tensor-core kernel: per-warp ring depth
-                       (2 or 3 at head_dim <= 128, 1 or 2 at 256) */
+  int stages;       /* 0: planner; tensor-core kernel: ring depth per block
+                       lane, the tile's shallow or deep ring (at head_dim <= 128:
+                       2 or 3 with one column group, 3 or 4 with two, 4 or 6
+                       with three to five; 1 or 2 at 256; twice these for FP8
+                       caches); other values are refused */
   int rows_per_cta; /* 0: planner; cap on the query rows one CTA serves */
   int merge;        /* split-K merge: 0 planner, 1 by the sequence's last CTA,
                        2 by a separate kernel */
