@@ -277,7 +277,8 @@ def test_tree_workload_full_size():
 # ---- fused append + attention (one launch) --------------------------------
 @pytest.mark.parametrize("dtype,kernel", [("f32", "simt"), ("bf16", "simt"), ("bf16", "mma"),
                                           ("f16", "mma")])
-@pytest.mark.parametrize("Q,Hq,Hkv", [(1, 8, 2), (1, 4, 4), (5, 32, 8), (3, 8, 1)])
+@pytest.mark.parametrize("Q,Hq,Hkv", [(1, 8, 2), (1, 4, 4), (5, 32, 8), (3, 8, 1), (8, 32, 8),
+                                     (10, 16, 4), (13, 8, 2)])
 @pytest.mark.parametrize("split_blocks", [0, 1, 3])
 def test_fused_append_attention(dtype, kernel, Q, Hq, Hkv, split_blocks):
     import paged_kv_cache_18_gb300 as pkv
