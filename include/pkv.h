@@ -81,7 +81,8 @@ typedef enum pkv_status {
   PKV_ERR_UNSUPPORTED = 2, /* valid but not built: head_dim, block_size, dtype */
   PKV_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
   PKV_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
-  PKV_ERR_ALIGNMENT = 5    /* a tensor pointer is not 16-byte aligned */
+  PKV_ERR_ALIGNMENT = 5,   /* a tensor pointer is not 16-byte aligned */
+  PKV_ERR_HOST_MEMORY = 6  /* a host allocation failed (block manager) */
 } pkv_status;
 
 /* Element types.  PKV_FP8_E4M3 is a cache type only (one byte per element,
@@ -561,7 +562,9 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
  *   - hash = 64-bit FNV-1a over (parent hash as 8 little-endian bytes, 0 for
  *     the first block) then the block's token ids as 4 little-endian bytes.
  * The manager is host memory only and not thread-safe: serialise calls on
- * one manager.  Block ids index the caches' first dimension.
+ * one manager.  Block ids index the caches' first dimension.  A call that
+ * returns PKV_ERR_HOST_MEMORY (the host ran out of memory part-way) may have
+ * left the manager inconsistent: destroy it.
  */
 typedef struct pkv_block_manager pkv_block_manager;
 

@@ -139,16 +139,34 @@ struct pkv_block_manager {
 
 using pkv_bm = pkv_block_manager;
 
+namespace {
+// The manager's vectors, maps and sets allocate host memory and may throw
+// std::bad_alloc; no exception crosses the C boundary.
+template <typename F> pkv_status guarded(F &&body) {
+  try {
+    return body();
+  } catch (...) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+}
+}  // namespace
+
 extern "C" {
 
 pkv_block_manager *pkv_bm_create(int64_t num_blocks, int block_size) {
   if (num_blocks < 1 || num_blocks > (int64_t(1) << 31) - 1 || block_size < 1) return nullptr;
   pkv_bm *m = new (std::nothrow) pkv_bm;
   if (!m) return nullptr;
-  m->num_blocks = num_blocks;
-  m->block_size = block_size;
-  m->blocks.resize(static_cast<size_t>(num_blocks));
-  m->free_stack.reserve(static_cast<size_t>(num_blocks));
+  try {
+    m->num_blocks = num_blocks;
+    m->block_size = block_size;
+    m->blocks.resize(static_cast<size_t>(num_blocks));
+    m->free_stack.reserve(static_cast<size_t>(num_blocks));
+  } catch (...) {
+    delete m;
+    return nullptr;
+  }
+  // within the reserved capacity: no allocation
   for (int64_t b = num_blocks - 1; b >= 0; --b) m->free_stack.push_back(static_cast<int32_t>(b));
   return m;
 }
@@ -180,36 +198,38 @@ pkv_status pkv_bm_append(pkv_block_manager *m, int64_t seq_id, const int32_t *to
 pkv_status pkv_bm_add_sequence(pkv_block_manager *m, int64_t seq_id, const int32_t *tokens, int n,
                                int use_prefix_cache, int *cached_tokens, int64_t *slots) {
   if (!m || n < 0 || (n > 0 && !tokens) || m->seqs.count(seq_id)) return PKV_ERR_INVALID_ARG;
-  const int bs = m->block_size;
-  // Prefix lookup, taking nothing yet: walk the prompt's full blocks from the
-  // start and stop at the first miss.
-  std::vector<int32_t> hits;
-  if (use_prefix_cache) {
-    uint64_t parent = 0;
-    for (int i = 0; static_cast<int64_t>(i + 1) * bs <= n; ++i) {
-      const uint64_t h = pkv::block_hash(parent, tokens + static_cast<int64_t>(i) * bs, bs);
-      const auto it = m->by_hash.find(h);
-      if (it == m->by_hash.end()) break;
-      hits.push_back(it->second);
-      parent = h;
+  return guarded([&]() -> pkv_status {
+    const int bs = m->block_size;
+    // Prefix lookup, taking nothing yet: walk the prompt's full blocks from the
+    // start and stop at the first miss.
+    std::vector<int32_t> hits;
+    if (use_prefix_cache) {
+      uint64_t parent = 0;
+      for (int i = 0; static_cast<int64_t>(i + 1) * bs <= n; ++i) {
+        const uint64_t h = pkv::block_hash(parent, tokens + static_cast<int64_t>(i) * bs, bs);
+        const auto it = m->by_hash.find(h);
+        if (it == m->by_hash.end()) break;
+        hits.push_back(it->second);
+        parent = h;
+      }
     }
-  }
-  const int cached = static_cast<int>(hits.size()) * bs;
-  // Capacity for the rest of the prompt, checked before anything changes; a
-  // hit that nobody holds stops being evictable once it is taken.
-  int64_t avail = static_cast<int64_t>(m->free_stack.size() + m->evictable.size());
-  for (int32_t b : hits)
-    if (m->blocks[b].ref == 0) --avail;
-  if ((static_cast<int64_t>(n - cached) + bs - 1) / bs > avail) return PKV_ERR_WORKSPACE;
-  pkv::Sequence &s = m->seqs[seq_id];
-  for (int32_t b : hits) {
-    m->retain(b);
-    s.blocks.push_back(b);
-  }
-  s.tokens.assign(tokens, tokens + cached);
-  if (cached_tokens) *cached_tokens = cached;
-  int num_cow = 0;
-  return pkv_bm_append(m, seq_id, tokens + cached, n - cached, slots, nullptr, nullptr, &num_cow);
+    const int cached = static_cast<int>(hits.size()) * bs;
+    // Capacity for the rest of the prompt, checked before anything changes; a
+    // hit that nobody holds stops being evictable once it is taken.
+    int64_t avail = static_cast<int64_t>(m->free_stack.size() + m->evictable.size());
+    for (int32_t b : hits)
+      if (m->blocks[b].ref == 0) --avail;
+    if ((static_cast<int64_t>(n - cached) + bs - 1) / bs > avail) return PKV_ERR_WORKSPACE;
+    pkv::Sequence &s = m->seqs[seq_id];
+    for (int32_t b : hits) {
+      m->retain(b);
+      s.blocks.push_back(b);
+    }
+    s.tokens.assign(tokens, tokens + cached);
+    if (cached_tokens) *cached_tokens = cached;
+    int num_cow = 0;
+    return pkv_bm_append(m, seq_id, tokens + cached, n - cached, slots, nullptr, nullptr, &num_cow);
+  });
 }
 
 pkv_status pkv_bm_append(pkv_block_manager *m, int64_t seq_id, const int32_t *tokens, int n,
@@ -217,60 +237,70 @@ pkv_status pkv_bm_append(pkv_block_manager *m, int64_t seq_id, const int32_t *to
   if (!m || n < 0 || (n > 0 && !tokens)) return PKV_ERR_INVALID_ARG;
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end()) return PKV_ERR_INVALID_ARG;
-  pkv::Sequence &s = it->second;
-  const int bs = m->block_size;
-  // Blocks this call needs: new ones, plus one copy if the last block is
-  // shared and will be written.  Checked first, so a call that cannot be
-  // served changes nothing.
-  const size_t len = s.tokens.size();
-  const size_t have = s.blocks.size();
-  const size_t need = (len + static_cast<size_t>(n) + bs - 1) / bs;
-  int64_t want = static_cast<int64_t>(need > have ? need - have : 0);
-  const bool cow = n > 0 && len % bs != 0 && m->blocks[s.blocks.back()].ref > 1;
-  if (cow) ++want;
-  if (want > static_cast<int64_t>(m->free_stack.size() + m->evictable.size()))
-    return PKV_ERR_WORKSPACE;
-  int ncow = 0;
-  if (cow) {
-    // copy-on-write: the sequence gets its own copy of the shared partial
-    // block before writing into it
-    const int32_t src = s.blocks.back();
-    const int32_t dst = m->allocate();
-    m->release(src);
-    s.blocks.back() = dst;
-    if (cow_src) cow_src[0] = src;
-    if (cow_dst) cow_dst[0] = dst;
-    ncow = 1;
-  }
-  for (int t = 0; t < n; ++t) {
-    const size_t pos = s.tokens.size();
-    if (pos % bs == 0) s.blocks.push_back(m->allocate());
-    const int32_t b = s.blocks[pos / bs];
-    if (slots) slots[t] = static_cast<int64_t>(b) * bs + static_cast<int64_t>(pos % bs);
-    s.tokens.push_back(tokens[t]);
-    if ((pos + 1) % bs == 0) m->seal(s, pos / bs);
-  }
-  if (num_cow) *num_cow = ncow;
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    pkv::Sequence &s = it->second;
+    const int bs = m->block_size;
+    // Blocks this call needs: new ones, plus one copy if the last block is
+    // shared and will be written.  Checked first, so a call that cannot be
+    // served changes nothing.
+    const size_t len = s.tokens.size();
+    const size_t have = s.blocks.size();
+    const size_t need = (len + static_cast<size_t>(n) + bs - 1) / bs;
+    int64_t want = static_cast<int64_t>(need > have ? need - have : 0);
+    const bool cow = n > 0 && len % bs != 0 && m->blocks[s.blocks.back()].ref > 1;
+    if (cow) ++want;
+    if (want > static_cast<int64_t>(m->free_stack.size() + m->evictable.size()))
+      return PKV_ERR_WORKSPACE;
+    // the sequence's own growth, reserved before anything changes
+    s.blocks.reserve(need);
+    s.tokens.reserve(len + static_cast<size_t>(n));
+    int ncow = 0;
+    if (cow) {
+      // copy-on-write: the sequence gets its own copy of the shared partial
+      // block before writing into it
+      const int32_t src = s.blocks.back();
+      const int32_t dst = m->allocate();
+      m->release(src);
+      s.blocks.back() = dst;
+      if (cow_src) cow_src[0] = src;
+      if (cow_dst) cow_dst[0] = dst;
+      ncow = 1;
+    }
+    for (int t = 0; t < n; ++t) {
+      const size_t pos = s.tokens.size();
+      if (pos % bs == 0) s.blocks.push_back(m->allocate());
+      const int32_t b = s.blocks[pos / bs];
+      if (slots) slots[t] = static_cast<int64_t>(b) * bs + static_cast<int64_t>(pos % bs);
+      s.tokens.push_back(tokens[t]);
+      if ((pos + 1) % bs == 0) m->seal(s, pos / bs);
+    }
+    if (num_cow) *num_cow = ncow;
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_bm_fork(pkv_block_manager *m, int64_t parent, int64_t child) {
   if (!m || m->seqs.count(child)) return PKV_ERR_INVALID_ARG;
   const auto it = m->seqs.find(parent);
   if (it == m->seqs.end()) return PKV_ERR_INVALID_ARG;
-  pkv::Sequence copy = it->second;
-  for (int32_t b : copy.blocks) m->retain(b);
-  m->seqs.emplace(child, std::move(copy));
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    pkv::Sequence copy = it->second;  // allocated before any count changes
+    auto &slot = m->seqs[child];
+    for (int32_t b : copy.blocks) m->retain(b);
+    slot = std::move(copy);
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_bm_free(pkv_block_manager *m, int64_t seq_id) {
   if (!m) return PKV_ERR_INVALID_ARG;
   const auto it = m->seqs.find(seq_id);
   if (it == m->seqs.end()) return PKV_ERR_INVALID_ARG;
-  for (int32_t b : it->second.blocks) m->release(b);
-  m->seqs.erase(it);
-  return PKV_OK;
+  return guarded([&]() -> pkv_status {
+    for (int32_t b : it->second.blocks) m->release(b);
+    m->seqs.erase(it);
+    return PKV_OK;
+  });
 }
 
 pkv_status pkv_bm_sequence(const pkv_block_manager *m, int64_t seq_id, int32_t *blocks,

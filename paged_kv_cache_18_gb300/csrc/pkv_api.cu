@@ -492,6 +492,7 @@ const char *pkv_status_string(pkv_status status) {
     case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case PKV_ERR_CUDA: return "CUDA runtime or launch error";
     case PKV_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case PKV_ERR_HOST_MEMORY: return "host memory allocation failed";
     default: return "unknown status";
   }
 }

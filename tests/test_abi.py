@@ -44,8 +44,9 @@ def test_only_the_c_abi_is_exported(L):
 
 def test_version_and_status_strings(L):
     assert "sm_103a" in binding.version()
-    names = [L.pkv_status_string(i).decode() for i in range(7)]
-    assert names[0] == "ok" and len(set(names)) == 7
+    names = [L.pkv_status_string(i).decode() for i in range(8)]
+    assert names[0] == "ok" and len(set(names)) == 8
+    assert names[6] == "host memory allocation failed" and names[7] == "unknown status"
 
 
 # --- argument validation (returns before any CUDA call) -------------------
