@@ -61,13 +61,15 @@ cudaError_t current_sm_count(int *device, int *sms) {
 }
 
 // Once per (kernel, device): allow the kernel's dynamic shared memory and
-// ask the occupancy calculator how many CTAs fit on one SM.
+// ask the occupancy calculator how many CTAs fit on one SM.  One slot per
+// kernel instantiation a process uses (the library builds about 250).
+constexpr int kMaxKernels = 1024;
 struct FuncSlot {
   const void *func;
   std::atomic<int> ctas[kMaxDevices];
 };
 std::mutex g_func_mu;
-FuncSlot g_funcs[256];
+FuncSlot g_funcs[kMaxKernels];
 int g_nfuncs = 0;
 
 cudaError_t prepare_kernel(const KernelInfo &k, int device, int *ctas_per_sm) {
@@ -77,7 +79,7 @@ cudaError_t prepare_kernel(const KernelInfo &k, int device, int *ctas_per_sm) {
     for (int i = 0; i < g_nfuncs; ++i)
       if (g_funcs[i].func == k.func) slot = &g_funcs[i];
     if (!slot) {
-      if (g_nfuncs >= 256) return cudaErrorMemoryAllocation;
+      if (g_nfuncs >= kMaxKernels) return cudaErrorMemoryAllocation;
       slot = &g_funcs[g_nfuncs++];
       slot->func = k.func;
       for (auto &c : slot->ctas) c.store(0);
