@@ -117,6 +117,8 @@ def test_plan_kernel_choice():
     (128, 1, 32, 8, 128, 4096, torch.bfloat16), (2, 1, 32, 8, 128, 65536, torch.bfloat16),
     (16, 5, 32, 8, 128, 8192, torch.bfloat16), (3, 7, 64, 2, 64, 1000, torch.float16),
     (1, 1, 128, 1, 256, 300, torch.bfloat16), (5, 3, 16, 2, 256, 70, torch.float32),
+    (16, 10, 32, 8, 128, 8192, torch.bfloat16), (3, 9, 12, 3, 128, 500, torch.float16),
+    (2, 13, 8, 2, 128, 3000, torch.bfloat16), (4, 33, 8, 8, 64, 900, torch.float16),
 ])
 @pytest.mark.parametrize("kernel", [0, 1])
 def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
