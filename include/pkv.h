@@ -202,8 +202,12 @@ PKV_API pkv_status pkv_attention_plan_for(int batch, int num_queries, int num_he
 /*
  * pkv_attention_workspace_size -- device workspace bytes an attention call
  * with these sizes needs on the current device (the split-K partials: one
- * float32 output vector and one float32 log-sum-exp per query row and split).
- * 0 when the plan does not split.
+ * float32 output vector and one float32 log-sum-exp per query row and split;
+ * when the last CTA of a sequence merges its splits, also one 32-bit arrival
+ * counter per (sequence, KV head, row chunk), which every call zeroes on its
+ * stream, by a small kernel enqueued just before the attention launch).
+ * 0 when the plan does not split.  Nothing in the workspace needs to be
+ * initialised by the caller.
  */
 PKV_API pkv_status pkv_attention_workspace_size(int batch, int num_queries,
                                         int num_heads, int num_kv_heads,
@@ -226,9 +230,12 @@ PKV_API pkv_status pkv_attention_workspace_size(int batch, int num_queries,
  *   context_lens  : [batch] int32, device, 0 <= L_b <= max_context_len
  *   max_context_len: host-side upper bound of context_lens (sizes the
  *                   split-K grid; no device read is made to find it)
- *   scale         : softmax scale (1/sqrt(head_dim) for standard attention)
+ *   scale         : softmax scale; zero or negative selects 1/sqrt(head_dim),
+ *                   the scale of standard attention; NaN or infinite is
+ *                   PKV_ERR_INVALID_ARG
  *   workspace     : device buffer of pkv_attention_workspace_size() bytes
- *                   (may be NULL when that size is 0), 16-byte aligned
+ *                   (may be NULL when that size is 0), 16-byte aligned; its
+ *                   contents before the call do not matter
  *   options       : NULL or launch controls; error_word: NULL or device int32
  * Supported: head_dim in {64, 128, 256}, block_size 16, dtype F32/BF16/F16.
  */
@@ -464,7 +471,8 @@ PKV_API pkv_status pkv_mla_append(const void *ckv_new, void *ckv_cache,
  *   context_lens device int32 [batch]: rows in sequence b's cache, the
  *                chunk's own rows included (L_b >= q_len_b).
  *   Row j of sequence b sees cache rows i <= L_b - q_len_b + j.
- *   scale: the softmax scale, > 0 (PKV_ERR_INVALID_ARG otherwise).
+ *   scale: the softmax scale; zero or negative selects 1/sqrt(head_dim);
+ *          NaN or infinite is PKV_ERR_INVALID_ARG.
  *   head_dim 64 or 128; block_size 16; num_heads / num_kv_heads must divide
  *   128.  No workspace: the work is split over query rows (256 per CTA),
  *   not over keys.  options: only `stages` is read: the K/V ring depth
@@ -525,11 +533,16 @@ PKV_API pkv_status pkv_check_bounded_wait(int32_t *error_word, uint32_t limit_us
  *     nothing enqueued; a larger split_blocks in `options` shrinks the need.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
- *   - All calls share the one array.  Nothing in it needs to start at zero
- *     (every partial is written before it is read within a call), but calls
- *     whose work overlaps on the GPU (other streams, other threads) race on
- *     it: serialise them.
+ *     stream capture.  With lazy module loading (the CUDA default), that
+ *     lookup may also be what loads the library's device code on the device
+ *     and commits the array's memory, so it can fail under memory pressure
+ *     (PKV_ERR_CUDA): make the first call at start-up.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Nothing in it needs to start at zero: every partial is written before
+ *     it is read within a call, and the split-K arrival counters are zeroed
+ *     by each call on its stream before its attention kernel counts in them.
+ *     Calls whose work overlaps on the GPU (other streams, other threads)
+ *     race on it: serialise them.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
 PKV_API pkv_status pkv_paged_decode_attention_noalloc(

@@ -9,7 +9,6 @@ been built, or a call fails, an exception is raised.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 from typing import Optional
@@ -282,7 +281,7 @@ def _attention(q, k_cache, v_cache, block_table, context_lens, scale, max_contex
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0  # device read
     if scale is None:
-        scale = 1.0 / math.sqrt(D)
+        scale = 0.0  # the library's default: 1/sqrt(head_dim)
     if out is None:
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
@@ -372,7 +371,7 @@ def append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0  # device read
     if scale is None:
-        scale = 1.0 / math.sqrt(D)
+        scale = 0.0  # the library's default: 1/sqrt(head_dim)
     if out is None:
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
@@ -433,7 +432,7 @@ def append_attention_host(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
     _need(context_lens.dtype == torch.int32 and context_lens.shape == (B,), "context_lens")
     _need(staging.is_cuda and staging.device == k_cache.device, "staging must be on the caches' GPU")
     if scale is None:
-        scale = 1.0 / math.sqrt(D)
+        scale = 0.0  # the library's default: 1/sqrt(head_dim)
     _check("pkv_append_attention_host", lib().pkv_append_attention_host(
         out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
         v_cache.data_ptr(), block_table.data_ptr(), block_table.shape[1],
@@ -560,7 +559,7 @@ def tree_verify_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0  # device read
     if scale is None:
-        scale = 1.0 / math.sqrt(D)
+        scale = 0.0  # the library's default: 1/sqrt(head_dim)
     if out is None:
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
@@ -627,7 +626,7 @@ def paged_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if B else 0  # device read
     if scale is None:
-        scale = 1.0 / math.sqrt(D)
+        scale = 0.0  # the library's default: 1/sqrt(head_dim)
     if out is None:
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")
@@ -799,7 +798,7 @@ def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     if max_query_len is None:
         max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if B else 0
     if scale is None:
-        scale = 1.0 / math.sqrt(D)
+        scale = 0.0  # the library's default: 1/sqrt(head_dim)
     if out is None:
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out")

@@ -23,6 +23,8 @@
 // The kernel is a programmatic dependent of the attention kernel: it may be
 // scheduled while that kernel still runs (which hides its launch), reads
 // only the call's inputs before pdl_wait, and the partials after it.
+#include <algorithm>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -144,7 +146,25 @@ cudaError_t merge_t(int D, const AttnParams &p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// Zero the split-K arrival counters of one call.  The attention kernel is
+// launched right after it as its programmatic dependent, so that kernel's
+// launch and main loop overlap this one; it waits for it (pdl_wait) only
+// before its first arrival.
+__global__ void __launch_bounds__(256) zero_words_kernel(unsigned int *words, int n) {
+  pdl_launch_dependents();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    words[i] = 0u;
+}
+
 }  // namespace
+
+cudaError_t zero_counters_launch(unsigned int *words, int64_t n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  if (n > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int ctas = static_cast<int>(std::min<int64_t>((n + 255) / 256, 64));
+  zero_words_kernel<<<ctas, 256, 0, stream>>>(words, static_cast<int>(n));
+  return cudaGetLastError();
+}
 
 cudaError_t merge_launch(pkv_dtype dtype, int head_dim, const AttnParams &p, int /*sm_count*/,
                          cudaStream_t stream) {

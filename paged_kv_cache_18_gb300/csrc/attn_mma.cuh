@@ -687,9 +687,11 @@ template <typename T, typename TC, int D, int CG, int NT, int KB, bool DEEP>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
   const KernelInfo k = mma_info_t<T, TC, D, CG, NT, KB, DEEP>();
-  attn_mma_kernel<T, TC, D, CG, NT, KB, mma_lanes<CG>(), mma_stages_t<TC, D, CG, DEEP>()>
-      <<<grid, k.threads, k.smem, stream>>>(km, vm, p);
-  return cudaGetLastError();
+  // with split-K counters: a dependent of the kernel that zeroes them
+  return launch_kernel(p.counters != nullptr,
+                       attn_mma_kernel<T, TC, D, CG, NT, KB, mma_lanes<CG>(),
+                                       mma_stages_t<TC, D, CG, DEEP>()>,
+                       grid, k.threads, k.smem, stream, km, vm, p);
 }
 
 // Default ring: the shallow one (for one column group at head_dim <= 128,

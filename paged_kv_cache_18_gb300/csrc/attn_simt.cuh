@@ -360,9 +360,10 @@ KernelInfo simt_info_t() {
 template <typename TQ, typename TC, int D, int R>
 cudaError_t simt_launch_t(const AttnParams &p, dim3 grid, cudaStream_t stream) {
   const KernelInfo k = simt_info_t<TQ, TC, D, R>();
-  attn_simt_kernel<TQ, TC, D, R, kSimtWarps, simt_stages<TC, D>()>
-      <<<grid, k.threads, k.smem, stream>>>(p);
-  return cudaGetLastError();
+  // with split-K counters: a dependent of the kernel that zeroes them
+  return launch_kernel(p.counters != nullptr,
+                       attn_simt_kernel<TQ, TC, D, R, kSimtWarps, simt_stages<TC, D>()>, grid,
+                       k.threads, k.smem, stream, p);
 }
 
 // Query rows per CTA: R * D / 8 registers of query and of accumulator per

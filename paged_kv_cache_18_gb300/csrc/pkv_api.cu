@@ -41,6 +41,12 @@ bool valid_cache_dtype(int dt) { return valid_dtype(dt) || dt == PKV_FP8_E4M3; }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// The softmax scale of a call: a positive argument as given; zero or a
+// negative value selects 1/sqrt(head_dim), the scale of standard attention.
+float softmax_scale(float scale, int head_dim) {
+  return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim)));
+}
+
 struct DeviceInfo {
   std::atomic<int> sm_count{0};
 };
@@ -186,8 +192,9 @@ bool choose_kernel(const Shape &s, const pkv_options *opt, pkv_plan *pl, KernelI
 
 // Split-K workspace: float32 partial outputs, their log-sum-exps and, when
 // the last CTA of a sequence merges (at most kMaxFusedSplits splits), one
-// 64-bit arrival counter per (sequence, KV head, row chunk).  Regions are
-// 256-byte aligned.
+// 32-bit arrival counter per (sequence, KV head, row chunk), zeroed by every
+// call before its attention kernel counts in it.  Regions are 256-byte
+// aligned.
 struct WorkspaceLayout {
   size_t lse_off, ctr_off, total;
   bool fused_merge;
@@ -207,11 +214,9 @@ WorkspaceLayout workspace_layout(const Shape &s, int num_splits, int row_chunks,
   w.total = w.ctr_off;
   if (w.fused_merge)
     w.total += up(static_cast<size_t>(s.batch) * s.num_kv_heads * row_chunks *
-                  sizeof(unsigned long long));
+                  sizeof(unsigned int));
   return w;
 }
-
-std::atomic<uint32_t> g_epoch{1};
 
 // Split-K partition.  A sequence of n blocks is cut into chunks of
 // split_blocks blocks; each chunk is one CTA.  Splitting pays when the
@@ -384,6 +389,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
     return PKV_ERR_INVALID_ARG;
   if (num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
+  scale = softmax_scale(scale, s.head_dim);
   if (static_cast<int64_t>(s.max_context_len) >
       static_cast<int64_t>(max_blocks_per_seq) * s.block_size)
     return PKV_ERR_INVALID_ARG;
@@ -442,10 +448,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
     p.part_o = reinterpret_cast<float *>(base);
     p.part_lse = reinterpret_cast<float *>(base + w.lse_off);
     if (w.fused_merge) {
-      p.counters = reinterpret_cast<unsigned long long *>(base + w.ctr_off);
-      uint32_t e = g_epoch.fetch_add(1, std::memory_order_relaxed);
-      if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed);  // 0 never tags a call
-      p.epoch = e;
+      p.counters = reinterpret_cast<unsigned int *>(base + w.ctr_off);
     } else {
       merge_kernel = true;
     }
@@ -453,6 +456,13 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
 
   const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
   cudaError_t e;
+  if (p.counters != nullptr) {
+    // whatever the workspace held: the counters start at zero
+    e = zero_counters_launch(p.counters,
+                             static_cast<int64_t>(s.batch) * s.num_kv_heads * pl.row_chunks,
+                             stream);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+  }
   if (pl.kernel == PKV_KERNEL_MMA) {
     CUtensorMap kmap, vmap;
     if (!encode_cache_map(&kmap, k_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks) ||
@@ -587,7 +597,7 @@ pkv_status pkv_paged_prefill_attention(void *out, const void *q, const void *k_c
   if (batch == 0 || total_q == 0 || max_query_len == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens || !query_start)
     return PKV_ERR_INVALID_ARG;
-  if (num_blocks < 1 || max_blocks_per_seq < 1 || !(scale > 0.f) || !std::isfinite(scale))
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || !std::isfinite(scale))
     return PKV_ERR_INVALID_ARG;
   const int64_t rows = static_cast<int64_t>(max_query_len) * group;
   const int64_t pairs = (rows + prefill_rows_per_cta() - 1) / prefill_rows_per_cta();
@@ -616,7 +626,7 @@ pkv_status pkv_paged_prefill_attention(void *out, const void *q, const void *k_c
   p.num_kv_heads = num_kv_heads;
   p.group = group;
   p.pairs = static_cast<int>(pairs);
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale_log2 = softmax_scale(scale, head_dim) * 1.4426950408889634f;
   const cudaError_t e = prefill_launch(dtype, head_dim, stages, qmap, kmap, vmap, p,
                                        reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -1172,6 +1182,9 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(
     int block_size, int64_t num_blocks, float scale, pkv_dtype dtype,
     const pkv_options *options, int32_t *error_word, pkv_stream_t stream) {
   if (batch == 0) return PKV_OK;
+  // The size checked here and the size the launch below uses come from the
+  // same planner (device_plan, on the current device, with these arguments
+  // and options), so the launch never needs more than the bound checked.
   size_t need = 0;
   pkv_status st = pkv_attention_workspace_size(batch, 1, num_heads, num_kv_heads, head_dim,
                                                block_size, max_context_len, dtype, options, &need);

@@ -33,9 +33,9 @@ struct AttnParams {
   const void *v_new;            //   (nullptr: the cache already holds them)
   float *part_o;                // [B*Q*Hq, num_splits, D]   (split-K only)
   float *part_lse;              // [B*Q*Hq, num_splits]      (log2 units)
-  unsigned long long *counters; // [B, Hkv, row_chunks] arrivals (epoch << 32 | count);
+  unsigned int *counters;       // [B, Hkv, row_chunks] split arrivals, zeroed by a kernel
+                                //   launched just before this one (see split_arrive);
                                 //   nullptr: a separate merge kernel runs after
-  uint32_t epoch;               // tag of this call in the counters
   const unsigned long long *tree_mask;  // [B, Q] with stride mask_stride (0: shared),
                                         //   or nullptr: causal among the Q rows
   int64_t mask_stride;
@@ -121,6 +121,26 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel` on `stream`, as a programmatic dependent of the kernel
+// enqueued just before it when `dependent` is true (then it may start while
+// that kernel still runs, and must pdl_wait before it touches what that
+// kernel writes).
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(bool dependent, void (*kernel)(Params...), dim3 grid, int threads,
+                          size_t smem, cudaStream_t stream, Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = dependent ? attr : nullptr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -359,24 +379,18 @@ __device__ __forceinline__ void patch_new_rows(const AttnParams &p, uint32_t kti
 constexpr int kMaxFusedSplits = 32;
 
 // Split-K arrival: count this CTA in its (sequence, KV head, row chunk)
-// counter; true for the CTA that completes the count.  The counter word
-// holds (epoch << 32 | arrivals); a word left with another call's epoch
-// (or garbage) restarts at 1, and the completing CTA resets the count to 0
-// for the next call with the same epoch (a replayed CUDA graph).
+// counter; true for the CTA that completes the count.  The counters start at
+// zero whatever the workspace held before the call: the host enqueues a
+// zeroing kernel (zero_words_kernel) right before this launch, which runs as
+// its programmatic dependent, and the wait below returns only once that
+// kernel has completed and its writes are visible.  Everything before this
+// point overlaps it.
 __device__ __forceinline__ bool split_arrive(const AttnParams &p, int b, int kvh, int chunk,
                                              int ns_b) {
-  unsigned long long *ctr =
+  unsigned int *ctr =
       p.counters + (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * p.row_chunks + chunk;
-  const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
-  unsigned long long cur = atomicAdd(ctr, 0ull);
-  for (int it = 0; it < (1 << 20); ++it) {
-    const unsigned long long next = ((cur >> 32) == p.epoch) ? cur + 1 : (tag | 1ull);
-    const unsigned long long prev = atomicCAS(ctr, cur, next);
-    if (prev == cur) return static_cast<int>(next & 0xffffffffull) == ns_b;
-    cur = prev;
-  }
-  record_error(p.err, PKV_DEVERR_TIMEOUT);
-  return false;
+  pdl_wait();
+  return atomicAdd(ctr, 1u) + 1u == static_cast<unsigned int>(ns_b);
 }
 
 // CTA epilogue.  Every warp w has left, for each of the NC query columns of
@@ -494,9 +508,6 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
 #pragma unroll
     for (int e = 0; e < 4; ++e) dst[e] = from_float<T>(acc[e] * inv);
   }
-  if (tid == 0)
-    atomicExch(p.counters + (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * p.row_chunks + chunk,
-               static_cast<unsigned long long>(p.epoch) << 32);
 }
 
 }  // namespace pkv

@@ -79,6 +79,9 @@ constexpr int kMlaHeadsPerCta = 16;
 bool mla_kernel_info(pkv_dtype dtype, int rope_dim, int stages, KernelInfo *info);
 cudaError_t mla_launch(pkv_dtype dtype, int rope_dim, int stages, const CUtensorMap &cmap,
                        const AttnParams &p, dim3 grid, cudaStream_t stream);
+// Zero n 32-bit split-K arrival counters; the attention launch that follows
+// is its programmatic dependent.
+cudaError_t zero_counters_launch(unsigned int *words, int64_t n, cudaStream_t stream);
 // Split-K log-sum-exp merge.
 cudaError_t merge_launch(pkv_dtype dtype, int head_dim, const AttnParams &p, int sm_count,
                          cudaStream_t stream);

@@ -96,10 +96,11 @@ def errors(got: np.ndarray, ref: np.ndarray):
 
 def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what=""):
     """The stated bound per element, max-abs tol_abs, except where the output
-    type cannot hold it: a bf16 output of |ref| >= 2.56 is already up to half
-    an ulp (> 1e-2) from the exact value when correctly rounded (for example
-    4.07614 -> 4.0625), so there the bound is that half ulp plus 1e-3 of
-    arithmetic error.  Relative L2 over all elements: tol_rel."""
+    type cannot hold it: a bf16 output of |ref| >= 4 is already up to half an
+    ulp (2^-6 = 0.0156 > 1e-2) from the exact value when correctly rounded
+    (for example 4.07614 -> 4.0625), so there the bound is that half ulp plus
+    1e-3 of arithmetic error (below 4, half an ulp is at most 2^-8 and the
+    bound stays 1e-2).  Relative L2 over all elements: tol_rel."""
     mask = ~np.isnan(ref)
     assert np.isfinite(got[mask]).all(), f"{what}: non-finite output"
     max_abs, rel = errors(got, ref)

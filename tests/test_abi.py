@@ -136,7 +136,7 @@ def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
         o = B * Q * Hq * p["num_splits"] * D * 4
         lse = B * Q * Hq * p["num_splits"] * 4
         fused = p["num_splits"] <= 32 and p["rows_per_cta"] * p["num_splits"] <= 64
-        ctr = B * Hkv * p["row_chunks"] * 8 if fused else 0
+        ctr = B * Hkv * p["row_chunks"] * 4 if fused else 0   # 32-bit arrival counters
         assert p["workspace_bytes"] == (-(-o // 256) * 256 + -(-lse // 256) * 256
                                         + -(-ctr // 256) * 256)
         assert p["merge_kernel"] == (0 if fused else 1)

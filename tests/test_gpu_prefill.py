@@ -201,11 +201,18 @@ def test_prefill_rejects_what_it_does_not_run():
     with pytest.raises(binding.PkvError):
         pkv.paged_prefill_attention(d.q, d.k, d.v, d.table, d.lens, d.qs, max_query_len=8)
     wl = W.PrefillWorkload("rej", 1, 8, 2, 128, "bf16", chunk_lens=[8], prefix_lens=[0])
-    d = DevicePrefill(W.make_prefill_batch(wl))   # the scale must be positive
-    for bad in (0.0, -0.1):
+    d = DevicePrefill(W.make_prefill_batch(wl))   # the scale must be finite
+    for bad in (float("nan"), float("inf")):
         with pytest.raises(binding.PkvError):
             pkv.paged_prefill_attention(d.q, d.k, d.v, d.table, d.lens, d.qs, max_query_len=8,
                                         scale=bad)
+    # zero or below: the library's default 1/sqrt(head_dim), bitwise
+    pkv.kv_append(d.k_new, d.v_new, d.k, d.v, d.slots)
+    outs = [pkv.paged_prefill_attention(d.q, d.k, d.v, d.table, d.lens, d.qs, max_query_len=8,
+                                        scale=s).clone()
+            for s in (float(np.float32(1 / np.sqrt(128))), 0.0, -0.1)]
+    assert torch.isfinite(outs[0].float()).all()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     wl = W.PrefillWorkload("rej", 1, 8, 2, 256, "bf16", chunk_lens=[8], prefix_lens=[0])
     d = DevicePrefill(W.make_prefill_batch(wl))   # head_dim 256
     with pytest.raises(binding.PkvError):
@@ -214,7 +221,7 @@ def test_prefill_rejects_what_it_does_not_run():
 
 def test_prefill_full_size_workload():
     wl = W.PREFILL_WORKLOADS["prefill_llama3_8b"]
-    check(W.make_prefill_batch(wl), rows_per_seq=384, what=wl.name)
+    check(W.make_prefill_batch(wl), what=wl.name)   # every (position, head) row
 
 
 def test_prefill_step_replays_from_a_cuda_graph():
