@@ -16,6 +16,13 @@ from pinned host memory and the output read back every step.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the float64 CPU oracle, timed
 
+With the default workload the same line also carries `workloads`: every other
+named configuration (tiny, Llama-3-8B GQA, long-context split-K, speculative
+verify) timed the same way in the same run, each with its plan, roofline,
+clocks and a short oracle sample, and `cpu_baseline_twin`, the NumPy dense
+twin of the oracle timed in one process on the headline workload
+(`--no-workloads` skips both).
+
 `--workload mla_deepseek_v2` times an MLA decode step (mla_append of each
 sequence's newest latent row, then mla_decode_attention over the latent
 cache; value = latent GB/s).
@@ -499,26 +506,17 @@ def dev_tensor(a: np.ndarray, dtype: str, device):
     return torch.from_numpy(a).to(device)
 
 
-def run_ours(args):
+def decode_leg(args, name: str, dev, rank: int, world: int, local: int, steps: int,
+               warmup: int, e2e_on: bool, cpu_budget: float, clocks_on: bool) -> dict:
+    """Time one decode / verify workload: `warmup` untimed steps, then `steps`
+    timed ones (CUDA events on the launching stream, barrier and synchronise
+    on both sides); optionally the end-to-end leg through the host-buffer API
+    and the oracle's cpu_baseline.  Returns the measured fields (aggregated
+    over ranks where that applies)."""
     import torch
-    import torch.distributed as dist
-
-    rank, world, local = dist_env()
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    from paged_kv_cache_18_gb300 import build as pkv_build
-    if rank == 0 or not os.path.exists(pkv_build.LIB):
-        pkv_build.build()
-    barrier()
     import paged_kv_cache_18_gb300 as pkv
-    pkv.binding.TUNING.update(rows_per_cta=args.rows_per_cta, merge=args.merge,
-                              warp_tiles=args.warp_tiles, blocks_per_iter=args.blocks_per_iter,
-                              persistent=args.persistent)
 
-    wl = decode_workload(args.workload)
+    wl = decode_workload(name)
     if rank > 0:
         wl = W.Workload(**{**wl.__dict__, "seed": wl.seed + 100 * rank})
     b = W.make_batch(wl)
@@ -574,20 +572,17 @@ def run_ours(args):
             pkv.kv_append(kn, vn, k_cache, v_cache, sl)
             attn(qq, k_cache, v_cache, tb, ln, **opts)
 
-    def step():
-        attend(q, k_new, v_new, slots, table, lens)
-
     stream = torch.cuda.current_stream(dev)
-    for _ in range(args.warmup):
-        step()
+    for _ in range(warmup):
+        attend(q, k_new, v_new, slots, table, lens)
     torch.cuda.synchronize(dev)
 
     # Device-timed region: K steps, events around the attention of each step.
-    K = args.steps
+    K = steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
+    sampler = ClockSampler(local) if rank == 0 and clocks_on else None
     if sampler:
         time.sleep(0.3)
     barrier()
@@ -624,7 +619,7 @@ def run_ours(args):
     # output read back, every step.
     e2e = None
     kv_step = b.kv_bytes() // W.ELT_BYTES[wl.dtype] if fp8 else b.kv_bytes()  # 1 byte / element
-    if not args.no_e2e:
+    if e2e_on:
         host = {n: t.cpu().pin_memory() for n, t in
                 (("q", q), ("k_new", k_new), ("v_new", v_new), ("slots", slots),
                  ("table", table), ("lens", lens))}
@@ -679,9 +674,6 @@ def run_ours(args):
 
     total_kv = dist_sum(kv_step, dev)
     total_tokens = dist_sum(wl.batch * Q, dev)
-    if rank != 0:
-        return 0
-
     value = total_kv / (step_ms * 1e-3) / 1e9
     peaks, peak_kind = measured_peaks()
     splits_per_seq = None
@@ -694,45 +686,132 @@ def run_ours(args):
                                       fused_append=fused, q_elt_bytes=W.ELT_BYTES[wl.dtype])
     achieved = algo["total"] / (attn_ms * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
-    traffic = recorded_traffic(args.workload)
-    launches_per_step = (1 if fused else 2) + plan["merge_kernel"]
+    # the fused-merge plans enqueue a counter-zeroing kernel before the attention
+    zeroing = plan["num_splits"] > 1 and plan["merge_kernel"] == 0
+    launches_per_step = ((1 if fused else 2) + plan["merge_kernel"] + (1 if zeroing else 0))
 
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        nbytes, secs, desc = oracle_sample(W.make_batch(decode_workload(args.workload)),
-                                           args.cpu_budget)
+    if cpu_budget > 0 and world == 1:
+        nbytes, secs, desc = oracle_sample(W.make_batch(decode_workload(name)), cpu_budget)
         import oracle
         cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
                "kind": "oracle", "sample": desc}
 
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 cache, " + wl.dtype
-        if fp8 else wl.dtype, "data": "synthetic",
-        "config": {**workload_config(wl, b, fused),
-                   **({"kv_cache": f"fp8 e4m3, scales {FP8_K_SCALE}/{FP8_V_SCALE}",
-                       "kv_bytes_per_step": kv_step,
-                       "step": f"kv_append_fp8 of {wl.batch * Q} rows + paged_attention_fp8"}
-                      if fp8 else {})},
-        "pct_of_hbm_peak": 100.0 * value / peak,
-        "tokens_per_s": total_tokens / (step_ms * 1e-3),
-        "attention_ms": attn_ms,
+    config = {**workload_config(wl, b, fused),
+              **({"kv_cache": f"fp8 e4m3, scales {FP8_K_SCALE}/{FP8_V_SCALE}",
+                  "kv_bytes_per_step": kv_step,
+                  "step": f"kv_append_fp8 of {wl.batch * Q} rows + paged_attention_fp8"}
+                 if fp8 else {})}
+    return {
+        "value": value, "ms_per_step": step_ms, "tokens_per_s": total_tokens / (step_ms * 1e-3),
+        "attention_ms": attn_ms, "config": config,
+        "dtype": "fp8-e4m3 cache, " + wl.dtype if fp8 else wl.dtype,
         "plan": {k: plan[k] for k in ("kernel", "rows_per_cta", "row_chunks", "split_blocks",
                                       "num_splits", "grid_x", "grid_y", "grid_z",
                                       "stages", "ctas_per_sm", "merge_kernel")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "traffic": recorded_traffic(name),
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": algo["total"],
                      "kernel": ("fused append + attention" if fused else "attention")
                                + (" + split-K merge" if plan["num_splits"] > 1 else ""),
+                     "kernel_us": 1e3 * attn_ms,
                      "launches_per_step": launches_per_step},
-        "cpu_baseline": cpu,
-        "e2e": e2e,
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * K,
-        "clocks": clocks,
     }
+
+
+def twin_sample(b: W.PagedBatch, budget_s: float):
+    """Time the NumPy dense twin of the oracle (O2), one process, on whole
+    sequences of the workload, cycling over them, until about `budget_s`
+    of CPU work; returns (KV bytes covered, seconds, description)."""
+    from oracle import twin
+    wl = b.wl
+    done, elapsed, seqs = 0, 0.0, 0
+    while elapsed < budget_s:
+        bi = seqs % wl.batch
+        t = time.perf_counter()
+        twin.contiguous_attention(b.q[bi:bi + 1], b.k_cache, b.v_cache, b.block_table[bi:bi + 1],
+                                  b.context_lens[bi:bi + 1], wl.softmax_scale, wl.dtype)
+        elapsed += time.perf_counter() - t
+        done += 2 * int(b.context_lens[bi]) * wl.num_kv_heads * wl.head_dim * W.ELT_BYTES[wl.dtype]
+        seqs += 1
+    return done, elapsed, (f"{seqs} sequence passes over the {wl.batch} sequences of the "
+                           f"workload, NumPy float64 dense twin, one process, {elapsed:.1f} s")
+
+
+# The named configurations besides the headline one, measured in the same run.
+OTHER_WORKLOADS = ["tiny", "llama3_8b_gqa", "long_splitk", "spec_verify"]
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_cache_18_gb300 import build as pkv_build
+    if rank == 0 or not os.path.exists(pkv_build.LIB):
+        pkv_build.build()
+    barrier()
+    import paged_kv_cache_18_gb300 as pkv
+    pkv.binding.TUNING.update(rows_per_cta=args.rows_per_cta, merge=args.merge,
+                              warp_tiles=args.warp_tiles, blocks_per_iter=args.blocks_per_iter,
+                              persistent=args.persistent)
+
+    lead = decode_leg(args, args.workload, dev, rank, world, local, args.steps, args.warmup,
+                      not args.no_e2e, 0.0 if args.no_cpu_baseline else args.cpu_budget,
+                      not args.no_clocks)
+    torch.cuda.empty_cache()
+    others = {}
+    extra_launches = 0
+    if (args.workload == "llama2_13b" and args.kv_dtype == "native" and not args.no_workloads
+            and not args.unfused):
+        # every other named configuration, same step definition and timing
+        # rules, a short oracle sample each (the headline fields stay the
+        # Llama-2-13B layer's)
+        for name in OTHER_WORKLOADS:
+            leg = decode_leg(args, name, dev, rank, world, local, args.steps, args.warmup,
+                             False, 0.0 if args.no_cpu_baseline else 3.0, not args.no_clocks)
+            torch.cuda.empty_cache()
+            extra_launches += leg["gpu_launches"]
+            wl = decode_workload(name)
+            others[name] = {
+                "config": leg["config"], "value": leg["value"], "unit": "GB/s",
+                "ms_per_step": leg["ms_per_step"], "tokens_per_s": leg["tokens_per_s"],
+                "pct_of_hbm_peak": 100.0 * leg["value"] / leg["roofline"]["peak"],
+                "roofline": leg["roofline"], "plan": leg["plan"], "clocks": leg["clocks"],
+                "cpu_baseline": leg["cpu_baseline"],
+                "tokens": ("verified positions" if wl.num_queries > 1 else "decode tokens")}
+    twin = None
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "llama2_13b"
+            and not args.no_workloads):
+        nbytes, secs, desc = twin_sample(W.make_batch(decode_workload(args.workload)), 3.0)
+        twin = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1,
+                "kind": "oracle twin (NumPy, dense, float64)", "sample": desc}
+    if rank != 0:
+        return 0
+
+    line = {
+        "metric": METRIC, "value": lead["value"], "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": lead["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": lead["dtype"], "data": "synthetic", "config": lead["config"],
+        "pct_of_hbm_peak": 100.0 * lead["value"] / lead["roofline"]["peak"],
+        "tokens_per_s": lead["tokens_per_s"], "attention_ms": lead["attention_ms"],
+        "plan": lead["plan"], "roofline": lead["roofline"], "cpu_baseline": lead["cpu_baseline"],
+        "e2e": lead["e2e"], "gpu_launches": lead["gpu_launches"] + extra_launches,
+        "clocks": lead["clocks"],
+    }
+    if others:
+        line["workloads"] = others
+    if twin:
+        line["cpu_baseline_twin"] = twin
     print(json.dumps(line))
     return 0
 
@@ -992,6 +1071,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the headline workload only (no other named configurations)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

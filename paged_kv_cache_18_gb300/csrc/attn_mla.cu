@@ -130,19 +130,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       bool ok = true;
       int issued = 0;
+      int next = n_my > 0 ? ld_keep(table) : 0;  // each entry loaded one block ahead
       for (int i = 0; i < n_my; ++i) {
         const int s = i % NS;
+        const int v = next;
+        if (i + 1 < n_my) next = ld_keep(table + i + 1);
         if (i >= NS && !mbar_wait_bounded(smem_u32(&empty[s]), ((i / NS) - 1) & 1)) ok = false;
         if (!ok || s_abort) break;
-        const int v = __ldg(table + i);
         const bool bad = v < 0 || static_cast<int64_t>(v) >= p.num_blocks;
         if (bad) record_error(p.err, PKV_DEVERR_BLOCK_ID);
         const uint32_t bar = smem_u32(&full[s]);
         mbar_arrive_expect_tx(bar, G::kTileBytes);
+        if (p.tile_box) {  // the block's 16 latent rows in one copy
+          tma_load_5d(sbase + s * G::kTileBytes, &cmap, bar, 0, 0, 0, 0, bad ? 0 : v);
+        } else {
 #pragma unroll
-        for (int pn = 0; pn < G::kPanels; ++pn)
-          tma_load_4d(sbase + s * G::kTileBytes + pn * G::kPanelBytes, &cmap, bar, pn * 64, 0, 0,
-                      bad ? 0 : v);
+          for (int pn = 0; pn < G::kPanels; ++pn)
+            tma_load_4d(sbase + s * G::kTileBytes + pn * G::kPanelBytes, &cmap, bar, pn * 64, 0,
+                        0, bad ? 0 : v);
+        }
         issued = i + 1;
       }
       if (!ok) {
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // table entries of blocks 32 j .. 32 j + 31, one per lane (bad-block flags)
     auto entries = [&](int j) {
       const int i = 32 * j + lane;
-      return i < n_my ? __ldg(table + i) : 0;
+      return i < n_my ? ld_keep(table + i) : 0;
     };
     int tab = entries(0);
     bool aborted = false;

@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
                          blk_begin + bl;
   auto load_entries = [&](int chunk32) -> int {
     const int i = chunk32 * 32 + lane;
-    return i < n_my ? __ldg(table + static_cast<int64_t>(i) * BL) : -1;
+    return i < n_my ? ld_keep(table + static_cast<int64_t>(i) * BL) : -1;
   };
   int tab_cur = load_entries(0);
   int tab_next = load_entries(1);
@@ -286,13 +286,19 @@ __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
       const uint32_t bar = my_bars + 8 * s;
       const uint32_t st = my_stages + s * G::kStageBytes;
       mbar_arrive_expect_tx(bar, G::kStageBytes);
+      if (p.tile_box) {  // one copy per tile
+        tma_load_5d(st, &kmap, bar, 0, 0, 0, kvh, phys);
+        tma_load_5d(st + G::kTileBytes, &vmap, bar, 0, 0, 0, kvh, phys);
+      } else {           // one copy per 128-byte column panel
 #pragma unroll
-      for (int part = 0; part < G::kParts; ++part)
-        tma_load_4d(st + part * G::kPanelBytes, &kmap, bar, part * G::kPanelElems, 0, kvh, phys);
+        for (int part = 0; part < G::kParts; ++part)
+          tma_load_4d(st + part * G::kPanelBytes, &kmap, bar, part * G::kPanelElems, 0, kvh,
+                      phys);
 #pragma unroll
-      for (int part = 0; part < G::kParts; ++part)
-        tma_load_4d(st + G::kTileBytes + part * G::kPanelBytes, &vmap, bar,
-                    part * G::kPanelElems, 0, kvh, phys);
+        for (int part = 0; part < G::kParts; ++part)
+          tma_load_4d(st + G::kTileBytes + part * G::kPanelBytes, &vmap, bar,
+                      part * G::kPanelElems, 0, kvh, phys);
+      }
     }
   };
 

@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
                          blk_begin + warp;
   auto load_entries = [&](int chunk32) -> int {
     const int i = chunk32 * 32 + lane;
-    return i < n_my ? __ldg(table + static_cast<int64_t>(i) * W) : -1;
+    return i < n_my ? ld_keep(table + static_cast<int64_t>(i) * W) : -1;
   };
   int tab_cur = load_entries(0);
   int tab_next = load_entries(1);

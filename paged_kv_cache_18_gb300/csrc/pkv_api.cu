@@ -373,6 +373,38 @@ bool encode_cache_map(CUtensorMap *map, const void *base, pkv_dtype dt, int D, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same cache as a 5-D tensor (d within a panel, row, panel, KV head,
+// block): one box is a whole (block, KV head) tile, all its 128-byte column
+// panels, laid out in shared memory panel after panel exactly as the 4-D
+// map's boxes are (so one copy instruction replaces one per panel).  The
+// panel and row dimensions are listed out of address order (rows 128 * parts
+// bytes apart, panels 128), which the encoder may refuse: then the caller
+// keeps the 4-D map.
+bool encode_cache_tile_map(CUtensorMap *map, const void *base, pkv_dtype dt, int D, int Hkv,
+                           int64_t NB) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const int eb = elt_bytes(dt);
+  const int parts = D * eb / 128;
+  if (parts < 1 || parts * 128 != D * eb || parts > 256) return false;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(128 / eb),
+                              static_cast<cuuint64_t>(kBlockSize),
+                              static_cast<cuuint64_t>(parts), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(NB)};
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * eb;
+  const cuuint64_t strides[4] = {row, 128, row * kBlockSize, row * kBlockSize * Hkv};
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(128 / eb),
+                             static_cast<cuuint32_t>(kBlockSize),
+                             static_cast<cuuint32_t>(parts), 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUtensorMapDataType type = dt == PKV_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dt == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(map, type, 5, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 pkv_status run_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_table, int max_blocks_per_seq,
                          const int32_t *context_lens, const Shape &s, int64_t num_blocks,
@@ -465,8 +497,12 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   }
   if (pl.kernel == PKV_KERNEL_MMA) {
     CUtensorMap kmap, vmap;
-    if (!encode_cache_map(&kmap, k_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks) ||
-        !encode_cache_map(&vmap, v_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks))
+    p.tile_box =
+        encode_cache_tile_map(&kmap, k_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks) &&
+        encode_cache_tile_map(&vmap, v_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks);
+    if (!p.tile_box &&
+        (!encode_cache_map(&kmap, k_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks) ||
+         !encode_cache_map(&vmap, v_cache, s.dtype, s.head_dim, s.num_kv_heads, num_blocks)))
       return PKV_ERR_CUDA;
     const MmaShape m{ceil_div(pl.rows_per_cta, 8), pl.warp_tiles, pl.blocks_per_iter, pl.stages};
     e = mma_launch(s.dtype, s.qdtype, s.head_dim, m, kmap, vmap, p, grid, stream);
@@ -1071,10 +1107,13 @@ pkv_status pkv_mla_decode_attention(void *out, const void *q, const void *ckv_ca
       (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.workspace))
     return PKV_ERR_WORKSPACE;
   CUtensorMap cmap;
-  if (!encode_cache_map(&cmap, ckv_cache, dtype, latent_dim + rope_dim, 1, num_blocks))
+  const bool tile_box =
+      encode_cache_tile_map(&cmap, ckv_cache, dtype, latent_dim + rope_dim, 1, num_blocks);
+  if (!tile_box && !encode_cache_map(&cmap, ckv_cache, dtype, latent_dim + rope_dim, 1, num_blocks))
     return PKV_ERR_CUDA;
 
   AttnParams p{};
+  p.tile_box = tile_box ? 1 : 0;
   p.out = out;
   p.q = q;
   p.block_table = block_table;

@@ -46,6 +46,8 @@ struct AttnParams {
   int rows_per_cta, row_chunks;
   int max_blocks_per_seq, max_context_len;
   int split_blocks, num_splits;
+  int tile_box;                 // the cache maps copy a whole (block, KV head) tile per box
+                                //   (5-D maps); 0: one 128-byte column panel per box (4-D)
   float scale_log2;             // softmax scale * log2(e) (* key scale of an FP8 cache)
   float out_scale;              // multiplies every output (value scale of an FP8 cache; else 1)
 };
@@ -142,6 +144,17 @@ cudaError_t launch_kernel(bool dependent, void (*kernel)(Params...), dim3 grid, 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
+// A load of read-only data that stays in the register it is loaded into.
+// Block-table entries are loaded a chunk ahead of their use; written as a
+// plain __ldg the compiler may drop the register and load again at the use
+// (the load is invariant), which puts a global-memory round trip on every
+// block of the loop.  An asm statement is neither duplicated nor moved.
+__device__ __forceinline__ int ld_keep(const int32_t *ptr) {
+  int v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -214,6 +227,17 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+// Tiled 5-D tensor copy (coordinates innermost first).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(bar)
       : "memory");
 }
 
