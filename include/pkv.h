@@ -127,6 +127,11 @@ typedef struct pkv_options {
                           takes per loop iteration (1 or 2; 2 with one tile) */
   int persistent;   /* tcgen05 kernel: 0 planner, 1 one CTA per resident slot
                        walks the work items, 2 one CTA per item */
+  int split_waves;  /* split-K partition from the batch's real lengths, read
+                       on the device (batch <= 32, CUDA-core and mma.sync
+                       kernels, split_blocks 0): k > 0 cuts the batch into at
+                       most k waves of resident CTAs; 0 or -1: the host plan
+                       (split length from max_context_len) */
 } pkv_options;
 
 /* What one attention call launches (see pkv_attention_plan). */
@@ -146,6 +151,10 @@ typedef struct pkv_plan {
                              0: no split, or the last CTA of each sequence merges */
   int warp_tiles;         /* tensor-core kernel: 8-column query tiles per warp */
   int blocks_per_iter;    /* tensor-core kernel: KV blocks per loop iteration */
+  int split_target;       /* > 0: the partition is made on the device from the
+                             real context lengths, into at most this many CTAs
+                             (grid_x; split_blocks 0, num_splits an upper bound
+                             per sequence); 0: the host partition above */
 } pkv_plan;
 
 /* Human-readable name of a status code (static string). */

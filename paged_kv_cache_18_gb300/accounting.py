@@ -55,3 +55,30 @@ def append_bytes(num_tokens: int, num_kv_heads: int, head_dim: int,
     """kv_append: read k_new and v_new, write them into the cache, + slots."""
     rows = 2 * num_tokens * num_kv_heads * head_dim * elt_bytes
     return 2 * rows + 8 * num_tokens
+
+
+MIN_DEVICE_SPLIT = 16  # smallest split of the device partition, in blocks
+
+
+def device_split_counts(context_lens: Sequence[int], block_size: int, units: int,
+                        target: int, max_context_len: int, max_blocks_per_seq: int) -> list:
+    """Splits per sequence of the split-K partition the decode kernels make
+    on the device from the real lengths (pkv_plan.split_target = target > 0;
+    units = KV heads x row chunks per sequence): the smallest split length
+    S >= MIN_DEVICE_SPLIT blocks with units * sum_b ceil(n_b / S) <= target,
+    each sequence getting max(1, ceil(n_b / S)) splits.  For the byte
+    accounting of the partials; the kernels compute it themselves."""
+    nb = []
+    for L in context_lens:
+        L = min(max(0, int(L)), max_context_len)
+        nb.append(min(-(-L // block_size), max_blocks_per_seq))
+    cap = max(target // units, 1)
+    lo = max(MIN_DEVICE_SPLIT, -(-sum(nb) // cap))
+    hi = max(lo, max(nb) if nb else lo)
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if sum(max(1, -(-n // mid)) for n in nb) <= cap:
+            hi = mid
+        else:
+            lo = mid + 1
+    return [max(1, -(-n // lo)) for n in nb]

@@ -52,12 +52,13 @@ class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("split_blocks", ctypes.c_int),
                 ("stages", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
                 ("merge", ctypes.c_int), ("warp_tiles", ctypes.c_int),
-                ("blocks_per_iter", ctypes.c_int), ("persistent", ctypes.c_int)]
+                ("blocks_per_iter", ctypes.c_int), ("persistent", ctypes.c_int),
+                ("split_waves", ctypes.c_int)]
 
 
 # Extra launch controls for tuning runs (pkv_options.rows_per_cta / .merge /
-# .warp_tiles / .blocks_per_iter); module-wide so that every binding call
-# passes them.  Empty = planner.
+# .warp_tiles / .blocks_per_iter / .persistent / .split_waves); module-wide so
+# that every binding call passes them.  Empty = planner.
 TUNING = {}
 
 
@@ -70,7 +71,7 @@ class Plan(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int),
                 ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
                 ("merge_kernel", ctypes.c_int), ("warp_tiles", ctypes.c_int),
-                ("blocks_per_iter", ctypes.c_int)]
+                ("blocks_per_iter", ctypes.c_int), ("split_target", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -179,9 +180,11 @@ def _opts(kernel: int, split_blocks: int, stages: int = 0, warp_tiles: int = 0):
     rows, merge = TUNING.get("rows_per_cta", 0), TUNING.get("merge", 0)
     warp_tiles = warp_tiles or TUNING.get("warp_tiles", 0)
     kb, pers = TUNING.get("blocks_per_iter", 0), TUNING.get("persistent", 0)
-    if not any((kernel, split_blocks, stages, rows, merge, warp_tiles, kb, pers)):
+    waves = TUNING.get("split_waves", 0)
+    if not any((kernel, split_blocks, stages, rows, merge, warp_tiles, kb, pers, waves)):
         return None
-    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge, warp_tiles, kb, pers))
+    return ctypes.byref(Options(kernel, split_blocks, stages, rows, merge, warp_tiles, kb, pers,
+                                waves))
 
 
 def _need(cond: bool, msg: str) -> None:

@@ -21,8 +21,8 @@
 // The warps then meet in shared memory: with M = max_w M_w,
 //   out = sum_w 2^(M_w - M) acc_w / sum_w 2^(M_w - M) l_w.
 // The kernel is a programmatic dependent of the attention kernel: it may be
-// scheduled while that kernel still runs (which hides its launch), reads
-// only the call's inputs before pdl_wait, and the partials after it.
+// scheduled while that kernel still runs (which hides its launch) and reads
+// nothing from global memory before pdl_wait.
 #include <algorithm>
 
 #include "pkv_device.cuh"
@@ -37,24 +37,51 @@ constexpr int kMergeWarps = 4;
 // two for the 512-wide latent rows of MLA (register budget).
 template <int D> __host__ __device__ constexpr int merge_unroll() { return D <= 256 ? 8 : 2; }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const AttnParams p) {
+// DEV: the partials of the device partition ([item][CTA column]); else the
+// host partition's [row][split].
+template <typename T, int D, bool DEV>
+__global__ void __launch_bounds__(kMergeWarps * 32, (D <= 128 ? (DEV ? 6 : 8) : 4))
+    attn_merge_kernel(const AttnParams p) {
   constexpr int PER = D / 32;  // elements per lane: 2, 4, 8 or 16
   constexpr int kMergeUnroll = merge_unroll<D>();
   const int64_t row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = static_cast<int>(row / (static_cast<int64_t>(p.num_queries) * p.num_heads));
-  const SeqExtent ext = seq_extent(p, b, false);
-  int ns = (ext.nblk + p.split_blocks - 1) / p.split_blocks;
-  ns = ns < 1 ? 1 : (ns > p.num_splits ? p.num_splits : ns);
+  // The attention kernel's partials are complete and visible after this wait,
+  // and so is everything enqueued before the attention kernel (which may
+  // itself have started early, as a programmatic dependent): the context
+  // lengths are read only after it.
+  pdl_wait();
+  // The partials of this row: split s at part_lse[first + s * stride] and
+  // part_o[(first + s * stride) * D ..].
+  int ns, stride;
+  int64_t first;
+  if constexpr (!DEV) {  // host partition: [row][split]
+    const SeqExtent ext = seq_extent(p, b, false);
+    ns = (ext.nblk + p.split_blocks - 1) / p.split_blocks;
+    ns = ns < 1 ? 1 : (ns > p.num_splits ? p.num_splits : ns);
+    first = row * p.num_splits;
+    stride = 1;
+  } else {  // device partition: [item][CTA column], the items of (b, unit) consecutive
+    ns = p.split_info[2 * b];
+    const int item0 = p.split_info[2 * b + 1];
+    const int h = static_cast<int>(row % p.num_heads);
+    const int j = static_cast<int>((row / p.num_heads) % p.num_queries);
+    const int kvh = h / p.group;
+    const int r = j * p.group + (h - kvh * p.group);  // row within its KV head's rows
+    const int chunk = r / p.rows_per_cta;
+    const int unit = kvh * p.row_chunks + chunk;
+    first = (static_cast<int64_t>(item0) + static_cast<int64_t>(unit) * ns) * p.rows_per_cta +
+            (r - chunk * p.rows_per_cta);
+    stride = p.rows_per_cta;
+  }
 
   __shared__ float red_max[kMergeWarps];
   __shared__ float red_sum[kMergeWarps];
   __shared__ float red_acc[kMergeWarps][D];
 
-  pdl_wait();  // the attention kernel's partials are complete and visible
-  const float *lse = p.part_lse + row * p.num_splits;
-  const float *po = p.part_o + row * p.num_splits * D + lane * PER;
+  const float *lse = p.part_lse + first;
+  const float *po = p.part_o + first * D + lane * PER;
   float Mw = -INFINITY, wsum = 0.f;
   float acc[PER];
 #pragma unroll
@@ -66,10 +93,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
     for (int u = 0; u < kMergeUnroll; ++u) {
       const int s = s0 + u * kMergeWarps;
       const bool ok = s < ns;
-      ls[u] = ok ? lse[s] : -INFINITY;
+      const int off = DEV ? s * stride : s;  // < splits x rows per CTA: fits an int
+      ls[u] = ok ? lse[off] : -INFINITY;
 #pragma unroll
       for (int e = 0; e < PER; e += 2) {
-        const float2 x = ok ? *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(s) * D + e)
+        const float2 x = ok ? *reinterpret_cast<const float2 *>(po + off * D + e)
                             : make_float2(0.f, 0.f);
         v[u][e] = x.x;
         v[u][e + 1] = x.y;
@@ -125,11 +153,16 @@ cudaError_t merge_t(int D, const AttnParams &p, cudaStream_t stream) {
   if (nrows == 0) return cudaSuccess;
   if (nrows > 0x7fffffffLL) return cudaErrorInvalidValue;
   void (*kernel)(const AttnParams);
+  const bool dev = p.split_target > 0;
   switch (D) {
-    case 64: kernel = attn_merge_kernel<T, 64>; break;
-    case 128: kernel = attn_merge_kernel<T, 128>; break;
-    case 256: kernel = attn_merge_kernel<T, 256>; break;
-    case 512: kernel = attn_merge_kernel<T, 512>; break;
+    case 64: kernel = dev ? attn_merge_kernel<T, 64, true> : attn_merge_kernel<T, 64, false>; break;
+    case 128:
+      kernel = dev ? attn_merge_kernel<T, 128, true> : attn_merge_kernel<T, 128, false>;
+      break;
+    case 256:
+      kernel = dev ? attn_merge_kernel<T, 256, true> : attn_merge_kernel<T, 256, false>;
+      break;
+    case 512: kernel = attn_merge_kernel<T, 512, false>; break;  // MLA: host partition
     default: return cudaErrorInvalidValue;
   }
   // launched as a programmatic dependent of the attention kernel before it

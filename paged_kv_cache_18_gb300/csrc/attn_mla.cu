@@ -87,7 +87,12 @@ template <typename T, int DR, int NS>
 __global__ void __launch_bounds__(kThreads, 2)
     attn_mla_kernel(const __grid_constant__ CUtensorMap cmap, const AttnParams p) {
   using G = Geom<DR, NS>;
-  pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for this grid
+  // The next kernel of the stream (the merge kernel, or the next call's
+  // attention) may be scheduled now; it waits for this grid.  This kernel is
+  // itself launched as a programmatic dependent of the one before it, so
+  // before touching global memory it waits for that one to complete.
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -368,8 +373,9 @@ using MlaLaunch = cudaError_t (*)(const CUtensorMap &, const AttnParams &, dim3,
 template <typename T, int DR, int NS>
 cudaError_t launch_t(const CUtensorMap &cmap, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
-  attn_mla_kernel<T, DR, NS><<<grid, kThreads, Geom<DR, NS>::kBytes + 1024, stream>>>(cmap, p);
-  return cudaGetLastError();
+  // a programmatic dependent of the kernel before it (see the kernel's entry)
+  return launch_kernel(true, attn_mla_kernel<T, DR, NS>, grid, kThreads,
+                       Geom<DR, NS>::kBytes + 1024, stream, cmap, p);
 }
 
 template <typename T, int DR, int NS> bool info_t(KernelInfo *info, MlaLaunch *launch) {

@@ -137,7 +137,12 @@ __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   static_assert(NS >= KB, "an iteration's blocks must all be in flight at once");
-  pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for this grid
+  // The next kernel of the stream (the merge kernel, or the next call's
+  // attention) may be scheduled now; it waits for this grid.  This kernel is
+  // itself launched as a programmatic dependent of the one before it, so
+  // before touching global memory it waits for that one to complete.
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr bool FP8 = std::is_same<TC, E4M3>::value;
   using TM = typename MmaType<T, TC>::type;
   using G = MmaGeom<D, Elt<TC>::bytes>;
@@ -158,19 +163,13 @@ __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
   const int bl = warp / CG, cg = warp - (warp / CG) * CG;
   const bool leader = cg == 0;
   const int g = lane >> 2, c = lane & 3;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / p.row_chunks;
-  const int chunk = blockIdx.y - kvh * p.row_chunks;
-  const int b = blockIdx.z;
-
-  const SeqExtent ext = seq_extent(p, b, split == 0 && chunk == 0 && kvh == 0 &&
-                                             threadIdx.x == 0);
+  const CtaWork wk = cta_work(p);
+  if (!wk.active) return;  // a split past its sequence's end (the whole CTA agrees)
+  const int kvh = wk.kvh, chunk = wk.chunk, b = wk.b;
+  const SeqExtent ext = wk.ext;
   const int L = ext.L;
-  const int blk_begin = split * p.split_blocks;
-  if (split > 0 && blk_begin >= ext.nblk) return;  // this sequence has fewer splits
-  const int blk_end = min(blk_begin + p.split_blocks, ext.nblk);
-  const int ns_b = max(1, min(p.num_splits, (ext.nblk + p.split_blocks - 1) / p.split_blocks));
-  const int nspan = max(blk_end - blk_begin, 0);
+  const int blk_begin = wk.blk_begin;
+  const int nspan = max(wk.blk_end - blk_begin, 0);
   const int n_my = nspan > bl ? (nspan - bl + BL - 1) / BL : 0;
   const int col0 = cg * NT * 8;
 
@@ -637,8 +636,7 @@ __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
       }
   }
   __syncthreads();
-  cta_epilogue<T, D, NC, BL, NW * 32>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split,
-                                      ns_b);
+  cta_epilogue<T, D, NC, BL, NW * 32>(p, red_m, red_l, red_o, wscale, wk);
 }
 
 // Block lanes for CG column groups: about four warps per CTA.
@@ -693,8 +691,9 @@ template <typename T, typename TC, int D, int CG, int NT, int KB, bool DEEP>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
   const KernelInfo k = mma_info_t<T, TC, D, CG, NT, KB, DEEP>();
-  // with split-K counters: a dependent of the kernel that zeroes them
-  return launch_kernel(p.counters != nullptr,
+  // a programmatic dependent of the kernel before it (with split-K counters,
+  // the kernel that zeroes them)
+  return launch_kernel(true,
                        attn_mma_kernel<T, TC, D, CG, NT, KB, mma_lanes<CG>(),
                                        mma_stages_t<TC, D, CG, DEEP>()>,
                        grid, k.threads, k.smem, stream, km, vm, p);

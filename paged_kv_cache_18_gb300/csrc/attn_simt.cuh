@@ -89,7 +89,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // TQ: element type of q and out; TC: element type of the caches.
 template <typename TQ, typename TC, int D, int R, int W, int NS>
 __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
-  pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for this grid
+  // The next kernel of the stream (the merge kernel, or the next call's
+  // attention) may be scheduled now; it waits for this grid.  This kernel is
+  // itself launched as a programmatic dependent of the one before it, so
+  // before touching global memory it waits for that one to complete.
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int ELT = Elt<TC>::bytes;
   constexpr int RB = D * ELT;             // bytes of one row
   constexpr int TILE = kBlockSize * RB;   // bytes of one (block, kv head) tile
@@ -107,19 +112,13 @@ __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rg = lane >> 3, t = lane & 7;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / p.row_chunks;
-  const int chunk = blockIdx.y - kvh * p.row_chunks;
-  const int b = blockIdx.z;
-
-  const SeqExtent ext = seq_extent(p, b, split == 0 && chunk == 0 && kvh == 0 &&
-                                             threadIdx.x == 0);
+  const CtaWork wk = cta_work(p);
+  if (!wk.active) return;  // a split past its sequence's end (the whole CTA agrees)
+  const int kvh = wk.kvh, chunk = wk.chunk, b = wk.b;
+  const SeqExtent ext = wk.ext;
   const int L = ext.L;
-  const int blk_begin = split * p.split_blocks;
-  if (split > 0 && blk_begin >= ext.nblk) return;
-  const int blk_end = min(blk_begin + p.split_blocks, ext.nblk);
-  const int ns_b = max(1, min(p.num_splits, (ext.nblk + p.split_blocks - 1) / p.split_blocks));
-  const int nspan = max(blk_end - blk_begin, 0);
+  const int blk_begin = wk.blk_begin;
+  const int nspan = max(wk.blk_end - blk_begin, 0);
   const int n_my = nspan > warp ? (nspan - warp + W - 1) / W : 0;
 
   // Query rows in registers (this lane's slice of the head dim).
@@ -322,7 +321,7 @@ __global__ void __launch_bounds__(W * 32) attn_simt_kernel(const AttnParams p) {
     }
   }
   __syncthreads();
-  cta_epilogue<TQ, D, NC, W, W * 32>(p, red_m, red_l, red_o, wscale, b, kvh, chunk, split, ns_b);
+  cta_epilogue<TQ, D, NC, W, W * 32>(p, red_m, red_l, red_o, wscale, wk);
 }
 
 constexpr int kSimtWarps = 4;
@@ -360,8 +359,9 @@ KernelInfo simt_info_t() {
 template <typename TQ, typename TC, int D, int R>
 cudaError_t simt_launch_t(const AttnParams &p, dim3 grid, cudaStream_t stream) {
   const KernelInfo k = simt_info_t<TQ, TC, D, R>();
-  // with split-K counters: a dependent of the kernel that zeroes them
-  return launch_kernel(p.counters != nullptr,
+  // a programmatic dependent of the kernel before it (with split-K counters,
+  // the kernel that zeroes them)
+  return launch_kernel(true,
                        attn_simt_kernel<TQ, TC, D, R, kSimtWarps, simt_stages<TC, D>()>, grid,
                        k.threads, k.smem, stream, p);
 }

@@ -19,6 +19,9 @@ __global__ void __launch_bounds__(256)
                      uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                      const int64_t *__restrict__ slots, int64_t num_tokens, int num_kv_heads,
                      int vec_per_row, int block_size, int64_t num_blocks, int32_t *err) {
+  // An attention kernel launched next (a programmatic dependent) may be
+  // scheduled now; it waits for this grid before it reads the cache.
+  pdl_launch_dependents();
   const int64_t per_token = static_cast<int64_t>(num_kv_heads) * vec_per_row;
   const int64_t total = num_tokens * per_token;
   const int64_t capacity = num_blocks * block_size;
@@ -111,6 +114,7 @@ __global__ void __launch_bounds__(256)
                          const int64_t *__restrict__ slots, int64_t num_tokens, int num_kv_heads,
                          int head_dim, int block_size, int64_t num_blocks, float k_scale,
                          float v_scale, int32_t *err) {
+  pdl_launch_dependents();  // as in kv_append_kernel
   const int vpr = head_dim / 16;  // 16-byte code vectors per row
   const int64_t per_token = static_cast<int64_t>(num_kv_heads) * vpr;
   const int64_t total = num_tokens * per_token;

@@ -200,10 +200,20 @@ struct WorkspaceLayout {
   bool fused_merge;
 };
 WorkspaceLayout workspace_layout(const Shape &s, int num_splits, int row_chunks, int rows_per_cta,
-                                 int merge) {
+                                 int merge, int split_target = 0) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rows = static_cast<size_t>(s.batch) * s.num_queries * s.num_heads;
   WorkspaceLayout w{};
+  if (split_target > 0) {
+    // device partition: one partial per (work item, CTA column), merged by
+    // the merge kernel
+    const size_t parts = static_cast<size_t>(split_target) * rows_per_cta;
+    w.lse_off = up(parts * s.head_dim * sizeof(float));
+    w.ctr_off = w.lse_off + up(parts * sizeof(float));  // here: (ns_b, first item) per sequence
+    w.total = w.ctr_off + up(static_cast<size_t>(s.batch) * 2 * sizeof(int));
+    w.fused_merge = false;
+    return w;
+  }
   w.lse_off = up(rows * num_splits * s.head_dim * sizeof(float));
   w.ctr_off = w.lse_off + up(rows * num_splits * sizeof(float));
   // The completing CTA reads back rows x splits partial vectors in its tail:
@@ -265,6 +275,37 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
     }
   }
   if (split_blocks < 1) split_blocks = 1;
+  // Partition from the real lengths (read on the device, cta_work), on
+  // request (split_waves = k > 0) for a batch of at most 32 sequences: k
+  // waves of resident CTAs with splits of nearly equal length, whatever
+  // max_context_len says.  It is not the default: measured on the long-context
+  // and verify workloads it lost to the host plan (two sequences of 32768 and
+  // 65536 rows: one exact wave of 456 CTAs, 0.806 of the HBM peak, against
+  // 0.842 for the host's 384; speculative verify 0.588 against 0.639), the
+  // kernels being bound by the bytes in flight rather than by idle slots.
+  const int waves = opt ? opt->split_waves : 0;
+  const int64_t unit_rows = static_cast<int64_t>(s.num_kv_heads) * pl->row_chunks;
+  if (!persistent && waves > 0 && !(opt && opt->split_blocks > 0) && s.batch <= 32 &&
+      max_blocks > 0 &&
+      static_cast<int64_t>(max_blocks) * s.batch < (int64_t(1) << 30)) {  // int sums on device
+    const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
+    int64_t target = (waves > 0 ? waves : 1) * slots;
+    if (target < units) target = (units + slots - 1) / slots * slots;  // one split each fits
+    if (target <= 0x7fffffffLL) {
+      pl->split_target = static_cast<int>(target);
+      pl->split_blocks = 0;
+      pl->num_splits = static_cast<int>(std::max<int64_t>(1, target / unit_rows));
+      pl->grid_x = pl->split_target;
+      pl->grid_y = pl->grid_z = 1;
+      pl->ctas_per_sm = ctas_per_sm;
+      const WorkspaceLayout w =
+          workspace_layout(s, pl->num_splits, pl->row_chunks, pl->rows_per_cta, 2, pl->split_target);
+      pl->workspace_bytes = w.total;
+      pl->merge_kernel = 1;
+      return;
+    }
+  }
+  pl->split_target = 0;
   int num_splits = max_blocks > 0 ? ceil_div(max_blocks, split_blocks) : 1;
   if (num_splits <= 1) {
     num_splits = 1;
@@ -302,7 +343,8 @@ pkv_status make_plan(const Shape &s, const pkv_options *opt, int num_sms, int ct
   pkv_status st = check_shape(s);
   if (st != PKV_OK) return st;
   if (opt && (opt->split_blocks < 0 || opt->stages < 0 || opt->rows_per_cta < 0 ||
-              opt->merge < 0 || opt->merge > 2))
+              opt->merge < 0 || opt->merge > 2 || opt->split_waves < -1 ||
+              opt->split_waves > 64))
     return PKV_ERR_INVALID_ARG;
   if (!choose_kernel(s, opt, pl, info)) return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(s.num_kv_heads) * pl->row_chunks > 65535) return PKV_ERR_UNSUPPORTED;
@@ -468,17 +510,20 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   p.max_context_len = s.max_context_len;
   p.split_blocks = pl.split_blocks;
   p.num_splits = pl.num_splits;
+  p.split_target = pl.split_target;
   p.scale_log2 =
       static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * k_scale);
   p.out_scale = v_scale;
   bool merge_kernel = false;
-  if (pl.num_splits > 1) {
+  if (pl.num_splits > 1 || pl.split_target > 0) {
     const WorkspaceLayout w =
         workspace_layout(s, pl.num_splits, pl.row_chunks, pl.rows_per_cta,
-                         pl.kernel == PKV_KERNEL_TC ? 2 : (opt ? opt->merge : 0));
+                         pl.kernel == PKV_KERNEL_TC ? 2 : (opt ? opt->merge : 0),
+                         pl.split_target);
     char *base = static_cast<char *>(workspace);
     p.part_o = reinterpret_cast<float *>(base);
     p.part_lse = reinterpret_cast<float *>(base + w.lse_off);
+    if (pl.split_target > 0) p.split_info = reinterpret_cast<int *>(base + w.ctr_off);
     if (w.fused_merge) {
       p.counters = reinterpret_cast<unsigned int *>(base + w.ctr_off);
     } else {
@@ -991,7 +1036,8 @@ pkv_status mla_plan(int batch, int num_heads, int latent_dim, int rope_dim, int 
       num_heads / kMlaHeadsPerCta > 65535)
     return PKV_ERR_UNSUPPORTED;
   if (opt && (opt->kernel != PKV_KERNEL_AUTO || opt->rows_per_cta != 0 || opt->merge != 0 ||
-              opt->warp_tiles != 0 || opt->blocks_per_iter != 0 || opt->persistent != 0))
+              opt->warp_tiles != 0 || opt->blocks_per_iter != 0 || opt->persistent != 0 ||
+              opt->split_waves != 0))
     return PKV_ERR_UNSUPPORTED;  // only stages and split_blocks apply here
   if (!mla_kernel_info(dtype, rope_dim, opt ? opt->stages : 0, &pl->info))
     return PKV_ERR_UNSUPPORTED;

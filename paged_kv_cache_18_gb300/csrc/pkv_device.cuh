@@ -46,6 +46,10 @@ struct AttnParams {
   int rows_per_cta, row_chunks;
   int max_blocks_per_seq, max_context_len;
   int split_blocks, num_splits;
+  int split_target;             // > 0: split-K partition made on the device into at most
+                                //   this many work items (see cta_work); 0: host partition
+  int *split_info;              // device partition: [batch][2] = (ns_b, first item of b),
+                                //   written by the attention kernel for the merge kernel
   int tile_box;                 // the cache maps copy a whole (block, KV head) tile per box
                                 //   (5-D maps); 0: one 128-byte column panel per box (4-D)
   float scale_log2;             // softmax scale * log2(e) (* key scale of an FP8 cache)
@@ -356,6 +360,131 @@ __device__ __forceinline__ SeqExtent seq_extent(const AttnParams &p, int b, bool
   return {L, nblk};
 }
 
+// ---- split-K partition ------------------------------------------------------
+// Host partition (split_target == 0): the grid is (splits, KV heads x row
+// chunks, batch) and split s of a sequence covers blocks s * split_blocks ..
+// s * split_blocks + split_blocks - 1 (planned from max_context_len).
+//
+// Device partition (split_target = T > 0, batch <= 32): the split length is
+// chosen here from the batch's real block counts n_b, so that the work items
+// -- (sequence, unit, split), a unit being one KV head x row chunk -- number
+// at most T (the host makes T whole waves of resident CTAs):  S is the
+// smallest length >= kMinDeviceSplit with  units * sum_b ns_b <= T,  where
+// ns_b = max(1, ceil(n_b / S)).  Sequence b's blocks are cut into ns_b
+// nearly equal runs, and the grid is flat: CTA t takes item t, items being
+// numbered sequence by sequence, unit by unit, split by split.  Partials are
+// stored per item: [item][rows_per_cta] vectors of head_dim floats and one
+// log-sum-exp each.  Every warp that needs the partition computes it alike.
+constexpr int kMinDeviceSplit = 16;
+
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_max_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// Warp-collective: lane b < batch holds n_b (others 0); returns S.
+__device__ __forceinline__ int device_split_len(const AttnParams &p, int nb, int units) {
+  const int lane = threadIdx.x & 31;
+  const int cap = max(p.split_target / units, 1);  // sum over sequences of ns_b
+  const int total = warp_sum_i(nb);
+  int lo = max(kMinDeviceSplit, (total + cap - 1) / cap);
+  int hi = max(lo, warp_max_i(nb));  // one split per sequence: batch <= cap (host)
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const int cnt = warp_sum_i(lane < p.batch ? max(1, (nb + mid - 1) / mid) : 0);
+    if (cnt <= cap) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+// Per-sequence split layout of the device partition (warp-collective):
+// lane b < batch gets ns_b and the index of its first item.
+struct SeqSplits {
+  int nb, ns, first_item;
+};
+__device__ __forceinline__ SeqSplits device_splits(const AttnParams &p) {
+  const int lane = threadIdx.x & 31;
+  const int units = p.num_kv_heads * p.row_chunks;
+  SeqSplits r;
+  r.nb = lane < p.batch ? seq_extent(p, lane, false).nblk : 0;
+  const int S = device_split_len(p, r.nb, units);
+  r.ns = lane < p.batch ? max(1, (r.nb + S - 1) / S) : 0;
+  int incl = r.ns * units;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  r.first_item = incl - r.ns * units;
+  return r;
+}
+
+// The work of this CTA.
+struct CtaWork {
+  int b, kvh, chunk, split, ns_b, blk_begin, blk_end;
+  int64_t item;  // device partition: the item index (blockIdx.x); else -1
+  SeqExtent ext;
+  bool active;   // false: nothing to do (a split past its sequence's end)
+};
+__device__ __forceinline__ CtaWork cta_work(const AttnParams &p) {
+  CtaWork w;
+  if (p.split_target == 0) {
+    w.split = blockIdx.x;
+    w.kvh = blockIdx.y / p.row_chunks;
+    w.chunk = blockIdx.y - w.kvh * p.row_chunks;
+    w.b = blockIdx.z;
+    w.ext = seq_extent(p, w.b, w.split == 0 && w.chunk == 0 && w.kvh == 0 && threadIdx.x == 0);
+    w.blk_begin = w.split * p.split_blocks;
+    w.active = !(w.split > 0 && w.blk_begin >= w.ext.nblk);
+    w.blk_end = min(w.blk_begin + p.split_blocks, w.ext.nblk);
+    w.ns_b = max(1, min(p.num_splits, (w.ext.nblk + p.split_blocks - 1) / p.split_blocks));
+    w.item = -1;
+    return w;
+  }
+  const SeqSplits sp = device_splits(p);
+  const int t = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const unsigned hit =
+      __ballot_sync(kFull, lane < p.batch && sp.first_item + sp.ns * p.num_kv_heads *
+                                                                  p.row_chunks > t);
+  w.active = hit != 0u;
+  const int b = w.active ? __ffs(hit) - 1 : 0;
+  const int ns = __shfl_sync(kFull, sp.ns, b);
+  const int first = __shfl_sync(kFull, sp.first_item, b);
+  const int nb = __shfl_sync(kFull, sp.nb, b);
+  w.b = b;
+  w.item = t;
+  if (!w.active) return w;
+  const int r = t - first;
+  const int u = r / ns;
+  w.split = r - u * ns;
+  w.kvh = u / p.row_chunks;
+  w.chunk = u - w.kvh * p.row_chunks;
+  w.ns_b = ns;
+  w.ext = seq_extent(p, b, w.split == 0 && u == 0 && threadIdx.x == 0);
+  if (r == 0 && threadIdx.x == 0) {  // the sequence's first item publishes its layout
+    p.split_info[2 * b] = ns;
+    p.split_info[2 * b + 1] = first;
+  }
+  w.blk_begin = static_cast<int>(static_cast<int64_t>(w.split) * nb / ns);
+  w.blk_end = static_cast<int>(static_cast<int64_t>(w.split + 1) * nb / ns);
+  return w;
+}
+
+// Index of the partial (output vector and log-sum-exp) of CTA column `col`
+// of work item w, for flat output row `row`.
+__device__ __forceinline__ int64_t partial_index(const AttnParams &p, const CtaWork &w,
+                                                 int64_t row, int col) {
+  return p.split_target == 0 ? row * p.num_splits + w.split
+                             : w.item * p.rows_per_cta + col;
+}
+
 // Fused append.  The Q new rows of sequence b sit at logical positions
 // L - Q .. L - 1.  A warp that has just received the tile of block `blk`
 // (first row key0) overwrites the tile rows of any new position in it with
@@ -429,8 +558,8 @@ __device__ __forceinline__ bool split_arrive(const AttnParams &p, int b, int kvh
 //     (the Flash-Decoding reduction: weights 2^(lse_s - max lse)).
 template <typename T, int D, int NC, int W, int NTHR>
 __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, float *red_l,
-                                             float *red_o, float *wscale, int b, int kvh,
-                                             int chunk, int split, int ns_b) {
+                                             float *red_o, float *wscale, const CtaWork &wk) {
+  const int b = wk.b, kvh = wk.kvh, chunk = wk.chunk, ns_b = wk.ns_b;
   constexpr int DP = D + 4;
   constexpr int QV = D / 4;
   const int tid = threadIdx.x;
@@ -451,7 +580,9 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
     wscale[(W + 1) * NC + tid] = lsum > 0.f ? M + __log2f(lsum) : -INFINITY;
   }
   __syncthreads();
-  const bool direct = p.num_splits == 1 || (ns_b == 1 && p.counters != nullptr);
+  // (the device partition always leaves partials for the merge kernel)
+  const bool direct =
+      p.split_target == 0 && (p.num_splits == 1 || (ns_b == 1 && p.counters != nullptr));
   // 2) 4 consecutive d per thread-step.
   for (int idx = tid; idx < NC * QV; idx += NTHR) {
     const int col = idx / QV;
@@ -476,8 +607,9 @@ __device__ __forceinline__ void cta_epilogue(const AttnParams &p, float *red_m, 
       for (int e = 0; e < 4; ++e) dst[e] = from_float<T>(acc[e] * os);
     } else {
       float4 v = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<float4 *>(&p.part_o[(row * p.num_splits + split) * D + d0]) = v;
-      if (d0 == 0) p.part_lse[row * p.num_splits + split] = wscale[(W + 1) * NC + col];
+      const int64_t pi = partial_index(p, wk, row, col);
+      *reinterpret_cast<float4 *>(&p.part_o[pi * D + d0]) = v;
+      if (d0 == 0) p.part_lse[pi] = wscale[(W + 1) * NC + col];
     }
   }
   if (direct || p.counters == nullptr) return;

@@ -1,6 +1,7 @@
 """The C-ABI library without a GPU: it loads, exports every symbol the header
 declares, validates arguments synchronously (nothing reaches CUDA on bad
 input), and its launch planner is self-consistent."""
+import contextlib
 import ctypes
 import os
 import re
@@ -9,6 +10,18 @@ import pytest
 import torch
 
 from paged_kv_cache_18_gb300 import binding, build
+
+
+@contextlib.contextmanager
+def tuning(**kw):
+    """Extra pkv_options fields for every binding call inside the block."""
+    saved = dict(binding.TUNING)
+    binding.TUNING.update(kw)
+    try:
+        yield
+    finally:
+        binding.TUNING.clear()
+        binding.TUNING.update(saved)
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                       "include", "pkv.h")
@@ -127,6 +140,20 @@ def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
     assert p["rows_per_cta"] * p["row_chunks"] >= rows
     assert (p["rows_per_cta"] - 1) * p["row_chunks"] < rows
     max_blocks = -(-ctx // 16)
+    if p["split_target"] > 0:
+        # partition from the real lengths, on the device: a flat grid of at
+        # most split_target work items, whole waves of resident CTAs, one
+        # partial per (item, CTA column), merged by the merge kernel
+        T, U = p["split_target"], Hkv * p["row_chunks"]
+        assert B <= 32 and p["split_blocks"] == 0 and p["merge_kernel"] == 1
+        assert T % (152 * p["ctas_per_sm"]) == 0 and T >= B * U
+        assert (p["grid_x"], p["grid_y"], p["grid_z"]) == (T, 1, 1)
+        assert p["num_splits"] == max(1, T // U)
+        parts = T * p["rows_per_cta"]
+        assert p["workspace_bytes"] == (-(-parts * D * 4 // 256) * 256 + -(-parts * 4 // 256) * 256
+                                        + -(-B * 8 // 256) * 256)
+        assert p["smem_bytes"] <= 227 * 1024
+        return
     assert p["num_splits"] * p["split_blocks"] >= max_blocks
     assert (p["num_splits"] - 1) * p["split_blocks"] < max(max_blocks, 1)
     assert (p["grid_x"], p["grid_y"], p["grid_z"]) == (p["num_splits"], Hkv * p["row_chunks"], B)
@@ -144,9 +171,19 @@ def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
 
 
 def test_plan_splits_long_contexts_and_honours_override():
+    # 16 (sequence, KV head) pairs cannot fill 152 SMs: split, at most 32
+    # ways, the split length from max_context_len
     p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152)
-    # 16 (sequence, KV head) pairs cannot fill 152 SMs: split, at most 32 ways
-    assert 16 <= p["num_splits"] <= 32
+    assert p["split_target"] == 0 and 16 <= p["num_splits"] <= 32
+    # on request, the partition from the real lengths, made on the device
+    for waves in (1, 2):
+        with tuning(split_waves=waves):
+            p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152)
+        assert p["split_target"] == waves * 152 * p["ctas_per_sm"]
+        assert p["grid_x"] == p["split_target"]
+    with tuning(split_waves=1):   # not for more than 32 sequences
+        p = binding.plan_for(33, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152)
+    assert p["split_target"] == 0 and p["num_splits"] > 1
     p = binding.plan_for(2, 1, 32, 8, 128, 65536, torch.bfloat16, num_sms=152, split_blocks=7)
     assert p["split_blocks"] == 7 and p["num_splits"] == -(-4096 // 7)
     p = binding.plan_for(2, 1, 32, 8, 128, 100, torch.bfloat16, num_sms=152, split_blocks=1000)
@@ -157,7 +194,7 @@ def test_plan_does_not_split_when_waves_gain_nothing():
     # 1280 equal units of 128 blocks on 152 SMs x 3 CTAs: 3 waves whole, and
     # 6 waves of 64-block halves: no split
     p = binding.plan_for(32, 1, 40, 40, 128, 2048, torch.bfloat16, num_sms=152, ctas_per_sm=3)
-    assert p["num_splits"] == 1
+    assert p["num_splits"] == 1 and p["split_target"] == 0
     # 1024 units of up to 256 blocks: 3 waves of 256 against 9 of 64: split
     p = binding.plan_for(128, 1, 32, 8, 128, 4096, torch.bfloat16, num_sms=152, ctas_per_sm=3)
     assert p["num_splits"] == 4 and p["split_blocks"] == 64

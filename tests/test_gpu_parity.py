@@ -707,3 +707,146 @@ def test_tc_many_items_per_cta(persistent, stages, split_blocks):
                         128, "bf16", len_range=(1, 3000), num_queries=3,
                         seed=1850 + stages + split_blocks)
         run_case(wl, kernel=3, stages=stages, split_blocks=split_blocks)
+
+
+# ---- split-K partition made on the device from the real lengths -----------
+DEVICE_LENS = [
+    [32768, 65536],                                  # long contexts, unequal
+    [1, 15, 16, 17, 300, 2000, 0, 5000],             # ragged, with an empty sequence
+    [700] * 32,                                      # the most sequences it takes
+    [40, 40],                                        # fewer items than CTAs
+]
+
+
+@pytest.mark.parametrize("lens_i", range(len(DEVICE_LENS)))
+@pytest.mark.parametrize("Q,Hq,Hkv", [(1, 32, 8), (5, 32, 8), (1, 8, 8), (3, 16, 2)])
+@pytest.mark.parametrize("kernel,waves", [(2, 1), (2, 3), (1, 1)])
+def test_device_split_partition(lens_i, Q, Hq, Hkv, kernel, waves):
+    """The partition the kernels derive on the device (split length from the
+    batch's block counts, flat grid of work items, one partial per item and
+    CTA column) gives the oracle's result; the merge kernel finds every
+    item of every row."""
+    import paged_kv_cache_18_gb300 as pkv
+    lens = DEVICE_LENS[lens_i]
+    if Q > 1:
+        lens = [max(L, Q) for L in lens]
+    D = 128
+    dtype = "bf16"
+    wl = W.Workload(f"device split {lens_i} Q{Q} {Hq}/{Hkv} k{kernel} w{waves}", len(lens), Hq,
+                    Hkv, D, dtype, context_lens=lens, num_queries=Q,
+                    seed=800 + lens_i * 7 + Q + Hq + kernel + waves)
+    b = W.make_batch(wl)
+    with tuning(split_waves=waves):
+        pl = pkv.plan(wl.batch, Q, Hq, Hkv, D, b.max_context_len, torch.bfloat16, kernel=kernel)
+        assert pl["split_target"] > 0
+        run_case(wl, kernel=kernel)
+
+
+def test_device_split_partition_equals_host_partition():
+    """Same inputs through both partitions: the same answer to within the
+    output rounding (each equals the oracle), and the device one is
+    deterministic."""
+    import paged_kv_cache_18_gb300 as pkv
+    wl = W.Workload("dev vs host", 12, 32, 8, 128, "bf16", len_range=(100, 9000), seed=830,
+                    num_queries=5)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    ref = oracle_after_append(b)
+    outs = {}
+    for waves in (-1, 1, 2):
+        with tuning(split_waves=waves):
+            pl = pkv.plan(wl.batch, 5, 32, 8, 128, b.max_context_len, torch.bfloat16)
+            assert (pl["split_target"] > 0) == (waves > 0)
+            o1 = d.attend().clone()
+            o2 = d.attend()
+        assert torch.equal(o1, o2)
+        outs[waves] = host_f64(o1, "bf16")
+        assert_close(outs[waves], ref, "bf16", f"waves {waves}")
+    assert np.abs(outs[1] - outs[-1]).max() <= 2 ** -7
+
+
+def test_device_split_partition_fused_append_tree_fp8_and_graph():
+    """The fused append, tree verification and FP8 caches take the same
+    partition; a captured graph replays it."""
+    import oracle
+    import paged_kv_cache_18_gb300 as pkv
+    from tests.gpu_util import assert_close_fp8
+    lens = [37, 4000, 900, 16, 12000, 9]   # every row below L holds data (L >= 7 tree nodes)
+    # fused append + verify
+    wl = W.Workload("dev fused", len(lens), 32, 8, 128, "bf16", context_lens=lens, num_queries=5,
+                    seed=840)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    pkv.binding.TUNING["split_waves"] = 1
+    try:
+        _device_split_calls(wl, b, d)
+    finally:
+        pkv.binding.TUNING.pop("split_waves", None)
+
+
+def _device_split_calls(wl, b, d):
+    import oracle
+    import paged_kv_cache_18_gb300 as pkv
+    from tests.gpu_util import assert_close_fp8
+    lens = list(wl.context_lens)
+    pl = pkv.plan(wl.batch, 5, 32, 8, 128, b.max_context_len, torch.bfloat16)
+    assert pl["split_target"] > 0
+    kn, vn = d.k_new.view(wl.batch, 5, 8, 128), d.v_new.view(wl.batch, 5, 8, 128)
+    out = pkv.append_attention(d.q, kn, vn, d.k_cache, d.v_cache, d.table, d.lens,
+                               max_context_len=b.max_context_len, error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    assert_close(host_f64(out, "bf16"), oracle_after_append(b), "bf16", "fused device split")
+    # tree verification over the same cache
+    masks = W.tree_mask_bits(W.medusa_parents((2, 2)))
+    q7 = torch.randn(wl.batch, len(masks), 32, 128, device="cuda").to(torch.bfloat16)
+    lens7 = d.lens
+    t = pkv.tree_verify_attention(q7, d.k_cache, d.v_cache, d.table, lens7,
+                                  torch.from_numpy(masks.view(np.int64)).cuda(),
+                                  max_context_len=b.max_context_len)
+    from tests.gpu_util import cache_bits
+    kbits, vbits = cache_bits(d.k_cache), cache_bits(d.v_cache)
+    q7h = q7.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.tree_attention(q7h, kbits, vbits, b.block_table, lens7.cpu().numpy(),
+                                1 / np.sqrt(128), "bf16", masks)
+    assert_close(host_f64(t, "bf16"), ref, "bf16", "tree device split")
+    # FP8 cache
+    kc8, vc8 = W.fp8_caches(b, 0.0123, 0.0171)
+    k8, v8 = torch.from_numpy(kc8).cuda(), torch.from_numpy(vc8).cuda()
+    o8 = pkv.paged_attention_fp8(d.q, k8, v8, d.table, d.lens, 0.0123, 0.0171,
+                                 max_context_len=b.max_context_len)
+    ref8 = oracle.paged_attention_fp8(b.q, kc8, vc8, b.block_table, b.context_lens,
+                                      1 / np.sqrt(128), "bf16", 0.0123, 0.0171)
+    assert_close_fp8(host_f64(o8, "bf16"), ref8, "bf16", "fp8 device split")
+    # graph replay
+    ws = torch.empty(pl["workspace_bytes"], dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(d.q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d.attend(out=o, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d.attend(out=o, workspace=ws)
+    for _ in range(2):
+        o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(host_f64(o, "bf16"), oracle_after_append(b), "bf16", "graph device split")
+
+
+def test_device_split_reports_long_context_once():
+    """A context above max_context_len is clamped and recorded, as in the
+    host partition."""
+    wl = W.Workload("dev err", 3, 32, 8, 128, "bf16", context_lens=[3000, 50, 800], seed=850)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    d.lens[1] = 5000   # beyond max_context_len = 3000
+    with tuning(split_waves=1):
+        out = d.attend()
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 3
+    assert torch.isfinite(out.float()).all()
