@@ -645,12 +645,22 @@ def decode_leg(args, name: str, dev, rank: int, world: int, local: int, steps: i
                 max_ctx, dt, kernel=args.kernel, split_blocks=args.split_blocks,
                 stages=args.stages), dtype=torch.uint8, device=dev)
             hkn, hvn = host["k_new"].view(shape4), host["v_new"].view(shape4)
+            # the C ABI call itself, its arguments marshalled once (the
+            # Python binding's per-call checks would add ~20 us of host time)
+            c_call = pkv.binding.lib().pkv_append_attention_host
+            c_args = (out_host.data_ptr(), host["q"].data_ptr(), hkn.data_ptr(), hvn.data_ptr(),
+                      k_cache.data_ptr(), v_cache.data_ptr(), host["table"].data_ptr(),
+                      table.shape[1], host["lens"].data_ptr(), max_ctx, wl.batch, Q,
+                      wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                      k_cache.shape[0], wl.softmax_scale, pkv.binding._DTYPE[dt],
+                      staging.data_ptr(), staging.numel(),
+                      pkv.binding._opts(args.kernel, args.split_blocks, args.stages), None,
+                      stream.cuda_stream)
 
             def e2e_step():
-                pkv.append_attention_host(host["q"], hkn, hvn, k_cache, v_cache, host["table"],
-                                          host["lens"], out_host, staging, max_ctx,
-                                          scale=wl.softmax_scale, kernel=args.kernel,
-                                          split_blocks=args.split_blocks, stages=args.stages)
+                st = c_call(*c_args)
+                if st != 0:
+                    raise RuntimeError(f"pkv_append_attention_host: status {st}")
                 stream.synchronize()
         else:
             def e2e_step():
@@ -674,8 +684,13 @@ def decode_leg(args, name: str, dev, rank: int, world: int, local: int, steps: i
         e2e = {"value": dist_sum(kv_step, dev) / e2e_s / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
                "ms_per_step": 1e3 * e2e_s,
-               "api": ("append_attention_host (pkv_append_attention_host): host buffers in "
-                       "and out, one call per step, then a stream synchronise") if fused else
+               "api": ("pkv_append_attention_host through the C ABI (ctypes, arguments "
+                       "marshalled once): pinned host buffers in and out; q and the new "
+                       "K/V rows read by the kernels in place and the output written in "
+                       "place over the chip-to-chip link, the block table and lengths "
+                       "pulled in by one gather kernel; one call per step, then a stream "
+                       "synchronise")
+                      if fused else
                       ("pinned host tensors copied in with torch, the library's calls, the "
                        "output copied out, then a stream synchronise")}
 

@@ -319,13 +319,19 @@ PKV_API pkv_status pkv_host_step_staging_size(int batch, int num_queries, int nu
  * pkv_append_attention_host -- one decode (or verify) step with the inputs
  * and the output in HOST memory: q_host, k_new_host, v_new_host,
  * block_table_host and context_lens_host (same layouts as for
- * pkv_append_attention) are copied into `staging`, one host-to-device copy
- * each; pkv_append_attention runs on those copies (the caches k_cache /
- * v_cache are device memory, written in place); out is copied back into
- * out_host.  All of it is enqueued on `stream` in that order, and the call
- * returns without waiting: the caller synchronises the stream before it
- * reads out_host or rewrites the host inputs.  Page-locked (pinned) host
- * buffers make the copies asynchronous.
+ * pkv_append_attention) and out_host; pkv_append_attention runs on them
+ * (the caches k_cache / v_cache are device memory, written in place).  A
+ * buffer the GPU can address -- page-locked memory mapped into the device's
+ * address space, as cudaHostAlloc / cudaHostRegister give it under unified
+ * addressing; on GB300 the chip-to-chip link carries the accesses -- needs
+ * no copy: the new rows, and q when the plan splits a sequence at most 4
+ * ways, are read by the kernels in place, out_host is written in place, and
+ * the block table, the lengths (read first by every CTA) and any other q
+ * are pulled into `staging` by one gather kernel.  Any other
+ * buffer takes one host-to-device copy into `staging` (the output: one copy
+ * back).  All of it is enqueued on `stream`, and the call returns without
+ * waiting: the caller synchronises the stream before it reads out_host or
+ * rewrites the host inputs.
  *
  *   staging : device, 256-byte aligned, >= pkv_host_step_staging_size()
  *             bytes (PKV_ERR_WORKSPACE otherwise); owned by the caller and

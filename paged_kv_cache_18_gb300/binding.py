@@ -80,6 +80,8 @@ class Plan(ctypes.Structure):
 def lib() -> ctypes.CDLL:
     """The loaded library (raises if it has not been built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -172,7 +174,14 @@ def version() -> str:
     return lib().pkv_version().decode()
 
 
+# The current stream's raw handle, without building a torch.cuda.Stream object
+# on every call (that costs several microseconds of host time per call).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(t: torch.Tensor) -> int:
+    if _raw_stream is not None:
+        return _raw_stream(t.get_device())
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
@@ -414,11 +423,11 @@ def append_attention_host(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
     """One step with host inputs and output (pkv_append_attention_host).
 
     q, k_new, v_new, block_table, context_lens and out are CPU tensors in the
-    layouts of append_attention (pinned memory makes the copies asynchronous);
-    the caches and ``staging`` (uint8, host_step_staging_size bytes) live on
-    the GPU.  The copies in, the fused append + attention and the copy of the
-    output into ``out`` are enqueued on the caches' current stream; ``out``
-    holds the result once that stream has been synchronised."""
+    layouts of append_attention; the caches and ``staging`` (uint8,
+    host_step_staging_size bytes) live on the GPU.  Pinned tensors are read
+    (out: written) by the kernels in place; pageable ones go through
+    ``staging``.  Everything is enqueued on the caches' current stream;
+    ``out`` holds the result once that stream has been synchronised."""
     NB, Hkv, bs, D = _cache_args(k_cache, v_cache)
     q4 = q if q.dim() == 4 else q.unsqueeze(1)
     B, Q, Hq, _ = q4.shape

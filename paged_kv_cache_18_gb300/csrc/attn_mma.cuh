@@ -173,61 +173,6 @@ __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
   const int n_my = nspan > bl ? (nspan - bl + BL - 1) / BL : 0;
   const int col0 = cg * NT * 8;
 
-  // Q^T operand fragments of this warp's columns (B operand: k = head dim).
-  // 16-bit caches: the natural k order.  FP8 caches: k-step ks covers head
-  // dims 16 ks .. 16 ks + 15 with lane c holding 16 ks + 4c .. 4c + 3 (the
-  // order the K fragments arrive in), shifted by 2^qshift into f16 range.
-  uint32_t qf[KS][NT][2];
-  float colfac[NT][2];  // score scale of my two columns of each tile
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int64_t row = cta_row_index(p, b, kvh, chunk, col0 + nt * 8 + g);
-    const T *qrow = reinterpret_cast<const T *>(p.q) + (row < 0 ? 0 : row) * D;
-    colfac[nt][0] = colfac[nt][1] = p.scale_log2;
-    if constexpr (!FP8) {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qf[ks][nt][0] =
-            row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
-        qf[ks][nt][1] =
-            row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * c);
-      }
-    } else {
-      float qv[KS][4];
-      float amax = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t w0 = 0u, w1 = 0u;
-        if (row >= 0) {
-          const uint2 w = *reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * c);
-          w0 = w.x;
-          w1 = w.y;
-        }
-        Mma<T>::unpack(w0, qv[ks][0], qv[ks][1]);
-        Mma<T>::unpack(w1, qv[ks][2], qv[ks][3]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qv[ks][e]));
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-      // amax in [2^(ex-1), 2^ex): scaling by 2^(15 - ex) puts the row's
-      // largest magnitude in [2^14, 2^15), inside f16 range.
-      const int ex = amax > 0.f ? ((__float_as_int(amax) >> 23) & 0xff) - 126 : 15;
-      const int qshift = max(-120, min(120, 15 - ex));
-      const float up = exp2f(static_cast<float>(qshift));
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qf[ks][nt][0] = Mma<__half>::pack(qv[ks][0] * up, qv[ks][1] * up);
-        qf[ks][nt][1] = Mma<__half>::pack(qv[ks][2] * up, qv[ks][3] * up);
-      }
-      // my score columns 2c, 2c+1 were shifted by the lanes of groups 2c, 2c+1
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int sh = __shfl_sync(kFull, qshift, 4 * (2 * c + e));
-        colfac[nt][e] = p.scale_log2 * exp2f(static_cast<float>(-sh));
-      }
-    }
-  }
   const int mask_from = L - p.num_queries;  // first row some column may not see
 
   // Online-softmax state.
@@ -304,6 +249,64 @@ __global__ void __launch_bounds__(BL * CG * 32, (mma_min_ctas<CG, NT>()))
   const int npre = min(NS, n_my);
   for (int i = 0; i < npre; ++i) issue(i);
   int issued = npre;
+
+  // q is loaded once the first copies are in flight, so that its latency
+  // (a round trip to wherever q lives) overlaps theirs.
+  // Q^T operand fragments of this warp's columns (B operand: k = head dim).
+  // 16-bit caches: the natural k order.  FP8 caches: k-step ks covers head
+  // dims 16 ks .. 16 ks + 15 with lane c holding 16 ks + 4c .. 4c + 3 (the
+  // order the K fragments arrive in), shifted by 2^qshift into f16 range.
+  uint32_t qf[KS][NT][2];
+  float colfac[NT][2];  // score scale of my two columns of each tile
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int64_t row = cta_row_index(p, b, kvh, chunk, col0 + nt * 8 + g);
+    const T *qrow = reinterpret_cast<const T *>(p.q) + (row < 0 ? 0 : row) * D;
+    colfac[nt][0] = colfac[nt][1] = p.scale_log2;
+    if constexpr (!FP8) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qf[ks][nt][0] =
+            row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * c);
+        qf[ks][nt][1] =
+            row < 0 ? 0u : *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * c);
+      }
+    } else {
+      float qv[KS][4];
+      float amax = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t w0 = 0u, w1 = 0u;
+        if (row >= 0) {
+          const uint2 w = *reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * c);
+          w0 = w.x;
+          w1 = w.y;
+        }
+        Mma<T>::unpack(w0, qv[ks][0], qv[ks][1]);
+        Mma<T>::unpack(w1, qv[ks][2], qv[ks][3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qv[ks][e]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      // amax in [2^(ex-1), 2^ex): scaling by 2^(15 - ex) puts the row's
+      // largest magnitude in [2^14, 2^15), inside f16 range.
+      const int ex = amax > 0.f ? ((__float_as_int(amax) >> 23) & 0xff) - 126 : 15;
+      const int qshift = max(-120, min(120, 15 - ex));
+      const float up = exp2f(static_cast<float>(qshift));
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qf[ks][nt][0] = Mma<__half>::pack(qv[ks][0] * up, qv[ks][1] * up);
+        qf[ks][nt][1] = Mma<__half>::pack(qv[ks][2] * up, qv[ks][3] * up);
+      }
+      // my score columns 2c, 2c+1 were shifted by the lanes of groups 2c, 2c+1
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int sh = __shfl_sync(kFull, qshift, 4 * (2 * c + e));
+        colfac[nt][e] = p.scale_log2 * exp2f(static_cast<float>(-sh));
+      }
+    }
+  }
 
   int consumed = 0;
   bool aborted = false;

@@ -231,6 +231,61 @@ cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src,
 
 }  // namespace pkv
 
+// ---- host inputs gathered into device memory ---------------------------------
+// One launch copies up to kMaxGather buffers from mapped page-locked host
+// memory (reached over the chip-to-chip link) into device memory: every CTA
+// walks all of them in 16-byte vectors (4-byte words for a buffer whose
+// addresses or size are not multiples of 16), so the link sees many requests
+// in flight at once.  The kernel that follows is its programmatic dependent.
+namespace pkv {
+namespace {
+
+__global__ void __launch_bounds__(256) gather_kernel(const GatherList list) {
+  pdl_launch_dependents();
+  // All buffers' units (16-byte vectors of the wide ones, 4-byte words of the
+  // others) form one index space, so every thread's loads are independent
+  // and one round trip over the link serves the whole gather.
+  int64_t first[kMaxGather + 1];
+  bool wide[kMaxGather];
+  first[0] = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxGather; ++k) {
+    const GatherItem &g = list.item[k];
+    wide[k] = ((reinterpret_cast<uintptr_t>(g.src) | reinterpret_cast<uintptr_t>(g.dst) |
+                static_cast<uintptr_t>(g.bytes)) & 15) == 0;
+    first[k + 1] = first[k] + (k < list.count ? g.bytes / (wide[k] ? 16 : 4) : 0);
+  }
+  const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < first[list.count]; i += nthr) {
+    int k = 0;
+    while (i >= first[k + 1]) ++k;
+    const int64_t j = i - first[k];
+    const GatherItem &g = list.item[k];
+    if (wide[k]) {
+      static_cast<uint4 *>(g.dst)[j] = static_cast<const uint4 *>(g.src)[j];
+    } else {
+      static_cast<uint32_t *>(g.dst)[j] = static_cast<const uint32_t *>(g.src)[j];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t gather_launch(const GatherList &list, int sm_count, cudaStream_t stream) {
+  if (list.count < 1 || list.count > kMaxGather) return list.count == 0 ? cudaSuccess
+                                                                        : cudaErrorInvalidValue;
+  int64_t units = 0;  // an upper bound: every buffer in 4-byte words
+  for (int k = 0; k < list.count; ++k) units += list.item[k].bytes / 4;
+  if (units == 0) return cudaSuccess;
+  const int64_t want = (units + 255) / 256;
+  const int grid = static_cast<int>(want < 4LL * sm_count ? want : 4LL * sm_count);
+  gather_kernel<<<grid, 256, 0, stream>>>(list);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv
+
 // ---- the bounded wait, exercised ---------------------------------------------
 // Every wait of the library's kernels on an mbarrier gives up after a time
 // limit, records PKV_DEVERR_TIMEOUT and lets the kernel return.  This kernel

@@ -883,6 +883,19 @@ pkv_status pkv_host_step_staging_size(int batch, int num_queries, int num_heads,
   return s;
 }
 
+// Device address through which kernels can read or write host memory `p`
+// in place (page-locked, mapped memory: on GB300 the GPU reaches it over the
+// chip-to-chip link), or nullptr when they cannot (pageable memory, or a
+// pointer the runtime does not know).
+void *host_mapped(const void *p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();  // clear the lookup's error
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 pkv_status pkv_append_attention_host(void *out_host, const void *q_host, const void *k_new_host,
                                      const void *v_new_host, void *k_cache, void *v_cache,
                                      const int32_t *block_table_host, int max_blocks_per_seq,
@@ -909,36 +922,87 @@ pkv_status pkv_append_attention_host(void *out_host, const void *q_host, const v
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const Shape shape = make_shape(batch, num_queries, num_heads, num_kv_heads, head_dim,
                                  block_size, max_context_len, dtype);
-  // Every check of the launch, on the staged pointers, before anything is enqueued.
-  auto attend = [&](bool check_only) {
-    return run_attention(base + st.out, base + st.q, k_cache, v_cache,
-                         reinterpret_cast<const int32_t *>(base + st.table), max_blocks_per_seq,
-                         reinterpret_cast<const int32_t *>(base + st.lens), shape, num_blocks,
-                         scale, base + st.ws, staging_bytes - st.ws, options, error_word, cs,
-                         base + st.k_new, base + st.v_new, nullptr, 0, 1.f, 1.f, check_only);
-  };
-  s = attend(true);
-  if (s != PKV_OK) return s;
   const size_t rows = static_cast<size_t>(batch) * num_queries;
   const size_t q_bytes = rows * num_heads * head_dim * elt_bytes(dtype);
   const size_t kv_bytes = rows * num_kv_heads * head_dim * elt_bytes(dtype);
-  // The inputs, one copy each (host to device), in stream order before the launch.
-  const struct {
+  // Where the kernels find each input.  The block table and the lengths are
+  // read at the start of every CTA, before its first copy can be issued, so
+  // they are staged in device memory: pulled in by one gather kernel when
+  // the GPU can address them (mapped page-locked memory; on GB300 the
+  // chip-to-chip link carries the accesses).  The new K/V rows are read by
+  // the kernels in place (only where a sequence ends), and so is q when the
+  // plan splits a sequence at most 4 ways (each q row is read by its splits'
+  // CTAs, after their first copies are in flight; with more splits the
+  // repeated fetches across the link cost more than one gather: 22 splits of
+  // the speculative-verify step, 0.11 ms in place against 0.095 gathered),
+  // so those bytes cross the link while the cache streams from HBM.
+  // An input the GPU cannot address takes one host-to-device copy into the
+  // staging buffer.  The output is written straight into mapped host memory
+  // (stores do not wait), else staged and copied back.
+  pkv_plan plan{};
+  {
+    KernelInfo info;
+    int device = 0, sms = 0;
+    s = device_plan(shape, options, &plan, &info, &device, &sms);
+    if (s != PKV_OK) return s;
+  }
+  const bool q_in_place = plan.num_splits <= 4 && plan.split_target == 0;
+  struct In {
     size_t off;
     const void *src;
     size_t n;
-  } in[] = {{st.q, q_host, q_bytes},
-            {st.k_new, k_new_host, kv_bytes},
-            {st.v_new, v_new_host, kv_bytes},
+    bool in_place_ok;
+    const void *use;  // what the kernels read
+    bool copy;        // a host-to-device copy into the staging buffer
+  } in[] = {{st.q, q_host, q_bytes, q_in_place, nullptr, false},
+            {st.k_new, k_new_host, kv_bytes, true, nullptr, false},
+            {st.v_new, v_new_host, kv_bytes, true, nullptr, false},
             {st.table, block_table_host,
-             static_cast<size_t>(batch) * max_blocks_per_seq * sizeof(int32_t)},
-            {st.lens, context_lens_host, static_cast<size_t>(batch) * sizeof(int32_t)}};
-  for (const auto &c : in)
-    if (cudaMemcpyAsync(base + c.off, c.src, c.n, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+             static_cast<size_t>(batch) * max_blocks_per_seq * sizeof(int32_t), false, nullptr,
+             false},
+            {st.lens, context_lens_host, static_cast<size_t>(batch) * sizeof(int32_t), false,
+             nullptr, false}};
+  GatherList gather{};
+  for (auto &c : in) {
+    const void *mapped = host_mapped(c.src);
+    if (mapped && c.in_place_ok && aligned(mapped, 16)) {
+      c.use = mapped;
+    } else if (mapped && aligned(mapped, 4)) {
+      gather.item[gather.count++] = {mapped, base + c.off, static_cast<int64_t>(c.n)};
+      c.use = base + c.off;
+    } else {
+      c.copy = true;
+      c.use = base + c.off;
+    }
+  }
+  void *out_dev = host_mapped(out_host);
+  if (out_dev && !aligned(out_dev, 16)) out_dev = nullptr;
+  const bool out_staged = out_dev == nullptr;
+  if (out_staged) out_dev = base + st.out;
+  // Every check of the launch, on the pointers it will use, before anything is enqueued.
+  auto attend = [&](bool check_only) {
+    return run_attention(out_dev, in[0].use, k_cache, v_cache,
+                         static_cast<const int32_t *>(in[3].use), max_blocks_per_seq,
+                         static_cast<const int32_t *>(in[4].use), shape, num_blocks, scale,
+                         base + st.ws, staging_bytes - st.ws, options, error_word, cs, in[1].use,
+                         in[2].use, nullptr, 0, 1.f, 1.f, check_only);
+  };
+  s = attend(true);
+  if (s != PKV_OK) return s;
+  for (const auto &c : in)  // host to device, one copy per input the GPU cannot address
+    if (c.copy && cudaMemcpyAsync(base + c.off, c.src, c.n, cudaMemcpyHostToDevice, cs) !=
+                      cudaSuccess)
       return PKV_ERR_CUDA;
+  if (gather.count > 0) {
+    int device = 0, sms = 0;
+    if (current_sm_count(&device, &sms) != cudaSuccess ||
+        gather_launch(gather, sms, cs) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
   s = attend(false);
   if (s != PKV_OK) return s;
-  if (cudaMemcpyAsync(out_host, base + st.out, q_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+  if (out_staged &&
+      cudaMemcpyAsync(out_host, base + st.out, q_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;
 }

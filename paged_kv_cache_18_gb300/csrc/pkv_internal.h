@@ -100,6 +100,21 @@ cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src,
                                int64_t num_blocks, int32_t *err, int sm_count,
                                cudaStream_t stream);
 
+// Copies of mapped host buffers into device memory, in one launch (the
+// kernel after it is its programmatic dependent).  Sizes are multiples of 4
+// bytes, addresses 4-byte aligned.
+constexpr int kMaxGather = 6;
+struct GatherItem {
+  const void *src;
+  void *dst;
+  int64_t bytes;
+};
+struct GatherList {
+  GatherItem item[kMaxGather];
+  int count;
+};
+cudaError_t gather_launch(const GatherList &list, int sm_count, cudaStream_t stream);
+
 // kv_append.
 cudaError_t append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           const int64_t *slots, int64_t num_tokens, int num_kv_heads,

@@ -1,8 +1,10 @@
 """The host-buffer step (pkv_append_attention_host): inputs and output in
-pinned host memory, copied in and out around the fused append + attention on
-the caller's stream.  Its output must equal the oracle within tolerance, its
-cache writes must be bit-exact, and it must give exactly what the same
-launch gives on device copies of the inputs."""
+host memory.  Page-locked (pinned, mapped) buffers are read and written by
+the kernels in place; pageable ones are copied in and out around the fused
+append + attention on the caller's stream.  Either way the output must
+equal the oracle within tolerance, the cache writes must be bit-exact, and
+the result must be exactly what the same launch gives on device copies of
+the inputs."""
 import numpy as np
 import pytest
 import torch
@@ -124,3 +126,37 @@ def test_host_step_small_staging_is_rejected_before_any_copy():
     torch.cuda.synchronize()
     assert bool((out == 7.0).all())
     np.testing.assert_array_equal(cache_bits(d.k_cache), before)
+
+
+@pytest.mark.parametrize("pinned_mask", [0b000000, 0b101010, 0b010101, 0b111110])
+def test_host_step_pageable_and_mixed_buffers(pinned_mask):
+    """Bit k of pinned_mask: buffer k of (q, k_new, v_new, table, lens, out)
+    is page-locked (read or written in place), else pageable (staged)."""
+    Q = 5
+    wl = W.Workload("host step mixed", 5, 32, 8, 128, "bf16", context_lens=[5, 17, 90, 700, 3000],
+                    num_queries=Q, seed=940 + pinned_mask)
+    b = W.make_batch(wl)
+    d_host, d_dev = DeviceBatch(b), DeviceBatch(b)
+    h = host_inputs(d_host, Q)
+    names = ["q", "k_new", "v_new", "table", "lens"]
+    for k, n in enumerate(names):
+        if not (pinned_mask >> k) & 1:
+            h[n] = h[n].clone()           # a pageable copy
+            assert not h[n].is_pinned()
+    out = torch.full_like(h["q"], float("nan"))
+    if (pinned_mask >> 5) & 1:
+        out = out.pin_memory()
+    staging = staging_for(b, Q)
+    pkv.append_attention_host(h["q"], h["k_new"], h["v_new"], d_host.k_cache, d_host.v_cache,
+                              h["table"], h["lens"], out, staging, b.max_context_len,
+                              error_word=d_host.err)
+    torch.cuda.current_stream().synchronize()
+    assert int(d_host.err.item()) == 0
+    ref_dev = pkv.append_attention(d_dev.q, d_dev.k_new.view(5, Q, 8, 128),
+                                   d_dev.v_new.view(5, Q, 8, 128), d_dev.k_cache, d_dev.v_cache,
+                                   d_dev.table, d_dev.lens, max_context_len=b.max_context_len)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_dev.cpu())
+    for a, c in ((d_host.k_cache, d_dev.k_cache), (d_host.v_cache, d_dev.v_cache)):
+        np.testing.assert_array_equal(cache_bits(a), cache_bits(c))
+    assert_close(host_f64(out, "bf16"), oracle_after_append(b), "bf16", wl.name)
