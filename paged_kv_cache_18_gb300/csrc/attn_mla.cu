@@ -71,10 +71,6 @@ __device__ __forceinline__ uint32_t tile_off(int row, int d) {
   return (bo >> 7) * (kBlockSize * 128) + row * 128 + ((((bo & 127) >> 4) ^ (row & 7)) << 4);
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 // Named barrier of one column group's four warps (ids 1 and 2).
 __device__ __forceinline__ void group_sync(int cg) {
   if (cg == 0)
