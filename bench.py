@@ -128,6 +128,14 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
+    def ready(self, n: int = 3, timeout_s: float = 5.0):
+        """Wait until the sampler has taken n samples: nvidia-smi's start-up
+        (driver initialisation) disturbs the GPU for a moment, which must not
+        fall inside a timed region."""
+        t0 = time.time()
+        while self.proc is not None and len(self.samples) < n and time.time() - t0 < timeout_s:
+            time.sleep(0.02)
+
     def _read(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
@@ -361,7 +369,7 @@ def run_prefill(args):
     ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
     if sampler:
-        time.sleep(0.3)
+        sampler.ready()
     barrier()
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
@@ -574,6 +582,8 @@ def decode_leg(args, name: str, dev, rank: int, world: int, local: int, steps: i
             attn(qq, k_cache, v_cache, tb, ln, **opts)
 
     stream = torch.cuda.current_stream(dev)
+    # the clock sampler starts now, so that nvidia-smi's start-up falls in the warm-up
+    sampler = ClockSampler(local) if rank == 0 and clocks_on else None
     # Warm-up: the requested steps, then more until WARMUP_S of GPU work has
     # run, so that the clocks and the memory system are at their working
     # state when the timed region starts (after the host-side set-up the GPU
@@ -595,9 +605,8 @@ def decode_leg(args, name: str, dev, rank: int, world: int, local: int, steps: i
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local) if rank == 0 and clocks_on else None
     if sampler:
-        time.sleep(0.3)
+        sampler.ready()
     barrier()
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
@@ -971,7 +980,7 @@ def run_mla(args):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
     if sampler:
-        time.sleep(0.3)
+        sampler.ready()
     barrier()
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
