@@ -64,7 +64,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32, (D <= 128 ? (DEV ? 6 : 8) : 
     stride = 1;
   } else {  // device partition: [item][CTA column], the items of (b, unit) consecutive
     ns = p.split_info[2 * b];
-    const int item0 = p.split_info[2 * b + 1];
+    int item0 = p.split_info[2 * b + 1];
+    // A layout that cannot be the attention kernel's (never, unless that
+    // kernel did not publish it) is recorded and merged as no split at all
+    // rather than read outside the workspace.
+    const int units = p.num_kv_heads * p.row_chunks;
+    if (ns < 1 || item0 < 0 ||
+        static_cast<int64_t>(item0) + static_cast<int64_t>(ns) * units > p.split_target) {
+      if (threadIdx.x == 0) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
+      ns = 0;
+      item0 = 0;
+    }
     const int h = static_cast<int>(row % p.num_heads);
     const int j = static_cast<int>((row / p.num_heads) % p.num_queries);
     const int kvh = h / p.group;

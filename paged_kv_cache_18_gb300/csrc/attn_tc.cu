@@ -112,12 +112,48 @@ struct StageInfo {
 // A work item: one split of one (sequence, KV head, row chunk).  Items are
 // numbered split-fastest; the persistent CTA g takes items g, g + G, ...,
 // every role enumerating the same sequence.
+//
+// With the device partition (split_target > 0), items are the flat list of
+// cta_work in pkv_device.cuh: the kernel's prologue leaves, per sequence b,
+// its split count, first item and block count in shared memory (`dev`),
+// and item i is found there; its partials go to [item][CTA column].
 struct Item {
-  int b, kvh, chunk_row, split, L, blk_begin, nspan, n_chunks, ns_b;
+  int b, kvh, chunk_row, split, L, blk_begin, nspan, n_chunks, ns_b, idx;
   bool valid;
 };
-__device__ __forceinline__ Item decode_item(const AttnParams &p, int i, bool report) {
+struct DevSplits {
+  int ns[32], first[32], nb[32];
+};
+__device__ __forceinline__ Item decode_item(const AttnParams &p, int i, bool report,
+                                            const DevSplits *dev) {
   Item it;
+  it.idx = i;
+  if (p.split_target > 0) {
+    const int units = p.num_kv_heads * p.row_chunks;
+    int b = -1;
+    for (int bb = 0; bb < p.batch; ++bb)
+      if (i < dev->first[bb] + dev->ns[bb] * units) {
+        b = bb;
+        break;
+      }
+    it.valid = b >= 0;
+    it.b = b < 0 ? 0 : b;
+    const int ns = b < 0 ? 1 : dev->ns[b];
+    const int r = b < 0 ? 0 : i - dev->first[b];
+    const int u = r / ns;
+    it.split = r - u * ns;
+    it.kvh = u / p.row_chunks;
+    it.chunk_row = u - it.kvh * p.row_chunks;
+    const SeqExtent ext = seq_extent(p, it.b, report && it.valid && r == 0);
+    it.L = ext.L;
+    const int nb = b < 0 ? 0 : dev->nb[b];
+    it.blk_begin = static_cast<int>(static_cast<int64_t>(it.split) * nb / ns);
+    const int blk_end = static_cast<int>(static_cast<int64_t>(it.split + 1) * nb / ns);
+    it.nspan = it.valid ? max(blk_end - it.blk_begin, 0) : 0;
+    it.n_chunks = (it.nspan + kChunkBlocks - 1) / kChunkBlocks;
+    it.ns_b = ns;
+    return it;
+  }
   const int ns = p.num_splits, Y = p.num_kv_heads * p.row_chunks;
   it.split = i % ns;
   const int t = i / ns;
@@ -134,6 +170,13 @@ __device__ __forceinline__ Item decode_item(const AttnParams &p, int i, bool rep
   it.n_chunks = (it.nspan + kChunkBlocks - 1) / kChunkBlocks;
   it.ns_b = max(1, min(ns, (ext.nblk + p.split_blocks - 1) / p.split_blocks));
   return it;
+}
+
+// Index of the partial of CTA column `col` (output row `row`) of item `it`.
+__device__ __forceinline__ int64_t tc_partial(const AttnParams &p, const Item &it, int64_t row,
+                                              int col) {
+  return p.split_target == 0 ? row * p.num_splits + it.split
+                             : static_cast<int64_t>(it.idx) * p.rows_per_cta + col;
 }
 
 template <typename T, int D, int NC, int NS, int PB>
@@ -160,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float red[4][NC];
   __shared__ volatile int s_abort;
+  __shared__ DevSplits dev;  // the device partition's per-sequence layout
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G0 = blockIdx.x, GS = gridDim.x;
@@ -193,6 +237,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&mma_idle), 1);
     fence_mbar_init();
   }
+  if (p.split_target > 0 && warp == 0) {  // warp-collective; read by every role below
+    const SeqSplits sp = device_splits(p);
+    dev.ns[lane] = sp.ns;
+    dev.first[lane] = sp.first_item;
+    dev.nb[lane] = sp.nb;
+    // the merge kernel finds each sequence's items from this (every CTA
+    // computes the same layout; the first one publishes it)
+    if (blockIdx.x == 0 && lane < p.batch) {
+      p.split_info[2 * lane] = sp.ns;
+      p.split_info[2 * lane + 1] = sp.first_item;
+    }
+  }
   if (warp == kIssuerWarp) {
     asm volatile(
         "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -225,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0, na = 0, issued = 0;
     bool ok = true;
     for (int i = G0; i < num_items && ok; i += GS) {
-      const Item it = decode_item(p, i, false);
+      const Item it = decode_item(p, i, false, &dev);
       if (!active(it)) continue;
       const int qb = na & 1;
       if (is_k) {
@@ -317,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item it_s{}, it_v{};
       auto next_active = [&](int &i, Item &it) {
         for (; i < num_items; i += GS) {
-          it = decode_item(p, i, false);
+          it = decode_item(p, i, false, &dev);
           if (active(it)) return true;
         }
         return false;
@@ -409,18 +465,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0, na = 0;
     bool ok = true;
     for (int i = G0; i < num_items && ok; i += GS) {
-      const Item it = decode_item(p, i, tid == 0);
+      const Item it = decode_item(p, i, tid == 0, &dev);
       if (!it.valid) continue;
       if (it.n_chunks == 0) {
         // an empty sequence: zero output rows (one split)
         for (int j = 0; j < NCW; ++j) {
           const int64_t row = cta_row_index(p, it.b, it.kvh, it.chunk_row, col0 + j);
           if (row < 0) continue;
-          if (p.num_splits == 1) {
+          if (p.num_splits == 1 && p.split_target == 0) {
             reinterpret_cast<T *>(p.out)[row * D + kl] = from_float<T>(0.f);
           } else {
-            p.part_o[(row * p.num_splits + it.split) * D + kl] = 0.f;
-            if (quad == 0 && lane == 0) p.part_lse[row * p.num_splits + it.split] = -INFINITY;
+            const int64_t pi = tc_partial(p, it, row, col0 + j);
+            p.part_o[pi * D + kl] = 0.f;
+            if (quad == 0 && lane == 0) p.part_lse[pi] = -INFINITY;
           }
         }
         continue;
@@ -638,17 +695,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!real) continue;
         const float inv = lsum[j] > 0.f ? __fdividef(1.f, lsum[j]) : 0.f;
         const float o = o_hi[j] + o_lo[j];
-        if (p.num_splits == 1) {
+        if (p.num_splits == 1 && p.split_target == 0) {
           reinterpret_cast<T *>(p.out)[row * D + kl] = from_float<T>(o * inv * p.out_scale);
         } else {
-          __stcg(p.part_o + (row * p.num_splits + it.split) * D + kl, o * inv);
+          const int64_t pi = tc_partial(p, it, row, col);
+          __stcg(p.part_o + pi * D + kl, o * inv);
           if (lane == j) {
             lse_mine = lsum[j] > 0.f ? m[j] + __log2f(lsum[j]) : -INFINITY;
-            row_mine = row;
+            row_mine = pi;
           }
         }
       }
-      if (quad == 0 && row_mine >= 0) __stcg(p.part_lse + row_mine * p.num_splits + it.split, lse_mine);
+      if (quad == 0 && row_mine >= 0) __stcg(p.part_lse + row_mine, lse_mine);
       softmax_sync();  // red[] is reused by the next item
       ++na;
     }
@@ -691,8 +749,10 @@ template <typename T, int NC, int NS>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
   const KernelInfo k = info_t<T, NC, NS>();
-  // persistent: grid.x CTAs walk the grid.y x grid.z x splits items
-  const int items = p.num_splits * p.num_kv_heads * p.row_chunks * p.batch;
+  // persistent: grid.x CTAs walk the grid.y x grid.z x splits items (or the
+  // device partition's split_target items)
+  const int items = p.split_target > 0 ? p.split_target
+                                       : p.num_splits * p.num_kv_heads * p.row_chunks * p.batch;
   attn_tc_kernel<T, 128, NC, NS, p_buffers<NS>()>
       <<<dim3(grid.x), k.threads, k.smem, stream>>>(km, vm, p, items);
   return cudaGetLastError();

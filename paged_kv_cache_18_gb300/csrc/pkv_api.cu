@@ -283,10 +283,14 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
   // 65536 rows: one exact wave of 456 CTAs, 0.806 of the HBM peak, against
   // 0.842 for the host's 384; speculative verify 0.588 against 0.639), the
   // kernels being bound by the bytes in flight rather than by idle slots.
-  const int waves = opt ? opt->split_waves : 0;
+  // The tcgen05 kernel (one CTA per SM, each taking whole items) takes the
+  // device partition by default, two waves of items of nearly equal length
+  // (verify: 0.527 of the HBM peak, against 0.483 for the host plan's
+  // 256-block items, which leave 1.7 waves, and 0.492 for one wave).
+  int waves = opt ? opt->split_waves : 0;
+  if (persistent && waves == 0) waves = 2;
   const int64_t unit_rows = static_cast<int64_t>(s.num_kv_heads) * pl->row_chunks;
-  if (!persistent && waves > 0 && !(opt && opt->split_blocks > 0) && s.batch <= 32 &&
-      max_blocks > 0 &&
+  if (waves > 0 && !(opt && opt->split_blocks > 0) && s.batch <= 32 && max_blocks > 0 &&
       static_cast<int64_t>(max_blocks) * s.batch < (int64_t(1) << 30)) {  // int sums on device
     const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
     int64_t target = (waves > 0 ? waves : 1) * slots;
@@ -296,10 +300,12 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
       pl->split_blocks = 0;
       pl->num_splits = static_cast<int>(std::max<int64_t>(1, target / unit_rows));
       pl->grid_x = pl->split_target;
+      if (persistent && opt && opt->persistent == 1)  // walk: one CTA per resident slot
+        pl->grid_x = static_cast<int>(std::min<int64_t>(target, slots));
       pl->grid_y = pl->grid_z = 1;
       pl->ctas_per_sm = ctas_per_sm;
-      const WorkspaceLayout w =
-          workspace_layout(s, pl->num_splits, pl->row_chunks, pl->rows_per_cta, 2, pl->split_target);
+      const WorkspaceLayout w = workspace_layout(s, pl->num_splits, pl->row_chunks,
+                                                 pl->rows_per_cta, 2, pl->split_target);
       pl->workspace_bytes = w.total;
       pl->merge_kernel = 1;
       return;

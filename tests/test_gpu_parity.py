@@ -850,3 +850,22 @@ def test_device_split_reports_long_context_once():
     torch.cuda.synchronize()
     assert int(d.err.item()) == 3
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("lens_i", range(len(DEVICE_LENS)))
+@pytest.mark.parametrize("Q,Hq,Hkv", [(5, 32, 8), (1, 32, 8), (3, 36, 9)])
+@pytest.mark.parametrize("waves,persistent", [(0, 0), (2, 0), (3, 1)])
+def test_tc_device_partition(lens_i, Q, Hq, Hkv, waves, persistent):
+    """The tcgen05 kernel takes the device partition by default (items of
+    nearly equal length, one wave of SMs): one CTA per item, or CTAs walking
+    several items (persistent 1)."""
+    import paged_kv_cache_18_gb300 as pkv
+    lens = [max(L, Q) for L in DEVICE_LENS[lens_i]]
+    wl = W.Workload(f"tc dev {lens_i} Q{Q} w{waves} p{persistent}", len(lens), Hq, Hkv, 128,
+                    "bf16", context_lens=lens, num_queries=Q,
+                    seed=1900 + lens_i * 11 + Q + waves + persistent)
+    with tuning(split_waves=waves, persistent=persistent):
+        b_max = max(lens)
+        pl = pkv.plan(len(lens), Q, Hq, Hkv, 128, b_max, torch.bfloat16, kernel=3)
+        assert pl["split_target"] > 0
+        run_case(wl, kernel=3)
