@@ -366,8 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk = smem_desc(0, 16, 1024, kSwizzle128);
       const uint64_t dv = smem_desc(0, G::kPanelBytes, 1024, kSwizzle128);
       const uint64_t dp = smem_desc(0, 128, kChunkKeys * 16, kSwizzleNone);
-      // Cursors over the flat chunk sequence: S^T runs up to one chunk ahead
-      // of P.V (two S^T buffers), across item boundaries.
+      // Cursors over the flat chunk sequence, across item boundaries: S^T
+      // runs ahead of P.V as far as its two buffers allow.
       int i_s = G0, c_s = 0, na_s = 0, g_s = 0;   // next S^T: item, chunk, active index, flat
       int i_v = G0, c_v = 0, na_v = 0, g_v = 0;   // next P.V
       Item it_s{}, it_v{};
@@ -412,21 +412,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           more_s = next_active(i_s, it_s);
         }
       };
-      bool ok = true;
-      if (more_s) {
-        ok = s_ready(true);
-        if (ok) issue_s();
-      }
-      while (ok && more_v) {
-        if (more_s && g_s == g_v + 1 && s_ready(false)) issue_s();
+      // P.V of the next chunk: its P^T written, its V landed and, for an
+      // item's first chunk, the O^T buffer released by the item two back.
+      auto pv_ready = [&]() -> bool {
         const int ob = na_v & 1;
-        if (!mbar_wait_bounded(smem_u32(&p_full[g_v % PB]), (g_v / PB) & 1) ||
-            !mbar_wait_bounded(smem_u32(&v_full[g_v % NS]), (g_v / NS) & 1) ||
-            (c_v == 0 && na_v >= 2 &&
-             !mbar_wait_bounded(smem_u32(&o_free[ob]), ((na_v >> 1) - 1) & 1))) {
-          ok = false;
-          break;
-        }
+        return mbar_test(smem_u32(&p_full[g_v % PB]), (g_v / PB) & 1) &&
+               mbar_test(smem_u32(&v_full[g_v % NS]), (g_v / NS) & 1) &&
+               (c_v > 0 || na_v < 2 || mbar_test(smem_u32(&o_free[ob]), ((na_v >> 1) - 1) & 1));
+      };
+      auto issue_pv = [&]() {
+        const int ob = na_v & 1;
         fence_after();
         const uint64_t va = dv | ((sbase + G::kVOff + (g_v % NS) * G::kTileBytes) >> 4);
         const uint64_t pa = dp | ((sbase + G::kPOff + (g_v % PB) * 2 * G::kPBytes) >> 4);
@@ -442,12 +437,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           i_v += GS;
           more_v = next_active(i_v, it_v);
         }
-        if (more_s && g_s == g_v) {
-          if (!s_ready(true)) {
-            ok = false;
-            break;
-          }
+      };
+      // The two MMA streams are issued as soon as each is ready, each in
+      // chunk order: S^T of chunk g goes out once K has landed and the
+      // softmax has read S^T of chunk g - 2 (the buffer it reuses), without
+      // waiting for the P.V of chunk g - 1, whose V may land later; so the
+      // softmax finds each chunk's scores ready when it finishes the last.
+      // (With S^T issued only after the previous P.V, the softmax warps
+      // waited ~40 % of every chunk for it.)  A stream that makes no progress
+      // for the wait limit gives up.
+      bool ok = true;
+      unsigned long long t_last = global_ns();
+      while (ok && (more_v || more_s)) {
+        bool progress = false;
+        if (more_s && s_ready(false)) {
           issue_s();
+          progress = true;
+        }
+        if (more_v && g_v < g_s && pv_ready()) {
+          issue_pv();
+          progress = true;
+        }
+        if (progress) {
+          t_last = global_ns();
+        } else if (global_ns() - t_last > kWaitLimitNs || s_abort) {
+          ok = false;
+        } else {
+          __nanosleep(20);  // leave the sub-partition's issue slots to the softmax warps
         }
       }
       if (!ok) abort_all();
@@ -603,6 +619,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         // Keys no column sees get their V rows zeroed, once V has landed.
+        // A parity wait is exact only once the barrier's previous phase has
+        // completed.  With two or more stages the P^T wait above implies it
+        // (chunk g - NS's P.V has read its V); with one stage the previous
+        // phase is chunk g - 1's V, which the issuer may still be waiting
+        // for (S^T runs ahead of P.V), so wait for that P.V first.
+        if (NS == 1 && need_mask && g >= 1 &&
+            !softmax_all(mbar_wait_bounded(smem_u32(&pv_done[(g - 1) % PB]),
+                                           ((g - 1) / PB) & 1))) {
+          ok = false;
+          break;
+        }
         if (need_mask && !softmax_all(mbar_wait_bounded(smem_u32(&v_full[s]), (g / NS) & 1))) {
           ok = false;
           break;
