@@ -717,7 +717,11 @@ def decode_leg(args, name: str, dev, rank: int, world: int, local: int, steps: i
     value = total_kv / (step_ms * 1e-3) / 1e9
     peaks, peak_kind = measured_peaks()
     splits_per_seq = None
-    if plan["split_target"] > 0:  # partitioned on the device from the real lengths
+    if plan["stream_k"]:  # the balanced partition, made on the device
+        splits_per_seq = accounting.stream_k_splits(
+            b.context_lens.tolist(), wl.block_size, wl.num_kv_heads * plan["row_chunks"],
+            plan["split_target"], max_ctx, table.shape[1])
+    elif plan["split_target"] > 0:  # partitioned on the device from the real lengths
         splits_per_seq = accounting.device_split_counts(
             b.context_lens.tolist(), wl.block_size, wl.num_kv_heads * plan["row_chunks"],
             plan["split_target"], max_ctx, table.shape[1])
@@ -760,7 +764,7 @@ def decode_leg(args, name: str, dev, rank: int, world: int, local: int, steps: i
         "plan": {**{k: plan[k] for k in ("kernel", "rows_per_cta", "row_chunks", "split_blocks",
                                          "num_splits", "grid_x", "grid_y", "grid_z",
                                          "stages", "ctas_per_sm", "merge_kernel",
-                                         "split_target")},
+                                         "split_target", "stream_k")},
                  **({"splits_per_seq": splits_per_seq} if plan["split_target"] > 0 else {})},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(name),

@@ -128,10 +128,14 @@ typedef struct pkv_options {
   int persistent;   /* tcgen05 kernel: 0 planner, 1 one CTA per resident slot
                        walks the work items, 2 one CTA per item */
   int split_waves;  /* split-K partition from the batch's real lengths, read
-                       on the device (batch <= 32, CUDA-core and mma.sync
-                       kernels, split_blocks 0): k > 0 cuts the batch into at
-                       most k waves of resident CTAs; 0 or -1: the host plan
-                       (split length from max_context_len) */
+                       on the device (batch <= 32, split_blocks 0): k > 0
+                       cuts the batch into at most k waves of resident CTAs
+                       with splits of nearly equal length; -1: the host plan
+                       (split length from max_context_len); 0: the default,
+                       the host plan for the CUDA-core and mma.sync kernels
+                       and the balanced partition for the tcgen05 kernel
+                       (one CTA per SM, each taking an equal share of the
+                       batch's blocks; see pkv_plan.stream_k) */
 } pkv_options;
 
 /* What one attention call launches (see pkv_attention_plan). */
@@ -155,6 +159,13 @@ typedef struct pkv_plan {
                              real context lengths, into at most this many CTAs
                              (grid_x; split_blocks 0, num_splits an upper bound
                              per sequence); 0: the host partition above */
+  int stream_k;           /* 1 (with split_target = grid_x > 0): the balanced
+                             partition -- the (sequence, KV head) units of the
+                             batch laid end to end as one list of blocks, and
+                             CTA c of the grid_x taking the list's blocks
+                             floor(c T / grid_x) .. floor((c + 1) T / grid_x) - 1
+                             (T blocks in all), a split wherever its range meets
+                             a unit; 0: otherwise */
 } pkv_plan;
 
 /* Human-readable name of a status code (static string). */

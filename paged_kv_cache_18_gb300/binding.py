@@ -71,7 +71,8 @@ class Plan(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int),
                 ("smem_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
                 ("merge_kernel", ctypes.c_int), ("warp_tiles", ctypes.c_int),
-                ("blocks_per_iter", ctypes.c_int), ("split_target", ctypes.c_int)]
+                ("blocks_per_iter", ctypes.c_int), ("split_target", ctypes.c_int),
+                ("stream_k", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

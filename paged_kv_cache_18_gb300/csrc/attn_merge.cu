@@ -37,10 +37,11 @@ constexpr int kMergeWarps = 4;
 // two for the 512-wide latent rows of MLA (register budget).
 template <int D> __host__ __device__ constexpr int merge_unroll() { return D <= 256 ? 8 : 2; }
 
-// DEV: the partials of the device partition ([item][CTA column]); else the
-// host partition's [row][split].
-template <typename T, int D, bool DEV>
-__global__ void __launch_bounds__(kMergeWarps * 32, (D <= 128 ? (DEV ? 6 : 8) : 4))
+// LAYOUT 0: the host partition's partials, [row][split]; 1: the device
+// partition's, [item][CTA column]; 2: the balanced partition's,
+// [slot][CTA column] (sk_begin in pkv_device.cuh).
+template <typename T, int D, int LAYOUT>
+__global__ void __launch_bounds__(kMergeWarps * 32, (D <= 128 ? (LAYOUT ? 6 : 8) : 4))
     attn_merge_kernel(const AttnParams p) {
   constexpr int PER = D / 32;  // elements per lane: 2, 4, 8 or 16
   constexpr int kMergeUnroll = merge_unroll<D>();
@@ -56,12 +57,43 @@ __global__ void __launch_bounds__(kMergeWarps * 32, (D <= 128 ? (DEV ? 6 : 8) : 
   // part_o[(first + s * stride) * D ..].
   int ns, stride;
   int64_t first;
-  if constexpr (!DEV) {  // host partition: [row][split]
+  int sk_c0 = 0;           // balanced partition: the CTA of the row's first split
+  int64_t sk_total = 0;    //   and the list's length
+  if constexpr (LAYOUT == 0) {  // host partition: [row][split]
     const SeqExtent ext = seq_extent(p, b, false);
     ns = (ext.nblk + p.split_blocks - 1) / p.split_blocks;
     ns = ns < 1 ? 1 : (ns > p.num_splits ? p.num_splits : ns);
     first = row * p.num_splits;
     stride = 1;
+  } else if constexpr (LAYOUT == 2) {  // balanced partition: [slot][CTA column]
+    const int units = p.num_kv_heads * p.row_chunks;
+    const int h = static_cast<int>(row % p.num_heads);
+    const int j = static_cast<int>((row / p.num_heads) % p.num_queries);
+    const int kvh = h / p.group;
+    const int r = j * p.group + (h - kvh * p.group);
+    const int chunk = r / p.rows_per_cta;
+    const int u = kvh * p.row_chunks + chunk;
+    const int64_t s_b = p.split_info[2 * b], nb = p.split_info[2 * b + 1];
+    const int64_t total = p.split_info[2 * p.batch];
+    const int G = p.split_target;
+    ns = 0;
+    first = 0;
+    stride = p.rows_per_cta;
+    // (validated as for LAYOUT 1; a sequence without blocks gets zeros)
+    if (s_b < 0 || nb < 0 || total < 0 || s_b + nb * units > total) {
+      if (threadIdx.x == 0) record_error(p.err, PKV_DEVERR_CONTEXT_LEN);
+    } else if (nb > 0) {
+      // the unit's blocks s_u .. s_u + nb - 1 lie in CTAs c0 .. c1, its
+      // splits in slots c0 + U .. c1 + U (a CTA in between whose range is
+      // empty -- fewer blocks than CTAs -- wrote nothing and is skipped)
+      const int64_t s_u = s_b + static_cast<int64_t>(u) * nb;
+      const int c0 = sk_cta_of(total, G, s_u), c1 = sk_cta_of(total, G, s_u + nb - 1);
+      const int64_t U = static_cast<int64_t>(b) * units + u;
+      ns = c1 - c0 + 1;
+      first = (c0 + U) * p.rows_per_cta + (r - chunk * p.rows_per_cta);
+      sk_c0 = c0;
+      sk_total = total;
+    }
   } else {  // device partition: [item][CTA column], the items of (b, unit) consecutive
     ns = p.split_info[2 * b];
     int item0 = p.split_info[2 * b + 1];
@@ -102,8 +134,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32, (D <= 128 ? (DEV ? 6 : 8) : 
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
       const int s = s0 + u * kMergeWarps;
-      const bool ok = s < ns;
-      const int off = DEV ? s * stride : s;  // < splits x rows per CTA: fits an int
+      bool ok = s < ns;
+      if constexpr (LAYOUT == 2)
+        ok = ok && sk_begin(sk_total, p.split_target, sk_c0 + s) <
+                       sk_begin(sk_total, p.split_target, sk_c0 + s + 1);
+      const int off = LAYOUT ? s * stride : s;  // < splits x rows per CTA: fits an int
       ls[u] = ok ? lse[off] : -INFINITY;
 #pragma unroll
       for (int e = 0; e < PER; e += 2) {
@@ -163,16 +198,24 @@ cudaError_t merge_t(int D, const AttnParams &p, cudaStream_t stream) {
   if (nrows == 0) return cudaSuccess;
   if (nrows > 0x7fffffffLL) return cudaErrorInvalidValue;
   void (*kernel)(const AttnParams);
-  const bool dev = p.split_target > 0;
+  const int layout = p.split_target == 0 ? 0 : (p.stream_k ? 2 : 1);
+  void (*const k64[3])(const AttnParams) = {attn_merge_kernel<T, 64, 0>,
+                                            attn_merge_kernel<T, 64, 1>,
+                                            attn_merge_kernel<T, 64, 2>};
+  void (*const k128[3])(const AttnParams) = {attn_merge_kernel<T, 128, 0>,
+                                             attn_merge_kernel<T, 128, 1>,
+                                             attn_merge_kernel<T, 128, 2>};
+  void (*const k256[3])(const AttnParams) = {attn_merge_kernel<T, 256, 0>,
+                                             attn_merge_kernel<T, 256, 1>,
+                                             attn_merge_kernel<T, 256, 2>};
   switch (D) {
-    case 64: kernel = dev ? attn_merge_kernel<T, 64, true> : attn_merge_kernel<T, 64, false>; break;
-    case 128:
-      kernel = dev ? attn_merge_kernel<T, 128, true> : attn_merge_kernel<T, 128, false>;
+    case 64: kernel = k64[layout]; break;
+    case 128: kernel = k128[layout]; break;
+    case 256: kernel = k256[layout]; break;
+    case 512:  // MLA: host partition
+      if (layout != 0) return cudaErrorInvalidValue;
+      kernel = attn_merge_kernel<T, 512, 0>;
       break;
-    case 256:
-      kernel = dev ? attn_merge_kernel<T, 256, true> : attn_merge_kernel<T, 256, false>;
-      break;
-    case 512: kernel = attn_merge_kernel<T, 512, false>; break;  // MLA: host partition
     default: return cudaErrorInvalidValue;
   }
   // launched as a programmatic dependent of the attention kernel before it

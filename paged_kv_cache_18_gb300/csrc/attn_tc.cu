@@ -122,12 +122,38 @@ struct Item {
   bool valid;
 };
 struct DevSplits {
-  int ns[32], first[32], nb[32];
+  int ns[32], first[32], nb[32], L[32];
+  // balanced partition: first[b] = the flat block where sequence b's units
+  // start, nb[b] = n_b, L[b] its length; this CTA's blocks [lo, hi) span
+  // n_local units from unit u0 on
+  int u0, n_local;
+  long long lo, hi;
 };
 __device__ __forceinline__ Item decode_item(const AttnParams &p, int i, bool report,
                                             const DevSplits *dev) {
   Item it;
   it.idx = i;
+  if (p.stream_k) {
+    // item i: the part of this CTA's range in its i-th unit
+    const int units = p.num_kv_heads * p.row_chunks;
+    const int U = dev->u0 + i;
+    const int b = U / units, u = U - b * units;
+    it.b = b;
+    it.kvh = u / p.row_chunks;
+    it.chunk_row = u - it.kvh * p.row_chunks;
+    const int nb = dev->nb[b];
+    const long long s_u = static_cast<long long>(dev->first[b]) + static_cast<long long>(u) * nb;
+    const long long lo = max(dev->lo, s_u), hi = min(dev->hi, s_u + nb);
+    it.valid = hi > lo;
+    it.blk_begin = it.valid ? static_cast<int>(lo - s_u) : 0;
+    it.nspan = it.valid ? static_cast<int>(hi - lo) : 0;
+    it.n_chunks = (it.nspan + kChunkBlocks - 1) / kChunkBlocks;
+    it.L = dev->L[b];
+    it.split = 0;
+    it.ns_b = 0;
+    it.idx = static_cast<int>(blockIdx.x) + U;  // the split's slot
+    return it;
+  }
   if (p.split_target > 0) {
     const int units = p.num_kv_heads * p.row_chunks;
     int b = -1;
@@ -172,7 +198,56 @@ __device__ __forceinline__ Item decode_item(const AttnParams &p, int i, bool rep
   return it;
 }
 
-// Index of the partial of CTA column `col` (output row `row`) of item `it`.
+// Fused append (p.k_new set): fill the stage rows of the chunk's blocks in
+// `mixed` (bit j: block j holds some of the Q new rows of the sequence, at
+// positions L - Q .. L - 1) by hand: rows before L - Q from the cache, the
+// new rows from k_new (K producer) or v_new (V producer), zeros past L.  The
+// item of row chunk 0 also stores the new rows into the cache for the steps
+// that follow (its split is the only one holding those blocks).  The layout
+// is the copy's: row r of the chunk at r * 128 in the panel of its 64
+// dimensions, 16-byte piece q at (q ^ (r % 8)) * 16 (128-byte swizzle).
+// Warp-collective; `entry` is lane j's table entry for block j.
+template <typename T>
+__device__ __forceinline__ void fill_new_rows(const AttnParams &p, const Item &it, bool is_k,
+                                              uint32_t mixed, int entry, int key0c,
+                                              uint32_t stage, int panel_bytes) {
+  constexpr int VPR = 128 * sizeof(T) / 16;  // 16-byte pieces per row (16)
+  const int lane = threadIdx.x & 31;
+  const int first_new = it.L - p.num_queries;
+  const uint4 *cache = reinterpret_cast<const uint4 *>(is_k ? p.k_cache : p.v_cache);
+  uint4 *cache_w = reinterpret_cast<uint4 *>(const_cast<void *>(is_k ? p.k_cache : p.v_cache));
+  const uint4 *src = reinterpret_cast<const uint4 *>(is_k ? p.k_new : p.v_new);
+  const bool write_cache = it.chunk_row == 0;
+  for (uint32_t m = mixed; m != 0u; m &= m - 1u) {
+    const int j = __ffs(m) - 1;
+    const int64_t phys = __shfl_sync(kFull, entry, j);
+    const int64_t tile = (phys * p.num_kv_heads + it.kvh) * kBlockSize * VPR;
+#pragma unroll 2
+    for (int idx = lane; idx < kBlockSize * VPR; idx += 32) {
+      const int r = idx / VPR, vec = idx - r * VPR;
+      const int pos = key0c + j * kBlockSize + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (pos >= first_new && pos < it.L) {
+        const int64_t k =
+            (static_cast<int64_t>(it.b) * p.num_queries + (pos - first_new)) * p.num_kv_heads +
+            it.kvh;
+        v = __ldg(src + k * VPR + vec);
+        if (write_cache) cache_w[tile + r * VPR + vec] = v;
+      } else if (pos < first_new) {
+        v = __ldg(cache + tile + r * VPR + vec);
+      }
+      const int row = j * kBlockSize + r, part = vec >> 3, q = vec & 7;
+      st_shared_v4(stage + part * panel_bytes + row * 128 + ((q ^ (row & 7)) << 4), v.x, v.y,
+                   v.z, v.w);
+    }
+  }
+  // generic writes, read next by the tensor core (async proxy)
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
+// Index of the partial of CTA column `col` (output row `row`) of item `it`
+// (device partitions: slot it.idx, one partial per CTA column).
 __device__ __forceinline__ int64_t tc_partial(const AttnParams &p, const Item &it, int64_t row,
                                               int col) {
   return p.split_target == 0 ? row * p.num_splits + it.split
@@ -237,7 +312,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&mma_idle), 1);
     fence_mbar_init();
   }
-  if (p.split_target > 0 && warp == 0) {  // warp-collective; read by every role below
+  if (p.stream_k && warp == 0) {  // warp-collective; read by every role below
+    // The balanced partition: the flat list's offsets, this CTA's range and
+    // the units it meets.  CTA 0 reports bad lengths (once) and publishes the
+    // layout for the merge kernel.
+    const int units = p.num_kv_heads * p.row_chunks;
+    const SeqExtent ext = lane < p.batch ? seq_extent(p, lane, blockIdx.x == 0) : SeqExtent{0, 0};
+    int incl = ext.nblk * units;  // < 2^31 (checked by the host)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int s_b = incl - ext.nblk * units;
+    const int total = __shfl_sync(kFull, incl, 31);
+    dev.first[lane] = s_b;
+    dev.nb[lane] = ext.nblk;
+    dev.L[lane] = ext.L;
+    dev.ns[lane] = 0;
+    const long long lo = sk_begin(total, gridDim.x, blockIdx.x);
+    const long long hi = sk_begin(total, gridDim.x, blockIdx.x + 1);
+    // the unit holding flat block x (-1: none, never for 0 <= x < total)
+    auto unit_of = [&](long long x) -> int {
+      const unsigned m = __ballot_sync(
+          kFull, lane < p.batch && ext.nblk > 0 && x >= s_b &&
+                     x < s_b + static_cast<long long>(ext.nblk) * units);
+      const int b = m ? __ffs(m) - 1 : 0;
+      const int sb = __shfl_sync(kFull, s_b, b), nb = __shfl_sync(kFull, ext.nblk, b);
+      return m ? b * units + static_cast<int>((x - sb) / nb) : -1;
+    };
+    int u0 = 0, n = 0;
+    if (lo < hi) {
+      const int a = unit_of(lo), z = unit_of(hi - 1);
+      if (a >= 0 && z >= a) {
+        u0 = a;
+        n = z - a + 1;
+      }
+    }
+    if (lane == 0) {
+      dev.u0 = u0;
+      dev.n_local = n;
+      dev.lo = lo;
+      dev.hi = hi;
+    }
+    if (blockIdx.x == 0) {
+      if (lane < p.batch) {
+        p.split_info[2 * lane] = s_b;
+        p.split_info[2 * lane + 1] = ext.nblk;
+      }
+      if (lane == 0) p.split_info[2 * p.batch] = total;
+    }
+  } else if (p.split_target > 0 && warp == 0) {
     const SeqSplits sp = device_splits(p);
     dev.ns[lane] = sp.ns;
     dev.first[lane] = sp.first_item;
@@ -261,6 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   const uint32_t tmem = tmem_base_s;
   const uint32_t tmem_s[2] = {tmem, tmem + NC};
+  // This CTA's items: i = i0, i0 + di, ... below i_end (every role walks
+  // the same sequence).
+  const int i0 = p.stream_k ? 0 : G0, di = p.stream_k ? 1 : GS;
+  const int i_end = p.stream_k ? dev.n_local : num_items;
   const uint32_t tmem_o[2] = {tmem + 2 * NC, tmem + 4 * NC};
 
   auto abort_all = [&]() {
@@ -280,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring = sbase + (is_k ? 0 : G::kVOff);
     int g = 0, na = 0, issued = 0;
     bool ok = true;
-    for (int i = G0; i < num_items && ok; i += GS) {
+    for (int i = i0; i < i_end && ok; i += di) {
       const Item it = decode_item(p, i, false, &dev);
       if (!active(it)) continue;
       const int qb = na & 1;
@@ -328,21 +457,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool bad = lane < nb && (entry < 0 || static_cast<int64_t>(entry) >= p.num_blocks);
         const uint32_t bad_mask = __ballot_sync(kFull, bad);
         const uint32_t bar = smem_u32(&full[s]);
+        // Fused append: blocks holding new rows (positions L - Q .. L - 1)
+        // are filled by this warp instead of a copy -- older rows from the
+        // cache, new rows from k_new / v_new -- and the stage's barrier
+        // completes only after that (its one arrival comes last).
+        const int key0c = (it.blk_begin + c * kChunkBlocks) * kBlockSize;
+        const uint32_t mixed =
+            p.k_new == nullptr
+                ? 0u
+                : __ballot_sync(kFull, lane < nb && !bad &&
+                                           key0c + (lane + 1) * kBlockSize > it.L - p.num_queries);
         if (lane == 0) {
           if (is_k) {
             if (bad_mask) record_error(p.err, PKV_DEVERR_BLOCK_ID);
             stage_info[g % (NS + 2)].nb = nb;
             stage_info[g % (NS + 2)].bad_mask = bad_mask;
           }
-          mbar_arrive_expect_tx(bar, nb * 2 * 2048);
+          const uint32_t bytes = (nb - __popc(mixed)) * 2 * 2048;
+          if (mixed)
+            mbar_expect_tx(bar, bytes);
+          else
+            mbar_arrive_expect_tx(bar, bytes);
         }
         __syncwarp();
-        if (lane < nb) {
+        if (lane < nb && !((mixed >> lane) & 1u)) {
           const int phys = bad ? 0 : entry;
           const uint32_t st = ring + s * G::kTileBytes + lane * 2048;
 #pragma unroll
           for (int part = 0; part < 2; ++part)
             tma_load_4d(st + part * G::kPanelBytes, map, bar, part * 64, 0, it.kvh, phys);
+        }
+        if (mixed) {
+          fill_new_rows<T>(p, it, is_k, mixed, entry, key0c,
+                           ring + s * G::kTileBytes, G::kPanelBytes);
+          if (lane == 0) mbar_arrive(bar);
         }
         issued = g + 1;
       }
@@ -368,11 +516,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dp = smem_desc(0, 128, kChunkKeys * 16, kSwizzleNone);
       // Cursors over the flat chunk sequence, across item boundaries: S^T
       // runs ahead of P.V as far as its two buffers allow.
-      int i_s = G0, c_s = 0, na_s = 0, g_s = 0;   // next S^T: item, chunk, active index, flat
-      int i_v = G0, c_v = 0, na_v = 0, g_v = 0;   // next P.V
+      int i_s = i0, c_s = 0, na_s = 0, g_s = 0;   // next S^T: item, chunk, active index, flat
+      int i_v = i0, c_v = 0, na_v = 0, g_v = 0;   // next P.V
       Item it_s{}, it_v{};
       auto next_active = [&](int &i, Item &it) {
-        for (; i < num_items; i += GS) {
+        for (; i < i_end; i += di) {
           it = decode_item(p, i, false, &dev);
           if (active(it)) return true;
         }
@@ -408,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           commit(smem_u32(&qt_empty[qb]));
           c_s = 0;
           ++na_s;
-          i_s += GS;
+          i_s += di;
           more_s = next_active(i_s, it_s);
         }
       };
@@ -434,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++c_v == it_v.n_chunks) {
           c_v = 0;
           ++na_v;
-          i_v += GS;
+          i_v += di;
           more_v = next_active(i_v, it_v);
         }
       };
@@ -480,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m[NCW], l[NCW];
     int g = 0, na = 0;
     bool ok = true;
-    for (int i = G0; i < num_items && ok; i += GS) {
-      const Item it = decode_item(p, i, tid == 0, &dev);
+    for (int i = i0; i < i_end && ok; i += di) {
+      const Item it = decode_item(p, i, tid == 0 && !p.stream_k, &dev);
       if (!it.valid) continue;
       if (it.n_chunks == 0) {
         // an empty sequence: zero output rows (one split)

@@ -200,17 +200,20 @@ struct WorkspaceLayout {
   bool fused_merge;
 };
 WorkspaceLayout workspace_layout(const Shape &s, int num_splits, int row_chunks, int rows_per_cta,
-                                 int merge, int split_target = 0) {
+                                 int merge, int split_target = 0, int stream_k = 0) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rows = static_cast<size_t>(s.batch) * s.num_queries * s.num_heads;
   WorkspaceLayout w{};
   if (split_target > 0) {
-    // device partition: one partial per (work item, CTA column), merged by
-    // the merge kernel
-    const size_t parts = static_cast<size_t>(split_target) * rows_per_cta;
+    // device partitions: one partial per (work item, CTA column), merged by
+    // the merge kernel; the balanced partition's slots are its CTAs plus
+    // its units (a split in slot c + U)
+    const size_t slots = static_cast<size_t>(split_target) +
+                         (stream_k ? static_cast<size_t>(s.batch) * s.num_kv_heads * row_chunks : 0);
+    const size_t parts = slots * rows_per_cta;
     w.lse_off = up(parts * s.head_dim * sizeof(float));
-    w.ctr_off = w.lse_off + up(parts * sizeof(float));  // here: (ns_b, first item) per sequence
-    w.total = w.ctr_off + up(static_cast<size_t>(s.batch) * 2 * sizeof(int));
+    w.ctr_off = w.lse_off + up(parts * sizeof(float));  // here: the layout per sequence
+    w.total = w.ctr_off + up((static_cast<size_t>(s.batch) * 2 + 2) * sizeof(int));
     w.fused_merge = false;
     return w;
   }
@@ -283,13 +286,31 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
   // 65536 rows: one exact wave of 456 CTAs, 0.806 of the HBM peak, against
   // 0.842 for the host's 384; speculative verify 0.588 against 0.639), the
   // kernels being bound by the bytes in flight rather than by idle slots.
-  // The tcgen05 kernel (one CTA per SM, each taking whole items) takes the
-  // device partition by default, two waves of items of nearly equal length
-  // (verify: 0.527 of the HBM peak, against 0.483 for the host plan's
-  // 256-block items, which leave 1.7 waves, and 0.492 for one wave).
   int waves = opt ? opt->split_waves : 0;
-  if (persistent && waves == 0) waves = 2;
   const int64_t unit_rows = static_cast<int64_t>(s.num_kv_heads) * pl->row_chunks;
+  pl->stream_k = 0;
+  // The tcgen05 kernel (one CTA per SM) takes the balanced partition by
+  // default: every CTA the same number of blocks, whatever the lengths.  Any
+  // whole-item partition leaves SMs idle at the end: the verify step's two
+  // waves of items of 13 to 19 chunks measured 0.537 of the HBM peak, the
+  // host plan's 256-block items 0.512.
+  if (persistent && waves == 0 && !(opt && opt->split_blocks > 0) && s.batch <= 32 &&
+      max_blocks > 0 && units * max_blocks < (int64_t(1) << 31)) {  // int offsets on device
+    const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
+    pl->split_target = static_cast<int>(std::min<int64_t>(slots, 0x7fffffff));
+    pl->stream_k = 1;
+    pl->split_blocks = 0;
+    // a unit's splits: at most one per CTA, and each holds a block
+    pl->num_splits = static_cast<int>(std::min<int64_t>(slots, max_blocks));
+    pl->grid_x = pl->split_target;
+    pl->grid_y = pl->grid_z = 1;
+    pl->ctas_per_sm = ctas_per_sm;
+    const WorkspaceLayout w = workspace_layout(s, pl->num_splits, pl->row_chunks,
+                                               pl->rows_per_cta, 2, pl->split_target, 1);
+    pl->workspace_bytes = w.total;
+    pl->merge_kernel = 1;
+    return;
+  }
   if (waves > 0 && !(opt && opt->split_blocks > 0) && s.batch <= 32 && max_blocks > 0 &&
       static_cast<int64_t>(max_blocks) * s.batch < (int64_t(1) << 30)) {  // int sums on device
     const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
@@ -484,7 +505,6 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   int device = 0, sms = 0;
   st = device_plan(s, opt, &pl, &info, &device, &sms);
   if (st != PKV_OK) return st;
-  if (k_new && pl.kernel == PKV_KERNEL_TC) return PKV_ERR_UNSUPPORTED;
   if (pl.workspace_bytes > 0) {
     if (!workspace || !aligned(workspace, 16) || workspace_bytes < pl.workspace_bytes)
       return PKV_ERR_WORKSPACE;
@@ -517,6 +537,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   p.split_blocks = pl.split_blocks;
   p.num_splits = pl.num_splits;
   p.split_target = pl.split_target;
+  p.stream_k = pl.stream_k;
   p.scale_log2 =
       static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * k_scale);
   p.out_scale = v_scale;
@@ -525,7 +546,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
     const WorkspaceLayout w =
         workspace_layout(s, pl.num_splits, pl.row_chunks, pl.rows_per_cta,
                          pl.kernel == PKV_KERNEL_TC ? 2 : (opt ? opt->merge : 0),
-                         pl.split_target);
+                         pl.split_target, pl.stream_k);
     char *base = static_cast<char *>(workspace);
     p.part_o = reinterpret_cast<float *>(base);
     p.part_lse = reinterpret_cast<float *>(base + w.lse_off);

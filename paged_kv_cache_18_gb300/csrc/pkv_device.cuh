@@ -48,8 +48,11 @@ struct AttnParams {
   int split_blocks, num_splits;
   int split_target;             // > 0: split-K partition made on the device into at most
                                 //   this many work items (see cta_work); 0: host partition
-  int *split_info;              // device partition: [batch][2] = (ns_b, first item of b),
-                                //   written by the attention kernel for the merge kernel
+  int *split_info;              // device partition: [batch][2] = (ns_b, first item of b);
+                                //   balanced partition: (first flat block, n_b), then the
+                                //   total; written by the attention kernel for the merge
+  int stream_k;                 // with split_target = G > 0: the balanced partition
+                                //   (sk_begin below), G CTAs; else split_target items
   int tile_box;                 // the cache maps copy a whole (block, KV head) tile per box
                                 //   (5-D maps); 0: one 128-byte column panel per box (4-D)
   float scale_log2;             // softmax scale * log2(e) (* key scale of an FP8 cache)
@@ -171,6 +174,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Expect `bytes` more of copies in the current phase, without an arrival.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
@@ -427,6 +435,26 @@ __device__ __forceinline__ SeqSplits device_splits(const AttnParams &p) {
   }
   r.first_item = incl - r.ns * units;
   return r;
+}
+
+// Balanced partition (split_target = G > 0 with stream_k set; batch <= 32;
+// the tcgen05 kernel).  The units of the batch -- (sequence, KV head, row
+// chunk), every unit of sequence b holding n_b blocks -- are laid end to end
+// in one list of T = units * sum_b n_b blocks, sequence after sequence, and
+// CTA c of the G takes the list's blocks sk_begin(c) .. sk_begin(c + 1) - 1:
+// each CTA the same number of blocks to within one, however ragged the
+// lengths, so that no CTA waits at the end for a long item of another.  The
+// part of a CTA's range inside one unit U (U = its index in the list) is a
+// split of that unit; its partials go to slot c + U.  Slots are distinct
+// (a later unit in the list never meets an earlier CTA) and those of one
+// unit consecutive, so G + units slots hold them all and the merge finds a
+// unit's splits from its first and last block alone (skipping the CTAs whose
+// range is empty, which exist when T < G).
+__device__ __forceinline__ int64_t sk_begin(int64_t T, int G, int c) { return T * c / G; }
+// The CTA whose range holds flat block x (0 <= x < T): the largest c with
+// sk_begin(c) <= x.
+__device__ __forceinline__ int sk_cta_of(int64_t T, int G, int64_t x) {
+  return static_cast<int>(((x + 1) * G - 1) / T);
 }
 
 // The work of this CTA.

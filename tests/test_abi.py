@@ -151,7 +151,7 @@ def test_plan_invariants(B, Q, Hq, Hkv, D, ctx, dt, kernel):
         assert p["num_splits"] == max(1, T // U)
         parts = T * p["rows_per_cta"]
         assert p["workspace_bytes"] == (-(-parts * D * 4 // 256) * 256 + -(-parts * 4 // 256) * 256
-                                        + -(-B * 8 // 256) * 256)
+                                        + -(-(2 * B + 2) * 4 // 256) * 256)
         assert p["smem_bytes"] <= 227 * 1024
         return
     assert p["num_splits"] * p["split_blocks"] >= max_blocks
@@ -280,3 +280,81 @@ def test_mla_append_and_workspace_argument_errors(L):
     assert g(2, 8, 512, 64, 16, 100, 1, None, ctypes.byref(n)) == 2  # heads
     opt = binding.Options(2, 0, 0, 0, 0, 0, 0, 0)                   # a kernel choice
     assert g(2, 16, 512, 64, 16, 100, 1, ctypes.byref(opt), ctypes.byref(n)) == 2
+
+
+@pytest.mark.parametrize("B,Q,Hq,Hkv,ctx", [(16, 5, 32, 8, 8192), (1, 1, 32, 8, 100),
+                                            (32, 1, 32, 8, 4096), (3, 3, 36, 9, 65536)])
+def test_tc_plan_balanced_partition(B, Q, Hq, Hkv, ctx):
+    """The tcgen05 kernel's default plan: the balanced partition over one CTA
+    per SM, with slots for every CTA plus every unit (a split in slot c + U)."""
+    p = binding.plan_for(B, Q, Hq, Hkv, 128, ctx, torch.bfloat16, num_sms=152, kernel=3)
+    assert p["kernel"] == 3 and p["stream_k"] == 1 and p["ctas_per_sm"] == 1
+    G = 152
+    assert p["split_target"] == p["grid_x"] == G and (p["grid_y"], p["grid_z"]) == (1, 1)
+    assert p["split_blocks"] == 0 and p["merge_kernel"] == 1
+    assert p["num_splits"] == min(G, -(-ctx // 16))
+    slots = (G + B * Hkv * p["row_chunks"]) * p["rows_per_cta"]
+    assert p["workspace_bytes"] == (-(-slots * 128 * 4 // 256) * 256 + -(-slots * 4 // 256) * 256
+                                    + -(-(2 * B + 2) * 4 // 256) * 256)
+    # more than 32 sequences, or an explicit split length: the host plan
+    p = binding.plan_for(33, Q, Hq, Hkv, 128, ctx, torch.bfloat16, num_sms=152, kernel=3)
+    assert p["stream_k"] == 0 and p["split_target"] == 0
+    p = binding.plan_for(B, Q, Hq, Hkv, 128, ctx, torch.bfloat16, num_sms=152, kernel=3,
+                         split_blocks=64)
+    assert p["stream_k"] == 0 and p["split_blocks"] == min(64, -(-ctx // 16))
+    with tuning(split_waves=2):   # on request, the whole-item device partition
+        p = binding.plan_for(B, Q, Hq, Hkv, 128, ctx, torch.bfloat16, num_sms=152, kernel=3)
+    assert p["stream_k"] == 0 and p["split_target"] >= 2 * 152
+
+
+def _stream_k_pieces_brute(lens, units, ctas):
+    """(unit, CTA) pairs whose ranges meet, by walking every block."""
+    nb = [-(-L // 16) for L in lens]
+    T = units * sum(nb)
+    owner = []
+    for c in range(ctas):
+        owner += [c] * (T * (c + 1) // ctas - T * c // ctas)
+    assert len(owner) == T
+    pieces, x = [], 0
+    for b, n in enumerate(nb):
+        for u in range(units):
+            cs = sorted(set(owner[x:x + n]))
+            pieces.append((b * units + u, cs))
+            x += n
+    return pieces
+
+
+@pytest.mark.parametrize("lens,units,ctas", [([0, 1, 15, 16, 17, 300, 2000, 5000], 8, 152),
+                                             ([40, 40], 8, 152), ([700] * 32, 8, 152),
+                                             ([65536, 1, 32768], 9, 152), ([3, 5], 1, 7)])
+def test_stream_k_partition_mirror(lens, units, ctas):
+    """The balanced partition's arithmetic (the CTA of a block, the slot of a
+    split), checked against a block-by-block walk: each unit's splits are the
+    CTAs between those of its first and last block whose ranges are not
+    empty, the slots c + U are
+    distinct and fit in ctas + units, and the splits per unit the byte
+    accounting uses agree."""
+    from paged_kv_cache_18_gb300 import accounting
+    pieces = _stream_k_pieces_brute(lens, units, ctas)
+    T = units * sum(-(-L // 16) for L in lens)
+    seen = set()
+    for U, cs in pieces:
+        if not cs:
+            continue
+        # the CTAs between the first block's and the last's, less those whose
+        # range is empty (fewer blocks than CTAs)
+        assert cs == [c for c in range(cs[0], cs[-1] + 1) if T * (c + 1) // ctas > T * c // ctas]
+        for c in cs:
+            slot = c + U
+            assert slot not in seen and slot < ctas + units * len(lens)
+            seen.add(slot)
+    x = 0
+    for U, cs in pieces:
+        n = -(-lens[U // units] // 16)
+        if n:
+            assert cs[0] == ((x + 1) * ctas - 1) // T and cs[-1] == ((x + n) * ctas - 1) // T
+        x += n
+    got = accounting.stream_k_splits(lens, 16, units, ctas, max(lens), 10 ** 6)
+    for b in range(len(lens)):
+        want = sum(len(cs) for U, cs in pieces if U // units == b) / units
+        assert got[b] == want

@@ -869,3 +869,166 @@ def test_tc_device_partition(lens_i, Q, Hq, Hkv, waves, persistent):
         pl = pkv.plan(len(lens), Q, Hq, Hkv, 128, b_max, torch.bfloat16, kernel=3)
         assert pl["split_target"] > 0
         run_case(wl, kernel=3)
+
+
+# ---- balanced partition of the tcgen05 kernel (its default) ------------------
+STREAM_K_LENS = [
+    [0, 1, 15, 16, 17, 300, 2000, 5000],         # ragged, with an empty sequence
+    [700] * 32,                                  # the most sequences it takes
+    [40, 40],                                    # fewer blocks than CTAs
+    [65536, 1, 32768],                           # long contexts beside a tiny one
+    [8192, 512] * 8,                             # the verify shape's extremes
+]
+
+
+@pytest.mark.parametrize("lens_i", range(len(STREAM_K_LENS)))
+@pytest.mark.parametrize("Q,Hq,Hkv", [(1, 32, 8), (5, 32, 8), (3, 36, 9), (2, 32, 4)])
+@pytest.mark.parametrize("stages", [0, 1, 3])
+def test_tc_stream_k(lens_i, Q, Hq, Hkv, stages):
+    """Every CTA takes an equal share of the batch's (unit, block) list; a
+    unit is split wherever a CTA boundary falls in it and the merge finds its
+    splits from its first and last block.  Empty sequences (decode) give
+    zeros."""
+    import paged_kv_cache_18_gb300 as pkv
+    lens = STREAM_K_LENS[lens_i]
+    if Q > 1:
+        lens = [max(L, Q) for L in lens]
+    wl = W.Workload(f"tc stream-k {lens_i} Q{Q} {Hq}/{Hkv} st{stages}", len(lens), Hq, Hkv, 128,
+                    "bf16", context_lens=lens, num_queries=Q,
+                    seed=2100 + lens_i * 13 + Q + Hq + stages)
+    pl = pkv.plan(len(lens), Q, Hq, Hkv, 128, max(lens), torch.bfloat16, kernel=3,
+                  stages=stages)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert pl["stream_k"] == 1 and pl["split_target"] == pl["grid_x"] == sms * pl["ctas_per_sm"]
+    run_case(wl, kernel=3, stages=stages)
+
+
+def test_tc_stream_k_workspace_graph_and_errors():
+    """The balanced partition ignores what the workspace held, replays from a
+    graph, is deterministic, and records a context above max_context_len
+    (clamped) like the other partitions."""
+    import paged_kv_cache_18_gb300 as pkv
+    wl = W.Workload("tc stream-k ws", 16, 32, 8, 128, "bf16", len_range=(512, 8192),
+                    num_queries=5, seed=2200)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    ref = oracle_after_append(b)
+    pl = pkv.plan(wl.batch, 5, 32, 8, 128, b.max_context_len, torch.bfloat16, kernel=3)
+    assert pl["stream_k"] == 1
+    ws = torch.full((pl["workspace_bytes"],), 0xFF, dtype=torch.uint8, device="cuda")  # NaN floats
+    o = torch.empty_like(d.q)
+    d.attend(kernel=3, out=o, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    first = o.clone()
+    assert_close(host_f64(o, "bf16"), ref, "bf16", "stream-k, NaN-filled workspace")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d.attend(kernel=3, out=o, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d.attend(kernel=3, out=o, workspace=ws)
+    for _ in range(2):
+        o.zero_()
+        ws.fill_(0xFF)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, first)
+    # a length beyond max_context_len: clamped and recorded
+    wl2 = W.Workload("tc stream-k err", 3, 32, 8, 128, "bf16", context_lens=[3000, 50, 800],
+                     seed=2210)
+    b2 = W.make_batch(wl2)
+    d2 = DeviceBatch(b2)
+    d2.append()
+    d2.lens[1] = 5000
+    out = d2.attend(kernel=3)
+    torch.cuda.synchronize()
+    assert int(d2.err.item()) == 3
+    assert torch.isfinite(out.float()).all()
+
+
+def test_tc_stream_k_tree_masks():
+    """Tree verification (7-node tree over 4 query heads per KV head: 28 rows)
+    through the tcgen05 kernel's balanced partition."""
+    import oracle
+    import paged_kv_cache_18_gb300 as pkv
+    from tests.gpu_util import cache_bits
+    lens = [37, 4000, 900, 16, 12000, 9]
+    wl = W.Workload("tc stream-k tree", len(lens), 32, 8, 128, "bf16", context_lens=lens,
+                    seed=2220)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    masks = W.tree_mask_bits(W.medusa_parents((2, 2)))
+    q7 = torch.randn(wl.batch, len(masks), 32, 128, device="cuda").to(torch.bfloat16)
+    t = pkv.tree_verify_attention(q7, d.k_cache, d.v_cache, d.table, d.lens,
+                                  torch.from_numpy(masks.view(np.int64)).cuda(),
+                                  max_context_len=b.max_context_len, kernel=3,
+                                  error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    oracle_after_append(b)
+    q7h = q7.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.tree_attention(q7h, cache_bits(d.k_cache), cache_bits(d.v_cache),
+                                b.block_table, d.lens.cpu().numpy(), 1 / np.sqrt(128), "bf16",
+                                masks)
+    assert_close(host_f64(t, "bf16"), ref, "bf16", "tc stream-k tree")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("Q,Hq,Hkv", [(1, 8, 2), (1, 4, 4), (5, 32, 8), (3, 8, 1), (8, 32, 8),
+                                     (16, 8, 4), (2, 32, 8)])
+@pytest.mark.parametrize("split_blocks", [0, 1, 3, 9])
+def test_tc_fused_append_attention(dtype, Q, Hq, Hkv, split_blocks):
+    """The tcgen05 kernel's fused append: the producers fill the blocks that
+    hold new rows themselves (older rows from the cache, new rows from k_new /
+    v_new) and row chunk 0 writes the new rows into the cache, bit for bit;
+    with the balanced partition (split_blocks 0) and the host's."""
+    import paged_kv_cache_18_gb300 as pkv
+    lens = [max(1, Q - 1), Q, Q + 1, 16, 17, 31, 33, 100, 250, 129, 4000]
+    D = 128
+    wl = W.Workload(f"tc fused {dtype} Q{Q} {Hq}/{Hkv} sb{split_blocks}", len(lens), Hq, Hkv, D,
+                    dtype, context_lens=lens, num_queries=Q,
+                    seed=2300 + Q + Hq + split_blocks)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    B = wl.batch
+    kn = d.k_new.view(B, Q, Hkv, D)
+    vn = d.v_new.view(B, Q, Hkv, D)
+    q = d.q if Q > 1 else d.q[:, 0]
+    out = pkv.append_attention(q, kn, vn, d.k_cache, d.v_cache, d.table, d.lens,
+                               scale=wl.softmax_scale, max_context_len=b.max_context_len,
+                               kernel=3, split_blocks=split_blocks, error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    ref = oracle_after_append(b)
+    for cache, host in ((d.k_cache, b.k_cache), (d.v_cache, b.v_cache)):
+        bits = cache_bits(cache)
+        np.testing.assert_array_equal(bits, host.view(bits.dtype))
+    got = host_f64(out if Q > 1 else out[:, None], dtype)
+    assert_close(got, ref, dtype, wl.name)
+
+
+def test_tc_fused_matches_two_calls_bitwise():
+    """The tcgen05 kernel: the fused launch and append-then-attend give
+    bit-identical outputs and caches (the same plan, the same arithmetic)."""
+    import paged_kv_cache_18_gb300 as pkv
+    wl = W.Workload("tc fused bitwise", 16, 32, 8, 128, "bf16", len_range=(20, 8192), seed=2350)
+    for Q in (1, 5):
+        wl.num_queries = Q
+        b = W.make_batch(wl)
+        d1, d2 = DeviceBatch(b), DeviceBatch(b)
+        d1.append()
+        o1 = d1.attend(kernel=3)
+        kn = d2.k_new.view(wl.batch, Q, 8, 128)
+        vn = d2.v_new.view(wl.batch, Q, 8, 128)
+        o2 = pkv.append_attention(d2.q if Q > 1 else d2.q[:, 0], kn, vn, d2.k_cache,
+                                  d2.v_cache, d2.table, d2.lens,
+                                  max_context_len=b.max_context_len, kernel=3)
+        o2 = o2 if Q > 1 else o2[:, None]
+        assert torch.equal(o1, o2)
+        for a, c in ((d1.k_cache, d2.k_cache), (d1.v_cache, d2.v_cache)):
+            assert torch.equal(a.view(torch.int16), c.view(torch.int16))
