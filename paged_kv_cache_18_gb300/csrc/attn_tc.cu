@@ -78,20 +78,22 @@ __device__ __forceinline__ void softmax_sync() {
 }
 
 // ---- geometry ----------------------------------------------------------------
-// Two rings of NS stages, one for K and one for V: a stage is one chunk's K
-// (or V) tile, two 64-dim panels of 128 rows x 128 B (block j of the chunk
-// at rows 16 j .. 16 j + 15).  K is free again as soon as S^T is computed,
-// V only after P.V, so the K ring runs ahead.
-template <int D, int NC, int NS, int PB> struct TcGeom {
+// Two rings, NS stages for K and NV for V: a stage is one chunk's K (or V)
+// tile, two 64-dim panels of 128 rows x 128 B (block j of the chunk at rows
+// 16 j .. 16 j + 15).  K is free again as soon as S^T is computed, V only
+// after P.V, so V's ring is the one that bounds the copies in flight.
+template <int D, int NC, int NS, int NV, int PB> struct TcGeom {
   static_assert(D == 128, "head_dim 128");
   static constexpr int kPanelBytes = kChunkKeys * 128;      // 16 KB
   static constexpr int kTileBytes = 2 * kPanelBytes;        // 32 KB: one stage
   static constexpr int kVOff = NS * kTileBytes;             // the V ring
   static constexpr int kQtPanelBytes = NC * 128;            // Q^T: NC rows per panel
-  static constexpr int kQtOff = 2 * NS * kTileBytes;        // two Q^T buffers of 2 panels
+  static constexpr int kQtOff = (NS + NV) * kTileBytes;     // two Q^T buffers of 2 panels
   static constexpr int kPOff = kQtOff + 4 * kQtPanelBytes;  // P^T buffers: (high, low) x PB
   static constexpr int kPBytes = kChunkKeys * NC * 2;
-  static constexpr int kBytes = kPOff + PB * 2 * kPBytes;
+  // an item's partial outputs, [column][head dim] fp32, for one bulk store
+  static constexpr int kStgOff = kPOff + PB * 2 * kPBytes;
+  static constexpr int kBytes = kStgOff + NC * D * 4;
   // S^T (two buffers of NC) and two O^T buffers (items alternate) of 2 NC
   // (NC columns for the high part of P, NC for the remainder, summed at
   // the end)
@@ -107,8 +109,8 @@ struct StageInfo {
 
 // --------------------------------------------------------------------------------
 //
-// NS chunk stages; PB = 1 or 2 P^T buffers (with one, chunk c's softmax
-// writes P^T only after chunk c - 1's P.V has read it).
+// NS K stages and NV V stages; PB = 1 or 2 P^T buffers (with one, chunk c's
+// softmax writes P^T only after chunk c - 1's P.V has read it).
 // A work item: one split of one (sequence, KV head, row chunk).  Items are
 // numbered split-fastest; the persistent CTA g takes items g, g + G, ...,
 // every role enumerating the same sequence.
@@ -254,11 +256,11 @@ __device__ __forceinline__ int64_t tc_partial(const AttnParams &p, const Item &i
                              : static_cast<int64_t>(it.idx) * p.rows_per_cta + col;
 }
 
-template <typename T, int D, int NC, int NS, int PB>
+template <typename T, int D, int NC, int NS, int NV, int PB>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const AttnParams p, int num_items) {
-  using G = TcGeom<D, NC, NS, PB>;
+  using G = TcGeom<D, NC, NS, NV, PB>;
   constexpr int NCW = NC / 2;  // query columns of one softmax warp
   pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for this grid
   extern __shared__ uint8_t smem_raw[];
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // One barrier per buffer wherever a producer may run two phases ahead of
   // a waiter otherwise (P^T is double-buffered: the softmax can write chunk
   // g + 1's P^T before the issuer has waited for chunk g's).
-  __shared__ uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], s_free[2],
+  __shared__ uint64_t k_full[NS], k_empty[NS], v_full[NV], v_empty[NV], s_full[2], s_free[2],
       p_full[PB], pv_done[PB], qt_full[2], qt_empty[2], o_free[2], mma_idle;
   // Chunk facts from the K producer, a ring of NS + 2: the slot of chunk g
   // is rewritten (for chunk g + NS + 2) only after a K stage reuse that
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ StageInfo stage_info[NS + 2];
   __shared__ uint32_t tmem_base_s;
   __shared__ __align__(16) float red[4][NC];
+  __shared__ float lse_stg[NC];  // an item's log-sum-exps (device partitions)
   __shared__ volatile int s_abort;
   __shared__ DevSplits dev;  // the device partition's per-sequence layout
 
@@ -295,6 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
       mbar_init(smem_u32(&k_empty[s]), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
@@ -407,53 +412,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *empty = is_k ? k_empty : v_empty;
     const CUtensorMap *map = is_k ? &kmap : &vmap;
     const uint32_t ring = sbase + (is_k ? 0 : G::kVOff);
+    const int NR = is_k ? NS : NV;  // this ring's stages
     int g = 0, na = 0, issued = 0;
     bool ok = true;
-    for (int i = i0; i < i_end && ok; i += di) {
-      const Item it = decode_item(p, i, false, &dev);
-      if (!active(it)) continue;
-      const int qb = na & 1;
-      if (is_k) {
-        // Q^T of the item: query columns as rows of the K-major swizzled
-        // operand (padding columns zero), once the Q^T buffer is free.
-        bool w = na < 2 || mbar_wait_bounded(smem_u32(&qt_empty[qb]), ((na >> 1) - 1) & 1);
-        if (!__all_sync(kFull, w && !s_abort)) {
-          ok = false;
-          break;
-        }
-        // (all of the lane's loads in flight first, then the stores)
-        const uint32_t qt = sbase + G::kQtOff + qb * 2 * G::kQtPanelBytes;
-        constexpr int kPer = NC * (D / 8) / 32;  // 16-byte pieces per lane
-        uint4 v[kPer];
+    // The producers read one step ahead of their copies, so that no global
+    // load sits between a stage becoming free and its copy: the table
+    // entries of the next chunk (the next item's first, at an item's last
+    // chunk) and, for K, the next item's query rows (in registers until its
+    // Q^T buffer is free, stored after that item's first K copy is issued).
+    constexpr int kPer = NC * (D / 8) / 32;  // 16-byte query pieces per lane
+    uint4 qv[kPer];
+    auto load_q = [&](const Item &x) {
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int e = lane + 32 * k, col = e / (D / 8), q = e - col * (D / 8);
-          const int64_t row = cta_row_index(p, it.b, it.kvh, it.chunk_row, col);
-          v[k] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(
-                                reinterpret_cast<const T *>(p.q) + row * D + q * 8))
-                          : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int e = lane + 32 * k, col = e / (D / 8), q = e - col * (D / 8);
-          st_shared_v4(qt + (q >> 3) * G::kQtPanelBytes + col * 128 + (((q & 7) ^ (col & 7)) << 4),
-                       v[k].x, v[k].y, v[k].z, v[k].w);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&qt_full[qb]));
+      for (int k = 0; k < kPer; ++k) {
+        const int e = lane + 32 * k, col = e / (D / 8), q = e - col * (D / 8);
+        const int64_t row = cta_row_index(p, x.b, x.kvh, x.chunk_row, col);
+        qv[k] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(
+                               reinterpret_cast<const T *>(p.q) + row * D + q * 8))
+                         : make_uint4(0u, 0u, 0u, 0u);
       }
-      const int32_t *table = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks_per_seq;
+    };
+    auto entries = [&](const Item &x, int c) -> int {
+      const int nb = min(kChunkBlocks, x.nspan - c * kChunkBlocks);
+      return lane < nb ? ld_keep(p.block_table + static_cast<int64_t>(x.b) * p.max_blocks_per_seq +
+                                 x.blk_begin + c * kChunkBlocks + lane)
+                       : 0;
+    };
+    auto next_item = [&](int &ii, Item &out) -> bool {
+      for (; ii < i_end; ii += di) {
+        out = decode_item(p, ii, false, &dev);
+        if (active(out)) {
+          ii += di;
+          return true;
+        }
+      }
+      return false;
+    };
+    int i = i0;
+    Item it{};
+    bool have = next_item(i, it);
+    int entry_nx = have ? entries(it, 0) : 0;
+    if (have && is_k) load_q(it);
+    while (have && ok) {
+      const int qb = na & 1;
+      Item nx{};
+      bool have_nx = false, looked = false;
       for (int c = 0; c < it.n_chunks; ++c, ++g) {
-        const int s = g % NS;
+        const int s = g % NR;
+        const int entry = entry_nx;
+        if (c + 1 < it.n_chunks) {
+          entry_nx = entries(it, c + 1);
+        } else {
+          have_nx = next_item(i, nx);
+          looked = true;
+          entry_nx = have_nx ? entries(nx, 0) : 0;
+        }
         bool w = !s_abort;
-        if (w && g >= NS) w = mbar_wait_bounded(smem_u32(&empty[s]), ((g / NS) - 1) & 1);
+        if (w && g >= NR) w = mbar_wait_bounded(smem_u32(&empty[s]), ((g / NR) - 1) & 1);
         if (!__all_sync(kFull, w)) {
           ok = false;
           break;
         }
         const int nb = min(kChunkBlocks, it.nspan - c * kChunkBlocks);
-        const int entry = lane < nb ? __ldg(table + it.blk_begin + c * kChunkBlocks + lane) : 0;
         const bool bad = lane < nb && (entry < 0 || static_cast<int64_t>(entry) >= p.num_blocks);
         const uint32_t bad_mask = __ballot_sync(kFull, bad);
         const uint32_t bar = smem_u32(&full[s]);
@@ -493,15 +513,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar);
         }
         issued = g + 1;
+        if (is_k && c == 0) {
+          // Q^T of the item: query columns as rows of the K-major swizzled
+          // operand (padding columns zero), once the Q^T buffer is free.
+          const bool wq =
+              na < 2 || mbar_wait_bounded(smem_u32(&qt_empty[qb]), ((na >> 1) - 1) & 1);
+          if (!__all_sync(kFull, wq && !s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t qt = sbase + G::kQtOff + qb * 2 * G::kQtPanelBytes;
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int e = lane + 32 * k, col = e / (D / 8), q = e - col * (D / 8);
+            st_shared_v4(qt + (q >> 3) * G::kQtPanelBytes + col * 128 +
+                             (((q & 7) ^ (col & 7)) << 4),
+                         qv[k].x, qv[k].y, qv[k].z, qv[k].w);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&qt_full[qb]));
+        }
+        if (is_k && looked && have_nx) load_q(nx);  // the next item's rows, in flight
       }
+      if (!looked) have_nx = next_item(i, nx);  // (only after a break: ok is false)
+      it = nx;
+      have = have_nx;
       ++na;
     }
     if (!ok && lane == 0) abort_all();
     // Copies issued but perhaps never consumed (an aborted CTA): give them a
     // bounded chance to land before the CTA exits.
     if (lane == 0 && s_abort)
-      for (int c = max(0, issued - NS); c < issued; ++c)
-        mbar_wait_bounded(smem_u32(&full[c % NS]), (c / NS) & 1);
+      for (int c = max(0, issued - NR); c < issued; ++c)
+        mbar_wait_bounded(smem_u32(&full[c % NR]), (c / NR) & 1);
   } else if (warp == kIssuerWarp) {
     // ---- MMA issuer --------------------------------------------------------------
     if (lane == 0) {
@@ -565,18 +610,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto pv_ready = [&]() -> bool {
         const int ob = na_v & 1;
         return mbar_test(smem_u32(&p_full[g_v % PB]), (g_v / PB) & 1) &&
-               mbar_test(smem_u32(&v_full[g_v % NS]), (g_v / NS) & 1) &&
+               mbar_test(smem_u32(&v_full[g_v % NV]), (g_v / NV) & 1) &&
                (c_v > 0 || na_v < 2 || mbar_test(smem_u32(&o_free[ob]), ((na_v >> 1) - 1) & 1));
       };
       auto issue_pv = [&]() {
         const int ob = na_v & 1;
         fence_after();
-        const uint64_t va = dv | ((sbase + G::kVOff + (g_v % NS) * G::kTileBytes) >> 4);
+        const uint64_t va = dv | ((sbase + G::kVOff + (g_v % NV) * G::kTileBytes) >> 4);
         const uint64_t pa = dp | ((sbase + G::kPOff + (g_v % PB) * 2 * G::kPBytes) >> 4);
 #pragma unroll
         for (int j = 0; j < kChunkKeys / 16; ++j)
           mma(tmem_o[ob], va + ((j * 2048) >> 4), pa + ((j * 256) >> 4), id_pv, c_v > 0 || j > 0);
-        commit(smem_u32(&v_empty[g_v % NS]));
+        commit(smem_u32(&v_empty[g_v % NV]));
         commit(smem_u32(&pv_done[g_v % PB]));
         ++g_v;
         if (++c_v == it_v.n_chunks) {
@@ -654,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l[j] = 0.f;
       }
       for (int c = 0; c < it.n_chunks; ++c, ++g) {
-        const int s = g % NS, sb = g & 1;
+        const int s = g % NV, sb = g & 1;  // s: the chunk's V stage
         if (!softmax_all(mbar_wait_bounded(smem_u32(&s_full[sb]), (g >> 1) & 1) && !s_abort)) {
           ok = false;
           break;
@@ -768,17 +813,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Keys no column sees get their V rows zeroed, once V has landed.
         // A parity wait is exact only once the barrier's previous phase has
-        // completed.  With two or more stages the P^T wait above implies it
-        // (chunk g - NS's P.V has read its V); with one stage the previous
-        // phase is chunk g - 1's V, which the issuer may still be waiting
-        // for (S^T runs ahead of P.V), so wait for that P.V first.
-        if (NS == 1 && need_mask && g >= 1 &&
+        // completed: chunk g - NV's V.  With NV >= PB the P^T wait above
+        // implies it (chunk g - PB's P.V has read its V and every earlier
+        // one); with fewer V stages than P^T buffers the issuer may still be
+        // waiting for chunk g - 1's V (S^T runs ahead of P.V), so wait for
+        // that P.V first.
+        if (NV < PB && need_mask && g >= 1 &&
             !softmax_all(mbar_wait_bounded(smem_u32(&pv_done[(g - 1) % PB]),
                                            ((g - 1) / PB) & 1))) {
           ok = false;
           break;
         }
-        if (need_mask && !softmax_all(mbar_wait_bounded(smem_u32(&v_full[s]), (g / NS) & 1))) {
+        if (need_mask && !softmax_all(mbar_wait_bounded(smem_u32(&v_full[s]), (g / NV) & 1))) {
           ok = false;
           break;
         }
@@ -829,6 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
         if (lane == 0) red[quad][col0 + j] = v;
       }
+      if (p.split_target > 0 && tid == 0) bulk_wait_read();  // the staging buffer is free
       softmax_sync();
       // Every shared-memory read first (vectorised), then only stores: the
       // tensor core and the copies keep shared memory busy, and a read
@@ -850,42 +897,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         lsum[j + 2] = a.z;
         lsum[j + 3] = a.w;
       }
-      // Output rows of the columns, walked without divisions: column col is
-      // query row r = chunk_row * rows_per_cta + col, query r / G, head
-      // kvh * G + r % G.
-      const int r0 = it.chunk_row * p.rows_per_cta + col0;
-      int jq = r0 / p.group, hh = r0 - jq * p.group;
-      float lse_mine = -INFINITY;  // column col0 + lane's log-sum-exp (lanes < NCW)
-      int64_t row_mine = -1;
+      if (p.split_target > 0) {
+        // Device partitions: the item's columns are consecutive partials
+        // ([slot][column]).  They are staged in shared memory and one bulk
+        // copy takes them out while the warps go on with the next item; the
+        // warps' own global stores would queue behind the copies that keep
+        // HBM busy.  (Padding columns are staged too but not copied.)
+        float lse_mine = -INFINITY;  // column col0 + lane's log-sum-exp (lanes < NCW)
 #pragma unroll
-      for (int j = 0; j < NCW; ++j) {
-        const int col = col0 + j;
-        const bool real = col < p.rows_per_cta && r0 + j < p.rows;
-        const int64_t row =
-            (static_cast<int64_t>(it.b) * p.num_queries + jq) * p.num_heads + it.kvh * p.group + hh;
-        if (++hh == p.group) {
-          hh = 0;
-          ++jq;
+        for (int j = 0; j < NCW; ++j) {
+          const float inv = lsum[j] > 0.f ? __fdividef(1.f, lsum[j]) : 0.f;
+          st_shared_f32(sbase + G::kStgOff + ((col0 + j) * D + kl) * 4, (o_hi[j] + o_lo[j]) * inv);
+          if (lane == j) lse_mine = lsum[j] > 0.f ? m[j] + __log2f(lsum[j]) : -INFINITY;
         }
-        if (!real) continue;
-        const float inv = lsum[j] > 0.f ? __fdividef(1.f, lsum[j]) : 0.f;
-        const float o = o_hi[j] + o_lo[j];
-        if (p.num_splits == 1 && p.split_target == 0) {
-          reinterpret_cast<T *>(p.out)[row * D + kl] = from_float<T>(o * inv * p.out_scale);
-        } else {
-          const int64_t pi = tc_partial(p, it, row, col);
-          __stcg(p.part_o + pi * D + kl, o * inv);
-          if (lane == j) {
-            lse_mine = lsum[j] > 0.f ? m[j] + __log2f(lsum[j]) : -INFINITY;
-            row_mine = pi;
+        if (quad == 0 && lane < NCW) lse_stg[col0 + lane] = lse_mine;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        softmax_sync();  // (red[] and the staging are reused by the next item)
+        const int n = min(p.rows_per_cta, p.rows - it.chunk_row * p.rows_per_cta);
+        const int64_t slot0 = static_cast<int64_t>(it.idx) * p.rows_per_cta;
+        if (tid == 0) {  // read back by bulk_wait_read at the next epilogue
+          bulk_s2g(p.part_o + slot0 * D, sbase + G::kStgOff, static_cast<uint32_t>(n) * D * 4);
+          bulk_commit();
+        }
+        if (warp == 0 && lane < n) __stcg(p.part_lse + slot0 + lane, lse_stg[lane]);
+      } else {
+        // Output rows of the columns, walked without divisions: column col is
+        // query row r = chunk_row * rows_per_cta + col, query r / G, head
+        // kvh * G + r % G.
+        const int r0 = it.chunk_row * p.rows_per_cta + col0;
+        int jq = r0 / p.group, hh = r0 - jq * p.group;
+        float lse_mine = -INFINITY;  // column col0 + lane's log-sum-exp (lanes < NCW)
+        int64_t row_mine = -1;
+#pragma unroll
+        for (int j = 0; j < NCW; ++j) {
+          const int col = col0 + j;
+          const bool real = col < p.rows_per_cta && r0 + j < p.rows;
+          const int64_t row = (static_cast<int64_t>(it.b) * p.num_queries + jq) * p.num_heads +
+                              it.kvh * p.group + hh;
+          if (++hh == p.group) {
+            hh = 0;
+            ++jq;
+          }
+          if (!real) continue;
+          const float inv = lsum[j] > 0.f ? __fdividef(1.f, lsum[j]) : 0.f;
+          const float o = o_hi[j] + o_lo[j];
+          if (p.num_splits == 1) {
+            reinterpret_cast<T *>(p.out)[row * D + kl] = from_float<T>(o * inv * p.out_scale);
+          } else {
+            const int64_t pi = tc_partial(p, it, row, col);
+            __stcg(p.part_o + pi * D + kl, o * inv);
+            if (lane == j) {
+              lse_mine = lsum[j] > 0.f ? m[j] + __log2f(lsum[j]) : -INFINITY;
+              row_mine = pi;
+            }
           }
         }
+        if (quad == 0 && row_mine >= 0) __stcg(p.part_lse + row_mine, lse_mine);
+        softmax_sync();  // red[] is reused by the next item
       }
-      if (quad == 0 && row_mine >= 0) __stcg(p.part_lse + row_mine, lse_mine);
-      softmax_sync();  // red[] is reused by the next item
       ++na;
     }
     if (!ok && tid == 0) abort_all();
+    if (tid == 0) bulk_wait_all();  // the partials are written before the CTA exits
   }
 
   fence_before();
@@ -902,33 +975,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace pkv {
 namespace tc {
 
-// Rings: 1, 2 or 3 stages of 32 KB each for K and for V (bf16/fp16,
-// head_dim 128), with two P^T buffers (one with three stages, for shared
-// memory).
-template <int NS> constexpr int p_buffers() { return NS >= 3 ? 1 : 2; }
+// Rings of 32 KB stages (bf16/fp16, head_dim 128).  `stages` names the V
+// ring's depth; the K ring takes min(stages, 2) (K is released as soon as
+// S^T is computed, so two stages keep its copies ahead), and two P^T
+// buffers fit beside them in shared memory.
+template <int NV> constexpr int k_stages() { return NV < 2 ? NV : 2; }
+template <int NV> constexpr int p_buffers() { return 2; }
 constexpr int kDefaultStages = 2;
 
-template <typename T, int NC, int NS>
+template <typename T, int NC, int NV>
 KernelInfo info_t() {
   KernelInfo k;
-  k.func = reinterpret_cast<const void *>(&attn_tc_kernel<T, 128, NC, NS, p_buffers<NS>()>);
+  k.func = reinterpret_cast<const void *>(
+      &attn_tc_kernel<T, 128, NC, k_stages<NV>(), NV, p_buffers<NV>()>);
   k.threads = kThreads;
   k.warps = kThreads / 32;
-  k.stages = NS;
-  k.smem = static_cast<size_t>(TcGeom<128, NC, NS, p_buffers<NS>()>::kBytes) + 1024;
+  k.stages = NV;
+  k.smem = static_cast<size_t>(TcGeom<128, NC, k_stages<NV>(), NV, p_buffers<NV>()>::kBytes) +
+           1024;
   k.warp_tiles = NC / 8;
   return k;
 }
 
-template <typename T, int NC, int NS>
+template <typename T, int NC, int NV>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
-  const KernelInfo k = info_t<T, NC, NS>();
+  const KernelInfo k = info_t<T, NC, NV>();
   // persistent: grid.x CTAs walk the grid.y x grid.z x splits items (or the
   // device partition's split_target items)
   const int items = p.split_target > 0 ? p.split_target
                                        : p.num_splits * p.num_kv_heads * p.row_chunks * p.batch;
-  attn_tc_kernel<T, 128, NC, NS, p_buffers<NS>()>
+  attn_tc_kernel<T, 128, NC, k_stages<NV>(), NV, p_buffers<NV>()>
       <<<dim3(grid.x), k.threads, k.smem, stream>>>(km, vm, p, items);
   return cudaGetLastError();
 }

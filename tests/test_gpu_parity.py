@@ -669,15 +669,9 @@ def test_tc_refuses_what_it_does_not_build():
     # more than 32 rows per KV head: split over row chunks of <= 32
     p = pkv.plan(2, 9, 32, 8, 128, 100, torch.bfloat16, kernel=3)
     assert p["rows_per_cta"] <= 32 and p["row_chunks"] == 2
-    # the fused append stays on the other kernels
-    wl = W.Workload("tc fused", 2, 32, 8, 128, "bf16", context_lens=[20, 40], num_queries=5,
-                    seed=1670)
-    b = W.make_batch(wl)
-    d = DeviceBatch(b)
+    # FP8 caches stay on the other kernels
     with pytest.raises(pkv.PkvError):
-        pkv.append_attention(d.q, d.k_new.view(2, 5, 8, 128), d.v_new.view(2, 5, 8, 128),
-                             d.k_cache, d.v_cache, d.table, d.lens,
-                             max_context_len=b.max_context_len, kernel=3)
+        pkv.plan(2, 1, 8, 8, 128, 100, "fp8", kernel=3)
 
 
 @pytest.mark.parametrize("stages", [1, 2, 3])
@@ -980,13 +974,14 @@ def test_tc_stream_k_tree_masks():
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("Q,Hq,Hkv", [(1, 8, 2), (1, 4, 4), (5, 32, 8), (3, 8, 1), (8, 32, 8),
-                                     (16, 8, 4), (2, 32, 8)])
+                                     (16, 8, 4), (2, 32, 8), (9, 32, 8)])
 @pytest.mark.parametrize("split_blocks", [0, 1, 3, 9])
 def test_tc_fused_append_attention(dtype, Q, Hq, Hkv, split_blocks):
     """The tcgen05 kernel's fused append: the producers fill the blocks that
     hold new rows themselves (older rows from the cache, new rows from k_new /
-    v_new) and row chunk 0 writes the new rows into the cache, bit for bit;
-    with the balanced partition (split_blocks 0) and the host's."""
+    v_new) and row chunk 0 writes the new rows into the cache, bit for bit
+    (36 rows per KV head: two row chunks reading the same blocks); with the
+    balanced partition (split_blocks 0) and the host's."""
     import paged_kv_cache_18_gb300 as pkv
     lens = [max(1, Q - 1), Q, Q + 1, 16, 17, 31, 33, 100, 250, 129, 4000]
     D = 128
