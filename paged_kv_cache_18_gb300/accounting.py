@@ -84,30 +84,36 @@ def device_split_counts(context_lens: Sequence[int], block_size: int, units: int
     return [max(1, -(-n // lo)) for n in nb]
 
 
+STREAM_K_WEIGHT = 24  # the balanced partition's per-unit weight, in blocks (as the library's)
+
+
 def stream_k_splits(context_lens: Sequence[int], block_size: int, units: int, ctas: int,
-                    max_context_len: int, max_blocks_per_seq: int) -> list:
+                    max_context_len: int, max_blocks_per_seq: int,
+                    weight: int = STREAM_K_WEIGHT) -> list:
     """Splits per unit, averaged over each sequence's units, of the balanced
     partition (pkv_plan.stream_k = 1, ctas = grid_x): the units laid end to end
-    as one list of T blocks, CTA c taking blocks floor(c T / ctas) ..
-    floor((c + 1) T / ctas) - 1, and a unit split wherever a CTA boundary
-    falls inside it (with fewer blocks than CTAs some CTAs take none).  For
-    the byte accounting of the partials; the kernel
-    computes the partition itself."""
+    as one list, a unit with n blocks taking weight + n places (the weight
+    first, then its blocks), CTA c taking places floor(c T / ctas) ..
+    floor((c + 1) T / ctas) - 1 of T, and a unit split wherever a CTA
+    boundary falls among its blocks (with fewer places than CTAs some CTAs
+    take none).  For the byte accounting of the partials; the kernel computes
+    the partition itself."""
     nb = []
     for L in context_lens:
         L = min(max(0, int(L)), max_context_len)
         nb.append(min(-(-L // block_size), max_blocks_per_seq))
-    total = units * sum(nb)
+    total = units * sum(n + weight for n in nb if n > 0)
     cta_of = lambda x: ((x + 1) * ctas - 1) // total  # noqa: E731
     begin = lambda c: total * c // ctas  # noqa: E731
     out, start = [], 0
     for n in nb:
         pieces = 0
+        vlen = n + weight if n > 0 else 0
         for u in range(units):
             if n > 0:  # the CTAs from the first block's to the last's, empty ranges aside
-                s = start + u * n
+                s = start + u * vlen + weight
                 pieces += sum(1 for c in range(cta_of(s), cta_of(s + n - 1) + 1)
                               if begin(c + 1) > begin(c))
         out.append(pieces / units)
-        start += units * n
+        start += units * vlen
     return out

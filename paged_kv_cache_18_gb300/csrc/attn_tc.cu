@@ -144,7 +144,9 @@ __device__ __forceinline__ Item decode_item(const AttnParams &p, int i, bool rep
     it.kvh = u / p.row_chunks;
     it.chunk_row = u - it.kvh * p.row_chunks;
     const int nb = dev->nb[b];
-    const long long s_u = static_cast<long long>(dev->first[b]) + static_cast<long long>(u) * nb;
+    // the unit's blocks: places s_u .. s_u + nb - 1 of the list
+    const long long s_u = static_cast<long long>(dev->first[b]) +
+                          static_cast<long long>(u) * (nb + p.sk_weight) + p.sk_weight;
     const long long lo = max(dev->lo, s_u), hi = min(dev->hi, s_u + nb);
     it.valid = hi > lo;
     it.blk_begin = it.valid ? static_cast<int>(lo - s_u) : 0;
@@ -317,19 +319,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&mma_idle), 1);
     fence_mbar_init();
   }
+  // Everything above overlaps the previous kernel in the stream; its writes
+  // (the cache rows of an append, the previous call's merge reading the
+  // workspace this kernel rewrites) are complete and visible after this.
+  pdl_wait();
   if (p.stream_k && warp == 0) {  // warp-collective; read by every role below
     // The balanced partition: the flat list's offsets, this CTA's range and
     // the units it meets.  CTA 0 reports bad lengths (once) and publishes the
     // layout for the merge kernel.
     const int units = p.num_kv_heads * p.row_chunks;
     const SeqExtent ext = lane < p.batch ? seq_extent(p, lane, blockIdx.x == 0) : SeqExtent{0, 0};
-    int incl = ext.nblk * units;  // < 2^31 (checked by the host)
+    const int vlen = ext.nblk > 0 ? ext.nblk + p.sk_weight : 0;  // places of each unit of b
+    int incl = vlen * units;  // < 2^31 (checked by the host)
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int t = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += t;
     }
-    const int s_b = incl - ext.nblk * units;
+    const int s_b = incl - vlen * units;
     const int total = __shfl_sync(kFull, incl, 31);
     dev.first[lane] = s_b;
     dev.nb[lane] = ext.nblk;
@@ -337,14 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev.ns[lane] = 0;
     const long long lo = sk_begin(total, gridDim.x, blockIdx.x);
     const long long hi = sk_begin(total, gridDim.x, blockIdx.x + 1);
-    // the unit holding flat block x (-1: none, never for 0 <= x < total)
+    // the unit holding place x (-1: none, never for 0 <= x < total)
     auto unit_of = [&](long long x) -> int {
       const unsigned m = __ballot_sync(
-          kFull, lane < p.batch && ext.nblk > 0 && x >= s_b &&
-                     x < s_b + static_cast<long long>(ext.nblk) * units);
+          kFull, lane < p.batch && vlen > 0 && x >= s_b &&
+                     x < s_b + static_cast<long long>(vlen) * units);
       const int b = m ? __ffs(m) - 1 : 0;
-      const int sb = __shfl_sync(kFull, s_b, b), nb = __shfl_sync(kFull, ext.nblk, b);
-      return m ? b * units + static_cast<int>((x - sb) / nb) : -1;
+      const int sb = __shfl_sync(kFull, s_b, b), vl = __shfl_sync(kFull, vlen, b);
+      return m ? b * units + static_cast<int>((x - sb) / vl) : -1;
     };
     int u0 = 0, n = 0;
     if (lo < hi) {
@@ -1005,9 +1012,10 @@ cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnPar
   // device partition's split_target items)
   const int items = p.split_target > 0 ? p.split_target
                                        : p.num_splits * p.num_kv_heads * p.row_chunks * p.batch;
-  attn_tc_kernel<T, 128, NC, k_stages<NV>(), NV, p_buffers<NV>()>
-      <<<dim3(grid.x), k.threads, k.smem, stream>>>(km, vm, p, items);
-  return cudaGetLastError();
+  // a programmatic dependent of the kernel before it (it waits for that
+  // kernel before touching global memory)
+  return launch_kernel(true, attn_tc_kernel<T, 128, NC, k_stages<NV>(), NV, p_buffers<NV>()>,
+                       dim3(grid.x), k.threads, k.smem, stream, km, vm, p, items);
 }
 
 using Launch = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const AttnParams &, dim3,

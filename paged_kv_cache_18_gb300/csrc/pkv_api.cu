@@ -29,6 +29,11 @@ constexpr int kTargetWaves = 3;         // CTAs ~ this many times the resident s
                                         // (the 20-row verify tile: 0.641 of the HBM
                                         // peak at 4 waves, 0.673 at 3)
 constexpr int kMaxSplits = 32;          // per sequence: each split adds merge work
+// The balanced partition's weight of a unit, in blocks: what starting and
+// finishing a piece of work costs the tcgen05 kernel (its query rows, the
+// first chunk's scores, the epilogue: ~5 us against ~0.2 us a block on the
+// verify step).
+constexpr int kStreamKWeight = 24;
 constexpr size_t kUsableSmemPerSm = 228 * 1024;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -295,7 +300,8 @@ void plan_splits(const Shape &s, const pkv_options *opt, int num_sms, int ctas_p
   // waves of items of 13 to 19 chunks measured 0.537 of the HBM peak, the
   // host plan's 256-block items 0.512.
   if (persistent && waves == 0 && !(opt && opt->split_blocks > 0) && s.batch <= 32 &&
-      max_blocks > 0 && units * max_blocks < (int64_t(1) << 31)) {  // int offsets on device
+      max_blocks > 0 &&
+      units * (max_blocks + kStreamKWeight) < (int64_t(1) << 31)) {  // int offsets on device
     const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
     pl->split_target = static_cast<int>(std::min<int64_t>(slots, 0x7fffffff));
     pl->stream_k = 1;
@@ -538,6 +544,7 @@ pkv_status run_attention(void *out, const void *q, const void *k_cache, const vo
   p.num_splits = pl.num_splits;
   p.split_target = pl.split_target;
   p.stream_k = pl.stream_k;
+  p.sk_weight = pl.stream_k ? kStreamKWeight : 0;
   p.scale_log2 =
       static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * k_scale);
   p.out_scale = v_scale;

@@ -53,6 +53,7 @@ struct AttnParams {
                                 //   total; written by the attention kernel for the merge
   int stream_k;                 // with split_target = G > 0: the balanced partition
                                 //   (sk_begin below), G CTAs; else split_target items
+  int sk_weight;                //   its per-unit weight W, in blocks (sk_begin below)
   int tile_box;                 // the cache maps copy a whole (block, KV head) tile per box
                                 //   (5-D maps); 0: one 128-byte column panel per box (4-D)
   float scale_log2;             // softmax scale * log2(e) (* key scale of an FP8 cache)
@@ -440,16 +441,19 @@ __device__ __forceinline__ SeqSplits device_splits(const AttnParams &p) {
 // Balanced partition (split_target = G > 0 with stream_k set; batch <= 32;
 // the tcgen05 kernel).  The units of the batch -- (sequence, KV head, row
 // chunk), every unit of sequence b holding n_b blocks -- are laid end to end
-// in one list of T = units * sum_b n_b blocks, sequence after sequence, and
-// CTA c of the G takes the list's blocks sk_begin(c) .. sk_begin(c + 1) - 1:
-// each CTA the same number of blocks to within one, however ragged the
-// lengths, so that no CTA waits at the end for a long item of another.  The
-// part of a CTA's range inside one unit U (U = its index in the list) is a
-// split of that unit; its partials go to slot c + U.  Slots are distinct
-// (a later unit in the list never meets an earlier CTA) and those of one
-// unit consecutive, so G + units slots hold them all and the merge finds a
-// unit's splits from its first and last block alone (skipping the CTAs whose
-// range is empty, which exist when T < G).
+// in one list, sequence after sequence; a unit with blocks takes W + n_b
+// places in it (W = sk_weight: the fixed cost of starting and finishing a
+// piece of work, counted in blocks, then its n_b blocks), a unit without
+// none.  CTA c of the G takes the list's places sk_begin(c) ..
+// sk_begin(c + 1) - 1 of T: each CTA the same amount of work to within one
+// block, however ragged the lengths, so that no CTA waits at the end for a
+// long item of another.  The blocks of a CTA's range inside one unit U (U =
+// its index in the list) are a split of that unit; its partials go to slot
+// c + U.  Slots are distinct (a later unit in the list never meets an earlier
+// CTA) and those of one unit consecutive, so G + units slots hold them all
+// and the merge finds a unit's splits from its first and last block alone
+// (skipping the CTAs whose range is empty, which exist when T < G: a CTA
+// strictly between those two has all its places among the unit's blocks).
 __device__ __forceinline__ int64_t sk_begin(int64_t T, int G, int c) { return T * c / G; }
 // The CTA whose range holds flat block x (0 <= x < T): the largest c with
 // sk_begin(c) <= x.

@@ -307,10 +307,12 @@ def test_tc_plan_balanced_partition(B, Q, Hq, Hkv, ctx):
     assert p["stream_k"] == 0 and p["split_target"] >= 2 * 152
 
 
-def _stream_k_pieces_brute(lens, units, ctas):
-    """(unit, CTA) pairs whose ranges meet, by walking every block."""
+def _stream_k_pieces_brute(lens, units, ctas, weight):
+    """(unit, CTAs whose ranges hold some of its blocks), by walking every
+    place of the list: a unit with n blocks is `weight` places of no block,
+    then its n blocks."""
     nb = [-(-L // 16) for L in lens]
-    T = units * sum(nb)
+    T = units * sum(n + weight for n in nb if n > 0)
     owner = []
     for c in range(ctas):
         owner += [c] * (T * (c + 1) // ctas - T * c // ctas)
@@ -318,43 +320,41 @@ def _stream_k_pieces_brute(lens, units, ctas):
     pieces, x = [], 0
     for b, n in enumerate(nb):
         for u in range(units):
-            cs = sorted(set(owner[x:x + n]))
-            pieces.append((b * units + u, cs))
-            x += n
-    return pieces
+            if n == 0:
+                pieces.append((b * units + u, [], x))
+                continue
+            cs = sorted(set(owner[x + weight:x + weight + n]))
+            pieces.append((b * units + u, cs, x + weight))
+            x += n + weight
+    return pieces, T
 
 
+@pytest.mark.parametrize("weight", [0, 24])
 @pytest.mark.parametrize("lens,units,ctas", [([0, 1, 15, 16, 17, 300, 2000, 5000], 8, 152),
                                              ([40, 40], 8, 152), ([700] * 32, 8, 152),
                                              ([65536, 1, 32768], 9, 152), ([3, 5], 1, 7)])
-def test_stream_k_partition_mirror(lens, units, ctas):
-    """The balanced partition's arithmetic (the CTA of a block, the slot of a
-    split), checked against a block-by-block walk: each unit's splits are the
+def test_stream_k_partition_mirror(lens, units, ctas, weight):
+    """The balanced partition's arithmetic (the CTA of a place, the slot of a
+    split), checked against a place-by-place walk: each unit's splits are the
     CTAs between those of its first and last block whose ranges are not
-    empty, the slots c + U are
-    distinct and fit in ctas + units, and the splits per unit the byte
-    accounting uses agree."""
+    empty, the slots c + U are distinct and fit in ctas + units, and the
+    splits per unit the byte accounting uses agree."""
     from paged_kv_cache_18_gb300 import accounting
-    pieces = _stream_k_pieces_brute(lens, units, ctas)
-    T = units * sum(-(-L // 16) for L in lens)
+    pieces, T = _stream_k_pieces_brute(lens, units, ctas, weight)
     seen = set()
-    for U, cs in pieces:
+    for U, cs, first in pieces:
         if not cs:
             continue
         # the CTAs between the first block's and the last's, less those whose
-        # range is empty (fewer blocks than CTAs)
+        # range is empty (fewer places than CTAs)
         assert cs == [c for c in range(cs[0], cs[-1] + 1) if T * (c + 1) // ctas > T * c // ctas]
+        n = -(-lens[U // units] // 16)
+        assert cs[0] == ((first + 1) * ctas - 1) // T and cs[-1] == ((first + n) * ctas - 1) // T
         for c in cs:
             slot = c + U
             assert slot not in seen and slot < ctas + units * len(lens)
             seen.add(slot)
-    x = 0
-    for U, cs in pieces:
-        n = -(-lens[U // units] // 16)
-        if n:
-            assert cs[0] == ((x + 1) * ctas - 1) // T and cs[-1] == ((x + n) * ctas - 1) // T
-        x += n
-    got = accounting.stream_k_splits(lens, 16, units, ctas, max(lens), 10 ** 6)
+    got = accounting.stream_k_splits(lens, 16, units, ctas, max(lens), 10 ** 6, weight=weight)
     for b in range(len(lens)):
-        want = sum(len(cs) for U, cs in pieces if U // units == b) / units
+        want = sum(len(cs) for U, cs, _ in pieces if U // units == b) / units
         assert got[b] == want

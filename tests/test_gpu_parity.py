@@ -1027,3 +1027,21 @@ def test_tc_fused_matches_two_calls_bitwise():
         assert torch.equal(o1, o2)
         for a, c in ((d1.k_cache, d2.k_cache), (d1.v_cache, d2.v_cache)):
             assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_merge_rows_kernel_many_splits():
+    """The warp-per-row merge (from 1024 output rows, device partitions) over
+    rows with more than 32 splits: the log-sum-exps are taken 32 at a time."""
+    import paged_kv_cache_18_gb300 as pkv
+    from paged_kv_cache_18_gb300 import accounting
+    lens = [16384, 12000]
+    Q, Hq, Hkv = 16, 32, 8
+    wl = W.Workload("merge rows", len(lens), Hq, Hkv, 128, "bf16", context_lens=lens,
+                    num_queries=Q, seed=2400)
+    assert wl.batch * Q * Hq >= 1024
+    with tuning(split_waves=16):
+        pl = pkv.plan(wl.batch, Q, Hq, Hkv, 128, max(lens), torch.bfloat16, kernel=2)
+        ns = accounting.device_split_counts(lens, 16, Hkv * pl["row_chunks"], pl["split_target"],
+                                            max(lens), -(-max(lens) // 16))
+        assert max(ns) > 32
+        run_case(wl, kernel=2)
