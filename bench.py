@@ -63,6 +63,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 L2_FLUSH_BYTES = 256 << 20          # twice the 129 MB L2
 WARMUP_S = 0.25                     # least GPU time of warm-up steps before a timed region
+WARMUP_EXACT = False                # --warmup-exact: exactly --warmup steps (ncu launch lists)
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 # Sources whose change invalidates a recorded ncu traffic figure.
 KERNEL_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mma.cuh",
@@ -589,7 +590,8 @@ def decode_leg(args, name: str, dev, rank: int, world: int, local: int, steps: i
     # state when the timed region starts (after the host-side set-up the GPU
     # has idled for seconds; 5 steps of 0.2 ms do not wake it fully).
     warm_run, t_w = 0, time.perf_counter()
-    while warm_run < warmup or time.perf_counter() - t_w < WARMUP_S:
+    warm_s = 0.0 if WARMUP_EXACT else WARMUP_S
+    while warm_run < warmup or time.perf_counter() - t_w < warm_s:
         attend(q, k_new, v_new, slots, table, lens)
         warm_run += 1
         if warm_run >= warmup:
@@ -1109,6 +1111,10 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--warmup-exact", action="store_true",
+                    help="run exactly --warmup warm-up steps, without extending them to "
+                         f"{WARMUP_S} s of GPU work (for ncu launch lists, whose per-launch "
+                         "times are not bench values)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(W.WORKLOADS) + list(W.TREE_WORKLOADS)
                     + list(W.PREFILL_WORKLOADS) + list(W.MLA_WORKLOADS),
@@ -1140,6 +1146,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    global WARMUP_EXACT
+    WARMUP_EXACT = args.warmup_exact
     if args.workload in W.PREFILL_WORKLOADS:
         return run_reference_prefill(args) if args.impl == "reference" else run_prefill(args)
     if args.workload in W.MLA_WORKLOADS:
