@@ -4,10 +4,10 @@
 // Same arithmetic as attn_mma.cuh ("Inference part 1", sections "PagedAttention",
 // "FlashAttention" and "FlashDecoding"), organised for tcgen05: one thread
 // issues asynchronous 128-row MMAs over eight cache blocks at a time, and the
-// softmax runs on values read from TMEM.  It serves tiles of 9 to 32 query rows
-// (NC = 16 or 32 columns): the verification tile of K+1 drafts x the query
-// heads of one KV head, where the mma.sync kernel spends its time repeating a
-// per-block chain once per 8-column tile.
+// softmax runs on values read from TMEM.  It serves tiles of up to 64 query
+// rows (NC = 16, 32 or 64 columns): the verification tile of K+1 drafts (or a
+// tree's nodes) x the query heads of one KV head, where the mma.sync kernel
+// spends its time repeating a per-block chain once per 8-column tile.
 //
 // One CTA per (split, KV head x row chunk, sequence), 320 threads:
 //   warps 0-7  softmax and epilogue; warp w reads TMEM lanes 32 (w % 4) ..
@@ -82,14 +82,14 @@ __device__ __forceinline__ void softmax_sync() {
 // tile, two 64-dim panels of 128 rows x 128 B (block j of the chunk at rows
 // 16 j .. 16 j + 15).  K is free again as soon as S^T is computed, V only
 // after P.V, so V's ring is the one that bounds the copies in flight.
-template <int D, int NC, int NS, int NV, int PB> struct TcGeom {
+template <int D, int NC, int NS, int NV, int PB, int QB> struct TcGeom {
   static_assert(D == 128, "head_dim 128");
   static constexpr int kPanelBytes = kChunkKeys * 128;      // 16 KB
   static constexpr int kTileBytes = 2 * kPanelBytes;        // 32 KB: one stage
   static constexpr int kVOff = NS * kTileBytes;             // the V ring
   static constexpr int kQtPanelBytes = NC * 128;            // Q^T: NC rows per panel
-  static constexpr int kQtOff = (NS + NV) * kTileBytes;     // two Q^T buffers of 2 panels
-  static constexpr int kPOff = kQtOff + 4 * kQtPanelBytes;  // P^T buffers: (high, low) x PB
+  static constexpr int kQtOff = (NS + NV) * kTileBytes;     // QB Q^T buffers of 2 panels
+  static constexpr int kPOff = kQtOff + QB * 2 * kQtPanelBytes;  // P^T: (high, low) x PB
   static constexpr int kPBytes = kChunkKeys * NC * 2;
   // an item's partial outputs, [column][head dim] fp32, for one bulk store
   static constexpr int kStgOff = kPOff + PB * 2 * kPBytes;
@@ -97,7 +97,7 @@ template <int D, int NC, int NS, int NV, int PB> struct TcGeom {
   // S^T (two buffers of NC) and two O^T buffers (items alternate) of 2 NC
   // (NC columns for the high part of P, NC for the remainder, summed at
   // the end)
-  static constexpr int kTmemCols = 6 * NC <= 128 ? 128 : 256;
+  static constexpr int kTmemCols = 6 * NC <= 128 ? 128 : (6 * NC <= 256 ? 256 : 512);
 };
 
 // Per-stage facts the producer hands to the consumers (published before its
@@ -110,7 +110,9 @@ struct StageInfo {
 // --------------------------------------------------------------------------------
 //
 // NS K stages and NV V stages; PB = 1 or 2 P^T buffers (with one, chunk c's
-// softmax writes P^T only after chunk c - 1's P.V has read it).
+// softmax writes P^T only after chunk c - 1's P.V has read it); QB = 1 or 2
+// Q^T buffers (with one, an item's Q^T is stored once the last S^T of the
+// item before has been computed).
 // A work item: one split of one (sequence, KV head, row chunk).  Items are
 // numbered split-fastest; the persistent CTA g takes items g, g + G, ...,
 // every role enumerating the same sequence.
@@ -258,11 +260,11 @@ __device__ __forceinline__ int64_t tc_partial(const AttnParams &p, const Item &i
                              : static_cast<int64_t>(it.idx) * p.rows_per_cta + col;
 }
 
-template <typename T, int D, int NC, int NS, int NV, int PB>
+template <typename T, int D, int NC, int NS, int NV, int PB, int QB>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const AttnParams p, int num_items) {
-  using G = TcGeom<D, NC, NS, NV, PB>;
+  using G = TcGeom<D, NC, NS, NV, PB, QB>;
   constexpr int NCW = NC / 2;  // query columns of one softmax warp
   pdl_launch_dependents();  // the merge kernel may be scheduled now; it waits for this grid
   extern __shared__ uint8_t smem_raw[];
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a waiter otherwise (P^T is double-buffered: the softmax can write chunk
   // g + 1's P^T before the issuer has waited for chunk g's).
   __shared__ uint64_t k_full[NS], k_empty[NS], v_full[NV], v_empty[NV], s_full[2], s_free[2],
-      p_full[PB], pv_done[PB], qt_full[2], qt_empty[2], o_free[2], mma_idle;
+      p_full[PB], pv_done[PB], qt_full[QB], qt_empty[QB], o_free[2], mma_idle;
   // Chunk facts from the K producer, a ring of NS + 2: the slot of chunk g
   // is rewritten (for chunk g + NS + 2) only after a K stage reuse that
   // waits on the softmax having released S^T of chunk g, read after them.
@@ -308,9 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), kSoftmaxWarps);
+      mbar_init(smem_u32(&o_free[i]), kSoftmaxWarps);
+    }
+    for (int i = 0; i < QB; ++i) {
       mbar_init(smem_u32(&qt_full[i]), 1);
       mbar_init(smem_u32(&qt_empty[i]), 1);
-      mbar_init(smem_u32(&o_free[i]), kSoftmaxWarps);
     }
     for (int i = 0; i < PB; ++i) {
       mbar_init(smem_u32(&p_full[i]), kSoftmaxWarps);
@@ -461,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int entry_nx = have ? entries(it, 0) : 0;
     if (have && is_k) load_q(it);
     while (have && ok) {
-      const int qb = na & 1;
+      const int qb = na % QB;
       Item nx{};
       bool have_nx = false, looked = false;
       for (int c = 0; c < it.n_chunks; ++c, ++g) {
@@ -524,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Q^T of the item: query columns as rows of the K-major swizzled
           // operand (padding columns zero), once the Q^T buffer is free.
           const bool wq =
-              na < 2 || mbar_wait_bounded(smem_u32(&qt_empty[qb]), ((na >> 1) - 1) & 1);
+              na < QB || mbar_wait_bounded(smem_u32(&qt_empty[qb]), ((na / QB) - 1) & 1);
           if (!__all_sync(kFull, wq && !s_abort)) {
             ok = false;
             break;
@@ -580,10 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool more_s = next_active(i_s, it_s), more_v = next_active(i_v, it_v);
       auto s_ready = [&](bool block) -> bool {
-        const int s = g_s % NS, sb = g_s & 1, qb = na_s & 1;
+        const int s = g_s % NS, sb = g_s & 1, qb = na_s % QB;
         const uint32_t kf = smem_u32(&k_full[s]), sf = smem_u32(&s_free[sb]);
         const uint32_t qf = smem_u32(&qt_full[qb]);
-        const uint32_t pk = (g_s / NS) & 1, ps = ((g_s >> 1) - 1) & 1, pq = (na_s >> 1) & 1;
+        const uint32_t pk = (g_s / NS) & 1, ps = ((g_s >> 1) - 1) & 1, pq = (na_s / QB) & 1;
         if (block)
           return (c_s > 0 || mbar_wait_bounded(qf, pq)) && mbar_wait_bounded(kf, pk) &&
                  (g_s < 2 || mbar_wait_bounded(sf, ps));
@@ -591,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                (g_s < 2 || mbar_test(sf, ps));
       };
       auto issue_s = [&]() {
-        const int s = g_s % NS, sb = g_s & 1, qb = na_s & 1;
+        const int s = g_s % NS, sb = g_s & 1, qb = na_s % QB;
         fence_after();
         const uint64_t ka = dk | ((sbase + s * G::kTileBytes) >> 4);
         const uint64_t qa = dk | ((sbase + G::kQtOff + qb * 2 * G::kQtPanelBytes) >> 4);
@@ -926,7 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_s2g(p.part_o + slot0 * D, sbase + G::kStgOff, static_cast<uint32_t>(n) * D * 4);
           bulk_commit();
         }
-        if (warp == 0 && lane < n) __stcg(p.part_lse + slot0 + lane, lse_stg[lane]);
+        if (warp == 0)  // (up to 64 columns)
+          for (int c = lane; c < n; c += 32) __stcg(p.part_lse + slot0 + c, lse_stg[c]);
       } else {
         // Output rows of the columns, walked without divisions: column col is
         // query row r = chunk_row * rows_per_cta + col, query r / G, head
@@ -984,22 +989,26 @@ namespace tc {
 
 // Rings of 32 KB stages (bf16/fp16, head_dim 128).  `stages` names the V
 // ring's depth; the K ring takes min(stages, 2) (K is released as soon as
-// S^T is computed, so two stages keep its copies ahead), and two P^T
-// buffers fit beside them in shared memory.
-template <int NV> constexpr int k_stages() { return NV < 2 ? NV : 2; }
-template <int NV> constexpr int p_buffers() { return 2; }
+// S^T is computed, so two stages keep its copies ahead).  Up to 32 columns,
+// two P^T and two Q^T buffers fit beside them in shared memory; the 64-column
+// tile (up to 64 query rows, a 10-node tree over four heads) takes one of
+// each (and at most two V stages).
+template <int NC, int NV> struct TcConfig {
+  static constexpr int NS = NV < 2 ? NV : 2;
+  static constexpr int PB = NC > 32 ? 1 : 2;
+  static constexpr int QB = NC > 32 ? 1 : 2;
+};
 constexpr int kDefaultStages = 2;
 
 template <typename T, int NC, int NV>
 KernelInfo info_t() {
+  using C = TcConfig<NC, NV>;
   KernelInfo k;
-  k.func = reinterpret_cast<const void *>(
-      &attn_tc_kernel<T, 128, NC, k_stages<NV>(), NV, p_buffers<NV>()>);
+  k.func = reinterpret_cast<const void *>(&attn_tc_kernel<T, 128, NC, C::NS, NV, C::PB, C::QB>);
   k.threads = kThreads;
   k.warps = kThreads / 32;
   k.stages = NV;
-  k.smem = static_cast<size_t>(TcGeom<128, NC, k_stages<NV>(), NV, p_buffers<NV>()>::kBytes) +
-           1024;
+  k.smem = static_cast<size_t>(TcGeom<128, NC, C::NS, NV, C::PB, C::QB>::kBytes) + 1024;
   k.warp_tiles = NC / 8;
   return k;
 }
@@ -1007,6 +1016,7 @@ KernelInfo info_t() {
 template <typename T, int NC, int NV>
 cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnParams &p, dim3 grid,
                      cudaStream_t stream) {
+  using C = TcConfig<NC, NV>;
   const KernelInfo k = info_t<T, NC, NV>();
   // persistent: grid.x CTAs walk the grid.y x grid.z x splits items (or the
   // device partition's split_target items)
@@ -1014,8 +1024,8 @@ cudaError_t launch_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnPar
                                        : p.num_splits * p.num_kv_heads * p.row_chunks * p.batch;
   // a programmatic dependent of the kernel before it (it waits for that
   // kernel before touching global memory)
-  return launch_kernel(true, attn_tc_kernel<T, 128, NC, k_stages<NV>(), NV, p_buffers<NV>()>,
-                       dim3(grid.x), k.threads, k.smem, stream, km, vm, p, items);
+  return launch_kernel(true, attn_tc_kernel<T, 128, NC, C::NS, NV, C::PB, C::QB>, dim3(grid.x),
+                       k.threads, k.smem, stream, km, vm, p, items);
 }
 
 using Launch = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const AttnParams &, dim3,
@@ -1026,7 +1036,13 @@ bool pick_ns(int stages, KernelInfo *info, Launch *launch) {
   switch (stages == 0 ? kDefaultStages : stages) {
     case 1: *info = info_t<T, NC, 1>(); if (launch) *launch = &launch_t<T, NC, 1>; return true;
     case 2: *info = info_t<T, NC, 2>(); if (launch) *launch = &launch_t<T, NC, 2>; return true;
-    case 3: *info = info_t<T, NC, 3>(); if (launch) *launch = &launch_t<T, NC, 3>; return true;
+    case 3:
+      if constexpr (NC > 32) return false;  // shared memory
+      else {
+        *info = info_t<T, NC, 3>();
+        if (launch) *launch = &launch_t<T, NC, 3>;
+        return true;
+      }
     default: return false;
   }
 }
@@ -1035,6 +1051,7 @@ template <typename T>
 bool pick_t(int rows, int stages, KernelInfo *info, Launch *launch) {
   if (rows <= 16) return pick_ns<T, 16>(stages, info, launch);
   if (rows <= 32) return pick_ns<T, 32>(stages, info, launch);
+  if (rows <= 64) return pick_ns<T, 64>(stages, info, launch);
   return false;
 }
 

@@ -41,9 +41,9 @@ cudaError_t mma_launch(pkv_dtype cache_dtype, pkv_dtype q_dtype, int head_dim, c
                        dim3 grid, cudaStream_t stream);
 
 // tcgen05 kernel (TMEM accumulators, 128-key chunks): bf16 / f16 caches, q of
-// the same type, head_dim 128, up to 32 query rows per CTA.
-constexpr int kTcMaxRows = 32;
-// stages: chunk ring depth 1..3 (0 = default).
+// the same type, head_dim 128, up to 64 query rows per CTA.
+constexpr int kTcMaxRows = 64;
+// stages: V ring depth 1..3 (1..2 above 32 rows; 0 = default).
 bool tc_kernel_info(pkv_dtype dtype, int head_dim, int rows_per_cta, int stages,
                     KernelInfo *info);
 cudaError_t tc_launch(pkv_dtype dtype, int head_dim, int rows_per_cta, int stages,

@@ -138,11 +138,28 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
       "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
       : "memory");
 }
+// N = 8, 16 or 32 consecutive columns (32: two loads of 16).
 template <int N> __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
-  if constexpr (N == 8) tmem_ld8(taddr, v); else tmem_ld16(taddr, v);
+  if constexpr (N == 8) {
+    tmem_ld8(taddr, v);
+  } else if constexpr (N == 16) {
+    tmem_ld16(taddr, v);
+  } else {
+    static_assert(N == 32, "8, 16 or 32 columns");
+    tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(&v[0]));
+    tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+  }
 }
 template <int N> __device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[N]) {
-  if constexpr (N == 8) tmem_st8(taddr, v); else tmem_st16(taddr, v);
+  if constexpr (N == 8) {
+    tmem_st8(taddr, v);
+  } else if constexpr (N == 16) {
+    tmem_st16(taddr, v);
+  } else {
+    static_assert(N == 32, "8, 16 or 32 columns");
+    tmem_st16(taddr, *reinterpret_cast<const float(*)[16]>(&v[0]));
+    tmem_st16(taddr + 16, *reinterpret_cast<const float(*)[16]>(&v[16]));
+  }
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

@@ -666,9 +666,14 @@ def test_tc_refuses_what_it_does_not_build():
                  (2, 1, 8, 8, 128, 100, torch.float32)]:   # float32
         with pytest.raises(pkv.PkvError):
             pkv.plan(*args, kernel=3)
-    # more than 32 rows per KV head: split over row chunks of <= 32
+    # up to 64 rows per KV head in one CTA (the 64-column tile); more are
+    # split over row chunks of <= 64
     p = pkv.plan(2, 9, 32, 8, 128, 100, torch.bfloat16, kernel=3)
-    assert p["rows_per_cta"] <= 32 and p["row_chunks"] == 2
+    assert p["rows_per_cta"] == 36 and p["row_chunks"] == 1
+    p = pkv.plan(2, 18, 32, 8, 128, 100, torch.bfloat16, kernel=3)
+    assert p["rows_per_cta"] == 36 and p["row_chunks"] == 2
+    with pytest.raises(pkv.PkvError):   # three V stages do not fit beside the wide tile
+        pkv.plan(2, 9, 32, 8, 128, 100, torch.bfloat16, kernel=3, stages=3)
     # FP8 caches stay on the other kernels
     with pytest.raises(pkv.PkvError):
         pkv.plan(2, 1, 8, 8, 128, 100, "fp8", kernel=3)
@@ -1045,3 +1050,45 @@ def test_merge_rows_kernel_many_splits():
                                             max(lens), -(-max(lens) // 16))
         assert max(ns) > 32
         run_case(wl, kernel=2)
+
+
+@pytest.mark.parametrize("stages", [1, 2])
+@pytest.mark.parametrize("Q,Hq,Hkv", [(9, 32, 8), (16, 32, 8), (5, 64, 8), (17, 16, 4)])
+@pytest.mark.parametrize("split_blocks", [0, 3, 17])
+def test_tc_wide_tile(stages, Q, Hq, Hkv, split_blocks):
+    """The tcgen05 kernel's 64-column tile (33..64 query rows per KV head: one
+    Q^T and one P^T buffer, 512 TMEM columns), with the balanced partition
+    and the host's; 68 rows take two row chunks."""
+    lens = [Q, 16, 129, 300, 1000, 2100, 5000]
+    wl = W.Workload(f"tc wide st{stages} Q{Q} {Hq}/{Hkv} sb{split_blocks}", len(lens), Hq, Hkv,
+                    128, "bf16", context_lens=lens, num_queries=Q,
+                    seed=2500 + 10 * stages + Q + Hq + split_blocks)
+    run_case(wl, kernel=3, stages=stages, split_blocks=split_blocks)
+
+
+@pytest.mark.parametrize("branching", [(3, 2), (4, 3), (2, 2, 2)])
+def test_tc_wide_tile_tree(branching):
+    """Medusa-style trees over four query heads per KV head (40, 68 and 60
+    rows) through the tcgen05 kernel: per-node ancestor masks."""
+    import oracle
+    import paged_kv_cache_18_gb300 as pkv
+    from tests.gpu_util import cache_bits
+    parents = W.medusa_parents(branching)
+    n = len(parents)
+    lens = [n, n + 3, 600, 4000, 9000, 130]
+    wl = W.Workload(f"tc tree {branching}", len(lens), 32, 8, 128, "bf16", context_lens=lens,
+                    num_queries=n, seed=2600 + n)
+    b = W.make_batch(wl)
+    d = DeviceBatch(b)
+    d.append()
+    masks = W.tree_mask_bits(parents)
+    out = pkv.tree_verify_attention(d.q, d.k_cache, d.v_cache, d.table, d.lens,
+                                    torch.from_numpy(masks.view(np.int64)).cuda(),
+                                    scale=wl.softmax_scale, max_context_len=b.max_context_len,
+                                    kernel=3, error_word=d.err)
+    torch.cuda.synchronize()
+    assert int(d.err.item()) == 0
+    oracle_after_append(b)
+    ref = oracle.tree_attention(b.q, cache_bits(d.k_cache), cache_bits(d.v_cache),
+                                b.block_table, b.context_lens, wl.softmax_scale, "bf16", masks)
+    assert_close(host_f64(out, "bf16"), ref, "bf16", wl.name)
