@@ -106,18 +106,21 @@ typedef enum pkv_kernel {
                           up to 40 query rows per KV head in one CTA at head_dim
                           <= 128 (8 at 256), more cut into row chunks */
   PKV_KERNEL_TC = 3    /* tcgen05 tiles with TMEM accumulators: bf16 / fp16 caches,
-                          head_dim 128, up to 32 query rows per CTA, no fused append */
+                          head_dim 128, up to 64 query rows per CTA (more cut into
+                          row chunks), fused append included; opt-in */
 } pkv_kernel;
 
 /* Optional launch controls (pass NULL for the planner's choice). */
 typedef struct pkv_options {
   int kernel;       /* pkv_kernel */
   int split_blocks; /* 0: planner; > 0: KV blocks per split-K chunk */
-  int stages;       /* 0: planner; tensor-core kernel: ring depth per block
+  int stages;       /* 0: planner; mma.sync kernel: ring depth per block
                        lane, the tile's shallow or deep ring (at head_dim <= 128:
                        2 or 3 with one column group, 3 or 4 with two, 4 or 6
                        with three to five; 1 or 2 at 256; twice these for FP8
-                       caches); other values are refused */
+                       caches); tcgen05 kernel: the V ring's depth in 128-key
+                       chunks, 1..3 (1..2 above 32 rows); other values are
+                       refused */
   int rows_per_cta; /* 0: planner; cap on the query rows one CTA serves */
   int merge;        /* split-K merge: 0 planner, 1 by the sequence's last CTA,
                        2 by a separate kernel */
@@ -140,14 +143,14 @@ typedef struct pkv_options {
 
 /* What one attention call launches (see pkv_attention_plan). */
 typedef struct pkv_plan {
-  int kernel;             /* PKV_KERNEL_SIMT or PKV_KERNEL_MMA */
+  int kernel;             /* PKV_KERNEL_SIMT, PKV_KERNEL_MMA or PKV_KERNEL_TC */
   int rows_per_cta;       /* query rows (queries x heads of one KV head) per CTA */
   int row_chunks;         /* CTAs that share one (sequence, KV head) */
   int split_blocks;       /* KV blocks per split */
   int num_splits;         /* splits of the longest sequence; 1 = no merge */
   int grid_x, grid_y, grid_z;
   int threads_per_cta;
-  int stages;             /* shared-memory stages per warp */
+  int stages;             /* shared-memory stages per warp (tcgen05: V ring depth) */
   int ctas_per_sm;        /* occupancy the planner assumed */
   size_t smem_bytes;      /* dynamic shared memory per CTA */
   size_t workspace_bytes; /* device workspace the call needs (0 = none) */
