@@ -882,7 +882,6 @@ def run_ours(args):
 
 # ------------------------------------------------------- MLA decode ------
 MLA_SOURCES = ["paged_kv_cache_18_gb300/csrc/attn_mla.cu",
-               "paged_kv_cache_18_gb300/csrc/attn_merge.cu",
                "paged_kv_cache_18_gb300/csrc/pkv_device.cuh"]
 
 

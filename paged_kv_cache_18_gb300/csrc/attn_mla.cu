@@ -405,7 +405,95 @@ bool pick(pkv_dtype dtype, int rope_dim, int stages, KernelInfo *info, MlaLaunch
   return false;
 }
 
+// ---- split-K merge of the 512-wide latent outputs -----------------------------
+// The Flash-Decoding reduction ("Inference part 1", section "FlashDecoding")
+// of the partials this kernel leaves per (row, split), [row][split]: split s
+// holds O_s / l_s and lse_s = m_s + log2(l_s); with M = max_s lse_s,
+//   out = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M).
+// One CTA per output row (a (sequence, head) pair), warp w taking head dims
+// 128 w .. 128 w + 127 (four a lane): every warp reads the row's log-sum-exps
+// (lane s the split s, 32 at a time), takes their maximum and weights by
+// shuffles, and accumulates its dims with eight splits' vectors in flight --
+// no block barrier, and the 1,024 rows of the DeepSeek-V2-shaped step in one
+// wave.  (A CTA per row with its warps sharing the splits and meeting in
+// shared memory took 11.5 us cold there; a warp per row, 12.4 us.)  A
+// programmatic dependent of the attention kernel: nothing is read before
+// pdl_wait.
+constexpr int kMergeWarps = kMlaLatent / 128;  // 4
+template <typename T>
+__global__ void __launch_bounds__(kMergeWarps * 32) mla_merge_kernel(const AttnParams p) {
+  constexpr int D = kMlaLatent;  // 512
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = static_cast<int>(row / p.num_heads);
+  const SeqExtent ext = seq_extent(p, b, false);
+  int ns = (ext.nblk + p.split_blocks - 1) / p.split_blocks;
+  ns = ns < 1 ? 1 : (ns > p.num_splits ? p.num_splits : ns);
+  const int64_t first = row * p.num_splits;
+  auto lse_of = [&](int s) -> float { return s < ns ? __ldcg(p.part_lse + first + s) : -INFINITY; };
+  const float l0 = lse_of(lane);
+  float M = l0;
+  for (int s0 = 32; s0 < ns; s0 += 32) M = fmaxf(M, lse_of(s0 + lane));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  const int dim = 128 * warp + 4 * lane;
+  if (M != -INFINITY) {
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const float w_mine = ex2((s0 == 0 ? l0 : lse_of(s0 + lane)) - M);  // 0 for -inf
+      wsum += w_mine;
+      const int n = min(32, ns - s0);
+      for (int t0 = 0; t0 < n; t0 += 8) {
+        float4 v[8];
+        float w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          w[u] = __shfl_sync(kFull, w_mine, (t0 + u) & 31);
+          if (t0 + u >= n) w[u] = 0.f;
+          v[u] = w[u] > 0.f ? __ldcg(reinterpret_cast<const float4 *>(
+                                  p.part_o + (first + s0 + t0 + u) * D + dim))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc.x = fmaf(w[u], v[u].x, acc.x);
+          acc.y = fmaf(w[u], v[u].y, acc.y);
+          acc.z = fmaf(w[u], v[u].z, acc.z);
+          acc.w = fmaf(w[u], v[u].w, acc.w);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(kFull, wsum, o);
+  const float inv = wsum > 0.f ? p.out_scale / wsum : 0.f;
+  T *dst = reinterpret_cast<T *>(p.out) + row * D + dim;
+  dst[0] = from_float<T>(acc.x * inv);
+  dst[1] = from_float<T>(acc.y * inv);
+  dst[2] = from_float<T>(acc.z * inv);
+  dst[3] = from_float<T>(acc.w * inv);
+}
+
 }  // namespace mla
+
+cudaError_t mla_merge_launch(pkv_dtype dtype, const AttnParams &p, cudaStream_t stream) {
+  const int64_t nrows = static_cast<int64_t>(p.batch) * p.num_heads;
+  if (nrows == 0) return cudaSuccess;
+  if (nrows > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(nrows));
+  switch (dtype) {
+    case PKV_BF16:
+      return launch_kernel(true, mla::mla_merge_kernel<__nv_bfloat16>, grid,
+                           mla::kMergeWarps * 32, 0, stream, p);
+    case PKV_F16:
+      return launch_kernel(true, mla::mla_merge_kernel<__half>, grid, mla::kMergeWarps * 32, 0,
+                           stream, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 bool mla_kernel_info(pkv_dtype dtype, int rope_dim, int stages, KernelInfo *info) {
   mla::MlaLaunch launch = nullptr;

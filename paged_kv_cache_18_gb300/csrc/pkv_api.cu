@@ -1287,8 +1287,7 @@ pkv_status pkv_mla_decode_attention(void *out, const void *q, const void *ckv_ca
   if (mla_launch(dtype, rope_dim, options ? options->stages : 0, cmap, p, grid, cs) !=
       cudaSuccess)
     return PKV_ERR_CUDA;
-  if (pl.num_splits > 1 && merge_launch(dtype, kMlaLatent, p, pl.sms, cs) != cudaSuccess)
-    return PKV_ERR_CUDA;
+  if (pl.num_splits > 1 && mla_merge_launch(dtype, p, cs) != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }
 

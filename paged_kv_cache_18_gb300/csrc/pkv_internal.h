@@ -83,6 +83,8 @@ cudaError_t mla_launch(pkv_dtype dtype, int rope_dim, int stages, const CUtensor
 // is its programmatic dependent.
 cudaError_t zero_counters_launch(unsigned int *words, int64_t n, cudaStream_t stream);
 // Split-K log-sum-exp merge.
+// The MLA step's split-K merge (512-wide rows, [row][split] partials).
+cudaError_t mla_merge_launch(pkv_dtype dtype, const AttnParams &p, cudaStream_t stream);
 cudaError_t merge_launch(pkv_dtype dtype, int head_dim, const AttnParams &p, int sm_count,
                          cudaStream_t stream);
 
