@@ -358,3 +358,22 @@ def test_stream_k_partition_mirror(lens, units, ctas, weight):
     for b in range(len(lens)):
         want = sum(len(cs) for U, cs, _ in pieces if U // units == b) / units
         assert got[b] == want
+
+
+def test_tc_plan_wide_tile():
+    """The tcgen05 kernel serves up to 64 query rows per KV head in one CTA
+    (its 64-column tile: one Q^T and one P^T buffer, at most two V stages);
+    more rows are cut into row chunks of at most 64."""
+    for Q, rows in ((9, 36), (16, 64)):
+        p = binding.plan_for(4, Q, 32, 8, 128, 4096, torch.bfloat16, num_sms=152, kernel=3)
+        assert (p["rows_per_cta"], p["row_chunks"]) == (rows, 1)
+        assert p["smem_bytes"] <= 227 * 1024 and p["warp_tiles"] == 8
+    p = binding.plan_for(4, 17, 32, 8, 128, 4096, torch.bfloat16, num_sms=152, kernel=3)
+    assert (p["rows_per_cta"], p["row_chunks"]) == (34, 2)
+    for st in (1, 2):
+        p = binding.plan_for(4, 9, 32, 8, 128, 4096, torch.bfloat16, num_sms=152, kernel=3,
+                             stages=st)
+        assert p["stages"] == st
+    with pytest.raises(binding.PkvError):   # a third V stage does not fit beside it
+        binding.plan_for(4, 9, 32, 8, 128, 4096, torch.bfloat16, num_sms=152, kernel=3,
+                         stages=3)
